@@ -1,0 +1,340 @@
+"""Benchmark of the cache-fusion hot path at the critical layer on GB300.
+
+One step = score (query -> cached keys, RoPE in-kernel) + per-span top-k + gather of the
+recompute rows + fused attention of recomputed and query rows over cached-minus-selected plus
+fresh KV, on one batch of synthetic input already resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--pct P] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica of the workload
+(requests shard with no exchange: weak scaling); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workload import CONFIGS, hidden_rows, make_batch  # noqa: E402
+
+METRIC = "fused-prefill tokens/s per layer; attention TFLOP/s vs GB300 bf16 tensor peak"
+DESCR = {
+    "tiny": "1 request, 4 spans x 128 cached tokens + 32 query tokens, 8q/2kv heads, d=64, theta 1e4",
+    "llama8b_layer": "Llama-3-8B-shaped layer: 1 request, 8 spans x 512 cached tokens (random offset) "
+                     "+ 64 query tokens, 32q/8kv heads, d=128, page 16, theta 5e5",
+    "concurrent_reuse": "32 requests x 10 spans (Zipf 1.1 over a pool of 64 x 1024-token spans) + 64 query "
+                        "tokens, 32q/8kv, d=128",
+    "long_context": "1 request, 64 spans x 512 = 32768 cached tokens + 128 query tokens, 32q/8kv, d=128",
+    "batch70b": "64 requests x 16 spans x 1024 tokens (Zipf 1.0, pool 256 spans) + 128 query tokens, "
+                "64q/8kv, d=128",
+}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d["bf16_tflops"], d.get("bf16_tflops_sustained"), d["hbm_gbs"], "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.05)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in out.strip().splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def attention_flops(b, sel, row_pos, d, hq):
+    """Algorithmic attention flops 4*d*Hq*sum_rows |visible keys| (excluded cached copies of
+    recomputed tokens are not counted)."""
+    total = 0
+    tb = sb = rb = 0
+    for r in b.requests:
+        kpos = (np.concatenate([s.pos0 + np.arange(s.n_pages * 16) for s in r.spans])
+                if r.spans else np.zeros(0, dtype=np.int64))
+        keep = np.ones(len(kpos), dtype=bool)
+        keep[sel[sb: sb + r.n_sel]] = False
+        rp = row_pos[rb: rb + r.n_rows]
+        keys = np.sort(np.concatenate([kpos[keep], rp]))
+        total += int(np.searchsorted(keys, rp, side="right").sum())
+        tb += r.n_cached
+        sb += r.n_sel
+        rb += r.n_rows
+    return 4.0 * d * hq * total
+
+
+def oracle_prepare(b):
+    kp = b.k_pool.double().numpy()
+    vp = b.v_pool.double().numpy()
+    return dict(kp=kp, vp=vp, qq=b.q_query.double().numpy(), qf=b.q_fresh.double().numpy(),
+                kf=b.k_fresh.double().numpy(), vf=b.v_fresh.double().numpy())
+
+
+def oracle_step(b, prep, req_ids):
+    """The fp64 oracle on the given requests: score, per-span top-k, gather, fused attention.
+    Returns the tokens (cached + query) it processed."""
+    from oracle import method
+    qb, rb = b.query_bases(), b.row_bases()
+    tokens = 0
+    for i in req_ids:
+        r = b.requests[i]
+        K, V, kpos = method.request_cached(r.spans, prep["kp"], prep["vp"])
+        q = prep["qq"][qb[i]: qb[i] + r.n_query]
+        imp = method.score_request(q, r.query_pos0 + np.arange(r.n_query), K, kpos, b.theta)
+        sel = method.select_topk_request(imp.astype(np.float32), [s.n_pages * 16 for s in r.spans],
+                                         [s.k for s in r.spans])
+        method.gather_rows(np.arange(r.n_cached), sel)
+        row_pos = method.row_positions(sel, kpos, r.n_query, r.query_pos0)
+        sl = slice(rb[i], rb[i] + r.n_rows)
+        method.fused_attention_request(prep["qf"][sl], prep["kf"][sl], prep["vf"][sl], row_pos, K, V, kpos,
+                                       sel, b.theta)
+        tokens += r.n_cached + r.n_query
+    return tokens
+
+
+def _oracle_sample(b):
+    """Requests the bounded oracle sample covers (whole requests, ~10-30 s of CPU work)."""
+    n = len(b.requests)
+    budget = {"tiny": n, "llama8b_layer": n, "concurrent_reuse": 1, "long_context": 1, "batch70b": 1}
+    return list(range(min(n, budget.get(b.cfg_name, 1))))
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    b = make_batch(args.config, args.pct)
+    prep = oracle_prepare(b)
+    ids = _oracle_sample(b)
+    for _ in range(args.warmup):
+        oracle_step(b, prep, ids)
+    t0 = time.perf_counter()
+    tokens = 0
+    for _ in range(args.steps):
+        tokens += oracle_step(b, prep, ids)
+    dt = time.perf_counter() - t0
+    value = tokens / dt
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"{len(ids)} of {len(b.requests)} requests of the {args.config} workload per step "
+              f"(score + top-k + gather + fused attention, fp64 NumPy)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{args.config}: {DESCR[args.config]}"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="llama8b_layer", choices=list(CONFIGS))
+    ap.add_argument("--pct", type=int, default=None)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    world, rank, local = _dist()
+    import position_independent_kv_critical_gb300 as pcf
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    b = make_batch(args.config, args.pct)
+    max_pos = b.max_pos + 1
+    L = pcf.Layout(b.requests, b.hq, b.hkv, b.d, b.n_phys_pages, max_pos, device=str(dev))
+    rope = pcf.rope_table(b.d, b.theta, max_pos).to(dev)
+    D = b.hq * b.d
+    cf = pcf.CacheFusion(L, rope, row_elems=D, device=str(dev))
+    g = lambda t: t.to(dev)
+    k_pool, v_pool = g(b.k_pool), g(b.v_pool)
+    q_query, q_fresh, k_fresh, v_fresh = g(b.q_query), g(b.q_fresh), g(b.k_fresh), g(b.v_fresh)
+    hidden = hidden_rows(torch.arange(L.total_tokens, device=dev), D)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
+
+    def front():
+        pcf.score(L, q_query, k_pool, rope, cf.importance, cf.ws_score)
+        pcf.select_topk(L, cf.importance, cf.sel_idx, cf.excl, cf.row_pos)
+        pcf.gather_rows(L, cf.sel_idx, hidden, cf.gathered)
+
+    def attn():
+        pcf.fused_attention(L, q_fresh, k_fresh, v_fresh, k_pool, v_pool, cf.excl, cf.row_pos, rope, cf.out,
+                            cf.ws_attn)
+
+    for _ in range(max(3, args.warmup)):
+        front()
+        attn()
+    pcf.check_device_error()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        pcf.score(L, q_query, k_pool, rope, cf.importance, cf.ws_score)
+        ev[i][1].record(stream)
+        pcf.select_topk(L, cf.importance, cf.sel_idx, cf.excl, cf.row_pos)
+        pcf.gather_rows(L, cf.sel_idx, hidden, cf.gathered)
+        ev[i][2].record(stream)
+        attn()
+        ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    pcf.check_device_error()
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    score_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    topk_gather_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    attn_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = sum(r.n_cached + r.n_query for r in b.requests)
+    value = world * tokens / (ms / 1e3)
+
+    sel = cf.sel_idx[: L.total_sel].cpu().numpy()
+    row_pos = cf.row_pos[: L.total_rows].cpu().numpy()
+    flops = attention_flops(b, sel, row_pos, b.d, b.hq)
+    a_ms = statistics.mean(attn_ms)
+    peak, peak_sus, hbm, src = _peaks()
+    achieved = flops / (a_ms / 1e3) / 1e12
+    score_flops = 2.0 * b.hq * b.d * sum(r.n_query * r.n_cached for r in b.requests)
+
+    # end to end through the public API: inputs from pinned host memory, result back to the host
+    hq_q = b.q_query.pin_memory()
+    hq_f = [b.q_fresh.pin_memory(), b.k_fresh.pin_memory(), b.v_fresh.pin_memory()]
+    out_h = torch.empty_like(cf.out, device="cpu").pin_memory()
+    sel_h = torch.empty_like(cf.sel_idx, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in [hq_q] + hq_f)
+    d2h = out_h.numel() * out_h.element_size() + sel_h.numel() * sel_h.element_size()
+    Ke = min(K, 50)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(Ke):
+        q_query.copy_(hq_q, non_blocking=True)
+        q_fresh.copy_(hq_f[0], non_blocking=True)
+        k_fresh.copy_(hq_f[1], non_blocking=True)
+        v_fresh.copy_(hq_f[2], non_blocking=True)
+        cf.step(q_query, k_pool, v_pool, q_fresh, k_fresh, v_fresh, hidden)
+        out_h.copy_(cf.out, non_blocking=True)
+        sel_h.copy_(cf.sel_idx, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    pcf.check_device_error()
+
+    launches_per_step = (3 if L.total_tokens else 0) + 1 + (1 if L.total_sel else 0) + 2
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.config}: {DESCR[args.config]}",
+                   "recompute_pct": args.pct if args.pct is not None else CONFIGS[args.config].pct,
+                   "tokens_per_step": tokens, "l2": "flushed between timed steps (512 MB write)"},
+        "roofline": {"bound": "tensor", "kernel": "pcf_fused_attention (fresh-row rotation + attention)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": src + " bf16 burst", "frac_of_sustained": achieved / peak_sus if peak_sus else None,
+                     "traffic": None, "algorithmic_flops_per_launch": flops, "ms_per_launch": a_ms},
+        "breakdown_ms": {"score": statistics.mean(score_ms), "topk_gather": statistics.mean(topk_gather_ms),
+                         "attention": a_ms},
+        "score_tflops": score_flops / (statistics.mean(score_ms) / 1e3) / 1e12,
+        "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "wall_s": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        prep = oracle_prepare(b)
+        ids = _oracle_sample(b)
+        t1 = time.perf_counter()
+        tok = oracle_step(b, prep, ids)
+        dt = time.perf_counter() - t1
+        line["cpu_baseline"] = {"value": tok / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                                "kind": "oracle",
+                                "sample": f"{len(ids)} of {len(b.requests)} requests, one full oracle step "
+                                          f"(fp64 NumPy, BLAS threads = all cores), {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * pcf.h -- C ABI of the position-free KV cache-fusion hot path (GB300, sm_103a).
+ *
+ * The operation (from the two methods this library implements):
+ *   - MiniPIC: Position-Independent Caching ..., section 2.1 "Position-free KV": the cache holds
+ *     UNROTATED keys k~_j in shared physical pages; attention applies RoPE on the fly from the
+ *     key's per-request logical position pi(j): score(t, j) = (R_t q_t)^T (R_pi(j) k~_j) / sqrt(d),
+ *     implemented as a cos/sin table lookup and fused multiply-adds per key element, so one
+ *     physical block serves concurrent requests at different offsets (section 1, "concurrency
+ *     barrier").
+ *   - QCFuse: Query-Centric Cache Fusion ..., section 2B "Critical-layer attention profiling": at
+ *     one critical layer the query attends to the key cache only; the attention weights rank the
+ *     context tokens and the Top-N guide selective recomputation (section 2C / Phase 4), done by a
+ *     sparse attention that keeps causal constraints.
+ *
+ * Conventions
+ *   - Every entry point returns pcf_status (0 = PCF_OK, negative = error) and never allocates
+ *     memory: all host and device buffers belong to the caller.
+ *   - Device calls are asynchronous on the caller's CUDA stream, passed as `void* stream`
+ *     (a cudaStream_t; NULL = legacy default stream).  Arguments are validated on the host before
+ *     any launch; an invalid call launches nothing.
+ *   - bf16 tensors are passed as `const uint16_t*` (raw bfloat16 bits).  Device pointers must be
+ *     16-byte aligned.
+ *   - Tensor layouts (row-major, innermost last):
+ *       k_pool, v_pool : [n_phys_pages][Hkv][16][d]     cached pages, keys UNROTATED
+ *       q_query        : [sum_b T_b][Hq][d]              scoring query, unrotated
+ *       q_fresh        : [sum_b rows_b][Hq][d]           rows of request b: its R_b recomputed
+ *       k_fresh,v_fresh: [sum_b rows_b][Hkv][d]          tokens (ascending token index) then its
+ *       out            : [sum_b rows_b][Hq][d]           T_b query tokens; all unrotated
+ *       rope           : [max_pos][d/2][2] fp32          (cos, sin) of p * theta^(-2i/d)
+ *     Query head h reads kv head h / (Hq/Hkv).  RoPE pairs dimension i with i + d/2.
+ *   - A batch is described once by a "layout": an int32 blob built on the host by
+ *     pcf_layout_build and copied by the caller to the device.  Calls take both copies
+ *     (pcf_layout.host for launch configuration, pcf_layout.dev for the kernels); they must hold
+ *     the same words.
+ *   - Device-side faults that the host cannot rule out (a bounded wait that ran out, an index out
+ *     of range) set a device error word and the kernel returns early; pcf_check_device_error
+ *     reports and clears it.
+ */
+#ifndef PCF_H
+#define PCF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t pcf_status;
+#define PCF_OK                        0
+#define PCF_ERR_INVALID_ARG          -1  /* bad pointer, size, span placement or layout blob */
+#define PCF_ERR_UNSUPPORTED          -2  /* head_dim not in {64,128}, group size not a divisor of 128 */
+#define PCF_ERR_CUDA                 -3  /* a CUDA runtime/driver call failed */
+#define PCF_ERR_DEVICE_TIMEOUT       -4  /* a kernel's bounded wait ran out (reported by check) */
+#define PCF_ERR_WORKSPACE_TOO_SMALL  -5
+#define PCF_ERR_DEVICE_BOUNDS        -6  /* a kernel met an out-of-range index (reported by check) */
+#define PCF_ERR_NO_DEVICE            -7  /* no sm_103 device is current */
+
+/* One cached span of a request: n_pages consecutive physical pages starting at phys_first_page,
+ * holding tokens at logical positions pos0 .. pos0 + 16*n_pages - 1; k of its tokens are to be
+ * recomputed (0 <= k <= 16*n_pages).  MiniPIC section 2.2: spans are padded to page boundaries. */
+typedef struct pcf_span_desc {
+    int32_t phys_first_page;
+    int32_t n_pages;
+    int32_t pos0;
+    int32_t k;
+} pcf_span_desc;
+
+/* One request: its spans in increasing position order, then n_query query tokens at positions
+ * query_pos0 .. query_pos0 + n_query - 1 (query_pos0 after the last span token). */
+typedef struct pcf_request_desc {
+    int32_t n_spans;
+    const pcf_span_desc* spans;
+    int32_t n_query;
+    int32_t query_pos0;
+} pcf_request_desc;
+
+typedef struct pcf_dims {
+    int32_t n_q_heads;     /* Hq */
+    int32_t n_kv_heads;    /* Hkv, divides Hq; g = Hq/Hkv must divide 128 */
+    int32_t head_dim;      /* d in {64, 128} */
+    int32_t n_phys_pages;  /* pages in the pool */
+    int32_t max_pos;       /* rows of the rope table; every position must be < max_pos <= 1<<20 */
+} pcf_dims;
+
+typedef struct pcf_layout {
+    const int32_t* host;   /* blob in host memory */
+    const int32_t* dev;    /* identical blob in device memory */
+} pcf_layout;
+
+/* Header words of a layout blob readable with pcf_layout_query (sizes for the caller). */
+enum {
+    PCF_L_WORDS = 1, PCF_L_N_REQS = 2, PCF_L_HQ = 3, PCF_L_HKV = 4, PCF_L_D = 5,
+    PCF_L_N_PHYS_PAGES = 6, PCF_L_MAX_POS = 7, PCF_L_TOTAL_TOKENS = 8, PCF_L_TOTAL_QUERY = 9,
+    PCF_L_TOTAL_ROWS = 10, PCF_L_TOTAL_SEL = 11, PCF_L_TOTAL_PAGES = 12, PCF_L_N_SPANS = 13
+};
+
+/* Text for a status code (static storage). */
+const char* pcf_status_string(pcf_status s);
+
+/* ceil(pct * span_len / 100) in integer arithmetic; -1 for pct < 0 or span_len < 0. */
+int32_t pcf_k_from_percent(int32_t pct, int32_t span_len);
+
+/* Host-only.  Fills table[max_pos][head_dim/2][2] (caller-owned, host memory) with
+ * (cos, sin)(p * theta^(-2i/d)) computed in fp64 and rounded to fp32 (MiniPIC 2.1, "cos/sin table
+ * lookup").  The caller copies it to the device.  Errors: null table, head_dim not in {64,128},
+ * theta <= 0, max_pos < 16 or > 1<<20. */
+pcf_status pcf_rope_table_init(float* table, int32_t head_dim, double theta, int32_t max_pos);
+
+/* Host-only.  Number of int32 words of the layout blob for this batch (validates like build). */
+pcf_status pcf_layout_words(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims* dims,
+                            int64_t* n_words);
+
+/* Host-only.  Validates the batch and writes the layout blob: per request, the block table
+ * (logical page -> physical page), the logical position of every page's first token, span
+ * records, row/selection offsets and the kernels' work lists.  Errors (PCF_ERR_INVALID_ARG):
+ * null pointers, n_reqs < 1, a span outside the pool or with n_pages < 1, positions not strictly
+ * increasing inside a request, query_pos0 before the end of the last span, any position >=
+ * max_pos, k outside [0, 16*n_pages], n_query < 0, n_words too small.  PCF_ERR_UNSUPPORTED for
+ * head_dim not in {64,128} or Hq/Hkv not dividing 128. */
+pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims* dims,
+                            int32_t* blob, int64_t n_words);
+
+/* Host-only.  Reads one PCF_L_* header word of a built blob into *value. */
+pcf_status pcf_layout_query(const int32_t* blob, int32_t field, int64_t* value);
+
+/* Bytes of device workspace pcf_score needs for this layout. */
+pcf_status pcf_score_workspace_bytes(const int32_t* layout_host, size_t* bytes);
+
+/* Critical-layer scoring (QCFuse 2B; MiniPIC 2.1 score equation).  For every request b and every
+ * cached token j of b:
+ *   importance[tok_base_b + j] = sum_{h < Hq} sum_{t < T_b}
+ *       softmax_j( (R_{pos(t)} q_{t,h}) . (R_{pi(j)} k~_{j, h/g}) / sqrt(d) )
+ * with the softmax over all cached tokens of request b.  Output fp32 [total_tokens].
+ * ws: device workspace of >= pcf_score_workspace_bytes bytes, contents need not be initialised
+ * (PCF_ERR_WORKSPACE_TOO_SMALL otherwise).  Deterministic (fixed summation order). */
+pcf_status pcf_score(const pcf_layout* layout, const uint16_t* q_query, const uint16_t* k_pool,
+                     const float* rope, float* importance, void* ws, size_t ws_bytes, void* stream);
+
+/* Per-span Top-k (QCFuse 2B "Top-N tokens", taken per span).  For every span s of request b:
+ * the k_s request-local token indices with the largest importance, ties to the lower index,
+ * written in ascending order to sel_idx[sel_base_b + offset of s ...].  Also writes
+ *   excl[page]     uint16 per logical page (global page index = tok_base_b/16 + page): bit r set
+ *                  iff token 16*page + r of that request is recomputed;
+ *   row_pos[row]   logical position of every row: the selected tokens' pi(j), then
+ *                  query_pos0 + t for the query rows.
+ * Comparison is on the fp32 bit patterns (values must not be NaN); bit-exact and deterministic. */
+pcf_status pcf_select_topk(const pcf_layout* layout, const float* importance, int32_t* sel_idx,
+                           uint16_t* excl, int32_t* row_pos, void* stream);
+
+/* Row gather of the recompute batch: dst[sel_base_b + i][:] = src[tok_base_b + sel_idx[...]][:]
+ * for every selected row; src [total_tokens][row_elems], dst [total_sel][row_elems], bf16;
+ * row_elems a positive multiple of 8. */
+pcf_status pcf_gather_rows(const pcf_layout* layout, const int32_t* sel_idx, const uint16_t* src,
+                           int32_t row_elems, uint16_t* dst, void* stream);
+
+/* Bytes of device workspace pcf_fused_attention needs for this layout. */
+pcf_status pcf_attention_workspace_bytes(const int32_t* layout_host, size_t* bytes);
+
+/* Fused prefill attention over the merged cached + fresh KV (QCFuse 2C, Phase 4; MiniPIC 2.1).
+ * For each row r of request b (its recomputed tokens then its query tokens) and q head h:
+ *   out[r][h] = sum_u softmax_u(s_u) v_u,  s_u = (R_{pos(r)} q_{r,h}) . (R_{pos(u)} k_u) / sqrt(d)
+ * over keys u = the cached tokens of b whose excl bit is clear, at pi(j), plus the fresh rows of
+ * b at row_pos; u is visible iff pos(u) <= row_pos[r].  Cached keys are rotated in the kernel,
+ * in shared memory, from the unrotated pool.  ws: >= pcf_attention_workspace_bytes bytes. */
+pcf_status pcf_fused_attention(const pcf_layout* layout, const uint16_t* q_fresh,
+                               const uint16_t* k_fresh, const uint16_t* v_fresh,
+                               const uint16_t* k_pool, const uint16_t* v_pool,
+                               const uint16_t* excl, const int32_t* row_pos, const float* rope,
+                               uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronizes `stream`, then reads and clears the device error word: PCF_OK,
+ * PCF_ERR_DEVICE_TIMEOUT or PCF_ERR_DEVICE_BOUNDS (PCF_ERR_CUDA if the sync itself failed). */
+pcf_status pcf_check_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PCF_H */

@@ -1,0 +1,199 @@
+"""GB300-native query-centric cache fusion over a position-free paged KV cache.
+
+Python binding of the C ABI in ``include/pcf.h``.  Every step of the hot path runs in the
+library's sm_103a kernels; this module only marshals arguments (torch tensors -> raw pointers,
+the current CUDA stream) and allocates buffers through torch.  There is no CPU fallback: without
+the built library or an sm_103 device the calls raise.
+
+Hot path for one batch at the critical layer:
+  ``score``          importance of every cached token (query -> cached keys, RoPE in-kernel)
+  ``select_topk``    per-span top-k tokens to recompute, exclusion bits, row positions
+  ``gather_rows``    rows of the selected tokens (input of the recomputation)
+  ``fused_attention`` recomputed + query rows over cached-minus-selected + fresh KV
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import PcfError  # noqa: F401
+
+__all__ = ["Layout", "CacheFusion", "PcfError", "k_from_percent", "rope_table", "score", "select_topk",
+           "gather_rows", "fused_attention", "check_device_error", "load_library"]
+
+
+def load_library():
+    return _lib.load()
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None or t.numel() == 0:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, name: str):
+    if t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous {dtype} tensor, got {t.dtype} "
+                         f"(contiguous={t.is_contiguous()})")
+
+
+def k_from_percent(pct: int, span_len: int) -> int:
+    return int(_lib.load().pcf_k_from_percent(int(pct), int(span_len)))
+
+
+def rope_table(head_dim: int, theta: float, max_pos: int) -> torch.Tensor:
+    """Host fp32 table [max_pos][head_dim/2][2] of (cos, sin)(p * theta^(-2i/d))."""
+    t = torch.empty((max_pos, head_dim // 2, 2), dtype=torch.float32)
+    _lib.check("pcf_rope_table_init", _lib.load().pcf_rope_table_init(
+        ctypes.c_void_p(t.data_ptr()), head_dim, float(theta), max_pos))
+    return t
+
+
+class Layout:
+    """Host + device copies of the layout blob of one batch (block table, page positions, spans,
+    row offsets and work lists).  ``requests`` are objects with ``.spans`` (each with
+    ``phys_first_page, n_pages, pos0, k``), ``.n_query`` and ``.query_pos0``."""
+
+    def __init__(self, requests: Sequence, hq: int, hkv: int, d: int, n_phys_pages: int,
+                 max_pos: int, device: str = "cuda"):
+        lib = _lib.load()
+        self._span_arrays = []
+        reqs = (_lib.RequestDesc * len(requests))()
+        for i, r in enumerate(requests):
+            arr = (_lib.SpanDesc * max(1, len(r.spans)))()
+            for j, s in enumerate(r.spans):
+                arr[j] = _lib.SpanDesc(int(s.phys_first_page), int(s.n_pages), int(s.pos0), int(s.k))
+            self._span_arrays.append(arr)
+            reqs[i] = _lib.RequestDesc(len(r.spans), arr, int(r.n_query), int(r.query_pos0))
+        dims = _lib.Dims(hq, hkv, d, n_phys_pages, max_pos)
+        n = ctypes.c_int64(0)
+        _lib.check("pcf_layout_words", lib.pcf_layout_words(reqs, len(requests), ctypes.byref(dims),
+                                                            ctypes.byref(n)))
+        host = torch.empty(n.value, dtype=torch.int32)
+        if device != "cpu" and torch.cuda.is_available():
+            host = host.pin_memory()
+        _lib.check("pcf_layout_build", lib.pcf_layout_build(reqs, len(requests), ctypes.byref(dims),
+                                                            ctypes.c_void_p(host.data_ptr()), n.value))
+        self.host = host
+        self.dev = host.to(device) if device != "cpu" else host.clone()
+        self.ref = _lib.LayoutRef(host.data_ptr(), self.dev.data_ptr())
+        self.hq, self.hkv, self.d = hq, hkv, d
+        self.requests = list(requests)
+
+    def field(self, name: str) -> int:
+        v = ctypes.c_int64(0)
+        _lib.check("pcf_layout_query", _lib.load().pcf_layout_query(
+            ctypes.c_void_p(self.host.data_ptr()), _lib.HEADER_FIELDS[name], ctypes.byref(v)))
+        return int(v.value)
+
+    @property
+    def total_tokens(self) -> int:
+        return self.field("total_tokens")
+
+    @property
+    def total_query(self) -> int:
+        return self.field("total_query")
+
+    @property
+    def total_rows(self) -> int:
+        return self.field("total_rows")
+
+    @property
+    def total_sel(self) -> int:
+        return self.field("total_sel")
+
+    @property
+    def total_pages(self) -> int:
+        return self.field("total_pages")
+
+    def score_workspace_bytes(self) -> int:
+        v = ctypes.c_size_t(0)
+        _lib.check("pcf_score_workspace_bytes", _lib.load().pcf_score_workspace_bytes(
+            ctypes.c_void_p(self.host.data_ptr()), ctypes.byref(v)))
+        return int(v.value)
+
+    def attention_workspace_bytes(self) -> int:
+        v = ctypes.c_size_t(0)
+        _lib.check("pcf_attention_workspace_bytes", _lib.load().pcf_attention_workspace_bytes(
+            ctypes.c_void_p(self.host.data_ptr()), ctypes.byref(v)))
+        return int(v.value)
+
+
+def score(layout: Layout, q_query, k_pool, rope, importance, ws, stream=None):
+    _need(q_query, torch.bfloat16, "q_query")
+    _need(k_pool, torch.bfloat16, "k_pool")
+    _need(rope, torch.float32, "rope")
+    _need(importance, torch.float32, "importance")
+    _lib.check("pcf_score", _lib.load().pcf_score(
+        ctypes.byref(layout.ref), _p(q_query), _p(k_pool), _p(rope), _p(importance), _p(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def select_topk(layout: Layout, importance, sel_idx, excl, row_pos, stream=None):
+    _need(importance, torch.float32, "importance")
+    _need(sel_idx, torch.int32, "sel_idx")
+    _need(excl, torch.int16, "excl")
+    _need(row_pos, torch.int32, "row_pos")
+    _lib.check("pcf_select_topk", _lib.load().pcf_select_topk(
+        ctypes.byref(layout.ref), _p(importance), _p(sel_idx), _p(excl), _p(row_pos), _stream(stream)))
+
+
+def gather_rows(layout: Layout, sel_idx, src, dst, stream=None):
+    _need(src, torch.bfloat16, "src")
+    _need(dst, torch.bfloat16, "dst")
+    _lib.check("pcf_gather_rows", _lib.load().pcf_gather_rows(
+        ctypes.byref(layout.ref), _p(sel_idx), _p(src), int(src.shape[-1]), _p(dst), _stream(stream)))
+
+
+def fused_attention(layout: Layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope,
+                    out, ws, stream=None):
+    for t, n in ((q_fresh, "q_fresh"), (k_fresh, "k_fresh"), (v_fresh, "v_fresh"), (k_pool, "k_pool"),
+                 (v_pool, "v_pool"), (out, "out")):
+        _need(t, torch.bfloat16, n)
+    _lib.check("pcf_fused_attention", _lib.load().pcf_fused_attention(
+        ctypes.byref(layout.ref), _p(q_fresh), _p(k_fresh), _p(v_fresh), _p(k_pool), _p(v_pool),
+        _p(excl), _p(row_pos), _p(rope), _p(out), _p(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def check_device_error(stream=None):
+    _lib.check("pcf_check_device_error", _lib.load().pcf_check_device_error(_stream(stream)))
+
+
+class CacheFusion:
+    """Buffers for one batch on one device plus the four calls of the hot path in order."""
+
+    def __init__(self, layout: Layout, rope_dev: torch.Tensor, row_elems: int = 0,
+                 device: str = "cuda"):
+        L = layout
+        self.layout = L
+        self.rope = rope_dev
+        self.importance = torch.empty(max(1, L.total_tokens), dtype=torch.float32, device=device)
+        self.sel_idx = torch.empty(max(1, L.total_sel), dtype=torch.int32, device=device)
+        self.excl = torch.zeros(max(1, L.total_pages), dtype=torch.int16, device=device)
+        self.row_pos = torch.empty(max(1, L.total_rows), dtype=torch.int32, device=device)
+        self.out = torch.empty((max(1, L.total_rows), L.hq, L.d), dtype=torch.bfloat16, device=device)
+        self.ws_score = torch.empty(max(16, L.score_workspace_bytes()), dtype=torch.uint8, device=device)
+        self.ws_attn = torch.empty(max(16, L.attention_workspace_bytes()), dtype=torch.uint8, device=device)
+        self.gathered = (torch.empty((max(1, L.total_sel), row_elems), dtype=torch.bfloat16, device=device)
+                         if row_elems else None)
+
+    def step(self, q_query, k_pool, v_pool, q_fresh, k_fresh, v_fresh, hidden=None, stream=None):
+        L = self.layout
+        score(L, q_query, k_pool, self.rope, self.importance, self.ws_score, stream)
+        select_topk(L, self.importance, self.sel_idx, self.excl, self.row_pos, stream)
+        if hidden is not None and self.gathered is not None:
+            gather_rows(L, self.sel_idx, hidden, self.gathered, stream)
+        fused_attention(L, q_fresh, k_fresh, v_fresh, k_pool, v_pool, self.excl, self.row_pos,
+                        self.rope, self.out, self.ws_attn, stream)
+        return self.out

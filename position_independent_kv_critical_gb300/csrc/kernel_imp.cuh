@@ -1,0 +1,252 @@
+// Critical-layer importance, second pass (QCFuse, section 2B "Critical-layer attention
+// profiling"; second summary, Phase 3: the query attends to the key cache of one layer only).
+//
+// imp[j] = sum_h sum_t exp2(s_{h,t,j} * log2e/sqrt(d) - lse2_{h,t}), lse2 being the log2-sum-exp
+// of row (h,t) over all cached keys of the request (from the first pass).  The tile is computed
+// transposed, S^T = K_rot Q^T with M = 128 keys (TMEM lanes) and N = 256 query rows (columns), so
+// that each thread owns one key and sums its own TMEM row -- no cross-thread reduction.  The K
+// tile is rotated in shared memory at its logical positions (MiniPIC 2.1), the query rows arrive
+// pre-rotated.  One CTA per (request, key tile, kv head); the per-kv-head partial sums are
+// reduced in fixed head order by the last CTA of each key tile (deterministic).
+#pragma once
+#include "kernel_attn.cuh"
+
+namespace pcf {
+
+constexpr int kImpThreads = 192;
+constexpr int kImpQRows = 256;
+
+struct ImpParams {
+    const int32_t* layout;
+    const float2* rope;
+    const float2* lse_part;
+    float* part;             // [Hkv][total_tokens]
+    int32_t* counters;       // [total key tiles], zero on entry, left zero on exit
+    float* importance;       // [total_tokens]
+    float scale_log2;
+};
+
+template <int D>
+struct ImpSmem {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kK = kTileKeys * D * 2;
+    static constexpr int kQ = kImpQRows * D * 2;
+    static constexpr int kCs = kPagesPerTile * (D / 2) * 8;
+    static constexpr int oK = 0;
+    static constexpr int oQ = oK + kK;
+    static constexpr int oCs = oQ + 2 * kQ;
+    static constexpr int oLse = oCs + kCs;
+    static constexpr int oKpos = oLse + 2 * kImpQRows * 4;
+    static constexpr int oBar = oKpos + kTileKeys * 4;
+    static constexpr int kNumBars = 12;
+    static constexpr int oMisc = oBar + kNumBars * 8;
+    static constexpr int kBytes = oMisc + 64;
+    static constexpr int kAlloc = kBytes + 1024;
+    static constexpr uint32_t kTmemCols = 512;
+};
+
+enum : int { I_K_FULL = 0, I_KROT = 1, I_Q_FULL = 2 /*2*/, I_Q_EMPTY = 4 /*2*/, I_ACC_FULL = 6 /*2*/,
+             I_ACC_FREE = 8 /*2*/, I_DRAIN = 10 };
+
+__device__ __forceinline__ void named_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int D>
+__global__ void __launch_bounds__(kImpThreads, 1)
+imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kpool,
+           const ImpParams prm) {
+    using SM = ImpSmem<D>;
+    constexpr int H = SM::kHalves;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sK = smem + SM::oK;
+    auto sQs = [&](int b) { return smem + SM::oQ + b * SM::kQ; };
+    float2* sCs = reinterpret_cast<float2*>(smem + SM::oCs);
+    auto sLse = [&](int b) { return reinterpret_cast<float*>(smem + SM::oLse) + b * kImpQRows; };
+    int32_t* sKpos = reinterpret_cast<int32_t*>(smem + SM::oKpos);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::oBar);
+    int32_t* misc = reinterpret_cast<int32_t*>(smem + SM::oMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t* L = prm.layout;
+    const int32_t* item = L + L[L_OFF_IMP] + kItemWords * blockIdx.x;
+    const int req = item[0], t = item[1], kvh = item[2];
+    const int32_t* R = L + L[L_OFF_REQ] + req * R_STRIDE;
+    const int Hkv = L[L_HKV], g = L[L_GROUP];
+    const int n_pages = R[R_N_PAGES];
+    const int32_t page_base = R[R_PAGE_BASE];
+    const int32_t* page_pos = L + L[L_OFF_PAGEPOS] + page_base;
+    const int32_t* blk = L + L[L_OFF_BLOCK] + page_base;
+    const int n_q = R[R_N_QUERY] * g;
+    const int n_qc = (n_q + kImpQRows - 1) / kImpQRows;
+
+    if (tid == 0) {
+        mbar_init(&bars[I_K_FULL], 1);
+        mbar_init(&bars[I_KROT], 128);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[I_Q_FULL + s], 1);
+            mbar_init(&bars[I_Q_EMPTY + s], 1);
+            mbar_init(&bars[I_ACC_FULL + s], 1);
+            mbar_init(&bars[I_ACC_FREE + s], 128);
+        }
+        mbar_init(&bars[I_DRAIN], 1);
+        fence_mbar_init();
+        misc[4] = 0;
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(reinterpret_cast<uint32_t*>(misc), SM::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = static_cast<uint32_t>(misc[0]);
+
+    if (warp == kWarpTma) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_kpool);
+            const int lp0 = t * kPagesPerTile;
+            const int np = min(kPagesPerTile, n_pages - lp0);
+            const int n_phys = L[L_N_PHYS];
+            mbar_arrive_expect_tx(&bars[I_K_FULL], np * (H * 2048 + (D / 2) * 8));
+            for (int p = 0; p < np; ++p) {
+                int32_t phys = blk[lp0 + p];
+                if (phys < 0 || phys >= n_phys) { set_dev_error(kDevErrBounds); phys = 0; }
+                const int32_t y = (phys * Hkv + kvh) * kPage;
+                for (int hb = 0; hb < H; ++hb)
+                    tma_load_2d(sK + hb * 16384 + p * 2048, &tm_kpool, &bars[I_K_FULL], hb * 64, y);
+                bulk_load(sCs + p * (D / 2), prm.rope + (int64_t)page_pos[lp0 + p] * (D / 2), (D / 2) * 8,
+                          &bars[I_K_FULL]);
+            }
+            const int32_t qy0 = (kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE]) * g;
+            int last[2] = {-1, -1};
+            for (int qc = 0; qc < n_qc; ++qc) {
+                const int b = qc & 1;
+                if (qc >= 2 && !mbar_wait(&bars[I_Q_EMPTY + b], ((qc >> 1) - 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(&bars[I_Q_FULL + b], H * kImpQRows * 128);
+                for (int hb = 0; hb < H; ++hb)
+                    tma_load_2d(sQs(b) + hb * kImpQRows * 128, &tm_q, &bars[I_Q_FULL + b], hb * 64,
+                                qy0 + qc * kImpQRows);
+                last[b] = qc;
+            }
+            mbar_drain(&bars[I_K_FULL], 0);
+            for (int s = 0; s < 2; ++s)
+                if (last[s] >= 0) mbar_drain(&bars[I_Q_FULL + s], (last[s] >> 1) & 1);
+        }
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(128, kImpQRows);
+            const uint32_t aK = smem_u32(sK);
+            bool ok = mbar_wait(&bars[I_KROT], 0, abort_flag);
+            for (int qc = 0; ok && qc < n_qc; ++qc) {
+                const int b = qc & 1;
+                if (!mbar_wait(&bars[I_Q_FULL + b], (qc >> 1) & 1, abort_flag)) break;
+                if (qc >= 2 && !mbar_wait(&bars[I_ACC_FREE + b], ((qc >> 1) - 1) & 1, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t aQ = smem_u32(sQs(b));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t a = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
+                    const uint64_t bq = desc_sw128_kmajor(aQ + (kk >> 2) * (kImpQRows * 128) + (kk & 3) * 32);
+                    mma_bf16_ss(tmem + b * kImpQRows, a, bq, idesc, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars[I_ACC_FULL + b]);
+                mma_commit(&bars[I_Q_EMPTY + b]);
+            }
+            mma_commit(&bars[I_DRAIN]);
+            mbar_drain(&bars[I_DRAIN], 0);
+        }
+    } else {
+        // warps 0-3: rotate the key tile, then sum exp over the query rows for one key per thread
+        constexpr int CPR = D / 16;
+        constexpr int RGN = kTileKeys / (CPR * kPagesPerTile);
+        constexpr int RPT = kPage / RGN;
+        const int c = tid % CPR;
+        const int rg = tid / (CPR * kPagesPerTile);
+        float2 cs_start[8], cs_step[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            cs_start[i] = prm.rope[(rg * RPT) * (D / 2) + 8 * c + i];
+            cs_step[i] = prm.rope[1 * (D / 2) + 8 * c + i];
+        }
+        bool ok = mbar_wait(&bars[I_K_FULL], 0, abort_flag);
+        if (ok) rotate_cached_tile<D, false>(sK, sCs, sKpos, tid, t, n_pages, page_pos, nullptr, cs_start, cs_step);
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[I_KROT]);
+        const int chunks = R[R_LSE_CHUNKS];
+        const float2* part_in = prm.lse_part + R[R_LSE_BASE] + (int64_t)kvh * n_q * chunks;
+        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        const float scale = prm.scale_log2;
+        float acc = 0.f;
+        // every one of the 128 threads runs every iteration (named barriers inside): after an
+        // abort the work is skipped, the barrier count stays the same
+        for (int qc = 0; qc < n_qc; ++qc) {
+            const int b = qc & 1;
+            for (int rr = tid; rr < kImpQRows; rr += 128) {
+                const int n = qc * kImpQRows + rr;
+                float lse = INFINITY;
+                if (n < n_q) {
+                    float M = -INFINITY;
+                    for (int cidx = 0; cidx < chunks; ++cidx) M = fmaxf(M, part_in[(int64_t)n * chunks + cidx].x);
+                    float S = 0.f;
+                    for (int cidx = 0; cidx < chunks; ++cidx) {
+                        const float2 pl = part_in[(int64_t)n * chunks + cidx];
+                        S += pl.y * ex2(pl.x - M);
+                    }
+                    lse = S > 0.f ? M + log2f(S) : INFINITY;
+                }
+                sLse(b)[rr] = lse;
+            }
+            named_sync_128();
+            if (ok) ok = mbar_wait(&bars[I_ACC_FULL + b], (qc >> 1) & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) continue;
+            tc_fence_after();
+            const int nvalid = min(kImpQRows, n_q - qc * kImpQRows);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t sv[4][32];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    tmem_ld32(tmem + lane_addr + b * kImpQRows + half * 128 + cc * 32, sv[cc]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int n = half * 128 + cc * 32 + e;
+                        if (n < nvalid) acc += ex2(fmaf(__uint_as_float(sv[cc][e]), scale, -sLse(b)[n]));
+                    }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars[I_ACC_FREE + b]);
+        }
+        // per-kv-head partial, then the last CTA of this key tile sums the heads in order
+        const int total_tokens = L[L_TOTAL_TOKENS];
+        const bool valid_key = (t * kPagesPerTile + tid / kPage) < n_pages;
+        const int32_t tok = R[R_TOK_BASE] + t * kTileKeys + tid;
+        if (ok && valid_key) prm.part[(int64_t)kvh * total_tokens + tok] = acc;
+        __threadfence();
+        named_sync_128();
+        if (tid == 0) misc[5] = (atomicAdd(&prm.counters[R[R_KTILE_BASE] + t], 1) == Hkv - 1) ? 1 : 0;
+        named_sync_128();
+        if (misc[5]) {
+            __threadfence();
+            if (valid_key) {
+                float s = 0.f;
+                for (int h = 0; h < Hkv; ++h) s += __ldcg(prm.part + (int64_t)h * total_tokens + tok);
+                prm.importance[tok] = s;
+            }
+            if (tid == 0) prm.counters[R[R_KTILE_BASE] + t] = 0;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, SM::kTmemCols);
+    }
+}
+
+}  // namespace pcf

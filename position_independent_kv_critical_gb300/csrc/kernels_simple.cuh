@@ -1,0 +1,249 @@
+// Bandwidth-bound kernels of the hot path: rotation of per-request rows (query, fresh keys),
+// per-span radix top-k and the row gather of the recompute batch.
+#pragma once
+#include "layout_format.h"
+#include "ptx.cuh"
+
+namespace pcf {
+
+// ------------------------------------------------------------------ rope_rows
+// Rotates rows x[n_rows][H][D] (unrotated, bf16) at per-row positions and writes them in fp16
+// (the operand type of the Q K^T contractions), grouped by kv head for TMA:
+// out[((h / gg) * n_rows + row) * gg + h % gg][D].  Used for the query rows (gg = Hq/Hkv) and the
+// fresh keys (gg = 1) -- per-request data, rotated once; cached keys are never written rotated
+// (MiniPIC 2.1: the shared blocks stay position-free).
+struct RopeJob {
+    const __nv_bfloat16* x;
+    const int32_t* pos;      // [n_rows] logical position of every row
+    __half* out;
+    int32_t n_rows, heads, gg;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob a, RopeJob b, const float2* __restrict__ rope,
+                                                        int32_t max_pos, int64_t n_a) {
+    constexpr int CPR = D / 16;   // 16-byte chunk pairs per head row
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const RopeJob& J = gid < n_a ? a : b;
+    const int64_t lid = gid < n_a ? gid : gid - n_a;
+    const int64_t total = (int64_t)J.n_rows * J.heads * CPR;
+    if (J.x == nullptr || lid >= total) return;
+    const int c = (int)(lid % CPR);
+    const int64_t rh = lid / CPR;
+    const int h = (int)(rh % J.heads);
+    const int32_t row = (int32_t)(rh / J.heads);
+    const int32_t p = J.pos[row];
+    if (p < 0 || p >= max_pos) { set_dev_error(kDevErrBounds); return; }
+    const __nv_bfloat16* src = J.x + ((int64_t)row * J.heads + h) * D;
+    const uint4 xa = *reinterpret_cast<const uint4*>(src + 8 * c);
+    const uint4 xb = *reinterpret_cast<const uint4*>(src + D / 2 + 8 * c);
+    const float4* cs4 = reinterpret_cast<const float4*>(rope + (int64_t)p * (D / 2) + 8 * c);
+    float cs[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 v = __ldg(cs4 + q);
+        cs[4 * q] = v.x; cs[4 * q + 1] = v.y; cs[4 * q + 2] = v.z; cs[4 * q + 3] = v.w;
+    }
+    const uint32_t ia[4] = {xa.x, xa.y, xa.z, xa.w};
+    const uint32_t ib[4] = {xb.x, xb.y, xb.z, xb.w};
+    uint32_t oa[4], ob[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float c0 = cs[4 * e], s0 = cs[4 * e + 1], c1 = cs[4 * e + 2], s1 = cs[4 * e + 3];
+        const float a0 = bf16_lo(ia[e]), a1 = bf16_hi(ia[e]);
+        const float b0 = bf16_lo(ib[e]), b1 = bf16_hi(ib[e]);
+        oa[e] = pack_f16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
+        ob[e] = pack_f16x2(fmaf(b0, c0, a0 * s0), fmaf(b1, c1, a1 * s1));
+    }
+    const int64_t orow = ((int64_t)(h / J.gg) * J.n_rows + row) * J.gg + (h % J.gg);
+    __half* dst = J.out + orow * D;
+    *reinterpret_cast<uint4*>(dst + 8 * c) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    *reinterpret_cast<uint4*>(dst + D / 2 + 8 * c) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+}
+
+// ------------------------------------------------------------------ block scan helper
+template <int NT>
+__device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int t = lane < NW ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < NW) s_warp[lane] = t;   // inclusive warp prefix
+    }
+    __syncthreads();
+    const int before = (w > 0 ? s_warp[w - 1] : 0) + x - v;
+    if (total) *total = s_warp[NW - 1];
+    __syncthreads();
+    return before;
+}
+
+// ------------------------------------------------------------------ per-span top-k
+// QCFuse 2B: the Top-N tokens by critical-layer attention weight guide the recomputation; here
+// N is taken per span (k_s), ties go to the lower index.  Radix select on the fp32 bit patterns
+// (4 passes of 8 bits, shared-memory histograms), then two block scans in index order place the
+// selected tokens in ascending order.  Blocks [0, n_spans) handle one span each; blocks
+// [n_spans, n_spans + n_reqs) write the query rows' positions of one request each.
+constexpr int kTopkThreads = 256;
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const int32_t* __restrict__ L,
+                                                           const float* __restrict__ imp,
+                                                           int32_t* __restrict__ sel_idx,
+                                                           uint16_t* __restrict__ excl,
+                                                           int32_t* __restrict__ row_pos) {
+    extern __shared__ uint32_t s_bits[];   // selected-token bitmap of the span
+    __shared__ int s_hist[256];
+    __shared__ int s_warp[kTopkThreads / 32];
+    __shared__ int s_bucket, s_above;
+    const int n_spans = L[L_N_SPANS];
+    const int tid = threadIdx.x;
+    if ((int)blockIdx.x >= n_spans) {
+        const int b = blockIdx.x - n_spans;
+        const int32_t* R = L + L[L_OFF_REQ] + b * R_STRIDE;
+        const int32_t rb = R[R_ROW_BASE] + R[R_N_SEL];
+        for (int t = tid; t < R[R_N_QUERY]; t += kTopkThreads) row_pos[rb + t] = R[R_QUERY_POS0] + t;
+        return;
+    }
+    const int32_t* S = L + L[L_OFF_SPAN] + blockIdx.x * S_STRIDE;
+    const int32_t* R = L + L[L_OFF_REQ] + S[S_REQ] * R_STRIDE;
+    const int len = S[S_N_PAGES] * kPage;
+    const int k = S[S_K];
+    const int tok0 = S[S_PAGE_OFF] * kPage;              // request-local index of the span's first token
+    const float* v = imp + R[R_TOK_BASE] + tok0;
+    const int nwords = (len + 31) >> 5;
+    for (int i = tid; i < nwords; i += kTopkThreads) s_bits[i] = 0u;
+
+    uint32_t thr = 0;      // key of the k-th largest value
+    int need_eq = 0;       // how many tokens equal to thr are taken (lowest indices first)
+    if (k > 0 && k < len) {
+        uint32_t prefix = 0, pmask = 0;
+        int remaining = k;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            s_hist[tid] = 0;
+            __syncthreads();
+            for (int i = tid; i < len; i += kTopkThreads) {
+                const uint32_t key = order_key(v[i]);
+                if ((key & pmask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
+            }
+            __syncthreads();
+            if (tid < 32) {
+                // lane l owns buckets 255-8l .. 248-8l (descending)
+                int cnt[8], tot = 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) { cnt[q] = s_hist[255 - 8 * tid - q]; tot += cnt[q]; }
+                int incl = tot;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o) incl += y;
+                }
+                const int excl_sum = incl - tot;
+                const bool here = excl_sum < remaining && incl >= remaining;
+                const unsigned m = __ballot_sync(0xffffffffu, here);
+                if (here && tid == __ffs(m) - 1) {
+                    int acc = excl_sum;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        if (acc + cnt[q] >= remaining) { s_bucket = 255 - 8 * tid - q; s_above = acc; break; }
+                        acc += cnt[q];
+                    }
+                }
+            }
+            __syncthreads();
+            const int bucket = s_bucket;
+            remaining -= s_above;
+            prefix |= (uint32_t)bucket << shift;
+            pmask |= 255u << shift;
+            __syncthreads();
+        }
+        thr = prefix;
+        need_eq = remaining;
+    }
+    // contiguous index range per thread keeps index order in the scans
+    const int per = (len + kTopkThreads - 1) / kTopkThreads;
+    const int i0 = min(len, tid * per), i1 = min(len, i0 + per);
+    int n_eq = 0;
+    if (k > 0 && k < len)
+        for (int i = i0; i < i1; ++i) n_eq += (order_key(v[i]) == thr);
+    const int eq_before = block_excl_scan<kTopkThreads>(n_eq, s_warp, nullptr);
+    int n_sel = 0;
+    {
+        int eq_rank = eq_before;
+        for (int i = i0; i < i1; ++i) {
+            bool take;
+            if (k >= len) take = true;
+            else if (k == 0) take = false;
+            else {
+                const uint32_t key = order_key(v[i]);
+                take = key > thr || (key == thr && eq_rank < need_eq);
+                eq_rank += (key == thr);
+            }
+            if (take) { ++n_sel; atomicOr(&s_bits[i >> 5], 1u << (i & 31)); }
+        }
+    }
+    int total = 0;
+    const int out_before = block_excl_scan<kTopkThreads>(n_sel, s_warp, &total);
+    if (tid == 0 && total != k) set_dev_error(kDevErrBounds);
+    const int32_t sel_base = R[R_SEL_BASE] + S[S_SEL_OFF];
+    const int32_t rrow = R[R_ROW_BASE] + S[S_SEL_OFF];
+    const int32_t* ppos = L + L[L_OFF_PAGEPOS] + R[R_PAGE_BASE] + S[S_PAGE_OFF];
+    int o = out_before;
+    for (int i = i0; i < i1; ++i) {
+        if ((s_bits[i >> 5] >> (i & 31)) & 1u) {
+            if (o < k) {
+                sel_idx[sel_base + o] = tok0 + i;
+                row_pos[rrow + o] = ppos[i >> 4] + (i & 15);
+            }
+            ++o;
+        }
+    }
+    __syncthreads();
+    uint16_t* ex = excl + R[R_PAGE_BASE] + S[S_PAGE_OFF];
+    for (int p = tid; p < S[S_N_PAGES]; p += kTopkThreads)
+        ex[p] = (uint16_t)((s_bits[p >> 1] >> ((p & 1) * 16)) & 0xFFFFu);
+}
+
+// ------------------------------------------------------------------ row gather
+// dst[sel_base_b + i] = src[tok_base_b + sel_idx[sel_base_b + i]] -- the inputs of the tokens
+// chosen for recomputation (QCFuse Phase 4: discrete recomputation of the Top-N indices).
+__global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__ L,
+                                                     const int32_t* __restrict__ sel_idx,
+                                                     const uint4* __restrict__ src, int32_t row_chunks,
+                                                     uint4* __restrict__ dst) {
+    const int32_t r = blockIdx.x;
+    const int n_reqs = L[L_N_REQS];
+    const int32_t* REQ = L + L[L_OFF_REQ];
+    int lo = 0, hi = n_reqs - 1;   // last request with sel_base <= r
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (REQ[mid * R_STRIDE + R_SEL_BASE] <= r) lo = mid; else hi = mid - 1;
+    }
+    const int32_t* R = REQ + lo * R_STRIDE;
+    const int32_t j = sel_idx[r];
+    if (j < 0 || j >= R[R_N_PAGES] * kPage) {
+        if (threadIdx.x == 0) set_dev_error(kDevErrBounds);
+        return;
+    }
+    const uint4* s = src + (int64_t)(R[R_TOK_BASE] + j) * row_chunks;
+    uint4* d = dst + (int64_t)r * row_chunks;
+    for (int c = threadIdx.x; c < row_chunks; c += blockDim.x) d[c] = __ldg(s + c);
+}
+
+}  // namespace pcf

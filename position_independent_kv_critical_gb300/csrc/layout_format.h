@@ -1,0 +1,51 @@
+// Word map of the layout blob built by pcf_layout_build and read by the kernels.
+//
+// The blob carries everything the position-free cache needs per batch (MiniPIC, section 2.1:
+// per-request logical positions over shared physical blocks; section 2.2: spans padded to page
+// boundaries): the block table (logical page -> physical page), the logical position of each
+// page's first token, span and request records, and precomputed work lists so that no launch
+// needs host-side knowledge beyond the header.
+#pragma once
+#include <stdint.h>
+
+namespace pcf {
+
+constexpr int32_t kMagic = 0x4C464350;   // "PCFL"
+constexpr int kPage = 16;                // tokens per page
+constexpr int kTileRows = 128;           // TMEM lanes = rows of one MMA tile
+constexpr int kTileKeys = 128;           // keys per KV tile
+constexpr int kPagesPerTile = kTileKeys / kPage;
+constexpr int kMaxPosLimit = 1 << 20;
+constexpr int kItemWords = 4;
+constexpr int kLseTargetCtas = 2 * 152;  // GB300: 152 SMs; split keys until ~2 CTAs per SM
+
+enum : int {
+    L_MAGIC = 0, L_WORDS = 1, L_N_REQS = 2, L_HQ = 3, L_HKV = 4, L_D = 5, L_N_PHYS = 6,
+    L_MAX_POS = 7, L_TOTAL_TOKENS = 8, L_TOTAL_QUERY = 9, L_TOTAL_ROWS = 10, L_TOTAL_SEL = 11,
+    L_TOTAL_PAGES = 12, L_N_SPANS = 13, L_MAX_TOKENS = 14, L_MAX_ROWS = 15, L_MAX_QUERY = 16,
+    L_TOTAL_KTILES = 17, L_N_ATTN_ITEMS = 18, L_N_LSE_ITEMS = 19, L_N_IMP_ITEMS = 20,
+    L_LSE_SLOTS = 21, L_GROUP = 22, L_MAX_SPAN_LEN = 23,
+    L_OFF_REQ = 24, L_OFF_SPAN = 25, L_OFF_BLOCK = 26, L_OFF_PAGEPOS = 27, L_OFF_ATTN = 28,
+    L_OFF_LSE = 29, L_OFF_IMP = 30, L_OFF_QPOS = 31,
+    L_HEADER = 32
+};
+
+// per-request record
+enum : int {
+    R_N_PAGES = 0, R_TOK_BASE = 1, R_PAGE_BASE = 2, R_Q_BASE = 3, R_ROW_BASE = 4, R_SEL_BASE = 5,
+    R_QUERY_POS0 = 6, R_N_SPANS = 7, R_SPAN_BASE = 8, R_N_QUERY = 9, R_N_SEL = 10, R_N_ROWS = 11,
+    R_LSE_BASE = 12, R_LSE_CHUNKS = 13, R_KTILE_BASE = 14, R_N_KTILES = 15, R_STRIDE = 16
+};
+
+// per-span record
+enum : int {
+    S_REQ = 0, S_PAGE_OFF = 1, S_N_PAGES = 2, S_K = 3, S_SEL_OFF = 4, S_POS0 = 5,
+    S_PHYS_FIRST = 6, S_STRIDE = 8
+};
+
+// work items (kItemWords each)
+//   attention : {req, kv head, q tile, estimated cost}   sorted by cost, largest first
+//   lse       : {req, kv head, q tile, key chunk}
+//   importance: {req, key tile, kv head, 0}
+
+}  // namespace pcf

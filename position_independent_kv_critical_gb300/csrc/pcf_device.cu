@@ -1,0 +1,314 @@
+// Device entry points of the C ABI (include/pcf.h): argument checks, TMA tensor maps, workspace
+// carving and launches.  Every device buffer is the caller's; nothing here allocates.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/pcf.h"
+#include "kernel_attn.cuh"
+#include "kernel_imp.cuh"
+#include "kernels_simple.cuh"
+#include "layout_format.h"
+
+using namespace pcf;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// 2-D bf16 map over rows of `inner` elements (row stride `stride_bytes`), 128-byte swizzle,
+// box = 64 elements x box_rows rows.  An empty tensor gives an all-zero (never used) map.
+pcf_status make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_bytes,
+                       uint32_t box_rows, CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+    std::memset(m, 0, sizeof(*m));
+    if (rows == 0 || base == nullptr) return PCF_OK;
+    if (!get_encode()) return PCF_ERR_CUDA;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PCF_OK : PCF_ERR_CUDA;
+}
+
+// 3-D map over [n2][n1][inner] (v_fresh: [rows][Hkv][D]), box = 64 x 1 x box2.
+pcf_status make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t n1, uint64_t n2,
+                       uint32_t box2) {
+    std::memset(m, 0, sizeof(*m));
+    if (n2 == 0 || base == nullptr) return PCF_OK;
+    if (!get_encode()) return PCF_ERR_CUDA;
+    const cuuint64_t dims[3] = {inner, n1, n2};
+    const cuuint64_t strides[2] = {inner * 2, inner * n1 * 2};
+    const cuuint32_t box[3] = {64, 1, box2};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PCF_OK : PCF_ERR_CUDA;
+}
+
+constexpr CUtensorMapDataType kF16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pcf_status check_layout(const pcf_layout* lay) {
+    if (!lay || !lay->host || !lay->dev) return PCF_ERR_INVALID_ARG;
+    const int32_t* H = lay->host;
+    if (H[L_MAGIC] != kMagic || H[L_WORDS] < L_HEADER) return PCF_ERR_INVALID_ARG;
+    if (H[L_D] != 64 && H[L_D] != 128) return PCF_ERR_UNSUPPORTED;
+    return PCF_OK;
+}
+
+// sm_103 (GB300) must be the current device
+pcf_status check_device() {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PCF_ERR_NO_DEVICE;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return PCF_ERR_NO_DEVICE;
+    return (major == 10 && minor == 3) ? PCF_OK : PCF_ERR_NO_DEVICE;
+}
+
+pcf_status launched() { return cudaGetLastError() == cudaSuccess ? PCF_OK : PCF_ERR_CUDA; }
+
+size_t align_up(size_t x) { return (x + 1023) & ~size_t(1023); }
+
+struct ScoreWs {
+    size_t q, lse, part, cnt, total;
+};
+ScoreWs score_ws(const int32_t* H) {
+    ScoreWs w;
+    w.q = 0;
+    w.lse = align_up(w.q + (size_t)H[L_TOTAL_QUERY] * H[L_HQ] * H[L_D] * 2);
+    w.part = align_up(w.lse + (size_t)H[L_LSE_SLOTS] * sizeof(float2));
+    w.cnt = align_up(w.part + (size_t)H[L_HKV] * H[L_TOTAL_TOKENS] * sizeof(float));
+    w.total = align_up(w.cnt + (size_t)H[L_TOTAL_KTILES] * sizeof(int32_t));
+    return w;
+}
+
+struct AttnWs {
+    size_t q, k, total;
+};
+AttnWs attn_ws(const int32_t* H) {
+    AttnWs w;
+    w.q = 0;
+    w.k = align_up((size_t)H[L_TOTAL_ROWS] * H[L_HQ] * H[L_D] * 2);
+    w.total = align_up(w.k + (size_t)H[L_TOTAL_ROWS] * H[L_HKV] * H[L_D] * 2);
+    return w;
+}
+
+template <typename K>
+pcf_status set_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess
+               ? PCF_OK
+               : PCF_ERR_CUDA;
+}
+
+template <int D>
+pcf_status launch_rope(RopeJob a, RopeJob b, const float2* rope, int32_t max_pos, cudaStream_t st) {
+    const int64_t n_a = a.x ? (int64_t)a.n_rows * a.heads * (D / 16) : 0;
+    const int64_t n_b = b.x ? (int64_t)b.n_rows * b.heads * (D / 16) : 0;
+    if (n_a + n_b == 0) return PCF_OK;
+    const int64_t blocks = (n_a + n_b + 255) / 256;
+    rope_rows_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(a, b, rope, max_pos, n_a);
+    return launched();
+}
+
+template <int D>
+pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint16_t* k_pool, const float* rope,
+                      float* importance, void* ws, cudaStream_t st) {
+    const int32_t* H = lay->host;
+    const ScoreWs w = score_ws(H);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    __half* q_rot = reinterpret_cast<__half*>(base + w.q);
+    float2* lse = reinterpret_cast<float2*>(base + w.lse);
+    float* part = reinterpret_cast<float*>(base + w.part);
+    int32_t* cnt = reinterpret_cast<int32_t*>(base + w.cnt);
+    const int g = H[L_GROUP];
+    const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    const float2* rope2 = reinterpret_cast<const float2*>(rope);
+
+    if (H[L_TOTAL_KTILES] > 0 &&
+        cudaMemsetAsync(cnt, 0, (size_t)H[L_TOTAL_KTILES] * sizeof(int32_t), st) != cudaSuccess)
+        return PCF_ERR_CUDA;
+    RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_query), lay->dev + H[L_OFF_QPOS], q_rot, H[L_TOTAL_QUERY],
+               H[L_HQ], g};
+    RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1};
+    pcf_status s = launch_rope<D>(qj, none, rope2, H[L_MAX_POS], st);
+    if (s != PCF_OK) return s;
+
+    CUtensorMap tq128, tq256, tk, zero;
+    std::memset(&zero, 0, sizeof(zero));
+    const uint64_t qrows = (uint64_t)H[L_HKV] * H[L_TOTAL_QUERY] * g;
+    if ((s = make_map_2d(&tq128, q_rot, D, qrows, D * 2, 128, kF16)) != PCF_OK) return s;
+    if ((s = make_map_2d(&tq256, q_rot, D, qrows, D * 2, 256, kF16)) != PCF_OK) return s;
+    if ((s = make_map_2d(&tk, k_pool, D, (uint64_t)H[L_N_PHYS] * H[L_HKV] * kPage, D * 2, kPage)) != PCF_OK)
+        return s;
+
+    if (H[L_N_LSE_ITEMS] > 0) {
+        using SM = AttnSmem<D, true>;
+        auto kern = attn_kernel<D, true>;
+        if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
+        AttnParams p{lay->dev, nullptr, nullptr, rope2, nullptr, lse, scale_log2};
+        kern<<<H[L_N_LSE_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq128, tk, zero, zero, zero, p);
+        if ((s = launched()) != PCF_OK) return s;
+    }
+    if (H[L_N_IMP_ITEMS] > 0) {
+        using SM = ImpSmem<D>;
+        auto kern = imp_kernel<D>;
+        if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
+        ImpParams p{lay->dev, rope2, lse, part, cnt, importance, scale_log2};
+        kern<<<H[L_N_IMP_ITEMS], kImpThreads, SM::kAlloc, st>>>(tq256, tk, p);
+        if ((s = launched()) != PCF_OK) return s;
+    }
+    return PCF_OK;
+}
+
+template <int D>
+pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const uint16_t* k_fresh,
+                          const uint16_t* v_fresh, const uint16_t* k_pool, const uint16_t* v_pool,
+                          const uint16_t* excl, const int32_t* row_pos, const float* rope, uint16_t* out, void* ws,
+                          cudaStream_t st) {
+    const int32_t* H = lay->host;
+    if (H[L_N_ATTN_ITEMS] == 0) return PCF_OK;
+    const AttnWs w = attn_ws(H);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    __half* q_rot = reinterpret_cast<__half*>(base + w.q);
+    __half* k_rot = reinterpret_cast<__half*>(base + w.k);
+    const int g = H[L_GROUP];
+    const float2* rope2 = reinterpret_cast<const float2*>(rope);
+    const int32_t rows = H[L_TOTAL_ROWS];
+    RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_fresh), row_pos, q_rot, rows, H[L_HQ], g};
+    RopeJob kj{reinterpret_cast<const __nv_bfloat16*>(k_fresh), row_pos, k_rot, rows, H[L_HKV], 1};
+    pcf_status s = launch_rope<D>(qj, kj, rope2, H[L_MAX_POS], st);
+    if (s != PCF_OK) return s;
+
+    CUtensorMap tq, tkp, tvp, tkf, tvf;
+    const uint64_t pool_rows = (uint64_t)H[L_N_PHYS] * H[L_HKV] * kPage;
+    if ((s = make_map_2d(&tq, q_rot, D, (uint64_t)H[L_HKV] * rows * g, D * 2, 128, kF16)) != PCF_OK) return s;
+    if ((s = make_map_2d(&tkp, k_pool, D, pool_rows, D * 2, kPage)) != PCF_OK) return s;
+    if ((s = make_map_2d(&tvp, v_pool, D, pool_rows, D * 2, kPage)) != PCF_OK) return s;
+    if ((s = make_map_2d(&tkf, k_rot, D, (uint64_t)H[L_HKV] * rows, D * 2, 128, kF16)) != PCF_OK) return s;
+    if ((s = make_map_3d(&tvf, v_fresh, D, H[L_HKV], rows, 128)) != PCF_OK) return s;
+
+    using SM = AttnSmem<D, false>;
+    auto kern = attn_kernel<D, false>;
+    if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
+    const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    AttnParams p{lay->dev, excl, row_pos, rope2, reinterpret_cast<__nv_bfloat16*>(out), nullptr, scale_log2};
+    kern<<<H[L_N_ATTN_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq, tkp, tvp, tkf, tvf, p);
+    return launched();
+}
+
+}  // namespace
+
+extern "C" pcf_status pcf_score_workspace_bytes(const int32_t* layout_host, size_t* bytes) {
+    if (!layout_host || !bytes || layout_host[L_MAGIC] != kMagic) return PCF_ERR_INVALID_ARG;
+    *bytes = score_ws(layout_host).total;
+    return PCF_OK;
+}
+
+extern "C" pcf_status pcf_attention_workspace_bytes(const int32_t* layout_host, size_t* bytes) {
+    if (!layout_host || !bytes || layout_host[L_MAGIC] != kMagic) return PCF_ERR_INVALID_ARG;
+    *bytes = attn_ws(layout_host).total;
+    return PCF_OK;
+}
+
+extern "C" pcf_status pcf_score(const pcf_layout* layout, const uint16_t* q_query, const uint16_t* k_pool,
+                                const float* rope, float* importance, void* ws, size_t ws_bytes, void* stream) {
+    pcf_status s = check_layout(layout);
+    if (s != PCF_OK) return s;
+    const int32_t* H = layout->host;
+    if (H[L_TOTAL_TOKENS] == 0) return PCF_OK;
+    if (!k_pool || !rope || !importance || !ws || (H[L_TOTAL_QUERY] > 0 && !q_query)) return PCF_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(rope) || !aligned16(ws) || (q_query && !aligned16(q_query)))
+        return PCF_ERR_INVALID_ARG;
+    if (ws_bytes < score_ws(H).total) return PCF_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_device()) != PCF_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return H[L_D] == 128 ? score_impl<128>(layout, q_query, k_pool, rope, importance, ws, st)
+                         : score_impl<64>(layout, q_query, k_pool, rope, importance, ws, st);
+}
+
+extern "C" pcf_status pcf_select_topk(const pcf_layout* layout, const float* importance, int32_t* sel_idx,
+                                      uint16_t* excl, int32_t* row_pos, void* stream) {
+    pcf_status s = check_layout(layout);
+    if (s != PCF_OK) return s;
+    const int32_t* H = layout->host;
+    if ((H[L_TOTAL_TOKENS] > 0 && (!importance || !excl)) || (H[L_TOTAL_SEL] > 0 && !sel_idx) ||
+        (H[L_TOTAL_ROWS] > 0 && !row_pos))
+        return PCF_ERR_INVALID_ARG;
+    if ((s = check_device()) != PCF_OK) return s;
+    const int blocks = H[L_N_SPANS] + H[L_N_REQS];
+    const int words = (H[L_MAX_SPAN_LEN] + 31) / 32;
+    if (words * 4 > 48 * 1024) return PCF_ERR_UNSUPPORTED;
+    topk_kernel<<<blocks, kTopkThreads, words * 4, static_cast<cudaStream_t>(stream)>>>(layout->dev, importance,
+                                                                                        sel_idx, excl, row_pos);
+    return launched();
+}
+
+extern "C" pcf_status pcf_gather_rows(const pcf_layout* layout, const int32_t* sel_idx, const uint16_t* src,
+                                      int32_t row_elems, uint16_t* dst, void* stream) {
+    pcf_status s = check_layout(layout);
+    if (s != PCF_OK) return s;
+    const int32_t* H = layout->host;
+    if (row_elems <= 0 || row_elems % 8 != 0) return PCF_ERR_INVALID_ARG;
+    if (H[L_TOTAL_SEL] == 0) return PCF_OK;
+    if (!sel_idx || !src || !dst || !aligned16(src) || !aligned16(dst)) return PCF_ERR_INVALID_ARG;
+    if ((s = check_device()) != PCF_OK) return s;
+    gather_kernel<<<H[L_TOTAL_SEL], 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        layout->dev, sel_idx, reinterpret_cast<const uint4*>(src), row_elems / 8, reinterpret_cast<uint4*>(dst));
+    return launched();
+}
+
+extern "C" pcf_status pcf_fused_attention(const pcf_layout* layout, const uint16_t* q_fresh, const uint16_t* k_fresh,
+                                          const uint16_t* v_fresh, const uint16_t* k_pool, const uint16_t* v_pool,
+                                          const uint16_t* excl, const int32_t* row_pos, const float* rope,
+                                          uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+    pcf_status s = check_layout(layout);
+    if (s != PCF_OK) return s;
+    const int32_t* H = layout->host;
+    if (H[L_TOTAL_ROWS] == 0) return PCF_OK;
+    if (!q_fresh || !k_fresh || !v_fresh || !row_pos || !rope || !out || !ws) return PCF_ERR_INVALID_ARG;
+    if (H[L_TOTAL_TOKENS] > 0 && (!k_pool || !v_pool || !excl)) return PCF_ERR_INVALID_ARG;
+    const void* al[] = {q_fresh, k_fresh, v_fresh, rope, out, ws};
+    for (const void* p : al)
+        if (!aligned16(p)) return PCF_ERR_INVALID_ARG;
+    if ((k_pool && !aligned16(k_pool)) || (v_pool && !aligned16(v_pool))) return PCF_ERR_INVALID_ARG;
+    if (ws_bytes < attn_ws(H).total) return PCF_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_device()) != PCF_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return H[L_D] == 128
+               ? attention_impl<128>(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope, out, ws, st)
+               : attention_impl<64>(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope, out, ws, st);
+}
+
+extern "C" pcf_status pcf_check_device_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PCF_ERR_CUDA;
+    int code = 0;
+    if (cudaMemcpyFromSymbol(&code, g_pcf_dev_error, sizeof(int)) != cudaSuccess) return PCF_ERR_CUDA;
+    if (code != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_pcf_dev_error, &zero, sizeof(int)) != cudaSuccess) return PCF_ERR_CUDA;
+    }
+    if (code == kDevErrTimeout) return PCF_ERR_DEVICE_TIMEOUT;
+    if (code == kDevErrBounds) return PCF_ERR_DEVICE_BOUNDS;
+    return PCF_OK;
+}

@@ -1,0 +1,230 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs.
+
+Tolerances (stated for this path): fp32 importance within 1e-3 relative; bf16 attention output
+within 2e-2 absolute + 1e-2 relative; top-k, exclusion bits, row positions and the gather are
+bit-exact.  Top-k is fed the oracle's scores; the attention is fed the oracle's selection, so
+near-ties in the GPU scores cannot change which keys the attention sees.  Large workloads run in
+their full launch configuration and are checked on sampled requests / rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import position_independent_kv_critical_gb300 as pcf
+from oracle import method
+from workload import CONFIGS, PAGE, hidden_rows, make_batch, make_layout, small_custom_batch
+
+from gpu_util import GpuBatch, assert_close_imp, assert_close_out
+
+pytestmark = pytest.mark.gpu
+
+_cache = {}
+
+
+def gpu_batch(name, pct=None):
+    key = (name, pct)
+    if key not in _cache:
+        _cache.clear()
+        torch.cuda.empty_cache()
+        _cache[key] = GpuBatch(make_batch(name, pct))
+    return _cache[key]
+
+
+def _sample_rows(n_rows, n_sel, k=48):
+    rows = set(range(min(8, n_rows)))
+    rows |= set(range(max(0, n_sel - 4), min(n_rows, n_sel + 4)))
+    rows |= set(range(max(0, n_rows - 12), n_rows))
+    rng = np.random.default_rng(n_rows)
+    rows |= set(rng.choice(n_rows, size=min(n_rows, k), replace=False).tolist())
+    return np.array(sorted(rows))
+
+
+def check_batch(gb: GpuBatch, req_ids=None, sample_rows=False):
+    b = gb.b
+    ids = list(range(len(b.requests))) if req_ids is None else list(req_ids)
+    # 1) importance
+    got_imp = gb.score()
+    imps = {}
+    for i in ids:
+        r = b.requests[i]
+        exp = gb.oracle_score(i)
+        t0 = gb.tok_base[i]
+        assert_close_imp(got_imp[t0: t0 + r.n_cached], exp, f"importance req {i}")
+        imps[i] = exp.astype(np.float32)
+    # 2) top-k bit-exact on the oracle's scores (other requests: their GPU scores)
+    feed = got_imp.copy()
+    for i in ids:
+        feed[gb.tok_base[i]: gb.tok_base[i] + b.requests[i].n_cached] = imps[i]
+    sel, excl, row_pos = gb.topk(feed)
+    sels = []
+    for i, r in enumerate(b.requests):
+        s0 = gb.sel_base[i]
+        sels.append(sel[s0: s0 + r.n_sel].astype(np.int64))
+    for i in ids:
+        exp_sel = gb.oracle_select(i, imps[i])
+        assert np.array_equal(sels[i], exp_sel), f"top-k req {i}"
+    exp_excl, exp_rp = gb.selection_inputs(sels)
+    assert np.array_equal(excl, exp_excl)
+    assert np.array_equal(row_pos, exp_rp)
+    # 3) attention with the oracle's selection
+    out = gb.attention(exp_excl, exp_rp)
+    for i in ids:
+        r = b.requests[i]
+        rows = _sample_rows(r.n_rows, r.n_sel) if sample_rows else None
+        exp, _ = gb.oracle_attention(i, sels[i], rows=rows)
+        rb = gb.row_base[i]
+        got = out[rb: rb + r.n_rows]
+        got = got if rows is None else got[rows]
+        assert_close_out(got, exp, f"attention req {i}")
+
+
+# ------------------------------------------------------------------ the five workloads
+
+def test_tiny_full():
+    check_batch(gpu_batch("tiny"))
+
+
+def test_llama8b_layer_full():
+    check_batch(gpu_batch("llama8b_layer"))
+
+
+def test_concurrent_reuse_sampled():
+    check_batch(gpu_batch("concurrent_reuse"), req_ids=[0, 7, 31], sample_rows=True)
+
+
+@pytest.mark.parametrize("pct", [5, 10, 15, 20, 30])
+def test_long_context_sweep_sampled(pct):
+    check_batch(gpu_batch("long_context", pct), sample_rows=True)
+
+
+def test_batch70b_sampled():
+    check_batch(gpu_batch("batch70b"), req_ids=[0, 63], sample_rows=True)
+
+
+# ------------------------------------------------------------------ top-k at full size, planted ties
+
+@pytest.mark.parametrize("name", list(CONFIGS))
+def test_topk_bit_exact_planted_ties_full_size(name):
+    cfg = CONFIGS[name]
+    reqs = make_layout(cfg)
+    n_phys = cfg.pool_spans * cfg.span_len // PAGE
+    L = pcf.Layout(reqs, cfg.hq, cfg.hkv, cfg.d, n_phys, max(r.query_pos0 + r.n_query for r in reqs) + 1)
+    rng = np.random.default_rng(cfg.seed)
+    imp = (rng.integers(0, 24, size=L.total_tokens) * 0.03125).astype(np.float32)
+    dev_imp = torch.as_tensor(imp).cuda()
+    sel = torch.empty(L.total_sel, dtype=torch.int32, device="cuda")
+    ex = torch.empty(L.total_pages, dtype=torch.int16, device="cuda")
+    rp = torch.empty(L.total_rows, dtype=torch.int32, device="cuda")
+    pcf.select_topk(L, dev_imp, sel, ex, rp)
+    pcf.check_device_error()
+    sel = sel.cpu().numpy()
+    tb = sb = 0
+    for r in reqs:
+        exp = method.select_topk_request(imp[tb: tb + r.n_cached], [s.n_pages * 16 for s in r.spans],
+                                         [s.k for s in r.spans])
+        assert np.array_equal(sel[sb: sb + r.n_sel], exp)
+        tb += r.n_cached
+        sb += r.n_sel
+
+
+# ------------------------------------------------------------------ gather
+
+@pytest.mark.parametrize("name", ["tiny", "llama8b_layer"])
+def test_gather_bit_exact(name):
+    gb = gpu_batch(name)
+    D = gb.b.hq * gb.b.d
+    src = hidden_rows(torch.arange(gb.L.total_tokens, device="cuda"), D)
+    gb.score()
+    sel, _, _ = gb.topk()
+    dst = torch.empty((gb.L.total_sel, D), dtype=torch.bfloat16, device="cuda")
+    pcf.gather_rows(gb.L, gb.cf.sel_idx, src, dst)
+    pcf.check_device_error()
+    glob = np.concatenate([gb.tok_base[i] + sel[gb.sel_base[i]: gb.sel_base[i] + r.n_sel]
+                           for i, r in enumerate(gb.b.requests)])
+    exp = method.gather_rows(hidden_rows(torch.arange(gb.L.total_tokens), D).view(torch.int16).numpy(), glob)
+    assert np.array_equal(dst.cpu().view(torch.int16).numpy(), exp)
+
+
+def test_gpu_scores_to_gpu_topk_overlap():
+    gb = gpu_batch("llama8b_layer")
+    gb.score()
+    sel, _, _ = gb.topk()
+    exp = gb.oracle_select(0, gb.oracle_score(0).astype(np.float32))
+    overlap = len(np.intersect1d(sel, exp)) / len(exp)
+    assert overlap >= 0.99, overlap
+
+
+def test_score_is_deterministic():
+    gb = gpu_batch("llama8b_layer")
+    a = gb.score().copy()
+    b = gb.score().copy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+# ------------------------------------------------------------------ scenarios from the pages
+
+def test_offset_0_and_2048_share_physical_pages():
+    """MiniPIC 1 / 2.1: one physical span serves a request at offset 0 and one at 2048."""
+    b = small_custom_batch([(0, 8, 0, 20)], n_query=16, hq=8, hkv=2, d=128, theta=5e5,
+                           extra_requests=[([(0, 8, 2048, 20)], 16, 2048 + 128)])
+    check_batch(GpuBatch(b))
+
+
+def test_full_recompute_equals_full_prefill():
+    b = small_custom_batch([(0, 4, 0, 64), (4, 3, 64, 48)], n_query=9, hq=8, hkv=2, d=128, theta=5e5)
+    gb = GpuBatch(b)
+    r = b.requests[0]
+    sel = np.arange(r.n_cached)
+    excl, row_pos = gb.selection_inputs([sel])
+    out = gb.attention(excl, row_pos)
+    exp = method.full_prefill(b.q_fresh.double().numpy(), b.k_fresh.double().numpy(),
+                              b.v_fresh.double().numpy(), row_pos.astype(np.int64), b.theta)
+    assert_close_out(out, exp, "100% recompute")
+
+
+def test_fresh_equal_cached_gives_no_recompute_attention():
+    b = small_custom_batch([(0, 6, 0, 30), (6, 5, 100, 25)], n_query=12, hq=8, hkv=2, d=128, theta=5e5)
+    r = b.requests[0]
+    gb = GpuBatch(b)
+    rng = np.random.default_rng(3)
+    sel = np.sort(np.concatenate([rng.choice(96, 30, replace=False), 96 + rng.choice(80, 25, replace=False)]))
+    pages = [s.phys_first_page + i for s in r.spans for i in range(s.n_pages)]
+    kc = b.k_pool[pages].permute(0, 2, 1, 3).reshape(-1, b.hkv, b.d)
+    vc = b.v_pool[pages].permute(0, 2, 1, 3).reshape(-1, b.hkv, b.d)
+    gb.k_fresh[: len(sel)] = kc[sel].cuda()
+    gb.v_fresh[: len(sel)] = vc[sel].cuda()
+    excl, row_pos = gb.selection_inputs([sel])
+    out = gb.attention(excl, row_pos)[-r.n_query:]
+    _, K, V, kpos = gb.oracle_request(0)
+    qpos = method.row_positions(np.zeros(0, dtype=np.int64), kpos, r.n_query, r.query_pos0)
+    exp = method.fused_attention_request(b.q_fresh[-r.n_query:].double().numpy(),
+                                         b.k_fresh[-r.n_query:].double().numpy(),
+                                         b.v_fresh[-r.n_query:].double().numpy(), qpos, K, V, kpos,
+                                         np.zeros(0, dtype=np.int64), b.theta)
+    assert_close_out(out, exp, "fresh == cached")
+
+
+@pytest.mark.parametrize("case", [
+    dict(spans=[(0, 1, 0, 0)], n_query=1),                         # one page, nothing recomputed, T=1
+    dict(spans=[(0, 2, 5, 32)], n_query=3),                        # k = L
+    dict(spans=[(0, 3, 0, 1), (3, 5, 48, 7), (8, 1, 200, 16)], n_query=7),   # ragged spans
+    dict(spans=[], n_query=5),                                     # no cached spans at all
+    dict(spans=[(0, 9, 0, 30)], n_query=0),                        # no query rows
+])
+@pytest.mark.parametrize("shape", [dict(hq=4, hkv=4, d=64), dict(hq=16, hkv=2, d=128),
+                                   dict(hq=8, hkv=2, d=64)])
+def test_edge_cases(case, shape):
+    b = small_custom_batch(case["spans"], case["n_query"], n_phys_pages=12, theta=1e4, **shape)
+    check_batch(GpuBatch(b))
+
+
+def test_mixed_requests_in_one_batch():
+    b = small_custom_batch([(0, 3, 7, 5)], n_query=2, hq=8, hkv=2, d=128, theta=5e5, n_phys_pages=40,
+                           extra_requests=[([(3, 17, 100, 40), (20, 9, 2000, 3)], 33, 3000),
+                                           ([], 4, 10),
+                                           ([(0, 3, 9000, 48), (29, 11, 9100, 100)], 130, 9400)])
+    check_batch(GpuBatch(b))
+
+
+def test_device_error_word_clean_after_runs():
+    pcf.check_device_error()

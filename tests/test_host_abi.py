@@ -1,0 +1,191 @@
+"""Host-side tests of the C ABI (CPU only, no device compute): exports, layout build and
+validation, RoPE table, recompute counts."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import position_independent_kv_critical_gb300 as pcf
+from position_independent_kv_critical_gb300 import _lib
+from workload import CONFIGS, PAGE, make_layout, small_custom_batch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+# word map of the blob (mirrors the library's internal layout format; checked against totals)
+L_OFF_REQ, L_OFF_SPAN, L_OFF_BLOCK, L_OFF_PAGEPOS = 24, 25, 26, 27
+L_OFF_ATTN, L_OFF_LSE, L_OFF_IMP, L_OFF_QPOS = 28, 29, 30, 31
+L_N_ATTN, L_N_LSE, L_N_IMP = 18, 19, 20
+
+
+def test_library_exports_every_declared_symbol(lib):
+    with open(os.path.join(ROOT, "include", "pcf.h")) as fh:
+        text = fh.read()
+    declared = set(re.findall(r"^\s*(?:pcf_status|const char\*|int32_t)\s+(pcf_\w+)\s*\(", text, re.M))
+    assert declared == set(_lib.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(-7, 1):
+        s = lib.pcf_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.pcf_status_string(-99).decode() == "unknown status"
+
+
+def test_k_from_percent_matches_golden(lib):
+    with open(os.path.join(GOLDEN, "recompute_counts.txt")) as fh:
+        rows = [ln.split("#")[0].split() for ln in fh if ln.split("#")[0].strip()]
+    for pct, L, k in rows:
+        assert lib.pcf_k_from_percent(int(pct), int(L)) == int(k)
+    assert lib.pcf_k_from_percent(-1, 10) == -1
+
+
+@pytest.mark.parametrize("d,theta", [(64, 1e4), (128, 5e5)])
+def test_rope_table_within_one_ulp_of_fp64(d, theta):
+    max_pos = 4096
+    t = pcf.rope_table(d, theta, max_pos).numpy()
+    inv = theta ** (-2.0 * np.arange(d // 2) / d)
+    ang = np.arange(max_pos)[:, None] * inv[None, :]
+    for k, f in ((0, np.cos), (1, np.sin)):
+        ref = f(ang)
+        got = t[:, :, k].astype(np.float64)
+        ulp = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+        assert np.all(np.abs(got - ref) <= ulp)
+
+
+def test_rope_table_rejects_bad_args(lib):
+    buf = torch.empty(16 * 32 * 2, dtype=torch.float32)
+    p = ctypes.c_void_p(buf.data_ptr())
+    assert lib.pcf_rope_table_init(None, 64, 1e4, 16) == -1
+    assert lib.pcf_rope_table_init(p, 96, 1e4, 16) == -2
+    assert lib.pcf_rope_table_init(p, 64, 0.0, 16) == -1
+    assert lib.pcf_rope_table_init(p, 64, 1e4, 8) == -1
+
+
+def _blob(layout):
+    return layout.host.numpy()
+
+
+@pytest.mark.parametrize("name", list(CONFIGS))
+def test_layout_totals_and_block_table(name):
+    cfg = CONFIGS[name]
+    reqs = make_layout(cfg)
+    n_phys = cfg.pool_spans * cfg.span_len // PAGE
+    max_pos = max(r.query_pos0 + r.n_query for r in reqs)
+    L = pcf.Layout(reqs, cfg.hq, cfg.hkv, cfg.d, n_phys, max_pos, device="cpu")
+    assert L.total_tokens == sum(r.n_cached for r in reqs)
+    assert L.total_query == sum(r.n_query for r in reqs)
+    assert L.total_sel == sum(r.n_sel for r in reqs)
+    assert L.total_rows == sum(r.n_rows for r in reqs)
+    assert L.total_pages * PAGE == L.total_tokens
+    B = _blob(L)
+    blk = B[B[L_OFF_BLOCK]: B[L_OFF_BLOCK] + L.total_pages]
+    ppos = B[B[L_OFF_PAGEPOS]: B[L_OFF_PAGEPOS] + L.total_pages]
+    exp_blk = [s.phys_first_page + i for r in reqs for s in r.spans for i in range(s.n_pages)]
+    exp_pos = [s.pos0 + PAGE * i for r in reqs for s in r.spans for i in range(s.n_pages)]
+    assert blk.tolist() == exp_blk
+    assert ppos.tolist() == exp_pos
+    qpos = B[B[L_OFF_QPOS]: B[L_OFF_QPOS] + L.total_query]
+    assert qpos.tolist() == [r.query_pos0 + t for r in reqs for t in range(r.n_query)]
+    # every (request, kv head, 128-row tile) appears once in the attention work list
+    g = cfg.hq // cfg.hkv
+    items = B[B[L_OFF_ATTN]: B[L_OFF_ATTN] + 4 * B[L_N_ATTN]].reshape(-1, 4)
+    want = {(b, h, t) for b, r in enumerate(reqs) for h in range(cfg.hkv)
+            for t in range(-(-r.n_rows * g // 128))}
+    got = {tuple(x) for x in items[:, :3].tolist()}
+    assert got == want and len(items) == len(want)
+    assert np.all(np.diff(items[:, 3]) <= 0)   # largest estimated cost first
+    imp = B[B[L_OFF_IMP]: B[L_OFF_IMP] + 4 * B[L_N_IMP]].reshape(-1, 4)
+    assert len(imp) == sum(-(-r.n_cached // 128) for r in reqs) * cfg.hkv
+
+
+def test_shared_pages_at_two_offsets_in_one_batch():
+    # one physical span, two requests, logical offsets 0 and 2048 (position-free reuse)
+    b = small_custom_batch([(0, 2, 0, 3)], n_query=4, extra_requests=[([(0, 2, 2048, 3)], 4, 2080)])
+    L = pcf.Layout(b.requests, b.hq, b.hkv, b.d, b.n_phys_pages, 4096, device="cpu")
+    B = _blob(L)
+    blk = B[B[L_OFF_BLOCK]: B[L_OFF_BLOCK] + 4].tolist()
+    ppos = B[B[L_OFF_PAGEPOS]: B[L_OFF_PAGEPOS] + 4].tolist()
+    assert blk == [0, 1, 0, 1]
+    assert ppos == [0, 16, 2048, 2064]
+
+
+def _try_build(spans_list, hq=4, hkv=2, d=64, n_phys=8, max_pos=4096, n_query=4, qpos=None):
+    lib = _lib.load()
+    reqs = (_lib.RequestDesc * len(spans_list))()
+    keep = []
+    for i, spans in enumerate(spans_list):
+        arr = (_lib.SpanDesc * max(1, len(spans)))(*[_lib.SpanDesc(*s) for s in spans])
+        keep.append(arr)
+        end = max([s[2] + 16 * s[1] for s in spans] + [0])
+        reqs[i] = _lib.RequestDesc(len(spans), arr, n_query, end if qpos is None else qpos)
+    dims = _lib.Dims(hq, hkv, d, n_phys, max_pos)
+    n = ctypes.c_int64(0)
+    st = lib.pcf_layout_words(reqs, len(spans_list), ctypes.byref(dims), ctypes.byref(n))
+    if st != 0:
+        return st
+    buf = (ctypes.c_int32 * n.value)()
+    return lib.pcf_layout_build(reqs, len(spans_list), ctypes.byref(dims), buf, n.value)
+
+
+def test_layout_validation():
+    ok = [(0, 2, 0, 3), (2, 1, 40, 16)]
+    assert _try_build([ok]) == 0
+    assert _try_build([[(0, 2, 10, 3), (2, 1, 30, 0)]]) == -1       # overlapping positions
+    assert _try_build([[(0, 2, 10, 3), (2, 1, 5, 0)]]) == -1        # positions not increasing
+    assert _try_build([[(0, 2, 4090, 3)]]) == -1                     # beyond max_pos
+    assert _try_build([[(7, 2, 0, 3)]]) == -1                        # outside the pool
+    assert _try_build([[(0, 0, 0, 0)]]) == -1                        # empty span
+    assert _try_build([[(0, 1, 0, 17)]]) == -1                       # k > span length
+    assert _try_build([[(0, 1, 0, -1)]]) == -1                       # k < 0
+    assert _try_build([ok], qpos=20) == -1                           # query inside the spans
+    assert _try_build([ok], hq=6, hkv=4) == -2                       # Hq % Hkv != 0
+    assert _try_build([ok], d=96) == -2                              # head_dim not 64/128
+    assert _try_build([ok], hq=256, hkv=1) == -2                     # group larger than a tile
+    assert _try_build([[]]) == 0                                     # a request with no spans
+    lib = _lib.load()
+    dims = _lib.Dims(4, 2, 64, 8, 4096)
+    n = ctypes.c_int64(0)
+    assert lib.pcf_layout_words(None, 1, ctypes.byref(dims), ctypes.byref(n)) == -1
+    assert lib.pcf_layout_build(None, 1, ctypes.byref(dims), None, 0) == -1
+
+
+def test_layout_too_small_buffer_and_query():
+    lib = _lib.load()
+    spans = (_lib.SpanDesc * 1)(_lib.SpanDesc(0, 2, 0, 3))
+    reqs = (_lib.RequestDesc * 1)(_lib.RequestDesc(1, spans, 4, 32))
+    dims = _lib.Dims(4, 2, 64, 8, 4096)
+    n = ctypes.c_int64(0)
+    assert lib.pcf_layout_words(reqs, 1, ctypes.byref(dims), ctypes.byref(n)) == 0
+    small = (ctypes.c_int32 * (n.value - 1))()
+    assert lib.pcf_layout_build(reqs, 1, ctypes.byref(dims), small, n.value - 1) == -1
+    buf = (ctypes.c_int32 * n.value)()
+    assert lib.pcf_layout_build(reqs, 1, ctypes.byref(dims), buf, n.value) == 0
+    v = ctypes.c_int64(0)
+    assert lib.pcf_layout_query(buf, 8, ctypes.byref(v)) == 0 and v.value == 32
+    assert lib.pcf_layout_query(buf, 99, ctypes.byref(v)) == -1
+    ws = ctypes.c_size_t(0)
+    assert lib.pcf_score_workspace_bytes(buf, ctypes.byref(ws)) == 0 and ws.value > 0
+    assert lib.pcf_attention_workspace_bytes(buf, ctypes.byref(ws)) == 0 and ws.value > 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_device_calls_fail_loudly_without_gpu():
+    b = small_custom_batch([(0, 2, 0, 3)], n_query=4)
+    L = pcf.Layout(b.requests, b.hq, b.hkv, b.d, b.n_phys_pages, 4096, device="cpu")
+    imp = torch.empty(32, dtype=torch.float32)
+    sel = torch.empty(3, dtype=torch.int32)
+    ex = torch.empty(2, dtype=torch.int16)
+    rp = torch.empty(7, dtype=torch.int32)
+    with pytest.raises(pcf.PcfError) as e:
+        lib = _lib.load()
+        _lib.check("pcf_select_topk", lib.pcf_select_topk(
+            ctypes.byref(L.ref), ctypes.c_void_p(imp.data_ptr()), ctypes.c_void_p(sel.data_ptr()),
+            ctypes.c_void_p(ex.data_ptr()), ctypes.c_void_p(rp.data_ptr()), None))
+    assert e.value.status == -7
