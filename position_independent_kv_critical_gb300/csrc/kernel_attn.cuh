@@ -107,22 +107,22 @@ __device__ __forceinline__ void rotate_chunk_pair(uint8_t* sK, int row, int c, c
 // c of rows rg*RPT .. rg*RPT+RPT-1 of page pg; it composes the page-base angle with its first
 // row's offset once and then advances the angle by one position per row.
 // Writes key_pos (INT_MAX for missing or excluded tokens).
-template <int D, bool WITH_EXCL>
+template <int D>
+__device__ __forceinline__ int rot_page_of(int rt) { return (rt / (D / 16)) % kPagesPerTile; }
+// `p0` / `ex`: logical position of the page's first token and its exclusion bits (prefetched by
+// the caller one tile ahead); `page_valid` false for pages past the request's end.
+template <int D>
 __device__ __forceinline__ void rotate_cached_tile(uint8_t* sK, const float2* sCs, int32_t* kpos, int rt,
-                                                   int tile, int n_pages, const int32_t* page_pos,
-                                                   const uint16_t* excl, const float2 (&cs_start)[8],
-                                                   const float2 (&cs_step)[8]) {
+                                                   bool page_valid, int32_t p0, uint32_t ex,
+                                                   const float2 (&cs_start)[8], const float2 (&cs_step)[8]) {
     constexpr int CPR = D / 16;
     constexpr int RGN = kTileKeys / (CPR * kPagesPerTile);
     constexpr int RPT = kPage / RGN;
     const int c = rt % CPR;
     const int pg = (rt / CPR) % kPagesPerTile;
     const int rg = rt / (CPR * kPagesPerTile);
-    const int lp = tile * kPagesPerTile + pg;
     const int row0 = pg * kPage + rg * RPT;
-    if (lp < n_pages) {
-        const int32_t p0 = page_pos[lp];
-        const uint32_t ex = WITH_EXCL ? (uint32_t)excl[lp] : 0u;
+    if (page_valid) {
         float2 cs[8];
         const float4* b4 = reinterpret_cast<const float4*>(sCs + pg * (D / 2) + 8 * c);
 #pragma unroll
@@ -234,6 +234,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ TMA producer
+        // Lane p (< 8) fetches the block-table entry and position of page p of the next tile while
+        // the current one is issued, then issues that page's copies itself.
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_kpool);
@@ -246,41 +248,55 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                                    : (kvh * L[L_TOTAL_ROWS] + row_base + row0) * g;
             mbar_arrive_expect_tx(&bars[B_Q_FULL], SM::kQ);
             for (int hb = 0; hb < H; ++hb) tma_load_2d(sQ + hb * 16384, &tm_q, &bars[B_Q_FULL], hb * 64, qy);
-            const int n_phys = L[L_N_PHYS];
-            int last[2] = {-1, -1};
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !mbar_wait(&bars[B_KV_EMPTY + st], ((j >> 1) - 1) & 1, abort_flag)) break;
-                uint64_t* full = &bars[B_TMA_FULL + st];
-                if (j < n_ct) {
-                    const int lp0 = (t0 + j) * kPagesPerTile;
-                    const int np = min(kPagesPerTile, n_pages - lp0);
-                    const uint32_t per_page = H * 2048 * (LSE ? 1 : 2) + (D / 2) * 8;
-                    mbar_arrive_expect_tx(full, per_page * np);
-                    for (int p = 0; p < np; ++p) {
-                        int32_t phys = blk[lp0 + p];
-                        if (phys < 0 || phys >= n_phys) { set_dev_error(kDevErrBounds); phys = 0; }
-                        const int32_t y = (phys * Hkv + kvh) * kPage;
-                        for (int hb = 0; hb < H; ++hb) {
-                            tma_load_2d(sKs(st) + hb * 16384 + p * 2048, &tm_kpool, full, hb * 64, y);
-                            if (!LSE) tma_load_2d(sVs(st) + hb * 16384 + p * 2048, &tm_vpool, full, hb * 64, y);
-                        }
-                        bulk_load(sCs(st) + p * (D / 2), prm.rope + (int64_t)page_pos[lp0 + p] * (D / 2),
-                                  (D / 2) * 8, full);
-                    }
-                } else if (!LSE) {
-                    const int32_t fr = row_base + (j - n_ct) * kTileKeys;
-                    mbar_arrive_expect_tx(full, H * 16384 * 2);
-                    for (int hb = 0; hb < H; ++hb) {
-                        tma_load_2d(sKs(st) + hb * 16384, &tm_kfresh, full, hb * 64, kvh * L[L_TOTAL_ROWS] + fr);
-                        tma_load_3d(sVs(st) + hb * 16384, &tm_vfresh, full, hb * 64, kvh, fr);
-                    }
-                }
-                last[st] = j;
+        }
+        const int n_phys = L[L_N_PHYS];
+        auto meta = [&](int j, int32_t& ph, int32_t& pp) {
+            ph = -1;
+            pp = 0;
+            if (j < n_ct && lane < kPagesPerTile) {
+                const int lp = (t0 + j) * kPagesPerTile + lane;
+                if (lp < n_pages) { ph = blk[lp]; pp = page_pos[lp]; }
             }
+        };
+        int32_t ph_next, pp_next;
+        meta(0, ph_next, pp_next);
+        int last[2] = {-1, -1};
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j & 1;
+            int32_t ph = ph_next, pp = pp_next;
+            meta(j + 1, ph_next, pp_next);
+            bool ok = j < 2 || mbar_wait(&bars[B_KV_EMPTY + st], ((j >> 1) - 1) & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            uint64_t* full = &bars[B_TMA_FULL + st];
+            if (j < n_ct) {
+                const int np = min(kPagesPerTile, n_pages - (t0 + j) * kPagesPerTile);
+                constexpr uint32_t per_page = H * 2048 * (LSE ? 1 : 2) + (D / 2) * 8;
+                if (lane == 0) mbar_arrive_expect_tx(full, per_page * np);
+                __syncwarp();
+                if (lane < np) {
+                    if (ph < 0 || ph >= n_phys) { set_dev_error(kDevErrBounds); ph = 0; }
+                    const int32_t y = (ph * Hkv + kvh) * kPage;
+#pragma unroll
+                    for (int hb = 0; hb < H; ++hb) {
+                        tma_load_2d(sKs(st) + hb * 16384 + lane * 2048, &tm_kpool, full, hb * 64, y);
+                        if (!LSE) tma_load_2d(sVs(st) + hb * 16384 + lane * 2048, &tm_vpool, full, hb * 64, y);
+                    }
+                    bulk_load(sCs(st) + lane * (D / 2), prm.rope + (int64_t)pp * (D / 2), (D / 2) * 8, full);
+                }
+            } else if (!LSE && lane == 0) {
+                const int32_t fr = row_base + (j - n_ct) * kTileKeys;
+                mbar_arrive_expect_tx(full, H * 16384 * 2);
+                for (int hb = 0; hb < H; ++hb) {
+                    tma_load_2d(sKs(st) + hb * 16384, &tm_kfresh, full, hb * 64, kvh * L[L_TOTAL_ROWS] + fr);
+                    tma_load_3d(sVs(st) + hb * 16384, &tm_vfresh, full, hb * 64, kvh, fr);
+                }
+            }
+            last[st] = j;
+        }
+        if (lane == 0) {
             mbar_drain(&bars[B_Q_FULL], 0);
-            for (int s = 0; s < 2; ++s)
-                if (last[s] >= 0) mbar_drain(&bars[B_TMA_FULL + s], (last[s] >> 1) & 1);
+            for (int s2 = 0; s2 < 2; ++s2)
+                if (last[s2] >= 0) mbar_drain(&bars[B_TMA_FULL + s2], (last[s2] >> 1) & 1);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
@@ -341,16 +357,38 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             cs_start[i] = prm.rope[(rg * RPT) * (D / 2) + 8 * c + i];
             cs_step[i] = prm.rope[1 * (D / 2) + 8 * c + i];
         }
+        const int pg = rot_page_of<D>(rt);
+        // metadata of the next tile, fetched one tile ahead: cached tiles (page position, exclusion
+        // bits of this thread's page), fresh tiles (position of key rt)
+        auto meta = [&](int j, int32_t& m0, uint32_t& m1) {
+            m0 = kNoPos;
+            m1 = 0u;
+            if (j < n_ct) {
+                const int lp = (t0 + j) * kPagesPerTile + pg;
+                if (lp < n_pages) {
+                    m0 = page_pos[lp];
+                    m1 = LSE ? 0u : (uint32_t)prm.excl[page_base + lp];
+                }
+            } else if (j < n_tiles) {
+                const int fr = (j - n_ct) * kTileKeys + rt;
+                if (fr < n_rows_req) m0 = prm.row_pos[row_base + fr];
+            }
+        };
+        int32_t m0n;
+        uint32_t m1n;
+        meta(0, m0n, m1n);
         for (int j = 0; j < n_tiles; ++j) {
             const int st = j & 1;
+            const int32_t m0 = m0n;
+            const uint32_t m1 = m1n;
+            meta(j + 1, m0n, m1n);
             if (!mbar_wait(&bars[B_TMA_FULL + st], (j >> 1) & 1, abort_flag)) break;
             if (j >= 2 && !mbar_wait(&bars[B_KPOS_FREE + st], ((j >> 1) - 1) & 1, abort_flag)) break;
             if (j < n_ct) {
-                rotate_cached_tile<D, !LSE>(sKs(st), sCs(st), sKpos(st), rt, t0 + j, n_pages, page_pos,
-                                            LSE ? nullptr : prm.excl + page_base, cs_start, cs_step);
+                const bool pv = (t0 + j) * kPagesPerTile + pg < n_pages;
+                rotate_cached_tile<D>(sKs(st), sCs(st), sKpos(st), rt, pv, m0, m1, cs_start, cs_step);
             } else {
-                const int fr = (j - n_ct) * kTileKeys + rt;
-                sKpos(st)[rt] = fr < n_rows_req ? prm.row_pos[row_base + fr] : kNoPos;
+                sKpos(st)[rt] = m0;
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars[B_KROT_FULL + st]);

@@ -103,22 +103,24 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint32_t tmem = static_cast<uint32_t>(misc[0]);
 
     if (warp == kWarpTma) {
+        const int lp0 = t * kPagesPerTile;
+        const int np = min(kPagesPerTile, n_pages - lp0);
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_kpool);
-            const int lp0 = t * kPagesPerTile;
-            const int np = min(kPagesPerTile, n_pages - lp0);
-            const int n_phys = L[L_N_PHYS];
             mbar_arrive_expect_tx(&bars[I_K_FULL], np * (H * 2048 + (D / 2) * 8));
-            for (int p = 0; p < np; ++p) {
-                int32_t phys = blk[lp0 + p];
-                if (phys < 0 || phys >= n_phys) { set_dev_error(kDevErrBounds); phys = 0; }
-                const int32_t y = (phys * Hkv + kvh) * kPage;
-                for (int hb = 0; hb < H; ++hb)
-                    tma_load_2d(sK + hb * 16384 + p * 2048, &tm_kpool, &bars[I_K_FULL], hb * 64, y);
-                bulk_load(sCs + p * (D / 2), prm.rope + (int64_t)page_pos[lp0 + p] * (D / 2), (D / 2) * 8,
-                          &bars[I_K_FULL]);
-            }
+        }
+        __syncwarp();
+        if (lane < np) {   // lane p issues page p
+            int32_t phys = blk[lp0 + lane];
+            const int32_t pp = page_pos[lp0 + lane];
+            if (phys < 0 || phys >= L[L_N_PHYS]) { set_dev_error(kDevErrBounds); phys = 0; }
+            const int32_t y = (phys * Hkv + kvh) * kPage;
+            for (int hb = 0; hb < H; ++hb)
+                tma_load_2d(sK + hb * 16384 + lane * 2048, &tm_kpool, &bars[I_K_FULL], hb * 64, y);
+            bulk_load(sCs + lane * (D / 2), prm.rope + (int64_t)pp * (D / 2), (D / 2) * 8, &bars[I_K_FULL]);
+        }
+        if (lane == 0) {
             const int32_t qy0 = (kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE]) * g;
             int last[2] = {-1, -1};
             for (int qc = 0; qc < n_qc; ++qc) {
@@ -170,8 +172,11 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             cs_start[i] = prm.rope[(rg * RPT) * (D / 2) + 8 * c + i];
             cs_step[i] = prm.rope[1 * (D / 2) + 8 * c + i];
         }
+        const int lp = t * kPagesPerTile + rot_page_of<D>(tid);
+        const bool pv = lp < n_pages;
+        const int32_t p0 = pv ? page_pos[lp] : 0;
         bool ok = mbar_wait(&bars[I_K_FULL], 0, abort_flag);
-        if (ok) rotate_cached_tile<D, false>(sK, sCs, sKpos, tid, t, n_pages, page_pos, nullptr, cs_start, cs_step);
+        if (ok) rotate_cached_tile<D>(sK, sCs, sKpos, tid, pv, p0, 0u, cs_start, cs_step);
         fence_proxy_async_smem();
         mbar_arrive(&bars[I_KROT]);
         const int chunks = R[R_LSE_CHUNKS];
