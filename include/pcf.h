@@ -170,6 +170,29 @@ pcf_status pcf_fused_attention(const pcf_layout* layout, const uint16_t* q_fresh
                                const uint16_t* excl, const int32_t* row_pos, const float* rope,
                                uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
+/* Largest scoring workspace pcf_score_noalloc can serve (16 MiB), i.e. the size of the scratch
+ * array built into the library. */
+#define PCF_SCORE_NOALLOC_MAX_WORKSPACE ((size_t)16 << 20)
+
+/* pcf_score without a caller workspace and without allocating anything.  (The paper has no
+ * counterpart: this is an integration aid.)  Same inputs, outputs, result and errors as pcf_score,
+ * but its scratch lives in a fixed array of PCF_SCORE_NOALLOC_MAX_WORKSPACE bytes compiled into
+ * the library, which every GPU that loads the library keeps until the process exits.
+ *   Who needs it: callers that may not call cudaMalloc or any allocating routine on this path --
+ *   e.g. a host engine whose memory pool has reserved all device memory up front, code running
+ *   under a strict real-time or fixed-memory budget, or plugin hosts whose allocator is not
+ *   reachable from the library.
+ *   Limit: a batch whose pcf_score_workspace_bytes exceeds the array size is rejected with
+ *   PCF_ERR_WORKSPACE_TOO_SMALL before any work is queued.
+ *   Set-up: the first call on each device looks up the array's device address (with that device
+ *   current); make that first call before any stream capture.
+ *   Sharing: every call on a device uses the same array, which keeps the last call's contents
+ *   (the call clears what must start at zero itself).  Calls that overlap on the GPU -- on
+ *   different streams, or from different threads -- race on it and must be serialized by the
+ *   caller. */
+pcf_status pcf_score_noalloc(const pcf_layout* layout, const uint16_t* q_query, const uint16_t* k_pool,
+                             const float* rope, float* importance, void* stream);
+
 /* Synchronizes `stream`, then reads and clears the device error word: PCF_OK,
  * PCF_ERR_DEVICE_TIMEOUT or PCF_ERR_DEVICE_BOUNDS (PCF_ERR_CUDA if the sync itself failed). */
 pcf_status pcf_check_device_error(void* stream);

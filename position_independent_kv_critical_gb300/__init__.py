@@ -22,7 +22,7 @@ from . import _lib
 from ._lib import PcfError  # noqa: F401
 
 __all__ = ["Layout", "CacheFusion", "PcfError", "k_from_percent", "rope_table", "score", "select_topk",
-           "gather_rows", "fused_attention", "check_device_error", "load_library"]
+           "gather_rows", "fused_attention", "check_device_error", "load_library", "score_noalloc"]
 
 
 def load_library():
@@ -137,6 +137,16 @@ def score(layout: Layout, q_query, k_pool, rope, importance, ws, stream=None):
     _lib.check("pcf_score", _lib.load().pcf_score(
         ctypes.byref(layout.ref), _p(q_query), _p(k_pool), _p(rope), _p(importance), _p(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def score_noalloc(layout: Layout, q_query, k_pool, rope, importance, stream=None):
+    """``score`` with the library's built-in scratch array instead of a workspace (no allocation)."""
+    _need(q_query, torch.bfloat16, "q_query")
+    _need(k_pool, torch.bfloat16, "k_pool")
+    _need(rope, torch.float32, "rope")
+    _need(importance, torch.float32, "importance")
+    _lib.check("pcf_score_noalloc", _lib.load().pcf_score_noalloc(
+        ctypes.byref(layout.ref), _p(q_query), _p(k_pool), _p(rope), _p(importance), _stream(stream)))
 
 
 def select_topk(layout: Layout, importance, sel_idx, excl, row_pos, stream=None):

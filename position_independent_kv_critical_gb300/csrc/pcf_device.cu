@@ -4,6 +4,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "../../include/pcf.h"
@@ -311,4 +312,48 @@ extern "C" pcf_status pcf_check_device_error(void* stream) {
     if (code == kDevErrTimeout) return PCF_ERR_DEVICE_TIMEOUT;
     if (code == kDevErrBounds) return PCF_ERR_DEVICE_BOUNDS;
     return PCF_OK;
+}
+
+// ------------------------------------------------------------------ allocation-free scoring
+// Scoring with its scratch inside the library image instead of a caller buffer, for callers that
+// must not allocate device memory on this path (see pcf_score_noalloc in pcf.h).  Every GPU that
+// loads the library holds this array until the process exits; all calls on a device share it.
+static __device__ __align__(256) uint8_t g_pcf_noalloc_ws[PCF_SCORE_NOALLOC_MAX_WORKSPACE];
+
+namespace {
+std::mutex g_noalloc_mu;
+std::map<int, void*> g_noalloc_ptr;   // device ordinal -> device address of g_pcf_noalloc_ws
+
+// The array's name is only a host-side stand-in in host code; its device address is looked up
+// once per device, with that device current.
+pcf_status noalloc_workspace(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PCF_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    auto it = g_noalloc_ptr.find(dev);
+    if (it == g_noalloc_ptr.end()) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pcf_noalloc_ws) != cudaSuccess || p == nullptr) return PCF_ERR_CUDA;
+        it = g_noalloc_ptr.emplace(dev, p).first;
+    }
+    *out = it->second;
+    return PCF_OK;
+}
+}  // namespace
+
+extern "C" pcf_status pcf_score_noalloc(const pcf_layout* layout, const uint16_t* q_query, const uint16_t* k_pool,
+                                        const float* rope, float* importance, void* stream) {
+    pcf_status s = check_layout(layout);
+    if (s != PCF_OK) return s;
+    const int32_t* H = layout->host;
+    if (H[L_TOTAL_TOKENS] == 0) return PCF_OK;
+    if (!k_pool || !rope || !importance || (H[L_TOTAL_QUERY] > 0 && !q_query)) return PCF_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(rope) || (q_query && !aligned16(q_query))) return PCF_ERR_INVALID_ARG;
+    if (score_ws(H).total > PCF_SCORE_NOALLOC_MAX_WORKSPACE) return PCF_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_device()) != PCF_OK) return s;
+    void* ws = nullptr;
+    if ((s = noalloc_workspace(&ws)) != PCF_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return H[L_D] == 128 ? score_impl<128>(layout, q_query, k_pool, rope, importance, ws, st)
+                         : score_impl<64>(layout, q_query, k_pool, rope, importance, ws, st);
 }
