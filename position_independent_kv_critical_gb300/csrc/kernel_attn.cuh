@@ -9,12 +9,14 @@
 //
 // One CTA = one tile of 128 query rows (the g query heads of 128/g consecutive rows of one
 // request, all sharing kv head `kvh`) against the request's KV tiles of 128 keys:
-//   warps 0-3  softmax: S row from TMEM, mask, online softmax (lazy rescale), P -> smem, O epilogue
-//   warp  4    TMEM allocation + single-thread tcgen05.mma issue
-//   warp  5    TMA producer: Q tile, cached K/V pages through the block table, page cos/sin rows,
-//              fresh K/V tiles
-//   warps 6-9  rotate cached K tiles in shared memory (in place, 128-byte swizzled K-major)
-// S = Q K^T (M=128, N=128, K=d) is double-buffered in TMEM; O (M=128, N=d) accumulates in TMEM.
+//   warps 0-3  softmax: S row from TMEM, mask, online softmax (lazy rescale), P -> TMEM, O epilogue
+//   warps 4-7  rotate cached K tiles in shared memory (in place, 128-byte swizzled K-major)
+//   warp  8    TMEM allocation + single-thread tcgen05.mma issue
+//   warp  9    K producer (TMA): Q tile, cached K pages through the block table with their page
+//              cos/sin rows, fresh K tiles; 3-stage ring, a stage is free once its Q K^T is done
+//   warp  10   V producer (TMA): cached V pages / fresh V tiles; 2-stage ring, freed by P V
+// S = Q K^T (M=128, N=128, K=d, fp16) is double-buffered in TMEM; P (bf16) is written to TMEM and
+// read from there as the A operand of O += P V (M=128, N=d, bf16); O accumulates in TMEM.
 // Cached keys are rotated by composing the page-base angle (cos/sin row of the page's first
 // position, copied per page) with the in-page offset, advanced row by row (angle addition).
 // LSE mode (critical-layer scoring, pass 1) runs the same pipeline without P/V and writes the
@@ -25,11 +27,17 @@
 
 namespace pcf {
 
-constexpr int kAttnThreads = 320;
-constexpr int kWarpMma = 4;
-constexpr int kWarpTma = 5;
-constexpr int kWarpRot0 = 6;
+constexpr int kAttnThreads = 352;
+constexpr int kWarpRot0 = 4;
+constexpr int kWarpMma = 8;
+constexpr int kWarpTma = 9;
+constexpr int kWarpTmaV = 10;
 constexpr int kNoPos = 0x7FFFFFFF;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+// TMEM columns: S double buffer [0,256), O [256, 256+d), P [384, 448) (bf16 pairs)
+constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemP = 384;
 
 struct AttnParams {
     const int32_t* layout;
@@ -38,7 +46,6 @@ struct AttnParams {
     const float2* rope;        // [max_pos][D/2] (cos, sin)
     __nv_bfloat16* out;        // attention: [rows][Hq][D]
     float2* lse_part;          // LSE: (running max in log2 units, running sum) per row and chunk
-    float scale_log2;          // log2(e) / sqrt(D)
 };
 
 template <int D, bool LSE>
@@ -47,16 +54,15 @@ struct AttnSmem {
     static constexpr int kQ = kTileRows * D * 2;
     static constexpr int kK = kTileKeys * D * 2;
     static constexpr int kV = LSE ? 0 : kTileKeys * D * 2;
-    static constexpr int kP = LSE ? 0 : kTileRows * kTileKeys * 2;
     static constexpr int kCs = kPagesPerTile * (D / 2) * 8;
     static constexpr int oQ = 0;
     static constexpr int oK = oQ + kQ;
-    static constexpr int oV = oK + 2 * kK;
-    static constexpr int oP = oV + 2 * kV;
-    static constexpr int oCs = oP + kP;
-    static constexpr int oKpos = oCs + 2 * kCs;
-    static constexpr int oBar = oKpos + 2 * kTileKeys * 4;
-    static constexpr int kNumBars = 16;
+    static constexpr int oV = oK + kKStages * kK;
+    static constexpr int oCs = oV + kVStages * kV;
+    static constexpr int oKpos = oCs + kKStages * kCs;
+    static constexpr int oKvalid = oKpos + kKStages * kTileKeys * 4;
+    static constexpr int oBar = oKvalid + kKStages * 16;
+    static constexpr int kNumBars = 24;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int kBytes = oMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
@@ -65,8 +71,18 @@ struct AttnSmem {
 
 // barrier slots
 enum : int {
-    B_Q_FULL = 0, B_TMA_FULL = 1 /*2*/, B_KROT_FULL = 3 /*2*/, B_KV_EMPTY = 5 /*2*/, B_S_FULL = 7 /*2*/,
-    B_S_FREE = 9 /*2*/, B_KPOS_FREE = 11 /*2*/, B_P_FULL = 13, B_P_FREE = 14, B_DRAIN = 15
+    B_Q_FULL = 0,
+    B_K_FULL = 1,      // [3] K pages (+ cos/sin rows) landed
+    B_KROT_FULL = 4,   // [3] K tile rotated, key positions written
+    B_K_EMPTY = 7,     // [3] Q K^T that read the stage is done
+    B_KPOS_FREE = 10,  // [3] softmax done with the stage's key positions
+    B_V_FULL = 13,     // [2]
+    B_V_EMPTY = 15,    // [2] P V that read the stage is done
+    B_S_FULL = 17,     // [2]
+    B_S_FREE = 19,     // [2]
+    B_P_FULL = 21,
+    B_P_FREE = 22,
+    B_DRAIN = 23
 };
 
 __device__ __forceinline__ float2 cmul(float2 a, float2 b) {
@@ -104,17 +120,16 @@ __device__ __forceinline__ void rotate_chunk_pair(uint8_t* sK, int row, int c, c
 }
 
 // Rotation of one cached K tile by 128 threads (rt = 0..127).  Thread (c, pg, rg) owns chunk pair
-// c of rows rg*RPT .. rg*RPT+RPT-1 of page pg; it composes the page-base angle with its first
-// row's offset once and then advances the angle by one position per row.
-// Writes key_pos (INT_MAX for missing or excluded tokens).
+// c of rows rg*RPT .. rg*RPT+RPT-1 of page pg; it composes the page-base angle (table row of the
+// page's first position, in sCs) with its first row's offset once and then advances the angle by
+// one position per row.  All rows are loaded before any is stored (no shared-memory round trip
+// per row).  Rows of missing pages hold stale finite data and are masked by the softmax.
 template <int D>
 __device__ __forceinline__ int rot_page_of(int rt) { return (rt / (D / 16)) % kPagesPerTile; }
-// `p0` / `ex`: logical position of the page's first token and its exclusion bits (prefetched by
-// the caller one tile ahead); `page_valid` false for pages past the request's end.
+
 template <int D>
-__device__ __forceinline__ void rotate_cached_tile(uint8_t* sK, const float2* sCs, int32_t* kpos, int rt,
-                                                   bool page_valid, int32_t p0, uint32_t ex,
-                                                   const float2 (&cs_start)[8], const float2 (&cs_step)[8]) {
+__device__ __forceinline__ void rotate_cached_tile(uint8_t* sK, const float2* sCs, int rt,
+                                                   const float2* __restrict__ cs_start_g, const float2 (&cs_step)[8]) {
     constexpr int CPR = D / 16;
     constexpr int RGN = kTileKeys / (CPR * kPagesPerTile);
     constexpr int RPT = kPage / RGN;
@@ -122,32 +137,62 @@ __device__ __forceinline__ void rotate_cached_tile(uint8_t* sK, const float2* sC
     const int pg = (rt / CPR) % kPagesPerTile;
     const int rg = rt / (CPR * kPagesPerTile);
     const int row0 = pg * kPage + rg * RPT;
-    if (page_valid) {
-        float2 cs[8];
-        const float4* b4 = reinterpret_cast<const float4*>(sCs + pg * (D / 2) + 8 * c);
+    const uint32_t off_b = D == 128 ? 16384u : 0u;
+    const int cb = D == 128 ? c : c + 4;
+    uint4 a[RPT], b[RPT];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 v = b4[q];
-            cs[2 * q] = cmul(make_float2(v.x, v.y), cs_start[2 * q]);
-            cs[2 * q + 1] = cmul(make_float2(v.z, v.w), cs_start[2 * q + 1]);
+    for (int r = 0; r < RPT; ++r) {
+        a[r] = *reinterpret_cast<const uint4*>(sK + sw128_off(row0 + r, c));
+        b[r] = *reinterpret_cast<const uint4*>(sK + off_b + sw128_off(row0 + r, cb));
+    }
+    float2 cs[8];
+    const float4* b4 = reinterpret_cast<const float4*>(sCs + pg * (D / 2) + 8 * c);
+    const float4* s4 = reinterpret_cast<const float4*>(cs_start_g);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 v = b4[q];
+        const float4 w = __ldg(s4 + q);
+        cs[2 * q] = cmul(make_float2(v.x, v.y), make_float2(w.x, w.y));
+        cs[2 * q + 1] = cmul(make_float2(v.z, v.w), make_float2(w.z, w.w));
+    }
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const uint32_t ia[4] = {a[r].x, a[r].y, a[r].z, a[r].w};
+        const uint32_t ib[4] = {b[r].x, b[r].y, b[r].z, b[r].w};
+        uint32_t oa[4], ob[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 c0 = cs[2 * e], c1 = cs[2 * e + 1];
+            const float a0 = bf16_lo(ia[e]), a1 = bf16_hi(ia[e]);
+            const float b0 = bf16_lo(ib[e]), b1 = bf16_hi(ib[e]);
+            oa[e] = pack_f16x2(fmaf(a0, c0.x, -b0 * c0.y), fmaf(a1, c1.x, -b1 * c1.y));
+            ob[e] = pack_f16x2(fmaf(b0, c0.x, a0 * c0.y), fmaf(b1, c1.x, a1 * c1.y));
         }
+        a[r] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+        b[r] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
 #pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-            const int off = rg * RPT + r;
-            const bool dropped = (ex >> off) & 1u;
-            if (!dropped) rotate_chunk_pair<D>(sK, row0 + r, c, cs);
-            if (c == 0) kpos[row0 + r] = dropped ? kNoPos : p0 + off;
+        for (int i = 0; i < 8; ++i) cs[i] = cmul(cs[i], cs_step[i]);
+    }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) cs[i] = cmul(cs[i], cs_step[i]);
-        }
-    } else if (c == 0) {
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) kpos[row0 + r] = kNoPos;
+    for (int r = 0; r < RPT; ++r) {
+        *reinterpret_cast<uint4*>(sK + sw128_off(row0 + r, c)) = a[r];
+        *reinterpret_cast<uint4*>(sK + off_b + sw128_off(row0 + r, cb)) = b[r];
     }
 }
 
+// Key bookkeeping of one tile, one key per thread (rt = key index): the key's logical position
+// (monotone over the tile: excluded tokens keep theirs, missing keys get INT_MAX) and a validity
+// mask word per warp (ballot) -- excluded and missing keys are invalid.
+__device__ __forceinline__ void write_key_info(int32_t* kpos, uint32_t* kvalid, int rt, int32_t pos, bool valid) {
+    kpos[rt] = pos;
+    const uint32_t w = __ballot_sync(0xffffffffu, valid);
+    if ((rt & 31) == 0) kvalid[rt >> 5] = w;
+}
+
+// 11 warps: at most 3 per SM sub-partition, so each thread may hold up to 168 registers; the
+// softmax works on 32-key slices of the S row to stay below that without spilling.
 template <int D, bool LSE>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kAttnThreads)
 attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kpool,
             const __grid_constant__ CUtensorMap tm_vpool, const __grid_constant__ CUtensorMap tm_kfresh,
             const __grid_constant__ CUtensorMap tm_vfresh, const AttnParams prm) {
@@ -158,9 +203,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     uint8_t* sQ = smem + SM::oQ;
     auto sKs = [&](int st) { return smem + SM::oK + st * SM::kK; };
     auto sVs = [&](int st) { return smem + SM::oV + st * SM::kV; };
-    uint8_t* sP = smem + SM::oP;
     auto sCs = [&](int st) { return reinterpret_cast<float2*>(smem + SM::oCs + st * SM::kCs); };
     auto sKpos = [&](int st) { return reinterpret_cast<int32_t*>(smem + SM::oKpos) + st * kTileKeys; };
+    auto sKvalid = [&](int st) { return reinterpret_cast<uint32_t*>(smem + SM::oKvalid) + st * 4; };
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::oBar);
     int32_t* misc = reinterpret_cast<int32_t*>(smem + SM::oMisc);
     // misc: [0] tmem base, [1] n cached tiles, [2] n fresh tiles, [3] first cached tile, [4] abort
@@ -184,13 +229,19 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
     if (tid == 0) {
         mbar_init(&bars[B_Q_FULL], 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars[B_TMA_FULL + s], 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&bars[B_K_FULL + s], 1);
             mbar_init(&bars[B_KROT_FULL + s], 128);
-            mbar_init(&bars[B_KV_EMPTY + s], 1);
+            mbar_init(&bars[B_K_EMPTY + s], 1);
+            mbar_init(&bars[B_KPOS_FREE + s], 128);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&bars[B_V_FULL + s], 1);
+            mbar_init(&bars[B_V_EMPTY + s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[B_S_FULL + s], 1);
             mbar_init(&bars[B_S_FREE + s], 128);
-            mbar_init(&bars[B_KPOS_FREE + s], 128);
         }
         mbar_init(&bars[B_P_FULL], 128);
         mbar_init(&bars[B_P_FREE], 1);
@@ -219,10 +270,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tmem_alloc(reinterpret_cast<uint32_t*>(misc), SM::kTmemCols);
         tmem_relinquish();
     }
-    // V stages and the P buffer start finite: masked keys contribute 0 * V
+    // V stages start finite: keys masked to P = 0 then contribute 0 * V
     if (!LSE) {
         uint4* z = reinterpret_cast<uint4*>(smem + SM::oV);
-        for (int i = tid; i < (2 * SM::kV) / 16; i += kAttnThreads) z[i] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < (kVStages * SM::kV) / 16; i += kAttnThreads) z[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -231,25 +282,21 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t tmem = static_cast<uint32_t>(misc[0]);
     const int n_ct = misc[1], n_ft = misc[2], t0 = misc[3];
     const int n_tiles = n_ct + n_ft;
+    const int n_phys = L[L_N_PHYS];
 
     if (warp == kWarpTma) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ K producer
         // Lane p (< 8) fetches the block-table entry and position of page p of the next tile while
-        // the current one is issued, then issues that page's copies itself.
+        // the current tile is issued, then issues that page's copies itself.
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_kpool);
-            if (!LSE) {
-                prefetch_tmap(&tm_vpool);
-                prefetch_tmap(&tm_kfresh);
-                prefetch_tmap(&tm_vfresh);
-            }
+            if (!LSE) prefetch_tmap(&tm_kfresh);
             const int32_t qy = LSE ? (kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row0) * g
                                    : (kvh * L[L_TOTAL_ROWS] + row_base + row0) * g;
             mbar_arrive_expect_tx(&bars[B_Q_FULL], SM::kQ);
             for (int hb = 0; hb < H; ++hb) tma_load_2d(sQ + hb * 16384, &tm_q, &bars[B_Q_FULL], hb * 64, qy);
         }
-        const int n_phys = L[L_N_PHYS];
         auto meta = [&](int j, int32_t& ph, int32_t& pp) {
             ph = -1;
             pp = 0;
@@ -260,43 +307,86 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         };
         int32_t ph_next, pp_next;
         meta(0, ph_next, pp_next);
-        int last[2] = {-1, -1};
+        int last[kKStages] = {-1, -1, -1};
         for (int j = 0; j < n_tiles; ++j) {
-            const int st = j & 1;
+            const int ks = j % kKStages;
             int32_t ph = ph_next, pp = pp_next;
             meta(j + 1, ph_next, pp_next);
-            bool ok = j < 2 || mbar_wait(&bars[B_KV_EMPTY + st], ((j >> 1) - 1) & 1, abort_flag);
+            const bool ok = j < kKStages ||
+                            mbar_wait(&bars[B_K_EMPTY + ks], ((j / kKStages) - 1) & 1, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) break;
-            uint64_t* full = &bars[B_TMA_FULL + st];
+            uint64_t* full = &bars[B_K_FULL + ks];
             if (j < n_ct) {
                 const int np = min(kPagesPerTile, n_pages - (t0 + j) * kPagesPerTile);
-                constexpr uint32_t per_page = H * 2048 * (LSE ? 1 : 2) + (D / 2) * 8;
+                constexpr uint32_t per_page = H * 2048 + (D / 2) * 8;
                 if (lane == 0) mbar_arrive_expect_tx(full, per_page * np);
                 __syncwarp();
                 if (lane < np) {
                     if (ph < 0 || ph >= n_phys) { set_dev_error(kDevErrBounds); ph = 0; }
                     const int32_t y = (ph * Hkv + kvh) * kPage;
 #pragma unroll
-                    for (int hb = 0; hb < H; ++hb) {
-                        tma_load_2d(sKs(st) + hb * 16384 + lane * 2048, &tm_kpool, full, hb * 64, y);
-                        if (!LSE) tma_load_2d(sVs(st) + hb * 16384 + lane * 2048, &tm_vpool, full, hb * 64, y);
-                    }
-                    bulk_load(sCs(st) + lane * (D / 2), prm.rope + (int64_t)pp * (D / 2), (D / 2) * 8, full);
+                    for (int hb = 0; hb < H; ++hb)
+                        tma_load_2d(sKs(ks) + hb * 16384 + lane * 2048, &tm_kpool, full, hb * 64, y);
+                    bulk_load(sCs(ks) + lane * (D / 2), prm.rope + (int64_t)pp * (D / 2), (D / 2) * 8, full);
                 }
             } else if (!LSE && lane == 0) {
                 const int32_t fr = row_base + (j - n_ct) * kTileKeys;
-                mbar_arrive_expect_tx(full, H * 16384 * 2);
-                for (int hb = 0; hb < H; ++hb) {
-                    tma_load_2d(sKs(st) + hb * 16384, &tm_kfresh, full, hb * 64, kvh * L[L_TOTAL_ROWS] + fr);
-                    tma_load_3d(sVs(st) + hb * 16384, &tm_vfresh, full, hb * 64, kvh, fr);
-                }
+                mbar_arrive_expect_tx(full, H * 16384);
+                for (int hb = 0; hb < H; ++hb)
+                    tma_load_2d(sKs(ks) + hb * 16384, &tm_kfresh, full, hb * 64, kvh * L[L_TOTAL_ROWS] + fr);
             }
-            last[st] = j;
+            last[ks] = j;
         }
         if (lane == 0) {
             mbar_drain(&bars[B_Q_FULL], 0);
-            for (int s2 = 0; s2 < 2; ++s2)
-                if (last[s2] >= 0) mbar_drain(&bars[B_TMA_FULL + s2], (last[s2] >> 1) & 1);
+            for (int s2 = 0; s2 < kKStages; ++s2)
+                if (last[s2] >= 0) mbar_drain(&bars[B_K_FULL + s2], (last[s2] / kKStages) & 1);
+        }
+    } else if (warp == kWarpTmaV) {
+        // ------------------------------------------------------------ V producer
+        if (!LSE) {
+            if (lane == 0) {
+                prefetch_tmap(&tm_vpool);
+                prefetch_tmap(&tm_vfresh);
+            }
+            auto meta = [&](int j) -> int32_t {
+                if (j < n_ct && lane < kPagesPerTile) {
+                    const int lp = (t0 + j) * kPagesPerTile + lane;
+                    if (lp < n_pages) return blk[lp];
+                }
+                return -1;
+            };
+            int32_t ph_next = meta(0);
+            int last[kVStages] = {-1, -1};
+            for (int j = 0; j < n_tiles; ++j) {
+                const int vs = j & 1;
+                int32_t ph = ph_next;
+                ph_next = meta(j + 1);
+                const bool ok = j < kVStages || mbar_wait(&bars[B_V_EMPTY + vs], ((j >> 1) - 1) & 1, abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                uint64_t* full = &bars[B_V_FULL + vs];
+                if (j < n_ct) {
+                    const int np = min(kPagesPerTile, n_pages - (t0 + j) * kPagesPerTile);
+                    if (lane == 0) mbar_arrive_expect_tx(full, H * 2048 * np);
+                    __syncwarp();
+                    if (lane < np) {
+                        if (ph < 0 || ph >= n_phys) { set_dev_error(kDevErrBounds); ph = 0; }
+                        const int32_t y = (ph * Hkv + kvh) * kPage;
+#pragma unroll
+                        for (int hb = 0; hb < H; ++hb)
+                            tma_load_2d(sVs(vs) + hb * 16384 + lane * 2048, &tm_vpool, full, hb * 64, y);
+                    }
+                } else if (lane == 0) {
+                    const int32_t fr = row_base + (j - n_ct) * kTileKeys;
+                    mbar_arrive_expect_tx(full, H * 16384);
+                    for (int hb = 0; hb < H; ++hb)
+                        tma_load_3d(sVs(vs) + hb * 16384, &tm_vfresh, full, hb * 64, kvh, fr);
+                }
+                last[vs] = j;
+            }
+            if (lane == 0)
+                for (int s2 = 0; s2 < kVStages; ++s2)
+                    if (last[s2] >= 0) mbar_drain(&bars[B_V_FULL + s2], (last[s2] >> 1) & 1);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
@@ -304,31 +394,32 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             constexpr uint32_t idesc_qk = idesc_f16(128, 128);
             constexpr uint32_t idesc_pv = idesc_bf16(128, 64, true);
             const uint32_t aQ = smem_u32(sQ);
-            const uint32_t aP = smem_u32(sP);
             bool ok = mbar_wait(&bars[B_Q_FULL], 0, abort_flag);
             auto issue_pv = [&](int i) -> bool {
+                const int vs = i & 1;
                 if (!mbar_wait(&bars[B_P_FULL], i & 1, abort_flag)) return false;
+                if (!mbar_wait(&bars[B_V_FULL + vs], (i >> 1) & 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t aV = smem_u32(sVs(i & 1));
+                const uint32_t aV = smem_u32(sVs(vs));
 #pragma unroll
                 for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-                    const uint64_t a = desc_sw128_kmajor(aP + (kk >> 2) * 16384 + (kk & 3) * 32);
 #pragma unroll
                     for (int nh = 0; nh < H; ++nh) {
                         const uint64_t b = desc_sw128_mn64(aV + nh * 16384 + kk * 2048);
-                        mma_bf16_ss(tmem + 256 + nh * 64, a, b, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                        mma_bf16_ts(tmem + kTmemO + nh * 64, tmem + kTmemP + kk * 8, b, idesc_pv,
+                                    (i > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
                 mma_commit(&bars[B_P_FREE]);
-                mma_commit(&bars[B_KV_EMPTY + (i & 1)]);
+                mma_commit(&bars[B_V_EMPTY + vs]);
                 return true;
             };
             for (int j = 0; ok && j < n_tiles; ++j) {
-                const int st = j & 1;
-                if (!mbar_wait(&bars[B_KROT_FULL + st], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+                const int st = j & 1, ks = j % kKStages;
+                if (!mbar_wait(&bars[B_KROT_FULL + ks], (j / kKStages) & 1, abort_flag)) { ok = false; break; }
                 if (j >= 2 && !mbar_wait(&bars[B_S_FREE + st], ((j >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t aK = smem_u32(sKs(st));
+                const uint32_t aK = smem_u32(sKs(ks));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t a = desc_sw128_kmajor(aQ + (kk >> 2) * 16384 + (kk & 3) * 32);
@@ -336,65 +427,63 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     mma_bf16_ss(tmem + st * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bars[B_S_FULL + st]);
-                if (LSE) mma_commit(&bars[B_KV_EMPTY + st]);
-                else if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+                mma_commit(&bars[B_K_EMPTY + ks]);
+                if (!LSE && j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
             }
             if (!LSE && ok && n_tiles > 0) issue_pv(n_tiles - 1);
             mma_commit(&bars[B_DRAIN]);
             mbar_drain(&bars[B_DRAIN], 0);
         }
-    } else if (warp >= kWarpRot0) {
-        // ------------------------------------------------------------ K rotation
+    } else if (warp >= kWarpRot0 && warp < kWarpMma) {
+        // ------------------------------------------------------------ K rotation (warps 4-7)
         const int rt = tid - kWarpRot0 * 32;
         constexpr int CPR = D / 16;
         constexpr int RGN = kTileKeys / (CPR * kPagesPerTile);
         constexpr int RPT = kPage / RGN;
         const int c = rt % CPR;
         const int rg = rt / (CPR * kPagesPerTile);
-        float2 cs_start[8], cs_step[8];
+        // angle of this thread's first in-page offset (table row rg*RPT) and of one position step
+        const float2* cs_start = prm.rope + (rg * RPT) * (D / 2) + 8 * c;
+        float2 cs_step[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            cs_start[i] = prm.rope[(rg * RPT) * (D / 2) + 8 * c + i];
-            cs_step[i] = prm.rope[1 * (D / 2) + 8 * c + i];
-        }
-        const int pg = rot_page_of<D>(rt);
-        // metadata of the next tile, fetched one tile ahead: cached tiles (page position, exclusion
-        // bits of this thread's page), fresh tiles (position of key rt)
-        auto meta = [&](int j, int32_t& m0, uint32_t& m1) {
-            m0 = kNoPos;
-            m1 = 0u;
+        for (int i = 0; i < 8; ++i) cs_step[i] = prm.rope[1 * (D / 2) + 8 * c + i];
+        // metadata of key rt of the next tile, fetched one tile ahead: logical position and
+        // whether the key takes part (cached: page present and token not recomputed; fresh: row
+        // present)
+        auto meta = [&](int j, int32_t& pos, bool& valid) {
+            pos = kNoPos;
+            valid = false;
             if (j < n_ct) {
-                const int lp = (t0 + j) * kPagesPerTile + pg;
+                const int lp = (t0 + j) * kPagesPerTile + rt / kPage;
                 if (lp < n_pages) {
-                    m0 = page_pos[lp];
-                    m1 = LSE ? 0u : (uint32_t)prm.excl[page_base + lp];
+                    pos = page_pos[lp] + (rt % kPage);
+                    const uint32_t ex = LSE ? 0u : (uint32_t)prm.excl[page_base + lp];
+                    valid = ((ex >> (rt % kPage)) & 1u) == 0u;
                 }
             } else if (j < n_tiles) {
                 const int fr = (j - n_ct) * kTileKeys + rt;
-                if (fr < n_rows_req) m0 = prm.row_pos[row_base + fr];
+                if (fr < n_rows_req) { pos = prm.row_pos[row_base + fr]; valid = true; }
             }
         };
-        int32_t m0n;
-        uint32_t m1n;
-        meta(0, m0n, m1n);
+        int32_t pos_n;
+        bool val_n;
+        meta(0, pos_n, val_n);
         for (int j = 0; j < n_tiles; ++j) {
-            const int st = j & 1;
-            const int32_t m0 = m0n;
-            const uint32_t m1 = m1n;
-            meta(j + 1, m0n, m1n);
-            if (!mbar_wait(&bars[B_TMA_FULL + st], (j >> 1) & 1, abort_flag)) break;
-            if (j >= 2 && !mbar_wait(&bars[B_KPOS_FREE + st], ((j >> 1) - 1) & 1, abort_flag)) break;
-            if (j < n_ct) {
-                const bool pv = (t0 + j) * kPagesPerTile + pg < n_pages;
-                rotate_cached_tile<D>(sKs(st), sCs(st), sKpos(st), rt, pv, m0, m1, cs_start, cs_step);
-            } else {
-                sKpos(st)[rt] = m0;
-            }
+            const int ks = j % kKStages;
+            const int32_t pos = pos_n;
+            const bool val = val_n;
+            meta(j + 1, pos_n, val_n);
+            bool ok = mbar_wait(&bars[B_K_FULL + ks], (j / kKStages) & 1, abort_flag);
+            ok = ok && (j < kKStages || mbar_wait(&bars[B_KPOS_FREE + ks], ((j / kKStages) - 1) & 1, abort_flag));
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (j < n_ct) rotate_cached_tile<D>(sKs(ks), sCs(ks), rt, cs_start, cs_step);
+            write_key_info(sKpos(ks), sKvalid(ks), rt, pos, val);
             fence_proxy_async_smem();
-            mbar_arrive(&bars[B_KROT_FULL + st]);
+            mbar_arrive(&bars[B_KROT_FULL + ks]);
         }
-    } else {
+    } else if (warp < kWarpRot0) {
         // ------------------------------------------------------------ softmax (warps 0-3)
+        // Scores arrive already in log2 units: the rotated query rows carry log2(e)/sqrt(d).
         const int m = tid;                 // tile row = TMEM lane
         const int tok = m / g, hl = m % g;
         const bool valid = tok < ntok;
@@ -403,104 +492,122 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (LSE) mypos = valid ? kNoPos - 1 : -1;
         else mypos = valid ? prm.row_pos[row_base + row] : -1;
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-        const float scale = prm.scale_log2;
+        // output locations, fixed before the tile loop so that only one pointer stays live across it
+        __nv_bfloat16* out_row = nullptr;
+        float2* lse_slot = nullptr;
+        if (valid) {
+            if (LSE)
+                lse_slot = prm.lse_part + R[R_LSE_BASE] +
+                           ((int64_t)kvh * (R[R_N_QUERY] * g) + row * g + hl) * R[R_LSE_CHUNKS] + chunk;
+            else
+                out_row = prm.out + ((int64_t)(row_base + row) * Hq + kvh * g + hl) * D;
+        }
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            const int st = j & 1;
+            const int st = j & 1, ks = j % kKStages;
             ok = mbar_wait(&bars[B_S_FULL + st], (j >> 1) & 1, abort_flag);
-            ok = ok && mbar_wait(&bars[B_KROT_FULL + st], (j >> 1) & 1, abort_flag);
+            ok = ok && mbar_wait(&bars[B_KROT_FULL + ks], (j / kKStages) & 1, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            uint32_t sv[4][32];
+            // visibility of the 128 keys for this row: keys are in increasing position order, so
+            // the visible ones are a prefix (binary search), minus the invalid ones (mask words)
+            uint32_t vis[4];
+            {
+                const int32_t* kp = sKpos(ks);
+                int lo = 0;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lane_addr + st * 128 + cc * 32, sv[cc]);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&bars[B_S_FREE + st]);
-            float mx = -INFINITY;
-            const int4* kp4 = reinterpret_cast<const int4*>(sKpos(st));
+                for (int step = 64; step >= 1; step >>= 1)
+                    if (kp[lo + step - 1] <= mypos) lo += step;
+                if (kp[lo] <= mypos) ++lo;   // lo <= 127 here; 128 when every key qualifies
+                const int cut = lo;   // number of keys with position <= mypos
+                const uint4 vw = *reinterpret_cast<const uint4*>(sKvalid(ks));
+                const uint32_t vv[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const int4 kp = kp4[q];
-                const int cc = q >> 3, e = (q & 7) * 4;
-                float v0 = kp.x <= mypos ? __uint_as_float(sv[cc][e + 0]) * scale : -INFINITY;
-                float v1 = kp.y <= mypos ? __uint_as_float(sv[cc][e + 1]) * scale : -INFINITY;
-                float v2 = kp.z <= mypos ? __uint_as_float(sv[cc][e + 2]) * scale : -INFINITY;
-                float v3 = kp.w <= mypos ? __uint_as_float(sv[cc][e + 3]) * scale : -INFINITY;
-                mx = fmaxf(mx, fmaxf(fmaxf(v0, v1), fmaxf(v2, v3)));
-                sv[cc][e + 0] = __float_as_uint(v0);
-                sv[cc][e + 1] = __float_as_uint(v1);
-                sv[cc][e + 2] = __float_as_uint(v2);
-                sv[cc][e + 3] = __float_as_uint(v3);
+                for (int w = 0; w < 4; ++w) {
+                    const int k = cut - 32 * w;
+                    const uint32_t pm = k >= 32 ? 0xffffffffu : (k <= 0 ? 0u : ((1u << k) - 1u));
+                    vis[w] = vv[w] & pm;
+                }
             }
-            mbar_arrive(&bars[B_KPOS_FREE + st]);
+            // pass 1: masked row max (two TMEM chunks per wait, four independent maxima)
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t sa[32], sb[32];
+                tmem_ld32(tmem + lane_addr + st * 128 + hh * 64, sa);
+                tmem_ld32(tmem + lane_addr + st * 128 + hh * 64 + 32, sb);
+                tmem_ld_wait();
+                const uint32_t va = vis[2 * hh], vb = vis[2 * hh + 1];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float x = ((va >> e) & 1u) ? __uint_as_float(sa[e]) : -INFINITY;
+                    const float y = ((vb >> e) & 1u) ? __uint_as_float(sb[e]) : -INFINITY;
+                    mx4[e & 3] = fmaxf(mx4[e & 3], fmaxf(x, y));
+                }
+            }
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            mbar_arrive(&bars[B_KPOS_FREE + ks]);
             const float m_new = fmaxf(m_run, mx);
             const bool need = m_new > m_run + 8.0f;     // lazy rescale: keep P <= 2^8
             const float alpha = need ? ex2(m_run - m_new) : 1.0f;
             if (need) { l_run *= alpha; m_run = m_new; }
             const float msub = m_run == -INFINITY ? 0.f : m_run;
             if (!LSE && j > 0) {
-                // PV_{j-1} must be done: it reads the single P buffer and accumulates into O
+                // PV_{j-1} must be done: it reads P from TMEM and accumulates into O
                 ok = mbar_wait(&bars[B_P_FREE], (j - 1) & 1, abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
             }
-            float sum = 0.f;
+            // pass 2: p = 2^(s - m) for visible keys, packed to bf16 pairs into the P columns
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                const int cc = ch >> 2, e = (ch & 3) * 8;
-                float p[8];
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t sv[32], pk[16];
+                tmem_ld32(tmem + lane_addr + st * 128 + cc * 32, sv);
+                tmem_ld_wait();
+                const uint32_t vb = vis[cc];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    p[u] = ex2(__uint_as_float(sv[cc][e + u]) - msub);
-                    sum += p[u];
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = ((vb >> (2 * e)) & 1u) ? ex2(__uint_as_float(sv[2 * e]) - msub) : 0.f;
+                    const float p1 = ((vb >> (2 * e + 1)) & 1u) ? ex2(__uint_as_float(sv[2 * e + 1]) - msub) : 0.f;
+                    sum4[e & 3] += p0 + p1;
+                    pk[e] = pack_bf16x2(p0, p1);
                 }
-                if (!LSE) {
-                    uint4 w;
-                    w.x = pack_bf16x2(p[0], p[1]);
-                    w.y = pack_bf16x2(p[2], p[3]);
-                    w.z = pack_bf16x2(p[4], p[5]);
-                    w.w = pack_bf16x2(p[6], p[7]);
-                    *reinterpret_cast<uint4*>(sP + (ch >> 3) * 16384 + sw128_off(m, ch & 7)) = w;
-                }
+                if (!LSE) tmem_st16(tmem + lane_addr + kTmemP + cc * 16, pk);
             }
+            const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+            tc_fence_before();
+            mbar_arrive(&bars[B_S_FREE + st]);
             l_run += sum;
             if (!LSE) {
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
+#pragma unroll 1
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t o[32];
-                        tmem_ld32(tmem + lane_addr + 256 + cc * 32, o);
+                        tmem_ld32(tmem + lane_addr + kTmemO + cc * 32, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(tmem + lane_addr + 256 + cc * 32, o);
+                        tmem_st32(tmem + lane_addr + kTmemO + cc * 32, o);
                     }
-                    tmem_st_wait();
                 }
-                fence_proxy_async_smem();
+                tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&bars[B_P_FULL]);
             }
         }
         if (LSE) {
-            if (ok && valid) {
-                const int chunks = R[R_LSE_CHUNKS];
-                const int n_q = R[R_N_QUERY] * g;
-                prm.lse_part[R[R_LSE_BASE] + ((int64_t)kvh * n_q + row * g + hl) * chunks + chunk] =
-                    make_float2(m_run, l_run);
-            }
+            if (ok && valid) *lse_slot = make_float2(m_run, l_run);
         } else if (ok && n_tiles > 0) {
             ok = mbar_wait(&bars[B_P_FREE], (n_tiles - 1) & 1, abort_flag);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-                __nv_bfloat16* dst = prm.out + ((int64_t)(row_base + row) * Hq + kvh * g + hl) * D;
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_addr + 256 + cc * 32, o);
+                    tmem_ld32(tmem + lane_addr + kTmemO + cc * 32, o);
                     tmem_ld_wait();
                     if (valid) {
 #pragma unroll
@@ -510,7 +617,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                             w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
                             w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
                             w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-                            *reinterpret_cast<uint4*>(dst + cc * 32 + 8 * q) = w;
+                            *reinterpret_cast<uint4*>(out_row + cc * 32 + 8 * q) = w;
                         }
                     }
                 }

@@ -1,8 +1,9 @@
 // Critical-layer importance, second pass (QCFuse, section 2B "Critical-layer attention
 // profiling"; second summary, Phase 3: the query attends to the key cache of one layer only).
 //
-// imp[j] = sum_h sum_t exp2(s_{h,t,j} * log2e/sqrt(d) - lse2_{h,t}), lse2 being the log2-sum-exp
-// of row (h,t) over all cached keys of the request (from the first pass).  The tile is computed
+// imp[j] = sum_h sum_t exp2(s_{h,t,j} - lse2_{h,t}) with s in log2 units (the rotated query rows
+// carry log2(e)/sqrt(d)) and lse2 the log2-sum-exp of row (h,t) over all cached keys of the request
+// (from the first pass).  The tile is computed
 // transposed, S^T = K_rot Q^T with M = 128 keys (TMEM lanes) and N = 256 query rows (columns), so
 // that each thread owns one key and sums its own TMEM row -- no cross-thread reduction.  The K
 // tile is rotated in shared memory at its logical positions (MiniPIC 2.1), the query rows arrive
@@ -14,6 +15,8 @@
 namespace pcf {
 
 constexpr int kImpThreads = 192;
+constexpr int kImpWarpMma = 4;
+constexpr int kImpWarpTma = 5;
 constexpr int kImpQRows = 256;
 
 struct ImpParams {
@@ -23,7 +26,6 @@ struct ImpParams {
     float* part;             // [Hkv][total_tokens]
     int32_t* counters;       // [total key tiles], zero on entry, left zero on exit
     float* importance;       // [total_tokens]
-    float scale_log2;
 };
 
 template <int D>
@@ -36,8 +38,7 @@ struct ImpSmem {
     static constexpr int oQ = oK + kK;
     static constexpr int oCs = oQ + 2 * kQ;
     static constexpr int oLse = oCs + kCs;
-    static constexpr int oKpos = oLse + 2 * kImpQRows * 4;
-    static constexpr int oBar = oKpos + kTileKeys * 4;
+    static constexpr int oBar = oLse + 2 * kImpQRows * 4;
     static constexpr int kNumBars = 12;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int kBytes = oMisc + 64;
@@ -62,7 +63,6 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     auto sQs = [&](int b) { return smem + SM::oQ + b * SM::kQ; };
     float2* sCs = reinterpret_cast<float2*>(smem + SM::oCs);
     auto sLse = [&](int b) { return reinterpret_cast<float*>(smem + SM::oLse) + b * kImpQRows; };
-    int32_t* sKpos = reinterpret_cast<int32_t*>(smem + SM::oKpos);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::oBar);
     int32_t* misc = reinterpret_cast<int32_t*>(smem + SM::oMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -93,7 +93,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         fence_mbar_init();
         misc[4] = 0;
     }
-    if (warp == kWarpMma) {
+    if (warp == kImpWarpMma) {
         tmem_alloc(reinterpret_cast<uint32_t*>(misc), SM::kTmemCols);
         tmem_relinquish();
     }
@@ -102,7 +102,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     tc_fence_after();
     const uint32_t tmem = static_cast<uint32_t>(misc[0]);
 
-    if (warp == kWarpTma) {
+    if (warp == kImpWarpTma) {
         const int lp0 = t * kPagesPerTile;
         const int np = min(kPagesPerTile, n_pages - lp0);
         if (lane == 0) {
@@ -136,7 +136,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             for (int s = 0; s < 2; ++s)
                 if (last[s] >= 0) mbar_drain(&bars[I_Q_FULL + s], (last[s] >> 1) & 1);
         }
-    } else if (warp == kWarpMma) {
+    } else if (warp == kImpWarpMma) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(128, kImpQRows);
             const uint32_t aK = smem_u32(sK);
@@ -166,23 +166,17 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         constexpr int RPT = kPage / RGN;
         const int c = tid % CPR;
         const int rg = tid / (CPR * kPagesPerTile);
-        float2 cs_start[8], cs_step[8];
+        const float2* cs_start = prm.rope + (rg * RPT) * (D / 2) + 8 * c;
+        float2 cs_step[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            cs_start[i] = prm.rope[(rg * RPT) * (D / 2) + 8 * c + i];
-            cs_step[i] = prm.rope[1 * (D / 2) + 8 * c + i];
-        }
-        const int lp = t * kPagesPerTile + rot_page_of<D>(tid);
-        const bool pv = lp < n_pages;
-        const int32_t p0 = pv ? page_pos[lp] : 0;
+        for (int i = 0; i < 8; ++i) cs_step[i] = prm.rope[1 * (D / 2) + 8 * c + i];
         bool ok = mbar_wait(&bars[I_K_FULL], 0, abort_flag);
-        if (ok) rotate_cached_tile<D>(sK, sCs, sKpos, tid, pv, p0, 0u, cs_start, cs_step);
+        if (ok) rotate_cached_tile<D>(sK, sCs, tid, cs_start, cs_step);
         fence_proxy_async_smem();
         mbar_arrive(&bars[I_KROT]);
         const int chunks = R[R_LSE_CHUNKS];
         const float2* part_in = prm.lse_part + R[R_LSE_BASE] + (int64_t)kvh * n_q * chunks;
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-        const float scale = prm.scale_log2;
         float acc = 0.f;
         // every one of the 128 threads runs every iteration (named barriers inside): after an
         // abort the work is skipped, the barrier count stays the same
@@ -221,7 +215,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int n = half * 128 + cc * 32 + e;
-                        if (n < nvalid) acc += ex2(fmaf(__uint_as_float(sv[cc][e]), scale, -sLse(b)[n]));
+                        if (n < nvalid) acc += ex2(__uint_as_float(sv[cc][e]) - sLse(b)[n]);
                     }
             }
             tc_fence_before();
@@ -248,7 +242,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kImpWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, SM::kTmemCols);
     }

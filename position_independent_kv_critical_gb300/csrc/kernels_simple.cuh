@@ -9,14 +9,15 @@ namespace pcf {
 // ------------------------------------------------------------------ rope_rows
 // Rotates rows x[n_rows][H][D] (unrotated, bf16) at per-row positions and writes them in fp16
 // (the operand type of the Q K^T contractions), grouped by kv head for TMA:
-// out[((h / gg) * n_rows + row) * gg + h % gg][D].  Used for the query rows (gg = Hq/Hkv) and the
-// fresh keys (gg = 1) -- per-request data, rotated once; cached keys are never written rotated
+// out[((h / gg) * n_rows + row) * gg + h % gg][D].  Used for the query rows (gg = Hq/Hkv, scaled
+// by log2(e)/sqrt(d) so that Q K^T comes out in log2 units) and the fresh keys (gg = 1) -- per-request data, rotated once; cached keys are never written rotated
 // (MiniPIC 2.1: the shared blocks stay position-free).
 struct RopeJob {
     const __nv_bfloat16* x;
     const int32_t* pos;      // [n_rows] logical position of every row
     __half* out;
     int32_t n_rows, heads, gg;
+    float scale;             // folded into the output: log2(e)/sqrt(d) for queries, 1 for keys
 };
 
 template <int D>
@@ -50,8 +51,8 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob a, RopeJob b, co
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const float c0 = cs[4 * e], s0 = cs[4 * e + 1], c1 = cs[4 * e + 2], s1 = cs[4 * e + 3];
-        const float a0 = bf16_lo(ia[e]), a1 = bf16_hi(ia[e]);
-        const float b0 = bf16_lo(ib[e]), b1 = bf16_hi(ib[e]);
+        const float a0 = bf16_lo(ia[e]) * J.scale, a1 = bf16_hi(ia[e]) * J.scale;
+        const float b0 = bf16_lo(ib[e]) * J.scale, b1 = bf16_hi(ib[e]) * J.scale;
         oa[e] = pack_f16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
         ob[e] = pack_f16x2(fmaf(b0, c0, a0 * s0), fmaf(b1, c1, a1 * s1));
     }

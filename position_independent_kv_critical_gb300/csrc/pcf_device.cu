@@ -150,8 +150,8 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
         cudaMemsetAsync(cnt, 0, (size_t)H[L_TOTAL_KTILES] * sizeof(int32_t), st) != cudaSuccess)
         return PCF_ERR_CUDA;
     RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_query), lay->dev + H[L_OFF_QPOS], q_rot, H[L_TOTAL_QUERY],
-               H[L_HQ], g};
-    RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1};
+               H[L_HQ], g, scale_log2};
+    RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f};
     pcf_status s = launch_rope<D>(qj, none, rope2, H[L_MAX_POS], st);
     if (s != PCF_OK) return s;
 
@@ -167,7 +167,7 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
         using SM = AttnSmem<D, true>;
         auto kern = attn_kernel<D, true>;
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
-        AttnParams p{lay->dev, nullptr, nullptr, rope2, nullptr, lse, scale_log2};
+        AttnParams p{lay->dev, nullptr, nullptr, rope2, nullptr, lse};
         kern<<<H[L_N_LSE_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq128, tk, zero, zero, zero, p);
         if ((s = launched()) != PCF_OK) return s;
     }
@@ -175,7 +175,7 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
         using SM = ImpSmem<D>;
         auto kern = imp_kernel<D>;
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
-        ImpParams p{lay->dev, rope2, lse, part, cnt, importance, scale_log2};
+        ImpParams p{lay->dev, rope2, lse, part, cnt, importance};
         kern<<<H[L_N_IMP_ITEMS], kImpThreads, SM::kAlloc, st>>>(tq256, tk, p);
         if ((s = launched()) != PCF_OK) return s;
     }
@@ -196,8 +196,9 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     const int g = H[L_GROUP];
     const float2* rope2 = reinterpret_cast<const float2*>(rope);
     const int32_t rows = H[L_TOTAL_ROWS];
-    RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_fresh), row_pos, q_rot, rows, H[L_HQ], g};
-    RopeJob kj{reinterpret_cast<const __nv_bfloat16*>(k_fresh), row_pos, k_rot, rows, H[L_HKV], 1};
+    const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_fresh), row_pos, q_rot, rows, H[L_HQ], g, scale_log2};
+    RopeJob kj{reinterpret_cast<const __nv_bfloat16*>(k_fresh), row_pos, k_rot, rows, H[L_HKV], 1, 1.f};
     pcf_status s = launch_rope<D>(qj, kj, rope2, H[L_MAX_POS], st);
     if (s != PCF_OK) return s;
 
@@ -212,8 +213,7 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     using SM = AttnSmem<D, false>;
     auto kern = attn_kernel<D, false>;
     if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
-    const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-    AttnParams p{lay->dev, excl, row_pos, rope2, reinterpret_cast<__nv_bfloat16*>(out), nullptr, scale_log2};
+    AttnParams p{lay->dev, excl, row_pos, rope2, reinterpret_cast<__nv_bfloat16*>(out), nullptr};
     kern<<<H[L_N_ATTN_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq, tkp, tvp, tkf, tvf, p);
     return launched();
 }
