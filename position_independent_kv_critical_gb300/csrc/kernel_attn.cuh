@@ -7,18 +7,25 @@
 // tokens and the query tokens attend over the cached keys minus the recomputed ones plus the
 // fresh rows, keeping causal order on logical positions.
 //
-// One CTA = one tile of 128 query rows (the g query heads of 128/g consecutive rows of one
-// request, all sharing kv head `kvh`) against the request's KV tiles of 128 keys:
-//   warps 0-3  softmax: S row from TMEM, mask, online softmax (lazy rescale), P -> TMEM, O epilogue
-//   warps 4-7  rotate cached K tiles in shared memory (in place, 128-byte swizzled K-major)
-//   warp  8    TMEM allocation + single-thread tcgen05.mma issue
-//   warp  9    K producer (TMA): Q tile, cached K pages through the block table with their page
-//              cos/sin rows, fresh K tiles; 3-stage ring, a stage is free once its Q K^T is done
-//   warp  10   V producer (TMA): cached V pages / fresh V tiles; 2-stage ring, freed by P V
-// S = Q K^T (M=128, N=128, K=d, fp16) is double-buffered in TMEM; P (bf16) is written to TMEM and
-// read from there as the A operand of O += P V (M=128, N=d, bf16); O accumulates in TMEM.
-// Cached keys are rotated by composing the page-base angle (cos/sin row of the page's first
-// position, copied per page) with the in-page offset, advanced row by row (angle addition).
+// One CTA = two tiles A and B of 128 query rows each (a tile packs the g query heads of 128/g
+// consecutive rows of one request, all sharing kv head `kvh`) against the request's KV tiles of
+// 128 keys; both tiles share every rotated K tile and every V tile:
+//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: S row from TMEM, mask, online
+//               softmax (lazy rescale), P -> TMEM (over the S columns), O epilogue
+//   warps 8-11  rotate cached K tiles in shared memory (in place, 128-byte swizzled K-major)
+//   warp  12    TMEM allocation + single-thread tcgen05.mma issue, in the order
+//               PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1), so that the tensor core works on one tile
+//               while the other tile's softmax runs
+//   warp  13    K producer (TMA): Q tiles, cached K pages through the block table with their page
+//               cos/sin rows, fresh K tiles; 2-stage ring, freed by the second QK^T of a stage
+//   warp  14    V producer (TMA): cached V pages / fresh V tiles; 2-stage ring, freed by PV_B
+// TMEM: S_A / P_A at columns [0,128), S_B / P_B at [128,256), O_A at [256,256+d), O_B at
+// [384,384+d).  S = Q K^T is fp16 x fp16 (M=128, N=128 keys, K=d); P (bf16) overwrites its own S
+// columns and is the A operand of O += P V (M=128, N=d, V as an MN-major bf16 operand).
+// Keys that do not take part (recomputed tokens' cached copies, missing pages or rows) are
+// removed by the tensor core itself: Q K^T gets one more K=16 step whose A slab is a column of
+// ones and whose B slab carries 0 or -30000 per key, so their scores (log2 units) underflow to
+// P = 0; only rows whose causal limit falls inside a tile need per-element masking.
 // LSE mode (critical-layer scoring, pass 1) runs the same pipeline without P/V and writes the
 // per-row running max and sum of one key chunk.
 #pragma once
@@ -27,17 +34,18 @@
 
 namespace pcf {
 
-constexpr int kAttnThreads = 352;
-constexpr int kWarpRot0 = 4;
-constexpr int kWarpMma = 8;
-constexpr int kWarpTma = 9;
-constexpr int kWarpTmaV = 10;
+constexpr int kAttnThreads = 480;   // 15 warps
+constexpr int kWarpSoftB = 4;
+constexpr int kWarpRot0 = 8;
+constexpr int kWarpMma = 12;
+constexpr int kWarpTma = 13;
+constexpr int kWarpTmaV = 14;
 constexpr int kNoPos = 0x7FFFFFFF;
-constexpr int kKStages = 3;
+constexpr int kKStages = 2;
 constexpr int kVStages = 2;
-// TMEM columns: S double buffer [0,256), O [256, 256+d), P [384, 448) (bf16 pairs)
-constexpr uint32_t kTmemO = 256;
-constexpr uint32_t kTmemP = 384;
+constexpr uint32_t kTmemO = 256;     // O_A at 256, O_B at 384
+constexpr int kSlab16 = kTileRows * 16 * 2;   // one [128][16] fp16 bias slab
+constexpr float kKeyOff = -30000.f;           // bias of a key that does not take part
 
 struct AttnParams {
     const int32_t* layout;
@@ -51,17 +59,18 @@ struct AttnParams {
 template <int D, bool LSE>
 struct AttnSmem {
     static constexpr int kHalves = D / 64;
-    static constexpr int kQ = kTileRows * D * 2;
+    static constexpr int kQ = kTileRows * D * 2;          // one Q tile
     static constexpr int kK = kTileKeys * D * 2;
     static constexpr int kV = LSE ? 0 : kTileKeys * D * 2;
     static constexpr int kCs = kPagesPerTile * (D / 2) * 8;
     static constexpr int oQ = 0;
-    static constexpr int oK = oQ + kQ;
+    static constexpr int oK = oQ + kQTilesPerCta * kQ;
     static constexpr int oV = oK + kKStages * kK;
     static constexpr int oCs = oV + kVStages * kV;
     static constexpr int oKpos = oCs + kKStages * kCs;
-    static constexpr int oKvalid = oKpos + kKStages * kTileKeys * 4;
-    static constexpr int oBar = oKvalid + kKStages * 16;
+    static constexpr int oQaug = oKpos + kKStages * kTileKeys * 4;   // ones column (1024-aligned)
+    static constexpr int oKaug = oQaug + kSlab16;                    // per K stage: key bias column
+    static constexpr int oBar = oKaug + kKStages * kSlab16;
     static constexpr int kNumBars = 24;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int kBytes = oMisc + 64;
@@ -72,17 +81,17 @@ struct AttnSmem {
 // barrier slots
 enum : int {
     B_Q_FULL = 0,
-    B_K_FULL = 1,      // [3] K pages (+ cos/sin rows) landed
-    B_KROT_FULL = 4,   // [3] K tile rotated, key positions written
-    B_K_EMPTY = 7,     // [3] Q K^T that read the stage is done
-    B_KPOS_FREE = 10,  // [3] softmax done with the stage's key positions
-    B_V_FULL = 13,     // [2]
-    B_V_EMPTY = 15,    // [2] P V that read the stage is done
-    B_S_FULL = 17,     // [2]
-    B_S_FREE = 19,     // [2]
-    B_P_FULL = 21,
-    B_P_FREE = 22,
-    B_DRAIN = 23
+    B_K_FULL = 1,      // [2] K pages (+ cos/sin rows) landed
+    B_KROT_FULL = 3,   // [2] K tile rotated, key positions and validity written
+    B_K_EMPTY = 5,     // [2] both Q K^T that read the stage are done
+    B_KPOS_FREE = 7,   // [2] both softmax groups are done with the stage's key info (256 arrivals)
+    B_V_FULL = 9,      // [2]
+    B_V_EMPTY = 11,    // [2] P_B V that read the stage is done
+    B_S_FULL = 13,     // [2] per Q tile: S = Q K^T landed
+    B_S_FREE = 15,     // [2] per Q tile (LSE mode): softmax done reading S
+    B_P_FULL = 17,     // [2] per Q tile: P written, O rescaled
+    B_PV_DONE = 19,    // [2] per Q tile: P V done (O final for this tile, S/P columns free)
+    B_DRAIN = 21
 };
 
 __device__ __forceinline__ float2 cmul(float2 a, float2 b) {
@@ -180,17 +189,8 @@ __device__ __forceinline__ void rotate_cached_tile(uint8_t* sK, const float2* sC
     }
 }
 
-// Key bookkeeping of one tile, one key per thread (rt = key index): the key's logical position
-// (monotone over the tile: excluded tokens keep theirs, missing keys get INT_MAX) and a validity
-// mask word per warp (ballot) -- excluded and missing keys are invalid.
-__device__ __forceinline__ void write_key_info(int32_t* kpos, uint32_t* kvalid, int rt, int32_t pos, bool valid) {
-    kpos[rt] = pos;
-    const uint32_t w = __ballot_sync(0xffffffffu, valid);
-    if ((rt & 31) == 0) kvalid[rt >> 5] = w;
-}
-
-// 11 warps: at most 3 per SM sub-partition, so each thread may hold up to 168 registers; the
-// softmax works on 32-key slices of the S row to stay below that without spilling.
+// 15 warps: 4 per SM sub-partition at most, so each thread may hold up to 128 registers; the
+// softmax works on 32-key slices of the S row to stay below that.
 template <int D, bool LSE>
 __global__ void __launch_bounds__(kAttnThreads)
 attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kpool,
@@ -200,12 +200,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     constexpr int H = SM::kHalves;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem + SM::oQ;
+    auto sQ = [&](int t) { return smem + SM::oQ + t * SM::kQ; };
     auto sKs = [&](int st) { return smem + SM::oK + st * SM::kK; };
     auto sVs = [&](int st) { return smem + SM::oV + st * SM::kV; };
     auto sCs = [&](int st) { return reinterpret_cast<float2*>(smem + SM::oCs + st * SM::kCs); };
     auto sKpos = [&](int st) { return reinterpret_cast<int32_t*>(smem + SM::oKpos) + st * kTileKeys; };
-    auto sKvalid = [&](int st) { return reinterpret_cast<uint32_t*>(smem + SM::oKvalid) + st * 4; };
+    uint8_t* sQaug = smem + SM::oQaug;
+    auto sKaug = [&](int st) { return smem + SM::oKaug + st * kSlab16; };
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::oBar);
     int32_t* misc = reinterpret_cast<int32_t*>(smem + SM::oMisc);
     // misc: [0] tmem base, [1] n cached tiles, [2] n fresh tiles, [3] first cached tile, [4] abort
@@ -214,13 +215,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t* L = prm.layout;
     const int32_t* item = L + (LSE ? L[L_OFF_LSE] : L[L_OFF_ATTN]) + kItemWords * blockIdx.x;
-    const int req = item[0], kvh = item[1], qt = item[2], chunk = item[3];
+    const int req = item[0], kvh = item[1], qpair = item[2], chunk = item[3];
     const int32_t* R = L + L[L_OFF_REQ] + req * R_STRIDE;
     const int Hq = L[L_HQ], Hkv = L[L_HKV], g = L[L_GROUP];
     const int toks_per_tile = kTileRows / g;
     const int n_rows_req = LSE ? R[R_N_QUERY] : R[R_N_ROWS];
-    const int row0 = qt * toks_per_tile;
-    const int ntok = min(toks_per_tile, n_rows_req - row0);
+    const int row0 = qpair * kQTilesPerCta * toks_per_tile;        // first row of tile A
+    const int nrow_cta = min(kQTilesPerCta * toks_per_tile, n_rows_req - row0);
     const int n_pages = R[R_N_PAGES];
     const int32_t page_base = R[R_PAGE_BASE];
     const int32_t row_base = R[R_ROW_BASE];
@@ -229,22 +230,22 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
     if (tid == 0) {
         mbar_init(&bars[B_Q_FULL], 1);
-        for (int s = 0; s < kKStages; ++s) {
-            mbar_init(&bars[B_K_FULL + s], 1);
-            mbar_init(&bars[B_KROT_FULL + s], 128);
-            mbar_init(&bars[B_K_EMPTY + s], 1);
-            mbar_init(&bars[B_KPOS_FREE + s], 128);
+        for (int s2 = 0; s2 < kKStages; ++s2) {
+            mbar_init(&bars[B_K_FULL + s2], 1);
+            mbar_init(&bars[B_KROT_FULL + s2], 128);
+            mbar_init(&bars[B_K_EMPTY + s2], 1);
+            mbar_init(&bars[B_KPOS_FREE + s2], 256);
         }
-        for (int s = 0; s < kVStages; ++s) {
-            mbar_init(&bars[B_V_FULL + s], 1);
-            mbar_init(&bars[B_V_EMPTY + s], 1);
+        for (int s2 = 0; s2 < kVStages; ++s2) {
+            mbar_init(&bars[B_V_FULL + s2], 1);
+            mbar_init(&bars[B_V_EMPTY + s2], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars[B_S_FULL + s], 1);
-            mbar_init(&bars[B_S_FREE + s], 128);
+        for (int t = 0; t < kQTilesPerCta; ++t) {
+            mbar_init(&bars[B_S_FULL + t], 1);
+            mbar_init(&bars[B_S_FREE + t], 128);
+            mbar_init(&bars[B_P_FULL + t], 128);
+            mbar_init(&bars[B_PV_DONE + t], 1);
         }
-        mbar_init(&bars[B_P_FULL], 128);
-        mbar_init(&bars[B_P_FREE], 1);
         mbar_init(&bars[B_DRAIN], 1);
         fence_mbar_init();
         int nct, nft = 0, t0 = 0;
@@ -255,7 +256,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             t0 = chunk * tpc;
             nct = max(0, min(tpc, nkt - t0));
         } else {
-            const int32_t pmax = ntok > 0 ? prm.row_pos[row_base + row0 + ntok - 1] : -1;
+            const int32_t pmax = nrow_cta > 0 ? prm.row_pos[row_base + row0 + nrow_cta - 1] : -1;
             nct = 0;
             while (nct < nkt && page_pos[nct * kPagesPerTile] <= pmax) ++nct;
             const int nft_total = (n_rows_req + kTileKeys - 1) / kTileKeys;
@@ -270,12 +271,19 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tmem_alloc(reinterpret_cast<uint32_t*>(misc), SM::kTmemCols);
         tmem_relinquish();
     }
-    // V stages start finite: keys masked to P = 0 then contribute 0 * V
+    // V stages start finite (keys masked to P = 0 then contribute 0 * V); bias slabs start at 0
+    // with a column of ones on the query side
     if (!LSE) {
         uint4* z = reinterpret_cast<uint4*>(smem + SM::oV);
         for (int i = tid; i < (kVStages * SM::kV) / 16; i += kAttnThreads) z[i] = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
     }
+    {
+        uint4* z = reinterpret_cast<uint4*>(sQaug);
+        for (int i = tid; i < ((1 + kKStages) * kSlab16) / 16; i += kAttnThreads) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    if (tid < kTileRows) *reinterpret_cast<__half*>(sQaug + slab16_off(tid, 0)) = __float2half(1.0f);
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -294,8 +302,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (!LSE) prefetch_tmap(&tm_kfresh);
             const int32_t qy = LSE ? (kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row0) * g
                                    : (kvh * L[L_TOTAL_ROWS] + row_base + row0) * g;
-            mbar_arrive_expect_tx(&bars[B_Q_FULL], SM::kQ);
-            for (int hb = 0; hb < H; ++hb) tma_load_2d(sQ + hb * 16384, &tm_q, &bars[B_Q_FULL], hb * 64, qy);
+            mbar_arrive_expect_tx(&bars[B_Q_FULL], kQTilesPerCta * SM::kQ);
+            for (int t = 0; t < kQTilesPerCta; ++t)
+                for (int hb = 0; hb < H; ++hb)
+                    tma_load_2d(sQ(t) + hb * 16384, &tm_q, &bars[B_Q_FULL], hb * 64, qy + t * kTileRows);
         }
         auto meta = [&](int j, int32_t& ph, int32_t& pp) {
             ph = -1;
@@ -307,13 +317,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         };
         int32_t ph_next, pp_next;
         meta(0, ph_next, pp_next);
-        int last[kKStages] = {-1, -1, -1};
+        int last[kKStages] = {-1, -1};
         for (int j = 0; j < n_tiles; ++j) {
-            const int ks = j % kKStages;
+            const int ks = j & 1;
             int32_t ph = ph_next, pp = pp_next;
             meta(j + 1, ph_next, pp_next);
-            const bool ok = j < kKStages ||
-                            mbar_wait(&bars[B_K_EMPTY + ks], ((j / kKStages) - 1) & 1, abort_flag);
+            const bool ok = j < kKStages || mbar_wait(&bars[B_K_EMPTY + ks], ((j >> 1) - 1) & 1, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) break;
             uint64_t* full = &bars[B_K_FULL + ks];
             if (j < n_ct) {
@@ -340,7 +349,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (lane == 0) {
             mbar_drain(&bars[B_Q_FULL], 0);
             for (int s2 = 0; s2 < kKStages; ++s2)
-                if (last[s2] >= 0) mbar_drain(&bars[B_K_FULL + s2], (last[s2] / kKStages) & 1);
+                if (last[s2] >= 0) mbar_drain(&bars[B_K_FULL + s2], (last[s2] >> 1) & 1);
         }
     } else if (warp == kWarpTmaV) {
         // ------------------------------------------------------------ V producer
@@ -393,49 +402,87 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_f16(128, 128);
             constexpr uint32_t idesc_pv = idesc_bf16(128, 64, true);
-            const uint32_t aQ = smem_u32(sQ);
-            bool ok = mbar_wait(&bars[B_Q_FULL], 0, abort_flag);
-            auto issue_pv = [&](int i) -> bool {
-                const int vs = i & 1;
-                if (!mbar_wait(&bars[B_P_FULL], i & 1, abort_flag)) return false;
-                if (!mbar_wait(&bars[B_V_FULL + vs], (i >> 1) & 1, abort_flag)) return false;
-                tc_fence_after();
-                const uint32_t aV = smem_u32(sVs(vs));
+            auto issue_qk = [&](int t, int j) {
+                const uint32_t aQ = smem_u32(sQ(t)), aK = smem_u32(sKs(j & 1));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t a = desc_sw128_kmajor(aQ + (kk >> 2) * 16384 + (kk & 3) * 32);
+                    const uint64_t b = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
+                    mma_bf16_ss(tmem + t * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                // + 1 * bias(key): 0 for taking part, -30000 for excluded / missing keys
+                mma_bf16_ss(tmem + t * 128, desc_noswz_kmajor(smem_u32(sQaug), 128, 256),
+                            desc_noswz_kmajor(smem_u32(sKaug(j & 1)), 128, 256), idesc_qk, 1u);
+                mma_commit(&bars[B_S_FULL + t]);
+            };
+            auto issue_pv = [&](int t, int j) {
+                const uint32_t aV = smem_u32(sVs(j & 1));
 #pragma unroll
                 for (int kk = 0; kk < kTileKeys / 16; ++kk) {
 #pragma unroll
                     for (int nh = 0; nh < H; ++nh) {
                         const uint64_t b = desc_sw128_mn64(aV + nh * 16384 + kk * 2048);
-                        mma_bf16_ts(tmem + kTmemO + nh * 64, tmem + kTmemP + kk * 8, b, idesc_pv,
-                                    (i > 0 || kk > 0) ? 1u : 0u);
+                        mma_bf16_ts(tmem + kTmemO + t * 128 + nh * 64, tmem + t * 128 + kk * 8, b, idesc_pv,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                mma_commit(&bars[B_P_FREE]);
-                mma_commit(&bars[B_V_EMPTY + vs]);
-                return true;
+                mma_commit(&bars[B_PV_DONE + t]);
             };
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int st = j & 1, ks = j % kKStages;
-                if (!mbar_wait(&bars[B_KROT_FULL + ks], (j / kKStages) & 1, abort_flag)) { ok = false; break; }
-                if (j >= 2 && !mbar_wait(&bars[B_S_FREE + st], ((j >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+            bool ok = mbar_wait(&bars[B_Q_FULL], 0, abort_flag);
+            ok = ok && (n_tiles == 0 || mbar_wait(&bars[B_KROT_FULL + 0], 0, abort_flag));
+            if (ok && n_tiles > 0) {
                 tc_fence_after();
-                const uint32_t aK = smem_u32(sKs(ks));
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = desc_sw128_kmajor(aQ + (kk >> 2) * 16384 + (kk & 3) * 32);
-                    const uint64_t b = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
-                    mma_bf16_ss(tmem + st * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&bars[B_S_FULL + st]);
-                mma_commit(&bars[B_K_EMPTY + ks]);
-                if (!LSE && j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+                issue_qk(0, 0);
+                issue_qk(1, 0);
+                mma_commit(&bars[B_K_EMPTY + 0]);
             }
-            if (!LSE && ok && n_tiles > 0) issue_pv(n_tiles - 1);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const bool more = j + 1 < n_tiles;
+                const int kn = (j + 1) & 1;
+                if (LSE) {
+                    if (more) {
+                        ok = mbar_wait(&bars[B_KROT_FULL + kn], ((j + 1) >> 1) & 1, abort_flag);
+                        for (int t = 0; ok && t < kQTilesPerCta; ++t) {
+                            ok = mbar_wait(&bars[B_S_FREE + t], j & 1, abort_flag);
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_qk(t, j + 1);
+                        }
+                        if (ok) mma_commit(&bars[B_K_EMPTY + kn]);
+                    }
+                    continue;
+                }
+                // tile A: P_A(j) V(j), then Q_A K(j+1); tile B likewise
+                ok = mbar_wait(&bars[B_P_FULL + 0], j & 1, abort_flag) &&
+                     mbar_wait(&bars[B_V_FULL + (j & 1)], (j >> 1) & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(0, j);
+                if (more) {
+                    ok = mbar_wait(&bars[B_KROT_FULL + kn], ((j + 1) >> 1) & 1, abort_flag) &&
+                         mbar_wait(&bars[B_PV_DONE + 0], j & 1, abort_flag);   // P_A columns reused by S_A
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_qk(0, j + 1);
+                }
+                ok = mbar_wait(&bars[B_P_FULL + 1], j & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(1, j);
+                mma_commit(&bars[B_V_EMPTY + (j & 1)]);
+                if (more) {
+                    ok = mbar_wait(&bars[B_PV_DONE + 1], j & 1, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_qk(1, j + 1);
+                    mma_commit(&bars[B_K_EMPTY + kn]);
+                }
+            }
             mma_commit(&bars[B_DRAIN]);
             mbar_drain(&bars[B_DRAIN], 0);
         }
-    } else if (warp >= kWarpRot0 && warp < kWarpMma) {
-        // ------------------------------------------------------------ K rotation (warps 4-7)
+    } else if (warp >= kWarpRot0) {
+        // ------------------------------------------------------------ K rotation (warps 8-11)
         const int rt = tid - kWarpRot0 * 32;
         constexpr int CPR = D / 16;
         constexpr int RGN = kTileKeys / (CPR * kPagesPerTile);
@@ -469,29 +516,34 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         bool val_n;
         meta(0, pos_n, val_n);
         for (int j = 0; j < n_tiles; ++j) {
-            const int ks = j % kKStages;
+            const int ks = j & 1;
             const int32_t pos = pos_n;
             const bool val = val_n;
             meta(j + 1, pos_n, val_n);
-            bool ok = mbar_wait(&bars[B_K_FULL + ks], (j / kKStages) & 1, abort_flag);
-            ok = ok && (j < kKStages || mbar_wait(&bars[B_KPOS_FREE + ks], ((j / kKStages) - 1) & 1, abort_flag));
+            bool ok = mbar_wait(&bars[B_K_FULL + ks], (j >> 1) & 1, abort_flag);
+            ok = ok && (j < kKStages || mbar_wait(&bars[B_KPOS_FREE + ks], ((j >> 1) - 1) & 1, abort_flag));
             if (!__all_sync(0xffffffffu, ok)) break;
             if (j < n_ct) rotate_cached_tile<D>(sKs(ks), sCs(ks), rt, cs_start, cs_step);
-            write_key_info(sKpos(ks), sKvalid(ks), rt, pos, val);
+            sKpos(ks)[rt] = pos;
+            *reinterpret_cast<__half*>(sKaug(ks) + slab16_off(rt, 0)) = __float2half(val ? 0.f : kKeyOff);
             fence_proxy_async_smem();
             mbar_arrive(&bars[B_KROT_FULL + ks]);
         }
-    } else if (warp < kWarpRot0) {
-        // ------------------------------------------------------------ softmax (warps 0-3)
-        // Scores arrive already in log2 units: the rotated query rows carry log2(e)/sqrt(d).
-        const int m = tid;                 // tile row = TMEM lane
+    } else {
+        // ------------------------------------------------------------ softmax (warps 0-7)
+        // Group t (warps 4t..4t+3) owns Q tile t.  Scores arrive already in log2 units: the
+        // rotated query rows carry log2(e)/sqrt(d).
+        const int t = warp >= kWarpSoftB ? 1 : 0;
+        const int m = tid - t * 128;           // tile row = TMEM lane
         const int tok = m / g, hl = m % g;
-        const bool valid = tok < ntok;
-        const int row = row0 + tok;
+        const int row = row0 + t * toks_per_tile + tok;
+        const bool valid = row < n_rows_req;
         int32_t mypos;
         if (LSE) mypos = valid ? kNoPos - 1 : -1;
         else mypos = valid ? prm.row_pos[row_base + row] : -1;
-        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_addr + t * 128;          // S (and P) columns of this tile
+        const uint32_t tO = tmem + lane_addr + kTmemO + t * 128;
         // output locations, fixed before the tile loop so that only one pointer stays live across it
         __nv_bfloat16* out_row = nullptr;
         float2* lse_slot = nullptr;
@@ -505,14 +557,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            const int st = j & 1, ks = j % kKStages;
-            ok = mbar_wait(&bars[B_S_FULL + st], (j >> 1) & 1, abort_flag);
-            ok = ok && mbar_wait(&bars[B_KROT_FULL + ks], (j / kKStages) & 1, abort_flag);
+            const int ks = j & 1;
+            ok = mbar_wait(&bars[B_S_FULL + t], j & 1, abort_flag);
+            ok = ok && mbar_wait(&bars[B_KROT_FULL + ks], (j >> 1) & 1, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            // visibility of the 128 keys for this row: keys are in increasing position order, so
-            // the visible ones are a prefix (binary search), minus the invalid ones (mask words)
-            uint32_t vis[4];
+            // causal limit of this row inside the tile: keys are in increasing position order, so
+            // the visible ones are a prefix (binary search); excluded keys are already at -30000
+            int cut;
             {
                 const int32_t* kp = sKpos(ks);
                 int lo = 0;
@@ -520,94 +572,100 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 for (int step = 64; step >= 1; step >>= 1)
                     if (kp[lo + step - 1] <= mypos) lo += step;
                 if (kp[lo] <= mypos) ++lo;   // lo <= 127 here; 128 when every key qualifies
-                const int cut = lo;   // number of keys with position <= mypos
-                const uint4 vw = *reinterpret_cast<const uint4*>(sKvalid(ks));
-                const uint32_t vv[4] = {vw.x, vw.y, vw.z, vw.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int k = cut - 32 * w;
-                    const uint32_t pm = k >= 32 ? 0xffffffffu : (k <= 0 ? 0u : ((1u << k) - 1u));
-                    vis[w] = vv[w] & pm;
-                }
+                cut = lo;
             }
-            // pass 1: masked row max (two TMEM chunks per wait, four independent maxima)
+            mbar_arrive(&bars[B_KPOS_FREE + ks]);
+            const bool full = __all_sync(0xffffffffu, cut == kTileKeys);   // no row of the warp is cut
+            // pass 1: row max
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t sa[32], sb[32];
-                tmem_ld32(tmem + lane_addr + st * 128 + hh * 64, sa);
-                tmem_ld32(tmem + lane_addr + st * 128 + hh * 64 + 32, sb);
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t sv[32];
+                tmem_ld32(tS + cc * 32, sv);
                 tmem_ld_wait();
-                const uint32_t va = vis[2 * hh], vb = vis[2 * hh + 1];
+                if (full) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float x = ((va >> e) & 1u) ? __uint_as_float(sa[e]) : -INFINITY;
-                    const float y = ((vb >> e) & 1u) ? __uint_as_float(sb[e]) : -INFINITY;
-                    mx4[e & 3] = fmaxf(mx4[e & 3], fmaxf(x, y));
+                    for (int e = 0; e < 32; e += 8) {
+                        mx4[0] = max3f(mx4[0], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+                        mx4[1] = max3f(mx4[1], __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
+                        mx4[2] = max3f(mx4[2], __uint_as_float(sv[e + 4]), __uint_as_float(sv[e + 5]));
+                        mx4[3] = max3f(mx4[3], __uint_as_float(sv[e + 6]), __uint_as_float(sv[e + 7]));
+                    }
+                } else {
+                    const int k = cut - 32 * cc;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float x = e < k ? __uint_as_float(sv[e]) : -INFINITY;
+                        mx4[e & 3] = fmaxf(mx4[e & 3], x);
+                    }
                 }
             }
             const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-            mbar_arrive(&bars[B_KPOS_FREE + ks]);
             const float m_new = fmaxf(m_run, mx);
             const bool need = m_new > m_run + 8.0f;     // lazy rescale: keep P <= 2^8
             const float alpha = need ? ex2(m_run - m_new) : 1.0f;
             if (need) { l_run *= alpha; m_run = m_new; }
             const float msub = m_run == -INFINITY ? 0.f : m_run;
             if (!LSE && j > 0) {
-                // PV_{j-1} must be done: it reads P from TMEM and accumulates into O
-                ok = mbar_wait(&bars[B_P_FREE], (j - 1) & 1, abort_flag);
+                // PV(j-1) of this tile must be done before O is rescaled
+                ok = mbar_wait(&bars[B_PV_DONE + t], (j - 1) & 1, abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
             }
-            // pass 2: p = 2^(s - m) for visible keys, packed to bf16 pairs into the P columns
+            // pass 2: p = 2^(s - m) for visible keys; P (bf16 pairs) overwrites the S columns
+            // already read (columns [16cc, 16cc+16) after S columns [32cc, 32cc+32) are loaded)
             float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t sv[32], pk[16];
-                tmem_ld32(tmem + lane_addr + st * 128 + cc * 32, sv);
+                tmem_ld32(tS + cc * 32, sv);
                 tmem_ld_wait();
-                const uint32_t vb = vis[cc];
+                const int k = full ? 32 : cut - 32 * cc;
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float p0 = ((vb >> (2 * e)) & 1u) ? ex2(__uint_as_float(sv[2 * e]) - msub) : 0.f;
-                    const float p1 = ((vb >> (2 * e + 1)) & 1u) ? ex2(__uint_as_float(sv[2 * e + 1]) - msub) : 0.f;
+                    float p0 = ex2(__uint_as_float(sv[2 * e]) - msub);
+                    float p1 = ex2(__uint_as_float(sv[2 * e + 1]) - msub);
+                    if (!full) {
+                        p0 = 2 * e < k ? p0 : 0.f;
+                        p1 = 2 * e + 1 < k ? p1 : 0.f;
+                    }
                     sum4[e & 3] += p0 + p1;
                     pk[e] = pack_bf16x2(p0, p1);
                 }
-                if (!LSE) tmem_st16(tmem + lane_addr + kTmemP + cc * 16, pk);
+                if (!LSE) tmem_st16(tS + cc * 16, pk);
             }
-            const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-            tc_fence_before();
-            mbar_arrive(&bars[B_S_FREE + st]);
-            l_run += sum;
-            if (!LSE) {
+            l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+            if (LSE) {
+                tc_fence_before();
+                mbar_arrive(&bars[B_S_FREE + t]);
+            } else {
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t o[32];
-                        tmem_ld32(tmem + lane_addr + kTmemO + cc * 32, o);
+                        tmem_ld32(tO + cc * 32, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(tmem + lane_addr + kTmemO + cc * 32, o);
+                        tmem_st32(tO + cc * 32, o);
                     }
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&bars[B_P_FULL]);
+                mbar_arrive(&bars[B_P_FULL + t]);
             }
         }
         if (LSE) {
             if (ok && valid) *lse_slot = make_float2(m_run, l_run);
         } else if (ok && n_tiles > 0) {
-            ok = mbar_wait(&bars[B_P_FREE], (n_tiles - 1) & 1, abort_flag);
+            ok = mbar_wait(&bars[B_PV_DONE + t], (n_tiles - 1) & 1, abort_flag);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
 #pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_addr + kTmemO + cc * 32, o);
+                    tmem_ld32(tO + cc * 32, o);
                     tmem_ld_wait();
                     if (valid) {
 #pragma unroll

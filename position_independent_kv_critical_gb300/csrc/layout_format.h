@@ -14,6 +14,7 @@ constexpr int32_t kMagic = 0x4C464350;   // "PCFL"
 constexpr int kPage = 16;                // tokens per page
 constexpr int kTileRows = 128;           // TMEM lanes = rows of one MMA tile
 constexpr int kTileKeys = 128;           // keys per KV tile
+constexpr int kQTilesPerCta = 2;         // 128-row query tiles sharing each rotated K/V tile
 constexpr int kPagesPerTile = kTileKeys / kPage;
 constexpr int kMaxPosLimit = 1 << 20;
 constexpr int kItemWords = 4;
@@ -44,8 +45,9 @@ enum : int {
 };
 
 // work items (kItemWords each)
-//   attention : {req, kv head, q tile, estimated cost}   sorted by cost, largest first
-//   lse       : {req, kv head, q tile, key chunk}
+//   attention : {req, kv head, q tile pair, estimated cost}   sorted by cost, largest first
+//   lse       : {req, kv head, q tile pair, key chunk}
+// (a "q tile pair" p covers the 128-row query tiles 2p and 2p+1 of the request)
 //   importance: {req, key tile, kv head, 0}
 
 }  // namespace pcf

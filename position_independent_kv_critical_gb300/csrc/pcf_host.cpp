@@ -107,7 +107,7 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
         const int32_t nkt = cdiv(n_tok / kPage, kPagesPerTile);
         tot_kt += nkt;
         if (nkt > 0 && r.n_query > 0)
-            base_lse_ctas += (int64_t)d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows);
+            base_lse_ctas += (int64_t)d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta);
         plan->max_tokens = std::max<int32_t>(plan->max_tokens, (int32_t)n_tok);
         plan->max_rows = std::max<int32_t>(plan->max_rows, (int32_t)(n_sel + r.n_query));
         plan->max_query = std::max<int32_t>(plan->max_query, r.n_query);
@@ -138,12 +138,12 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
         }
         const int32_t nkt = cdiv(n_tok / kPage, kPagesPerTile);
         const int64_t rows = n_sel + r.n_query;
-        n_attn += (int64_t)d.n_kv_heads * cdiv(rows * g, kTileRows);
+        n_attn += (int64_t)d.n_kv_heads * cdiv(rows * g, kTileRows * kQTilesPerCta);
         if (nkt > 0 && r.n_query > 0) {
             const int32_t tpc = cdiv(nkt, std::max(1, std::min(want, nkt)));
             const int32_t chunks = cdiv(nkt, tpc);
             plan->lse_chunks[b] = chunks;
-            n_lse += (int64_t)d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows) * chunks;
+            n_lse += (int64_t)d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta) * chunks;
             slots += (int64_t)r.n_query * d.n_q_heads * chunks;
         }
         if (nkt > 0) n_imp += (int64_t)nkt * d.n_kv_heads;
@@ -276,11 +276,12 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
         R[R_N_KTILES] = nkt;
         for (int t = 0; t < r.n_query; ++t) QPOS[q_base + t] = r.query_pos0 + t;
 
-        // attention work: one item per (kv head, 128-row tile); rows pack the g heads of a token
-        const int32_t toks_per_tile = kTileRows / g;
-        const int32_t n_qt = cdiv((int64_t)n_rows * g, kTileRows);
+        // attention work: one item per (kv head, pair of 128-row tiles); rows pack the g heads of a
+        // token
+        const int32_t toks_per_item = kQTilesPerCta * (kTileRows / g);
+        const int32_t n_qt = cdiv((int64_t)n_rows * g, kTileRows * kQTilesPerCta);
         for (int32_t qt = 0; qt < n_qt; ++qt) {
-            const int64_t last_row = std::min<int64_t>((int64_t)(qt + 1) * toks_per_tile, n_rows) - 1;
+            const int64_t last_row = std::min<int64_t>((int64_t)(qt + 1) * toks_per_item, n_rows) - 1;
             // estimated visible keys: query rows see everything, recomputed rows about the
             // fraction of the context before them
             int64_t cost;
@@ -289,9 +290,9 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
             for (int32_t h = 0; h < d.n_kv_heads; ++h)
                 attn.push_back({b, h, qt, cost, (int64_t)attn.size()});
         }
-        // LSE work: (kv head, query tile, key chunk)
+        // LSE work: (kv head, query tile pair, key chunk)
         if (plan.lse_chunks[b] > 0) {
-            const int32_t n_lqt = cdiv((int64_t)r.n_query * g, kTileRows);
+            const int32_t n_lqt = cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta);
             for (int32_t h = 0; h < d.n_kv_heads; ++h)
                 for (int32_t qt = 0; qt < n_lqt; ++qt)
                     for (int32_t c = 0; c < plan.lse_chunks[b]; ++c) {

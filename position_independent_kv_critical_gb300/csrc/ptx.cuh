@@ -211,6 +211,17 @@ __device__ __forceinline__ uint64_t desc_sw128_mn64(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(1024 >> 4) << 16) |
            ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
+// UMMA shared-memory descriptor, no swizzle, K-major: 8-row x 16-byte core matrices; `k_stride`
+// bytes between core matrices adjacent along K, `row_stride` bytes between 8-row groups.
+__device__ __forceinline__ uint64_t desc_noswz_kmajor(uint32_t saddr, uint32_t k_stride, uint32_t row_stride) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(k_stride >> 4) << 16) |
+           ((uint64_t)(row_stride >> 4) << 32) | ((uint64_t)1 << 46);
+}
+// Byte offset of element (row, k) of a [rows][16] 16-bit slab in that layout (k_stride 128,
+// row_stride 256).
+__device__ __forceinline__ uint32_t slab16_off(uint32_t row, uint32_t k) {
+    return (row >> 3) * 256u + (k >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
+}
 // Instruction descriptor, kind::f16: D fp32, A = B = bf16, A K-major, B K- or MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
@@ -222,6 +233,11 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
 }
 
 // ---------------------------------------------------------------- math
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

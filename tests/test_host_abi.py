@@ -93,11 +93,11 @@ def test_layout_totals_and_block_table(name):
     assert ppos.tolist() == exp_pos
     qpos = B[B[L_OFF_QPOS]: B[L_OFF_QPOS] + L.total_query]
     assert qpos.tolist() == [r.query_pos0 + t for r in reqs for t in range(r.n_query)]
-    # every (request, kv head, 128-row tile) appears once in the attention work list
+    # every (request, kv head, pair of 128-row tiles) appears once in the attention work list
     g = cfg.hq // cfg.hkv
     items = B[B[L_OFF_ATTN]: B[L_OFF_ATTN] + 4 * B[L_N_ATTN]].reshape(-1, 4)
     want = {(b, h, t) for b, r in enumerate(reqs) for h in range(cfg.hkv)
-            for t in range(-(-r.n_rows * g // 128))}
+            for t in range(-(-r.n_rows * g // 256))}
     got = {tuple(x) for x in items[:, :3].tolist()}
     assert got == want and len(items) == len(want)
     assert np.all(np.diff(items[:, 3]) <= 0)   # largest estimated cost first
