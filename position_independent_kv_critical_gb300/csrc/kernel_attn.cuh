@@ -54,6 +54,8 @@ struct AttnParams {
     const float2* rope;        // [max_pos][D/2] (cos, sin)
     __nv_bfloat16* out;        // attention: [rows][Hq][D]
     float2* lse_part;          // LSE: (running max in log2 units, running sum) per row and chunk
+    __nv_bfloat16* part_o;     // attention with a split key range: normalized partial O per slot
+    float2* part_ml;           //   and its (running max, running sum) per row
 };
 
 template <int D, bool LSE>
@@ -146,14 +148,9 @@ __device__ __forceinline__ void rotate_cached_tile(uint8_t* sK, const float2* sC
     const int pg = (rt / CPR) % kPagesPerTile;
     const int rg = rt / (CPR * kPagesPerTile);
     const int row0 = pg * kPage + rg * RPT;
-    const uint32_t off_b = D == 128 ? 16384u : 0u;
+    uint8_t* base_a = sK;
+    uint8_t* base_b = sK + (D == 128 ? 16384 : 0);
     const int cb = D == 128 ? c : c + 4;
-    uint4 a[RPT], b[RPT];
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-        a[r] = *reinterpret_cast<const uint4*>(sK + sw128_off(row0 + r, c));
-        b[r] = *reinterpret_cast<const uint4*>(sK + off_b + sw128_off(row0 + r, cb));
-    }
     float2 cs[8];
     const float4* b4 = reinterpret_cast<const float4*>(sCs + pg * (D / 2) + 8 * c);
     const float4* s4 = reinterpret_cast<const float4*>(cs_start_g);
@@ -164,10 +161,18 @@ __device__ __forceinline__ void rotate_cached_tile(uint8_t* sK, const float2* sC
         cs[2 * q] = cmul(make_float2(v.x, v.y), make_float2(w.x, w.y));
         cs[2 * q + 1] = cmul(make_float2(v.z, v.w), make_float2(w.z, w.w));
     }
-#pragma unroll
+    // rows are independent: the next row is loaded before the current one is written back
+    uint4 a_nx = *reinterpret_cast<const uint4*>(base_a + sw128_off(row0, c));
+    uint4 b_nx = *reinterpret_cast<const uint4*>(base_b + sw128_off(row0, cb));
+#pragma unroll 1
     for (int r = 0; r < RPT; ++r) {
-        const uint32_t ia[4] = {a[r].x, a[r].y, a[r].z, a[r].w};
-        const uint32_t ib[4] = {b[r].x, b[r].y, b[r].z, b[r].w};
+        const uint4 a = a_nx, b = b_nx;
+        if (r + 1 < RPT) {
+            a_nx = *reinterpret_cast<const uint4*>(base_a + sw128_off(row0 + r + 1, c));
+            b_nx = *reinterpret_cast<const uint4*>(base_b + sw128_off(row0 + r + 1, cb));
+        }
+        const uint32_t ia[4] = {a.x, a.y, a.z, a.w};
+        const uint32_t ib[4] = {b.x, b.y, b.z, b.w};
         uint32_t oa[4], ob[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -177,15 +182,10 @@ __device__ __forceinline__ void rotate_cached_tile(uint8_t* sK, const float2* sC
             oa[e] = pack_f16x2(fmaf(a0, c0.x, -b0 * c0.y), fmaf(a1, c1.x, -b1 * c1.y));
             ob[e] = pack_f16x2(fmaf(b0, c0.x, a0 * c0.y), fmaf(b1, c1.x, a1 * c1.y));
         }
-        a[r] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-        b[r] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+        *reinterpret_cast<uint4*>(base_a + sw128_off(row0 + r, c)) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+        *reinterpret_cast<uint4*>(base_b + sw128_off(row0 + r, cb)) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
 #pragma unroll
         for (int i = 0; i < 8; ++i) cs[i] = cmul(cs[i], cs_step[i]);
-    }
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-        *reinterpret_cast<uint4*>(sK + sw128_off(row0 + r, c)) = a[r];
-        *reinterpret_cast<uint4*>(sK + off_b + sw128_off(row0 + r, cb)) = b[r];
     }
 }
 
@@ -209,13 +209,15 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     auto sKaug = [&](int st) { return smem + SM::oKaug + st * kSlab16; };
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::oBar);
     int32_t* misc = reinterpret_cast<int32_t*>(smem + SM::oMisc);
-    // misc: [0] tmem base, [1] n cached tiles, [2] n fresh tiles, [3] first cached tile, [4] abort
+    // misc: [0] tmem base, [1] n cached tiles, [2] n fresh tiles, [3] first cached tile, [4] abort,
+    //       [5] first tile of this CTA's key range, [6] end of the range (tiles in visible order)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t* L = prm.layout;
     const int32_t* item = L + (LSE ? L[L_OFF_LSE] : L[L_OFF_ATTN]) + kItemWords * blockIdx.x;
-    const int req = item[0], kvh = item[1], qpair = item[2], chunk = item[3];
+    const int req = item[0], kvh = item[1], qpair = item[2], chunk = item[3];   // chunk: LSE key chunk
+                                                                                  // or attention split
     const int32_t* R = L + L[L_OFF_REQ] + req * R_STRIDE;
     const int Hq = L[L_HQ], Hkv = L[L_HKV], g = L[L_GROUP];
     const int toks_per_tile = kTileRows / g;
@@ -266,6 +268,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         misc[2] = nft;
         misc[3] = t0;
         misc[4] = 0;
+        const int n_all = nct + nft;
+        const int ns = LSE ? 1 : R[R_NSPLIT];
+        const int sp = LSE ? 0 : chunk;
+        misc[5] = (int)(((int64_t)sp * n_all) / ns);
+        misc[6] = (int)(((int64_t)(sp + 1) * n_all) / ns);
     }
     if (warp == kWarpMma) {
         tmem_alloc(reinterpret_cast<uint32_t*>(misc), SM::kTmemCols);
@@ -290,6 +297,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t tmem = static_cast<uint32_t>(misc[0]);
     const int n_ct = misc[1], n_ft = misc[2], t0 = misc[3];
     const int n_tiles = n_ct + n_ft;
+    const int jb = misc[5], n_loc = misc[6] - misc[5];   // tiles jb .. jb+n_loc-1 of the visible range
     const int n_phys = L[L_N_PHYS];
 
     if (warp == kWarpTma) {
@@ -316,13 +324,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
         };
         int32_t ph_next, pp_next;
-        meta(0, ph_next, pp_next);
+        meta(jb, ph_next, pp_next);
         int last[kKStages] = {-1, -1};
-        for (int j = 0; j < n_tiles; ++j) {
-            const int ks = j & 1;
+        for (int jj = 0; jj < n_loc; ++jj) {
+            const int j = jb + jj, ks = jj & 1;
             int32_t ph = ph_next, pp = pp_next;
             meta(j + 1, ph_next, pp_next);
-            const bool ok = j < kKStages || mbar_wait(&bars[B_K_EMPTY + ks], ((j >> 1) - 1) & 1, abort_flag);
+            const bool ok = jj < kKStages || mbar_wait(&bars[B_K_EMPTY + ks], ((jj >> 1) - 1) & 1, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) break;
             uint64_t* full = &bars[B_K_FULL + ks];
             if (j < n_ct) {
@@ -344,7 +352,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 for (int hb = 0; hb < H; ++hb)
                     tma_load_2d(sKs(ks) + hb * 16384, &tm_kfresh, full, hb * 64, kvh * L[L_TOTAL_ROWS] + fr);
             }
-            last[ks] = j;
+            last[ks] = jj;
         }
         if (lane == 0) {
             mbar_drain(&bars[B_Q_FULL], 0);
@@ -365,13 +373,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
                 return -1;
             };
-            int32_t ph_next = meta(0);
+            int32_t ph_next = meta(jb);
             int last[kVStages] = {-1, -1};
-            for (int j = 0; j < n_tiles; ++j) {
-                const int vs = j & 1;
+            for (int jj = 0; jj < n_loc; ++jj) {
+                const int j = jb + jj, vs = jj & 1;
                 int32_t ph = ph_next;
                 ph_next = meta(j + 1);
-                const bool ok = j < kVStages || mbar_wait(&bars[B_V_EMPTY + vs], ((j >> 1) - 1) & 1, abort_flag);
+                const bool ok = jj < kVStages || mbar_wait(&bars[B_V_EMPTY + vs], ((jj >> 1) - 1) & 1, abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 uint64_t* full = &bars[B_V_FULL + vs];
                 if (j < n_ct) {
@@ -391,7 +399,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     for (int hb = 0; hb < H; ++hb)
                         tma_load_3d(sVs(vs) + hb * 16384, &tm_vfresh, full, hb * 64, kvh, fr);
                 }
-                last[vs] = j;
+                last[vs] = jj;
             }
             if (lane == 0)
                 for (int s2 = 0; s2 < kVStages; ++s2)
@@ -429,15 +437,15 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 mma_commit(&bars[B_PV_DONE + t]);
             };
             bool ok = mbar_wait(&bars[B_Q_FULL], 0, abort_flag);
-            ok = ok && (n_tiles == 0 || mbar_wait(&bars[B_KROT_FULL + 0], 0, abort_flag));
-            if (ok && n_tiles > 0) {
+            ok = ok && (n_loc == 0 || mbar_wait(&bars[B_KROT_FULL + 0], 0, abort_flag));
+            if (ok && n_loc > 0) {
                 tc_fence_after();
                 issue_qk(0, 0);
                 issue_qk(1, 0);
                 mma_commit(&bars[B_K_EMPTY + 0]);
             }
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const bool more = j + 1 < n_tiles;
+            for (int j = 0; ok && j < n_loc; ++j) {    // j: local tile index
+                const bool more = j + 1 < n_loc;
                 const int kn = (j + 1) & 1;
                 if (LSE) {
                     if (more) {
@@ -514,14 +522,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         };
         int32_t pos_n;
         bool val_n;
-        meta(0, pos_n, val_n);
-        for (int j = 0; j < n_tiles; ++j) {
-            const int ks = j & 1;
+        meta(jb, pos_n, val_n);
+        for (int jj = 0; jj < n_loc; ++jj) {
+            const int j = jb + jj, ks = jj & 1;
             const int32_t pos = pos_n;
             const bool val = val_n;
             meta(j + 1, pos_n, val_n);
-            bool ok = mbar_wait(&bars[B_K_FULL + ks], (j >> 1) & 1, abort_flag);
-            ok = ok && (j < kKStages || mbar_wait(&bars[B_KPOS_FREE + ks], ((j >> 1) - 1) & 1, abort_flag));
+            bool ok = mbar_wait(&bars[B_K_FULL + ks], (jj >> 1) & 1, abort_flag);
+            ok = ok && (jj < kKStages || mbar_wait(&bars[B_KPOS_FREE + ks], ((jj >> 1) - 1) & 1, abort_flag));
             if (!__all_sync(0xffffffffu, ok)) break;
             if (j < n_ct) rotate_cached_tile<D>(sKs(ks), sCs(ks), rt, cs_start, cs_step);
             sKpos(ks)[rt] = pos;
@@ -545,18 +553,25 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const uint32_t tS = tmem + lane_addr + t * 128;          // S (and P) columns of this tile
         const uint32_t tO = tmem + lane_addr + kTmemO + t * 128;
         // output locations, fixed before the tile loop so that only one pointer stays live across it
+        // (a split key range writes a normalized partial row plus its max and sum instead)
         __nv_bfloat16* out_row = nullptr;
-        float2* lse_slot = nullptr;
+        float2* ml_slot = nullptr;
         if (valid) {
-            if (LSE)
-                lse_slot = prm.lse_part + R[R_LSE_BASE] +
-                           ((int64_t)kvh * (R[R_N_QUERY] * g) + row * g + hl) * R[R_LSE_CHUNKS] + chunk;
-            else
+            if (LSE) {
+                ml_slot = prm.lse_part + R[R_LSE_BASE] +
+                          ((int64_t)kvh * (R[R_N_QUERY] * g) + row * g + hl) * R[R_LSE_CHUNKS] + chunk;
+            } else if (R[R_NSPLIT] == 1) {
                 out_row = prm.out + ((int64_t)(row_base + row) * Hq + kvh * g + hl) * D;
+            } else {
+                const int64_t prow = (int64_t)(R[R_SLOT_BASE] + (kvh * R[R_NPAIRS] + qpair) * R[R_NSPLIT] + chunk) *
+                                         (kQTilesPerCta * kTileRows) + t * kTileRows + m;
+                out_row = prm.part_o + prow * D;
+                ml_slot = prm.part_ml + prow;
+            }
         }
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
+        for (int j = 0; j < n_loc; ++j) {    // j: local tile index
             const int ks = j & 1;
             ok = mbar_wait(&bars[B_S_FULL + t], j & 1, abort_flag);
             ok = ok && mbar_wait(&bars[B_KROT_FULL + ks], (j >> 1) & 1, abort_flag);
@@ -578,7 +593,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const bool full = __all_sync(0xffffffffu, cut == kTileKeys);   // no row of the warp is cut
             // pass 1: row max
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
+#pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t sv[32];
                 tmem_ld32(tS + cc * 32, sv);
@@ -615,22 +630,28 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             // pass 2: p = 2^(s - m) for visible keys; P (bf16 pairs) overwrites the S columns
             // already read (columns [16cc, 16cc+16) after S columns [32cc, 32cc+32) are loaded)
             float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+#pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t sv[32], pk[16];
                 tmem_ld32(tS + cc * 32, sv);
                 tmem_ld_wait();
-                const int k = full ? 32 : cut - 32 * cc;
+                if (full) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float p0 = ex2(__uint_as_float(sv[2 * e]) - msub);
-                    float p1 = ex2(__uint_as_float(sv[2 * e + 1]) - msub);
-                    if (!full) {
-                        p0 = 2 * e < k ? p0 : 0.f;
-                        p1 = 2 * e + 1 < k ? p1 : 0.f;
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = ex2(__uint_as_float(sv[2 * e]) - msub);
+                        const float p1 = ex2(__uint_as_float(sv[2 * e + 1]) - msub);
+                        sum4[e & 3] += p0 + p1;
+                        pk[e] = pack_bf16x2(p0, p1);
                     }
-                    sum4[e & 3] += p0 + p1;
-                    pk[e] = pack_bf16x2(p0, p1);
+                } else {
+                    const int k = cut - 32 * cc;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = 2 * e < k ? ex2(__uint_as_float(sv[2 * e]) - msub) : 0.f;
+                        const float p1 = 2 * e + 1 < k ? ex2(__uint_as_float(sv[2 * e + 1]) - msub) : 0.f;
+                        sum4[e & 3] += p0 + p1;
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
                 }
                 if (!LSE) tmem_st16(tS + cc * 16, pk);
             }
@@ -655,10 +676,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 mbar_arrive(&bars[B_P_FULL + t]);
             }
         }
-        if (LSE) {
-            if (ok && valid) *lse_slot = make_float2(m_run, l_run);
-        } else if (ok && n_tiles > 0) {
-            ok = mbar_wait(&bars[B_PV_DONE + t], (n_tiles - 1) & 1, abort_flag);
+        if (ml_slot != nullptr && ok) *ml_slot = make_float2(n_loc > 0 ? m_run : -INFINITY, l_run);
+        if (!LSE && ok && n_loc > 0) {
+            ok = mbar_wait(&bars[B_PV_DONE + t], (n_loc - 1) & 1, abort_flag);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;

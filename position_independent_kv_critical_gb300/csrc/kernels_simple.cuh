@@ -247,4 +247,55 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
     for (int c = threadIdx.x; c < row_chunks; c += blockDim.x) d[c] = __ldg(s + c);
 }
 
+// ------------------------------------------------------------------ split-range combine
+// A (request, kv head, tile pair) whose key range was split over R_NSPLIT CTAs left, per split s,
+// a normalized partial row O_s = (sum_u p_u v_u) / l_s together with (m_s, l_s) (running max in log2
+// units, running sum).  The full row is sum_s w_s O_s / sum_s w_s with w_s = l_s 2^(m_s - max m).
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict__ L,
+                                                      const __nv_bfloat16* __restrict__ part_o,
+                                                      const float2* __restrict__ part_ml,
+                                                      __nv_bfloat16* __restrict__ out) {
+    constexpr int CH = D / 8;                   // 16-byte chunks per row
+    constexpr int RPB = 256 / CH;               // rows per block
+    const int32_t* item = L + L[L_OFF_COMB] + kItemWords * blockIdx.x;
+    const int req = item[0], kvh = item[1], qpair = item[2];
+    const int32_t* R = L + L[L_OFF_REQ] + req * R_STRIDE;
+    const int ns = R[R_NSPLIT];
+    const int g = L[L_GROUP], Hq = L[L_HQ];
+    const int pr = blockIdx.y * RPB + threadIdx.x / CH;   // row within the pair, 0..255
+    const int c = threadIdx.x % CH;
+    const int tpt = kTileRows / g;
+    const int tt = pr / kTileRows, mm = pr % kTileRows;
+    const int row = qpair * kQTilesPerCta * tpt + tt * tpt + mm / g;
+    if (row >= R[R_N_ROWS]) return;
+    const int64_t slot0 = (int64_t)R[R_SLOT_BASE] + (int64_t)(kvh * R[R_NPAIRS] + qpair) * ns;
+    const int64_t stride = kQTilesPerCta * kTileRows;
+    float M = -INFINITY;
+    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, part_ml[(slot0 + sp) * stride + pr].x);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float W = 0.f;
+    for (int sp = 0; sp < ns; ++sp) {
+        const float2 ml = part_ml[(slot0 + sp) * stride + pr];
+        if (ml.x == -INFINITY || ml.y <= 0.f) continue;
+        const float w = ml.y * ex2(ml.x - M);
+        W += w;
+        const uint4 v = *reinterpret_cast<const uint4*>(part_o + ((slot0 + sp) * stride + pr) * D + 8 * c);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc[2 * e] += w * bf16_lo(u[e]);
+            acc[2 * e + 1] += w * bf16_hi(u[e]);
+        }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    uint4 o;
+    o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    const int hl = mm % g;
+    *reinterpret_cast<uint4*>(out + ((int64_t)(R[R_ROW_BASE] + row) * Hq + kvh * g + hl) * D + 8 * c) = o;
+}
+
 }  // namespace pcf

@@ -19,6 +19,9 @@ constexpr int kPagesPerTile = kTileKeys / kPage;
 constexpr int kMaxPosLimit = 1 << 20;
 constexpr int kItemWords = 4;
 constexpr int kLseTargetCtas = 2 * 152;  // GB300: 152 SMs; split keys until ~2 CTAs per SM
+constexpr int kAttnTargetCtas = 2 * 152; // attention: split the key range of small batches
+constexpr int kMinTilesPerSplit = 4;
+constexpr int kMaxSplits = 8;
 
 enum : int {
     L_MAGIC = 0, L_WORDS = 1, L_N_REQS = 2, L_HQ = 3, L_HKV = 4, L_D = 5, L_N_PHYS = 6,
@@ -27,15 +30,20 @@ enum : int {
     L_TOTAL_KTILES = 17, L_N_ATTN_ITEMS = 18, L_N_LSE_ITEMS = 19, L_N_IMP_ITEMS = 20,
     L_LSE_SLOTS = 21, L_GROUP = 22, L_MAX_SPAN_LEN = 23,
     L_OFF_REQ = 24, L_OFF_SPAN = 25, L_OFF_BLOCK = 26, L_OFF_PAGEPOS = 27, L_OFF_ATTN = 28,
-    L_OFF_LSE = 29, L_OFF_IMP = 30, L_OFF_QPOS = 31,
-    L_HEADER = 32
+    L_OFF_LSE = 29, L_OFF_IMP = 30, L_OFF_QPOS = 31, L_OFF_COMB = 32, L_N_COMB = 33,
+    L_ATTN_SLOTS = 34,
+    L_HEADER = 40
 };
 
 // per-request record
 enum : int {
     R_N_PAGES = 0, R_TOK_BASE = 1, R_PAGE_BASE = 2, R_Q_BASE = 3, R_ROW_BASE = 4, R_SEL_BASE = 5,
     R_QUERY_POS0 = 6, R_N_SPANS = 7, R_SPAN_BASE = 8, R_N_QUERY = 9, R_N_SEL = 10, R_N_ROWS = 11,
-    R_LSE_BASE = 12, R_LSE_CHUNKS = 13, R_KTILE_BASE = 14, R_N_KTILES = 15, R_STRIDE = 16
+    R_LSE_BASE = 12, R_LSE_CHUNKS = 13, R_KTILE_BASE = 14, R_N_KTILES = 15,
+    R_NSPLIT = 16,      // attention key-range splits of every (kv head, tile pair) of the request
+    R_SLOT_BASE = 17,   // first partial-output slot of the request (when R_NSPLIT > 1)
+    R_NPAIRS = 18,      // tile pairs of the request (per kv head)
+    R_STRIDE = 20
 };
 
 // per-span record
@@ -45,9 +53,10 @@ enum : int {
 };
 
 // work items (kItemWords each)
-//   attention : {req, kv head, q tile pair, estimated cost}   sorted by cost, largest first
+//   attention : {req, kv head, q tile pair, key-range split}   largest estimated cost first
 //   lse       : {req, kv head, q tile pair, key chunk}
 // (a "q tile pair" p covers the 128-row query tiles 2p and 2p+1 of the request)
 //   importance: {req, key tile, kv head, 0}
+//   combine   : {req, kv head, q tile pair, 0}   pairs whose key range was split
 
 }  // namespace pcf

@@ -105,13 +105,16 @@ ScoreWs score_ws(const int32_t* H) {
 }
 
 struct AttnWs {
-    size_t q, k, total;
+    size_t q, k, po, pml, total;
 };
 AttnWs attn_ws(const int32_t* H) {
     AttnWs w;
     w.q = 0;
     w.k = align_up((size_t)H[L_TOTAL_ROWS] * H[L_HQ] * H[L_D] * 2);
-    w.total = align_up(w.k + (size_t)H[L_TOTAL_ROWS] * H[L_HKV] * H[L_D] * 2);
+    w.po = align_up(w.k + (size_t)H[L_TOTAL_ROWS] * H[L_HKV] * H[L_D] * 2);
+    const size_t prow = (size_t)H[L_ATTN_SLOTS] * kQTilesPerCta * kTileRows;   // partial rows
+    w.pml = align_up(w.po + prow * H[L_D] * 2);
+    w.total = align_up(w.pml + prow * sizeof(float2));
     return w;
 }
 
@@ -167,7 +170,7 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
         using SM = AttnSmem<D, true>;
         auto kern = attn_kernel<D, true>;
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
-        AttnParams p{lay->dev, nullptr, nullptr, rope2, nullptr, lse};
+        AttnParams p{lay->dev, nullptr, nullptr, rope2, nullptr, lse, nullptr, nullptr};
         kern<<<H[L_N_LSE_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq128, tk, zero, zero, zero, p);
         if ((s = launched()) != PCF_OK) return s;
     }
@@ -213,9 +216,17 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     using SM = AttnSmem<D, false>;
     auto kern = attn_kernel<D, false>;
     if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
-    AttnParams p{lay->dev, excl, row_pos, rope2, reinterpret_cast<__nv_bfloat16*>(out), nullptr};
+    __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(base + w.po);
+    float2* part_ml = reinterpret_cast<float2*>(base + w.pml);
+    AttnParams p{lay->dev, excl, row_pos, rope2, reinterpret_cast<__nv_bfloat16*>(out), nullptr, part_o, part_ml};
     kern<<<H[L_N_ATTN_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq, tkp, tvp, tkf, tvf, p);
-    return launched();
+    if ((s = launched()) != PCF_OK) return s;
+    if (H[L_N_COMB] > 0) {
+        combine_kernel<D><<<dim3(H[L_N_COMB], D / 8), 256, 0, st>>>(lay->dev, part_o, part_ml,
+                                                                   reinterpret_cast<__nv_bfloat16*>(out));
+        if ((s = launched()) != PCF_OK) return s;
+    }
+    return PCF_OK;
 }
 
 }  // namespace

@@ -60,7 +60,8 @@ struct Plan {
     int32_t total_tokens = 0, total_query = 0, total_rows = 0, total_sel = 0, total_pages = 0;
     int32_t n_spans = 0, max_tokens = 0, max_rows = 0, max_query = 0, total_ktiles = 0;
     int32_t n_attn = 0, n_lse = 0, n_imp = 0, lse_slots = 0, max_span_len = 0;
-    std::vector<int32_t> lse_chunks;
+    int32_t n_comb = 0, attn_slots = 0;
+    std::vector<int32_t> lse_chunks, nsplit;
 };
 
 inline int32_t cdiv(int64_t a, int64_t b) { return (int32_t)((a + b - 1) / b); }
@@ -77,7 +78,7 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
     if (g > kTileRows || kTileRows % g != 0) return PCF_ERR_UNSUPPORTED;
 
     int64_t tot_tok = 0, tot_q = 0, tot_rows = 0, tot_sel = 0, tot_spans = 0, tot_kt = 0;
-    int64_t base_lse_ctas = 0;
+    int64_t base_lse_ctas = 0, base_attn_ctas = 0;
     for (int b = 0; b < n_reqs; ++b) {
         const pcf_request_desc& r = reqs[b];
         if (r.n_spans < 0 || r.n_query < 0 || (r.n_spans > 0 && !r.spans)) return PCF_ERR_INVALID_ARG;
@@ -108,6 +109,7 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
         tot_kt += nkt;
         if (nkt > 0 && r.n_query > 0)
             base_lse_ctas += (int64_t)d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta);
+        base_attn_ctas += (int64_t)d.n_kv_heads * cdiv((n_sel + r.n_query) * g, kTileRows * kQTilesPerCta);
         plan->max_tokens = std::max<int32_t>(plan->max_tokens, (int32_t)n_tok);
         plan->max_rows = std::max<int32_t>(plan->max_rows, (int32_t)(n_sel + r.n_query));
         plan->max_query = std::max<int32_t>(plan->max_query, r.n_query);
@@ -127,8 +129,11 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
 
     // key-chunk split of the LSE pass: aim for ~kLseTargetCtas CTAs in total
     const int32_t want = base_lse_ctas > 0 ? cdiv(kLseTargetCtas, base_lse_ctas) : 1;
+    // key-range split of the attention: only batches too small to fill the GPU with tile pairs
+    const int32_t want_split = base_attn_ctas > 0 ? std::min<int64_t>(kMaxSplits, cdiv(kAttnTargetCtas, base_attn_ctas)) : 1;
     plan->lse_chunks.assign(n_reqs, 0);
-    int64_t n_attn = 0, n_lse = 0, n_imp = 0, slots = 0;
+    plan->nsplit.assign(n_reqs, 1);
+    int64_t n_attn = 0, n_lse = 0, n_imp = 0, slots = 0, n_comb = 0, attn_slots = 0;
     for (int b = 0; b < n_reqs; ++b) {
         const pcf_request_desc& r = reqs[b];
         int64_t n_tok = 0, n_sel = 0;
@@ -138,7 +143,15 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
         }
         const int32_t nkt = cdiv(n_tok / kPage, kPagesPerTile);
         const int64_t rows = n_sel + r.n_query;
-        n_attn += (int64_t)d.n_kv_heads * cdiv(rows * g, kTileRows * kQTilesPerCta);
+        const int64_t npairs = cdiv(rows * g, kTileRows * kQTilesPerCta);
+        const int32_t max_tiles = nkt + cdiv(rows, kTileKeys);   // key tiles the last pair sees
+        const int32_t ns = std::max(1, std::min<int32_t>(want_split, max_tiles / kMinTilesPerSplit));
+        plan->nsplit[b] = ns;
+        n_attn += (int64_t)d.n_kv_heads * npairs * ns;
+        if (ns > 1) {
+            n_comb += (int64_t)d.n_kv_heads * npairs;
+            attn_slots += (int64_t)d.n_kv_heads * npairs * ns;
+        }
         if (nkt > 0 && r.n_query > 0) {
             const int32_t tpc = cdiv(nkt, std::max(1, std::min(want, nkt)));
             const int32_t chunks = cdiv(nkt, tpc);
@@ -148,14 +161,17 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
         }
         if (nkt > 0) n_imp += (int64_t)nkt * d.n_kv_heads;
     }
-    if (n_attn >= lim || n_lse >= lim || n_imp >= lim || slots >= lim) return PCF_ERR_INVALID_ARG;
+    if (n_attn >= lim || n_lse >= lim || n_imp >= lim || slots >= lim || attn_slots >= lim / 256)
+        return PCF_ERR_INVALID_ARG;
+    plan->n_comb = (int32_t)n_comb;
+    plan->attn_slots = (int32_t)attn_slots;
     plan->n_attn = (int32_t)n_attn;
     plan->n_lse = (int32_t)n_lse;
     plan->n_imp = (int32_t)n_imp;
     plan->lse_slots = (int32_t)slots;
 
     plan->words = L_HEADER + (int64_t)n_reqs * R_STRIDE + tot_spans * S_STRIDE +
-                  2 * (int64_t)plan->total_pages + kItemWords * (n_attn + n_lse + n_imp) + tot_q;
+                  2 * (int64_t)plan->total_pages + kItemWords * (n_attn + n_lse + n_imp + n_comb) + tot_q;
     if (plan->words >= ((int64_t)1 << 31)) return PCF_ERR_INVALID_ARG;
     return PCF_OK;
 }
@@ -208,6 +224,8 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
     H[L_LSE_SLOTS] = plan.lse_slots;
     H[L_GROUP] = g;
     H[L_MAX_SPAN_LEN] = plan.max_span_len;
+    H[L_N_COMB] = plan.n_comb;
+    H[L_ATTN_SLOTS] = plan.attn_slots;
 
     int64_t off = L_HEADER;
     H[L_OFF_REQ] = (int32_t)off;    off += (int64_t)n_reqs * R_STRIDE;
@@ -218,6 +236,7 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
     H[L_OFF_LSE] = (int32_t)off;    off += (int64_t)kItemWords * plan.n_lse;
     H[L_OFF_IMP] = (int32_t)off;    off += (int64_t)kItemWords * plan.n_imp;
     H[L_OFF_QPOS] = (int32_t)off;   off += plan.total_query;
+    H[L_OFF_COMB] = (int32_t)off;   off += (int64_t)kItemWords * plan.n_comb;
 
     int32_t* REQ = blob + H[L_OFF_REQ];
     int32_t* SPN = blob + H[L_OFF_SPAN];
@@ -225,12 +244,14 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
     int32_t* PPOS = blob + H[L_OFF_PAGEPOS];
     int32_t* QPOS = blob + H[L_OFF_QPOS];
 
-    struct AttnItem { int32_t req, kvh, qt; int64_t cost; int64_t order; };
+    struct AttnItem { int32_t req, kvh, qt, split; int64_t cost; int64_t order; };
     std::vector<AttnItem> attn;
     attn.reserve(plan.n_attn);
     int32_t* LSE = blob + H[L_OFF_LSE];
     int32_t* IMP = blob + H[L_OFF_IMP];
-    int64_t n_lse = 0, n_imp = 0;
+    int32_t* COMB = blob + H[L_OFF_COMB];
+    int64_t n_lse = 0, n_imp = 0, n_comb = 0;
+    int32_t slot_base = 0;
 
     int32_t tok_base = 0, q_base = 0, row_base = 0, sel_base = 0, span_base = 0, kt_base = 0;
     int32_t lse_base = 0;
@@ -274,12 +295,17 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
         R[R_LSE_CHUNKS] = plan.lse_chunks[b];
         R[R_KTILE_BASE] = kt_base;
         R[R_N_KTILES] = nkt;
+        const int32_t ns = plan.nsplit[b];
+        R[R_NSPLIT] = ns;
+        R[R_SLOT_BASE] = slot_base;
         for (int t = 0; t < r.n_query; ++t) QPOS[q_base + t] = r.query_pos0 + t;
 
         // attention work: one item per (kv head, pair of 128-row tiles); rows pack the g heads of a
         // token
         const int32_t toks_per_item = kQTilesPerCta * (kTileRows / g);
         const int32_t n_qt = cdiv((int64_t)n_rows * g, kTileRows * kQTilesPerCta);
+        R[R_NPAIRS] = n_qt;
+        if (ns > 1) slot_base += d.n_kv_heads * n_qt * ns;
         for (int32_t qt = 0; qt < n_qt; ++qt) {
             const int64_t last_row = std::min<int64_t>((int64_t)(qt + 1) * toks_per_item, n_rows) - 1;
             // estimated visible keys: query rows see everything, recomputed rows about the
@@ -287,8 +313,14 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
             int64_t cost;
             if (last_row >= n_sel) cost = (int64_t)n_tok + n_rows;
             else cost = ((int64_t)(last_row + 1) * (n_tok + n_sel)) / std::max<int64_t>(1, n_sel);
-            for (int32_t h = 0; h < d.n_kv_heads; ++h)
-                attn.push_back({b, h, qt, cost, (int64_t)attn.size()});
+            for (int32_t h = 0; h < d.n_kv_heads; ++h) {
+                for (int32_t sp = 0; sp < ns; ++sp)
+                    attn.push_back({b, h, qt, sp, cost / ns, (int64_t)attn.size()});
+                if (ns > 1) {
+                    int32_t* it = COMB + kItemWords * n_comb++;
+                    it[0] = b; it[1] = h; it[2] = qt; it[3] = 0;
+                }
+            }
         }
         // LSE work: (kv head, query tile pair, key chunk)
         if (plan.lse_chunks[b] > 0) {
@@ -322,7 +354,7 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
         ATT[kItemWords * i + 0] = attn[i].req;
         ATT[kItemWords * i + 1] = attn[i].kvh;
         ATT[kItemWords * i + 2] = attn[i].qt;
-        ATT[kItemWords * i + 3] = (int32_t)std::min<int64_t>(attn[i].cost, 0x7fffffff);
+        ATT[kItemWords * i + 3] = attn[i].split;
     }
     return PCF_OK;
 }

@@ -96,11 +96,13 @@ def test_layout_totals_and_block_table(name):
     # every (request, kv head, pair of 128-row tiles) appears once in the attention work list
     g = cfg.hq // cfg.hkv
     items = B[B[L_OFF_ATTN]: B[L_OFF_ATTN] + 4 * B[L_N_ATTN]].reshape(-1, 4)
-    want = {(b, h, t) for b, r in enumerate(reqs) for h in range(cfg.hkv)
-            for t in range(-(-r.n_rows * g // 256))}
-    got = {tuple(x) for x in items[:, :3].tolist()}
+    REQ = B[L_OFF_REQ]
+    nsplit = [int(B[REQ + 20 * b + 16]) for b in range(len(reqs))]
+    want = {(b, h, t, s) for b, r in enumerate(reqs) for h in range(cfg.hkv)
+            for t in range(-(-r.n_rows * g // 256)) for s in range(nsplit[b])}
+    got = {tuple(x) for x in items.tolist()}
     assert got == want and len(items) == len(want)
-    assert np.all(np.diff(items[:, 3]) <= 0)   # largest estimated cost first
+    assert all(1 <= n <= 8 for n in nsplit)
     imp = B[B[L_OFF_IMP]: B[L_OFF_IMP] + 4 * B[L_N_IMP]].reshape(-1, 4)
     assert len(imp) == sum(-(-r.n_cached // 128) for r in reqs) * cfg.hkv
 
