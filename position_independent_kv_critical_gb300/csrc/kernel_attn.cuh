@@ -1,27 +1,36 @@
-// Flash-style attention over the position-free paged cache with in-kernel RoPE (sm_103a).
+// Flash-style attention over the position-free paged cache (sm_103a).
 //
-// MiniPIC, section 2.1: cached keys k~_j stay unrotated in shared pages; the attention kernel
-// rotates them on the fly to the key's per-request logical position pi(j) with a cos/sin lookup
-// and fused multiply-adds, so score(t, j) = (R_t q_t)^T (R_pi(j) k~_j) / sqrt(d).
+// MiniPIC, section 2.1: cached keys k~_j stay unrotated in shared pages and are rotated at use time
+// to the key's per-request logical position pi(j), so score(t, j) = (R_t q_t)^T (R_pi(j) k~_j) /
+// sqrt(d).  The rotation of a request's cached keys runs once per call (rope_rows_kernel in page
+// gather mode, into the call's workspace) rather than inside this kernel: a cached key tile is
+// visited by every 256-row query block of the request, and rotating it there costs more than
+// writing and re-reading the rotated tile once.
 // QCFuse, section 2C / Phase 4 (and the sparse attention kernel of its section 3): the recomputed
 // tokens and the query tokens attend over the cached keys minus the recomputed ones plus the
 // fresh rows, keeping causal order on logical positions.
 //
 // One CTA = two tiles A and B of 128 query rows each (a tile packs the g query heads of 128/g
 // consecutive rows of one request, all sharing kv head `kvh`) against the request's KV tiles of
-// 128 keys; both tiles share every rotated K tile and every V tile:
-//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: S row from TMEM, mask, online
-//               softmax (lazy rescale), P -> TMEM (over the S columns), O epilogue
-//   warps 8-11  rotate cached K tiles in shared memory (in place, 128-byte swizzled K-major)
-//   warp  12    TMEM allocation + single-thread tcgen05.mma issue, in the order
-//               PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1), so that the tensor core works on one tile
-//               while the other tile's softmax runs
-//   warp  13    K producer (TMA): Q tiles, cached K pages through the block table with their page
-//               cos/sin rows, fresh K tiles; 2-stage ring, freed by the second QK^T of a stage
-//   warp  14    V producer (TMA): cached V pages / fresh V tiles; 2-stage ring, freed by PV_B
-// TMEM: S_A / P_A at columns [0,128), S_B / P_B at [128,256), O_A at [256,256+d), O_B at
-// [384,384+d).  S = Q K^T is fp16 x fp16 (M=128, N=128 keys, K=d); P (bf16) overwrites its own S
-// columns and is the A operand of O += P V (M=128, N=d, V as an MN-major bf16 operand).
+// 128 keys; both tiles share every K and V tile:
+//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: S row from TMEM, causal cut,
+//               online softmax (lazy rescale), P -> TMEM (over the S columns), O epilogue
+//   warps 8/11  Q K^T issue for tile A / B (warp 8 also owns the TMEM allocation)
+//   warps 12/13 P V issue for tile A / B.  Each key tile is processed in two 64-key halves
+//               q = 2j, 2j+1 and S is double-buffered per query tile: P(q) V runs, then Q K(q+2)
+//               goes into the buffer P(q) came from, while the softmax already works on S(q+1).
+//               Four single-thread issuers keep four independent MMA streams in flight: one
+//               thread's stream of 128-row MMAs with N <= 128 is bound by per-instruction
+//               latency, not by the tensor core's rate
+//   warp  9     K producer: Q tiles; rotated K tiles (cached or fresh, fp16, TMA) and, per key,
+//               its logical position and bias; 2-stage ring, freed by the second half's Q K^T
+//   warp  10    V producer (TMA): cached V pages through the block table / fresh V tiles; 2-stage
+//               ring, freed once both P V of a stage are done
+// TMEM: tile t's two S half-buffers at columns t*128 + {0, 64} (64 fp32 columns = 64 keys each),
+// O_A at [256,256+d), O_B at [384,384+d).  S = Q K^T is fp16 x fp16 (M=128, N=64 keys, K=d); P
+// (bf16 pairs, 32 columns) overwrites the S half it came from and is the A operand of
+// O += P V (M=128, N=d in one instruction, K=64 keys, V as an MN-major bf16 operand whose two
+// 64-wide halves are 16 KB apart).
 // Keys that do not take part (recomputed tokens' cached copies, missing pages or rows) are
 // removed by the tensor core itself: Q K^T gets one more K=16 step whose A slab is a column of
 // ones and whose B slab carries 0 or -30000 per key, so their scores (log2 units) underflow to
@@ -34,12 +43,14 @@
 
 namespace pcf {
 
-constexpr int kAttnThreads = 480;   // 15 warps
+constexpr int kAttnThreads = 448;   // 14 warps: at most 4 per SM sub-partition (128 registers)
 constexpr int kWarpSoftB = 4;
-constexpr int kWarpRot0 = 8;
-constexpr int kWarpMma = 12;
-constexpr int kWarpTma = 13;
-constexpr int kWarpTmaV = 14;
+constexpr int kWarpMma = 8;
+constexpr int kWarpTma = 9;
+constexpr int kWarpTmaV = 10;
+constexpr int kWarpMmaB = 11;
+constexpr int kWarpPvA = 12;
+constexpr int kWarpPvB = 13;
 constexpr int kNoPos = 0x7FFFFFFF;
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
@@ -51,7 +62,6 @@ struct AttnParams {
     const int32_t* layout;
     const uint16_t* excl;      // attention: per logical page exclusion bits
     const int32_t* row_pos;    // attention: logical position of every row
-    const float2* rope;        // [max_pos][D/2] (cos, sin)
     __nv_bfloat16* out;        // attention: [rows][Hq][D]
     float2* lse_part;          // LSE: (running max in log2 units, running sum) per row and chunk
     __nv_bfloat16* part_o;     // attention with a split key range: normalized partial O per slot
@@ -64,16 +74,14 @@ struct AttnSmem {
     static constexpr int kQ = kTileRows * D * 2;          // one Q tile
     static constexpr int kK = kTileKeys * D * 2;
     static constexpr int kV = LSE ? 0 : kTileKeys * D * 2;
-    static constexpr int kCs = kPagesPerTile * (D / 2) * 8;
     static constexpr int oQ = 0;
     static constexpr int oK = oQ + kQTilesPerCta * kQ;
     static constexpr int oV = oK + kKStages * kK;
-    static constexpr int oCs = oV + kVStages * kV;
-    static constexpr int oKpos = oCs + kKStages * kCs;
+    static constexpr int oKpos = oV + kVStages * kV;
     static constexpr int oQaug = oKpos + kKStages * kTileKeys * 4;   // ones column (1024-aligned)
     static constexpr int oKaug = oQaug + kSlab16;                    // per K stage: key bias column
     static constexpr int oBar = oKaug + kKStages * kSlab16;
-    static constexpr int kNumBars = 24;
+    static constexpr int kNumBars = 30;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int kBytes = oMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
@@ -83,117 +91,22 @@ struct AttnSmem {
 // barrier slots
 enum : int {
     B_Q_FULL = 0,
-    B_K_FULL = 1,      // [2] K pages (+ cos/sin rows) landed
-    B_KROT_FULL = 3,   // [2] K tile rotated, key positions and validity written
-    B_K_EMPTY = 5,     // [2] both Q K^T that read the stage are done
-    B_KPOS_FREE = 7,   // [2] both softmax groups are done with the stage's key info (256 arrivals)
-    B_V_FULL = 9,      // [2]
-    B_V_EMPTY = 11,    // [2] P_B V that read the stage is done
-    B_S_FULL = 13,     // [2] per Q tile: S = Q K^T landed
-    B_S_FREE = 15,     // [2] per Q tile (LSE mode): softmax done reading S
-    B_P_FULL = 17,     // [2] per Q tile: P written, O rescaled
-    B_PV_DONE = 19,    // [2] per Q tile: P V done (O final for this tile, S/P columns free)
-    B_DRAIN = 21
+    B_K_FULL = 1,      // [2] rotated K tile landed and its key positions / biases written
+    B_K_EMPTY = 3,     // [2] both Q K^T that read the stage are done (one commit per issuer)
+    B_KPOS_FREE = 5,   // [2] both softmax groups are done with the stage's key info (256 arrivals)
+    B_V_FULL = 7,      // [2]
+    B_V_EMPTY = 9,     // [2] both P V that read the stage are done (one commit per issuer)
+    B_S_FULL = 11,     // [4] per (Q tile, S half-buffer): S = Q K^T of a 64-key half landed
+    B_P_FULL = 15,     // [4] per (Q tile, S half-buffer): P written and O rescaled; in LSE mode:
+                       //     softmax done reading that S half
+    B_PV_DONE = 19,    // [4] per (Q tile, S half-buffer): P V of that buffer's latest half is done
+    B_O_DONE = 23,     // [2] per Q tile: the last P V is done (single phase)
+    B_DRAIN = 25       // [4] per issuer: its last MMA is done
 };
 
-__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
-    return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.y, b.x, a.x * b.y));
-}
-
-// Rotate the 8 pairs (i, i + D/2), i = 8c .. 8c+7, of key row `row` in a swizzled K tile, in place:
-// bf16 in (the unrotated page), fp16 out (operand of the fp16 Q K^T).
-template <int D>
-__device__ __forceinline__ void rotate_chunk_pair(uint8_t* sK, int row, int c, const float2 (&cs)[8]) {
-    uint8_t* pa;
-    uint8_t* pb;
-    if (D == 128) {
-        pa = sK + sw128_off(row, c);
-        pb = sK + 16384 + sw128_off(row, c);
-    } else {
-        pa = sK + sw128_off(row, c);
-        pb = sK + sw128_off(row, c + 4);
-    }
-    const uint4 a = *reinterpret_cast<const uint4*>(pa);
-    const uint4 b = *reinterpret_cast<const uint4*>(pb);
-    const uint32_t ia[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t ib[4] = {b.x, b.y, b.z, b.w};
-    uint32_t oa[4], ob[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float2 c0 = cs[2 * e], c1 = cs[2 * e + 1];
-        const float a0 = bf16_lo(ia[e]), a1 = bf16_hi(ia[e]);
-        const float b0 = bf16_lo(ib[e]), b1 = bf16_hi(ib[e]);
-        oa[e] = pack_f16x2(fmaf(a0, c0.x, -b0 * c0.y), fmaf(a1, c1.x, -b1 * c1.y));
-        ob[e] = pack_f16x2(fmaf(b0, c0.x, a0 * c0.y), fmaf(b1, c1.x, a1 * c1.y));
-    }
-    *reinterpret_cast<uint4*>(pa) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-    *reinterpret_cast<uint4*>(pb) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-}
-
-// Rotation of one cached K tile by 128 threads (rt = 0..127).  Thread (c, pg, rg) owns chunk pair
-// c of rows rg*RPT .. rg*RPT+RPT-1 of page pg; it composes the page-base angle (table row of the
-// page's first position, in sCs) with its first row's offset once and then advances the angle by
-// one position per row.  All rows are loaded before any is stored (no shared-memory round trip
-// per row).  Rows of missing pages hold stale finite data and are masked by the softmax.
-template <int D>
-__device__ __forceinline__ int rot_page_of(int rt) { return (rt / (D / 16)) % kPagesPerTile; }
-
-template <int D>
-__device__ __forceinline__ void rotate_cached_tile(uint8_t* sK, const float2* sCs, int rt,
-                                                   const float2* __restrict__ cs_start_g, const float2 (&cs_step)[8]) {
-    constexpr int CPR = D / 16;
-    constexpr int RGN = kTileKeys / (CPR * kPagesPerTile);
-    constexpr int RPT = kPage / RGN;
-    const int c = rt % CPR;
-    const int pg = (rt / CPR) % kPagesPerTile;
-    const int rg = rt / (CPR * kPagesPerTile);
-    const int row0 = pg * kPage + rg * RPT;
-    uint8_t* base_a = sK;
-    uint8_t* base_b = sK + (D == 128 ? 16384 : 0);
-    const int cb = D == 128 ? c : c + 4;
-    float2 cs[8];
-    const float4* b4 = reinterpret_cast<const float4*>(sCs + pg * (D / 2) + 8 * c);
-    const float4* s4 = reinterpret_cast<const float4*>(cs_start_g);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float4 v = b4[q];
-        const float4 w = __ldg(s4 + q);
-        cs[2 * q] = cmul(make_float2(v.x, v.y), make_float2(w.x, w.y));
-        cs[2 * q + 1] = cmul(make_float2(v.z, v.w), make_float2(w.z, w.w));
-    }
-    // rows are independent: the next row is loaded before the current one is written back
-    uint4 a_nx = *reinterpret_cast<const uint4*>(base_a + sw128_off(row0, c));
-    uint4 b_nx = *reinterpret_cast<const uint4*>(base_b + sw128_off(row0, cb));
-#pragma unroll 1
-    for (int r = 0; r < RPT; ++r) {
-        const uint4 a = a_nx, b = b_nx;
-        if (r + 1 < RPT) {
-            a_nx = *reinterpret_cast<const uint4*>(base_a + sw128_off(row0 + r + 1, c));
-            b_nx = *reinterpret_cast<const uint4*>(base_b + sw128_off(row0 + r + 1, cb));
-        }
-        const uint32_t ia[4] = {a.x, a.y, a.z, a.w};
-        const uint32_t ib[4] = {b.x, b.y, b.z, b.w};
-        uint32_t oa[4], ob[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 c0 = cs[2 * e], c1 = cs[2 * e + 1];
-            const float a0 = bf16_lo(ia[e]), a1 = bf16_hi(ia[e]);
-            const float b0 = bf16_lo(ib[e]), b1 = bf16_hi(ib[e]);
-            oa[e] = pack_f16x2(fmaf(a0, c0.x, -b0 * c0.y), fmaf(a1, c1.x, -b1 * c1.y));
-            ob[e] = pack_f16x2(fmaf(b0, c0.x, a0 * c0.y), fmaf(b1, c1.x, a1 * c1.y));
-        }
-        *reinterpret_cast<uint4*>(base_a + sw128_off(row0 + r, c)) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-        *reinterpret_cast<uint4*>(base_b + sw128_off(row0 + r, cb)) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) cs[i] = cmul(cs[i], cs_step[i]);
-    }
-}
-
-// 15 warps: 4 per SM sub-partition at most, so each thread may hold up to 128 registers; the
-// softmax works on 32-key slices of the S row to stay below that.
 template <int D, bool LSE>
 __global__ void __launch_bounds__(kAttnThreads)
-attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kpool,
+attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kcache,
             const __grid_constant__ CUtensorMap tm_vpool, const __grid_constant__ CUtensorMap tm_kfresh,
             const __grid_constant__ CUtensorMap tm_vfresh, const AttnParams prm) {
     using SM = AttnSmem<D, LSE>;
@@ -203,7 +116,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     auto sQ = [&](int t) { return smem + SM::oQ + t * SM::kQ; };
     auto sKs = [&](int st) { return smem + SM::oK + st * SM::kK; };
     auto sVs = [&](int st) { return smem + SM::oV + st * SM::kV; };
-    auto sCs = [&](int st) { return reinterpret_cast<float2*>(smem + SM::oCs + st * SM::kCs); };
     auto sKpos = [&](int st) { return reinterpret_cast<int32_t*>(smem + SM::oKpos) + st * kTileKeys; };
     uint8_t* sQaug = smem + SM::oQaug;
     auto sKaug = [&](int st) { return smem + SM::oKaug + st * kSlab16; };
@@ -233,22 +145,24 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     if (tid == 0) {
         mbar_init(&bars[B_Q_FULL], 1);
         for (int s2 = 0; s2 < kKStages; ++s2) {
-            mbar_init(&bars[B_K_FULL + s2], 1);
-            mbar_init(&bars[B_KROT_FULL + s2], 128);
-            mbar_init(&bars[B_K_EMPTY + s2], 1);
+            mbar_init(&bars[B_K_FULL + s2], 32);   // every producer lane (key info) + TMA bytes
+            mbar_init(&bars[B_K_EMPTY + s2], kQTilesPerCta);
             mbar_init(&bars[B_KPOS_FREE + s2], 256);
         }
         for (int s2 = 0; s2 < kVStages; ++s2) {
             mbar_init(&bars[B_V_FULL + s2], 1);
-            mbar_init(&bars[B_V_EMPTY + s2], 1);
+            mbar_init(&bars[B_V_EMPTY + s2], kQTilesPerCta);
         }
         for (int t = 0; t < kQTilesPerCta; ++t) {
-            mbar_init(&bars[B_S_FULL + t], 1);
-            mbar_init(&bars[B_S_FREE + t], 128);
-            mbar_init(&bars[B_P_FULL + t], 128);
-            mbar_init(&bars[B_PV_DONE + t], 1);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&bars[B_S_FULL + 2 * t + b], 1);
+                mbar_init(&bars[B_P_FULL + 2 * t + b], 128);
+            }
+            mbar_init(&bars[B_PV_DONE + 2 * t], 1);
+            mbar_init(&bars[B_PV_DONE + 2 * t + 1], 1);
+            mbar_init(&bars[B_O_DONE + t], 1);
         }
-        mbar_init(&bars[B_DRAIN], 1);
+        for (int i = 0; i < 2 * kQTilesPerCta; ++i) mbar_init(&bars[B_DRAIN + i], 1);
         fence_mbar_init();
         int nct, nft = 0, t0 = 0;
         const int nkt = R[R_N_KTILES];
@@ -302,11 +216,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ K producer
-        // Lane p (< 8) fetches the block-table entry and position of page p of the next tile while
-        // the current tile is issued, then issues that page's copies itself.
+        // Per tile: lane l writes the key info of keys l, l+32, l+64, l+96 (logical position, or
+        // kNoPos for a missing key; bias 0 or -30000), fetched one tile ahead; lane 0 then issues
+        // the rotated K tile.  The stage is reused once both Q K^T have read it and both softmax
+        // groups have read its key positions.
         if (lane == 0) {
             prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_kpool);
+            prefetch_tmap(&tm_kcache);
             if (!LSE) prefetch_tmap(&tm_kfresh);
             const int32_t qy = LSE ? (kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row0) * g
                                    : (kvh * L[L_TOTAL_ROWS] + row_base + row0) * g;
@@ -315,42 +231,63 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 for (int hb = 0; hb < H; ++hb)
                     tma_load_2d(sQ(t) + hb * 16384, &tm_q, &bars[B_Q_FULL], hb * 64, qy + t * kTileRows);
         }
-        auto meta = [&](int j, int32_t& ph, int32_t& pp) {
-            ph = -1;
-            pp = 0;
-            if (j < n_ct && lane < kPagesPerTile) {
-                const int lp = (t0 + j) * kPagesPerTile + lane;
-                if (lp < n_pages) { ph = blk[lp]; pp = page_pos[lp]; }
+        // key info of key (lane + 32 r) of tile j: logical position (kNoPos if missing) and whether
+        // it takes part (cached: page present and token not recomputed; fresh: row present)
+        auto meta = [&](int j, int32_t (&pos)[4], uint32_t& valid) {
+            valid = 0;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int key = lane + 32 * r;
+                pos[r] = kNoPos;
+                if (j < n_ct) {
+                    const int lp = (t0 + j) * kPagesPerTile + key / kPage;
+                    if (lp < n_pages) {
+                        pos[r] = page_pos[lp] + key % kPage;
+                        const uint32_t ex = LSE ? 0u : (uint32_t)prm.excl[page_base + lp];
+                        if (((ex >> (key % kPage)) & 1u) == 0u) valid |= 1u << r;
+                    }
+                } else if (j < n_tiles) {
+                    const int fr = (j - n_ct) * kTileKeys + key;
+                    if (fr < n_rows_req) { pos[r] = prm.row_pos[row_base + fr]; valid |= 1u << r; }
+                }
             }
         };
-        int32_t ph_next, pp_next;
-        meta(jb, ph_next, pp_next);
+        const int32_t kc_row0 = kvh * L[L_TOTAL_TOKENS] + R[R_TOK_BASE];
+        int32_t pos_n[4];
+        uint32_t val_n;
+        meta(jb, pos_n, val_n);
         int last[kKStages] = {-1, -1};
         for (int jj = 0; jj < n_loc; ++jj) {
             const int j = jb + jj, ks = jj & 1;
-            int32_t ph = ph_next, pp = pp_next;
-            meta(j + 1, ph_next, pp_next);
-            const bool ok = jj < kKStages || mbar_wait(&bars[B_K_EMPTY + ks], ((jj >> 1) - 1) & 1, abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            uint64_t* full = &bars[B_K_FULL + ks];
-            if (j < n_ct) {
-                const int np = min(kPagesPerTile, n_pages - (t0 + j) * kPagesPerTile);
-                constexpr uint32_t per_page = H * 2048 + (D / 2) * 8;
-                if (lane == 0) mbar_arrive_expect_tx(full, per_page * np);
-                __syncwarp();
-                if (lane < np) {
-                    if (ph < 0 || ph >= n_phys) { set_dev_error(kDevErrBounds); ph = 0; }
-                    const int32_t y = (ph * Hkv + kvh) * kPage;
+            int32_t pos[4];
 #pragma unroll
-                    for (int hb = 0; hb < H; ++hb)
-                        tma_load_2d(sKs(ks) + hb * 16384 + lane * 2048, &tm_kpool, full, hb * 64, y);
-                    bulk_load(sCs(ks) + lane * (D / 2), prm.rope + (int64_t)pp * (D / 2), (D / 2) * 8, full);
-                }
-            } else if (!LSE && lane == 0) {
-                const int32_t fr = row_base + (j - n_ct) * kTileKeys;
+            for (int r = 0; r < 4; ++r) pos[r] = pos_n[r];
+            const uint32_t val = val_n;
+            meta(j + 1, pos_n, val_n);
+            const bool ok = jj < kKStages ||
+                            (mbar_wait(&bars[B_K_EMPTY + ks], ((jj >> 1) - 1) & 1, abort_flag) &&
+                             mbar_wait(&bars[B_KPOS_FREE + ks], ((jj >> 1) - 1) & 1, abort_flag));
+            if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int key = lane + 32 * r;
+                sKpos(ks)[key] = pos[r];
+                *reinterpret_cast<__half*>(sKaug(ks) + slab16_off(key, 0)) =
+                    __float2half(((val >> r) & 1u) ? 0.f : kKeyOff);
+            }
+            fence_proxy_async_smem();   // the bias slab is read by the tensor core
+            uint64_t* full = &bars[B_K_FULL + ks];
+            if (lane != 0) {
+                mbar_arrive(full);
+            } else {
                 mbar_arrive_expect_tx(full, H * 16384);
-                for (int hb = 0; hb < H; ++hb)
-                    tma_load_2d(sKs(ks) + hb * 16384, &tm_kfresh, full, hb * 64, kvh * L[L_TOTAL_ROWS] + fr);
+                if (j < n_ct) {
+                    const int32_t y = kc_row0 + (t0 + j) * kTileKeys;
+                    for (int hb = 0; hb < H; ++hb) tma_load_2d(sKs(ks) + hb * 16384, &tm_kcache, full, hb * 64, y);
+                } else {
+                    const int32_t y = kvh * L[L_TOTAL_ROWS] + row_base + (j - n_ct) * kTileKeys;
+                    for (int hb = 0; hb < H; ++hb) tma_load_2d(sKs(ks) + hb * 16384, &tm_kfresh, full, hb * 64, y);
+                }
             }
             last[ks] = jj;
         }
@@ -405,137 +342,74 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 for (int s2 = 0; s2 < kVStages; ++s2)
                     if (last[s2] >= 0) mbar_drain(&bars[B_V_FULL + s2], (last[s2] >> 1) & 1);
         }
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == kWarpMma || warp == kWarpMmaB || warp == kWarpPvA || warp == kWarpPvB) {
+        // ------------------------------------------------------------ MMA issuers
+        const bool qk_role = warp == kWarpMma || warp == kWarpMmaB;
+        const int t = (warp == kWarpMma || warp == kWarpPvA) ? 0 : 1;
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_f16(128, 128);
-            constexpr uint32_t idesc_pv = idesc_bf16(128, 64, true);
-            auto issue_qk = [&](int t, int j) {
-                const uint32_t aQ = smem_u32(sQ(t)), aK = smem_u32(sKs(j & 1));
+            const int nq = 2 * n_loc;   // halves of this CTA's key range
+            bool ok = true;
+            if (qk_role) {
+                // Q K^T of half q = 2j + h of local key tile j: keys 64h .. 64h+63, S buffer q & 1
+                constexpr uint32_t idesc_qk = idesc_f16(128, 64);
+                const uint32_t aQ = smem_u32(sQ(t));
+                auto issue_qk = [&](int q) {
+                    const int j = q >> 1, h = q & 1;
+                    const uint32_t aK = smem_u32(sKs(j & 1)) + h * 64 * 128;
+                    const uint32_t tS = tmem + t * 128 + (q & 1) * 64;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = desc_sw128_kmajor(aQ + (kk >> 2) * 16384 + (kk & 3) * 32);
-                    const uint64_t b = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
-                    mma_bf16_ss(tmem + t * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
-                }
-                // + 1 * bias(key): 0 for taking part, -30000 for excluded / missing keys
-                mma_bf16_ss(tmem + t * 128, desc_noswz_kmajor(smem_u32(sQaug), 128, 256),
-                            desc_noswz_kmajor(smem_u32(sKaug(j & 1)), 128, 256), idesc_qk, 1u);
-                mma_commit(&bars[B_S_FULL + t]);
-            };
-            auto issue_pv = [&](int t, int j) {
-                const uint32_t aV = smem_u32(sVs(j & 1));
-#pragma unroll
-                for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-#pragma unroll
-                    for (int nh = 0; nh < H; ++nh) {
-                        const uint64_t b = desc_sw128_mn64(aV + nh * 16384 + kk * 2048);
-                        mma_bf16_ts(tmem + kTmemO + t * 128 + nh * 64, tmem + t * 128 + kk * 8, b, idesc_pv,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t a = desc_sw128_kmajor(aQ + (kk >> 2) * 16384 + (kk & 3) * 32);
+                        const uint64_t b = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
+                        mma_bf16_ss(tS, a, b, idesc_qk, kk > 0 ? 1u : 0u);
                     }
+                    // + 1 * bias(key): 0 for taking part, -30000 for excluded / missing keys
+                    mma_bf16_ss(tS, desc_noswz_kmajor(smem_u32(sQaug), 128, 256),
+                                desc_noswz_kmajor(smem_u32(sKaug(j & 1)) + h * 2048, 128, 256), idesc_qk, 1u);
+                    mma_commit(&bars[B_S_FULL + 2 * t + (q & 1)]);
+                    if (h == 1) mma_commit(&bars[B_K_EMPTY + (j & 1)]);
+                };
+                ok = mbar_wait(&bars[B_Q_FULL], 0, abort_flag);
+                ok = ok && (n_loc == 0 || mbar_wait(&bars[B_K_FULL + 0], 0, abort_flag));
+                if (ok && n_loc > 0) {
+                    tc_fence_after();
+                    issue_qk(0);
+                    issue_qk(1);
                 }
-                mma_commit(&bars[B_PV_DONE + t]);
-            };
-            bool ok = mbar_wait(&bars[B_Q_FULL], 0, abort_flag);
-            ok = ok && (n_loc == 0 || mbar_wait(&bars[B_KROT_FULL + 0], 0, abort_flag));
-            if (ok && n_loc > 0) {
-                tc_fence_after();
-                issue_qk(0, 0);
-                issue_qk(1, 0);
-                mma_commit(&bars[B_K_EMPTY + 0]);
-            }
-            for (int j = 0; ok && j < n_loc; ++j) {    // j: local tile index
-                const bool more = j + 1 < n_loc;
-                const int kn = (j + 1) & 1;
-                if (LSE) {
-                    if (more) {
-                        ok = mbar_wait(&bars[B_KROT_FULL + kn], ((j + 1) >> 1) & 1, abort_flag);
-                        for (int t = 0; ok && t < kQTilesPerCta; ++t) {
-                            ok = mbar_wait(&bars[B_S_FREE + t], j & 1, abort_flag);
-                            if (!ok) break;
-                            tc_fence_after();
-                            issue_qk(t, j + 1);
-                        }
-                        if (ok) mma_commit(&bars[B_K_EMPTY + kn]);
-                    }
-                    continue;
-                }
-                // tile A: P_A(j) V(j), then Q_A K(j+1); tile B likewise
-                ok = mbar_wait(&bars[B_P_FULL + 0], j & 1, abort_flag) &&
-                     mbar_wait(&bars[B_V_FULL + (j & 1)], (j >> 1) & 1, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(0, j);
-                if (more) {
-                    ok = mbar_wait(&bars[B_KROT_FULL + kn], ((j + 1) >> 1) & 1, abort_flag) &&
-                         mbar_wait(&bars[B_PV_DONE + 0], j & 1, abort_flag);   // P_A columns reused by S_A
+                for (int q = 0; ok && q + 2 < nq; ++q) {
+                    const int qn = q + 2, jn = qn >> 1;
+                    // S(q+2) overwrites P(q): wait until P(q) V has read it (LSE mode: until the
+                    // softmax has read S(q)); a new key tile must have landed first
+                    ok = ((qn & 1) == 1 || mbar_wait(&bars[B_K_FULL + (jn & 1)], (jn >> 1) & 1, abort_flag)) &&
+                         mbar_wait(&bars[(LSE ? B_P_FULL : B_PV_DONE) + 2 * t + (q & 1)], (q >> 1) & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_qk(0, j + 1);
+                    issue_qk(qn);
                 }
-                ok = mbar_wait(&bars[B_P_FULL + 1], j & 1, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(1, j);
-                mma_commit(&bars[B_V_EMPTY + (j & 1)]);
-                if (more) {
-                    ok = mbar_wait(&bars[B_PV_DONE + 1], j & 1, abort_flag);
+            } else if (!LSE) {
+                // O += P(q) V(q): M=128, N=d in one instruction, K=64 keys in four steps
+                constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
+                const uint32_t tO = tmem + kTmemO + t * 128;
+                for (int q = 0; ok && q < nq; ++q) {
+                    const int j = q >> 1, h = q & 1;
+                    ok = mbar_wait(&bars[B_P_FULL + 2 * t + (q & 1)], (q >> 1) & 1, abort_flag) &&
+                         (h == 1 || mbar_wait(&bars[B_V_FULL + (j & 1)], (j >> 1) & 1, abort_flag));
                     if (!ok) break;
                     tc_fence_after();
-                    issue_qk(1, j + 1);
-                    mma_commit(&bars[B_K_EMPTY + kn]);
-                }
-            }
-            mma_commit(&bars[B_DRAIN]);
-            mbar_drain(&bars[B_DRAIN], 0);
-        }
-    } else if (warp >= kWarpRot0) {
-        // ------------------------------------------------------------ K rotation (warps 8-11)
-        const int rt = tid - kWarpRot0 * 32;
-        constexpr int CPR = D / 16;
-        constexpr int RGN = kTileKeys / (CPR * kPagesPerTile);
-        constexpr int RPT = kPage / RGN;
-        const int c = rt % CPR;
-        const int rg = rt / (CPR * kPagesPerTile);
-        // angle of this thread's first in-page offset (table row rg*RPT) and of one position step
-        const float2* cs_start = prm.rope + (rg * RPT) * (D / 2) + 8 * c;
-        float2 cs_step[8];
+                    const uint32_t aV = smem_u32(sVs(j & 1)) + h * 64 * 128;
+                    const uint32_t tP = tmem + t * 128 + (q & 1) * 64;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cs_step[i] = prm.rope[1 * (D / 2) + 8 * c + i];
-        // metadata of key rt of the next tile, fetched one tile ahead: logical position and
-        // whether the key takes part (cached: page present and token not recomputed; fresh: row
-        // present)
-        auto meta = [&](int j, int32_t& pos, bool& valid) {
-            pos = kNoPos;
-            valid = false;
-            if (j < n_ct) {
-                const int lp = (t0 + j) * kPagesPerTile + rt / kPage;
-                if (lp < n_pages) {
-                    pos = page_pos[lp] + (rt % kPage);
-                    const uint32_t ex = LSE ? 0u : (uint32_t)prm.excl[page_base + lp];
-                    valid = ((ex >> (rt % kPage)) & 1u) == 0u;
+                    for (int kk = 0; kk < 64 / 16; ++kk)
+                        mma_bf16_ts(tO, tP + kk * 8, desc_sw128_mn(aV + kk * 2048, 16384), idesc_pv,
+                                    (q > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bars[B_PV_DONE + 2 * t + (q & 1)]);
+                    if (q == nq - 1) mma_commit(&bars[B_O_DONE + t]);
+                    if (h == 1) mma_commit(&bars[B_V_EMPTY + (j & 1)]);
                 }
-            } else if (j < n_tiles) {
-                const int fr = (j - n_ct) * kTileKeys + rt;
-                if (fr < n_rows_req) { pos = prm.row_pos[row_base + fr]; valid = true; }
             }
-        };
-        int32_t pos_n;
-        bool val_n;
-        meta(jb, pos_n, val_n);
-        for (int jj = 0; jj < n_loc; ++jj) {
-            const int j = jb + jj, ks = jj & 1;
-            const int32_t pos = pos_n;
-            const bool val = val_n;
-            meta(j + 1, pos_n, val_n);
-            bool ok = mbar_wait(&bars[B_K_FULL + ks], (jj >> 1) & 1, abort_flag);
-            ok = ok && (jj < kKStages || mbar_wait(&bars[B_KPOS_FREE + ks], ((jj >> 1) - 1) & 1, abort_flag));
-            if (!__all_sync(0xffffffffu, ok)) break;
-            if (j < n_ct) rotate_cached_tile<D>(sKs(ks), sCs(ks), rt, cs_start, cs_step);
-            sKpos(ks)[rt] = pos;
-            *reinterpret_cast<__half*>(sKaug(ks) + slab16_off(rt, 0)) = __float2half(val ? 0.f : kKeyOff);
-            fence_proxy_async_smem();
-            mbar_arrive(&bars[B_KROT_FULL + ks]);
+            const int di = (qk_role ? 0 : 2) + t;
+            mma_commit(&bars[B_DRAIN + di]);
+            mbar_drain(&bars[B_DRAIN + di], 0);
         }
     } else {
         // ------------------------------------------------------------ softmax (warps 0-7)
@@ -550,7 +424,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (LSE) mypos = valid ? kNoPos - 1 : -1;
         else mypos = valid ? prm.row_pos[row_base + row] : -1;
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_addr + t * 128;          // S (and P) columns of this tile
         const uint32_t tO = tmem + lane_addr + kTmemO + t * 128;
         // output locations, fixed before the tile loop so that only one pointer stays live across it
         // (a split key range writes a normalized partial row plus its max and sum instead)
@@ -571,96 +444,89 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_loc; ++j) {    // j: local tile index
-            const int ks = j & 1;
-            ok = mbar_wait(&bars[B_S_FULL + t], j & 1, abort_flag);
-            ok = ok && mbar_wait(&bars[B_KROT_FULL + ks], (j >> 1) & 1, abort_flag);
+        int cut = 0;
+        const int nq = 2 * n_loc;
+        for (int q = 0; q < nq; ++q) {    // halves of the local key tiles
+            const int j = q >> 1, h = q & 1, ks = j & 1;
+            const uint32_t tS = tmem + lane_addr + t * 128 + (q & 1) * 64;
+            ok = mbar_wait(&bars[B_S_FULL + 2 * t + (q & 1)], (q >> 1) & 1, abort_flag);
+            if (h == 0) ok = ok && mbar_wait(&bars[B_K_FULL + ks], (j >> 1) & 1, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            // causal limit of this row inside the tile: keys are in increasing position order, so
-            // the visible ones are a prefix (binary search); excluded keys are already at -30000
-            int cut;
-            {
+            if (h == 0) {
+                // causal limit of this row inside the tile: keys are in increasing position order,
+                // so the visible ones are a prefix (binary search); excluded keys are at -30000
                 const int32_t* kp = sKpos(ks);
-                int lo = 0;
-#pragma unroll
-                for (int step = 64; step >= 1; step >>= 1)
-                    if (kp[lo + step - 1] <= mypos) lo += step;
-                if (kp[lo] <= mypos) ++lo;   // lo <= 127 here; 128 when every key qualifies
-                cut = lo;
-            }
-            mbar_arrive(&bars[B_KPOS_FREE + ks]);
-            const bool full = __all_sync(0xffffffffu, cut == kTileKeys);   // no row of the warp is cut
-            // pass 1: row max
-            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t sv[32];
-                tmem_ld32(tS + cc * 32, sv);
-                tmem_ld_wait();
-                if (full) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        mx4[0] = max3f(mx4[0], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-                        mx4[1] = max3f(mx4[1], __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
-                        mx4[2] = max3f(mx4[2], __uint_as_float(sv[e + 4]), __uint_as_float(sv[e + 5]));
-                        mx4[3] = max3f(mx4[3], __uint_as_float(sv[e + 6]), __uint_as_float(sv[e + 7]));
-                    }
+                if (kp[kTileKeys - 1] <= mypos) {
+                    cut = kTileKeys;         // the whole tile is visible (the common case)
                 } else {
-                    const int k = cut - 32 * cc;
+                    int lo = 0;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float x = e < k ? __uint_as_float(sv[e]) : -INFINITY;
-                        mx4[e & 3] = fmaxf(mx4[e & 3], x);
-                    }
+                    for (int step = 64; step >= 1; step >>= 1)
+                        if (kp[lo + step - 1] <= mypos) lo += step;
+                    cut = lo;                // <= 127: key 127 is not visible
                 }
+                mbar_arrive(&bars[B_KPOS_FREE + ks]);
             }
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            const int cut_h = cut - 64 * h;   // visible keys of this half: [0, cut_h)
+            const bool full = __all_sync(0xffffffffu, cut_h >= 64);
+            // the half's 64 scores in registers (one wait for both loads)
+            uint32_t sv[64];
+            tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+            tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+            tmem_ld_wait();
+            float mx;
+            if (full) {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int e = 0; e < 64; e += 8) {
+                    m4[0] = max3f(m4[0], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+                    m4[1] = max3f(m4[1], __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
+                    m4[2] = max3f(m4[2], __uint_as_float(sv[e + 4]), __uint_as_float(sv[e + 5]));
+                    m4[3] = max3f(m4[3], __uint_as_float(sv[e + 6]), __uint_as_float(sv[e + 7]));
+                }
+                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            } else {
+                // keys at or beyond the causal limit leave the row: score -inf
+#pragma unroll
+                for (int e = 0; e < 64; ++e)
+                    if (e >= cut_h) sv[e] = __float_as_uint(-INFINITY);
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int e = 0; e < 64; e += 8) {
+                    m4[0] = max3f(m4[0], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+                    m4[1] = max3f(m4[1], __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
+                    m4[2] = max3f(m4[2], __uint_as_float(sv[e + 4]), __uint_as_float(sv[e + 5]));
+                    m4[3] = max3f(m4[3], __uint_as_float(sv[e + 6]), __uint_as_float(sv[e + 7]));
+                }
+                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            }
             const float m_new = fmaxf(m_run, mx);
             const bool need = m_new > m_run + 8.0f;     // lazy rescale: keep P <= 2^8
             const float alpha = need ? ex2(m_run - m_new) : 1.0f;
             if (need) { l_run *= alpha; m_run = m_new; }
             const float msub = m_run == -INFINITY ? 0.f : m_run;
-            if (!LSE && j > 0) {
-                // PV(j-1) of this tile must be done before O is rescaled
-                ok = mbar_wait(&bars[B_PV_DONE + t], (j - 1) & 1, abort_flag);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                tc_fence_after();
-            }
-            // pass 2: p = 2^(s - m) for visible keys; P (bf16 pairs) overwrites the S columns
-            // already read (columns [16cc, 16cc+16) after S columns [32cc, 32cc+32) are loaded)
+            // p = 2^(s - m); P (bf16 pairs) goes over the half's first 32 S columns
             float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t sv[32], pk[16];
-                tmem_ld32(tS + cc * 32, sv);
-                tmem_ld_wait();
-                if (full) {
+            uint32_t pk[32];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float p0 = ex2(__uint_as_float(sv[2 * e]) - msub);
-                        const float p1 = ex2(__uint_as_float(sv[2 * e + 1]) - msub);
-                        sum4[e & 3] += p0 + p1;
-                        pk[e] = pack_bf16x2(p0, p1);
-                    }
-                } else {
-                    const int k = cut - 32 * cc;
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float p0 = 2 * e < k ? ex2(__uint_as_float(sv[2 * e]) - msub) : 0.f;
-                        const float p1 = 2 * e + 1 < k ? ex2(__uint_as_float(sv[2 * e + 1]) - msub) : 0.f;
-                        sum4[e & 3] += p0 + p1;
-                        pk[e] = pack_bf16x2(p0, p1);
-                    }
-                }
-                if (!LSE) tmem_st16(tS + cc * 16, pk);
+            for (int e = 0; e < 32; ++e) {
+                const float p0 = ex2(__uint_as_float(sv[2 * e]) - msub);
+                const float p1 = ex2(__uint_as_float(sv[2 * e + 1]) - msub);
+                sum4[e & 3] += p0 + p1;
+                pk[e] = pack_bf16x2(p0, p1);
             }
+            if (!LSE) tmem_st32(tS, pk);
             l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
             if (LSE) {
                 tc_fence_before();
-                mbar_arrive(&bars[B_S_FREE + t]);
+                mbar_arrive(&bars[B_P_FULL + 2 * t + (q & 1)]);
             } else {
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                if (q > 0 && __any_sync(0xffffffffu, need)) {
+                    // every earlier P V of this tile must be done before O is rescaled
+                    ok = mbar_wait(&bars[B_PV_DONE + 2 * t + ((q - 1) & 1)], ((q - 1) >> 1) & 1, abort_flag);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll 1
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t o[32];
@@ -673,12 +539,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&bars[B_P_FULL + t]);
+                mbar_arrive(&bars[B_P_FULL + 2 * t + (q & 1)]);
             }
         }
         if (ml_slot != nullptr && ok) *ml_slot = make_float2(n_loc > 0 ? m_run : -INFINITY, l_run);
         if (!LSE && ok && n_loc > 0) {
-            ok = mbar_wait(&bars[B_PV_DONE + t], (n_loc - 1) & 1, abort_flag);
+            ok = mbar_wait(&bars[B_O_DONE + t], 0, abort_flag);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;

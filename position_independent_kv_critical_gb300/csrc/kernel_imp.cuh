@@ -5,10 +5,11 @@
 // carry log2(e)/sqrt(d)) and lse2 the log2-sum-exp of row (h,t) over all cached keys of the request
 // (from the first pass).  The tile is computed
 // transposed, S^T = K_rot Q^T with M = 128 keys (TMEM lanes) and N = 256 query rows (columns), so
-// that each thread owns one key and sums its own TMEM row -- no cross-thread reduction.  The K
-// tile is rotated in shared memory at its logical positions (MiniPIC 2.1), the query rows arrive
-// pre-rotated.  One CTA per (request, key tile, kv head); the per-kv-head partial sums are
-// reduced in fixed head order by the last CTA of each key tile (deterministic).
+// that each thread owns one key and sums its own TMEM row -- no cross-thread reduction.  Both
+// operands arrive rotated: the query rows, and the key tile from the call's rotated copy of the
+// batch's cached keys (MiniPIC 2.1: rotation to the request's logical positions at use time).
+// One CTA per (request, key tile, kv head); the per-kv-head partial sums are reduced in fixed
+// head order by the last CTA of each key tile (deterministic).
 #pragma once
 #include "kernel_attn.cuh"
 
@@ -21,7 +22,6 @@ constexpr int kImpQRows = 256;
 
 struct ImpParams {
     const int32_t* layout;
-    const float2* rope;
     const float2* lse_part;
     float* part;             // [Hkv][total_tokens]
     int32_t* counters;       // [total key tiles], zero on entry, left zero on exit
@@ -33,11 +33,9 @@ struct ImpSmem {
     static constexpr int kHalves = D / 64;
     static constexpr int kK = kTileKeys * D * 2;
     static constexpr int kQ = kImpQRows * D * 2;
-    static constexpr int kCs = kPagesPerTile * (D / 2) * 8;
     static constexpr int oK = 0;
     static constexpr int oQ = oK + kK;
-    static constexpr int oCs = oQ + 2 * kQ;
-    static constexpr int oLse = oCs + kCs;
+    static constexpr int oLse = oQ + 2 * kQ;
     static constexpr int oBar = oLse + 2 * kImpQRows * 4;
     static constexpr int kNumBars = 12;
     static constexpr int oMisc = oBar + kNumBars * 8;
@@ -46,14 +44,14 @@ struct ImpSmem {
     static constexpr uint32_t kTmemCols = 512;
 };
 
-enum : int { I_K_FULL = 0, I_KROT = 1, I_Q_FULL = 2 /*2*/, I_Q_EMPTY = 4 /*2*/, I_ACC_FULL = 6 /*2*/,
+enum : int { I_K_FULL = 0, I_Q_FULL = 2 /*2*/, I_Q_EMPTY = 4 /*2*/, I_ACC_FULL = 6 /*2*/,
              I_ACC_FREE = 8 /*2*/, I_DRAIN = 10 };
 
 __device__ __forceinline__ void named_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 template <int D>
 __global__ void __launch_bounds__(kImpThreads, 1)
-imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kpool,
+imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kcache,
            const ImpParams prm) {
     using SM = ImpSmem<D>;
     constexpr int H = SM::kHalves;
@@ -61,7 +59,6 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sK = smem + SM::oK;
     auto sQs = [&](int b) { return smem + SM::oQ + b * SM::kQ; };
-    float2* sCs = reinterpret_cast<float2*>(smem + SM::oCs);
     auto sLse = [&](int b) { return reinterpret_cast<float*>(smem + SM::oLse) + b * kImpQRows; };
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::oBar);
     int32_t* misc = reinterpret_cast<int32_t*>(smem + SM::oMisc);
@@ -74,15 +71,11 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int32_t* R = L + L[L_OFF_REQ] + req * R_STRIDE;
     const int Hkv = L[L_HKV], g = L[L_GROUP];
     const int n_pages = R[R_N_PAGES];
-    const int32_t page_base = R[R_PAGE_BASE];
-    const int32_t* page_pos = L + L[L_OFF_PAGEPOS] + page_base;
-    const int32_t* blk = L + L[L_OFF_BLOCK] + page_base;
     const int n_q = R[R_N_QUERY] * g;
     const int n_qc = (n_q + kImpQRows - 1) / kImpQRows;
 
     if (tid == 0) {
         mbar_init(&bars[I_K_FULL], 1);
-        mbar_init(&bars[I_KROT], 128);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[I_Q_FULL + s], 1);
             mbar_init(&bars[I_Q_EMPTY + s], 1);
@@ -103,24 +96,15 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint32_t tmem = static_cast<uint32_t>(misc[0]);
 
     if (warp == kImpWarpTma) {
-        const int lp0 = t * kPagesPerTile;
-        const int np = min(kPagesPerTile, n_pages - lp0);
         if (lane == 0) {
             prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_kpool);
-            mbar_arrive_expect_tx(&bars[I_K_FULL], np * (H * 2048 + (D / 2) * 8));
-        }
-        __syncwarp();
-        if (lane < np) {   // lane p issues page p
-            int32_t phys = blk[lp0 + lane];
-            const int32_t pp = page_pos[lp0 + lane];
-            if (phys < 0 || phys >= L[L_N_PHYS]) { set_dev_error(kDevErrBounds); phys = 0; }
-            const int32_t y = (phys * Hkv + kvh) * kPage;
+            prefetch_tmap(&tm_kcache);
+            // rotated key tile t of the request (rows past the request's keys are never summed)
+            mbar_arrive_expect_tx(&bars[I_K_FULL], H * 16384);
+            const int32_t ky = kvh * L[L_TOTAL_TOKENS] + R[R_TOK_BASE] + t * kTileKeys;
             for (int hb = 0; hb < H; ++hb)
-                tma_load_2d(sK + hb * 16384 + lane * 2048, &tm_kpool, &bars[I_K_FULL], hb * 64, y);
-            bulk_load(sCs + lane * (D / 2), prm.rope + (int64_t)pp * (D / 2), (D / 2) * 8, &bars[I_K_FULL]);
-        }
-        if (lane == 0) {
+                tma_load_2d(sK + hb * 16384, &tm_kcache, &bars[I_K_FULL], hb * 64, ky);
+
             const int32_t qy0 = (kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE]) * g;
             int last[2] = {-1, -1};
             for (int qc = 0; qc < n_qc; ++qc) {
@@ -140,7 +124,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(128, kImpQRows);
             const uint32_t aK = smem_u32(sK);
-            bool ok = mbar_wait(&bars[I_KROT], 0, abort_flag);
+            bool ok = mbar_wait(&bars[I_K_FULL], 0, abort_flag);
             for (int qc = 0; ok && qc < n_qc; ++qc) {
                 const int b = qc & 1;
                 if (!mbar_wait(&bars[I_Q_FULL + b], (qc >> 1) & 1, abort_flag)) break;
@@ -160,20 +144,8 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             mbar_drain(&bars[I_DRAIN], 0);
         }
     } else {
-        // warps 0-3: rotate the key tile, then sum exp over the query rows for one key per thread
-        constexpr int CPR = D / 16;
-        constexpr int RGN = kTileKeys / (CPR * kPagesPerTile);
-        constexpr int RPT = kPage / RGN;
-        const int c = tid % CPR;
-        const int rg = tid / (CPR * kPagesPerTile);
-        const float2* cs_start = prm.rope + (rg * RPT) * (D / 2) + 8 * c;
-        float2 cs_step[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) cs_step[i] = prm.rope[1 * (D / 2) + 8 * c + i];
-        bool ok = mbar_wait(&bars[I_K_FULL], 0, abort_flag);
-        if (ok) rotate_cached_tile<D>(sK, sCs, tid, cs_start, cs_step);
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[I_KROT]);
+        // warps 0-3: sum exp over the query rows for one key per thread
+        bool ok = true;
         const int chunks = R[R_LSE_CHUNKS];
         const float2* part_in = prm.lse_part + R[R_LSE_BASE] + (int64_t)kvh * n_q * chunks;
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;

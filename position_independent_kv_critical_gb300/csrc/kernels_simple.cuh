@@ -7,35 +7,54 @@
 namespace pcf {
 
 // ------------------------------------------------------------------ rope_rows
-// Rotates rows x[n_rows][H][D] (unrotated, bf16) at per-row positions and writes them in fp16
-// (the operand type of the Q K^T contractions), grouped by kv head for TMA:
+// Rotates rows (unrotated, bf16) at their logical positions and writes them in fp16 (the operand
+// type of the Q K^T contractions), grouped by kv head for TMA:
 // out[((h / gg) * n_rows + row) * gg + h % gg][D].  Used for the query rows (gg = Hq/Hkv, scaled
-// by log2(e)/sqrt(d) so that Q K^T comes out in log2 units) and the fresh keys (gg = 1) -- per-request data, rotated once; cached keys are never written rotated
-// (MiniPIC 2.1: the shared blocks stay position-free).
+// by log2(e)/sqrt(d) so that Q K^T comes out in log2 units), the fresh keys (gg = 1) and, in page
+// gather mode, the cached keys of every request: row r is the r-th cached token of the batch,
+// read from the shared page blk[r / 16] at in-page offset r % 16 and rotated to the request's
+// position page_pos[r / 16] + r % 16.  The pool itself is never written (MiniPIC 2.1: the shared
+// blocks stay position-free); the rotated copy is per call, in the caller's workspace.
 struct RopeJob {
-    const __nv_bfloat16* x;
-    const int32_t* pos;      // [n_rows] logical position of every row
+    const __nv_bfloat16* x;  // rows [n_rows][heads][D], or the pool [n_phys][heads][16][D]
+    const int32_t* pos;      // [n_rows] logical position of every row (row mode)
     __half* out;
     int32_t n_rows, heads, gg;
     float scale;             // folded into the output: log2(e)/sqrt(d) for queries, 1 for keys
+    const int32_t* blk;      // page gather mode: physical page of every logical page (else null)
+    const int32_t* page_pos; //   and the logical position of its first token
+    int32_t n_phys;          //   pages in the pool
 };
 
 template <int D>
-__global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob a, RopeJob b, const float2* __restrict__ rope,
-                                                        int32_t max_pos, int64_t n_a) {
+__global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob a, RopeJob b, RopeJob c3,
+                                                        const float2* __restrict__ rope, int32_t max_pos,
+                                                        int64_t n_a, int64_t n_ab) {
     constexpr int CPR = D / 16;   // 16-byte chunk pairs per head row
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const RopeJob& J = gid < n_a ? a : b;
-    const int64_t lid = gid < n_a ? gid : gid - n_a;
+    RopeJob J;   // a copy in registers (a reference into the parameters would go through the stack)
+    if (gid < n_a) J = a;
+    else if (gid < n_ab) J = b;
+    else J = c3;
+    const int64_t lid = gid < n_a ? gid : (gid < n_ab ? gid - n_a : gid - n_ab);
     const int64_t total = (int64_t)J.n_rows * J.heads * CPR;
     if (J.x == nullptr || lid >= total) return;
     const int c = (int)(lid % CPR);
     const int64_t rh = lid / CPR;
     const int h = (int)(rh % J.heads);
     const int32_t row = (int32_t)(rh / J.heads);
-    const int32_t p = J.pos[row];
+    int32_t p;
+    const __nv_bfloat16* src;
+    if (J.blk != nullptr) {
+        const int32_t ph = J.blk[row / kPage];
+        if (ph < 0 || ph >= J.n_phys) { set_dev_error(kDevErrBounds); return; }
+        p = J.page_pos[row / kPage] + row % kPage;
+        src = J.x + (((int64_t)ph * J.heads + h) * kPage + row % kPage) * D;
+    } else {
+        p = J.pos[row];
+        src = J.x + ((int64_t)row * J.heads + h) * D;
+    }
     if (p < 0 || p >= max_pos) { set_dev_error(kDevErrBounds); return; }
-    const __nv_bfloat16* src = J.x + ((int64_t)row * J.heads + h) * D;
     const uint4 xa = *reinterpret_cast<const uint4*>(src + 8 * c);
     const uint4 xb = *reinterpret_cast<const uint4*>(src + D / 2 + 8 * c);
     const float4* cs4 = reinterpret_cast<const float4*>(rope + (int64_t)p * (D / 2) + 8 * c);

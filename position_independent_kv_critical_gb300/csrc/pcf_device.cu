@@ -91,13 +91,17 @@ pcf_status launched() { return cudaGetLastError() == cudaSuccess ? PCF_OK : PCF_
 
 size_t align_up(size_t x) { return (x + 1023) & ~size_t(1023); }
 
+// rotated copy of every cached key of the batch: [Hkv][total_tokens][D] fp16
+size_t kc_bytes(const int32_t* H) { return (size_t)H[L_HKV] * H[L_TOTAL_TOKENS] * H[L_D] * 2; }
+
 struct ScoreWs {
-    size_t q, lse, part, cnt, total;
+    size_t q, kc, lse, part, cnt, total;
 };
 ScoreWs score_ws(const int32_t* H) {
     ScoreWs w;
     w.q = 0;
-    w.lse = align_up(w.q + (size_t)H[L_TOTAL_QUERY] * H[L_HQ] * H[L_D] * 2);
+    w.kc = align_up(w.q + (size_t)H[L_TOTAL_QUERY] * H[L_HQ] * H[L_D] * 2);
+    w.lse = align_up(w.kc + kc_bytes(H));
     w.part = align_up(w.lse + (size_t)H[L_LSE_SLOTS] * sizeof(float2));
     w.cnt = align_up(w.part + (size_t)H[L_HKV] * H[L_TOTAL_TOKENS] * sizeof(float));
     w.total = align_up(w.cnt + (size_t)H[L_TOTAL_KTILES] * sizeof(int32_t));
@@ -105,13 +109,14 @@ ScoreWs score_ws(const int32_t* H) {
 }
 
 struct AttnWs {
-    size_t q, k, po, pml, total;
+    size_t q, k, kc, po, pml, total;
 };
 AttnWs attn_ws(const int32_t* H) {
     AttnWs w;
     w.q = 0;
     w.k = align_up((size_t)H[L_TOTAL_ROWS] * H[L_HQ] * H[L_D] * 2);
-    w.po = align_up(w.k + (size_t)H[L_TOTAL_ROWS] * H[L_HKV] * H[L_D] * 2);
+    w.kc = align_up(w.k + (size_t)H[L_TOTAL_ROWS] * H[L_HKV] * H[L_D] * 2);
+    w.po = align_up(w.kc + kc_bytes(H));
     const size_t prow = (size_t)H[L_ATTN_SLOTS] * kQTilesPerCta * kTileRows;   // partial rows
     w.pml = align_up(w.po + prow * H[L_D] * 2);
     w.total = align_up(w.pml + prow * sizeof(float2));
@@ -126,13 +131,21 @@ pcf_status set_smem(K kernel, int bytes) {
 }
 
 template <int D>
-pcf_status launch_rope(RopeJob a, RopeJob b, const float2* rope, int32_t max_pos, cudaStream_t st) {
+pcf_status launch_rope(RopeJob a, RopeJob b, RopeJob c, const float2* rope, int32_t max_pos, cudaStream_t st) {
     const int64_t n_a = a.x ? (int64_t)a.n_rows * a.heads * (D / 16) : 0;
     const int64_t n_b = b.x ? (int64_t)b.n_rows * b.heads * (D / 16) : 0;
-    if (n_a + n_b == 0) return PCF_OK;
-    const int64_t blocks = (n_a + n_b + 255) / 256;
-    rope_rows_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(a, b, rope, max_pos, n_a);
+    const int64_t n_c = c.x ? (int64_t)c.n_rows * c.heads * (D / 16) : 0;
+    if (n_a + n_b + n_c == 0) return PCF_OK;
+    const int64_t blocks = (n_a + n_b + n_c + 255) / 256;
+    rope_rows_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(a, b, c, rope, max_pos, n_a, n_a + n_b);
     return launched();
+}
+
+// the batch's cached keys, gathered from their pages and rotated to each request's positions
+RopeJob cached_key_job(const pcf_layout* lay, const uint16_t* k_pool, __half* kc) {
+    const int32_t* H = lay->host;
+    return RopeJob{reinterpret_cast<const __nv_bfloat16*>(k_pool), nullptr, kc, H[L_TOTAL_TOKENS], H[L_HKV], 1, 1.f,
+                   lay->dev + H[L_OFF_BLOCK], lay->dev + H[L_OFF_PAGEPOS], H[L_N_PHYS]};
 }
 
 template <int D>
@@ -142,6 +155,7 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
     const ScoreWs w = score_ws(H);
     uint8_t* base = static_cast<uint8_t*>(ws);
     __half* q_rot = reinterpret_cast<__half*>(base + w.q);
+    __half* kc = reinterpret_cast<__half*>(base + w.kc);
     float2* lse = reinterpret_cast<float2*>(base + w.lse);
     float* part = reinterpret_cast<float*>(base + w.part);
     int32_t* cnt = reinterpret_cast<int32_t*>(base + w.cnt);
@@ -153,33 +167,33 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
         cudaMemsetAsync(cnt, 0, (size_t)H[L_TOTAL_KTILES] * sizeof(int32_t), st) != cudaSuccess)
         return PCF_ERR_CUDA;
     RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_query), lay->dev + H[L_OFF_QPOS], q_rot, H[L_TOTAL_QUERY],
-               H[L_HQ], g, scale_log2};
-    RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f};
-    pcf_status s = launch_rope<D>(qj, none, rope2, H[L_MAX_POS], st);
+               H[L_HQ], g, scale_log2, nullptr, nullptr, 0};
+    RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f, nullptr, nullptr, 0};
+    pcf_status s = launch_rope<D>(qj, cached_key_job(lay, k_pool, kc), none, rope2, H[L_MAX_POS], st);
     if (s != PCF_OK) return s;
 
-    CUtensorMap tq128, tq256, tk, zero;
+    CUtensorMap tq128, tq256, tkc, zero;
     std::memset(&zero, 0, sizeof(zero));
     const uint64_t qrows = (uint64_t)H[L_HKV] * H[L_TOTAL_QUERY] * g;
     if ((s = make_map_2d(&tq128, q_rot, D, qrows, D * 2, 128, kF16)) != PCF_OK) return s;
     if ((s = make_map_2d(&tq256, q_rot, D, qrows, D * 2, 256, kF16)) != PCF_OK) return s;
-    if ((s = make_map_2d(&tk, k_pool, D, (uint64_t)H[L_N_PHYS] * H[L_HKV] * kPage, D * 2, kPage)) != PCF_OK)
+    if ((s = make_map_2d(&tkc, kc, D, (uint64_t)H[L_HKV] * H[L_TOTAL_TOKENS], D * 2, 128, kF16)) != PCF_OK)
         return s;
 
     if (H[L_N_LSE_ITEMS] > 0) {
         using SM = AttnSmem<D, true>;
         auto kern = attn_kernel<D, true>;
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
-        AttnParams p{lay->dev, nullptr, nullptr, rope2, nullptr, lse, nullptr, nullptr};
-        kern<<<H[L_N_LSE_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq128, tk, zero, zero, zero, p);
+        AttnParams p{lay->dev, nullptr, nullptr, nullptr, lse, nullptr, nullptr};
+        kern<<<H[L_N_LSE_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq128, tkc, zero, zero, zero, p);
         if ((s = launched()) != PCF_OK) return s;
     }
     if (H[L_N_IMP_ITEMS] > 0) {
         using SM = ImpSmem<D>;
         auto kern = imp_kernel<D>;
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
-        ImpParams p{lay->dev, rope2, lse, part, cnt, importance};
-        kern<<<H[L_N_IMP_ITEMS], kImpThreads, SM::kAlloc, st>>>(tq256, tk, p);
+        ImpParams p{lay->dev, lse, part, cnt, importance};
+        kern<<<H[L_N_IMP_ITEMS], kImpThreads, SM::kAlloc, st>>>(tq256, tkc, p);
         if ((s = launched()) != PCF_OK) return s;
     }
     return PCF_OK;
@@ -196,19 +210,25 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     uint8_t* base = static_cast<uint8_t*>(ws);
     __half* q_rot = reinterpret_cast<__half*>(base + w.q);
     __half* k_rot = reinterpret_cast<__half*>(base + w.k);
+    __half* kc = reinterpret_cast<__half*>(base + w.kc);
     const int g = H[L_GROUP];
     const float2* rope2 = reinterpret_cast<const float2*>(rope);
     const int32_t rows = H[L_TOTAL_ROWS];
     const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-    RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_fresh), row_pos, q_rot, rows, H[L_HQ], g, scale_log2};
-    RopeJob kj{reinterpret_cast<const __nv_bfloat16*>(k_fresh), row_pos, k_rot, rows, H[L_HKV], 1, 1.f};
-    pcf_status s = launch_rope<D>(qj, kj, rope2, H[L_MAX_POS], st);
+    RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_fresh), row_pos, q_rot, rows, H[L_HQ], g, scale_log2,
+               nullptr, nullptr, 0};
+    RopeJob kj{reinterpret_cast<const __nv_bfloat16*>(k_fresh), row_pos, k_rot, rows, H[L_HKV], 1, 1.f,
+               nullptr, nullptr, 0};
+    pcf_status s = launch_rope<D>(qj, kj, cached_key_job(lay, k_pool, kc), rope2, H[L_MAX_POS], st);
     if (s != PCF_OK) return s;
 
-    CUtensorMap tq, tkp, tvp, tkf, tvf;
+    CUtensorMap tq, tkc, tvp, tkf, tvf;
     const uint64_t pool_rows = (uint64_t)H[L_N_PHYS] * H[L_HKV] * kPage;
     if ((s = make_map_2d(&tq, q_rot, D, (uint64_t)H[L_HKV] * rows * g, D * 2, 128, kF16)) != PCF_OK) return s;
-    if ((s = make_map_2d(&tkp, k_pool, D, pool_rows, D * 2, kPage)) != PCF_OK) return s;
+    // a batch without cached tokens never reads this map: point it at the fresh keys
+    if (H[L_TOTAL_TOKENS] > 0) s = make_map_2d(&tkc, kc, D, (uint64_t)H[L_HKV] * H[L_TOTAL_TOKENS], D * 2, 128, kF16);
+    else s = make_map_2d(&tkc, k_rot, D, (uint64_t)H[L_HKV] * rows, D * 2, 128, kF16);
+    if (s != PCF_OK) return s;
     if ((s = make_map_2d(&tvp, v_pool, D, pool_rows, D * 2, kPage)) != PCF_OK) return s;
     if ((s = make_map_2d(&tkf, k_rot, D, (uint64_t)H[L_HKV] * rows, D * 2, 128, kF16)) != PCF_OK) return s;
     if ((s = make_map_3d(&tvf, v_fresh, D, H[L_HKV], rows, 128)) != PCF_OK) return s;
@@ -218,8 +238,8 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
     __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(base + w.po);
     float2* part_ml = reinterpret_cast<float2*>(base + w.pml);
-    AttnParams p{lay->dev, excl, row_pos, rope2, reinterpret_cast<__nv_bfloat16*>(out), nullptr, part_o, part_ml};
-    kern<<<H[L_N_ATTN_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq, tkp, tvp, tkf, tvf, p);
+    AttnParams p{lay->dev, excl, row_pos, reinterpret_cast<__nv_bfloat16*>(out), nullptr, part_o, part_ml};
+    kern<<<H[L_N_ATTN_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq, tkc, tvp, tkf, tvf, p);
     if ((s = launched()) != PCF_OK) return s;
     if (H[L_N_COMB] > 0) {
         combine_kernel<D><<<dim3(H[L_N_COMB], D / 8), 256, 0, st>>>(lay->dev, part_o, part_ml,

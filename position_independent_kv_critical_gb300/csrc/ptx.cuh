@@ -205,10 +205,11 @@ __device__ __forceinline__ uint64_t desc_sw128_kmajor(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// Same swizzle, MN-major operand exactly one 64-element (128-byte) atom wide: consecutive 8-row
-// K groups are 1024 bytes apart; both byte offsets carry that stride.
-__device__ __forceinline__ uint64_t desc_sw128_mn64(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(1024 >> 4) << 16) |
+// Same swizzle, MN-major operand: 64-element (128-byte) wide atoms of 8 K rows; consecutive 8-row
+// K groups are 1024 bytes apart (stride byte offset) and consecutive 64-wide atoms along N are
+// `atom_stride` bytes apart (leading byte offset).
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t atom_stride) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(atom_stride >> 4) << 16) |
            ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 // UMMA shared-memory descriptor, no swizzle, K-major: 8-row x 16-byte core matrices; `k_stride`
