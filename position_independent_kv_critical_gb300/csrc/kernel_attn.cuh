@@ -64,6 +64,8 @@ struct AttnParams {
     const int32_t* row_pos;    // attention: logical position of every row
     __nv_bfloat16* out;        // attention: [rows][Hq][D]
     float2* lse_part;          // LSE: (running max in log2 units, running sum) per row and chunk
+    float* lse_final;          // LSE: log2-sum-exp per row, [Hkv][total query][g]
+    int32_t* lse_count;        // LSE: finished chunks per (request, kv head, pair); zero on entry and exit
     __nv_bfloat16* part_o;     // attention with a split key range: normalized partial O per slot
     float2* part_ml;           //   and its (running max, running sum) per row
 };
@@ -131,6 +133,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int req = item[0], kvh = item[1], qpair = item[2], chunk = item[3];   // chunk: LSE key chunk
                                                                                   // or attention split
     const int32_t* R = L + L[L_OFF_REQ] + req * R_STRIDE;
+    const int32_t* PR = L + L[L_OFF_PAIR] + (R[R_PAIR_BASE] + qpair) * P_STRIDE;   // attention only
     const int Hq = L[L_HQ], Hkv = L[L_HKV], g = L[L_GROUP];
     const int toks_per_tile = kTileRows / g;
     const int n_rows_req = LSE ? R[R_N_QUERY] : R[R_N_ROWS];
@@ -183,7 +186,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         misc[3] = t0;
         misc[4] = 0;
         const int n_all = nct + nft;
-        const int ns = LSE ? 1 : R[R_NSPLIT];
+        const int ns = LSE ? 1 : PR[P_NSPLIT];
         const int sp = LSE ? 0 : chunk;
         misc[5] = (int)(((int64_t)sp * n_all) / ns);
         misc[6] = (int)(((int64_t)(sp + 1) * n_all) / ns);
@@ -433,10 +436,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (LSE) {
                 ml_slot = prm.lse_part + R[R_LSE_BASE] +
                           ((int64_t)kvh * (R[R_N_QUERY] * g) + row * g + hl) * R[R_LSE_CHUNKS] + chunk;
-            } else if (R[R_NSPLIT] == 1) {
+            } else if (PR[P_NSPLIT] == 1) {
                 out_row = prm.out + ((int64_t)(row_base + row) * Hq + kvh * g + hl) * D;
             } else {
-                const int64_t prow = (int64_t)(R[R_SLOT_BASE] + (kvh * R[R_NPAIRS] + qpair) * R[R_NSPLIT] + chunk) *
+                const int64_t prow = (int64_t)(PR[P_SLOT_BASE] + kvh * PR[P_NSPLIT] + chunk) *
                                          (kQTilesPerCta * kTileRows) + t * kTileRows + m;
                 out_row = prm.part_o + prow * D;
                 ml_slot = prm.part_ml + prow;
@@ -543,6 +546,33 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
         }
         if (ml_slot != nullptr && ok) *ml_slot = make_float2(n_loc > 0 ? m_run : -INFINITY, l_run);
+        if (LSE) {
+            // The last key chunk of this (request, kv head, tile pair) to finish combines every row's
+            // chunks, in chunk order, into the row's log2-sum-exp over all cached keys.
+            const int chunks = R[R_LSE_CHUNKS];
+            const int cidx = R[R_LSE_PAIR_BASE] + kvh * ((R[R_N_QUERY] * g + 2 * kTileRows - 1) / (2 * kTileRows)) + qpair;
+            __threadfence();
+            asm volatile("bar.sync 1, 256;" ::: "memory");   // the 256 softmax threads
+            if (tid == 0) misc[7] = atomicAdd(prm.lse_count + cidx, 1) == chunks - 1 ? 1 : 0;
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (misc[7]) {
+                __threadfence();
+                if (valid) {
+                    const float2* ml = prm.lse_part + R[R_LSE_BASE] +
+                                       ((int64_t)kvh * (R[R_N_QUERY] * g) + row * g + hl) * chunks;
+                    float M = -INFINITY;
+                    for (int c = 0; c < chunks; ++c) M = fmaxf(M, __ldcg(&ml[c].x));
+                    float S = 0.f;
+                    for (int c = 0; c < chunks; ++c) {
+                        const float2 v = __ldcg(ml + c);
+                        S += v.y * ex2(v.x - M);
+                    }
+                    prm.lse_final[((int64_t)kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row) * g + hl] =
+                        S > 0.f ? M + log2f(S) : INFINITY;
+                }
+                if (tid == 0) prm.lse_count[cidx] = 0;
+            }
+        }
         if (!LSE && ok && n_loc > 0) {
             ok = mbar_wait(&bars[B_O_DONE + t], 0, abort_flag);
             if (__all_sync(0xffffffffu, ok)) {

@@ -3,13 +3,23 @@
 //
 // imp[j] = sum_h sum_t exp2(s_{h,t,j} - lse2_{h,t}) with s in log2 units (the rotated query rows
 // carry log2(e)/sqrt(d)) and lse2 the log2-sum-exp of row (h,t) over all cached keys of the request
-// (from the first pass).  The tile is computed
-// transposed, S^T = K_rot Q^T with M = 128 keys (TMEM lanes) and N = 256 query rows (columns), so
-// that each thread owns one key and sums its own TMEM row -- no cross-thread reduction.  Both
-// operands arrive rotated: the query rows, and the key tile from the call's rotated copy of the
-// batch's cached keys (MiniPIC 2.1: rotation to the request's logical positions at use time).
-// One CTA per (request, key tile, kv head); the per-kv-head partial sums are reduced in fixed
-// head order by the last CTA of each key tile (deterministic).
+// (written by the first pass).  Each tile is computed transposed, S^T = K_rot Q^T with M = 128
+// keys (TMEM lanes) and N = 256 query rows (columns), so that each thread owns one key and sums
+// its own TMEM row -- no cross-thread reduction.  The tensor core also subtracts the row's lse2: a
+// last K=16 step multiplies a column pair of ones (key side) with (-lse2 rounded to fp16, the
+// rounding remainder in fp16) on the query side, so S^T arrives as s - lse2 and each element costs
+// one exponential and one add.  Both operands arrive rotated: the query rows, and
+// the key tiles from the call's rotated copy of the batch's cached keys (MiniPIC 2.1: rotation to
+// the request's logical positions at use time).
+//
+// One CTA per (request, run of key tiles, kv head).  Key tiles and 256-row query chunks stream
+// through two-stage rings and the S^T accumulator is double-buffered in TMEM, so the tensor core
+// works on the next (tile, chunk) step while the exponentials of the current one run.  The
+// per-kv-head partial sums of a run are reduced in fixed head order by the last CTA of the run
+// (deterministic).
+//   warps 0-3  exp-sum (one key per thread)
+//   warp  4    TMEM allocation + single-thread tcgen05.mma issue
+//   warp  5    TMA producer (key tiles, query chunks)
 #pragma once
 #include "kernel_attn.cuh"
 
@@ -22,7 +32,7 @@ constexpr int kImpQRows = 256;
 
 struct ImpParams {
     const int32_t* layout;
-    const float2* lse_part;
+    const float* lse_final;  // [Hkv][total_query][g] log2-sum-exp of every query row
     float* part;             // [Hkv][total_tokens]
     int32_t* counters;       // [total key tiles], zero on entry, left zero on exit
     float* importance;       // [total_tokens]
@@ -33,19 +43,22 @@ struct ImpSmem {
     static constexpr int kHalves = D / 64;
     static constexpr int kK = kTileKeys * D * 2;
     static constexpr int kQ = kImpQRows * D * 2;
-    static constexpr int oK = 0;
-    static constexpr int oQ = oK + kK;
-    static constexpr int oLse = oQ + 2 * kQ;
-    static constexpr int oBar = oLse + 2 * kImpQRows * 4;
-    static constexpr int kNumBars = 12;
+    static constexpr int oK = 0;                       // 2 key-tile stages
+    static constexpr int oQ = oK + 2 * kK;             // 2 query-chunk buffers
+    static constexpr int kSlabQ = kImpQRows * 16 * 2;  // [256][16] fp16: -lse2 (hi, lo) per row
+    static constexpr int kSlabK = kTileKeys * 16 * 2;  // [128][16] fp16: ones in columns 0 and 1
+    static constexpr int oQlse = oQ + 2 * kQ;          // 2 slabs (one per query-chunk buffer)
+    static constexpr int oKones = oQlse + 2 * kSlabQ;
+    static constexpr int oBar = oKones + kSlabK;
+    static constexpr int kNumBars = 16;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int kBytes = oMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;
-    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kTmemCols = 512;         // 2 accumulators of 256 columns
 };
 
-enum : int { I_K_FULL = 0, I_Q_FULL = 2 /*2*/, I_Q_EMPTY = 4 /*2*/, I_ACC_FULL = 6 /*2*/,
-             I_ACC_FREE = 8 /*2*/, I_DRAIN = 10 };
+enum : int { I_K_FULL = 0 /*2*/, I_K_EMPTY = 2 /*2*/, I_Q_FULL = 4 /*2*/, I_Q_EMPTY = 6 /*2*/,
+             I_ACC_FULL = 8 /*2*/, I_ACC_FREE = 10 /*2*/, I_LSE_FULL = 12 /*2*/, I_DRAIN = 14 };
 
 __device__ __forceinline__ void named_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -57,9 +70,10 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     constexpr int H = SM::kHalves;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sK = smem + SM::oK;
+    auto sKs = [&](int b) { return smem + SM::oK + b * SM::kK; };
     auto sQs = [&](int b) { return smem + SM::oQ + b * SM::kQ; };
-    auto sLse = [&](int b) { return reinterpret_cast<float*>(smem + SM::oLse) + b * kImpQRows; };
+    auto sQlse = [&](int b) { return smem + SM::oQlse + b * SM::kSlabQ; };
+    uint8_t* sKones = smem + SM::oKones;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::oBar);
     int32_t* misc = reinterpret_cast<int32_t*>(smem + SM::oMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -67,20 +81,24 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t* L = prm.layout;
     const int32_t* item = L + L[L_OFF_IMP] + kItemWords * blockIdx.x;
-    const int req = item[0], t = item[1], kvh = item[2];
+    const int req = item[0], t0 = item[1], kvh = item[2], nt = item[3];
     const int32_t* R = L + L[L_OFF_REQ] + req * R_STRIDE;
     const int Hkv = L[L_HKV], g = L[L_GROUP];
     const int n_pages = R[R_N_PAGES];
     const int n_q = R[R_N_QUERY] * g;
     const int n_qc = (n_q + kImpQRows - 1) / kImpQRows;
+    const int n_steps = nt * n_qc;           // step s = (tile s / n_qc, query chunk s % n_qc)
+    const bool q_resident = n_qc == 1;       // a single chunk is loaded once
 
     if (tid == 0) {
-        mbar_init(&bars[I_K_FULL], 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars[I_Q_FULL + s], 1);
-            mbar_init(&bars[I_Q_EMPTY + s], 1);
-            mbar_init(&bars[I_ACC_FULL + s], 1);
-            mbar_init(&bars[I_ACC_FREE + s], 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars[I_K_FULL + b], 1);
+            mbar_init(&bars[I_K_EMPTY + b], 1);
+            mbar_init(&bars[I_Q_FULL + b], 1);
+            mbar_init(&bars[I_Q_EMPTY + b], 1);
+            mbar_init(&bars[I_ACC_FULL + b], 1);
+            mbar_init(&bars[I_ACC_FREE + b], 128);
+            mbar_init(&bars[I_LSE_FULL + b], 128);
         }
         mbar_init(&bars[I_DRAIN], 1);
         fence_mbar_init();
@@ -90,6 +108,15 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         tmem_alloc(reinterpret_cast<uint32_t*>(misc), SM::kTmemCols);
         tmem_relinquish();
     }
+    // the K=16 slabs start at zero; the key side gets its two columns of ones
+    for (int i = tid; i < (2 * SM::kSlabQ + SM::kSlabK) / 16; i += kImpThreads)
+        reinterpret_cast<uint4*>(sQlse(0))[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    if (tid < kTileKeys) {
+        *reinterpret_cast<__half*>(sKones + slab16_off(tid, 0)) = __float2half(1.0f);
+        *reinterpret_cast<__half*>(sKones + slab16_off(tid, 1)) = __float2half(1.0f);
+    }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -99,117 +126,141 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_kcache);
-            // rotated key tile t of the request (rows past the request's keys are never summed)
-            mbar_arrive_expect_tx(&bars[I_K_FULL], H * 16384);
-            const int32_t ky = kvh * L[L_TOTAL_TOKENS] + R[R_TOK_BASE] + t * kTileKeys;
-            for (int hb = 0; hb < H; ++hb)
-                tma_load_2d(sK + hb * 16384, &tm_kcache, &bars[I_K_FULL], hb * 64, ky);
-
+            const int32_t ky0 = kvh * L[L_TOTAL_TOKENS] + R[R_TOK_BASE] + t0 * kTileKeys;
             const int32_t qy0 = (kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE]) * g;
-            int last[2] = {-1, -1};
-            for (int qc = 0; qc < n_qc; ++qc) {
-                const int b = qc & 1;
-                if (qc >= 2 && !mbar_wait(&bars[I_Q_EMPTY + b], ((qc >> 1) - 1) & 1, abort_flag)) break;
-                mbar_arrive_expect_tx(&bars[I_Q_FULL + b], H * kImpQRows * 128);
+            int lastk[2] = {-1, -1}, lastq[2] = {-1, -1};
+            bool ok = true;
+            for (int i = 0; ok && i < nt; ++i) {
+                // rotated key tile t0 + i (rows past the request's keys are never summed)
+                const int kb = i & 1;
+                if (i >= 2 && !(ok = mbar_wait(&bars[I_K_EMPTY + kb], ((i >> 1) - 1) & 1, abort_flag))) break;
+                mbar_arrive_expect_tx(&bars[I_K_FULL + kb], H * 16384);
                 for (int hb = 0; hb < H; ++hb)
-                    tma_load_2d(sQs(b) + hb * kImpQRows * 128, &tm_q, &bars[I_Q_FULL + b], hb * 64,
-                                qy0 + qc * kImpQRows);
-                last[b] = qc;
+                    tma_load_2d(sKs(kb) + hb * 16384, &tm_kcache, &bars[I_K_FULL + kb], hb * 64, ky0 + i * kTileKeys);
+                lastk[kb] = i;
+                for (int qc = 0; qc < n_qc; ++qc) {
+                    const int s = i * n_qc + qc;
+                    if (q_resident && s > 0) break;
+                    const int qb = s & 1;
+                    if (s >= 2 && !(ok = mbar_wait(&bars[I_Q_EMPTY + qb], ((s >> 1) - 1) & 1, abort_flag))) break;
+                    mbar_arrive_expect_tx(&bars[I_Q_FULL + qb], H * kImpQRows * 128);
+                    for (int hb = 0; hb < H; ++hb)
+                        tma_load_2d(sQs(qb) + hb * kImpQRows * 128, &tm_q, &bars[I_Q_FULL + qb], hb * 64,
+                                    qy0 + qc * kImpQRows);
+                    lastq[qb] = s;
+                }
             }
-            mbar_drain(&bars[I_K_FULL], 0);
-            for (int s = 0; s < 2; ++s)
-                if (last[s] >= 0) mbar_drain(&bars[I_Q_FULL + s], (last[s] >> 1) & 1);
+            for (int b = 0; b < 2; ++b) {
+                if (lastk[b] >= 0) mbar_drain(&bars[I_K_FULL + b], (lastk[b] >> 1) & 1);
+                if (lastq[b] >= 0) mbar_drain(&bars[I_Q_FULL + b], (lastq[b] >> 1) & 1);
+            }
         }
     } else if (warp == kImpWarpMma) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(128, kImpQRows);
-            const uint32_t aK = smem_u32(sK);
-            bool ok = mbar_wait(&bars[I_K_FULL], 0, abort_flag);
-            for (int qc = 0; ok && qc < n_qc; ++qc) {
-                const int b = qc & 1;
-                if (!mbar_wait(&bars[I_Q_FULL + b], (qc >> 1) & 1, abort_flag)) break;
-                if (qc >= 2 && !mbar_wait(&bars[I_ACC_FREE + b], ((qc >> 1) - 1) & 1, abort_flag)) break;
+            bool ok = true;
+            for (int s = 0; ok && s < n_steps; ++s) {
+                const int i = s / n_qc, qc = s - i * n_qc, a = s & 1;
+                const int qb = q_resident ? 0 : (s & 1);
+                if (qc == 0) ok = mbar_wait(&bars[I_K_FULL + (i & 1)], (i >> 1) & 1, abort_flag);
+                ok = ok && mbar_wait(&bars[I_Q_FULL + qb], q_resident ? 0 : ((s >> 1) & 1), abort_flag) &&
+                     mbar_wait(&bars[I_LSE_FULL + qb], q_resident ? 0 : ((s >> 1) & 1), abort_flag);
+                ok = ok && (s < 2 || mbar_wait(&bars[I_ACC_FREE + a], ((s >> 1) - 1) & 1, abort_flag));
+                if (!ok) break;
                 tc_fence_after();
-                const uint32_t aQ = smem_u32(sQs(b));
+                const uint32_t aK = smem_u32(sKs(i & 1)), aQ = smem_u32(sQs(qb));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
-                    const uint64_t bq = desc_sw128_kmajor(aQ + (kk >> 2) * (kImpQRows * 128) + (kk & 3) * 32);
-                    mma_bf16_ss(tmem + b * kImpQRows, a, bq, idesc, kk > 0 ? 1u : 0u);
+                    const uint64_t da = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
+                    const uint64_t dq = desc_sw128_kmajor(aQ + (kk >> 2) * (kImpQRows * 128) + (kk & 3) * 32);
+                    mma_bf16_ss(tmem + a * kImpQRows, da, dq, idesc, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&bars[I_ACC_FULL + b]);
-                mma_commit(&bars[I_Q_EMPTY + b]);
+                // + 1 * (-lse2_hi) + 1 * (-lse2_lo) per query row
+                mma_bf16_ss(tmem + a * kImpQRows, desc_noswz_kmajor(smem_u32(sKones), 128, 256),
+                            desc_noswz_kmajor(smem_u32(sQlse(qb)), 128, 256), idesc, 1u);
+                mma_commit(&bars[I_ACC_FULL + a]);
+                if (!q_resident) mma_commit(&bars[I_Q_EMPTY + qb]);
+                if (qc == n_qc - 1) mma_commit(&bars[I_K_EMPTY + (i & 1)]);
             }
             mma_commit(&bars[I_DRAIN]);
             mbar_drain(&bars[I_DRAIN], 0);
         }
     } else {
-        // warps 0-3: sum exp over the query rows for one key per thread
-        bool ok = true;
-        const int chunks = R[R_LSE_CHUNKS];
-        const float2* part_in = prm.lse_part + R[R_LSE_BASE] + (int64_t)kvh * n_q * chunks;
+        // warps 0-3: thread tid owns key tid of every tile of the run
+        const float* lse_g = prm.lse_final + ((int64_t)kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE]) * g;
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-        float acc = 0.f;
-        // every one of the 128 threads runs every iteration (named barriers inside): after an
-        // abort the work is skipped, the barrier count stays the same
-        for (int qc = 0; qc < n_qc; ++qc) {
-            const int b = qc & 1;
+        const int total_tokens = L[L_TOTAL_TOKENS];
+        // -lse2 of step s's query chunk into its slab, as fp16 hi + lo (-30000 past the last row:
+        // those columns contribute 0)
+        auto prep = [&](int s) {
+            const int qc = s % n_qc;
+            uint8_t* slab = sQlse(q_resident ? 0 : (s & 1));
             for (int rr = tid; rr < kImpQRows; rr += 128) {
                 const int n = qc * kImpQRows + rr;
-                float lse = INFINITY;
-                if (n < n_q) {
-                    float M = -INFINITY;
-                    for (int cidx = 0; cidx < chunks; ++cidx) M = fmaxf(M, part_in[(int64_t)n * chunks + cidx].x);
-                    float S = 0.f;
-                    for (int cidx = 0; cidx < chunks; ++cidx) {
-                        const float2 pl = part_in[(int64_t)n * chunks + cidx];
-                        S += pl.y * ex2(pl.x - M);
-                    }
-                    lse = S > 0.f ? M + log2f(S) : INFINITY;
-                }
-                sLse(b)[rr] = lse;
+                const float v = n < n_q ? -__ldcg(lse_g + n) : -30000.f;
+                const __half hi = __float2half_rn(v);
+                *reinterpret_cast<__half*>(slab + slab16_off(rr, 0)) = hi;
+                *reinterpret_cast<__half*>(slab + slab16_off(rr, 1)) = __float2half_rn(v - __half2float(hi));
             }
-            named_sync_128();
-            if (ok) ok = mbar_wait(&bars[I_ACC_FULL + b], (qc >> 1) & 1, abort_flag);
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[I_LSE_FULL + (q_resident ? 0 : (s & 1))]);
+        };
+        if (n_steps > 0) prep(0);
+        if (!q_resident && n_steps > 1) prep(1);
+        bool ok = true;
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s = 0; s < n_steps; ++s) {
+            const int i = s / n_qc, qc = s - i * n_qc, a = s & 1;
+            if (ok) ok = mbar_wait(&bars[I_ACC_FULL + a], (s >> 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) continue;
-            tc_fence_after();
-            const int nvalid = min(kImpQRows, n_q - qc * kImpQRows);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sv[4][32];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t sv[4][32];
+                    for (int cc = 0; cc < 4; ++cc)
+                        tmem_ld32(tmem + lane_addr + a * kImpQRows + half * 128 + cc * 32, sv[cc]);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    tmem_ld32(tmem + lane_addr + b * kImpQRows + half * 128 + cc * 32, sv[cc]);
-                tmem_ld_wait();
+                    for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int n = half * 128 + cc * 32 + e;
-                        if (n < nvalid) acc += ex2(__uint_as_float(sv[cc][e]) - sLse(b)[n]);
-                    }
+                        for (int e = 0; e < 32; ++e) acc4[e & 3] += ex2(__uint_as_float(sv[cc][e]));
+                }
+                tc_fence_before();
+                mbar_arrive(&bars[I_ACC_FREE + a]);
+                // step s's MMA is complete, so its slab buffer takes step s + 2's chunk
+                if (!q_resident && s + 2 < n_steps) prep(s + 2);
             }
-            tc_fence_before();
-            mbar_arrive(&bars[I_ACC_FREE + b]);
+            if (qc == n_qc - 1) {
+                const int t = t0 + i;
+                const bool valid_key = (t * kPagesPerTile + tid / kPage) < n_pages;
+                const int32_t tok = R[R_TOK_BASE] + t * kTileKeys + tid;
+                if (ok && valid_key) prm.part[(int64_t)kvh * total_tokens + tok] = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+                acc4[0] = acc4[1] = acc4[2] = acc4[3] = 0.f;
+            }
         }
-        // per-kv-head partial, then the last CTA of this key tile sums the heads in order
-        const int total_tokens = L[L_TOTAL_TOKENS];
-        const bool valid_key = (t * kPagesPerTile + tid / kPage) < n_pages;
-        const int32_t tok = R[R_TOK_BASE] + t * kTileKeys + tid;
-        if (ok && valid_key) prm.part[(int64_t)kvh * total_tokens + tok] = acc;
+        if (n_qc == 0)   // a request without query rows: every importance is 0
+            for (int i = 0; i < nt; ++i)
+                if (((t0 + i) * kPagesPerTile + tid / kPage) < n_pages)
+                    prm.part[(int64_t)kvh * total_tokens + R[R_TOK_BASE] + (t0 + i) * kTileKeys + tid] = 0.f;
+        // the last of the run's Hkv CTAs sums the heads in order
         __threadfence();
         named_sync_128();
-        if (tid == 0) misc[5] = (atomicAdd(&prm.counters[R[R_KTILE_BASE] + t], 1) == Hkv - 1) ? 1 : 0;
+        const int cidx = R[R_KTILE_BASE] + t0;
+        if (tid == 0) misc[5] = (atomicAdd(&prm.counters[cidx], 1) == Hkv - 1) ? 1 : 0;
         named_sync_128();
         if (misc[5]) {
             __threadfence();
-            if (valid_key) {
-                float s = 0.f;
-                for (int h = 0; h < Hkv; ++h) s += __ldcg(prm.part + (int64_t)h * total_tokens + tok);
-                prm.importance[tok] = s;
+            for (int i = 0; i < nt; ++i) {
+                const int t = t0 + i;
+                if ((t * kPagesPerTile + tid / kPage) >= n_pages) continue;
+                const int32_t tok = R[R_TOK_BASE] + t * kTileKeys + tid;
+                float sum = 0.f;
+                for (int h = 0; h < Hkv; ++h) sum += __ldcg(prm.part + (int64_t)h * total_tokens + tok);
+                prm.importance[tok] = sum;
             }
-            if (tid == 0) prm.counters[R[R_KTILE_BASE] + t] = 0;
+            if (tid == 0) prm.counters[cidx] = 0;
         }
     }
     tc_fence_before();

@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
 }
 
 // ------------------------------------------------------------------ split-range combine
-// A (request, kv head, tile pair) whose key range was split over R_NSPLIT CTAs left, per split s,
+// A (request, kv head, tile pair) whose key range was split over P_NSPLIT CTAs left, per split s,
 // a normalized partial row O_s = (sum_u p_u v_u) / l_s together with (m_s, l_s) (running max in log2
 // units, running sum).  The full row is sum_s w_s O_s / sum_s w_s with w_s = l_s 2^(m_s - max m).
 template <int D>
@@ -280,7 +280,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict_
     const int32_t* item = L + L[L_OFF_COMB] + kItemWords * blockIdx.x;
     const int req = item[0], kvh = item[1], qpair = item[2];
     const int32_t* R = L + L[L_OFF_REQ] + req * R_STRIDE;
-    const int ns = R[R_NSPLIT];
+    const int32_t* PR = L + L[L_OFF_PAIR] + (R[R_PAIR_BASE] + qpair) * P_STRIDE;
+    const int ns = PR[P_NSPLIT];
     const int g = L[L_GROUP], Hq = L[L_HQ];
     const int pr = blockIdx.y * RPB + threadIdx.x / CH;   // row within the pair, 0..255
     const int c = threadIdx.x % CH;
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict_
     const int tt = pr / kTileRows, mm = pr % kTileRows;
     const int row = qpair * kQTilesPerCta * tpt + tt * tpt + mm / g;
     if (row >= R[R_N_ROWS]) return;
-    const int64_t slot0 = (int64_t)R[R_SLOT_BASE] + (int64_t)(kvh * R[R_NPAIRS] + qpair) * ns;
+    const int64_t slot0 = (int64_t)PR[P_SLOT_BASE] + (int64_t)kvh * ns;
     const int64_t stride = kQTilesPerCta * kTileRows;
     float M = -INFINITY;
     for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, part_ml[(slot0 + sp) * stride + pr].x);

@@ -18,10 +18,8 @@ constexpr int kQTilesPerCta = 2;         // 128-row query tiles sharing each rot
 constexpr int kPagesPerTile = kTileKeys / kPage;
 constexpr int kMaxPosLimit = 1 << 20;
 constexpr int kItemWords = 4;
-constexpr int kLseTargetCtas = 2 * 152;  // GB300: 152 SMs; split keys until ~2 CTAs per SM
-constexpr int kAttnTargetCtas = 2 * 152; // attention: split the key range of small batches
-constexpr int kMinTilesPerSplit = 4;
-constexpr int kMaxSplits = 8;
+constexpr int kNumSms = 152;            // GB300; the attention kernels run one CTA per SM
+constexpr int kMaxSplits = 16;          // key-range splits of one attention (or LSE) work unit
 
 enum : int {
     L_MAGIC = 0, L_WORDS = 1, L_N_REQS = 2, L_HQ = 3, L_HKV = 4, L_D = 5, L_N_PHYS = 6,
@@ -31,7 +29,7 @@ enum : int {
     L_LSE_SLOTS = 21, L_GROUP = 22, L_MAX_SPAN_LEN = 23,
     L_OFF_REQ = 24, L_OFF_SPAN = 25, L_OFF_BLOCK = 26, L_OFF_PAGEPOS = 27, L_OFF_ATTN = 28,
     L_OFF_LSE = 29, L_OFF_IMP = 30, L_OFF_QPOS = 31, L_OFF_COMB = 32, L_N_COMB = 33,
-    L_ATTN_SLOTS = 34,
+    L_ATTN_SLOTS = 34, L_OFF_PAIR = 35, L_N_PAIRS = 36, L_N_LSE_PAIRS = 37,
     L_HEADER = 40
 };
 
@@ -40,9 +38,9 @@ enum : int {
     R_N_PAGES = 0, R_TOK_BASE = 1, R_PAGE_BASE = 2, R_Q_BASE = 3, R_ROW_BASE = 4, R_SEL_BASE = 5,
     R_QUERY_POS0 = 6, R_N_SPANS = 7, R_SPAN_BASE = 8, R_N_QUERY = 9, R_N_SEL = 10, R_N_ROWS = 11,
     R_LSE_BASE = 12, R_LSE_CHUNKS = 13, R_KTILE_BASE = 14, R_N_KTILES = 15,
-    R_NSPLIT = 16,      // attention key-range splits of every (kv head, tile pair) of the request
-    R_SLOT_BASE = 17,   // first partial-output slot of the request (when R_NSPLIT > 1)
+    R_LSE_PAIR_BASE = 16,   // first (kv head, query tile pair) index of the request's LSE pass
     R_NPAIRS = 18,      // tile pairs of the request (per kv head)
+    R_PAIR_BASE = 19,   // first pair record of the request
     R_STRIDE = 20
 };
 
@@ -52,11 +50,17 @@ enum : int {
     S_PHYS_FIRST = 6, S_STRIDE = 8
 };
 
+// per-(request, tile pair) record: the pair's attention key range is split over P_NSPLIT CTAs per
+// kv head; with P_NSPLIT > 1 split s of kv head h writes partial slot P_SLOT_BASE + h*P_NSPLIT + s
+enum : int { P_NSPLIT = 0, P_SLOT_BASE = 1, P_STRIDE = 2 };
+
 // work items (kItemWords each)
 //   attention : {req, kv head, q tile pair, key-range split}   largest estimated cost first
 //   lse       : {req, kv head, q tile pair, key chunk}
+//               (the last chunk to finish turns the chunks' partial (max, sum) into the rows'
+//               log2-sum-exp; counter R_LSE_PAIR_BASE + kv head * query pairs + pair)
 // (a "q tile pair" p covers the 128-row query tiles 2p and 2p+1 of the request)
-//   importance: {req, key tile, kv head, 0}
+//   importance: {req, first key tile, kv head, key tiles}
 //   combine   : {req, kv head, q tile pair, 0}   pairs whose key range was split
 
 }  // namespace pcf

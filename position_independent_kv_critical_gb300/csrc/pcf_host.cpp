@@ -7,6 +7,8 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <functional>
+#include <queue>
 #include <vector>
 
 #include "../../include/pcf.h"
@@ -60,11 +62,66 @@ struct Plan {
     int32_t total_tokens = 0, total_query = 0, total_rows = 0, total_sel = 0, total_pages = 0;
     int32_t n_spans = 0, max_tokens = 0, max_rows = 0, max_query = 0, total_ktiles = 0;
     int32_t n_attn = 0, n_lse = 0, n_imp = 0, lse_slots = 0, max_span_len = 0;
-    int32_t n_comb = 0, attn_slots = 0;
-    std::vector<int32_t> lse_chunks, nsplit;
+    int32_t n_comb = 0, attn_slots = 0, n_pairs = 0, n_lse_pairs = 0, imp_tiles = 1;
+    std::vector<int32_t> lse_chunks;
+    std::vector<int32_t> pair_base;     // per request: first pair record
+    std::vector<int32_t> pair_tiles;    // per pair record: estimated key tiles of the pair
+    std::vector<int32_t> pair_split;    // per pair record: key-range splits
 };
 
 inline int32_t cdiv(int64_t a, int64_t b) { return (int32_t)((a + b - 1) / b); }
+
+// Estimated finishing time (in key tiles) of CTAs with the given costs on kNumSms SMs that take
+// one CTA each at a time, launched in decreasing cost order (the order of the work lists).
+double lpt_makespan(std::vector<double>& costs) {
+    std::sort(costs.begin(), costs.end(), std::greater<double>());
+    std::priority_queue<double, std::vector<double>, std::greater<double>> sm;
+    for (int i = 0; i < kNumSms; ++i) sm.push(0.0);
+    double end = 0.0;
+    for (double c : costs) {
+        const double t = sm.top() + c;
+        sm.pop();
+        sm.push(t);
+        end = std::max(end, t);
+    }
+    return end;
+}
+
+// Key-range splits per work unit (a unit runs once per kv head: `copies` CTAs) that minimise the
+// estimated finishing time when a CTA costs `overhead` tiles plus its share of the unit's tiles
+// and any split adds `combine` tiles (the merge of the partial results).  Batches with enough
+// units to fill the GPU several times are not split.
+void choose_splits(const std::vector<int32_t>& tiles, int32_t copies, double overhead, double combine,
+                   std::vector<int32_t>* splits) {
+    splits->assign(tiles.size(), 1);
+    if (tiles.empty() || (int64_t)tiles.size() * copies >= 4 * kNumSms) return;
+    int32_t max_t = 1;
+    for (int32_t t : tiles) max_t = std::max(max_t, t);
+    double best = 0.0;
+    int32_t best_c = max_t;
+    std::vector<double> costs;
+    for (int32_t c = max_t; c >= 1; --c) {   // candidate tiles per split, largest first
+        costs.clear();
+        bool any = false;
+        for (int32_t t : tiles) {
+            const int32_t sp = std::max(1, std::min({cdiv(t, c), kMaxSplits, t}));
+            any = any || sp > 1;
+            costs.insert(costs.end(), (size_t)copies * sp, overhead + (double)t / sp);
+        }
+        const double end = lpt_makespan(costs) + (any ? combine : 0.0);
+        if (c == max_t || end < best - 1e-9) {
+            best = end;
+            best_c = c;
+        }
+    }
+    for (size_t i = 0; i < tiles.size(); ++i)
+        (*splits)[i] = std::max(1, std::min({cdiv(tiles[i], best_c), kMaxSplits, tiles[i]}));
+}
+
+// Prologue + epilogue of an attention CTA in key tiles, and of the merge of split results.
+constexpr double kAttnCtaOverhead = 1.5;
+constexpr double kAttnCombineCost = 2.0;
+constexpr double kLseCtaOverhead = 2.0;
 
 pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims* dims, Plan* plan) {
     if (!reqs || !dims || n_reqs < 1 || n_reqs > (1 << 20)) return PCF_ERR_INVALID_ARG;
@@ -78,7 +135,6 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
     if (g > kTileRows || kTileRows % g != 0) return PCF_ERR_UNSUPPORTED;
 
     int64_t tot_tok = 0, tot_q = 0, tot_rows = 0, tot_sel = 0, tot_spans = 0, tot_kt = 0;
-    int64_t base_lse_ctas = 0, base_attn_ctas = 0;
     for (int b = 0; b < n_reqs; ++b) {
         const pcf_request_desc& r = reqs[b];
         if (r.n_spans < 0 || r.n_query < 0 || (r.n_spans > 0 && !r.spans)) return PCF_ERR_INVALID_ARG;
@@ -107,9 +163,6 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
         tot_spans += r.n_spans;
         const int32_t nkt = cdiv(n_tok / kPage, kPagesPerTile);
         tot_kt += nkt;
-        if (nkt > 0 && r.n_query > 0)
-            base_lse_ctas += (int64_t)d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta);
-        base_attn_ctas += (int64_t)d.n_kv_heads * cdiv((n_sel + r.n_query) * g, kTileRows * kQTilesPerCta);
         plan->max_tokens = std::max<int32_t>(plan->max_tokens, (int32_t)n_tok);
         plan->max_rows = std::max<int32_t>(plan->max_rows, (int32_t)(n_sel + r.n_query));
         plan->max_query = std::max<int32_t>(plan->max_query, r.n_query);
@@ -127,40 +180,98 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
     plan->n_spans = (int32_t)tot_spans;
     plan->total_ktiles = (int32_t)tot_kt;
 
-    // key-chunk split of the LSE pass: aim for ~kLseTargetCtas CTAs in total
-    const int32_t want = base_lse_ctas > 0 ? cdiv(kLseTargetCtas, base_lse_ctas) : 1;
-    // key-range split of the attention: only batches too small to fill the GPU with tile pairs
-    const int32_t want_split = base_attn_ctas > 0 ? std::min<int64_t>(kMaxSplits, cdiv(kAttnTargetCtas, base_attn_ctas)) : 1;
-    plan->lse_chunks.assign(n_reqs, 0);
-    plan->nsplit.assign(n_reqs, 1);
-    int64_t n_attn = 0, n_lse = 0, n_imp = 0, slots = 0, n_comb = 0, attn_slots = 0;
+    // Attention work units: (request, pair of 128-row query tiles), each run once per kv head.  A
+    // pair sees the cached key tiles up to its last row's position and the fresh tiles up to its
+    // last row.  Rows are selected tokens in position order, then query tokens; before the
+    // selection is known, a selected row is only known to lie inside its span, so the span's end
+    // bounds its cached tiles.
+    plan->pair_base.assign(n_reqs, 0);
+    plan->pair_tiles.clear();
     for (int b = 0; b < n_reqs; ++b) {
         const pcf_request_desc& r = reqs[b];
-        int64_t n_tok = 0, n_sel = 0;
+        int64_t n_sel = 0, n_pg = 0;
+        std::vector<int64_t> cum_k(1, 0), cum_pages(1, 0);
         for (int s = 0; s < r.n_spans; ++s) {
-            n_tok += (int64_t)r.spans[s].n_pages * kPage;
             n_sel += r.spans[s].k;
+            n_pg += r.spans[s].n_pages;
+            cum_k.push_back(n_sel);
+            cum_pages.push_back(n_pg);
         }
-        const int32_t nkt = cdiv(n_tok / kPage, kPagesPerTile);
+        const int32_t nkt = cdiv(n_pg, kPagesPerTile);
         const int64_t rows = n_sel + r.n_query;
         const int64_t npairs = cdiv(rows * g, kTileRows * kQTilesPerCta);
-        const int32_t max_tiles = nkt + cdiv(rows, kTileKeys);   // key tiles the last pair sees
-        const int32_t ns = std::max(1, std::min<int32_t>(want_split, max_tiles / kMinTilesPerSplit));
-        plan->nsplit[b] = ns;
-        n_attn += (int64_t)d.n_kv_heads * npairs * ns;
-        if (ns > 1) {
-            n_comb += (int64_t)d.n_kv_heads * npairs;
-            attn_slots += (int64_t)d.n_kv_heads * npairs * ns;
+        const int64_t toks_per_pair = (int64_t)kQTilesPerCta * (kTileRows / g);
+        plan->pair_base[b] = (int32_t)plan->pair_tiles.size();
+        size_t s = 0;
+        for (int64_t p = 0; p < npairs; ++p) {
+            const int64_t last = std::min<int64_t>((p + 1) * toks_per_pair, rows) - 1;
+            int32_t nct = nkt;
+            if (last < n_sel) {
+                while (s + 1 < cum_k.size() && cum_k[s + 1] <= last) ++s;
+                nct = cdiv(cum_pages[s + 1], kPagesPerTile);
+            }
+            plan->pair_tiles.push_back(nct + (int32_t)(last / kTileKeys) + 1);
+        }
+    }
+    choose_splits(plan->pair_tiles, d.n_kv_heads, kAttnCtaOverhead, kAttnCombineCost, &plan->pair_split);
+    // LSE pass: units (request, query tile pair) over all cached tiles, split into key chunks
+    std::vector<int32_t> lse_split;
+    {
+        std::vector<int32_t> tiles, copies;
+        for (int b = 0; b < n_reqs; ++b) {
+            const pcf_request_desc& r = reqs[b];
+            int64_t n_pg = 0;
+            for (int s = 0; s < r.n_spans; ++s) n_pg += r.spans[s].n_pages;
+            const int32_t nkt = cdiv(n_pg, kPagesPerTile);
+            if (nkt > 0 && r.n_query > 0)
+                for (int32_t p = 0; p < cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta); ++p) tiles.push_back(nkt);
+        }
+        std::vector<int32_t> sp;
+        choose_splits(tiles, d.n_kv_heads, kLseCtaOverhead, 0.0, &sp);
+        size_t u = 0;
+        for (int b = 0; b < n_reqs; ++b) {
+            const pcf_request_desc& r = reqs[b];
+            int64_t n_pg = 0;
+            for (int s = 0; s < r.n_spans; ++s) n_pg += r.spans[s].n_pages;
+            const int32_t nkt = cdiv(n_pg, kPagesPerTile);
+            int32_t want = 1;
+            if (nkt > 0 && r.n_query > 0) {
+                want = sp[u];   // every pair of a request has the same tiles, hence the same split
+                u += cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta);
+            }
+            lse_split.push_back(want);
+        }
+    }
+    plan->lse_chunks.assign(n_reqs, 0);
+    int64_t n_attn = 0, n_lse = 0, n_imp = 0, slots = 0, n_comb = 0, attn_slots = 0, n_lse_pairs = 0;
+    // importance pass: CTAs over runs of key tiles of one kv head, about two CTAs per SM in total
+    plan->imp_tiles = (int32_t)std::max<int64_t>(1, (tot_kt * d.n_kv_heads) / (2 * kNumSms));
+    for (int b = 0; b < n_reqs; ++b) {
+        const pcf_request_desc& r = reqs[b];
+        int64_t n_tok = 0;
+        for (int s = 0; s < r.n_spans; ++s) n_tok += (int64_t)r.spans[s].n_pages * kPage;
+        const int32_t nkt = cdiv(n_tok / kPage, kPagesPerTile);
+        const int32_t p0 = plan->pair_base[b];
+        const int32_t p1 = b + 1 < n_reqs ? plan->pair_base[b + 1] : (int32_t)plan->pair_tiles.size();
+        for (int32_t p = p0; p < p1; ++p) {
+            const int32_t ns = plan->pair_split[p];
+            n_attn += (int64_t)d.n_kv_heads * ns;
+            if (ns > 1) {
+                n_comb += d.n_kv_heads;
+                attn_slots += (int64_t)d.n_kv_heads * ns;
+            }
         }
         if (nkt > 0 && r.n_query > 0) {
-            const int32_t tpc = cdiv(nkt, std::max(1, std::min(want, nkt)));
+            const int32_t tpc = cdiv(nkt, std::max(1, std::min(lse_split[b], nkt)));
             const int32_t chunks = cdiv(nkt, tpc);
             plan->lse_chunks[b] = chunks;
             n_lse += (int64_t)d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta) * chunks;
+            n_lse_pairs += (int64_t)d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta);
             slots += (int64_t)r.n_query * d.n_q_heads * chunks;
         }
-        if (nkt > 0) n_imp += (int64_t)nkt * d.n_kv_heads;
+        if (nkt > 0) n_imp += (int64_t)cdiv(nkt, plan->imp_tiles) * d.n_kv_heads;
     }
+    plan->n_pairs = (int32_t)plan->pair_tiles.size();
     if (n_attn >= lim || n_lse >= lim || n_imp >= lim || slots >= lim || attn_slots >= lim / 256)
         return PCF_ERR_INVALID_ARG;
     plan->n_comb = (int32_t)n_comb;
@@ -168,10 +279,12 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
     plan->n_attn = (int32_t)n_attn;
     plan->n_lse = (int32_t)n_lse;
     plan->n_imp = (int32_t)n_imp;
+    plan->n_lse_pairs = (int32_t)n_lse_pairs;
     plan->lse_slots = (int32_t)slots;
 
     plan->words = L_HEADER + (int64_t)n_reqs * R_STRIDE + tot_spans * S_STRIDE +
-                  2 * (int64_t)plan->total_pages + kItemWords * (n_attn + n_lse + n_imp + n_comb) + tot_q;
+                  2 * (int64_t)plan->total_pages + kItemWords * (n_attn + n_lse + n_imp + n_comb) + tot_q +
+                  (int64_t)P_STRIDE * plan->n_pairs;
     if (plan->words >= ((int64_t)1 << 31)) return PCF_ERR_INVALID_ARG;
     return PCF_OK;
 }
@@ -226,6 +339,8 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
     H[L_MAX_SPAN_LEN] = plan.max_span_len;
     H[L_N_COMB] = plan.n_comb;
     H[L_ATTN_SLOTS] = plan.attn_slots;
+    H[L_N_PAIRS] = plan.n_pairs;
+    H[L_N_LSE_PAIRS] = plan.n_lse_pairs;
 
     int64_t off = L_HEADER;
     H[L_OFF_REQ] = (int32_t)off;    off += (int64_t)n_reqs * R_STRIDE;
@@ -237,6 +352,7 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
     H[L_OFF_IMP] = (int32_t)off;    off += (int64_t)kItemWords * plan.n_imp;
     H[L_OFF_QPOS] = (int32_t)off;   off += plan.total_query;
     H[L_OFF_COMB] = (int32_t)off;   off += (int64_t)kItemWords * plan.n_comb;
+    H[L_OFF_PAIR] = (int32_t)off;   off += (int64_t)P_STRIDE * plan.n_pairs;
 
     int32_t* REQ = blob + H[L_OFF_REQ];
     int32_t* SPN = blob + H[L_OFF_SPAN];
@@ -244,17 +360,18 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
     int32_t* PPOS = blob + H[L_OFF_PAGEPOS];
     int32_t* QPOS = blob + H[L_OFF_QPOS];
 
-    struct AttnItem { int32_t req, kvh, qt, split; int64_t cost; int64_t order; };
+    struct AttnItem { int32_t req, kvh, qt, split; double cost; };
     std::vector<AttnItem> attn;
     attn.reserve(plan.n_attn);
     int32_t* LSE = blob + H[L_OFF_LSE];
     int32_t* IMP = blob + H[L_OFF_IMP];
     int32_t* COMB = blob + H[L_OFF_COMB];
+    int32_t* PAIR = blob + H[L_OFF_PAIR];
     int64_t n_lse = 0, n_imp = 0, n_comb = 0;
     int32_t slot_base = 0;
 
     int32_t tok_base = 0, q_base = 0, row_base = 0, sel_base = 0, span_base = 0, kt_base = 0;
-    int32_t lse_base = 0;
+    int32_t lse_base = 0, lse_pair_base = 0;
     for (int b = 0; b < n_reqs; ++b) {
         const pcf_request_desc& r = reqs[b];
         int32_t* R = REQ + (int64_t)b * R_STRIDE;
@@ -293,29 +410,27 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
         R[R_N_ROWS] = n_rows;
         R[R_LSE_BASE] = lse_base;
         R[R_LSE_CHUNKS] = plan.lse_chunks[b];
+        R[R_LSE_PAIR_BASE] = lse_pair_base;
+        if (plan.lse_chunks[b] > 0)
+            lse_pair_base += d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta);
         R[R_KTILE_BASE] = kt_base;
         R[R_N_KTILES] = nkt;
-        const int32_t ns = plan.nsplit[b];
-        R[R_NSPLIT] = ns;
-        R[R_SLOT_BASE] = slot_base;
+        R[R_PAIR_BASE] = plan.pair_base[b];
         for (int t = 0; t < r.n_query; ++t) QPOS[q_base + t] = r.query_pos0 + t;
 
-        // attention work: one item per (kv head, pair of 128-row tiles); rows pack the g heads of a
-        // token
-        const int32_t toks_per_item = kQTilesPerCta * (kTileRows / g);
+        // attention work: per (pair of 128-row tiles, kv head), one item per key-range split; rows
+        // pack the g heads of a token
         const int32_t n_qt = cdiv((int64_t)n_rows * g, kTileRows * kQTilesPerCta);
         R[R_NPAIRS] = n_qt;
-        if (ns > 1) slot_base += d.n_kv_heads * n_qt * ns;
         for (int32_t qt = 0; qt < n_qt; ++qt) {
-            const int64_t last_row = std::min<int64_t>((int64_t)(qt + 1) * toks_per_item, n_rows) - 1;
-            // estimated visible keys: query rows see everything, recomputed rows about the
-            // fraction of the context before them
-            int64_t cost;
-            if (last_row >= n_sel) cost = (int64_t)n_tok + n_rows;
-            else cost = ((int64_t)(last_row + 1) * (n_tok + n_sel)) / std::max<int64_t>(1, n_sel);
+            const int32_t pr = plan.pair_base[b] + qt;
+            const int32_t ns = plan.pair_split[pr];
+            PAIR[P_STRIDE * pr + P_NSPLIT] = ns;
+            PAIR[P_STRIDE * pr + P_SLOT_BASE] = slot_base;
+            if (ns > 1) slot_base += d.n_kv_heads * ns;
+            const double cost = kAttnCtaOverhead + (double)plan.pair_tiles[pr] / ns;
             for (int32_t h = 0; h < d.n_kv_heads; ++h) {
-                for (int32_t sp = 0; sp < ns; ++sp)
-                    attn.push_back({b, h, qt, sp, cost / ns, (int64_t)attn.size()});
+                for (int32_t sp = 0; sp < ns; ++sp) attn.push_back({b, h, qt, sp, cost});
                 if (ns > 1) {
                     int32_t* it = COMB + kItemWords * n_comb++;
                     it[0] = b; it[1] = h; it[2] = qt; it[3] = 0;
@@ -333,12 +448,18 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
                     }
             lse_base += r.n_query * d.n_q_heads * plan.lse_chunks[b];
         }
-        // importance work: (key tile, kv head)
-        for (int32_t t = 0; t < nkt; ++t)
-            for (int32_t h = 0; h < d.n_kv_heads; ++h) {
-                int32_t* it = IMP + kItemWords * n_imp++;
-                it[0] = b; it[1] = t; it[2] = h; it[3] = 0;
+        // importance work: (run of key tiles, kv head); the request's tiles are cut into
+        // ceil(nkt / imp_tiles) runs of near-equal length
+        if (nkt > 0) {
+            const int32_t runs = cdiv(nkt, plan.imp_tiles);
+            for (int32_t u = 0; u < runs; ++u) {
+                const int32_t t0 = (int32_t)((int64_t)u * nkt / runs), t1 = (int32_t)((int64_t)(u + 1) * nkt / runs);
+                for (int32_t h = 0; h < d.n_kv_heads; ++h) {
+                    int32_t* it = IMP + kItemWords * n_imp++;
+                    it[0] = b; it[1] = t0; it[2] = h; it[3] = t1 - t0;
+                }
             }
+        }
         tok_base += n_tok;
         q_base += r.n_query;
         row_base += n_rows;

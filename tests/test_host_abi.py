@@ -20,6 +20,7 @@ GOLDEN = os.path.join(ROOT, "tests", "golden")
 L_OFF_REQ, L_OFF_SPAN, L_OFF_BLOCK, L_OFF_PAGEPOS = 24, 25, 26, 27
 L_OFF_ATTN, L_OFF_LSE, L_OFF_IMP, L_OFF_QPOS = 28, 29, 30, 31
 L_N_ATTN, L_N_LSE, L_N_IMP = 18, 19, 20
+L_OFF_COMB, L_N_COMB, L_OFF_PAIR, L_N_PAIRS = 32, 33, 35, 36
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -97,14 +98,35 @@ def test_layout_totals_and_block_table(name):
     g = cfg.hq // cfg.hkv
     items = B[B[L_OFF_ATTN]: B[L_OFF_ATTN] + 4 * B[L_N_ATTN]].reshape(-1, 4)
     REQ = B[L_OFF_REQ]
-    nsplit = [int(B[REQ + 20 * b + 16]) for b in range(len(reqs))]
-    want = {(b, h, t, s) for b, r in enumerate(reqs) for h in range(cfg.hkv)
-            for t in range(-(-r.n_rows * g // 256)) for s in range(nsplit[b])}
+    # per (request, tile pair): key-range splits and the first partial slot (pair records)
+    pair_base = [int(B[REQ + 20 * b + 19]) for b in range(len(reqs))]
+    n_pairs = [-(-r.n_rows * g // 256) for r in reqs]
+    PR = B[L_OFF_PAIR]
+    nsplit = {(b, t): int(B[PR + 2 * (pair_base[b] + t)]) for b in range(len(reqs)) for t in range(n_pairs[b])}
+    want = {(b, h, t, s) for b in range(len(reqs)) for h in range(cfg.hkv)
+            for t in range(n_pairs[b]) for s in range(nsplit[(b, t)])}
     got = {tuple(x) for x in items.tolist()}
     assert got == want and len(items) == len(want)
-    assert all(1 <= n <= 8 for n in nsplit)
+    assert all(1 <= n <= 16 for n in nsplit.values())
+    assert B[L_N_PAIRS] == sum(n_pairs)
+    # partial slots: consecutive blocks of Hkv * nsplit for the split pairs, in pair order
+    slot = 0
+    for b in range(len(reqs)):
+        for t in range(n_pairs[b]):
+            if nsplit[(b, t)] > 1:
+                assert B[PR + 2 * (pair_base[b] + t) + 1] == slot
+                slot += cfg.hkv * nsplit[(b, t)]
+    assert B[34] == slot                     # partial slots in total
+    # combine items: exactly the split (request, kv head, pair)s
+    comb = B[B[L_OFF_COMB]: B[L_OFF_COMB] + 4 * B[L_N_COMB]].reshape(-1, 4)
+    assert {tuple(x[:3]) for x in comb.tolist()} == {(b, h, t) for (b, t), n in nsplit.items() if n > 1
+                                                      for h in range(cfg.hkv)}
+    # importance runs {req, first tile, kv head, tiles}: every (request, key tile, kv head) once
     imp = B[B[L_OFF_IMP]: B[L_OFF_IMP] + 4 * B[L_N_IMP]].reshape(-1, 4)
-    assert len(imp) == sum(-(-r.n_cached // 128) for r in reqs) * cfg.hkv
+    covered = [(int(q), t, int(h)) for q, t0, h, nt in imp.tolist() for t in range(t0, t0 + nt)]
+    assert sorted(covered) == sorted((b, t, h) for b, r in enumerate(reqs)
+                                     for t in range(-(-r.n_cached // 128)) for h in range(cfg.hkv))
+    assert all(nt >= 1 for nt in imp[:, 3])
 
 
 def test_shared_pages_at_two_offsets_in_one_batch():
