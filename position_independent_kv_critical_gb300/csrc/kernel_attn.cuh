@@ -22,8 +22,9 @@
 //               Four single-thread issuers keep four independent MMA streams in flight: one
 //               thread's stream of 128-row MMAs with N <= 128 is bound by per-instruction
 //               latency, not by the tensor core's rate
-//   warp  9     K producer: Q tiles; rotated K tiles (cached or fresh, fp16, TMA) and, per key,
+//   warp  9     K producer: rotated K tiles (cached or fresh, fp16, TMA) and, per key,
 //               its logical position and bias; 2-stage ring, freed by the second half's Q K^T
+//   (warp 0 starts the Q tile loads during set-up)
 //   warp  10    V producer (TMA): cached V pages through the block table / fresh V tiles; 2-stage
 //               ring, freed once both P V of a stage are done
 // TMEM: tile t's two S half-buffers at columns t*128 + {0, 64} (64 fp32 columns = 64 keys each),
@@ -145,29 +146,39 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int32_t* page_pos = L + L[L_OFF_PAGEPOS] + page_base;
     const int32_t* blk = L + L[L_OFF_BLOCK] + page_base;
 
-    if (tid == 0) {
-        mbar_init(&bars[B_Q_FULL], 1);
-        for (int s2 = 0; s2 < kKStages; ++s2) {
-            mbar_init(&bars[B_K_FULL + s2], 32);   // every producer lane (key info) + TMA bytes
-            mbar_init(&bars[B_K_EMPTY + s2], kQTilesPerCta);
-            mbar_init(&bars[B_KPOS_FREE + s2], 256);
-        }
-        for (int s2 = 0; s2 < kVStages; ++s2) {
-            mbar_init(&bars[B_V_FULL + s2], 1);
-            mbar_init(&bars[B_V_EMPTY + s2], kQTilesPerCta);
-        }
-        for (int t = 0; t < kQTilesPerCta; ++t) {
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(&bars[B_S_FULL + 2 * t + b], 1);
-                mbar_init(&bars[B_P_FULL + 2 * t + b], 128);
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(&bars[B_Q_FULL], 1);
+            for (int s2 = 0; s2 < kKStages; ++s2) {
+                mbar_init(&bars[B_K_FULL + s2], 32);   // every producer lane (key info) + TMA bytes
+                mbar_init(&bars[B_K_EMPTY + s2], kQTilesPerCta);
+                mbar_init(&bars[B_KPOS_FREE + s2], 256);
             }
-            mbar_init(&bars[B_PV_DONE + 2 * t], 1);
-            mbar_init(&bars[B_PV_DONE + 2 * t + 1], 1);
-            mbar_init(&bars[B_O_DONE + t], 1);
+            for (int s2 = 0; s2 < kVStages; ++s2) {
+                mbar_init(&bars[B_V_FULL + s2], 1);
+                mbar_init(&bars[B_V_EMPTY + s2], kQTilesPerCta);
+            }
+            for (int t = 0; t < kQTilesPerCta; ++t) {
+                for (int b = 0; b < 2; ++b) {
+                    mbar_init(&bars[B_S_FULL + 2 * t + b], 1);
+                    mbar_init(&bars[B_P_FULL + 2 * t + b], 128);
+                }
+                mbar_init(&bars[B_PV_DONE + 2 * t], 1);
+                mbar_init(&bars[B_PV_DONE + 2 * t + 1], 1);
+                mbar_init(&bars[B_O_DONE + t], 1);
+            }
+            for (int i = 0; i < 2 * kQTilesPerCta; ++i) mbar_init(&bars[B_DRAIN + i], 1);
+            fence_mbar_init();
+            // the Q tiles do not depend on the key range: start them before it is computed
+            prefetch_tmap(&tm_q);
+            const int32_t qy = LSE ? (kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row0) * g
+                                   : (kvh * L[L_TOTAL_ROWS] + row_base + row0) * g;
+            mbar_arrive_expect_tx(&bars[B_Q_FULL], kQTilesPerCta * SM::kQ);
+            for (int t = 0; t < kQTilesPerCta; ++t)
+                for (int hb = 0; hb < H; ++hb)
+                    tma_load_2d(sQ(t) + hb * 16384, &tm_q, &bars[B_Q_FULL], hb * 64, qy + t * kTileRows);
         }
-        for (int i = 0; i < 2 * kQTilesPerCta; ++i) mbar_init(&bars[B_DRAIN + i], 1);
-        fence_mbar_init();
-        int nct, nft = 0, t0 = 0;
+        int nct = 0, nft = 0, t0 = 0;
         const int nkt = R[R_N_KTILES];
         if (LSE) {
             const int chunks = R[R_LSE_CHUNKS];
@@ -175,21 +186,28 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             t0 = chunk * tpc;
             nct = max(0, min(tpc, nkt - t0));
         } else {
+            // visible tiles: key positions increase along the cached tiles and along the fresh rows,
+            // so each count is the number of tiles whose first key is at or before the CTA's last
+            // row (the lanes test 32 tiles at a time)
             const int32_t pmax = nrow_cta > 0 ? prm.row_pos[row_base + row0 + nrow_cta - 1] : -1;
-            nct = 0;
-            while (nct < nkt && page_pos[nct * kPagesPerTile] <= pmax) ++nct;
             const int nft_total = (n_rows_req + kTileKeys - 1) / kTileKeys;
-            while (nft < nft_total && prm.row_pos[row_base + nft * kTileKeys] <= pmax) ++nft;
+            for (int b = 0; b < nkt; b += 32)
+                nct += __popc(__ballot_sync(0xffffffffu, b + lane < nkt && page_pos[(b + lane) * kPagesPerTile] <= pmax));
+            for (int b = 0; b < nft_total; b += 32)
+                nft += __popc(__ballot_sync(0xffffffffu, b + lane < nft_total &&
+                                                             prm.row_pos[row_base + (b + lane) * kTileKeys] <= pmax));
         }
-        misc[1] = nct;
-        misc[2] = nft;
-        misc[3] = t0;
-        misc[4] = 0;
-        const int n_all = nct + nft;
-        const int ns = LSE ? 1 : PR[P_NSPLIT];
-        const int sp = LSE ? 0 : chunk;
-        misc[5] = (int)(((int64_t)sp * n_all) / ns);
-        misc[6] = (int)(((int64_t)(sp + 1) * n_all) / ns);
+        if (lane == 0) {
+            misc[1] = nct;
+            misc[2] = nft;
+            misc[3] = t0;
+            misc[4] = 0;
+            const int n_all = nct + nft;
+            const int ns = LSE ? 1 : PR[P_NSPLIT];
+            const int sp = LSE ? 0 : chunk;
+            misc[5] = (int)(((int64_t)sp * n_all) / ns);
+            misc[6] = (int)(((int64_t)(sp + 1) * n_all) / ns);
+        }
     }
     if (warp == kWarpMma) {
         tmem_alloc(reinterpret_cast<uint32_t*>(misc), SM::kTmemCols);
@@ -219,20 +237,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ K producer
-        // Per tile: lane l writes the key info of keys l, l+32, l+64, l+96 (logical position, or
+        // (The Q tiles were started by warp 0 during set-up.)  Per tile: lane l writes the key info of keys l, l+32, l+64, l+96 (logical position, or
         // kNoPos for a missing key; bias 0 or -30000), fetched one tile ahead; lane 0 then issues
         // the rotated K tile.  The stage is reused once both Q K^T have read it and both softmax
         // groups have read its key positions.
         if (lane == 0) {
-            prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_kcache);
             if (!LSE) prefetch_tmap(&tm_kfresh);
-            const int32_t qy = LSE ? (kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row0) * g
-                                   : (kvh * L[L_TOTAL_ROWS] + row_base + row0) * g;
-            mbar_arrive_expect_tx(&bars[B_Q_FULL], kQTilesPerCta * SM::kQ);
-            for (int t = 0; t < kQTilesPerCta; ++t)
-                for (int hb = 0; hb < H; ++hb)
-                    tma_load_2d(sQ(t) + hb * 16384, &tm_q, &bars[B_Q_FULL], hb * 64, qy + t * kTileRows);
         }
         // key info of key (lane + 32 r) of tile j: logical position (kNoPos if missing) and whether
         // it takes part (cached: page present and token not recomputed; fresh: row present)
@@ -560,13 +571,17 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 if (valid) {
                     const float2* ml = prm.lse_part + R[R_LSE_BASE] +
                                        ((int64_t)kvh * (R[R_N_QUERY] * g) + row * g + hl) * chunks;
+                    // all chunks are loaded at once (chunks <= kMaxSplits), then combined in order
+                    float2 v[kMaxSplits];
+#pragma unroll
+                    for (int c = 0; c < kMaxSplits; ++c) v[c] = c < chunks ? __ldcg(ml + c) : make_float2(-INFINITY, 0.f);
                     float M = -INFINITY;
-                    for (int c = 0; c < chunks; ++c) M = fmaxf(M, __ldcg(&ml[c].x));
+#pragma unroll
+                    for (int c = 0; c < kMaxSplits; ++c) M = fmaxf(M, v[c].x);
                     float S = 0.f;
-                    for (int c = 0; c < chunks; ++c) {
-                        const float2 v = __ldcg(ml + c);
-                        S += v.y * ex2(v.x - M);
-                    }
+#pragma unroll
+                    for (int c = 0; c < kMaxSplits; ++c)
+                        if (c < chunks) S += v[c].y * ex2(v[c].x - M);
                     prm.lse_final[((int64_t)kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row) * g + hl] =
                         S > 0.f ? M + log2f(S) : INFINITY;
                 }

@@ -17,17 +17,20 @@
 // works on the next (tile, chunk) step while the exponentials of the current one run.  The
 // per-kv-head partial sums of a run are reduced in fixed head order by the last CTA of the run
 // (deterministic).
-//   warps 0-3  exp-sum (one key per thread)
-//   warp  4    TMEM allocation + single-thread tcgen05.mma issue
-//   warp  5    TMA producer (key tiles, query chunks)
+//   warps 0-7  exp-sum: warp w owns keys 32(w%4) .. +31 (its TMEM lane quarter) and the query
+//              columns 128(w/4) .. +127 of every step; the two column halves of a key are added
+//              through shared memory at the end of each tile
+//   warp  8    TMEM allocation + single-thread tcgen05.mma issue
+//   warp  9    TMA producer (key tiles, query chunks)
 #pragma once
 #include "kernel_attn.cuh"
 
 namespace pcf {
 
-constexpr int kImpThreads = 192;
-constexpr int kImpWarpMma = 4;
-constexpr int kImpWarpTma = 5;
+constexpr int kImpThreads = 320;
+constexpr int kImpExpThreads = 256;
+constexpr int kImpWarpMma = 8;
+constexpr int kImpWarpTma = 9;
 constexpr int kImpQRows = 256;
 
 struct ImpParams {
@@ -49,7 +52,8 @@ struct ImpSmem {
     static constexpr int kSlabK = kTileKeys * 16 * 2;  // [128][16] fp16: ones in columns 0 and 1
     static constexpr int oQlse = oQ + 2 * kQ;          // 2 slabs (one per query-chunk buffer)
     static constexpr int oKones = oQlse + 2 * kSlabQ;
-    static constexpr int oBar = oKones + kSlabK;
+    static constexpr int oPart = oKones + kSlabK;      // [128] second column half of each key
+    static constexpr int oBar = oPart + kTileKeys * 4;
     static constexpr int kNumBars = 16;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int kBytes = oMisc + 64;
@@ -60,7 +64,7 @@ struct ImpSmem {
 enum : int { I_K_FULL = 0 /*2*/, I_K_EMPTY = 2 /*2*/, I_Q_FULL = 4 /*2*/, I_Q_EMPTY = 6 /*2*/,
              I_ACC_FULL = 8 /*2*/, I_ACC_FREE = 10 /*2*/, I_LSE_FULL = 12 /*2*/, I_DRAIN = 14 };
 
-__device__ __forceinline__ void named_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void named_sync_exp() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 template <int D>
 __global__ void __launch_bounds__(kImpThreads, 1)
@@ -97,8 +101,8 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             mbar_init(&bars[I_Q_FULL + b], 1);
             mbar_init(&bars[I_Q_EMPTY + b], 1);
             mbar_init(&bars[I_ACC_FULL + b], 1);
-            mbar_init(&bars[I_ACC_FREE + b], 128);
-            mbar_init(&bars[I_LSE_FULL + b], 128);
+            mbar_init(&bars[I_ACC_FREE + b], kImpExpThreads);
+            mbar_init(&bars[I_LSE_FULL + b], kImpExpThreads);
         }
         mbar_init(&bars[I_DRAIN], 1);
         fence_mbar_init();
@@ -186,22 +190,22 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             mbar_drain(&bars[I_DRAIN], 0);
         }
     } else {
-        // warps 0-3: thread tid owns key tid of every tile of the run
+        // warps 0-7: thread owns key `key` of every tile of the run, query columns ch*128 .. +127
+        const int key = tid & 127, ch = tid >> 7;
+        float* sPart = reinterpret_cast<float*>(smem + SM::oPart);
         const float* lse_g = prm.lse_final + ((int64_t)kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE]) * g;
-        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         const int total_tokens = L[L_TOTAL_TOKENS];
         // -lse2 of step s's query chunk into its slab, as fp16 hi + lo (-30000 past the last row:
-        // those columns contribute 0)
+        // those columns contribute 0); thread tid writes row tid
         auto prep = [&](int s) {
             const int qc = s % n_qc;
             uint8_t* slab = sQlse(q_resident ? 0 : (s & 1));
-            for (int rr = tid; rr < kImpQRows; rr += 128) {
-                const int n = qc * kImpQRows + rr;
-                const float v = n < n_q ? -__ldcg(lse_g + n) : -30000.f;
-                const __half hi = __float2half_rn(v);
-                *reinterpret_cast<__half*>(slab + slab16_off(rr, 0)) = hi;
-                *reinterpret_cast<__half*>(slab + slab16_off(rr, 1)) = __float2half_rn(v - __half2float(hi));
-            }
+            const int n = qc * kImpQRows + tid;
+            const float v = n < n_q ? -__ldcg(lse_g + n) : -30000.f;
+            const __half hi = __float2half_rn(v);
+            *reinterpret_cast<__half*>(slab + slab16_off(tid, 0)) = hi;
+            *reinterpret_cast<__half*>(slab + slab16_off(tid, 1)) = __float2half_rn(v - __half2float(hi));
             fence_proxy_async_smem();
             mbar_arrive(&bars[I_LSE_FULL + (q_resident ? 0 : (s & 1))]);
         };
@@ -209,53 +213,58 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (!q_resident && n_steps > 1) prep(1);
         bool ok = true;
         float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        // every one of the 256 threads runs every step (a named barrier at each tile end): after an
+        // abort the work is skipped, the barrier count stays the same
         for (int s = 0; s < n_steps; ++s) {
             const int i = s / n_qc, qc = s - i * n_qc, a = s & 1;
             if (ok) ok = mbar_wait(&bars[I_ACC_FULL + a], (s >> 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t sv[4][32];
+                uint32_t sv[4][32];
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-                        tmem_ld32(tmem + lane_addr + a * kImpQRows + half * 128 + cc * 32, sv[cc]);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) acc4[e & 3] += ex2(__uint_as_float(sv[cc][e]));
-                }
+                for (int cc = 0; cc < 4; ++cc)
+                    tmem_ld32(tmem + lane_addr + a * kImpQRows + ch * 128 + cc * 32, sv[cc]);
+                tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(&bars[I_ACC_FREE + a]);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc4[e & 3] += ex2(__uint_as_float(sv[cc][e]));
                 // step s's MMA is complete, so its slab buffer takes step s + 2's chunk
                 if (!q_resident && s + 2 < n_steps) prep(s + 2);
             }
             if (qc == n_qc - 1) {
-                const int t = t0 + i;
-                const bool valid_key = (t * kPagesPerTile + tid / kPage) < n_pages;
-                const int32_t tok = R[R_TOK_BASE] + t * kTileKeys + tid;
-                if (ok && valid_key) prm.part[(int64_t)kvh * total_tokens + tok] = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+                const float accv = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
                 acc4[0] = acc4[1] = acc4[2] = acc4[3] = 0.f;
+                if (ch == 1) sPart[key] = accv;
+                named_sync_exp();
+                if (ch == 0) {
+                    const int t = t0 + i;
+                    const bool valid_key = (t * kPagesPerTile + key / kPage) < n_pages;
+                    const int32_t tok = R[R_TOK_BASE] + t * kTileKeys + key;
+                    if (ok && valid_key) prm.part[(int64_t)kvh * total_tokens + tok] = accv + sPart[key];
+                }
+                named_sync_exp();   // sPart is reused by the next tile
             }
         }
-        if (n_qc == 0)   // a request without query rows: every importance is 0
+        if (n_qc == 0 && ch == 0)   // a request without query rows: every importance is 0
             for (int i = 0; i < nt; ++i)
-                if (((t0 + i) * kPagesPerTile + tid / kPage) < n_pages)
-                    prm.part[(int64_t)kvh * total_tokens + R[R_TOK_BASE] + (t0 + i) * kTileKeys + tid] = 0.f;
+                if (((t0 + i) * kPagesPerTile + key / kPage) < n_pages)
+                    prm.part[(int64_t)kvh * total_tokens + R[R_TOK_BASE] + (t0 + i) * kTileKeys + key] = 0.f;
         // the last of the run's Hkv CTAs sums the heads in order
         __threadfence();
-        named_sync_128();
+        named_sync_exp();
         const int cidx = R[R_KTILE_BASE] + t0;
         if (tid == 0) misc[5] = (atomicAdd(&prm.counters[cidx], 1) == Hkv - 1) ? 1 : 0;
-        named_sync_128();
+        named_sync_exp();
         if (misc[5]) {
             __threadfence();
-            for (int i = 0; i < nt; ++i) {
-                const int t = t0 + i;
-                if ((t * kPagesPerTile + tid / kPage) >= n_pages) continue;
-                const int32_t tok = R[R_TOK_BASE] + t * kTileKeys + tid;
+            for (int idx = tid; idx < nt * kTileKeys; idx += kImpExpThreads) {
+                const int t = t0 + idx / kTileKeys, k = idx % kTileKeys;
+                if ((t * kPagesPerTile + k / kPage) >= n_pages) continue;
+                const int32_t tok = R[R_TOK_BASE] + t * kTileKeys + k;
                 float sum = 0.f;
                 for (int h = 0; h < Hkv; ++h) sum += __ldcg(prm.part + (int64_t)h * total_tokens + tok);
                 prm.importance[tok] = sum;

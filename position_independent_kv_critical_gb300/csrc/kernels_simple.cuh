@@ -269,7 +269,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
 // ------------------------------------------------------------------ split-range combine
 // A (request, kv head, tile pair) whose key range was split over P_NSPLIT CTAs left, per split s,
 // a normalized partial row O_s = (sum_u p_u v_u) / l_s together with (m_s, l_s) (running max in log2
-// units, running sum).  The full row is sum_s w_s O_s / sum_s w_s with w_s = l_s 2^(m_s - max m).
+// units, running sum).  The full row is sum_s w_s O_s / sum_s w_s with w_s = l_s 2^(m_s - max m),
+// accumulated in one pass in split order (the running max rescales what was summed so far), so
+// that the loads of several splits are in flight together.
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict__ L,
                                                       const __nv_bfloat16* __restrict__ part_o,
@@ -291,22 +293,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict_
     if (row >= R[R_N_ROWS]) return;
     const int64_t slot0 = (int64_t)PR[P_SLOT_BASE] + (int64_t)kvh * ns;
     const int64_t stride = kQTilesPerCta * kTileRows;
-    float M = -INFINITY;
-    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, part_ml[(slot0 + sp) * stride + pr].x);
+    float M = -INFINITY, W = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float W = 0.f;
+#pragma unroll 4
     for (int sp = 0; sp < ns; ++sp) {
         const float2 ml = part_ml[(slot0 + sp) * stride + pr];
-        if (ml.x == -INFINITY || ml.y <= 0.f) continue;
-        const float w = ml.y * ex2(ml.x - M);
-        W += w;
         const uint4 v = *reinterpret_cast<const uint4*>(part_o + ((slot0 + sp) * stride + pr) * D + 8 * c);
+        const bool live = ml.x != -INFINITY && ml.y > 0.f;
+        const float m_new = live ? fmaxf(M, ml.x) : M;
+        const float scale = m_new == M ? 1.f : ex2(M - m_new);
+        const float w = live ? ml.y * ex2(ml.x - m_new) : 0.f;
+        W = W * scale + w;
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            acc[2 * e] += w * bf16_lo(u[e]);
-            acc[2 * e + 1] += w * bf16_hi(u[e]);
+            acc[2 * e] = acc[2 * e] * scale + w * bf16_lo(u[e]);
+            acc[2 * e + 1] = acc[2 * e + 1] * scale + w * bf16_hi(u[e]);
         }
+        M = m_new;
     }
     const float inv = W > 0.f ? 1.f / W : 0.f;
     uint4 o;

@@ -137,8 +137,9 @@ pcf_status launch_rope(RopeJob a, RopeJob b, RopeJob c, const float2* rope, int3
     const int64_t n_a = a.x ? (int64_t)a.n_rows * a.heads * (D / 16) : 0;
     const int64_t n_b = b.x ? (int64_t)b.n_rows * b.heads * (D / 16) : 0;
     const int64_t n_c = c.x ? (int64_t)c.n_rows * c.heads * (D / 16) : 0;
-    if (n_a + n_b + n_c == 0) return PCF_OK;
-    const int64_t blocks = (n_a + n_b + n_c + 255) / 256;
+    const int64_t n = n_a + n_b + n_c;
+    if (n == 0) return PCF_OK;
+    const int64_t blocks = (n + 255) / 256;
     rope_rows_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(a, b, c, rope, max_pos, n_a, n_a + n_b);
     return launched();
 }

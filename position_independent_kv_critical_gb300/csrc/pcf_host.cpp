@@ -92,7 +92,7 @@ double lpt_makespan(std::vector<double>& costs) {
 // and any split adds `combine` tiles (the merge of the partial results).  Batches with enough
 // units to fill the GPU several times are not split.
 void choose_splits(const std::vector<int32_t>& tiles, int32_t copies, double overhead, double combine,
-                   std::vector<int32_t>* splits) {
+                   int32_t max_split, std::vector<int32_t>* splits) {
     splits->assign(tiles.size(), 1);
     if (tiles.empty() || (int64_t)tiles.size() * copies >= 4 * kNumSms) return;
     int32_t max_t = 1;
@@ -104,7 +104,7 @@ void choose_splits(const std::vector<int32_t>& tiles, int32_t copies, double ove
         costs.clear();
         bool any = false;
         for (int32_t t : tiles) {
-            const int32_t sp = std::max(1, std::min({cdiv(t, c), kMaxSplits, t}));
+            const int32_t sp = std::max(1, std::min({cdiv(t, c), max_split, t}));
             any = any || sp > 1;
             costs.insert(costs.end(), (size_t)copies * sp, overhead + (double)t / sp);
         }
@@ -115,13 +115,14 @@ void choose_splits(const std::vector<int32_t>& tiles, int32_t copies, double ove
         }
     }
     for (size_t i = 0; i < tiles.size(); ++i)
-        (*splits)[i] = std::max(1, std::min({cdiv(tiles[i], best_c), kMaxSplits, tiles[i]}));
+        (*splits)[i] = std::max(1, std::min({cdiv(tiles[i], best_c), max_split, tiles[i]}));
 }
 
 // Prologue + epilogue of an attention CTA in key tiles, and of the merge of split results.
 constexpr double kAttnCtaOverhead = 1.5;
 constexpr double kAttnCombineCost = 2.0;
 constexpr double kLseCtaOverhead = 2.0;
+constexpr double kImpCtaOverhead = 1.0;
 
 pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims* dims, Plan* plan) {
     if (!reqs || !dims || n_reqs < 1 || n_reqs > (1 << 20)) return PCF_ERR_INVALID_ARG;
@@ -213,7 +214,7 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
             plan->pair_tiles.push_back(nct + (int32_t)(last / kTileKeys) + 1);
         }
     }
-    choose_splits(plan->pair_tiles, d.n_kv_heads, kAttnCtaOverhead, kAttnCombineCost, &plan->pair_split);
+    choose_splits(plan->pair_tiles, d.n_kv_heads, kAttnCtaOverhead, kAttnCombineCost, kMaxSplits, &plan->pair_split);
     // LSE pass: units (request, query tile pair) over all cached tiles, split into key chunks
     std::vector<int32_t> lse_split;
     {
@@ -227,7 +228,7 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
                 for (int32_t p = 0; p < cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta); ++p) tiles.push_back(nkt);
         }
         std::vector<int32_t> sp;
-        choose_splits(tiles, d.n_kv_heads, kLseCtaOverhead, 0.0, &sp);
+        choose_splits(tiles, d.n_kv_heads, kLseCtaOverhead, 0.0, kMaxSplits, &sp);
         size_t u = 0;
         for (int b = 0; b < n_reqs; ++b) {
             const pcf_request_desc& r = reqs[b];
@@ -244,8 +245,20 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
     }
     plan->lse_chunks.assign(n_reqs, 0);
     int64_t n_attn = 0, n_lse = 0, n_imp = 0, slots = 0, n_comb = 0, attn_slots = 0, n_lse_pairs = 0;
-    // importance pass: CTAs over runs of key tiles of one kv head, about two CTAs per SM in total
-    plan->imp_tiles = (int32_t)std::max<int64_t>(1, (tot_kt * d.n_kv_heads) / (2 * kNumSms));
+    // importance pass: CTAs over runs of key tiles of one kv head; run lengths by the same
+    // estimate as the attention splits (a CTA costs about one step more than its tiles)
+    {
+        std::vector<int32_t> tiles, sp;
+        for (int b = 0; b < n_reqs; ++b) {
+            int64_t n_pg = 0;
+            for (int s = 0; s < reqs[b].n_spans; ++s) n_pg += reqs[b].spans[s].n_pages;
+            if (n_pg > 0) tiles.push_back(cdiv(n_pg, kPagesPerTile));
+        }
+        choose_splits(tiles, d.n_kv_heads, kImpCtaOverhead, 0.0, 1 << 20, &sp);
+        int32_t run = 1;
+        for (size_t u = 0; u < tiles.size(); ++u) run = std::max(run, cdiv(tiles[u], sp[u]));
+        plan->imp_tiles = run;
+    }
     for (int b = 0; b < n_reqs; ++b) {
         const pcf_request_desc& r = reqs[b];
         int64_t n_tok = 0;
@@ -365,8 +378,8 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
     attn.reserve(plan.n_attn);
     int32_t* LSE = blob + H[L_OFF_LSE];
     int32_t* IMP = blob + H[L_OFF_IMP];
-    int32_t* COMB = blob + H[L_OFF_COMB];
     int32_t* PAIR = blob + H[L_OFF_PAIR];
+    int32_t* COMB = blob + H[L_OFF_COMB];
     int64_t n_lse = 0, n_imp = 0, n_comb = 0;
     int32_t slot_base = 0;
 
