@@ -22,20 +22,21 @@
 //               Four single-thread issuers keep four independent MMA streams in flight: one
 //               thread's stream of 128-row MMAs with N <= 128 is bound by per-instruction
 //               latency, not by the tensor core's rate
-//   warp  9     K producer: rotated K tiles (cached or fresh, fp16, TMA) and, per key,
-//               its logical position and bias; 2-stage ring, freed by the second half's Q K^T
+//   warp  9     K producer: rotated K tiles (compacted cached or fresh, fp16, TMA) and, per
+//               key, its logical position; 2-stage ring, freed by the second half's Q K^T
 //   (warp 0 starts the Q tile loads during set-up)
-//   warp  10    V producer (TMA): cached V pages through the block table / fresh V tiles; 2-stage
-//               ring, freed once both P V of a stage are done
+//   warp  10    V producer (TMA): compacted cached V tiles / fresh V tiles; 2-stage ring, freed
+//               once both P V of a stage are done
 // TMEM: tile t's two S half-buffers at columns t*128 + {0, 64} (64 fp32 columns = 64 keys each),
 // O_A at [256,256+d), O_B at [384,384+d).  S = Q K^T is fp16 x fp16 (M=128, N=64 keys, K=d); P
 // (bf16 pairs, 32 columns) overwrites the S half it came from and is the A operand of
 // O += P V (M=128, N=d in one instruction, K=64 keys, V as an MN-major bf16 operand whose two
 // 64-wide halves are 16 KB apart).
-// Keys that do not take part (recomputed tokens' cached copies, missing pages or rows) are
-// removed by the tensor core itself: Q K^T gets one more K=16 step whose A slab is a column of
-// ones and whose B slab carries 0 or -30000 per key, so their scores (log2 units) underflow to
-// P = 0; only rows whose causal limit falls inside a tile need per-element masking.
+// The cached keys arrive compacted: recomputed tokens' cached copies are left out of the rotated
+// K/V copy, so every cached key streamed takes part.  Key positions increase along the cached
+// keys and along the fresh rows, and missing keys (past a ragged end) carry position kNoPos, so a
+// row's visible keys in a tile are a prefix of it; only rows whose causal limit falls inside a
+// tile need per-element masking.
 // LSE mode (critical-layer scoring, pass 1) runs the same pipeline without P/V and writes the
 // per-row running max and sum of one key chunk.
 #pragma once
@@ -56,12 +57,10 @@ constexpr int kNoPos = 0x7FFFFFFF;
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr uint32_t kTmemO = 256;     // O_A at 256, O_B at 384
-constexpr int kSlab16 = kTileRows * 16 * 2;   // one [128][16] fp16 bias slab
-constexpr float kKeyOff = -30000.f;           // bias of a key that does not take part
 
 struct AttnParams {
     const int32_t* layout;
-    const uint16_t* excl;      // attention: per logical page exclusion bits
+    const int32_t* kpos_c;     // attention: logical position of every compacted cached key
     const int32_t* row_pos;    // attention: logical position of every row
     __nv_bfloat16* out;        // attention: [rows][Hq][D]
     float2* lse_part;          // LSE: (running max in log2 units, running sum) per row and chunk
@@ -81,9 +80,7 @@ struct AttnSmem {
     static constexpr int oK = oQ + kQTilesPerCta * kQ;
     static constexpr int oV = oK + kKStages * kK;
     static constexpr int oKpos = oV + kVStages * kV;
-    static constexpr int oQaug = oKpos + kKStages * kTileKeys * 4;   // ones column (1024-aligned)
-    static constexpr int oKaug = oQaug + kSlab16;                    // per K stage: key bias column
-    static constexpr int oBar = oKaug + kKStages * kSlab16;
+    static constexpr int oBar = oKpos + kKStages * kTileKeys * 4;
     static constexpr int kNumBars = 30;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int kBytes = oMisc + 64;
@@ -110,7 +107,7 @@ enum : int {
 template <int D, bool LSE>
 __global__ void __launch_bounds__(kAttnThreads)
 attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kcache,
-            const __grid_constant__ CUtensorMap tm_vpool, const __grid_constant__ CUtensorMap tm_kfresh,
+            const __grid_constant__ CUtensorMap tm_vcache, const __grid_constant__ CUtensorMap tm_kfresh,
             const __grid_constant__ CUtensorMap tm_vfresh, const AttnParams prm) {
     using SM = AttnSmem<D, LSE>;
     constexpr int H = SM::kHalves;
@@ -120,8 +117,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     auto sKs = [&](int st) { return smem + SM::oK + st * SM::kK; };
     auto sVs = [&](int st) { return smem + SM::oV + st * SM::kV; };
     auto sKpos = [&](int st) { return reinterpret_cast<int32_t*>(smem + SM::oKpos) + st * kTileKeys; };
-    uint8_t* sQaug = smem + SM::oQaug;
-    auto sKaug = [&](int st) { return smem + SM::oKaug + st * kSlab16; };
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::oBar);
     int32_t* misc = reinterpret_cast<int32_t*>(smem + SM::oMisc);
     // misc: [0] tmem base, [1] n cached tiles, [2] n fresh tiles, [3] first cached tile, [4] abort,
@@ -144,7 +139,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int32_t page_base = R[R_PAGE_BASE];
     const int32_t row_base = R[R_ROW_BASE];
     const int32_t* page_pos = L + L[L_OFF_PAGEPOS] + page_base;
-    const int32_t* blk = L + L[L_OFF_BLOCK] + page_base;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -179,7 +173,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     tma_load_2d(sQ(t) + hb * 16384, &tm_q, &bars[B_Q_FULL], hb * 64, qy + t * kTileRows);
         }
         int nct = 0, nft = 0, t0 = 0;
-        const int nkt = R[R_N_KTILES];
+        // LSE: tiles of all the request's cached tokens; attention: tiles of the compacted ones
+        const int nkt = LSE ? R[R_N_KTILES] : (n_pages * kPage - R[R_N_SEL] + kTileKeys - 1) / kTileKeys;
         if (LSE) {
             const int chunks = R[R_LSE_CHUNKS];
             const int tpc = (nkt + chunks - 1) / chunks;
@@ -191,8 +186,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             // row (the lanes test 32 tiles at a time)
             const int32_t pmax = nrow_cta > 0 ? prm.row_pos[row_base + row0 + nrow_cta - 1] : -1;
             const int nft_total = (n_rows_req + kTileKeys - 1) / kTileKeys;
+            const int32_t* kpc = prm.kpos_c + R[R_CBASE];
             for (int b = 0; b < nkt; b += 32)
-                nct += __popc(__ballot_sync(0xffffffffu, b + lane < nkt && page_pos[(b + lane) * kPagesPerTile] <= pmax));
+                nct += __popc(__ballot_sync(0xffffffffu, b + lane < nkt && kpc[(b + lane) * kTileKeys] <= pmax));
             for (int b = 0; b < nft_total; b += 32)
                 nft += __popc(__ballot_sync(0xffffffffu, b + lane < nft_total &&
                                                              prm.row_pos[row_base + (b + lane) * kTileKeys] <= pmax));
@@ -213,19 +209,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tmem_alloc(reinterpret_cast<uint32_t*>(misc), SM::kTmemCols);
         tmem_relinquish();
     }
-    // V stages start finite (keys masked to P = 0 then contribute 0 * V); bias slabs start at 0
-    // with a column of ones on the query side
-    if (!LSE) {
-        uint4* z = reinterpret_cast<uint4*>(smem + SM::oV);
-        for (int i = tid; i < (kVStages * SM::kV) / 16; i += kAttnThreads) z[i] = make_uint4(0, 0, 0, 0);
-    }
-    {
-        uint4* z = reinterpret_cast<uint4*>(sQaug);
-        for (int i = tid; i < ((1 + kKStages) * kSlab16) / 16; i += kAttnThreads) z[i] = make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();
-    if (tid < kTileRows) *reinterpret_cast<__half*>(sQaug + slab16_off(tid, 0)) = __float2half(1.0f);
-    fence_proxy_async_smem();
+    // (every K and V stage is filled by whole-tile copies: rows past a tensor's end read as 0)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -233,63 +217,55 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int n_ct = misc[1], n_ft = misc[2], t0 = misc[3];
     const int n_tiles = n_ct + n_ft;
     const int jb = misc[5], n_loc = misc[6] - misc[5];   // tiles jb .. jb+n_loc-1 of the visible range
-    const int n_phys = L[L_N_PHYS];
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ K producer
-        // (The Q tiles were started by warp 0 during set-up.)  Per tile: lane l writes the key info of keys l, l+32, l+64, l+96 (logical position, or
-        // kNoPos for a missing key; bias 0 or -30000), fetched one tile ahead; lane 0 then issues
-        // the rotated K tile.  The stage is reused once both Q K^T have read it and both softmax
-        // groups have read its key positions.
+        // (The Q tiles were started by warp 0 during set-up.)  Per tile: lane l writes the
+        // positions of keys l, l+32, l+64, l+96 (kNoPos for a missing key), fetched one tile ahead;
+        // lane 0 then issues the rotated K tile.  The stage is reused once both Q K^T have read it
+        // and both softmax groups have read its key positions.
         if (lane == 0) {
             prefetch_tmap(&tm_kcache);
             if (!LSE) prefetch_tmap(&tm_kfresh);
         }
-        // key info of key (lane + 32 r) of tile j: logical position (kNoPos if missing) and whether
-        // it takes part (cached: page present and token not recomputed; fresh: row present)
-        auto meta = [&](int j, int32_t (&pos)[4], uint32_t& valid) {
-            valid = 0;
+        // logical position of key (lane + 32 r) of tile j (kNoPos if missing): LSE mode, every
+        // cached token; attention, the compacted cached keys, then the fresh rows
+        const int n_kept = n_pages * kPage - R[R_N_SEL];
+        auto meta = [&](int j, int32_t (&pos)[4]) {
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int key = lane + 32 * r;
                 pos[r] = kNoPos;
                 if (j < n_ct) {
-                    const int lp = (t0 + j) * kPagesPerTile + key / kPage;
-                    if (lp < n_pages) {
-                        pos[r] = page_pos[lp] + key % kPage;
-                        const uint32_t ex = LSE ? 0u : (uint32_t)prm.excl[page_base + lp];
-                        if (((ex >> (key % kPage)) & 1u) == 0u) valid |= 1u << r;
+                    if (LSE) {
+                        const int lp = (t0 + j) * kPagesPerTile + key / kPage;
+                        if (lp < n_pages) pos[r] = page_pos[lp] + key % kPage;
+                    } else {
+                        const int ci = j * kTileKeys + key;
+                        if (ci < n_kept) pos[r] = prm.kpos_c[R[R_CBASE] + ci];
                     }
                 } else if (j < n_tiles) {
                     const int fr = (j - n_ct) * kTileKeys + key;
-                    if (fr < n_rows_req) { pos[r] = prm.row_pos[row_base + fr]; valid |= 1u << r; }
+                    if (fr < n_rows_req) pos[r] = prm.row_pos[row_base + fr];
                 }
             }
         };
-        const int32_t kc_row0 = kvh * L[L_TOTAL_TOKENS] + R[R_TOK_BASE];
+        const int32_t kc_row0 = LSE ? kvh * L[L_TOTAL_TOKENS] + R[R_TOK_BASE] : kvh * L[L_TOTAL_VALID] + R[R_CBASE];
         int32_t pos_n[4];
-        uint32_t val_n;
-        meta(jb, pos_n, val_n);
+        meta(jb, pos_n);
         int last[kKStages] = {-1, -1};
         for (int jj = 0; jj < n_loc; ++jj) {
             const int j = jb + jj, ks = jj & 1;
             int32_t pos[4];
 #pragma unroll
             for (int r = 0; r < 4; ++r) pos[r] = pos_n[r];
-            const uint32_t val = val_n;
-            meta(j + 1, pos_n, val_n);
+            meta(j + 1, pos_n);
             const bool ok = jj < kKStages ||
                             (mbar_wait(&bars[B_K_EMPTY + ks], ((jj >> 1) - 1) & 1, abort_flag) &&
                              mbar_wait(&bars[B_KPOS_FREE + ks], ((jj >> 1) - 1) & 1, abort_flag));
             if (!__all_sync(0xffffffffu, ok)) break;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int key = lane + 32 * r;
-                sKpos(ks)[key] = pos[r];
-                *reinterpret_cast<__half*>(sKaug(ks) + slab16_off(key, 0)) =
-                    __float2half(((val >> r) & 1u) ? 0.f : kKeyOff);
-            }
-            fence_proxy_async_smem();   // the bias slab is read by the tensor core
+            for (int r = 0; r < 4; ++r) sKpos(ks)[lane + 32 * r] = pos[r];
             uint64_t* full = &bars[B_K_FULL + ks];
             if (lane != 0) {
                 mbar_arrive(full);
@@ -312,49 +288,27 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
     } else if (warp == kWarpTmaV) {
         // ------------------------------------------------------------ V producer
-        if (!LSE) {
-            if (lane == 0) {
-                prefetch_tmap(&tm_vpool);
-                prefetch_tmap(&tm_vfresh);
-            }
-            auto meta = [&](int j) -> int32_t {
-                if (j < n_ct && lane < kPagesPerTile) {
-                    const int lp = (t0 + j) * kPagesPerTile + lane;
-                    if (lp < n_pages) return blk[lp];
-                }
-                return -1;
-            };
-            int32_t ph_next = meta(jb);
+        if (!LSE && lane == 0) {
+            prefetch_tmap(&tm_vcache);
+            prefetch_tmap(&tm_vfresh);
             int last[kVStages] = {-1, -1};
             for (int jj = 0; jj < n_loc; ++jj) {
                 const int j = jb + jj, vs = jj & 1;
-                int32_t ph = ph_next;
-                ph_next = meta(j + 1);
-                const bool ok = jj < kVStages || mbar_wait(&bars[B_V_EMPTY + vs], ((jj >> 1) - 1) & 1, abort_flag);
-                if (!__all_sync(0xffffffffu, ok)) break;
+                if (jj >= kVStages && !mbar_wait(&bars[B_V_EMPTY + vs], ((jj >> 1) - 1) & 1, abort_flag)) break;
                 uint64_t* full = &bars[B_V_FULL + vs];
+                mbar_arrive_expect_tx(full, H * 16384);
                 if (j < n_ct) {
-                    const int np = min(kPagesPerTile, n_pages - (t0 + j) * kPagesPerTile);
-                    if (lane == 0) mbar_arrive_expect_tx(full, H * 2048 * np);
-                    __syncwarp();
-                    if (lane < np) {
-                        if (ph < 0 || ph >= n_phys) { set_dev_error(kDevErrBounds); ph = 0; }
-                        const int32_t y = (ph * Hkv + kvh) * kPage;
-#pragma unroll
-                        for (int hb = 0; hb < H; ++hb)
-                            tma_load_2d(sVs(vs) + hb * 16384 + lane * 2048, &tm_vpool, full, hb * 64, y);
-                    }
-                } else if (lane == 0) {
+                    const int32_t y = kvh * L[L_TOTAL_VALID] + R[R_CBASE] + j * kTileKeys;
+                    for (int hb = 0; hb < H; ++hb) tma_load_2d(sVs(vs) + hb * 16384, &tm_vcache, full, hb * 64, y);
+                } else {
                     const int32_t fr = row_base + (j - n_ct) * kTileKeys;
-                    mbar_arrive_expect_tx(full, H * 16384);
                     for (int hb = 0; hb < H; ++hb)
                         tma_load_3d(sVs(vs) + hb * 16384, &tm_vfresh, full, hb * 64, kvh, fr);
                 }
                 last[vs] = jj;
             }
-            if (lane == 0)
-                for (int s2 = 0; s2 < kVStages; ++s2)
-                    if (last[s2] >= 0) mbar_drain(&bars[B_V_FULL + s2], (last[s2] >> 1) & 1);
+            for (int s2 = 0; s2 < kVStages; ++s2)
+                if (last[s2] >= 0) mbar_drain(&bars[B_V_FULL + s2], (last[s2] >> 1) & 1);
         }
     } else if (warp == kWarpMma || warp == kWarpMmaB || warp == kWarpPvA || warp == kWarpPvB) {
         // ------------------------------------------------------------ MMA issuers
@@ -377,9 +331,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         const uint64_t b = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
                         mma_bf16_ss(tS, a, b, idesc_qk, kk > 0 ? 1u : 0u);
                     }
-                    // + 1 * bias(key): 0 for taking part, -30000 for excluded / missing keys
-                    mma_bf16_ss(tS, desc_noswz_kmajor(smem_u32(sQaug), 128, 256),
-                                desc_noswz_kmajor(smem_u32(sKaug(j & 1)) + h * 2048, 128, 256), idesc_qk, 1u);
                     mma_commit(&bars[B_S_FULL + 2 * t + (q & 1)]);
                     if (h == 1) mma_commit(&bars[B_K_EMPTY + (j & 1)]);
                 };
@@ -469,7 +420,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             tc_fence_after();
             if (h == 0) {
                 // causal limit of this row inside the tile: keys are in increasing position order,
-                // so the visible ones are a prefix (binary search); excluded keys are at -30000
+                // so the visible ones are a prefix (binary search)
                 const int32_t* kp = sKpos(ks);
                 if (kp[kTileKeys - 1] <= mypos) {
                     cut = kTileKeys;         // the whole tile is visible (the common case)

@@ -15,6 +15,10 @@ namespace pcf {
 // read from the shared page blk[r / 16] at in-page offset r % 16 and rotated to the request's
 // position page_pos[r / 16] + r % 16.  The pool itself is never written (MiniPIC 2.1: the shared
 // blocks stay position-free); the rotated copy is per call, in the caller's workspace.
+// With exclusion bits (the attention's copy), a token whose cached copy is replaced by a fresh
+// row is left out: the others are compacted to row cidx[page] + (their rank among the page's
+// kept tokens), their V rows are copied alongside and their positions recorded, so the attention
+// streams only the keys that take part.
 struct RopeJob {
     const __nv_bfloat16* x;  // rows [n_rows][heads][D], or the pool [n_phys][heads][16][D]
     const int32_t* pos;      // [n_rows] logical position of every row (row mode)
@@ -24,39 +28,63 @@ struct RopeJob {
     const int32_t* blk;      // page gather mode: physical page of every logical page (else null)
     const int32_t* page_pos; //   and the logical position of its first token
     int32_t n_phys;          //   pages in the pool
+    const uint16_t* excl;    // compaction (page gather mode): exclusion bits per logical page, or null
+    const int32_t* cidx;     //   compacted row of each page's first kept token
+    const __nv_bfloat16* v_src;   // the V pool (same addressing as x)
+    __nv_bfloat16* v_out;    //   V rows, [heads][n_out][D] like out
+    int32_t* pos_out;        //   logical position of every compacted row
+    int32_t n_out;           //   compacted rows
+    int32_t hpt;             // heads per thread (a multiple of 4, or all of them)
 };
 
+// One thread per (row, group of hpt heads, 16-byte chunk pair c): the row's position, its cos/sin
+// values and (in page gather mode) its page and compacted row are fetched once for the group,
+// whose heads are loaded four at a time.  Large jobs take all heads per thread (the least
+// repeated work); small ones split the heads for parallelism.
 template <int D>
 __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob a, RopeJob b, RopeJob c3,
                                                         const float2* __restrict__ rope, int32_t max_pos,
                                                         int64_t n_a, int64_t n_ab) {
     constexpr int CPR = D / 16;   // 16-byte chunk pairs per head row
+    constexpr int HB = 4;         // heads per thread
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     RopeJob J;   // a copy in registers (a reference into the parameters would go through the stack)
     if (gid < n_a) J = a;
     else if (gid < n_ab) J = b;
     else J = c3;
     const int64_t lid = gid < n_a ? gid : (gid < n_ab ? gid - n_a : gid - n_ab);
-    const int64_t total = (int64_t)J.n_rows * J.heads * CPR;
-    if (J.x == nullptr || lid >= total) return;
+    const int ng = (J.heads + J.hpt - 1) / J.hpt;
+    if (J.x == nullptr || lid >= (int64_t)J.n_rows * ng * CPR) return;
     const int c = (int)(lid % CPR);
-    const int64_t rh = lid / CPR;
-    const int h = (int)(rh % J.heads);
-    const int32_t row = (int32_t)(rh / J.heads);
+    const int hbeg = (int)((lid / CPR) % ng) * J.hpt;
+    const int hend = min(J.heads, hbeg + J.hpt);
+    const int32_t row = (int32_t)(lid / CPR / ng);
     int32_t p;
-    const __nv_bfloat16* src;
+    const __nv_bfloat16* src0;    // head 0 of the row
+    const __nv_bfloat16* vsrc0 = nullptr;
+    int64_t hstride;              // elements from one head of the row to the next
+    int32_t orow_n = J.n_rows, oi = row;
     if (J.blk != nullptr) {
         const int32_t ph = J.blk[row / kPage];
         if (ph < 0 || ph >= J.n_phys) { set_dev_error(kDevErrBounds); return; }
         p = J.page_pos[row / kPage] + row % kPage;
-        src = J.x + (((int64_t)ph * J.heads + h) * kPage + row % kPage) * D;
+        const int64_t off = ((int64_t)ph * J.heads * kPage + row % kPage) * D;
+        src0 = J.x + off;
+        hstride = (int64_t)kPage * D;
+        if (J.excl != nullptr) {
+            const uint32_t ex = J.excl[row / kPage], bit = 1u << (row % kPage);
+            if (ex & bit) return;   // recomputed: its fresh row replaces it
+            oi = J.cidx[row / kPage] + row % kPage - __popc(ex & (bit - 1u));   // kept tokens before it
+            orow_n = J.n_out;
+            vsrc0 = J.v_src + off;
+            if (c == 0 && hbeg == 0) J.pos_out[oi] = p;
+        }
     } else {
         p = J.pos[row];
-        src = J.x + ((int64_t)row * J.heads + h) * D;
+        src0 = J.x + (int64_t)row * J.heads * D;
+        hstride = D;
     }
     if (p < 0 || p >= max_pos) { set_dev_error(kDevErrBounds); return; }
-    const uint4 xa = *reinterpret_cast<const uint4*>(src + 8 * c);
-    const uint4 xb = *reinterpret_cast<const uint4*>(src + D / 2 + 8 * c);
     const float4* cs4 = reinterpret_cast<const float4*>(rope + (int64_t)p * (D / 2) + 8 * c);
     float cs[16];
 #pragma unroll
@@ -64,21 +92,47 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob a, RopeJob b, Ro
         const float4 v = __ldg(cs4 + q);
         cs[4 * q] = v.x; cs[4 * q + 1] = v.y; cs[4 * q + 2] = v.z; cs[4 * q + 3] = v.w;
     }
-    const uint32_t ia[4] = {xa.x, xa.y, xa.z, xa.w};
-    const uint32_t ib[4] = {xb.x, xb.y, xb.z, xb.w};
-    uint32_t oa[4], ob[4];
+    for (int h0 = hbeg; h0 < hend; h0 += HB) {
+        uint4 xa[HB], xb[HB], va[HB], vb[HB];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float c0 = cs[4 * e], s0 = cs[4 * e + 1], c1 = cs[4 * e + 2], s1 = cs[4 * e + 3];
-        const float a0 = bf16_lo(ia[e]) * J.scale, a1 = bf16_hi(ia[e]) * J.scale;
-        const float b0 = bf16_lo(ib[e]) * J.scale, b1 = bf16_hi(ib[e]) * J.scale;
-        oa[e] = pack_f16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
-        ob[e] = pack_f16x2(fmaf(b0, c0, a0 * s0), fmaf(b1, c1, a1 * s1));
+        for (int k = 0; k < HB; ++k) {
+            if (h0 + k < hend) {
+                const __nv_bfloat16* src = src0 + (h0 + k) * hstride;
+                xa[k] = *reinterpret_cast<const uint4*>(src + 8 * c);
+                xb[k] = *reinterpret_cast<const uint4*>(src + D / 2 + 8 * c);
+                if (vsrc0 != nullptr) {
+                    const __nv_bfloat16* vs = vsrc0 + (h0 + k) * hstride;
+                    va[k] = *reinterpret_cast<const uint4*>(vs + 8 * c);
+                    vb[k] = *reinterpret_cast<const uint4*>(vs + D / 2 + 8 * c);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < HB; ++k) {
+            const int h = h0 + k;
+            if (h >= hend) break;
+            const uint32_t ia[4] = {xa[k].x, xa[k].y, xa[k].z, xa[k].w};
+            const uint32_t ib[4] = {xb[k].x, xb[k].y, xb[k].z, xb[k].w};
+            uint32_t oa[4], ob[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float c0 = cs[4 * e], s0 = cs[4 * e + 1], c1 = cs[4 * e + 2], s1 = cs[4 * e + 3];
+                const float a0 = bf16_lo(ia[e]) * J.scale, a1 = bf16_hi(ia[e]) * J.scale;
+                const float b0 = bf16_lo(ib[e]) * J.scale, b1 = bf16_hi(ib[e]) * J.scale;
+                oa[e] = pack_f16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
+                ob[e] = pack_f16x2(fmaf(b0, c0, a0 * s0), fmaf(b1, c1, a1 * s1));
+            }
+            const int64_t orow = ((int64_t)(h / J.gg) * orow_n + oi) * J.gg + (h % J.gg);
+            __half* dst = J.out + orow * D;
+            *reinterpret_cast<uint4*>(dst + 8 * c) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+            *reinterpret_cast<uint4*>(dst + D / 2 + 8 * c) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+            if (vsrc0 != nullptr) {   // the compacted token's V row, unchanged
+                __nv_bfloat16* vd = J.v_out + orow * D;
+                *reinterpret_cast<uint4*>(vd + 8 * c) = va[k];
+                *reinterpret_cast<uint4*>(vd + D / 2 + 8 * c) = vb[k];
+            }
+        }
     }
-    const int64_t orow = ((int64_t)(h / J.gg) * J.n_rows + row) * J.gg + (h % J.gg);
-    __half* dst = J.out + orow * D;
-    *reinterpret_cast<uint4*>(dst + 8 * c) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-    *reinterpret_cast<uint4*>(dst + D / 2 + 8 * c) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
 }
 
 // ------------------------------------------------------------------ block scan helper
@@ -264,6 +318,28 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
     const uint4* s = src + (int64_t)(R[R_TOK_BASE] + j) * row_chunks;
     uint4* d = dst + (int64_t)r * row_chunks;
     for (int c = threadIdx.x; c < row_chunks; c += blockDim.x) d[c] = __ldg(s + c);
+}
+
+// ------------------------------------------------------------------ compaction scan
+// Per logical page, the compacted row of its first cached token that takes part in the attention
+// (exclusion bit clear): the request's base R_CBASE plus the kept tokens of the request's earlier
+// pages.  One block per request.
+constexpr int kScanThreads = 256;
+__global__ void __launch_bounds__(kScanThreads) compact_scan_kernel(const int32_t* __restrict__ L,
+                                                                    const uint16_t* __restrict__ excl,
+                                                                    int32_t* __restrict__ cidx) {
+    __shared__ int s_warp[kScanThreads / 32];
+    const int32_t* R = L + L[L_OFF_REQ] + blockIdx.x * R_STRIDE;
+    const int n_pages = R[R_N_PAGES], pb = R[R_PAGE_BASE];
+    int carry = R[R_CBASE];
+    for (int p0 = 0; p0 < n_pages; p0 += kScanThreads) {
+        const int p = p0 + threadIdx.x;
+        const int kept = p < n_pages ? kPage - __popc((uint32_t)excl[pb + p]) : 0;
+        int total;
+        const int before = block_excl_scan<kScanThreads>(kept, s_warp, &total);
+        if (p < n_pages) cidx[pb + p] = carry + before;
+        carry += total;
+    }
 }
 
 // ------------------------------------------------------------------ split-range combine

@@ -111,14 +111,18 @@ ScoreWs score_ws(const int32_t* H) {
 }
 
 struct AttnWs {
-    size_t q, k, kc, po, pml, total;
+    size_t q, k, kc, vc, kpos, cidx, po, pml, total;
 };
 AttnWs attn_ws(const int32_t* H) {
     AttnWs w;
+    const size_t valid_rows = (size_t)H[L_HKV] * H[L_TOTAL_VALID] * H[L_D];   // compacted K / V elements
     w.q = 0;
     w.k = align_up((size_t)H[L_TOTAL_ROWS] * H[L_HQ] * H[L_D] * 2);
     w.kc = align_up(w.k + (size_t)H[L_TOTAL_ROWS] * H[L_HKV] * H[L_D] * 2);
-    w.po = align_up(w.kc + kc_bytes(H));
+    w.vc = align_up(w.kc + valid_rows * 2);
+    w.kpos = align_up(w.vc + valid_rows * 2);
+    w.cidx = align_up(w.kpos + (size_t)H[L_TOTAL_VALID] * sizeof(int32_t));
+    w.po = align_up(w.cidx + (size_t)H[L_TOTAL_PAGES] * sizeof(int32_t));
     const size_t prow = (size_t)H[L_ATTN_SLOTS] * kQTilesPerCta * kTileRows;   // partial rows
     w.pml = align_up(w.po + prow * H[L_D] * 2);
     w.total = align_up(w.pml + prow * sizeof(float2));
@@ -132,11 +136,19 @@ pcf_status set_smem(K kernel, int bytes) {
                : PCF_ERR_CUDA;
 }
 
+// threads of a RoPE job: one per (row, head group, chunk pair); a job with enough rows to fill the
+// GPU a few times over takes all heads per thread, a smaller one groups of four
+template <int D>
+int64_t rope_threads(RopeJob& j) {
+    if (!j.x) return 0;
+    const int64_t rows_x = (int64_t)j.n_rows * (D / 16);
+    j.hpt = rows_x >= 4 * kNumSms * 256 ? j.heads : 4;
+    return rows_x * ((j.heads + j.hpt - 1) / j.hpt);
+}
+
 template <int D>
 pcf_status launch_rope(RopeJob a, RopeJob b, RopeJob c, const float2* rope, int32_t max_pos, cudaStream_t st) {
-    const int64_t n_a = a.x ? (int64_t)a.n_rows * a.heads * (D / 16) : 0;
-    const int64_t n_b = b.x ? (int64_t)b.n_rows * b.heads * (D / 16) : 0;
-    const int64_t n_c = c.x ? (int64_t)c.n_rows * c.heads * (D / 16) : 0;
+    const int64_t n_a = rope_threads<D>(a), n_b = rope_threads<D>(b), n_c = rope_threads<D>(c);
     const int64_t n = n_a + n_b + n_c;
     if (n == 0) return PCF_OK;
     const int64_t blocks = (n + 255) / 256;
@@ -148,7 +160,20 @@ pcf_status launch_rope(RopeJob a, RopeJob b, RopeJob c, const float2* rope, int3
 RopeJob cached_key_job(const pcf_layout* lay, const uint16_t* k_pool, __half* kc) {
     const int32_t* H = lay->host;
     return RopeJob{reinterpret_cast<const __nv_bfloat16*>(k_pool), nullptr, kc, H[L_TOTAL_TOKENS], H[L_HKV], 1, 1.f,
-                   lay->dev + H[L_OFF_BLOCK], lay->dev + H[L_OFF_PAGEPOS], H[L_N_PHYS]};
+                   lay->dev + H[L_OFF_BLOCK], lay->dev + H[L_OFF_PAGEPOS], H[L_N_PHYS],
+                   nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+}
+// the cached keys that take part in the attention, compacted (rotated K, V copied, positions)
+RopeJob kept_key_job(const pcf_layout* lay, const uint16_t* k_pool, const uint16_t* v_pool, const uint16_t* excl,
+                     const int32_t* cidx, __half* kc, __nv_bfloat16* vc, int32_t* kpos) {
+    RopeJob j = cached_key_job(lay, k_pool, kc);
+    j.excl = excl;
+    j.cidx = cidx;
+    j.v_src = reinterpret_cast<const __nv_bfloat16*>(v_pool);
+    j.v_out = vc;
+    j.pos_out = kpos;
+    j.n_out = lay->host[L_TOTAL_VALID];
+    return j;
 }
 
 template <int D>
@@ -170,8 +195,9 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
     const size_t n_cnt = (size_t)H[L_TOTAL_KTILES] + H[L_N_LSE_PAIRS];
     if (n_cnt > 0 && cudaMemsetAsync(cnt, 0, n_cnt * sizeof(int32_t), st) != cudaSuccess) return PCF_ERR_CUDA;
     RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_query), lay->dev + H[L_OFF_QPOS], q_rot, H[L_TOTAL_QUERY],
-               H[L_HQ], g, scale_log2, nullptr, nullptr, 0};
-    RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f, nullptr, nullptr, 0};
+               H[L_HQ], g, scale_log2, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+    RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
+                 nullptr, 0, 4};
     pcf_status s = launch_rope<D>(qj, cached_key_job(lay, k_pool, kc), none, rope2, H[L_MAX_POS], st);
     if (s != PCF_OK) return s;
 
@@ -214,25 +240,36 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     __half* q_rot = reinterpret_cast<__half*>(base + w.q);
     __half* k_rot = reinterpret_cast<__half*>(base + w.k);
     __half* kc = reinterpret_cast<__half*>(base + w.kc);
+    __nv_bfloat16* vc = reinterpret_cast<__nv_bfloat16*>(base + w.vc);
+    int32_t* kpos_c = reinterpret_cast<int32_t*>(base + w.kpos);
+    int32_t* cidx = reinterpret_cast<int32_t*>(base + w.cidx);
     const int g = H[L_GROUP];
     const float2* rope2 = reinterpret_cast<const float2*>(rope);
     const int32_t rows = H[L_TOTAL_ROWS];
     const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_fresh), row_pos, q_rot, rows, H[L_HQ], g, scale_log2,
-               nullptr, nullptr, 0};
+               nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
     RopeJob kj{reinterpret_cast<const __nv_bfloat16*>(k_fresh), row_pos, k_rot, rows, H[L_HKV], 1, 1.f,
-               nullptr, nullptr, 0};
-    pcf_status s = launch_rope<D>(qj, kj, cached_key_job(lay, k_pool, kc), rope2, H[L_MAX_POS], st);
+               nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+    pcf_status s;
+    if (H[L_TOTAL_PAGES] > 0) {
+        compact_scan_kernel<<<H[L_N_REQS], kScanThreads, 0, st>>>(lay->dev, excl, cidx);
+        if ((s = launched()) != PCF_OK) return s;
+    }
+    s = launch_rope<D>(qj, kj, kept_key_job(lay, k_pool, v_pool, excl, cidx, kc, vc, kpos_c), rope2, H[L_MAX_POS], st);
     if (s != PCF_OK) return s;
 
-    CUtensorMap tq, tkc, tvp, tkf, tvf;
-    const uint64_t pool_rows = (uint64_t)H[L_N_PHYS] * H[L_HKV] * kPage;
+    CUtensorMap tq, tkc, tvc, tkf, tvf;
     if ((s = make_map_2d(&tq, q_rot, D, (uint64_t)H[L_HKV] * rows * g, D * 2, 128, kF16)) != PCF_OK) return s;
-    // a batch without cached tokens never reads this map: point it at the fresh keys
-    if (H[L_TOTAL_TOKENS] > 0) s = make_map_2d(&tkc, kc, D, (uint64_t)H[L_HKV] * H[L_TOTAL_TOKENS], D * 2, 128, kF16);
-    else s = make_map_2d(&tkc, k_rot, D, (uint64_t)H[L_HKV] * rows, D * 2, 128, kF16);
-    if (s != PCF_OK) return s;
-    if ((s = make_map_2d(&tvp, v_pool, D, pool_rows, D * 2, kPage)) != PCF_OK) return s;
+    // a batch without taking-part cached keys never reads these maps: point them at the fresh rows
+    if (H[L_TOTAL_VALID] > 0) {
+        const uint64_t vr = (uint64_t)H[L_HKV] * H[L_TOTAL_VALID];
+        if ((s = make_map_2d(&tkc, kc, D, vr, D * 2, 128, kF16)) != PCF_OK) return s;
+        if ((s = make_map_2d(&tvc, vc, D, vr, D * 2, 128)) != PCF_OK) return s;
+    } else {
+        if ((s = make_map_2d(&tkc, k_rot, D, (uint64_t)H[L_HKV] * rows, D * 2, 128, kF16)) != PCF_OK) return s;
+        if ((s = make_map_2d(&tvc, v_fresh, D, (uint64_t)H[L_HKV] * rows, D * 2, 128)) != PCF_OK) return s;
+    }
     if ((s = make_map_2d(&tkf, k_rot, D, (uint64_t)H[L_HKV] * rows, D * 2, 128, kF16)) != PCF_OK) return s;
     if ((s = make_map_3d(&tvf, v_fresh, D, H[L_HKV], rows, 128)) != PCF_OK) return s;
 
@@ -241,9 +278,9 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
     __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(base + w.po);
     float2* part_ml = reinterpret_cast<float2*>(base + w.pml);
-    AttnParams p{lay->dev, excl, row_pos, reinterpret_cast<__nv_bfloat16*>(out), nullptr, nullptr, nullptr, part_o,
+    AttnParams p{lay->dev, kpos_c, row_pos, reinterpret_cast<__nv_bfloat16*>(out), nullptr, nullptr, nullptr, part_o,
                  part_ml};
-    kern<<<H[L_N_ATTN_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq, tkc, tvp, tkf, tvf, p);
+    kern<<<H[L_N_ATTN_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq, tkc, tvc, tkf, tvf, p);
     if ((s = launched()) != PCF_OK) return s;
     if (H[L_N_COMB] > 0) {
         combine_kernel<D><<<dim3(H[L_N_COMB], D / 8), 256, 0, st>>>(lay->dev, part_o, part_ml,

@@ -182,10 +182,10 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
     plan->total_ktiles = (int32_t)tot_kt;
 
     // Attention work units: (request, pair of 128-row query tiles), each run once per kv head.  A
-    // pair sees the cached key tiles up to its last row's position and the fresh tiles up to its
-    // last row.  Rows are selected tokens in position order, then query tokens; before the
-    // selection is known, a selected row is only known to lie inside its span, so the span's end
-    // bounds its cached tiles.
+    // pair sees the tiles of taking-part cached keys (the compacted copy: recomputed tokens left
+    // out) up to its last row's position and the fresh tiles up to its last row.  Rows are selected
+    // tokens in position order, then query tokens; before the selection is known, a selected row
+    // is only known to lie inside its span, so the span's end bounds its cached tiles.
     plan->pair_base.assign(n_reqs, 0);
     plan->pair_tiles.clear();
     for (int b = 0; b < n_reqs; ++b) {
@@ -198,7 +198,7 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
             cum_k.push_back(n_sel);
             cum_pages.push_back(n_pg);
         }
-        const int32_t nkt = cdiv(n_pg, kPagesPerTile);
+        const int32_t nkt_c = cdiv(n_pg * kPage - n_sel, kTileKeys);   // compacted cached tiles
         const int64_t rows = n_sel + r.n_query;
         const int64_t npairs = cdiv(rows * g, kTileRows * kQTilesPerCta);
         const int64_t toks_per_pair = (int64_t)kQTilesPerCta * (kTileRows / g);
@@ -206,10 +206,10 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
         size_t s = 0;
         for (int64_t p = 0; p < npairs; ++p) {
             const int64_t last = std::min<int64_t>((p + 1) * toks_per_pair, rows) - 1;
-            int32_t nct = nkt;
+            int32_t nct = nkt_c;
             if (last < n_sel) {
                 while (s + 1 < cum_k.size() && cum_k[s + 1] <= last) ++s;
-                nct = cdiv(cum_pages[s + 1], kPagesPerTile);
+                nct = cdiv(cum_pages[s + 1] * kPage - cum_k[s + 1], kTileKeys);
             }
             plan->pair_tiles.push_back(nct + (int32_t)(last / kTileKeys) + 1);
         }
@@ -338,6 +338,7 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
     H[L_TOTAL_QUERY] = plan.total_query;
     H[L_TOTAL_ROWS] = plan.total_rows;
     H[L_TOTAL_SEL] = plan.total_sel;
+    H[L_TOTAL_VALID] = plan.total_tokens - plan.total_sel;
     H[L_TOTAL_PAGES] = plan.total_pages;
     H[L_N_SPANS] = plan.n_spans;
     H[L_MAX_TOKENS] = plan.max_tokens;
@@ -429,6 +430,7 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
         R[R_KTILE_BASE] = kt_base;
         R[R_N_KTILES] = nkt;
         R[R_PAIR_BASE] = plan.pair_base[b];
+        R[R_CBASE] = tok_base - sel_base;   // taking-part cached keys of the requests before
         for (int t = 0; t < r.n_query; ++t) QPOS[q_base + t] = r.query_pos0 + t;
 
         // attention work: per (pair of 128-row tiles, kv head), one item per key-range split; rows
