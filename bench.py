@@ -325,8 +325,10 @@ def main():
     pcf.check_device_error()
 
     hw = L.host.numpy()   # layout header: LSE items [19], importance items [20], combine items [33]
+    # scoring: rotation, row LSE, importance; top-k; gather; attention: compaction scan, rotation,
+    # attention, split merge
     launches_per_step = ((1 + (hw[19] > 0) + (hw[20] > 0)) if L.total_tokens else 0) + 1 + (1 if L.total_sel else 0) \
-        + (2 if L.total_rows else 0) + (1 if hw[33] > 0 else 0)
+        + ((2 + (1 if L.total_tokens else 0)) if L.total_rows else 0) + (1 if hw[33] > 0 else 0)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

@@ -163,8 +163,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             for (int i = 0; i < 2 * kQTilesPerCta; ++i) mbar_init(&bars[B_DRAIN + i], 1);
             fence_mbar_init();
-            // the Q tiles do not depend on the key range: start them before it is computed
             prefetch_tmap(&tm_q);
+        }
+    }
+    // up to here only the layout and shared memory were touched: the previous kernel (which
+    // writes the rotated rows, the compacted keys and their positions) may still be running
+    grid_dep_wait();
+    grid_dep_launch();
+    if (warp == 0) {
+        if (lane == 0) {
+            // the Q tiles do not depend on the key range: start them before it is computed
             const int32_t qy = LSE ? (kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row0) * g
                                    : (kvh * L[L_TOTAL_ROWS] + row_base + row0) * g;
             mbar_arrive_expect_tx(&bars[B_Q_FULL], kQTilesPerCta * SM::kQ);

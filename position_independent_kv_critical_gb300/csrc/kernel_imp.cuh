@@ -108,6 +108,10 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         fence_mbar_init();
         misc[4] = 0;
     }
+    // the previous kernel (row LSE, which writes the log2-sum-exp read here) may still be running
+    // until this wait; the TMEM is taken only after it
+    grid_dep_wait();
+    grid_dep_launch();
     if (warp == kImpWarpMma) {
         tmem_alloc(reinterpret_cast<uint32_t*>(misc), SM::kTmemCols);
         tmem_relinquish();

@@ -44,10 +44,15 @@ struct RopeJob {
 template <int D>
 __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob a, RopeJob b, RopeJob c3,
                                                         const float2* __restrict__ rope, int32_t max_pos,
-                                                        int64_t n_a, int64_t n_ab) {
+                                                        int64_t n_a, int64_t n_ab, int32_t* __restrict__ zero,
+                                                        int32_t n_zero) {
     constexpr int CPR = D / 16;   // 16-byte chunk pairs per head row
     constexpr int HB = 4;         // heads per thread
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    grid_dep_wait();
+    grid_dep_launch();
+    // counters of the kernels that follow, cleared here rather than by a separate memset
+    for (int64_t i = gid; i < n_zero; i += (int64_t)gridDim.x * blockDim.x) zero[i] = 0;
     RopeJob J;   // a copy in registers (a reference into the parameters would go through the stack)
     if (gid < n_a) J = a;
     else if (gid < n_ab) J = b;
@@ -186,6 +191,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const int32_t* __res
     __shared__ int s_hist[256];
     __shared__ int s_warp[kTopkThreads / 32];
     __shared__ int s_bucket, s_above;
+    grid_dep_wait();
+    grid_dep_launch();
     const int n_spans = L[L_N_SPANS];
     const int tid = threadIdx.x;
     if ((int)blockIdx.x >= n_spans) {
@@ -301,6 +308,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
                                                      const int32_t* __restrict__ sel_idx,
                                                      const uint4* __restrict__ src, int32_t row_chunks,
                                                      uint4* __restrict__ dst) {
+    grid_dep_wait();
+    grid_dep_launch();
     const int32_t r = blockIdx.x;
     const int n_reqs = L[L_N_REQS];
     const int32_t* REQ = L + L[L_OFF_REQ];
@@ -329,6 +338,8 @@ __global__ void __launch_bounds__(kScanThreads) compact_scan_kernel(const int32_
                                                                     const uint16_t* __restrict__ excl,
                                                                     int32_t* __restrict__ cidx) {
     __shared__ int s_warp[kScanThreads / 32];
+    grid_dep_wait();
+    grid_dep_launch();
     const int32_t* R = L + L[L_OFF_REQ] + blockIdx.x * R_STRIDE;
     const int n_pages = R[R_N_PAGES], pb = R[R_PAGE_BASE];
     int carry = R[R_CBASE];
@@ -355,6 +366,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict_
                                                       __nv_bfloat16* __restrict__ out) {
     constexpr int CH = D / 8;                   // 16-byte chunks per row
     constexpr int RPB = 256 / CH;               // rows per block
+    grid_dep_wait();
+    grid_dep_launch();
     const int32_t* item = L + L[L_OFF_COMB] + kItemWords * blockIdx.x;
     const int req = item[0], kvh = item[1], qpair = item[2];
     const int32_t* R = L + L[L_OFF_REQ] + req * R_STRIDE;

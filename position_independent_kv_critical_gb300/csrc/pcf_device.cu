@@ -2,10 +2,12 @@
 // carving and launches.  Every device buffer is the caller's; nothing here allocates.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <utility>
 
 #include "../../include/pcf.h"
 #include "kernel_attn.cuh"
@@ -87,7 +89,24 @@ pcf_status check_device() {
     return (major == 10 && minor == 3) ? PCF_OK : PCF_ERR_NO_DEVICE;
 }
 
-pcf_status launched() { return cudaGetLastError() == cudaSuccess ? PCF_OK : PCF_ERR_CUDA; }
+// Every kernel of the library is launched with programmatic stream serialization: its CTAs may be
+// scheduled while the previous kernel in the stream is still running, set up what depends on no
+// other kernel, and wait for that kernel in grid_dep_wait().  This hides most of the launch gap
+// between the nine short kernels of a small batch.
+template <typename... KArgs, typename... Args>
+pcf_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? PCF_OK : PCF_ERR_CUDA;
+}
 
 size_t align_up(size_t x) { return (x + 1023) & ~size_t(1023); }
 
@@ -147,13 +166,14 @@ int64_t rope_threads(RopeJob& j) {
 }
 
 template <int D>
-pcf_status launch_rope(RopeJob a, RopeJob b, RopeJob c, const float2* rope, int32_t max_pos, cudaStream_t st) {
+pcf_status launch_rope(RopeJob a, RopeJob b, RopeJob c, const float2* rope, int32_t max_pos, cudaStream_t st,
+                       int32_t* zero = nullptr, int32_t n_zero = 0) {
     const int64_t n_a = rope_threads<D>(a), n_b = rope_threads<D>(b), n_c = rope_threads<D>(c);
-    const int64_t n = n_a + n_b + n_c;
+    const int64_t n = std::max<int64_t>(n_a + n_b + n_c, n_zero);
     if (n == 0) return PCF_OK;
     const int64_t blocks = (n + 255) / 256;
-    rope_rows_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(a, b, c, rope, max_pos, n_a, n_a + n_b);
-    return launched();
+    return launch(rope_rows_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, st, a, b, c, rope, max_pos, n_a,
+                  n_a + n_b, zero, n_zero);
 }
 
 // the batch's cached keys, gathered from their pages and rotated to each request's positions
@@ -192,13 +212,12 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
     const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     const float2* rope2 = reinterpret_cast<const float2*>(rope);
 
-    const size_t n_cnt = (size_t)H[L_TOTAL_KTILES] + H[L_N_LSE_PAIRS];
-    if (n_cnt > 0 && cudaMemsetAsync(cnt, 0, n_cnt * sizeof(int32_t), st) != cudaSuccess) return PCF_ERR_CUDA;
+    const int32_t n_cnt = H[L_TOTAL_KTILES] + H[L_N_LSE_PAIRS];   // cleared by the rotation kernel
     RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_query), lay->dev + H[L_OFF_QPOS], q_rot, H[L_TOTAL_QUERY],
                H[L_HQ], g, scale_log2, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
     RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
                  nullptr, 0, 4};
-    pcf_status s = launch_rope<D>(qj, cached_key_job(lay, k_pool, kc), none, rope2, H[L_MAX_POS], st);
+    pcf_status s = launch_rope<D>(qj, cached_key_job(lay, k_pool, kc), none, rope2, H[L_MAX_POS], st, cnt, n_cnt);
     if (s != PCF_OK) return s;
 
     CUtensorMap tq128, tq256, tkc, zero;
@@ -214,16 +233,17 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
         auto kern = attn_kernel<D, true>;
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
         AttnParams p{lay->dev, nullptr, nullptr, nullptr, lse, lse_final, cnt + H[L_TOTAL_KTILES], nullptr, nullptr};
-        kern<<<H[L_N_LSE_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq128, tkc, zero, zero, zero, p);
-        if ((s = launched()) != PCF_OK) return s;
+        if ((s = launch(kern, dim3(H[L_N_LSE_ITEMS]), dim3(kAttnThreads), SM::kAlloc, st, tq128, tkc, zero, zero,
+                        zero, p)) != PCF_OK)
+            return s;
     }
     if (H[L_N_IMP_ITEMS] > 0) {
         using SM = ImpSmem<D>;
         auto kern = imp_kernel<D>;
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
         ImpParams p{lay->dev, lse_final, part, cnt, importance};
-        kern<<<H[L_N_IMP_ITEMS], kImpThreads, SM::kAlloc, st>>>(tq256, tkc, p);
-        if ((s = launched()) != PCF_OK) return s;
+        if ((s = launch(kern, dim3(H[L_N_IMP_ITEMS]), dim3(kImpThreads), SM::kAlloc, st, tq256, tkc, p)) != PCF_OK)
+            return s;
     }
     return PCF_OK;
 }
@@ -253,8 +273,9 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
                nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
     pcf_status s;
     if (H[L_TOTAL_PAGES] > 0) {
-        compact_scan_kernel<<<H[L_N_REQS], kScanThreads, 0, st>>>(lay->dev, excl, cidx);
-        if ((s = launched()) != PCF_OK) return s;
+        if ((s = launch(compact_scan_kernel, dim3(H[L_N_REQS]), dim3(kScanThreads), 0, st, lay->dev, excl, cidx)) !=
+            PCF_OK)
+            return s;
     }
     s = launch_rope<D>(qj, kj, kept_key_job(lay, k_pool, v_pool, excl, cidx, kc, vc, kpos_c), rope2, H[L_MAX_POS], st);
     if (s != PCF_OK) return s;
@@ -280,12 +301,14 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     float2* part_ml = reinterpret_cast<float2*>(base + w.pml);
     AttnParams p{lay->dev, kpos_c, row_pos, reinterpret_cast<__nv_bfloat16*>(out), nullptr, nullptr, nullptr, part_o,
                  part_ml};
-    kern<<<H[L_N_ATTN_ITEMS], kAttnThreads, SM::kAlloc, st>>>(tq, tkc, tvc, tkf, tvf, p);
-    if ((s = launched()) != PCF_OK) return s;
+    if ((s = launch(kern, dim3(H[L_N_ATTN_ITEMS]), dim3(kAttnThreads), SM::kAlloc, st, tq, tkc, tvc, tkf, tvf, p)) !=
+        PCF_OK)
+        return s;
     if (H[L_N_COMB] > 0) {
-        combine_kernel<D><<<dim3(H[L_N_COMB], D / 8), 256, 0, st>>>(lay->dev, part_o, part_ml,
-                                                                   reinterpret_cast<__nv_bfloat16*>(out));
-        if ((s = launched()) != PCF_OK) return s;
+        if ((s = launch(combine_kernel<D>, dim3(H[L_N_COMB], D / 8), dim3(256), 0, st, lay->dev,
+                        (const __nv_bfloat16*)part_o, (const float2*)part_ml,
+                        reinterpret_cast<__nv_bfloat16*>(out))) != PCF_OK)
+            return s;
     }
     return PCF_OK;
 }
@@ -332,9 +355,8 @@ extern "C" pcf_status pcf_select_topk(const pcf_layout* layout, const float* imp
     const int blocks = H[L_N_SPANS] + H[L_N_REQS];
     const int words = (H[L_MAX_SPAN_LEN] + 31) / 32;
     if (words * 4 > 48 * 1024) return PCF_ERR_UNSUPPORTED;
-    topk_kernel<<<blocks, kTopkThreads, words * 4, static_cast<cudaStream_t>(stream)>>>(layout->dev, importance,
-                                                                                        sel_idx, excl, row_pos);
-    return launched();
+    return launch(topk_kernel, dim3(blocks), dim3(kTopkThreads), words * 4, static_cast<cudaStream_t>(stream),
+                  layout->dev, importance, sel_idx, excl, row_pos);
 }
 
 extern "C" pcf_status pcf_gather_rows(const pcf_layout* layout, const int32_t* sel_idx, const uint16_t* src,
@@ -346,9 +368,8 @@ extern "C" pcf_status pcf_gather_rows(const pcf_layout* layout, const int32_t* s
     if (H[L_TOTAL_SEL] == 0) return PCF_OK;
     if (!sel_idx || !src || !dst || !aligned16(src) || !aligned16(dst)) return PCF_ERR_INVALID_ARG;
     if ((s = check_device()) != PCF_OK) return s;
-    gather_kernel<<<H[L_TOTAL_SEL], 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        layout->dev, sel_idx, reinterpret_cast<const uint4*>(src), row_elems / 8, reinterpret_cast<uint4*>(dst));
-    return launched();
+    return launch(gather_kernel, dim3(H[L_TOTAL_SEL]), dim3(256), 0, static_cast<cudaStream_t>(stream), layout->dev,
+                  sel_idx, reinterpret_cast<const uint4*>(src), row_elems / 8, reinterpret_cast<uint4*>(dst));
 }
 
 extern "C" pcf_status pcf_fused_attention(const pcf_layout* layout, const uint16_t* q_fresh, const uint16_t* k_fresh,

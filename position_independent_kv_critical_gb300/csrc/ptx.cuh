@@ -20,6 +20,16 @@ __device__ __forceinline__ void set_dev_error(int code) { atomicCAS(&g_pcf_dev_e
 // About 1 s at GB300 clocks: no correct pipeline wait comes anywhere near this.
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// The library's kernels are launched with programmatic stream serialization, so a kernel's CTAs
+// may start while the previous kernel in the stream is still running.  Everything before
+// grid_dep_wait() may touch only data no kernel writes (the layout, tensor maps, shared memory);
+// grid_dep_wait() returns once the previous grid has finished and its writes are visible (and,
+// since every kernel here waits before it finishes, every earlier grid too).  grid_dep_launch()
+// lets the next grid start its own prologue.  Both are no-ops without the launch attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
