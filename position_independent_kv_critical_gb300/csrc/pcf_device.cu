@@ -124,13 +124,14 @@ ScoreWs score_ws(const int32_t* H) {
     w.lsef = align_up(w.lse + (size_t)H[L_LSE_SLOTS] * sizeof(float2));
     w.part = align_up(w.lsef + (size_t)H[L_TOTAL_QUERY] * H[L_HQ] * sizeof(float));
     w.cnt = align_up(w.part + (size_t)H[L_HKV] * H[L_TOTAL_TOKENS] * sizeof(float));
-    // counters: importance runs (one per key tile at most), then the LSE pass's (kv head, pair)s
-    w.total = align_up(w.cnt + ((size_t)H[L_TOTAL_KTILES] + H[L_N_LSE_PAIRS]) * sizeof(int32_t));
+    // counters: importance runs (one per key tile at most), the LSE pass's (kv head, pair)s, and
+    // the LSE kernel's item counter
+    w.total = align_up(w.cnt + ((size_t)H[L_TOTAL_KTILES] + H[L_N_LSE_PAIRS] + 1) * sizeof(int32_t));
     return w;
 }
 
 struct AttnWs {
-    size_t q, k, kc, vc, kpos, cidx, po, pml, total;
+    size_t q, k, kc, vc, kpos, cidx, po, pml, sched, total;
 };
 AttnWs attn_ws(const int32_t* H) {
     AttnWs w;
@@ -144,7 +145,8 @@ AttnWs attn_ws(const int32_t* H) {
     w.po = align_up(w.cidx + (size_t)H[L_TOTAL_PAGES] * sizeof(int32_t));
     const size_t prow = (size_t)H[L_ATTN_SLOTS] * kQTilesPerCta * kTileRows;   // partial rows
     w.pml = align_up(w.po + prow * H[L_D] * 2);
-    w.total = align_up(w.pml + prow * sizeof(float2));
+    w.sched = align_up(w.pml + prow * sizeof(float2));   // the attention kernel's item counter
+    w.total = align_up(w.sched + sizeof(int32_t));
     return w;
 }
 
@@ -212,7 +214,7 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
     const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     const float2* rope2 = reinterpret_cast<const float2*>(rope);
 
-    const int32_t n_cnt = H[L_TOTAL_KTILES] + H[L_N_LSE_PAIRS];   // cleared by the rotation kernel
+    const int32_t n_cnt = H[L_TOTAL_KTILES] + H[L_N_LSE_PAIRS] + 1;   // cleared by the rotation kernel
     RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_query), lay->dev + H[L_OFF_QPOS], q_rot, H[L_TOTAL_QUERY],
                H[L_HQ], g, scale_log2, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
     RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
@@ -232,9 +234,12 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
         using SM = AttnSmem<D, true>;
         auto kern = attn_kernel<D, true>;
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
-        AttnParams p{lay->dev, nullptr, nullptr, nullptr, lse, lse_final, cnt + H[L_TOTAL_KTILES], nullptr, nullptr};
-        if ((s = launch(kern, dim3(H[L_N_LSE_ITEMS]), dim3(kAttnThreads), SM::kAlloc, st, tq128, tkc, zero, zero,
-                        zero, p)) != PCF_OK)
+        AttnParams p{lay->dev, nullptr, nullptr, nullptr, lse, lse_final, cnt + H[L_TOTAL_KTILES], nullptr, nullptr,
+                     cnt + H[L_TOTAL_KTILES] + H[L_N_LSE_PAIRS]};
+        // persistent: at most one CTA per SM, items handed out in list order
+        const int grid = std::min<int>(H[L_N_LSE_ITEMS], kNumSms);
+        if ((s = launch(kern, dim3(grid), dim3(kAttnThreads), SM::kAlloc, st, tq128, tkc, zero, zero, zero, p)) !=
+            PCF_OK)
             return s;
     }
     if (H[L_N_IMP_ITEMS] > 0) {
@@ -277,7 +282,9 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
             PCF_OK)
             return s;
     }
-    s = launch_rope<D>(qj, kj, kept_key_job(lay, k_pool, v_pool, excl, cidx, kc, vc, kpos_c), rope2, H[L_MAX_POS], st);
+    int32_t* sched = reinterpret_cast<int32_t*>(base + w.sched);
+    s = launch_rope<D>(qj, kj, kept_key_job(lay, k_pool, v_pool, excl, cidx, kc, vc, kpos_c), rope2, H[L_MAX_POS], st,
+                       sched, 1);
     if (s != PCF_OK) return s;
 
     CUtensorMap tq, tkc, tvc, tkf, tvf;
@@ -300,9 +307,10 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(base + w.po);
     float2* part_ml = reinterpret_cast<float2*>(base + w.pml);
     AttnParams p{lay->dev, kpos_c, row_pos, reinterpret_cast<__nv_bfloat16*>(out), nullptr, nullptr, nullptr, part_o,
-                 part_ml};
-    if ((s = launch(kern, dim3(H[L_N_ATTN_ITEMS]), dim3(kAttnThreads), SM::kAlloc, st, tq, tkc, tvc, tkf, tvf, p)) !=
-        PCF_OK)
+                 part_ml, sched};
+    // persistent: at most one CTA per SM, items handed out in list order (largest estimate first)
+    const int grid = std::min<int>(H[L_N_ATTN_ITEMS], kNumSms);
+    if ((s = launch(kern, dim3(grid), dim3(kAttnThreads), SM::kAlloc, st, tq, tkc, tvc, tkf, tvf, p)) != PCF_OK)
         return s;
     if (H[L_N_COMB] > 0) {
         if ((s = launch(combine_kernel<D>, dim3(H[L_N_COMB], D / 8), dim3(256), 0, st, lay->dev,
