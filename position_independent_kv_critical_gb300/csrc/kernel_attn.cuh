@@ -25,8 +25,8 @@
 //               is double-buffered per query tile: P(q) V runs, then Q K(q+2) goes into the
 //               buffer P(q) came from, while the softmax already works on S(q+1).  Four
 //               single-thread issuers keep four independent MMA streams in flight: one thread's
-//               stream of 128-row MMAs with N <= 128 is bound by per-instruction latency, not by
-//               the tensor core's rate
+//               stream of 128-row MMAs with N <= 128 is bound by per-instruction latency (about
+//               100 cycles an instruction), not by the tensor core's rate
 //   warp  9     scheduler (takes the next item, counts its visible key tiles, publishes it in one
 //               of two shared-memory slots), Q loads, K producer: rotated K tiles (compacted
 //               cached or fresh, fp16, TMA) and, per key, its logical position; 2-stage ring
@@ -82,7 +82,13 @@ struct AttnItem {
     int32_t n_ct, n_ft;        // visible cached / fresh key tiles of the pair (LSE: the chunk's tiles)
     int32_t t0;                // LSE: first key tile of the chunk
     int32_t jb, n_loc;         // this item's tiles: jb .. jb+n_loc-1 of the visible range
-    int32_t pad[3];
+    // request / pair fields the other roles need, copied here so that they need no layout loads
+    int32_t n_rows;            // the request's rows (LSE: its query tokens)
+    int32_t row_base;          // first row of the request
+    int32_t cbase;             // first compacted cached key of the request
+    int32_t nsplit, slot_base; // attention: key-range splits of the pair and its first partial slot
+    int32_t lse_base, lse_chunks, lse_cidx, q_base;   // LSE: partials, chunks, counter, query base
+    int32_t pad[2];
 };
 
 template <int D, bool LSE>
@@ -96,7 +102,7 @@ struct AttnSmem {
     static constexpr int oV = oK + kKStages * kK;
     static constexpr int oKpos = oV + kVStages * kV;
     static constexpr int oBar = oKpos + kKStages * kTileKeys * 4;
-    static constexpr int kNumBars = 38;
+    static constexpr int kNumBars = 40;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int oItem = oMisc + 64;
     static constexpr int kBytes = oItem + 2 * (int)sizeof(AttnItem);
@@ -107,7 +113,7 @@ struct AttnSmem {
 // barrier slots
 enum : int {
     B_Q_FULL = 0,      // the item's Q tiles landed (one phase per item)
-    B_K_FULL = 1,      // [2] rotated K tile landed and its key positions written
+    B_K_FULL = 1,      // [2] rotated K tile landed
     B_K_EMPTY = 3,     // [2] both Q K^T that read the stage are done (one commit per issuer)
     B_KPOS_FREE = 5,   // [2] both softmax groups are done with the stage's key positions (256 arrivals)
     B_V_FULL = 7,      // [2]
@@ -123,7 +129,8 @@ enum : int {
     B_ITEM_FULL = 32,  // [2] item slot written by the scheduler
     B_ITEM_EMPTY = 34, // [2] every consumer role has read the slot
     B_FIN = 36,        // LSE: the softmax threads wrote the item's chunk (256 arrivals, one phase per item)
-    B_FIN2 = 37        // LSE: thread 0 counted the chunk (misc[7] says whether it was the pair's last)
+    B_FIN2 = 37,       // LSE: thread 0 counted the chunk (misc[7] says whether it was the pair's last)
+    B_KPOS_FULL = 38   // [2] the K tile's key positions written (every producer lane)
 };
 
 template <int D, bool LSE>
@@ -159,7 +166,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         mbar_init(&bars[B_Q_FULL], 1);
         mbar_init(&bars[B_Q_EMPTY], kQTilesPerCta);
         for (int s2 = 0; s2 < kKStages; ++s2) {
-            mbar_init(&bars[B_K_FULL + s2], 32);   // every producer lane (key positions) + TMA bytes
+            mbar_init(&bars[B_K_FULL + s2], 1);
+            mbar_init(&bars[B_KPOS_FULL + s2], 32);
             mbar_init(&bars[B_K_EMPTY + s2], kQTilesPerCta);
             mbar_init(&bars[B_KPOS_FREE + s2], 256);
         }
@@ -225,7 +233,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             AttnItem w;
             w.req = -1;
             w.kvh = w.qpair = w.chunk = w.n_ct = w.n_ft = w.t0 = w.jb = w.n_loc = 0;
-            w.pad[0] = w.pad[1] = w.pad[2] = 0;
+            w.n_rows = w.row_base = w.cbase = w.nsplit = w.slot_base = 0;
+            w.lse_base = w.lse_chunks = w.lse_cidx = w.q_base = 0;
+            w.pad[0] = w.pad[1] = 0;
             const int32_t* R = L;
             if (idx < n_items) {
                 const int32_t* item = items + kItemWords * idx;
@@ -234,6 +244,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 w.qpair = item[2];
                 w.chunk = item[3];
                 R = L + L[L_OFF_REQ] + w.req * R_STRIDE;
+                w.n_rows = LSE ? R[R_N_QUERY] : R[R_N_ROWS];
+                w.row_base = R[R_ROW_BASE];
+                w.cbase = R[R_CBASE];
                 if (LSE) {
                     // LSE: tiles of all the request's cached tokens, cut into chunks
                     const int nkt = R[R_N_KTILES], chunks = R[R_LSE_CHUNKS];
@@ -241,6 +254,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     w.t0 = w.chunk * tpc;
                     w.n_ct = max(0, min(tpc, nkt - w.t0));
                     w.n_loc = w.n_ct;
+                    w.lse_base = R[R_LSE_BASE];
+                    w.lse_chunks = chunks;
+                    w.lse_cidx = R[R_LSE_PAIR_BASE] +
+                                 w.kvh * ((R[R_N_QUERY] * g + 2 * kTileRows - 1) / (2 * kTileRows)) + w.qpair;
+                    w.q_base = R[R_Q_BASE];
                 } else {
                     // visible tiles: key positions increase along the compacted cached tiles and
                     // along the fresh rows, so each count is the number of tiles whose first key
@@ -263,6 +281,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     const int n_all = nct + nft, ns = PR[P_NSPLIT];
                     w.n_ct = nct;
                     w.n_ft = nft;
+                    w.nsplit = ns;
+                    w.slot_base = PR[P_SLOT_BASE];
                     w.jb = (int)(((int64_t)w.chunk * n_all) / ns);
                     w.n_loc = (int)(((int64_t)(w.chunk + 1) * n_all) / ns) - w.jb;
                 }
@@ -283,29 +303,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const int32_t kc_row0 = LSE ? w.kvh * L[L_TOTAL_TOKENS] + R[R_TOK_BASE]
                                         : w.kvh * L[L_TOTAL_VALID] + R[R_CBASE];
             const int32_t kf_row0 = w.kvh * L[L_TOTAL_ROWS] + row_base;
-            // the item's Q tiles, once both Q K^T issuers are done with the previous item's
-            if (lane == 0) {
-                const int32_t qy = LSE ? (w.kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row0) * g
-                                       : (w.kvh * L[L_TOTAL_ROWS] + row_base + row0) * g;
-                if (it > 0) {
-                    // warm L2 with the Q rows while the previous item drains
-                    for (int t = 0; t < kQTilesPerCta; ++t)
-                        for (int hb = 0; hb < H; ++hb) tma_prefetch_2d(&tm_q, hb * 64, qy + t * kTileRows);
-                    ok = mbar_wait(&bars[B_Q_EMPTY], (it - 1) & 1, abort_flag);
-                }
-                if (ok) {
-                    mbar_arrive_expect_tx(&bars[B_Q_FULL], kQTilesPerCta * SM::kQ);
-                    for (int t = 0; t < kQTilesPerCta; ++t)
-                        for (int hb = 0; hb < H; ++hb)
-                            tma_load_2d(sQ(t) + hb * 16384, &tm_q, &bars[B_Q_FULL], hb * 64, qy + t * kTileRows);
-                    last_q = it;
-                }
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            // its K tiles: lane 0 issues the copy as soon as the stage is free; then lane l writes
-            // the positions of keys l, l+32, l+64, l+96 (kNoPos for a missing key; fetched one
-            // tile ahead) and every lane arrives
+            // key positions, which only the softmax waits for: lane l holds those of keys l, l+32,
+            // l+64, l+96 of a tile (kNoPos for a missing key), loaded one tile ahead; the first
+            // tile's are requested now, before the wait for the Q buffer
             const int n_ct = w.n_ct, n_tiles = w.n_ct + w.n_ft;
             const int n_kept = R[R_N_PAGES] * kPage - R[R_N_SEL];
             const int32_t* page_pos = L + L[L_OFF_PAGEPOS] + R[R_PAGE_BASE];
@@ -330,18 +330,36 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             };
             int32_t pos_n[4];
             if (w.n_loc > 0) meta(w.jb, pos_n);
+            // the item's Q tiles, once both Q K^T issuers are done with the previous item's
+            if (lane == 0) {
+                const int32_t qy = LSE ? (w.kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row0) * g
+                                       : (w.kvh * L[L_TOTAL_ROWS] + row_base + row0) * g;
+                if (it > 0) {
+                    // warm L2 with the Q rows while the previous item drains
+                    for (int t = 0; t < kQTilesPerCta; ++t)
+                        for (int hb = 0; hb < H; ++hb) tma_prefetch_2d(&tm_q, hb * 64, qy + t * kTileRows);
+                    ok = mbar_wait(&bars[B_Q_EMPTY], (it - 1) & 1, abort_flag);
+                }
+                if (ok) {
+                    mbar_arrive_expect_tx(&bars[B_Q_FULL], kQTilesPerCta * SM::kQ);
+                    for (int t = 0; t < kQTilesPerCta; ++t)
+                        for (int hb = 0; hb < H; ++hb)
+                            tma_load_2d(sQ(t) + hb * 16384, &tm_q, &bars[B_Q_FULL], hb * 64, qy + t * kTileRows);
+                    last_q = it;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            // its K tiles: lane 0 issues the copy as soon as the stage is free (the Q K^T wait only
+            // for it); then the lanes write the tile's key positions
             for (int jj = 0; jj < w.n_loc; ++jj, ++kc) {
                 const int j = w.jb + jj, ks = kc & 1;
-                int32_t pos[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) pos[r] = pos_n[r];
-                if (jj + 1 < w.n_loc) meta(j + 1, pos_n);
                 if (lane == 0) {
                     ok = kc < kKStages || (mbar_wait(&bars[B_K_EMPTY + ks], ((kc >> 1) - 1) & 1, abort_flag) &&
                                            mbar_wait(&bars[B_KPOS_FREE + ks], ((kc >> 1) - 1) & 1, abort_flag));
                     if (ok) {
                         uint64_t* full = &bars[B_K_FULL + ks];
-                        mbar_expect_tx(full, H * 16384);
+                        mbar_arrive_expect_tx(full, H * 16384);
                         const CUtensorMap* map = j < n_ct ? &tm_kcache : &tm_kfresh;
                         const int32_t y = j < n_ct ? kc_row0 + (w.t0 + j) * kTileKeys : kf_row0 + (j - n_ct) * kTileKeys;
                         for (int hb = 0; hb < H; ++hb) tma_load_2d(sKs(ks) + hb * 16384, map, full, hb * 64, y);
@@ -349,10 +367,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
-#pragma unroll
-                for (int r = 0; r < 4; ++r) sKpos(ks)[lane + 32 * r] = pos[r];
-                mbar_arrive(&bars[B_K_FULL + ks]);
                 last_k[ks] = kc;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sKpos(ks)[lane + 32 * r] = pos_n[r];
+                mbar_arrive(&bars[B_KPOS_FULL + ks]);
+                if (jj + 1 < w.n_loc) meta(j + 1, pos_n);
             }
         }
         // every copy this warp started has landed before the CTA exits
@@ -373,7 +392,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 if (!take_item(it, w)) break;
                 mbar_arrive(&bars[B_ITEM_EMPTY + (it & 1)]);
                 if (w.req < 0) break;
-                const int32_t* R = L + L[L_OFF_REQ] + w.req * R_STRIDE;
                 bool ok = true;
                 for (int jj = 0; jj < w.n_loc; ++jj, ++vc) {
                     const int j = w.jb + jj, vs = vc & 1;
@@ -382,10 +400,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     uint64_t* full = &bars[B_V_FULL + vs];
                     mbar_arrive_expect_tx(full, H * 16384);
                     if (j < w.n_ct) {
-                        const int32_t y = w.kvh * L[L_TOTAL_VALID] + R[R_CBASE] + j * kTileKeys;
+                        const int32_t y = w.kvh * L[L_TOTAL_VALID] + w.cbase + j * kTileKeys;
                         for (int hb = 0; hb < H; ++hb) tma_load_2d(sVs(vs) + hb * 16384, &tm_vcache, full, hb * 64, y);
                     } else {
-                        const int32_t fr = R[R_ROW_BASE] + (j - w.n_ct) * kTileKeys;
+                        const int32_t fr = w.row_base + (j - w.n_ct) * kTileKeys;
                         for (int hb = 0; hb < H; ++hb)
                             tma_load_3d(sVs(vs) + hb * 16384, &tm_vfresh, full, hb * 64, w.kvh, fr);
                     }
@@ -475,6 +493,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const uint32_t tO = tmem + lane_addr + kTmemO + t * 128;
         int hq = 0, kc = 0;   // halves / key tiles this CTA processed before the item
         bool ok = true;
+        bool have_pre = false;   // this row's position for the item was loaded during the last epilogue
+        int32_t pos_pre = -1;
         for (int it = 0; ok; ++it) {
             AttnItem w;
             ok = take_item(it, w);
@@ -482,28 +502,27 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_ITEM_EMPTY + (it & 1)]);
             if (w.req < 0) break;
-            const int32_t* R = L + L[L_OFF_REQ] + w.req * R_STRIDE;
-            const int n_rows_req = LSE ? R[R_N_QUERY] : R[R_N_ROWS];
-            const int32_t row_base = R[R_ROW_BASE];
+            const int n_rows_req = w.n_rows;
+            const int32_t row_base = w.row_base;
             const int row = w.qpair * kQTilesPerCta * toks_per_tile + t * toks_per_tile + tok;
             const bool valid = row < n_rows_req;
             int32_t mypos;
             if (LSE) mypos = valid ? kNoPos - 1 : -1;
-            else mypos = valid ? prm.row_pos[row_base + row] : -1;
+            else mypos = have_pre ? pos_pre : (valid ? prm.row_pos[row_base + row] : -1);
+            have_pre = false;
             // output locations, fixed before the tile loop so that only one pointer stays live
             // across it (a split key range writes a normalized partial row plus its max and sum)
             __nv_bfloat16* out_row = nullptr;
             float2* ml_slot = nullptr;
             if (valid) {
                 if (LSE) {
-                    ml_slot = prm.lse_part + R[R_LSE_BASE] +
-                              ((int64_t)w.kvh * (R[R_N_QUERY] * g) + row * g + hl) * R[R_LSE_CHUNKS] + w.chunk;
+                    ml_slot = prm.lse_part + w.lse_base +
+                              ((int64_t)w.kvh * (n_rows_req * g) + row * g + hl) * w.lse_chunks + w.chunk;
                 } else {
-                    const int32_t* PR = L + L[L_OFF_PAIR] + (R[R_PAIR_BASE] + w.qpair) * P_STRIDE;
-                    if (PR[P_NSPLIT] == 1) {
+                    if (w.nsplit == 1) {
                         out_row = prm.out + ((int64_t)(row_base + row) * Hq + w.kvh * g + hl) * D;
                     } else {
-                        const int64_t prow = (int64_t)(PR[P_SLOT_BASE] + w.kvh * PR[P_NSPLIT] + w.chunk) *
+                        const int64_t prow = (int64_t)(w.slot_base + w.kvh * w.nsplit + w.chunk) *
                                                  (kQTilesPerCta * kTileRows) + t * kTileRows + m;
                         out_row = prm.part_o + prow * D;
                         ml_slot = prm.part_ml + prow;
@@ -517,7 +536,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 const int hg = hq + q, kt = kc + (q >> 1), h = q & 1, ks = kt & 1;
                 const uint32_t tS = tmem + lane_addr + t * 128 + (hg & 1) * 64;
                 ok = mbar_wait(&bars[B_S_FULL + 2 * t + (hg & 1)], (hg >> 1) & 1, abort_flag);
-                if (h == 0) ok = ok && mbar_wait(&bars[B_K_FULL + ks], (kt >> 1) & 1, abort_flag);
+                if (h == 0) ok = ok && mbar_wait(&bars[B_KPOS_FULL + ks], (kt >> 1) & 1, abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
                 if (h == 0) {
@@ -603,9 +622,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (LSE) {
                 // The last key chunk of this (request, kv head, tile pair) to finish combines every
                 // row's chunks, in chunk order, into the row's log2-sum-exp over all cached keys.
-                const int chunks = R[R_LSE_CHUNKS];
-                const int cidx = R[R_LSE_PAIR_BASE] +
-                                 w.kvh * ((R[R_N_QUERY] * g + 2 * kTileRows - 1) / (2 * kTileRows)) + w.qpair;
+                const int chunks = w.lse_chunks;
+                const int cidx = w.lse_cidx;
                 // (mbarriers with bounded waits rather than a named barrier: a softmax warp that
                 // gave up on an earlier wait must not leave the others blocked)
                 __threadfence();
@@ -620,8 +638,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 if (misc[7]) {
                     __threadfence();
                     if (valid) {
-                        const float2* ml = prm.lse_part + R[R_LSE_BASE] +
-                                           ((int64_t)w.kvh * (R[R_N_QUERY] * g) + row * g + hl) * chunks;
+                        const float2* ml = prm.lse_part + w.lse_base +
+                                           ((int64_t)w.kvh * (n_rows_req * g) + row * g + hl) * chunks;
                         // all chunks are loaded at once (chunks <= kMaxSplits), then combined in order
                         float2 v[kMaxSplits];
 #pragma unroll
@@ -634,12 +652,22 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
                         for (int c = 0; c < kMaxSplits; ++c)
                             if (c < chunks) S += v[c].y * ex2(v[c].x - M);
-                        prm.lse_final[((int64_t)w.kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row) * g + hl] =
+                        prm.lse_final[((int64_t)w.kvh * L[L_TOTAL_QUERY] + w.q_base + row) * g + hl] =
                             S > 0.f ? M + log2f(S) : INFINITY;
                     }
                     if (tid == 0) prm.lse_count[cidx] = 0;
                 }
             } else {
+                // if the next item is already published, start loading this row's position for it
+                // now, so that the load runs under the epilogue
+                if (__all_sync(0xffffffffu, mbar_test_wait(&bars[B_ITEM_FULL + ((it + 1) & 1)], ((it + 1) >> 1) & 1))) {
+                    const AttnItem& wn = slots[(it + 1) & 1];
+                    if (wn.req >= 0) {
+                        const int rn = wn.qpair * kQTilesPerCta * toks_per_tile + t * toks_per_tile + tok;
+                        pos_pre = rn < wn.n_rows ? prm.row_pos[wn.row_base + rn] : -1;
+                        have_pre = true;
+                    }
+                }
                 // epilogue: O / l once the item's last P V is done (an item without key tiles has no
                 // O to read); then O is free for the next item's first P V
                 ok = mbar_wait(&bars[B_O_DONE + t], it & 1, abort_flag);
