@@ -581,18 +581,26 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 const float alpha = need ? ex2(m_run - m_new) : 1.0f;
                 if (need) { l_run *= alpha; m_run = m_new; }
                 const float msub = m_run == -INFINITY ? 0.f : m_run;
-                // p = 2^(s - m); P (bf16 pairs) goes over the half's first 32 S columns
-                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                // p = 2^(s - m); P (bf16 pairs) goes over the half's first 32 S columns.  The
+                // subtraction and the running sums use packed fp32 pairs.
+                const uint64_t negm2 = f2_pack(-msub, -msub);
+                uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2(__uint_as_float(sv[2 * e]) - msub);
-                    const float p1 = ex2(__uint_as_float(sv[2 * e + 1]) - msub);
-                    sum4[e & 3] += p0 + p1;
+                    float d0, d1;
+                    f2_unpack(f2_add(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), negm2), d0, d1);
+                    const float p0 = ex2(d0), p1 = ex2(d1);
+                    acc2[e & 1] = f2_add(acc2[e & 1], f2_pack(p0, p1));
                     pk[e] = pack_bf16x2(p0, p1);
                 }
                 if (!LSE) tmem_st32(tS, pk);
-                l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                {
+                    float a0, a1, b0, b1;
+                    f2_unpack(acc2[0], a0, a1);
+                    f2_unpack(acc2[1], b0, b1);
+                    l_run += (a0 + b0) + (a1 + b1);
+                }
                 if (LSE) {
                     tc_fence_before();
                     mbar_arrive(&bars[B_P_FULL + 2 * t + (hg & 1)]);
