@@ -191,15 +191,16 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const int32_t* __res
     __shared__ int s_hist[256];
     __shared__ int s_warp[kTopkThreads / 32];
     __shared__ int s_bucket, s_above;
-    grid_dep_wait();
-    grid_dep_launch();
+    // layout fields first: they do not depend on the previous kernel, which may still be running
     const int n_spans = L[L_N_SPANS];
     const int tid = threadIdx.x;
     if ((int)blockIdx.x >= n_spans) {
         const int b = blockIdx.x - n_spans;
         const int32_t* R = L + L[L_OFF_REQ] + b * R_STRIDE;
-        const int32_t rb = R[R_ROW_BASE] + R[R_N_SEL];
-        for (int t = tid; t < R[R_N_QUERY]; t += kTopkThreads) row_pos[rb + t] = R[R_QUERY_POS0] + t;
+        const int32_t rb = R[R_ROW_BASE] + R[R_N_SEL], nq = R[R_N_QUERY], p0 = R[R_QUERY_POS0];
+        grid_dep_wait();
+        grid_dep_launch();
+        for (int t = tid; t < nq; t += kTopkThreads) row_pos[rb + t] = p0 + t;
         return;
     }
     const int32_t* S = L + L[L_OFF_SPAN] + blockIdx.x * S_STRIDE;
@@ -208,8 +209,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const int32_t* __res
     const int k = S[S_K];
     const int tok0 = S[S_PAGE_OFF] * kPage;              // request-local index of the span's first token
     const float* v = imp + R[R_TOK_BASE] + tok0;
+    const int32_t sel_base = R[R_SEL_BASE] + S[S_SEL_OFF];
+    const int32_t rrow = R[R_ROW_BASE] + S[S_SEL_OFF];
+    const int32_t* ppos = L + L[L_OFF_PAGEPOS] + R[R_PAGE_BASE] + S[S_PAGE_OFF];
+    uint16_t* ex = excl + R[R_PAGE_BASE] + S[S_PAGE_OFF];
     const int nwords = (len + 31) >> 5;
     for (int i = tid; i < nwords; i += kTopkThreads) s_bits[i] = 0u;
+    grid_dep_wait();
+    grid_dep_launch();
 
     uint32_t thr = 0;      // key of the k-th largest value
     int need_eq = 0;       // how many tokens equal to thr are taken (lowest indices first)
@@ -282,9 +289,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const int32_t* __res
     int total = 0;
     const int out_before = block_excl_scan<kTopkThreads>(n_sel, s_warp, &total);
     if (tid == 0 && total != k) set_dev_error(kDevErrBounds);
-    const int32_t sel_base = R[R_SEL_BASE] + S[S_SEL_OFF];
-    const int32_t rrow = R[R_ROW_BASE] + S[S_SEL_OFF];
-    const int32_t* ppos = L + L[L_OFF_PAGEPOS] + R[R_PAGE_BASE] + S[S_PAGE_OFF];
     int o = out_before;
     for (int i = i0; i < i1; ++i) {
         if ((s_bits[i >> 5] >> (i & 31)) & 1u) {
@@ -296,8 +300,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const int32_t* __res
         }
     }
     __syncthreads();
-    uint16_t* ex = excl + R[R_PAGE_BASE] + S[S_PAGE_OFF];
-    for (int p = tid; p < S[S_N_PAGES]; p += kTopkThreads)
+    for (int p = tid; p < len / kPage; p += kTopkThreads)
         ex[p] = (uint16_t)((s_bits[p >> 1] >> ((p & 1) * 16)) & 0xFFFFu);
 }
 
@@ -308,8 +311,6 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
                                                      const int32_t* __restrict__ sel_idx,
                                                      const uint4* __restrict__ src, int32_t row_chunks,
                                                      uint4* __restrict__ dst) {
-    grid_dep_wait();
-    grid_dep_launch();
     const int32_t r = blockIdx.x;
     const int n_reqs = L[L_N_REQS];
     const int32_t* REQ = L + L[L_OFF_REQ];
@@ -319,12 +320,16 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
         if (REQ[mid * R_STRIDE + R_SEL_BASE] <= r) lo = mid; else hi = mid - 1;
     }
     const int32_t* R = REQ + lo * R_STRIDE;
+    const int32_t n_tok = R[R_N_PAGES] * kPage, tok_base = R[R_TOK_BASE];
+    // the layout search above does not depend on the previous kernel (which writes sel_idx)
+    grid_dep_wait();
+    grid_dep_launch();
     const int32_t j = sel_idx[r];
-    if (j < 0 || j >= R[R_N_PAGES] * kPage) {
+    if (j < 0 || j >= n_tok) {
         if (threadIdx.x == 0) set_dev_error(kDevErrBounds);
         return;
     }
-    const uint4* s = src + (int64_t)(R[R_TOK_BASE] + j) * row_chunks;
+    const uint4* s = src + (int64_t)(tok_base + j) * row_chunks;
     uint4* d = dst + (int64_t)r * row_chunks;
     for (int c = threadIdx.x; c < row_chunks; c += blockDim.x) d[c] = __ldg(s + c);
 }
@@ -338,11 +343,11 @@ __global__ void __launch_bounds__(kScanThreads) compact_scan_kernel(const int32_
                                                                     const uint16_t* __restrict__ excl,
                                                                     int32_t* __restrict__ cidx) {
     __shared__ int s_warp[kScanThreads / 32];
-    grid_dep_wait();
-    grid_dep_launch();
     const int32_t* R = L + L[L_OFF_REQ] + blockIdx.x * R_STRIDE;
     const int n_pages = R[R_N_PAGES], pb = R[R_PAGE_BASE];
     int carry = R[R_CBASE];
+    grid_dep_wait();   // the exclusion bits come from the previous kernels
+    grid_dep_launch();
     for (int p0 = 0; p0 < n_pages; p0 += kScanThreads) {
         const int p = p0 + threadIdx.x;
         const int kept = p < n_pages ? kPage - __popc((uint32_t)excl[pb + p]) : 0;
@@ -366,8 +371,6 @@ __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict_
                                                       __nv_bfloat16* __restrict__ out) {
     constexpr int CH = D / 8;                   // 16-byte chunks per row
     constexpr int RPB = 256 / CH;               // rows per block
-    grid_dep_wait();
-    grid_dep_launch();
     const int32_t* item = L + L[L_OFF_COMB] + kItemWords * blockIdx.x;
     const int req = item[0], kvh = item[1], qpair = item[2];
     const int32_t* R = L + L[L_OFF_REQ] + req * R_STRIDE;
@@ -379,8 +382,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict_
     const int tpt = kTileRows / g;
     const int tt = pr / kTileRows, mm = pr % kTileRows;
     const int row = qpair * kQTilesPerCta * tpt + tt * tpt + mm / g;
-    if (row >= R[R_N_ROWS]) return;
+    const int32_t out_row = R[R_ROW_BASE] + row;
     const int64_t slot0 = (int64_t)PR[P_SLOT_BASE] + (int64_t)kvh * ns;
+    const bool in_range = row < R[R_N_ROWS];
+    // the layout fields above do not depend on the attention kernel, which may still be running
+    grid_dep_wait();
+    grid_dep_launch();
+    if (!in_range) return;
     const int64_t stride = kQTilesPerCta * kTileRows;
     float M = -INFINITY, W = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -408,7 +416,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict_
     o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
     o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
     const int hl = mm % g;
-    *reinterpret_cast<uint4*>(out + ((int64_t)(R[R_ROW_BASE] + row) * Hq + kvh * g + hl) * D + 8 * c) = o;
+    *reinterpret_cast<uint4*>(out + ((int64_t)out_row * Hq + kvh * g + hl) * D + 8 * c) = o;
 }
 
 }  // namespace pcf
