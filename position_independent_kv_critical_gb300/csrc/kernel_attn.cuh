@@ -120,7 +120,7 @@ enum : int {
     B_V_EMPTY = 9,     // [2] both P V that read the stage are done (one commit per issuer)
     B_S_FULL = 11,     // [4] per (Q tile, S half-buffer): S = Q K^T of a 64-key half landed
     B_P_FULL = 15,     // [4] per (Q tile, S half-buffer): P written and O rescaled; in LSE mode:
-                       //     softmax done reading that S half
+                       //     the softmax has loaded that S half into registers
     B_PV_DONE = 19,    // [4] per (Q tile, S half-buffer): P V of that buffer's latest half is done
     B_O_DONE = 23,     // [2] per Q tile: the item's last P V is done (one phase per item)
     B_DRAIN = 25,      // [4] per issuer: its last MMA is done
@@ -561,6 +561,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
                 tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
                 tmem_ld_wait();
+                if (LSE) {
+                    // nothing goes back to TMEM in LSE mode: the S buffer is free for the next Q K^T
+                    // as soon as its scores are in registers
+                    tc_fence_before();
+                    mbar_arrive(&bars[B_P_FULL + 2 * t + (hg & 1)]);
+                }
                 if (!full) {
                     // keys at or beyond the causal limit leave the row: score -inf
 #pragma unroll
@@ -601,10 +607,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     f2_unpack(acc2[1], b0, b1);
                     l_run += (a0 + b0) + (a1 + b1);
                 }
-                if (LSE) {
-                    tc_fence_before();
-                    mbar_arrive(&bars[B_P_FULL + 2 * t + (hg & 1)]);
-                } else {
+                if (!LSE) {
                     if (q > 0 && __any_sync(0xffffffffu, need)) {
                         // every earlier P V of this tile must be done before O is rescaled
                         ok = mbar_wait(&bars[B_PV_DONE + 2 * t + ((hg - 1) & 1)], ((hg - 1) >> 1) & 1, abort_flag);

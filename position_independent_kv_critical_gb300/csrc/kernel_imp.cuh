@@ -14,12 +14,11 @@
 //
 // One CTA per (request, run of key tiles, kv head).  Key tiles and 256-row query chunks stream
 // through two-stage rings and the S^T accumulator is double-buffered in TMEM, so the tensor core
-// works on the next (tile, chunk) step while the exponentials of the current one run.  The
-// per-kv-head partial sums of a run are reduced in fixed head order by the last CTA of the run
-// (deterministic).
+// works on the next (tile, chunk) step while the exponentials of the current one run.  Each
+// (kv head, query column half) writes its own partial sum per key; the last CTA of a run adds them
+// in fixed order (heads, then halves: deterministic).
 //   warps 0-7  exp-sum: warp w owns keys 32(w%4) .. +31 (its TMEM lane quarter) and the query
-//              columns 128(w/4) .. +127 of every step; the two column halves of a key are added
-//              through shared memory at the end of each tile
+//              columns 128(w/4) .. +127 of every step
 //   warp  8    TMEM allocation + single-thread tcgen05.mma issue
 //   warp  9    TMA producer (key tiles, query chunks)
 #pragma once
@@ -36,7 +35,7 @@ constexpr int kImpQRows = 256;
 struct ImpParams {
     const int32_t* layout;
     const float* lse_final;  // [Hkv][total_query][g] log2-sum-exp of every query row
-    float* part;             // [Hkv][total_tokens]
+    float* part;             // [2][Hkv][total_tokens]: query column half, kv head, token
     int32_t* counters;       // [total key tiles], zero on entry, left zero on exit
     float* importance;       // [total_tokens]
 };
@@ -52,8 +51,7 @@ struct ImpSmem {
     static constexpr int kSlabK = kTileKeys * 16 * 2;  // [128][16] fp16: ones in columns 0 and 1
     static constexpr int oQlse = oQ + 2 * kQ;          // 2 slabs (one per query-chunk buffer)
     static constexpr int oKones = oQlse + 2 * kSlabQ;
-    static constexpr int oPart = oKones + kSlabK;      // [128] second column half of each key
-    static constexpr int oBar = oPart + kTileKeys * 4;
+    static constexpr int oBar = oKones + kSlabK;
     static constexpr int kNumBars = 16;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int kBytes = oMisc + 64;
@@ -196,10 +194,10 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     } else {
         // warps 0-7: thread owns key `key` of every tile of the run, query columns ch*128 .. +127
         const int key = tid & 127, ch = tid >> 7;
-        float* sPart = reinterpret_cast<float*>(smem + SM::oPart);
         const float* lse_g = prm.lse_final + ((int64_t)kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE]) * g;
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         const int total_tokens = L[L_TOTAL_TOKENS];
+        const int32_t tok_base = R[R_TOK_BASE];
         // -lse2 of step s's query chunk into its slab, as fp16 hi + lo (-30000 past the last row:
         // those columns contribute 0); thread tid writes row tid
         auto prep = [&](int s) {
@@ -216,9 +214,8 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (n_steps > 0) prep(0);
         if (!q_resident && n_steps > 1) prep(1);
         bool ok = true;
-        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
-        // every one of the 256 threads runs every step (a named barrier at each tile end): after an
-        // abort the work is skipped, the barrier count stays the same
+        uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+        float* part_h = prm.part + ((int64_t)ch * Hkv + kvh) * total_tokens;   // this thread's half
         for (int s = 0; s < n_steps; ++s) {
             const int i = s / n_qc, qc = s - i * n_qc, a = s & 1;
             if (ok) ok = mbar_wait(&bars[I_ACC_FULL + a], (s >> 1) & 1, abort_flag);
@@ -235,28 +232,26 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) acc4[e & 3] += ex2(__uint_as_float(sv[cc][e]));
+                    for (int e = 0; e < 32; e += 2)
+                        acc2[(e >> 1) & 1] = f2_add(acc2[(e >> 1) & 1], f2_pack(ex2(__uint_as_float(sv[cc][e])),
+                                                                              ex2(__uint_as_float(sv[cc][e + 1]))));
                 // step s's MMA is complete, so its slab buffer takes step s + 2's chunk
                 if (!q_resident && s + 2 < n_steps) prep(s + 2);
             }
             if (qc == n_qc - 1) {
-                const float accv = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-                acc4[0] = acc4[1] = acc4[2] = acc4[3] = 0.f;
-                if (ch == 1) sPart[key] = accv;
-                named_sync_exp();
-                if (ch == 0) {
-                    const int t = t0 + i;
-                    const bool valid_key = (t * kPagesPerTile + key / kPage) < n_pages;
-                    const int32_t tok = R[R_TOK_BASE] + t * kTileKeys + key;
-                    if (ok && valid_key) prm.part[(int64_t)kvh * total_tokens + tok] = accv + sPart[key];
-                }
-                named_sync_exp();   // sPart is reused by the next tile
+                float a0, a1, b0, b1;
+                f2_unpack(acc2[0], a0, a1);
+                f2_unpack(acc2[1], b0, b1);
+                acc2[0] = acc2[1] = f2_pack(0.f, 0.f);
+                const int t = t0 + i;
+                const bool valid_key = (t * kPagesPerTile + key / kPage) < n_pages;
+                if (ok && valid_key) part_h[tok_base + t * kTileKeys + key] = (a0 + b0) + (a1 + b1);
             }
         }
-        if (n_qc == 0 && ch == 0)   // a request without query rows: every importance is 0
+        if (n_qc == 0)   // a request without query rows: every importance is 0
             for (int i = 0; i < nt; ++i)
                 if (((t0 + i) * kPagesPerTile + key / kPage) < n_pages)
-                    prm.part[(int64_t)kvh * total_tokens + R[R_TOK_BASE] + (t0 + i) * kTileKeys + key] = 0.f;
+                    part_h[tok_base + (t0 + i) * kTileKeys + key] = 0.f;
         // the last of the run's Hkv CTAs sums the heads in order
         __threadfence();
         named_sync_exp();
@@ -270,7 +265,9 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 if ((t * kPagesPerTile + k / kPage) >= n_pages) continue;
                 const int32_t tok = R[R_TOK_BASE] + t * kTileKeys + k;
                 float sum = 0.f;
-                for (int h = 0; h < Hkv; ++h) sum += __ldcg(prm.part + (int64_t)h * total_tokens + tok);
+                for (int h = 0; h < Hkv; ++h)
+                    sum += __ldcg(prm.part + (int64_t)h * total_tokens + tok) +
+                           __ldcg(prm.part + ((int64_t)Hkv + h) * total_tokens + tok);
                 prm.importance[tok] = sum;
             }
             if (tid == 0) prm.counters[cidx] = 0;

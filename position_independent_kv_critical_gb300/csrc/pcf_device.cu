@@ -123,7 +123,8 @@ ScoreWs score_ws(const int32_t* H) {
     w.lse = align_up(w.kc + kc_bytes(H));
     w.lsef = align_up(w.lse + (size_t)H[L_LSE_SLOTS] * sizeof(float2));
     w.part = align_up(w.lsef + (size_t)H[L_TOTAL_QUERY] * H[L_HQ] * sizeof(float));
-    w.cnt = align_up(w.part + (size_t)H[L_HKV] * H[L_TOTAL_TOKENS] * sizeof(float));
+    // importance partials: per kv head and token, one per half of the query columns
+    w.cnt = align_up(w.part + 2 * (size_t)H[L_HKV] * H[L_TOTAL_TOKENS] * sizeof(float));
     // counters: importance runs (one per key tile at most), the LSE pass's (kv head, pair)s, and
     // the LSE kernel's item counter
     w.total = align_up(w.cnt + ((size_t)H[L_TOTAL_KTILES] + H[L_N_LSE_PAIRS] + 1) * sizeof(int32_t));
