@@ -636,18 +636,18 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 const int chunks = w.lse_chunks;
                 const int cidx = w.lse_cidx;
                 // (mbarriers with bounded waits rather than a named barrier: a softmax warp that
-                // gave up on an earlier wait must not leave the others blocked)
-                __threadfence();
+                // gave up on an earlier wait must not leave the others blocked; the barriers order
+                // the 256 threads' partial writes before, and their reads after, thread 0's
+                // acquire-release increment)
                 mbar_arrive(&bars[B_FIN]);
                 if (tid == 0) {
                     const bool okf = mbar_wait(&bars[B_FIN], it & 1, abort_flag);
-                    misc[7] = okf && atomicAdd(prm.lse_count + cidx, 1) == chunks - 1 ? 1 : 0;
+                    misc[7] = okf && atomic_add_acq_rel_gpu(prm.lse_count + cidx, 1) == chunks - 1 ? 1 : 0;
                     mbar_arrive(&bars[B_FIN2]);
                 }
                 ok = mbar_wait(&bars[B_FIN2], it & 1, abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 if (misc[7]) {
-                    __threadfence();
                     if (valid) {
                         const float2* ml = prm.lse_part + w.lse_base +
                                            ((int64_t)w.kvh * (n_rows_req * g) + row * g + hl) * chunks;

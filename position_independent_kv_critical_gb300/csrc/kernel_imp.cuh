@@ -252,14 +252,13 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             for (int i = 0; i < nt; ++i)
                 if (((t0 + i) * kPagesPerTile + key / kPage) < n_pages)
                     part_h[tok_base + (t0 + i) * kTileKeys + key] = 0.f;
-        // the last of the run's Hkv CTAs sums the heads in order
-        __threadfence();
+        // the last of the run's Hkv CTAs sums the heads in order (the named barriers order the
+        // partial writes before, and the reads after, thread 0's acquire-release increment)
         named_sync_exp();
         const int cidx = R[R_KTILE_BASE] + t0;
-        if (tid == 0) misc[5] = (atomicAdd(&prm.counters[cidx], 1) == Hkv - 1) ? 1 : 0;
+        if (tid == 0) misc[5] = (atomic_add_acq_rel_gpu(&prm.counters[cidx], 1) == Hkv - 1) ? 1 : 0;
         named_sync_exp();
         if (misc[5]) {
-            __threadfence();
             for (int idx = tid; idx < nt * kTileKeys; idx += kImpExpThreads) {
                 const int t = t0 + idx / kTileKeys, k = idx % kTileKeys;
                 if ((t * kPagesPerTile + k / kPage) >= n_pages) continue;

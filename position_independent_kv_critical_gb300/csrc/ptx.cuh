@@ -114,6 +114,18 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
     }
 }
 
+// ---------------------------------------------------------------- cross-CTA hand-off
+// "Last one finishes the job": a CTA's threads write their results, meet at a CTA barrier, and one
+// thread adds 1 to a counter with acquire-release semantics at GPU scope.  The release makes
+// everything the CTA wrote before the barrier visible with the increment (release is cumulative);
+// the acquire lets the CTA that sees the final count read what every other CTA wrote, once its
+// other threads are ordered after that thread by a second CTA barrier.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // ---------------------------------------------------------------- proxies / fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
