@@ -309,16 +309,15 @@ def main():
     d2h = out_h.numel() * out_h.element_size() + sel_h.numel() * sel_h.element_size()
     Ke = min(K, 50)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(2):   # warm-up: the pipelined step allocates its input slots and streams once
+        cf.step_from_host(hq_q, *hq_f, k_pool, v_pool, out_h, sel_h, hidden)
+    cf.wait_host_results()
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(Ke):
-        q_query.copy_(hq_q, non_blocking=True)
-        q_fresh.copy_(hq_f[0], non_blocking=True)
-        k_fresh.copy_(hq_f[1], non_blocking=True)
-        v_fresh.copy_(hq_f[2], non_blocking=True)
-        cf.step(q_query, k_pool, v_pool, q_fresh, k_fresh, v_fresh, hidden)
-        out_h.copy_(cf.out, non_blocking=True)
-        sel_h.copy_(cf.sel_idx, non_blocking=True)
+        # every step uploads its query and fresh rows and brings O and the selection back
+        cf.step_from_host(hq_q, *hq_f, k_pool, v_pool, out_h, sel_h, hidden)
+    cf.wait_host_results()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / Ke

@@ -207,3 +207,65 @@ class CacheFusion:
         fused_attention(L, q_fresh, k_fresh, v_fresh, k_pool, v_pool, self.excl, self.row_pos,
                         self.rope, self.out, self.ws_attn, stream)
         return self.out
+
+    def step_from_host(self, q_query_h, q_fresh_h, k_fresh_h, v_fresh_h, k_pool, v_pool, out_h, sel_h,
+                       hidden=None):
+        """``step`` with the per-step inputs in pinned host memory and the results (O and the
+        selected token indices) copied back to pinned host buffers.
+
+        The copies run on two streams of their own and overlap the kernels: the query rows go up
+        first (scoring needs only them), the fresh Q/K/V rows while scoring runs, and the results
+        come down while the next step starts.  Device input buffers alternate between two slots, so
+        a step's uploads never overwrite rows the previous step's kernels may still read.  The host
+        inputs must stay unchanged, and ``out_h`` / ``sel_h`` unread, until ``wait_host_results()``
+        (or a device synchronisation) has returned."""
+        L = self.layout
+        main = torch.cuda.current_stream()
+        if not hasattr(self, "_h2d"):
+            self._h2d = torch.cuda.Stream()
+            self._d2h = torch.cuda.Stream()
+            self._slots = [tuple(torch.empty_like(t, device=self.out.device)
+                                 for t in (q_query_h, q_fresh_h, k_fresh_h, v_fresh_h)) for _ in range(2)]
+            self._ev_q = [torch.cuda.Event() for _ in range(2)]
+            self._ev_fresh = [torch.cuda.Event() for _ in range(2)]
+            self._ev_used = [None, None]     # the last step that read slot i has finished with it
+            self._ev_down = None             # the last step's results have reached the host
+            self._it = 0
+        i = self._it & 1
+        qq, qf, kf, vf = self._slots[i]
+        with torch.cuda.stream(self._h2d):
+            if self._ev_used[i] is not None:
+                self._h2d.wait_event(self._ev_used[i])
+            qq.copy_(q_query_h, non_blocking=True)
+            self._ev_q[i].record(self._h2d)
+            qf.copy_(q_fresh_h, non_blocking=True)
+            kf.copy_(k_fresh_h, non_blocking=True)
+            vf.copy_(v_fresh_h, non_blocking=True)
+            self._ev_fresh[i].record(self._h2d)
+        main.wait_event(self._ev_q[i])
+        score(L, qq, k_pool, self.rope, self.importance, self.ws_score)
+        if self._ev_down is not None:      # sel_idx and out of the previous step are on their way down
+            main.wait_event(self._ev_down)
+        select_topk(L, self.importance, self.sel_idx, self.excl, self.row_pos)
+        if hidden is not None and self.gathered is not None:
+            gather_rows(L, self.sel_idx, hidden, self.gathered)
+        main.wait_event(self._ev_fresh[i])
+        fused_attention(L, qf, kf, vf, k_pool, v_pool, self.excl, self.row_pos, self.rope, self.out,
+                        self.ws_attn)
+        used = torch.cuda.Event()
+        used.record(main)
+        self._ev_used[i] = used
+        with torch.cuda.stream(self._d2h):
+            self._d2h.wait_event(used)
+            out_h.copy_(self.out, non_blocking=True)
+            sel_h.copy_(self.sel_idx, non_blocking=True)
+            down = torch.cuda.Event()
+            down.record(self._d2h)
+        self._ev_down = down
+        self._it += 1
+        return out_h
+
+    def wait_host_results(self):
+        """Make the current stream wait until the last ``step_from_host`` results are on the host."""
+        if getattr(self, "_ev_down", None) is not None:
+            torch.cuda.current_stream().wait_event(self._ev_down)

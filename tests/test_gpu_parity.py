@@ -161,6 +161,52 @@ def test_score_is_deterministic():
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
+def test_step_from_host_matches_device_step():
+    """The pipelined host-input step (uploads and downloads on their own streams, two input slots)
+    gives bit for bit the device step's O and selection, with four steps on two different input
+    sets issued back to back before any of them is waited for."""
+    b = make_batch("llama8b_layer")
+    mp = b.max_pos + 1
+    L = pcf.Layout(b.requests, b.hq, b.hkv, b.d, b.n_phys_pages, mp)
+    rope = pcf.rope_table(b.d, b.theta, mp).cuda()
+    cf = pcf.CacheFusion(L, rope)
+    k_pool, v_pool = b.k_pool.cuda(), b.v_pool.cuda()
+    sets = [(b.q_query, b.q_fresh, b.k_fresh, b.v_fresh),
+            ((b.q_query.float() * -0.75).to(torch.bfloat16), (b.q_fresh.float() * 0.5).to(torch.bfloat16),
+             b.k_fresh.flip(0).contiguous(), (b.v_fresh.float() * -1.0).to(torch.bfloat16))]
+    refs = []
+    for qq, qf, kf, vf in sets:
+        out = cf.step(qq.cuda(), k_pool, v_pool, qf.cuda(), kf.cuda(), vf.cuda())
+        refs.append((out.cpu().clone(), cf.sel_idx.cpu().clone()))
+    torch.cuda.synchronize()
+    host = [[t.pin_memory() for t in st] for st in sets]
+    outs = [torch.zeros_like(cf.out, device="cpu").pin_memory() for _ in range(4)]
+    sels = [torch.zeros_like(cf.sel_idx, device="cpu").pin_memory() for _ in range(4)]
+    for k in range(4):
+        cf.step_from_host(*host[k % 2], k_pool, v_pool, outs[k], sels[k])
+    cf.wait_host_results()
+    torch.cuda.synchronize()
+    pcf.check_device_error()
+    for k in range(4):
+        ref_out, ref_sel = refs[k % 2]
+        assert torch.equal(outs[k].view(torch.int16), ref_out.view(torch.int16)), k
+        assert torch.equal(sels[k], ref_sel), k
+
+
+def test_attention_is_deterministic_under_dynamic_item_order():
+    """The persistent attention kernel hands items to CTAs in whatever order they free up; each
+    item's rows (or partial slot) are written by whichever CTA runs it, so two runs must agree
+    bit for bit (long context: about four items per CTA, no key-range splits; Llama-8B layer:
+    split items merged afterwards)."""
+    for name in ("llama8b_layer", "long_context"):
+        gb = gpu_batch(name)
+        gb.score()
+        gb.topk()
+        a = gb.attention().copy()
+        b = gb.attention().copy()
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), name
+
+
 # ------------------------------------------------------------------ scenarios from the pages
 
 def test_offset_0_and_2048_share_physical_pages():
