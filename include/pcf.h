@@ -197,6 +197,16 @@ pcf_status pcf_score_noalloc(const pcf_layout* layout, const uint16_t* q_query, 
  * PCF_ERR_DEVICE_TIMEOUT or PCF_ERR_DEVICE_BOUNDS (PCF_ERR_CUDA if the sync itself failed). */
 pcf_status pcf_check_device_error(void* stream);
 
+/* Queues `n` asynchronous copies on `stream`, in order: copy i moves bytes[i] bytes from src[i]
+ * to dst[i] with one cudaMemcpyAsync of kind cudaMemcpyDefault (the direction follows from the
+ * pointers: device memory or page-locked host memory).  Used by the pipelined host-input step to
+ * move a step's inputs and results in one call; the arrays are read before the call returns, the
+ * buffers must stay valid until the copies have run.  n == 0 queues nothing.
+ * Errors: PCF_ERR_INVALID_ARG if n < 0, or n > 0 and an array is null (nothing queued);
+ * PCF_ERR_NO_DEVICE without a usable device; PCF_ERR_CUDA if a copy fails to queue (the copies
+ * before it stay queued). */
+pcf_status pcf_copy_async(int32_t n, void* const* dst, const void* const* src, const size_t* bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -220,28 +220,44 @@ class CacheFusion:
         inputs must stay unchanged, and ``out_h`` / ``sel_h`` unread, until ``wait_host_results()``
         (or a device synchronisation) has returned."""
         L = self.layout
+        lib = _lib.load()
         main = torch.cuda.current_stream()
+        host_in = (q_query_h, q_fresh_h, k_fresh_h, v_fresh_h)
         if not hasattr(self, "_h2d"):
+            for t in host_in + (out_h, sel_h):
+                if t.is_cuda or not t.is_pinned():
+                    raise ValueError("step_from_host takes pinned host tensors")
             self._h2d = torch.cuda.Stream()
             self._d2h = torch.cuda.Stream()
-            self._slots = [tuple(torch.empty_like(t, device=self.out.device)
-                                 for t in (q_query_h, q_fresh_h, k_fresh_h, v_fresh_h)) for _ in range(2)]
+            self._slots = [tuple(torch.empty_like(t, device=self.out.device) for t in host_in) for _ in range(2)]
             self._ev_q = [torch.cuda.Event() for _ in range(2)]
             self._ev_fresh = [torch.cuda.Event() for _ in range(2)]
-            self._ev_used = [None, None]     # the last step that read slot i has finished with it
+            self._ev_used = [torch.cuda.Event() for _ in range(2)]   # slot i's last reader is done
+            self._ev_down_slot = [torch.cuda.Event() for _ in range(2)]
             self._ev_down = None             # the last step's results have reached the host
             self._it = 0
         i = self._it & 1
         qq, qf, kf, vf = self._slots[i]
-        with torch.cuda.stream(self._h2d):
-            if self._ev_used[i] is not None:
-                self._h2d.wait_event(self._ev_used[i])
-            qq.copy_(q_query_h, non_blocking=True)
-            self._ev_q[i].record(self._h2d)
-            qf.copy_(q_fresh_h, non_blocking=True)
-            kf.copy_(k_fresh_h, non_blocking=True)
-            vf.copy_(v_fresh_h, non_blocking=True)
-            self._ev_fresh[i].record(self._h2d)
+        n_in = [t.numel() * t.element_size() for t in host_in]
+        if any(n != d.numel() * d.element_size() for n, d in zip(n_in, self._slots[i])):
+            raise ValueError("step_from_host inputs changed size between steps")
+        if (out_h.numel() * out_h.element_size() != self.out.numel() * self.out.element_size()
+                or sel_h.numel() * sel_h.element_size() != self.sel_idx.numel() * self.sel_idx.element_size()):
+            raise ValueError("step_from_host result buffers must match out and sel_idx in size")
+
+        def copies(dst, src, nbytes, stream):
+            n = len(dst)
+            _lib.check("pcf_copy_async", lib.pcf_copy_async(
+                n, (ctypes.c_void_p * n)(*[t.data_ptr() for t in dst]),
+                (ctypes.c_void_p * n)(*[t.data_ptr() for t in src]), (ctypes.c_size_t * n)(*nbytes),
+                ctypes.c_void_p(stream.cuda_stream)))
+
+        if self._it >= 2:
+            self._h2d.wait_event(self._ev_used[i])
+        copies([qq], [q_query_h], n_in[:1], self._h2d)
+        self._ev_q[i].record(self._h2d)
+        copies([qf, kf, vf], [q_fresh_h, k_fresh_h, v_fresh_h], n_in[1:], self._h2d)
+        self._ev_fresh[i].record(self._h2d)
         main.wait_event(self._ev_q[i])
         score(L, qq, k_pool, self.rope, self.importance, self.ws_score)
         if self._ev_down is not None:      # sel_idx and out of the previous step are on their way down
@@ -252,16 +268,12 @@ class CacheFusion:
         main.wait_event(self._ev_fresh[i])
         fused_attention(L, qf, kf, vf, k_pool, v_pool, self.excl, self.row_pos, self.rope, self.out,
                         self.ws_attn)
-        used = torch.cuda.Event()
-        used.record(main)
-        self._ev_used[i] = used
-        with torch.cuda.stream(self._d2h):
-            self._d2h.wait_event(used)
-            out_h.copy_(self.out, non_blocking=True)
-            sel_h.copy_(self.sel_idx, non_blocking=True)
-            down = torch.cuda.Event()
-            down.record(self._d2h)
-        self._ev_down = down
+        self._ev_used[i].record(main)
+        self._d2h.wait_event(self._ev_used[i])
+        copies([out_h, sel_h], [self.out, self.sel_idx],
+               [out_h.numel() * out_h.element_size(), sel_h.numel() * sel_h.element_size()], self._d2h)
+        self._ev_down_slot[i].record(self._d2h)
+        self._ev_down = self._ev_down_slot[i]
         self._it += 1
         return out_h
 

@@ -29,7 +29,7 @@ EXPORTS = (
     "pcf_status_string", "pcf_k_from_percent", "pcf_rope_table_init", "pcf_layout_words",
     "pcf_layout_build", "pcf_layout_query", "pcf_score_workspace_bytes", "pcf_score",
     "pcf_select_topk", "pcf_gather_rows", "pcf_attention_workspace_bytes", "pcf_fused_attention",
-    "pcf_check_device_error", "pcf_score_noalloc",
+    "pcf_check_device_error", "pcf_score_noalloc", "pcf_copy_async",
 )
 
 
@@ -90,6 +90,8 @@ def _declare(lib):
     lib.pcf_score_noalloc.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     lib.pcf_check_device_error.restype = c_int32
     lib.pcf_check_device_error.argtypes = [c_void_p]
+    lib.pcf_copy_async.restype = c_int32
+    lib.pcf_copy_async.argtypes = [c_int32, c_void_p, c_void_p, c_void_p, c_void_p]
 
 
 def load(build_if_missing: bool = True):

@@ -3,10 +3,13 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <set>
+#include <tuple>
 #include <utility>
 
 #include "../../include/pcf.h"
@@ -34,21 +37,59 @@ bool get_encode() {
     return g_encode != nullptr;
 }
 
+// Tensor maps are pure functions of their arguments; a small per-thread cache keeps the
+// encoding off the per-call host path when a caller reuses its buffers from call to call.
+struct MapKey {
+    const void* base;
+    uint64_t dims[3], strides[2];
+    uint32_t box[3];
+    int32_t rank, dt;
+};
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    bool valid;
+};
+thread_local MapEntry t_maps[16];
+thread_local int t_maps_next = 0;
+
+pcf_status encode_cached(CUtensorMap* m, const MapKey& k) {
+    for (const MapEntry& e : t_maps)
+        if (e.valid && std::memcmp(&e.key, &k, sizeof(k)) == 0) {
+            *m = e.map;
+            return PCF_OK;
+        }
+    if (!get_encode()) return PCF_ERR_CUDA;
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, static_cast<CUtensorMapDataType>(k.dt), k.rank, const_cast<void*>(k.base), k.dims,
+                          k.strides, k.box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return PCF_ERR_CUDA;
+    MapEntry& e = t_maps[t_maps_next];
+    t_maps_next = (t_maps_next + 1) % 16;
+    e.key = k;
+    e.map = *m;
+    e.valid = true;
+    return PCF_OK;
+}
+
 // 2-D bf16 map over rows of `inner` elements (row stride `stride_bytes`), 128-byte swizzle,
 // box = 64 elements x box_rows rows.  An empty tensor gives an all-zero (never used) map.
 pcf_status make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_bytes,
                        uint32_t box_rows, CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     std::memset(m, 0, sizeof(*m));
     if (rows == 0 || base == nullptr) return PCF_OK;
-    if (!get_encode()) return PCF_ERR_CUDA;
-    const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {stride_bytes};
-    const cuuint32_t box[2] = {64, box_rows};
-    const cuuint32_t es[2] = {1, 1};
-    CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? PCF_OK : PCF_ERR_CUDA;
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.base = base;
+    k.dims[0] = inner;
+    k.dims[1] = rows;
+    k.strides[0] = stride_bytes;
+    k.box[0] = 64;
+    k.box[1] = box_rows;
+    k.rank = 2;
+    k.dt = static_cast<int32_t>(dt);
+    return encode_cached(m, k);
 }
 
 // 3-D map over [n2][n1][inner] (v_fresh: [rows][Hkv][D]), box = 64 x 1 x box2.
@@ -56,15 +97,20 @@ pcf_status make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_
                        uint32_t box2) {
     std::memset(m, 0, sizeof(*m));
     if (n2 == 0 || base == nullptr) return PCF_OK;
-    if (!get_encode()) return PCF_ERR_CUDA;
-    const cuuint64_t dims[3] = {inner, n1, n2};
-    const cuuint64_t strides[2] = {inner * 2, inner * n1 * 2};
-    const cuuint32_t box[3] = {64, 1, box2};
-    const cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? PCF_OK : PCF_ERR_CUDA;
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.base = base;
+    k.dims[0] = inner;
+    k.dims[1] = n1;
+    k.dims[2] = n2;
+    k.strides[0] = inner * 2;
+    k.strides[1] = inner * n1 * 2;
+    k.box[0] = 64;
+    k.box[1] = 1;
+    k.box[2] = box2;
+    k.rank = 3;
+    k.dt = static_cast<int32_t>(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    return encode_cached(m, k);
 }
 
 constexpr CUtensorMapDataType kF16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -79,14 +125,21 @@ pcf_status check_layout(const pcf_layout* lay) {
     return PCF_OK;
 }
 
-// sm_103 (GB300) must be the current device
+// sm_103 (GB300) must be the current device (the answer is kept per device ordinal)
 pcf_status check_device() {
+    static std::atomic<signed char> known[256];   // 0 unknown, 1 sm_103, -1 other
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PCF_ERR_NO_DEVICE;
+    if (dev >= 0 && dev < 256) {
+        const signed char k = known[dev].load(std::memory_order_relaxed);
+        if (k != 0) return k > 0 ? PCF_OK : PCF_ERR_NO_DEVICE;
+    }
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return PCF_ERR_NO_DEVICE;
-    return (major == 10 && minor == 3) ? PCF_OK : PCF_ERR_NO_DEVICE;
+    const bool ok = major == 10 && minor == 3;
+    if (dev >= 0 && dev < 256) known[dev].store(ok ? 1 : -1, std::memory_order_relaxed);
+    return ok ? PCF_OK : PCF_ERR_NO_DEVICE;
 }
 
 // Every kernel of the library is launched with programmatic stream serialization: its CTAs may be
@@ -151,11 +204,23 @@ AttnWs attn_ws(const int32_t* H) {
     return w;
 }
 
+// the dynamic shared-memory limit of a kernel, raised once per (kernel, device, size)
+std::mutex g_smem_mu;
+std::set<std::tuple<const void*, int, int>> g_smem_done;
 template <typename K>
 pcf_status set_smem(K kernel, int bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess
-               ? PCF_OK
-               : PCF_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PCF_ERR_CUDA;
+    const auto key = std::make_tuple(reinterpret_cast<const void*>(kernel), dev, bytes);
+    {
+        std::lock_guard<std::mutex> lock(g_smem_mu);
+        if (g_smem_done.count(key)) return PCF_OK;
+    }
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return PCF_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_smem_mu);
+    g_smem_done.insert(key);
+    return PCF_OK;
 }
 
 // threads of a RoPE job: one per (row, head group, chunk pair); a job with enough rows to fill the
@@ -401,6 +466,19 @@ extern "C" pcf_status pcf_fused_attention(const pcf_layout* layout, const uint16
     return H[L_D] == 128
                ? attention_impl<128>(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope, out, ws, st)
                : attention_impl<64>(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope, out, ws, st);
+}
+
+extern "C" pcf_status pcf_copy_async(int32_t n, void* const* dst, const void* const* src, const size_t* bytes,
+                                     void* stream) {
+    if (n < 0 || (n > 0 && (!dst || !src || !bytes))) return PCF_ERR_INVALID_ARG;
+    if (n == 0) return PCF_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PCF_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int32_t i = 0; i < n; ++i)
+        if (bytes[i] > 0 && cudaMemcpyAsync(dst[i], src[i], bytes[i], cudaMemcpyDefault, st) != cudaSuccess)
+            return PCF_ERR_CUDA;
+    return PCF_OK;
 }
 
 extern "C" pcf_status pcf_check_device_error(void* stream) {

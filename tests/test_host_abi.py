@@ -32,6 +32,13 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_copy_async_rejects_bad_arguments_before_touching_a_device(lib):
+    PCF_OK, PCF_ERR_INVALID_ARG = 0, -1
+    assert lib.pcf_copy_async(-1, None, None, None, None) == PCF_ERR_INVALID_ARG
+    assert lib.pcf_copy_async(2, None, None, None, None) == PCF_ERR_INVALID_ARG
+    assert lib.pcf_copy_async(0, None, None, None, None) == PCF_OK
+
+
 def test_status_strings(lib):
     for code in range(-7, 1):
         s = lib.pcf_status_string(code).decode()
