@@ -12,8 +12,9 @@
 // the key tiles from the call's rotated copy of the batch's cached keys (MiniPIC 2.1: rotation to
 // the request's logical positions at use time).
 //
-// One CTA per (request, run of key tiles, kv head).  Key tiles and 256-row query chunks stream
-// through two-stage rings and the S^T accumulator is double-buffered in TMEM, so the tensor core
+// One CTA per (request, run of key tiles, kv head).  Key tiles stream through a two-stage ring;
+// up to two 256-row query chunks stay in the two query buffers for the whole run (more chunks
+// stream through them), and the S^T accumulator is double-buffered in TMEM, so the tensor core
 // works on the next (tile, chunk) step while the exponentials of the current one run.  Each
 // (kv head, query column half) writes its own partial sum per key; the last CTA of a run adds them
 // in fixed order (heads, then halves: deterministic).
@@ -90,7 +91,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int n_q = R[R_N_QUERY] * g;
     const int n_qc = (n_q + kImpQRows - 1) / kImpQRows;
     const int n_steps = nt * n_qc;           // step s = (tile s / n_qc, query chunk s % n_qc)
-    const bool q_resident = n_qc == 1;       // a single chunk is loaded once
+    const bool q_resident = n_qc <= 2;       // up to two chunks stay in their own buffers, loaded once
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -146,9 +147,10 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 lastk[kb] = i;
                 for (int qc = 0; qc < n_qc; ++qc) {
                     const int s = i * n_qc + qc;
-                    if (q_resident && s > 0) break;
-                    const int qb = s & 1;
-                    if (s >= 2 && !(ok = mbar_wait(&bars[I_Q_EMPTY + qb], ((s >> 1) - 1) & 1, abort_flag))) break;
+                    if (q_resident && i > 0) break;
+                    const int qb = q_resident ? qc : (s & 1);
+                    if (!q_resident && s >= 2 && !(ok = mbar_wait(&bars[I_Q_EMPTY + qb], ((s >> 1) - 1) & 1, abort_flag)))
+                        break;
                     mbar_arrive_expect_tx(&bars[I_Q_FULL + qb], H * kImpQRows * 128);
                     for (int hb = 0; hb < H; ++hb)
                         tma_load_2d(sQs(qb) + hb * kImpQRows * 128, &tm_q, &bars[I_Q_FULL + qb], hb * 64,
@@ -167,7 +169,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             bool ok = true;
             for (int s = 0; ok && s < n_steps; ++s) {
                 const int i = s / n_qc, qc = s - i * n_qc, a = s & 1;
-                const int qb = q_resident ? 0 : (s & 1);
+                const int qb = q_resident ? qc : (s & 1);
                 if (qc == 0) ok = mbar_wait(&bars[I_K_FULL + (i & 1)], (i >> 1) & 1, abort_flag);
                 ok = ok && mbar_wait(&bars[I_Q_FULL + qb], q_resident ? 0 : ((s >> 1) & 1), abort_flag) &&
                      mbar_wait(&bars[I_LSE_FULL + qb], q_resident ? 0 : ((s >> 1) & 1), abort_flag);
@@ -202,17 +204,17 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         // those columns contribute 0); thread tid writes row tid
         auto prep = [&](int s) {
             const int qc = s % n_qc;
-            uint8_t* slab = sQlse(q_resident ? 0 : (s & 1));
+            uint8_t* slab = sQlse(q_resident ? qc : (s & 1));
             const int n = qc * kImpQRows + tid;
             const float v = n < n_q ? -__ldcg(lse_g + n) : -30000.f;
             const __half hi = __float2half_rn(v);
             *reinterpret_cast<__half*>(slab + slab16_off(tid, 0)) = hi;
             *reinterpret_cast<__half*>(slab + slab16_off(tid, 1)) = __float2half_rn(v - __half2float(hi));
             fence_proxy_async_smem();
-            mbar_arrive(&bars[I_LSE_FULL + (q_resident ? 0 : (s & 1))]);
+            mbar_arrive(&bars[I_LSE_FULL + (q_resident ? qc : (s & 1))]);
         };
         if (n_steps > 0) prep(0);
-        if (!q_resident && n_steps > 1) prep(1);
+        if ((n_qc == 2 || !q_resident) && n_steps > 1) prep(1);
         bool ok = true;
         uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
         float* part_h = prm.part + ((int64_t)ch * Hkv + kvh) * total_tokens;   // this thread's half
