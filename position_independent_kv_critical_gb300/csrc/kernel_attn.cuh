@@ -42,7 +42,10 @@
 // row's visible keys in a tile are a prefix of it; only rows whose causal limit falls inside a
 // tile need per-element masking.
 // LSE mode (critical-layer scoring, pass 1) runs the same pipeline without P/V and writes the
-// per-row running max and sum of one key chunk.
+// per-row running max and sum of one key chunk.  Having no O, it gives each query tile two S
+// buffers of a whole key tile (128 columns) and issues Q K^T with N = 128: half the MMA
+// instructions of two 64-key halves, and back-to-back MMAs on changing operands complete at about
+// one per 100 cycles whatever N <= 128 is.
 #pragma once
 #include "layout_format.h"
 #include "ptx.cuh"
@@ -107,7 +110,7 @@ struct AttnSmem {
     static constexpr int oItem = oMisc + 64;
     static constexpr int kBytes = oItem + 2 * (int)sizeof(AttnItem);
     static constexpr int kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
-    static constexpr uint32_t kTmemCols = LSE ? 256 : 512;
+    static constexpr uint32_t kTmemCols = 512;   // LSE: 2 tiles x 2 S buffers of 128 columns
 };
 
 // barrier slots
@@ -118,9 +121,10 @@ enum : int {
     B_KPOS_FREE = 5,   // [2] both softmax groups are done with the stage's key positions (256 arrivals)
     B_V_FULL = 7,      // [2]
     B_V_EMPTY = 9,     // [2] both P V that read the stage are done (one commit per issuer)
-    B_S_FULL = 11,     // [4] per (Q tile, S half-buffer): S = Q K^T of a 64-key half landed
+    B_S_FULL = 11,     // [4] per (Q tile, S half-buffer): S = Q K^T of a 64-key half landed (LSE:
+                       //     of a whole key tile, per 128-column buffer)
     B_P_FULL = 15,     // [4] per (Q tile, S half-buffer): P written and O rescaled; in LSE mode:
-                       //     the softmax has loaded that S half into registers
+                       //     the softmax has loaded that S buffer into registers
     B_PV_DONE = 19,    // [4] per (Q tile, S half-buffer): P V of that buffer's latest half is done
     B_O_DONE = 23,     // [2] per Q tile: the item's last P V is done (one phase per item)
     B_DRAIN = 25,      // [4] per issuer: its last MMA is done
@@ -427,17 +431,41 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 mbar_arrive(&bars[B_ITEM_EMPTY + (it & 1)]);
                 if (w.req < 0) break;
                 const int nq = 2 * w.n_loc;   // halves of this item's key range
-                if (qk_role) {
+                if (qk_role && LSE) {
+                    // LSE mode: Q K^T of a whole key tile (N = 128 keys: half the instructions of two
+                    // halves) into S buffer kt & 1 of 128 columns, which the softmax frees once it has
+                    // loaded the tile two before
+                    constexpr uint32_t idesc_qk = idesc_f16(128, 128);
+                    const uint32_t aQ = smem_u32(sQ(t));
+                    ok = mbar_wait(&bars[B_Q_FULL], it & 1, abort_flag);
+                    for (int j = 0; ok && j < w.n_loc; ++j) {
+                        const int kt = kc + j;
+                        ok = mbar_wait(&bars[B_K_FULL + (kt & 1)], (kt >> 1) & 1, abort_flag) &&
+                             (kt < 2 || mbar_wait(&bars[B_P_FULL + 2 * t + (kt & 1)], ((kt - 2) >> 1) & 1, abort_flag));
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t aK = smem_u32(sKs(kt & 1));
+                        const uint32_t tS = tmem + t * 256 + (kt & 1) * 128;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t a = desc_sw128_kmajor(aQ + (kk >> 2) * 16384 + (kk & 3) * 32);
+                            const uint64_t b = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
+                            mma_bf16_ss(tS, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bars[B_S_FULL + 2 * t + (kt & 1)]);
+                        mma_commit(&bars[B_K_EMPTY + (kt & 1)]);
+                    }
+                    if (ok) mma_commit(&bars[B_Q_EMPTY]);
+                } else if (qk_role) {
                     // Q K^T of half q = 2j + h of local key tile j: keys 64h .. 64h+63 into S buffer
-                    // (hq + q) & 1, which the half two before it (P V done; LSE: softmax done) frees
+                    // (hq + q) & 1, which the half two before it (P V done) frees
                     constexpr uint32_t idesc_qk = idesc_f16(128, 64);
                     const uint32_t aQ = smem_u32(sQ(t));
                     ok = mbar_wait(&bars[B_Q_FULL], it & 1, abort_flag);
                     for (int q = 0; ok && q < nq; ++q) {
                         const int hg = hq + q, kt = kc + (q >> 1), h = q & 1;
                         ok = (h == 1 || mbar_wait(&bars[B_K_FULL + (kt & 1)], (kt >> 1) & 1, abort_flag)) &&
-                             (hg < 2 || mbar_wait(&bars[(LSE ? B_P_FULL : B_PV_DONE) + 2 * t + (hg & 1)],
-                                                  ((hg - 2) >> 1) & 1, abort_flag));
+                             (hg < 2 || mbar_wait(&bars[B_PV_DONE + 2 * t + (hg & 1)], ((hg - 2) >> 1) & 1, abort_flag));
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t aK = smem_u32(sKs(kt & 1)) + h * 64 * 128;
@@ -532,6 +560,78 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             float m_run = -INFINITY, l_run = 0.f;
             int cut = 0;
             const int nq = 2 * w.n_loc;
+            if constexpr (LSE) {
+                // LSE mode: S of a whole key tile per buffer (128 columns), read in two 64-column
+                // parts; the buffer is released once both parts are in registers (nothing goes
+                // back to TMEM), the running max and sum are kept as in the attention
+                for (int j = 0; j < w.n_loc; ++j) {
+                    const int kt = kc + j, ks = kt & 1;
+                    const uint32_t tS0 = tmem + lane_addr + t * 256 + ks * 128;
+                    ok = mbar_wait(&bars[B_S_FULL + 2 * t + ks], (kt >> 1) & 1, abort_flag) &&
+                         mbar_wait(&bars[B_KPOS_FULL + ks], (kt >> 1) & 1, abort_flag);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc_fence_after();
+                    {
+                        // visible keys of this row: a prefix of the tile (missing keys carry kNoPos)
+                        const int32_t* kp = sKpos(ks);
+                        if (kp[kTileKeys - 1] <= mypos) {
+                            cut = kTileKeys;
+                        } else {
+                            int lo = 0;
+#pragma unroll
+                            for (int step = 64; step >= 1; step >>= 1)
+                                if (kp[lo + step - 1] <= mypos) lo += step;
+                            cut = lo;
+                        }
+                        mbar_arrive(&bars[B_KPOS_FREE + ks]);
+                    }
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
+                        const int cut_h = cut - 64 * h;
+                        const bool full = __all_sync(0xffffffffu, cut_h >= 64);
+                        uint32_t sv[64];
+                        tmem_ld32(tS0 + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                        tmem_ld32(tS0 + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                        tmem_ld_wait();
+                        if (h == 1) {
+                            tc_fence_before();
+                            mbar_arrive(&bars[B_P_FULL + 2 * t + ks]);
+                        }
+                        if (!full) {
+#pragma unroll
+                            for (int e = 0; e < 64; ++e)
+                                if (e >= cut_h) sv[e] = __float_as_uint(-INFINITY);
+                        }
+                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                        for (int e = 0; e < 64; e += 8) {
+                            m4[0] = max3f(m4[0], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+                            m4[1] = max3f(m4[1], __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
+                            m4[2] = max3f(m4[2], __uint_as_float(sv[e + 4]), __uint_as_float(sv[e + 5]));
+                            m4[3] = max3f(m4[3], __uint_as_float(sv[e + 6]), __uint_as_float(sv[e + 7]));
+                        }
+                        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                        const float m_new = fmaxf(m_run, mx);
+                        if (m_new > m_run + 8.0f) {   // lazy rescale: keep the terms <= 2^8
+                            l_run *= ex2(m_run - m_new);
+                            m_run = m_new;
+                        }
+                        const float msub = m_run == -INFINITY ? 0.f : m_run;
+                        const uint64_t negm2 = f2_pack(-msub, -msub);
+                        uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            float d0, d1;
+                            f2_unpack(f2_add(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), negm2), d0, d1);
+                            acc2[e & 1] = f2_add(acc2[e & 1], f2_pack(ex2(d0), ex2(d1)));
+                        }
+                        float a0, a1, b0, b1;
+                        f2_unpack(acc2[0], a0, a1);
+                        f2_unpack(acc2[1], b0, b1);
+                        l_run += (a0 + b0) + (a1 + b1);
+                    }
+                }
+            } else
             for (int q = 0; q < nq; ++q) {    // halves of the item's key tiles
                 const int hg = hq + q, kt = kc + (q >> 1), h = q & 1, ks = kt & 1;
                 const uint32_t tS = tmem + lane_addr + t * 128 + (hg & 1) * 64;
