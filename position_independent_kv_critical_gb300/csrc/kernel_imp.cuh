@@ -90,8 +90,16 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int n_pages = R[R_N_PAGES];
     const int n_q = R[R_N_QUERY] * g;
     const int n_qc = (n_q + kImpQRows - 1) / kImpQRows;
-    const int n_steps = nt * n_qc;           // step s = (tile s / n_qc, query chunk s % n_qc)
-    const bool q_resident = n_qc <= 2;       // up to two chunks stay in their own buffers, loaded once
+    const int n_steps = nt * n_qc;
+    // up to two chunks stay in their own buffers, loaded once, and the steps go tile by tile
+    // (step s = tile s / n_qc, chunk s % n_qc); with more chunks the steps go chunk by chunk
+    // (chunk s / nt, tile s % nt): each chunk is loaded once while the run's key tiles stream
+    // past it, and the per-key sums are carried from chunk to chunk through the partials
+    const bool q_resident = n_qc <= 2;
+    auto step_of = [&](int s, int& i, int& qc) {
+        if (q_resident) { i = s / n_qc; qc = s - i * n_qc; }
+        else { qc = s / nt; i = s - qc * nt; }
+    };
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -137,7 +145,26 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             const int32_t qy0 = (kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE]) * g;
             int lastk[2] = {-1, -1}, lastq[2] = {-1, -1};
             bool ok = true;
-            for (int i = 0; ok && i < nt; ++i) {
+            for (int qc = 0; !q_resident && ok && qc < n_qc; ++qc) {
+                // chunk qc into buffer qc & 1 once chunk qc - 2 is done with it, then the run's tiles
+                const int qb = qc & 1;
+                if (qc >= 2 && !(ok = mbar_wait(&bars[I_Q_EMPTY + qb], ((qc >> 1) - 1) & 1, abort_flag))) break;
+                mbar_arrive_expect_tx(&bars[I_Q_FULL + qb], H * kImpQRows * 128);
+                for (int hb = 0; hb < H; ++hb)
+                    tma_load_2d(sQs(qb) + hb * kImpQRows * 128, &tm_q, &bars[I_Q_FULL + qb], hb * 64,
+                                qy0 + qc * kImpQRows);
+                lastq[qb] = qc;
+                for (int i = 0; i < nt; ++i) {
+                    const int s = qc * nt + i, kb = s & 1;
+                    if (s >= 2 && !(ok = mbar_wait(&bars[I_K_EMPTY + kb], ((s >> 1) - 1) & 1, abort_flag))) break;
+                    mbar_arrive_expect_tx(&bars[I_K_FULL + kb], H * 16384);
+                    for (int hb = 0; hb < H; ++hb)
+                        tma_load_2d(sKs(kb) + hb * 16384, &tm_kcache, &bars[I_K_FULL + kb], hb * 64,
+                                    ky0 + i * kTileKeys);
+                    lastk[kb] = s;
+                }
+            }
+            for (int i = 0; q_resident && ok && i < nt; ++i) {
                 // rotated key tile t0 + i (rows past the request's keys are never summed)
                 const int kb = i & 1;
                 if (i >= 2 && !(ok = mbar_wait(&bars[I_K_EMPTY + kb], ((i >> 1) - 1) & 1, abort_flag))) break;
@@ -145,17 +172,12 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 for (int hb = 0; hb < H; ++hb)
                     tma_load_2d(sKs(kb) + hb * 16384, &tm_kcache, &bars[I_K_FULL + kb], hb * 64, ky0 + i * kTileKeys);
                 lastk[kb] = i;
-                for (int qc = 0; qc < n_qc; ++qc) {
-                    const int s = i * n_qc + qc;
-                    if (q_resident && i > 0) break;
-                    const int qb = q_resident ? qc : (s & 1);
-                    if (!q_resident && s >= 2 && !(ok = mbar_wait(&bars[I_Q_EMPTY + qb], ((s >> 1) - 1) & 1, abort_flag)))
-                        break;
-                    mbar_arrive_expect_tx(&bars[I_Q_FULL + qb], H * kImpQRows * 128);
+                for (int qc = 0; i == 0 && qc < n_qc; ++qc) {   // each chunk once, into buffer qc
+                    mbar_arrive_expect_tx(&bars[I_Q_FULL + qc], H * kImpQRows * 128);
                     for (int hb = 0; hb < H; ++hb)
-                        tma_load_2d(sQs(qb) + hb * kImpQRows * 128, &tm_q, &bars[I_Q_FULL + qb], hb * 64,
+                        tma_load_2d(sQs(qc) + hb * kImpQRows * 128, &tm_q, &bars[I_Q_FULL + qc], hb * 64,
                                     qy0 + qc * kImpQRows);
-                    lastq[qb] = s;
+                    lastq[qc] = 0;
                 }
             }
             for (int b = 0; b < 2; ++b) {
@@ -168,15 +190,18 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             constexpr uint32_t idesc = idesc_f16(128, kImpQRows);
             bool ok = true;
             for (int s = 0; ok && s < n_steps; ++s) {
-                const int i = s / n_qc, qc = s - i * n_qc, a = s & 1;
-                const int qb = q_resident ? qc : (s & 1);
-                if (qc == 0) ok = mbar_wait(&bars[I_K_FULL + (i & 1)], (i >> 1) & 1, abort_flag);
-                ok = ok && mbar_wait(&bars[I_Q_FULL + qb], q_resident ? 0 : ((s >> 1) & 1), abort_flag) &&
-                     mbar_wait(&bars[I_LSE_FULL + qb], q_resident ? 0 : ((s >> 1) & 1), abort_flag);
+                int i, qc;
+                step_of(s, i, qc);
+                const int a = s & 1, qb = qc & 1;
+                // K stage: per tile in tile order, per step in chunk order
+                const int kidx = q_resident ? i : s;
+                if (!q_resident || qc == 0) ok = mbar_wait(&bars[I_K_FULL + (kidx & 1)], (kidx >> 1) & 1, abort_flag);
+                ok = ok && mbar_wait(&bars[I_Q_FULL + qb], q_resident ? 0 : ((qc >> 1) & 1), abort_flag) &&
+                     mbar_wait(&bars[I_LSE_FULL + qb], q_resident ? 0 : ((qc >> 1) & 1), abort_flag);
                 ok = ok && (s < 2 || mbar_wait(&bars[I_ACC_FREE + a], ((s >> 1) - 1) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t aK = smem_u32(sKs(i & 1)), aQ = smem_u32(sQs(qb));
+                const uint32_t aK = smem_u32(sKs(kidx & 1)), aQ = smem_u32(sQs(qb));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t da = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
@@ -187,8 +212,12 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 mma_bf16_ss(tmem + a * kImpQRows, desc_noswz_kmajor(smem_u32(sKones), 128, 256),
                             desc_noswz_kmajor(smem_u32(sQlse(qb)), 128, 256), idesc, 1u);
                 mma_commit(&bars[I_ACC_FULL + a]);
-                if (!q_resident) mma_commit(&bars[I_Q_EMPTY + qb]);
-                if (qc == n_qc - 1) mma_commit(&bars[I_K_EMPTY + (i & 1)]);
+                if (q_resident) {
+                    if (qc == n_qc - 1) mma_commit(&bars[I_K_EMPTY + (i & 1)]);
+                } else {
+                    mma_commit(&bars[I_K_EMPTY + (s & 1)]);
+                    if (i == nt - 1) mma_commit(&bars[I_Q_EMPTY + qb]);
+                }
             }
             mma_commit(&bars[I_DRAIN]);
             mbar_drain(&bars[I_DRAIN], 0);
@@ -200,26 +229,32 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         const int total_tokens = L[L_TOTAL_TOKENS];
         const int32_t tok_base = R[R_TOK_BASE];
-        // -lse2 of step s's query chunk into its slab, as fp16 hi + lo (-30000 past the last row:
+        // -lse2 of query chunk qc into slab qc & 1, as fp16 hi + lo (-30000 past the last row:
         // those columns contribute 0); thread tid writes row tid
-        auto prep = [&](int s) {
-            const int qc = s % n_qc;
-            uint8_t* slab = sQlse(q_resident ? qc : (s & 1));
+        auto prep = [&](int qc) {
+            uint8_t* slab = sQlse(qc & 1);
             const int n = qc * kImpQRows + tid;
             const float v = n < n_q ? -__ldcg(lse_g + n) : -30000.f;
             const __half hi = __float2half_rn(v);
             *reinterpret_cast<__half*>(slab + slab16_off(tid, 0)) = hi;
             *reinterpret_cast<__half*>(slab + slab16_off(tid, 1)) = __float2half_rn(v - __half2float(hi));
             fence_proxy_async_smem();
-            mbar_arrive(&bars[I_LSE_FULL + (q_resident ? qc : (s & 1))]);
+            mbar_arrive(&bars[I_LSE_FULL + (qc & 1)]);
         };
         if (n_steps > 0) prep(0);
-        if ((n_qc == 2 || !q_resident) && n_steps > 1) prep(1);
+        if (n_qc >= 2 && n_steps > 1) prep(1);
         bool ok = true;
         uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
         float* part_h = prm.part + ((int64_t)ch * Hkv + kvh) * total_tokens;   // this thread's half
         for (int s = 0; s < n_steps; ++s) {
-            const int i = s / n_qc, qc = s - i * n_qc, a = s & 1;
+            int i, qc;
+            step_of(s, i, qc);
+            const int a = s & 1;
+            const int t = t0 + i;
+            const bool valid_key = (t * kPagesPerTile + key / kPage) < n_pages;
+            float* dst = part_h + tok_base + t * kTileKeys + key;
+            // chunk order: the key's sum over the earlier chunks, read while this step runs
+            const float carried = (!q_resident && qc > 0 && valid_key) ? *dst : 0.f;
             if (ok) ok = mbar_wait(&bars[I_ACC_FULL + a], (s >> 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
@@ -237,17 +272,15 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     for (int e = 0; e < 32; e += 2)
                         acc2[(e >> 1) & 1] = f2_add(acc2[(e >> 1) & 1], f2_pack(ex2(__uint_as_float(sv[cc][e])),
                                                                               ex2(__uint_as_float(sv[cc][e + 1]))));
-                // step s's MMA is complete, so its slab buffer takes step s + 2's chunk
-                if (!q_resident && s + 2 < n_steps) prep(s + 2);
+                // the last step of chunk qc is complete, so its slab takes chunk qc + 2
+                if (!q_resident && i == nt - 1 && qc + 2 < n_qc) prep(qc + 2);
             }
-            if (qc == n_qc - 1) {
+            if (!q_resident || qc == n_qc - 1) {
                 float a0, a1, b0, b1;
                 f2_unpack(acc2[0], a0, a1);
                 f2_unpack(acc2[1], b0, b1);
                 acc2[0] = acc2[1] = f2_pack(0.f, 0.f);
-                const int t = t0 + i;
-                const bool valid_key = (t * kPagesPerTile + key / kPage) < n_pages;
-                if (ok && valid_key) part_h[tok_base + t * kTileKeys + key] = (a0 + b0) + (a1 + b1);
+                if (ok && valid_key) *dst = carried + ((a0 + b0) + (a1 + b1));
             }
         }
         if (n_qc == 0)   // a request without query rows: every importance is 0
