@@ -42,7 +42,7 @@
 // row's visible keys in a tile are a prefix of it; only rows whose causal limit falls inside a
 // tile need per-element masking.
 // LSE mode (critical-layer scoring, pass 1) runs the same pipeline without P/V and writes the
-// per-row running max and sum of one key chunk.  Having no O, it gives each query tile two S
+// per-row running max and sum of one key chunk (the importance kernel combines a row's chunks).  Having no O, it gives each query tile two S
 // buffers of a whole key tile (128 columns) and issues Q K^T with N = 128: half the MMA
 // instructions of two 64-key halves, and back-to-back MMAs on changing operands complete at about
 // one per 100 cycles whatever N <= 128 is.
@@ -70,9 +70,8 @@ struct AttnParams {
     const int32_t* kpos_c;     // attention: logical position of every compacted cached key
     const int32_t* row_pos;    // attention: logical position of every row
     __nv_bfloat16* out;        // attention: [rows][Hq][D]
-    float2* lse_part;          // LSE: (running max in log2 units, running sum) per row and chunk
-    float* lse_final;          // LSE: log2-sum-exp per row, [Hkv][total query][g]
-    int32_t* lse_count;        // LSE: finished chunks per (request, kv head, pair); zero on entry and exit
+    float2* lse_part;          // LSE: (running max in log2 units, running sum); per request
+                               //      [kv head][key chunk][query row x g]
     __nv_bfloat16* part_o;     // attention with a split key range: normalized partial O per slot
     float2* part_ml;           //   and its (running max, running sum) per row
     int32_t* sched;            // items handed out beyond the first gridDim.x; zero on entry
@@ -90,8 +89,8 @@ struct AttnItem {
     int32_t row_base;          // first row of the request
     int32_t cbase;             // first compacted cached key of the request
     int32_t nsplit, slot_base; // attention: key-range splits of the pair and its first partial slot
-    int32_t lse_base, lse_chunks, lse_cidx, q_base;   // LSE: partials, chunks, counter, query base
-    int32_t pad[2];
+    int32_t lse_base, lse_chunks;   // LSE: the request's partials and its chunks
+    int32_t pad[4];
 };
 
 template <int D, bool LSE>
@@ -105,7 +104,7 @@ struct AttnSmem {
     static constexpr int oV = oK + kKStages * kK;
     static constexpr int oKpos = oV + kVStages * kV;
     static constexpr int oBar = oKpos + kKStages * kTileKeys * 4;
-    static constexpr int kNumBars = 40;
+    static constexpr int kNumBars = 38;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int oItem = oMisc + 64;
     static constexpr int kBytes = oItem + 2 * (int)sizeof(AttnItem);
@@ -132,9 +131,7 @@ enum : int {
     B_O_FREE = 30,     // [2] per Q tile: the softmax group has read the item's O (128 arrivals)
     B_ITEM_FULL = 32,  // [2] item slot written by the scheduler
     B_ITEM_EMPTY = 34, // [2] every consumer role has read the slot
-    B_FIN = 36,        // LSE: the softmax threads wrote the item's chunk (256 arrivals, one phase per item)
-    B_FIN2 = 37,       // LSE: thread 0 counted the chunk (misc[7] says whether it was the pair's last)
-    B_KPOS_FULL = 38   // [2] the K tile's key positions written (every producer lane)
+    B_KPOS_FULL = 36   // [2] the K tile's key positions written (every producer lane)
 };
 
 template <int D, bool LSE>
@@ -155,7 +152,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     auto sKpos = [&](int st) { return reinterpret_cast<int32_t*>(smem + SM::oKpos) + st * kTileKeys; };
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::oBar);
     int32_t* misc = reinterpret_cast<int32_t*>(smem + SM::oMisc);
-    // misc: [0] tmem base, [4] abort, [7] LSE: this chunk finished its (kv head, pair) last
+    // misc: [0] tmem base, [4] abort
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
     AttnItem* slots = reinterpret_cast<AttnItem*>(smem + SM::oItem);
 
@@ -193,8 +190,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             mbar_init(&bars[B_ITEM_FULL + b], 1);
             mbar_init(&bars[B_ITEM_EMPTY + b], kItemReaders);
         }
-        mbar_init(&bars[B_FIN], 256);
-        mbar_init(&bars[B_FIN2], 1);
         fence_mbar_init();
         misc[4] = 0;
         prefetch_tmap(&tm_q);
@@ -229,6 +224,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         int kc = 0;                                   // K tiles this CTA issued before the item
         int last_k[kKStages] = {-1, -1}, last_q = -1;  // for the final drain
         bool ok = true;
+        // layout values the producer needs after publishing an item, read into registers up front:
+        // every barrier call is a compiler memory barrier, after which a layout word would be
+        // loaded again on the item's critical path (the Q copy waits for it)
+        const int32_t tot_tok = L[L_TOTAL_TOKENS], tot_valid = L[L_TOTAL_VALID], tot_rows = L[L_TOTAL_ROWS];
+        const int32_t tot_query = L[L_TOTAL_QUERY];
+        const int32_t* const page_pos_all = L + L[L_OFF_PAGEPOS];
         for (int it = 0; ok; ++it) {
             // the next item: the first is this CTA's own, the rest come in list order
             int idx = 0;
@@ -238,9 +239,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             w.req = -1;
             w.kvh = w.qpair = w.chunk = w.n_ct = w.n_ft = w.t0 = w.jb = w.n_loc = 0;
             w.n_rows = w.row_base = w.cbase = w.nsplit = w.slot_base = 0;
-            w.lse_base = w.lse_chunks = w.lse_cidx = w.q_base = 0;
+            w.lse_base = w.lse_chunks = 0;
             w.pad[0] = w.pad[1] = 0;
             const int32_t* R = L;
+            int32_t r_tok_base = 0, r_q_base = 0, r_n_kept = 0, r_page_base = 0, r_n_pages = 0;
             if (idx < n_items) {
                 const int32_t* item = items + kItemWords * idx;
                 w.req = item[0];
@@ -251,6 +253,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 w.n_rows = LSE ? R[R_N_QUERY] : R[R_N_ROWS];
                 w.row_base = R[R_ROW_BASE];
                 w.cbase = R[R_CBASE];
+                r_tok_base = R[R_TOK_BASE];
+                r_q_base = R[R_Q_BASE];
+                r_n_pages = R[R_N_PAGES];
+                r_n_kept = r_n_pages * kPage - R[R_N_SEL];
+                r_page_base = R[R_PAGE_BASE];
                 if (LSE) {
                     // LSE: tiles of all the request's cached tokens, cut into chunks
                     const int nkt = R[R_N_KTILES], chunks = R[R_LSE_CHUNKS];
@@ -260,21 +267,18 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     w.n_loc = w.n_ct;
                     w.lse_base = R[R_LSE_BASE];
                     w.lse_chunks = chunks;
-                    w.lse_cidx = R[R_LSE_PAIR_BASE] +
-                                 w.kvh * ((R[R_N_QUERY] * g + 2 * kTileRows - 1) / (2 * kTileRows)) + w.qpair;
-                    w.q_base = R[R_Q_BASE];
                 } else {
                     // visible tiles: key positions increase along the compacted cached tiles and
                     // along the fresh rows, so each count is the number of tiles whose first key
                     // is at or before the pair's last row (the lanes test 32 tiles at a time)
-                    const int n_rows_req = R[R_N_ROWS];
-                    const int32_t row_base = R[R_ROW_BASE];
+                    const int n_rows_req = w.n_rows;
+                    const int32_t row_base = w.row_base;
                     const int row0 = w.qpair * kQTilesPerCta * toks_per_tile;
                     const int nrow = min(kQTilesPerCta * toks_per_tile, n_rows_req - row0);
-                    const int nkt = (R[R_N_PAGES] * kPage - R[R_N_SEL] + kTileKeys - 1) / kTileKeys;
+                    const int nkt = (r_n_kept + kTileKeys - 1) / kTileKeys;
                     const int32_t pmax = nrow > 0 ? prm.row_pos[row_base + row0 + nrow - 1] : -1;
                     const int nft_total = (n_rows_req + kTileKeys - 1) / kTileKeys;
-                    const int32_t* kpc = prm.kpos_c + R[R_CBASE];
+                    const int32_t* kpc = prm.kpos_c + w.cbase;
                     int nct = 0, nft = 0;
                     for (int b = 0; b < nkt; b += 32)
                         nct += __popc(__ballot_sync(0xffffffffu, b + lane < nkt && kpc[(b + lane) * kTileKeys] <= pmax));
@@ -301,18 +305,18 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok || w.req < 0) break;
-            const int n_rows_req = LSE ? R[R_N_QUERY] : R[R_N_ROWS];
-            const int32_t row_base = R[R_ROW_BASE];
+            const int n_rows_req = w.n_rows;
+            const int32_t row_base = w.row_base;
             const int row0 = w.qpair * kQTilesPerCta * toks_per_tile;
-            const int32_t kc_row0 = LSE ? w.kvh * L[L_TOTAL_TOKENS] + R[R_TOK_BASE]
-                                        : w.kvh * L[L_TOTAL_VALID] + R[R_CBASE];
-            const int32_t kf_row0 = w.kvh * L[L_TOTAL_ROWS] + row_base;
+            const int32_t kc_row0 = LSE ? w.kvh * tot_tok + r_tok_base : w.kvh * tot_valid + w.cbase;
+            const int32_t kf_row0 = w.kvh * tot_rows + row_base;
             // key positions, which only the softmax waits for: lane l holds those of keys l, l+32,
             // l+64, l+96 of a tile (kNoPos for a missing key), loaded one tile ahead; the first
             // tile's are requested now, before the wait for the Q buffer
             const int n_ct = w.n_ct, n_tiles = w.n_ct + w.n_ft;
-            const int n_kept = R[R_N_PAGES] * kPage - R[R_N_SEL];
-            const int32_t* page_pos = L + L[L_OFF_PAGEPOS] + R[R_PAGE_BASE];
+            const int n_kept = r_n_kept;
+            const int32_t* page_pos = page_pos_all + r_page_base;
+            const int32_t* kpc_req = prm.kpos_c + w.cbase;
             auto meta = [&](int j, int32_t (&pos)[4]) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
@@ -321,10 +325,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     if (j < n_ct) {
                         if (LSE) {
                             const int lp = (w.t0 + j) * kPagesPerTile + key / kPage;
-                            if (lp < R[R_N_PAGES]) pos[r] = page_pos[lp] + key % kPage;
+                            if (lp < r_n_pages) pos[r] = page_pos[lp] + key % kPage;
                         } else {
                             const int ci = j * kTileKeys + key;
-                            if (ci < n_kept) pos[r] = prm.kpos_c[R[R_CBASE] + ci];
+                            if (ci < n_kept) pos[r] = kpc_req[ci];
                         }
                     } else if (j < n_tiles) {
                         const int fr = (j - n_ct) * kTileKeys + key;
@@ -336,8 +340,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (w.n_loc > 0) meta(w.jb, pos_n);
             // the item's Q tiles, once both Q K^T issuers are done with the previous item's
             if (lane == 0) {
-                const int32_t qy = LSE ? (w.kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row0) * g
-                                       : (w.kvh * L[L_TOTAL_ROWS] + row_base + row0) * g;
+                const int32_t qy = LSE ? (w.kvh * tot_query + r_q_base + row0) * g
+                                       : (w.kvh * tot_rows + row_base + row0) * g;
                 if (it > 0) {
                     // warm L2 with the Q rows while the previous item drains
                     for (int t = 0; t < kQTilesPerCta; ++t)
@@ -391,6 +395,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             prefetch_tmap(&tm_vfresh);
             int vc = 0;
             int last_v[kVStages] = {-1, -1};
+            const int32_t tot_valid = L[L_TOTAL_VALID];
             for (int it = 0;; ++it) {
                 AttnItem w;
                 if (!take_item(it, w)) break;
@@ -404,7 +409,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     uint64_t* full = &bars[B_V_FULL + vs];
                     mbar_arrive_expect_tx(full, H * 16384);
                     if (j < w.n_ct) {
-                        const int32_t y = w.kvh * L[L_TOTAL_VALID] + w.cbase + j * kTileKeys;
+                        const int32_t y = w.kvh * tot_valid + w.cbase + j * kTileKeys;
                         for (int hb = 0; hb < H; ++hb) tma_load_2d(sVs(vs) + hb * 16384, &tm_vcache, full, hb * 64, y);
                     } else {
                         const int32_t fr = w.row_base + (j - w.n_ct) * kTileKeys;
@@ -544,8 +549,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             float2* ml_slot = nullptr;
             if (valid) {
                 if (LSE) {
+                    // [kv head][chunk][query row]: a warp's 32 rows are contiguous
                     ml_slot = prm.lse_part + w.lse_base +
-                              ((int64_t)w.kvh * (n_rows_req * g) + row * g + hl) * w.lse_chunks + w.chunk;
+                              ((int64_t)w.kvh * w.lse_chunks + w.chunk) * (n_rows_req * g) + row * g + hl;
                 } else {
                     if (w.nsplit == 1) {
                         out_row = prm.out + ((int64_t)(row_base + row) * Hq + w.kvh * g + hl) * D;
@@ -730,45 +736,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             if (!ok) break;
             if (ml_slot != nullptr) *ml_slot = make_float2(w.n_loc > 0 ? m_run : -INFINITY, l_run);
-            if (LSE) {
-                // The last key chunk of this (request, kv head, tile pair) to finish combines every
-                // row's chunks, in chunk order, into the row's log2-sum-exp over all cached keys.
-                const int chunks = w.lse_chunks;
-                const int cidx = w.lse_cidx;
-                // (mbarriers with bounded waits rather than a named barrier: a softmax warp that
-                // gave up on an earlier wait must not leave the others blocked; the barriers order
-                // the 256 threads' partial writes before, and their reads after, thread 0's
-                // acquire-release increment)
-                mbar_arrive(&bars[B_FIN]);
-                if (tid == 0) {
-                    const bool okf = mbar_wait(&bars[B_FIN], it & 1, abort_flag);
-                    misc[7] = okf && atomic_add_acq_rel_gpu(prm.lse_count + cidx, 1) == chunks - 1 ? 1 : 0;
-                    mbar_arrive(&bars[B_FIN2]);
-                }
-                ok = mbar_wait(&bars[B_FIN2], it & 1, abort_flag);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                if (misc[7]) {
-                    if (valid) {
-                        const float2* ml = prm.lse_part + w.lse_base +
-                                           ((int64_t)w.kvh * (n_rows_req * g) + row * g + hl) * chunks;
-                        // all chunks are loaded at once (chunks <= kMaxSplits), then combined in order
-                        float2 v[kMaxSplits];
-#pragma unroll
-                        for (int c = 0; c < kMaxSplits; ++c)
-                            v[c] = c < chunks ? __ldcg(ml + c) : make_float2(-INFINITY, 0.f);
-                        float M = -INFINITY;
-#pragma unroll
-                        for (int c = 0; c < kMaxSplits; ++c) M = fmaxf(M, v[c].x);
-                        float S = 0.f;
-#pragma unroll
-                        for (int c = 0; c < kMaxSplits; ++c)
-                            if (c < chunks) S += v[c].y * ex2(v[c].x - M);
-                        prm.lse_final[((int64_t)w.kvh * L[L_TOTAL_QUERY] + w.q_base + row) * g + hl] =
-                            S > 0.f ? M + log2f(S) : INFINITY;
-                    }
-                    if (tid == 0) prm.lse_count[cidx] = 0;
-                }
-            } else {
+            if (!LSE) {
                 // if the next item is already published, start loading this row's position for it
                 // now, so that the load runs under the epilogue
                 if (__all_sync(0xffffffffu, mbar_test_wait(&bars[B_ITEM_FULL + ((it + 1) & 1)], ((it + 1) >> 1) & 1))) {
@@ -786,20 +754,32 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tc_fence_after();
                 if (w.n_loc > 0) {
                     const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+                    // 64 columns per TMEM round trip; a row's bf16 values leave in whole 32-byte
+                    // sectors where the destination allows (half the store transactions of 16-byte
+                    // stores, whose sectors the L2 would take half-written)
+                    const bool wide = (reinterpret_cast<uintptr_t>(out_row) & 31u) == 0;
 #pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + cc * 32, o);
+                    for (int cc = 0; cc < D / 64; ++cc) {
+                        uint32_t o0[32], o1[32];
+                        tmem_ld32(tO + cc * 64, o0);
+                        tmem_ld32(tO + cc * 64 + 32, o1);
                         tmem_ld_wait();
                         if (valid) {
+                            uint32_t pk[32];
 #pragma unroll
-                            for (int qq = 0; qq < 4; ++qq) {
-                                uint4 v;
-                                v.x = pack_bf16x2(__uint_as_float(o[8 * qq + 0]) * inv, __uint_as_float(o[8 * qq + 1]) * inv);
-                                v.y = pack_bf16x2(__uint_as_float(o[8 * qq + 2]) * inv, __uint_as_float(o[8 * qq + 3]) * inv);
-                                v.z = pack_bf16x2(__uint_as_float(o[8 * qq + 4]) * inv, __uint_as_float(o[8 * qq + 5]) * inv);
-                                v.w = pack_bf16x2(__uint_as_float(o[8 * qq + 6]) * inv, __uint_as_float(o[8 * qq + 7]) * inv);
-                                *reinterpret_cast<uint4*>(out_row + cc * 32 + 8 * qq) = v;
+                            for (int e = 0; e < 16; ++e) {
+                                pk[e] = pack_bf16x2(__uint_as_float(o0[2 * e]) * inv, __uint_as_float(o0[2 * e + 1]) * inv);
+                                pk[16 + e] = pack_bf16x2(__uint_as_float(o1[2 * e]) * inv, __uint_as_float(o1[2 * e + 1]) * inv);
+                            }
+                            __nv_bfloat16* dst = out_row + cc * 64;
+                            if (wide) {
+#pragma unroll
+                                for (int qq = 0; qq < 4; ++qq) st_global_v8(dst + 16 * qq, pk + 8 * qq);
+                            } else {
+#pragma unroll
+                                for (int qq = 0; qq < 8; ++qq)
+                                    *reinterpret_cast<uint4*>(dst + 8 * qq) =
+                                        make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
                             }
                         }
                     }

@@ -35,7 +35,7 @@ constexpr int kImpQRows = 256;
 
 struct ImpParams {
     const int32_t* layout;
-    const float* lse_final;  // [Hkv][total_query][g] log2-sum-exp of every query row
+    const float2* lse_part;  // pass 1: (max, sum) in log2 units, per request [kv head][chunk][row]
     float* part;             // [2][Hkv][total_tokens]: query column half, kv head, token
     int32_t* counters;       // [total key tiles], zero on entry, left zero on exit
     float* importance;       // [total_tokens]
@@ -115,7 +115,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         fence_mbar_init();
         misc[4] = 0;
     }
-    // the previous kernel (row LSE, which writes the log2-sum-exp read here) may still be running
+    // the previous kernel (row LSE, whose per-chunk max and sum are read here) may still be running
     // until this wait; the TMEM is taken only after it
     grid_dep_wait();
     grid_dep_launch();
@@ -225,16 +225,33 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     } else {
         // warps 0-7: thread owns key `key` of every tile of the run, query columns ch*128 .. +127
         const int key = tid & 127, ch = tid >> 7;
-        const float* lse_g = prm.lse_final + ((int64_t)kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE]) * g;
+        // pass 1's (max, sum) pairs of this kv head's query rows, one per key chunk
+        const int chunks = R[R_LSE_CHUNKS];
+        const float2* ml_g = prm.lse_part + R[R_LSE_BASE] + (int64_t)kvh * chunks * n_q;   // [chunk][row]
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         const int total_tokens = L[L_TOTAL_TOKENS];
         const int32_t tok_base = R[R_TOK_BASE];
         // -lse2 of query chunk qc into slab qc & 1, as fp16 hi + lo (-30000 past the last row:
-        // those columns contribute 0); thread tid writes row tid
+        // those columns contribute 0); thread tid writes row tid.  lse2 combines the row's key
+        // chunks in chunk order: M = max of the maxima, lse2 = M + log2(sum_c s_c 2^(m_c - M)).
         auto prep = [&](int qc) {
             uint8_t* slab = sQlse(qc & 1);
             const int n = qc * kImpQRows + tid;
-            const float v = n < n_q ? -__ldcg(lse_g + n) : -30000.f;
+            float v = -30000.f;
+            if (n < n_q && chunks > 0) {
+                float2 c2[kMaxSplits];
+#pragma unroll
+                for (int c = 0; c < kMaxSplits; ++c)
+                    c2[c] = c < chunks ? __ldcg(ml_g + (int64_t)c * n_q + n) : make_float2(-INFINITY, 0.f);
+                float M = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kMaxSplits; ++c) M = fmaxf(M, c2[c].x);
+                float S = 0.f;
+#pragma unroll
+                for (int c = 0; c < kMaxSplits; ++c)
+                    if (c < chunks) S += c2[c].y * ex2(c2[c].x - M);
+                v = S > 0.f ? -(M + log2f(S)) : -INFINITY;
+            }
             const __half hi = __float2half_rn(v);
             *reinterpret_cast<__half*>(slab + slab16_off(tid, 0)) = hi;
             *reinterpret_cast<__half*>(slab + slab16_off(tid, 1)) = __float2half_rn(v - __half2float(hi));

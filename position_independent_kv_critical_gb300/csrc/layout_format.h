@@ -29,7 +29,7 @@ enum : int {
     L_LSE_SLOTS = 21, L_GROUP = 22, L_MAX_SPAN_LEN = 23,
     L_OFF_REQ = 24, L_OFF_SPAN = 25, L_OFF_BLOCK = 26, L_OFF_PAGEPOS = 27, L_OFF_ATTN = 28,
     L_OFF_LSE = 29, L_OFF_IMP = 30, L_OFF_QPOS = 31, L_OFF_COMB = 32, L_N_COMB = 33,
-    L_ATTN_SLOTS = 34, L_OFF_PAIR = 35, L_N_PAIRS = 36, L_N_LSE_PAIRS = 37,
+    L_ATTN_SLOTS = 34, L_OFF_PAIR = 35, L_N_PAIRS = 36,
     L_TOTAL_VALID = 38,   // cached keys that take part in the attention (not recomputed), all requests
     L_HEADER = 40
 };
@@ -39,7 +39,6 @@ enum : int {
     R_N_PAGES = 0, R_TOK_BASE = 1, R_PAGE_BASE = 2, R_Q_BASE = 3, R_ROW_BASE = 4, R_SEL_BASE = 5,
     R_QUERY_POS0 = 6, R_N_SPANS = 7, R_SPAN_BASE = 8, R_N_QUERY = 9, R_N_SEL = 10, R_N_ROWS = 11,
     R_LSE_BASE = 12, R_LSE_CHUNKS = 13, R_KTILE_BASE = 14, R_N_KTILES = 15,
-    R_LSE_PAIR_BASE = 16,   // first (kv head, query tile pair) index of the request's LSE pass
     R_CBASE = 17,       // first row of the request's taking-part cached keys in the compacted copy
     R_NPAIRS = 18,      // tile pairs of the request (per kv head)
     R_PAIR_BASE = 19,   // first pair record of the request
@@ -59,8 +58,8 @@ enum : int { P_NSPLIT = 0, P_SLOT_BASE = 1, P_STRIDE = 2 };
 // work items (kItemWords each)
 //   attention : {req, kv head, q tile pair, key-range split}   largest estimated cost first
 //   lse       : {req, kv head, q tile pair, key chunk}
-//               (the last chunk to finish turns the chunks' partial (max, sum) into the rows'
-//               log2-sum-exp; counter R_LSE_PAIR_BASE + kv head * query pairs + pair)
+//               (each chunk writes its rows' partial (max, sum); the importance kernel combines
+//               a row's chunks into its log2-sum-exp)
 // (a "q tile pair" p covers the 128-row query tiles 2p and 2p+1 of the request)
 //   importance: {req, first key tile, kv head, key tiles}
 //   combine   : {req, kv head, q tile pair, 0}   pairs whose key range was split

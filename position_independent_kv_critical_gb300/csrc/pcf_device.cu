@@ -167,20 +167,18 @@ size_t align_up(size_t x) { return (x + 1023) & ~size_t(1023); }
 size_t kc_bytes(const int32_t* H) { return (size_t)H[L_HKV] * H[L_TOTAL_TOKENS] * H[L_D] * 2; }
 
 struct ScoreWs {
-    size_t q, kc, lse, lsef, part, cnt, total;
+    size_t q, kc, lse, part, cnt, total;
 };
 ScoreWs score_ws(const int32_t* H) {
     ScoreWs w;
     w.q = 0;
     w.kc = align_up(w.q + (size_t)H[L_TOTAL_QUERY] * H[L_HQ] * H[L_D] * 2);
     w.lse = align_up(w.kc + kc_bytes(H));
-    w.lsef = align_up(w.lse + (size_t)H[L_LSE_SLOTS] * sizeof(float2));
-    w.part = align_up(w.lsef + (size_t)H[L_TOTAL_QUERY] * H[L_HQ] * sizeof(float));
+    w.part = align_up(w.lse + (size_t)H[L_LSE_SLOTS] * sizeof(float2));
     // importance partials: per kv head and token, one per half of the query columns
     w.cnt = align_up(w.part + 2 * (size_t)H[L_HKV] * H[L_TOTAL_TOKENS] * sizeof(float));
-    // counters: importance runs (one per key tile at most), the LSE pass's (kv head, pair)s, and
-    // the LSE kernel's item counter
-    w.total = align_up(w.cnt + ((size_t)H[L_TOTAL_KTILES] + H[L_N_LSE_PAIRS] + 1) * sizeof(int32_t));
+    // counters: importance runs (one per key tile at most) and the LSE kernel's item counter
+    w.total = align_up(w.cnt + ((size_t)H[L_TOTAL_KTILES] + 1) * sizeof(int32_t));
     return w;
 }
 
@@ -273,14 +271,13 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
     __half* q_rot = reinterpret_cast<__half*>(base + w.q);
     __half* kc = reinterpret_cast<__half*>(base + w.kc);
     float2* lse = reinterpret_cast<float2*>(base + w.lse);
-    float* lse_final = reinterpret_cast<float*>(base + w.lsef);
     float* part = reinterpret_cast<float*>(base + w.part);
     int32_t* cnt = reinterpret_cast<int32_t*>(base + w.cnt);
     const int g = H[L_GROUP];
     const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     const float2* rope2 = reinterpret_cast<const float2*>(rope);
 
-    const int32_t n_cnt = H[L_TOTAL_KTILES] + H[L_N_LSE_PAIRS] + 1;   // cleared by the rotation kernel
+    const int32_t n_cnt = H[L_TOTAL_KTILES] + 1;   // cleared by the rotation kernel
     RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_query), lay->dev + H[L_OFF_QPOS], q_rot, H[L_TOTAL_QUERY],
                H[L_HQ], g, scale_log2, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
     RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
@@ -300,8 +297,7 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
         using SM = AttnSmem<D, true>;
         auto kern = attn_kernel<D, true>;
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
-        AttnParams p{lay->dev, nullptr, nullptr, nullptr, lse, lse_final, cnt + H[L_TOTAL_KTILES], nullptr, nullptr,
-                     cnt + H[L_TOTAL_KTILES] + H[L_N_LSE_PAIRS]};
+        AttnParams p{lay->dev, nullptr, nullptr, nullptr, lse, nullptr, nullptr, cnt + H[L_TOTAL_KTILES]};
         // persistent: at most one CTA per SM, items handed out in list order
         const int grid = std::min<int>(H[L_N_LSE_ITEMS], kNumSms);
         if ((s = launch(kern, dim3(grid), dim3(kAttnThreads), SM::kAlloc, st, tq128, tkc, zero, zero, zero, p)) !=
@@ -312,7 +308,7 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
         using SM = ImpSmem<D>;
         auto kern = imp_kernel<D>;
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
-        ImpParams p{lay->dev, lse_final, part, cnt, importance};
+        ImpParams p{lay->dev, lse, part, cnt, importance};
         if ((s = launch(kern, dim3(H[L_N_IMP_ITEMS]), dim3(kImpThreads), SM::kAlloc, st, tq256, tkc, p)) != PCF_OK)
             return s;
     }
@@ -372,8 +368,7 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
     __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(base + w.po);
     float2* part_ml = reinterpret_cast<float2*>(base + w.pml);
-    AttnParams p{lay->dev, kpos_c, row_pos, reinterpret_cast<__nv_bfloat16*>(out), nullptr, nullptr, nullptr, part_o,
-                 part_ml, sched};
+    AttnParams p{lay->dev, kpos_c, row_pos, reinterpret_cast<__nv_bfloat16*>(out), nullptr, part_o, part_ml, sched};
     // persistent: at most one CTA per SM, items handed out in list order (largest estimate first)
     const int grid = std::min<int>(H[L_N_ATTN_ITEMS], kNumSms);
     if ((s = launch(kern, dim3(grid), dim3(kAttnThreads), SM::kAlloc, st, tq, tkc, tvc, tkf, tvf, p)) != PCF_OK)

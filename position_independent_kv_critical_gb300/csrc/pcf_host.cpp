@@ -62,7 +62,7 @@ struct Plan {
     int32_t total_tokens = 0, total_query = 0, total_rows = 0, total_sel = 0, total_pages = 0;
     int32_t n_spans = 0, max_tokens = 0, max_rows = 0, max_query = 0, total_ktiles = 0;
     int32_t n_attn = 0, n_lse = 0, n_imp = 0, lse_slots = 0, max_span_len = 0;
-    int32_t n_comb = 0, attn_slots = 0, n_pairs = 0, n_lse_pairs = 0, imp_tiles = 1;
+    int32_t n_comb = 0, attn_slots = 0, n_pairs = 0, imp_tiles = 1;
     std::vector<int32_t> lse_chunks;
     std::vector<int32_t> pair_base;     // per request: first pair record
     std::vector<int32_t> pair_tiles;    // per pair record: estimated key tiles of the pair
@@ -244,7 +244,7 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
         }
     }
     plan->lse_chunks.assign(n_reqs, 0);
-    int64_t n_attn = 0, n_lse = 0, n_imp = 0, slots = 0, n_comb = 0, attn_slots = 0, n_lse_pairs = 0;
+    int64_t n_attn = 0, n_lse = 0, n_imp = 0, slots = 0, n_comb = 0, attn_slots = 0;
     // importance pass: CTAs over runs of key tiles of one kv head; run lengths by the same
     // estimate as the attention splits (a CTA costs about one step more than its tiles)
     {
@@ -279,7 +279,6 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
             const int32_t chunks = cdiv(nkt, tpc);
             plan->lse_chunks[b] = chunks;
             n_lse += (int64_t)d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta) * chunks;
-            n_lse_pairs += (int64_t)d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta);
             slots += (int64_t)r.n_query * d.n_q_heads * chunks;
         }
         if (nkt > 0) n_imp += (int64_t)cdiv(nkt, plan->imp_tiles) * d.n_kv_heads;
@@ -292,7 +291,6 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
     plan->n_attn = (int32_t)n_attn;
     plan->n_lse = (int32_t)n_lse;
     plan->n_imp = (int32_t)n_imp;
-    plan->n_lse_pairs = (int32_t)n_lse_pairs;
     plan->lse_slots = (int32_t)slots;
 
     plan->words = L_HEADER + (int64_t)n_reqs * R_STRIDE + tot_spans * S_STRIDE +
@@ -354,7 +352,6 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
     H[L_N_COMB] = plan.n_comb;
     H[L_ATTN_SLOTS] = plan.attn_slots;
     H[L_N_PAIRS] = plan.n_pairs;
-    H[L_N_LSE_PAIRS] = plan.n_lse_pairs;
 
     int64_t off = L_HEADER;
     H[L_OFF_REQ] = (int32_t)off;    off += (int64_t)n_reqs * R_STRIDE;
@@ -385,7 +382,7 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
     int32_t slot_base = 0;
 
     int32_t tok_base = 0, q_base = 0, row_base = 0, sel_base = 0, span_base = 0, kt_base = 0;
-    int32_t lse_base = 0, lse_pair_base = 0;
+    int32_t lse_base = 0;
     for (int b = 0; b < n_reqs; ++b) {
         const pcf_request_desc& r = reqs[b];
         int32_t* R = REQ + (int64_t)b * R_STRIDE;
@@ -424,9 +421,6 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
         R[R_N_ROWS] = n_rows;
         R[R_LSE_BASE] = lse_base;
         R[R_LSE_CHUNKS] = plan.lse_chunks[b];
-        R[R_LSE_PAIR_BASE] = lse_pair_base;
-        if (plan.lse_chunks[b] > 0)
-            lse_pair_base += d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta);
         R[R_KTILE_BASE] = kt_base;
         R[R_N_KTILES] = nkt;
         R[R_PAIR_BASE] = plan.pair_base[b];
