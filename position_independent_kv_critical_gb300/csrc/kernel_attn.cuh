@@ -224,12 +224,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         int kc = 0;                                   // K tiles this CTA issued before the item
         int last_k[kKStages] = {-1, -1}, last_q = -1;  // for the final drain
         bool ok = true;
-        // layout values the producer needs after publishing an item, read into registers up front:
-        // every barrier call is a compiler memory barrier, after which a layout word would be
-        // loaded again on the item's critical path (the Q copy waits for it)
-        const int32_t tot_tok = L[L_TOTAL_TOKENS], tot_valid = L[L_TOTAL_VALID], tot_rows = L[L_TOTAL_ROWS];
-        const int32_t tot_query = L[L_TOTAL_QUERY];
-        const int32_t* const page_pos_all = L + L[L_OFF_PAGEPOS];
         for (int it = 0; ok; ++it) {
             // the next item: the first is this CTA's own, the rest come in list order
             int idx = 0;
@@ -242,7 +236,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             w.lse_base = w.lse_chunks = 0;
             w.pad[0] = w.pad[1] = 0;
             const int32_t* R = L;
-            int32_t r_tok_base = 0, r_q_base = 0, r_n_kept = 0, r_page_base = 0, r_n_pages = 0;
             if (idx < n_items) {
                 const int32_t* item = items + kItemWords * idx;
                 w.req = item[0];
@@ -253,11 +246,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 w.n_rows = LSE ? R[R_N_QUERY] : R[R_N_ROWS];
                 w.row_base = R[R_ROW_BASE];
                 w.cbase = R[R_CBASE];
-                r_tok_base = R[R_TOK_BASE];
-                r_q_base = R[R_Q_BASE];
-                r_n_pages = R[R_N_PAGES];
-                r_n_kept = r_n_pages * kPage - R[R_N_SEL];
-                r_page_base = R[R_PAGE_BASE];
                 if (LSE) {
                     // LSE: tiles of all the request's cached tokens, cut into chunks
                     const int nkt = R[R_N_KTILES], chunks = R[R_LSE_CHUNKS];
@@ -271,14 +259,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     // visible tiles: key positions increase along the compacted cached tiles and
                     // along the fresh rows, so each count is the number of tiles whose first key
                     // is at or before the pair's last row (the lanes test 32 tiles at a time)
-                    const int n_rows_req = w.n_rows;
-                    const int32_t row_base = w.row_base;
+                    const int n_rows_req = R[R_N_ROWS];
+                    const int32_t row_base = R[R_ROW_BASE];
                     const int row0 = w.qpair * kQTilesPerCta * toks_per_tile;
                     const int nrow = min(kQTilesPerCta * toks_per_tile, n_rows_req - row0);
-                    const int nkt = (r_n_kept + kTileKeys - 1) / kTileKeys;
+                    const int nkt = (R[R_N_PAGES] * kPage - R[R_N_SEL] + kTileKeys - 1) / kTileKeys;
                     const int32_t pmax = nrow > 0 ? prm.row_pos[row_base + row0 + nrow - 1] : -1;
                     const int nft_total = (n_rows_req + kTileKeys - 1) / kTileKeys;
-                    const int32_t* kpc = prm.kpos_c + w.cbase;
+                    const int32_t* kpc = prm.kpos_c + R[R_CBASE];
                     int nct = 0, nft = 0;
                     for (int b = 0; b < nkt; b += 32)
                         nct += __popc(__ballot_sync(0xffffffffu, b + lane < nkt && kpc[(b + lane) * kTileKeys] <= pmax));
@@ -305,18 +293,18 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok || w.req < 0) break;
-            const int n_rows_req = w.n_rows;
-            const int32_t row_base = w.row_base;
+            const int n_rows_req = LSE ? R[R_N_QUERY] : R[R_N_ROWS];
+            const int32_t row_base = R[R_ROW_BASE];
             const int row0 = w.qpair * kQTilesPerCta * toks_per_tile;
-            const int32_t kc_row0 = LSE ? w.kvh * tot_tok + r_tok_base : w.kvh * tot_valid + w.cbase;
-            const int32_t kf_row0 = w.kvh * tot_rows + row_base;
+            const int32_t kc_row0 = LSE ? w.kvh * L[L_TOTAL_TOKENS] + R[R_TOK_BASE]
+                                        : w.kvh * L[L_TOTAL_VALID] + R[R_CBASE];
+            const int32_t kf_row0 = w.kvh * L[L_TOTAL_ROWS] + row_base;
             // key positions, which only the softmax waits for: lane l holds those of keys l, l+32,
             // l+64, l+96 of a tile (kNoPos for a missing key), loaded one tile ahead; the first
             // tile's are requested now, before the wait for the Q buffer
             const int n_ct = w.n_ct, n_tiles = w.n_ct + w.n_ft;
-            const int n_kept = r_n_kept;
-            const int32_t* page_pos = page_pos_all + r_page_base;
-            const int32_t* kpc_req = prm.kpos_c + w.cbase;
+            const int n_kept = R[R_N_PAGES] * kPage - R[R_N_SEL];
+            const int32_t* page_pos = L + L[L_OFF_PAGEPOS] + R[R_PAGE_BASE];
             auto meta = [&](int j, int32_t (&pos)[4]) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
@@ -325,10 +313,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     if (j < n_ct) {
                         if (LSE) {
                             const int lp = (w.t0 + j) * kPagesPerTile + key / kPage;
-                            if (lp < r_n_pages) pos[r] = page_pos[lp] + key % kPage;
+                            if (lp < R[R_N_PAGES]) pos[r] = page_pos[lp] + key % kPage;
                         } else {
                             const int ci = j * kTileKeys + key;
-                            if (ci < n_kept) pos[r] = kpc_req[ci];
+                            if (ci < n_kept) pos[r] = prm.kpos_c[R[R_CBASE] + ci];
                         }
                     } else if (j < n_tiles) {
                         const int fr = (j - n_ct) * kTileKeys + key;
@@ -340,8 +328,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (w.n_loc > 0) meta(w.jb, pos_n);
             // the item's Q tiles, once both Q K^T issuers are done with the previous item's
             if (lane == 0) {
-                const int32_t qy = LSE ? (w.kvh * tot_query + r_q_base + row0) * g
-                                       : (w.kvh * tot_rows + row_base + row0) * g;
+                const int32_t qy = LSE ? (w.kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row0) * g
+                                       : (w.kvh * L[L_TOTAL_ROWS] + row_base + row0) * g;
                 if (it > 0) {
                     // warm L2 with the Q rows while the previous item drains
                     for (int t = 0; t < kQTilesPerCta; ++t)
@@ -395,7 +383,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             prefetch_tmap(&tm_vfresh);
             int vc = 0;
             int last_v[kVStages] = {-1, -1};
-            const int32_t tot_valid = L[L_TOTAL_VALID];
             for (int it = 0;; ++it) {
                 AttnItem w;
                 if (!take_item(it, w)) break;
@@ -409,7 +396,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     uint64_t* full = &bars[B_V_FULL + vs];
                     mbar_arrive_expect_tx(full, H * 16384);
                     if (j < w.n_ct) {
-                        const int32_t y = w.kvh * tot_valid + w.cbase + j * kTileKeys;
+                        const int32_t y = w.kvh * L[L_TOTAL_VALID] + w.cbase + j * kTileKeys;
                         for (int hb = 0; hb < H; ++hb) tma_load_2d(sVs(vs) + hb * 16384, &tm_vcache, full, hb * 64, y);
                     } else {
                         const int32_t fr = w.row_base + (j - w.n_ct) * kTileKeys;
@@ -667,12 +654,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
                 tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
                 tmem_ld_wait();
-                if (LSE) {
-                    // nothing goes back to TMEM in LSE mode: the S buffer is free for the next Q K^T
-                    // as soon as its scores are in registers
-                    tc_fence_before();
-                    mbar_arrive(&bars[B_P_FULL + 2 * t + (hg & 1)]);
-                }
                 if (!full) {
                     // keys at or beyond the causal limit leave the row: score -inf
 #pragma unroll
@@ -706,14 +687,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     acc2[e & 1] = f2_add(acc2[e & 1], f2_pack(p0, p1));
                     pk[e] = pack_bf16x2(p0, p1);
                 }
-                if (!LSE) tmem_st32(tS, pk);
+                tmem_st32(tS, pk);
                 {
                     float a0, a1, b0, b1;
                     f2_unpack(acc2[0], a0, a1);
                     f2_unpack(acc2[1], b0, b1);
                     l_run += (a0 + b0) + (a1 + b1);
                 }
-                if (!LSE) {
+                {
                     if (q > 0 && __any_sync(0xffffffffu, need)) {
                         // every earlier P V of this tile must be done before O is rescaled
                         ok = mbar_wait(&bars[B_PV_DONE + 2 * t + ((hg - 1) & 1)], ((hg - 1) >> 1) & 1, abort_flag);
@@ -754,32 +735,20 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tc_fence_after();
                 if (w.n_loc > 0) {
                     const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-                    // 64 columns per TMEM round trip; a row's bf16 values leave in whole 32-byte
-                    // sectors where the destination allows (half the store transactions of 16-byte
-                    // stores, whose sectors the L2 would take half-written)
-                    const bool wide = (reinterpret_cast<uintptr_t>(out_row) & 31u) == 0;
 #pragma unroll 1
-                    for (int cc = 0; cc < D / 64; ++cc) {
-                        uint32_t o0[32], o1[32];
-                        tmem_ld32(tO + cc * 64, o0);
-                        tmem_ld32(tO + cc * 64 + 32, o1);
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + cc * 32, o);
                         tmem_ld_wait();
                         if (valid) {
-                            uint32_t pk[32];
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                pk[e] = pack_bf16x2(__uint_as_float(o0[2 * e]) * inv, __uint_as_float(o0[2 * e + 1]) * inv);
-                                pk[16 + e] = pack_bf16x2(__uint_as_float(o1[2 * e]) * inv, __uint_as_float(o1[2 * e + 1]) * inv);
-                            }
-                            __nv_bfloat16* dst = out_row + cc * 64;
-                            if (wide) {
-#pragma unroll
-                                for (int qq = 0; qq < 4; ++qq) st_global_v8(dst + 16 * qq, pk + 8 * qq);
-                            } else {
-#pragma unroll
-                                for (int qq = 0; qq < 8; ++qq)
-                                    *reinterpret_cast<uint4*>(dst + 8 * qq) =
-                                        make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
+                            for (int qq = 0; qq < 4; ++qq) {
+                                uint4 v;
+                                v.x = pack_bf16x2(__uint_as_float(o[8 * qq + 0]) * inv, __uint_as_float(o[8 * qq + 1]) * inv);
+                                v.y = pack_bf16x2(__uint_as_float(o[8 * qq + 2]) * inv, __uint_as_float(o[8 * qq + 3]) * inv);
+                                v.z = pack_bf16x2(__uint_as_float(o[8 * qq + 4]) * inv, __uint_as_float(o[8 * qq + 5]) * inv);
+                                v.w = pack_bf16x2(__uint_as_float(o[8 * qq + 6]) * inv, __uint_as_float(o[8 * qq + 7]) * inv);
+                                *reinterpret_cast<uint4*>(out_row + cc * 32 + 8 * qq) = v;
                             }
                         }
                     }
