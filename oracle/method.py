@@ -10,11 +10,15 @@ Steps, in the order the pages give them:
    rotated explicitly at pi(j), each query at its own position, softmax over all cached keys of
    the request, weights summed over heads and query tokens (QCFuse, section 2B; second summary
    Phase 3);
-3. Top-N selection of the tokens to recompute, per span, ties to the lower index (QCFuse 2B);
+3. Top-N selection of the tokens to recompute, per span, ties to the lower index (QCFuse 2B),
+   or over the whole request with the same budget (the pages' own global Top-N);
 4. fused attention of the recomputed rows and the query rows over the merged key set: cached keys
    minus the recomputed tokens, plus the fresh rows at their positions, causal on logical
    position (QCFuse 2C and Phase 4; second summary section 3 "strictly keeps causal constraints";
    MiniPIC 2.1 score equation).
+
+Offline, before any request (QCFuse 2A, second summary Phase 1): each span's anchor tokens, the
+few with the highest key norm.
 
 Readings where the pages are silent (also listed in the design doc): rotate-half RoPE pairing; softmax
 over the request's cached keys only for scoring; a plain sum over heads and query tokens; query
@@ -108,6 +112,35 @@ def select_topk_request(imp: np.ndarray, span_lens: Sequence[int], span_k: Seque
         out.append(np.sort(order[:k]).astype(np.int64) + off)
         off += L
     return np.concatenate(out) if out else np.zeros((0,), dtype=np.int64)
+
+
+def select_topn_global_request(imp: np.ndarray, n_sel: int) -> np.ndarray:
+    """QCFuse, section 2B (Top-N tokens of the whole context) and its Phase 3 summary: the n_sel
+    request-local token indices with the largest importance over all of the request's cached
+    tokens, ties to the lower index, in ascending index order.  The budget n_sel is the sum of the
+    spans' k, so only the placement across spans differs from the per-span selection.
+
+    ``imp`` is taken exactly as given (pass fp32 values to take the decision in fp32)."""
+    imp = np.asarray(imp, dtype=np.float64)
+    order = np.lexsort((np.arange(imp.shape[0]), -imp))    # primary key: -value, then index
+    return np.sort(order[:n_sel]).astype(np.int64)
+
+
+def key_norms(K: np.ndarray) -> np.ndarray:
+    """QCFuse, section 2A (anchor extraction) and Phase 1: the magnitude of each cached token's
+    key, read here as the Euclidean norm of its unrotated key over all kv heads and dimensions,
+    ``K`` [N][Hkv][d] -> [N] (fp64).  Rotation preserves the norm, so the cached (position-free)
+    key gives the same value as the key at any position."""
+    K = np.asarray(K, dtype=np.float64)
+    return np.sqrt((K * K).reshape(K.shape[0], -1).sum(axis=1))
+
+
+def select_anchors_request(norms: np.ndarray, span_lens: Sequence[int], span_m: Sequence[int]
+                           ) -> np.ndarray:
+    """QCFuse, section 2A: per span, the m_s tokens with the highest key norm are its anchors
+    (a small share of the span's tokens), ties to the lower index, ascending; the same per-span
+    selection as the recompute Top-N, on the key norms instead of the importance."""
+    return select_topk_request(norms, span_lens, span_m)
 
 
 def row_positions(sel: np.ndarray, k_pos: np.ndarray, n_query: int, query_pos0: int) -> np.ndarray:

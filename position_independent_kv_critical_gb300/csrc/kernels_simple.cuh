@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob a, RopeJob b, Ro
             if (ex & bit) return;   // recomputed: its fresh row replaces it
             oi = J.cidx[row / kPage] + row % kPage - __popc(ex & (bit - 1u));   // kept tokens before it
             orow_n = J.n_out;
+            if (oi < 0 || oi >= J.n_out) { set_dev_error(kDevErrBounds); return; }
             vsrc0 = J.v_src + off;
             if (c == 0 && hbeg == 0) J.pos_out[oi] = p;
         }
@@ -356,6 +357,8 @@ __global__ void __launch_bounds__(kScanThreads) compact_scan_kernel(const int32_
         if (p < n_pages) cidx[pb + p] = carry + before;
         carry += total;
     }
+    // exclusion bits that do not leave exactly the request's kept count are a caller error
+    if (threadIdx.x == 0 && carry != R[R_CBASE] + n_pages * kPage - R[R_N_SEL]) set_dev_error(kDevErrBounds);
 }
 
 // ------------------------------------------------------------------ split-range combine

@@ -197,6 +197,75 @@ def test_topk_all_equal_takes_first_indices_and_boundary_ties():
     assert list(method.select_topk_request(w, [32], [32])) == list(range(32))
 
 
+# ---------- global Top-N (the pages' own reading) ----------
+
+def test_global_topn_worked_example():
+    v = np.array([0.1, 0.5, 0.5, 0.2, 0.9], dtype=np.float32)
+    assert list(method.select_topn_global_request(v, 2)) == [1, 4]     # 0.9, then the first 0.5
+    assert list(method.select_topn_global_request(v, 3)) == [1, 2, 4]
+    assert list(method.select_topn_global_request(v, 0)) == []
+    assert list(method.select_topn_global_request(v, 5)) == [0, 1, 2, 3, 4]
+
+
+def test_global_topn_single_span_equals_per_span_selection():
+    rng = np.random.default_rng(11)
+    vals = rng.integers(0, 9, size=96).astype(np.float32) * np.float32(0.25)
+    for k in (0, 1, 17, 50, 96):
+        assert list(method.select_topn_global_request(vals, k)) == list(method.select_topk_request(vals, [96], [k]))
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_global_topn_separates_chosen_from_the_rest(seed):
+    """Every chosen value is >= every other value; among values equal to the smallest chosen one,
+    the chosen are the lowest indices (checked by counting, not by sorting)."""
+    rng = np.random.default_rng(100 + seed)
+    vals = rng.integers(0, 6, size=200).astype(np.float32)
+    n = int(rng.integers(1, 200))
+    sel = method.select_topn_global_request(vals, n)
+    assert len(sel) == n and np.all(np.diff(sel) > 0)
+    rest = np.setdiff1d(np.arange(200), sel)
+    t = vals[sel].min()
+    assert len(rest) == 0 or vals[rest].max() <= t
+    ties = np.nonzero(vals == t)[0]
+    taken = np.intersect1d(ties, sel)
+    assert list(taken) == list(ties[:len(taken)])
+
+
+def test_global_topn_moves_the_budget_across_spans():
+    """Two spans of 16 with k = 4 each: per span takes 4 + 4; globally all 8 come from the span
+    holding the larger values."""
+    v = np.concatenate([np.linspace(1.0, 2.0, 16), np.linspace(0.0, 0.5, 16)]).astype(np.float32)
+    per_span = method.select_topk_request(v, [16, 16], [4, 4])
+    assert list(per_span) == [12, 13, 14, 15, 28, 29, 30, 31]
+    assert list(method.select_topn_global_request(v, 8)) == list(range(8, 16))
+
+
+# ---------- anchors: key norms and per-span top-m ----------
+
+def test_key_norms_closed_forms():
+    K = np.full((3, 8, 128), 0.5)
+    np.testing.assert_allclose(method.key_norms(K), 0.5 * math.sqrt(8 * 128), rtol=1e-15)
+    E = np.zeros((4, 2, 64))
+    E[0, 1, 5] = -3.0
+    E[1, 0, 63] = 2.5
+    E[3, 1, 0], E[3, 0, 1] = 3.0, 4.0       # a 3-4-5 triangle across two heads
+    np.testing.assert_allclose(method.key_norms(E), [3.0, 2.5, 0.0, 5.0], rtol=1e-15)
+
+
+def test_key_norms_do_not_depend_on_the_position():
+    """RoPE is a rotation: the norm of the cached (position-free) key equals that of the key
+    rotated to any position, so anchors need no positions."""
+    rng = np.random.default_rng(5)
+    K = rng.standard_normal((40, 4, 64))
+    pos = rng.integers(0, 60000, 40)
+    np.testing.assert_allclose(method.key_norms(rope.rotate(K, pos, 5e5)), method.key_norms(K), rtol=1e-12)
+
+
+def test_anchors_worked_example():
+    norms = np.array([1.0, 3.0, 2.0, 3.0, 0.5, 0.5, 4.0, 0.1], dtype=np.float32)
+    assert list(method.select_anchors_request(norms, [4, 4], [2, 1])) == [1, 3, 6]
+
+
 def test_k_from_percent_golden_table():
     with open(os.path.join(GOLDEN, "recompute_counts.txt")) as fh:
         rows = [ln.split("#")[0].split() for ln in fh if ln.split("#")[0].strip()]
