@@ -25,7 +25,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workload import CONFIGS, hidden_rows, make_batch  # noqa: E402
+from workload import CONFIGS, PAGE, Request, Span, hidden_rows, make_batch  # noqa: E402
 
 METRIC = "fused-prefill tokens/s per layer; attention TFLOP/s vs GB300 bf16 tensor peak"
 DESCR = {
@@ -206,6 +206,73 @@ def run_reference(args):
     }))
 
 
+def run_op(args, pcf, b, L, cf, k_pool, dev, world, rank, local):
+    """Time one selection variant alone: anchor key norms (HBM-bound: reads every cached key once)
+    or the global Top-N (one block per request, launch- and latency-bound)."""
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    if args.op == "key_norms":
+        # anchor extraction is offline, once per stored span: a layout that lists every span of
+        # the pool once (no query, nothing recomputed)
+        cfg = CONFIGS[args.config]
+        pps = cfg.span_len // PAGE
+        pool_req = Request(spans=[Span(i * pps, pps, i * cfg.span_len, 0) for i in range(cfg.pool_spans)],
+                           n_query=0, query_pos0=cfg.pool_spans * cfg.span_len)
+        L = pcf.Layout([pool_req], b.hq, b.hkv, b.d, b.n_phys_pages, cfg.pool_spans * cfg.span_len + 1,
+                       device=str(dev))
+    norms = torch.empty(max(1, L.total_tokens), dtype=torch.float32, device=dev)
+    pcf.key_norms(L, k_pool, norms)
+    if args.op == "key_norms":
+        call = lambda: pcf.key_norms(L, k_pool, norms)
+    else:
+        call = lambda: pcf.select_topn_global(L, norms, cf.sel_idx, cf.excl, cf.row_pos)
+    for _ in range(max(3, args.warmup)):
+        call()
+    pcf.check_device_error()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    pcf.check_device_error()
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    _, _, hbm, src = _peaks()
+    if args.op == "key_norms":
+        nbytes = L.total_tokens * (b.hkv * b.d * 2 + 4)     # every cached key read once, one fp32 out
+        gbs = world * nbytes / (ms / 1e3) / 1e9
+        metric, value, unit, hib = "anchor key norms over the span pool: key bytes read per second", gbs, "GB/s", True
+        roof = {"bound": "hbm", "achieved": gbs / world, "peak": hbm, "unit": "GB/s", "frac": gbs / world / hbm,
+                "peak_source": src + " copy", "traffic": None, "algorithmic_bytes_per_launch": nbytes}
+    else:
+        metric, value, unit, hib = "global Top-N selection time per call", ms * 1e3, "us", False
+        nbytes = L.total_tokens * 4 + L.total_sel * 8 + L.total_pages * 2 + L.total_rows * 4
+        gbs = nbytes / (ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                "peak_source": src + " copy", "traffic": None, "algorithmic_bytes_per_launch": nbytes}
+    if rank == 0:
+        print(json.dumps({
+            "op": args.op, "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": hib, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32" if args.op == "key_norms" else "u32", "data": "synthetic",
+            "config": {"workload": f"{args.config}: {DESCR[args.config]}", "tokens": L.total_tokens,
+                       "l2": "flushed between timed calls (512 MB write)"},
+            "roofline": roof, "gpu_launches": K, "clocks": clk,
+        }))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -215,6 +282,9 @@ def main():
     ap.add_argument("--pct", type=int, default=None)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="step", choices=["step", "key_norms", "topn_global"],
+                    help="step: the hot path (default); key_norms / topn_global: one of the two "
+                         "selection variants alone, on the workload's layout")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -237,6 +307,9 @@ def main():
     g = lambda t: t.to(dev)
     k_pool, v_pool = g(b.k_pool), g(b.v_pool)
     q_query, q_fresh, k_fresh, v_fresh = g(b.q_query), g(b.q_fresh), g(b.k_fresh), g(b.v_fresh)
+    if args.op != "step":
+        run_op(args, pcf, b, L, cf, k_pool, dev, world, rank, local)
+        return
     hidden = hidden_rows(torch.arange(L.total_tokens, device=dev), D)
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2

@@ -149,6 +149,23 @@ pcf_status pcf_score(const pcf_layout* layout, const uint16_t* q_query, const ui
 pcf_status pcf_select_topk(const pcf_layout* layout, const float* importance, int32_t* sel_idx,
                            uint16_t* excl, int32_t* row_pos, void* stream);
 
+/* Global Top-N (QCFuse 2B read literally: one selection over all of a request's cached tokens).
+ * For every request b: the N_b = sum over its spans of k_s request-local token indices with the
+ * largest importance over the whole request, ties to the lower index, in ascending order at
+ * sel_idx[sel_base_b ...]; excl and row_pos as for pcf_select_topk.  The budget per request,
+ * hence every row count and buffer size, is that of the per-span selection: only where the N_b
+ * tokens fall differs.  Bit-exact and deterministic; one block per request (its cached tokens
+ * must fit a 48 KB bitmap: at most 393216 of them, else PCF_ERR_UNSUPPORTED). */
+pcf_status pcf_select_topn_global(const pcf_layout* layout, const float* importance, int32_t* sel_idx,
+                                  uint16_t* excl, int32_t* row_pos, void* stream);
+
+/* Anchor key norms (QCFuse 2A / Phase 1, anchor extraction): norms[t] for every cached token t
+ * of the layout (same order as importance) = Euclidean norm of its unrotated key over all Hkv
+ * heads and d dimensions, fp32 accumulation of the bf16 squares.  A span's anchors are then its
+ * tokens with the largest norms: pcf_select_topk on a layout whose span k's are the anchor
+ * counts, fed these norms as the importance.  k_pool as for pcf_score (16-byte aligned). */
+pcf_status pcf_key_norms(const pcf_layout* layout, const uint16_t* k_pool, float* norms, void* stream);
+
 /* Row gather of the recompute batch: dst[sel_base_b + i][:] = src[tok_base_b + sel_idx[...]][:]
  * for every selected row; src [total_tokens][row_elems], dst [total_sel][row_elems], bf16;
  * row_elems a positive multiple of 8. */

@@ -158,6 +158,24 @@ def select_topk(layout: Layout, importance, sel_idx, excl, row_pos, stream=None)
         ctypes.byref(layout.ref), _p(importance), _p(sel_idx), _p(excl), _p(row_pos), _stream(stream)))
 
 
+def select_topn_global(layout: Layout, importance, sel_idx, excl, row_pos, stream=None):
+    """One Top-N per request over all its cached tokens (budget: the sum of its spans' k)."""
+    _need(importance, torch.float32, "importance")
+    _need(sel_idx, torch.int32, "sel_idx")
+    _need(excl, torch.int16, "excl")
+    _need(row_pos, torch.int32, "row_pos")
+    _lib.check("pcf_select_topn_global", _lib.load().pcf_select_topn_global(
+        ctypes.byref(layout.ref), _p(importance), _p(sel_idx), _p(excl), _p(row_pos), _stream(stream)))
+
+
+def key_norms(layout: Layout, k_pool, norms, stream=None):
+    """Key norm of every cached token of the layout (anchor extraction)."""
+    _need(k_pool, torch.bfloat16, "k_pool")
+    _need(norms, torch.float32, "norms")
+    _lib.check("pcf_key_norms", _lib.load().pcf_key_norms(
+        ctypes.byref(layout.ref), _p(k_pool), _p(norms), _stream(stream)))
+
+
 def gather_rows(layout: Layout, sel_idx, src, dst, stream=None):
     _need(src, torch.bfloat16, "src")
     _need(dst, torch.bfloat16, "dst")

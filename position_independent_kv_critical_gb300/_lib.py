@@ -29,7 +29,8 @@ EXPORTS = (
     "pcf_status_string", "pcf_k_from_percent", "pcf_rope_table_init", "pcf_layout_words",
     "pcf_layout_build", "pcf_layout_query", "pcf_score_workspace_bytes", "pcf_score",
     "pcf_select_topk", "pcf_gather_rows", "pcf_attention_workspace_bytes", "pcf_fused_attention",
-    "pcf_check_device_error", "pcf_score_noalloc", "pcf_copy_async",
+    "pcf_check_device_error", "pcf_score_noalloc", "pcf_copy_async", "pcf_select_topn_global",
+    "pcf_key_norms",
 )
 
 
@@ -82,6 +83,10 @@ def _declare(lib):
     lib.pcf_score.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
     lib.pcf_select_topk.restype = c_int32
     lib.pcf_select_topk.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    lib.pcf_select_topn_global.restype = c_int32
+    lib.pcf_select_topn_global.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    lib.pcf_key_norms.restype = c_int32
+    lib.pcf_key_norms.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p]
     lib.pcf_gather_rows.restype = c_int32
     lib.pcf_gather_rows.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_int32, c_void_p, c_void_p]
     lib.pcf_fused_attention.restype = c_int32

@@ -305,6 +305,171 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const int32_t* __res
         ex[p] = (uint16_t)((s_bits[p >> 1] >> ((p & 1) * 16)) & 0xFFFFu);
 }
 
+// ------------------------------------------------------------------ global Top-N
+// QCFuse section 2B read literally: one Top-N over all of a request's cached tokens, with the
+// request's budget N = sum of its spans' k (so the rows, their order and every buffer size stay
+// those of the per-span selection).  One block per request: a 4-pass 8-bit radix select of the
+// N-th largest key (fp32 bits, monotone for the non-negative importance and norms), then the
+// tokens above it and the lowest-indexed ones equal to it, written in ascending order with the
+// same outputs as topk_kernel; the block also writes the query rows' positions.
+constexpr int kTopnThreads = 1024;
+__global__ void __launch_bounds__(kTopnThreads) topn_global_kernel(const int32_t* __restrict__ L,
+                                                                   const float* __restrict__ imp,
+                                                                   int32_t* __restrict__ sel_idx,
+                                                                   uint16_t* __restrict__ excl,
+                                                                   int32_t* __restrict__ row_pos) {
+    extern __shared__ uint32_t s_bits[];   // selected-token bitmap of the request
+    __shared__ int s_hist[256];
+    __shared__ int s_warp[kTopnThreads / 32];
+    __shared__ int s_bucket, s_above;
+    const int tid = threadIdx.x;
+    // layout fields first: they do not depend on the previous kernel, which may still be running
+    const int32_t* R = L + L[L_OFF_REQ] + blockIdx.x * R_STRIDE;
+    const int len = R[R_N_PAGES] * kPage;
+    const int k = R[R_N_SEL];
+    const float* v = imp + R[R_TOK_BASE];
+    const int32_t sel_base = R[R_SEL_BASE];
+    const int32_t rrow = R[R_ROW_BASE];
+    const int32_t* ppos = L + L[L_OFF_PAGEPOS] + R[R_PAGE_BASE];
+    uint16_t* ex = excl + R[R_PAGE_BASE];
+    const int nq = R[R_N_QUERY], p0 = R[R_QUERY_POS0];
+    const int nwords = (len + 31) >> 5;
+    for (int i = tid; i < nwords; i += kTopnThreads) s_bits[i] = 0u;
+    grid_dep_wait();
+    grid_dep_launch();
+    for (int t = tid; t < nq; t += kTopnThreads) row_pos[rrow + k + t] = p0 + t;
+
+    uint32_t thr = 0;      // key of the k-th largest value
+    int need_eq = 0;       // how many tokens equal to thr are taken (lowest indices first)
+    if (k > 0 && k < len) {
+        uint32_t prefix = 0, pmask = 0;
+        int remaining = k;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            if (tid < 256) s_hist[tid] = 0;
+            __syncthreads();
+            for (int i = tid; i < len; i += kTopnThreads) {
+                const uint32_t key = order_key(v[i]);
+                if ((key & pmask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
+            }
+            __syncthreads();
+            if (tid < 32) {
+                // lane l owns buckets 255-8l .. 248-8l (descending)
+                int cnt[8], tot = 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) { cnt[q] = s_hist[255 - 8 * tid - q]; tot += cnt[q]; }
+                int incl = tot;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o) incl += y;
+                }
+                const int excl_sum = incl - tot;
+                const bool here = excl_sum < remaining && incl >= remaining;
+                const unsigned m = __ballot_sync(0xffffffffu, here);
+                if (here && tid == __ffs(m) - 1) {
+                    int acc = excl_sum;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        if (acc + cnt[q] >= remaining) { s_bucket = 255 - 8 * tid - q; s_above = acc; break; }
+                        acc += cnt[q];
+                    }
+                }
+            }
+            __syncthreads();
+            const int bucket = s_bucket;
+            remaining -= s_above;
+            prefix |= (uint32_t)bucket << shift;
+            pmask |= 255u << shift;
+            __syncthreads();
+        }
+        thr = prefix;
+        need_eq = remaining;
+    }
+    // contiguous index range per thread keeps index order in the scans
+    const int per = (len + kTopnThreads - 1) / kTopnThreads;
+    const int i0 = min(len, tid * per), i1 = min(len, i0 + per);
+    int n_eq = 0;
+    if (k > 0 && k < len)
+        for (int i = i0; i < i1; ++i) n_eq += (order_key(v[i]) == thr);
+    const int eq_before = block_excl_scan<kTopnThreads>(n_eq, s_warp, nullptr);
+    int n_sel = 0;
+    {
+        int eq_rank = eq_before;
+        for (int i = i0; i < i1; ++i) {
+            bool take;
+            if (k >= len) take = true;
+            else if (k == 0) take = false;
+            else {
+                const uint32_t key = order_key(v[i]);
+                take = key > thr || (key == thr && eq_rank < need_eq);
+                eq_rank += (key == thr);
+            }
+            if (take) { ++n_sel; atomicOr(&s_bits[i >> 5], 1u << (i & 31)); }
+        }
+    }
+    int total = 0;
+    const int out_before = block_excl_scan<kTopnThreads>(n_sel, s_warp, &total);
+    if (tid == 0 && total != k) set_dev_error(kDevErrBounds);
+    int o = out_before;
+    for (int i = i0; i < i1; ++i) {
+        if ((s_bits[i >> 5] >> (i & 31)) & 1u) {
+            if (o < k) {
+                sel_idx[sel_base + o] = i;
+                row_pos[rrow + o] = ppos[i >> 4] + (i & 15);
+            }
+            ++o;
+        }
+    }
+    __syncthreads();
+    for (int p = tid; p < len / kPage; p += kTopnThreads)
+        ex[p] = (uint16_t)((s_bits[p >> 1] >> ((p & 1) * 16)) & 0xFFFFu);
+}
+
+// ------------------------------------------------------------------ anchor key norms
+// QCFuse section 2A / Phase 1: a cached token's key magnitude, read as the Euclidean norm of its
+// unrotated key over every kv head and dimension (rotation preserves it, so positions do not
+// matter).  One warp per token of the layout (global token t sits at in-page row t % 16 of
+// logical page t / 16): lane l sums the squares of the 16-byte chunks l, l+32, ... of the
+// token's Hkv x D values in fp32, a butterfly adds the lanes.  The pool is read before the
+// dependency wait (no kernel writes it); the norms are written after it.
+template <int D>
+__global__ void __launch_bounds__(256) key_norm_kernel(const int32_t* __restrict__ L,
+                                                       const __nv_bfloat16* __restrict__ k_pool,
+                                                       float* __restrict__ norms) {
+    constexpr int CPH = D / 8;   // 16-byte chunks per head row
+    const int64_t tok = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int32_t total = L[L_TOTAL_TOKENS], hkv = L[L_HKV], n_phys = L[L_N_PHYS];
+    float acc = 0.f;
+    bool ok = true;
+    if (tok < total) {
+        const int32_t ph = L[L[L_OFF_BLOCK] + (int32_t)(tok / kPage)];
+        ok = ph >= 0 && ph < n_phys;
+        if (ok) {
+            const __nv_bfloat16* base = k_pool + ((int64_t)ph * hkv * kPage + tok % kPage) * D;
+            for (int q = lane; q < hkv * CPH; q += 32) {
+                const int h = q / CPH, c = q % CPH;
+                const uint4 x = *reinterpret_cast<const uint4*>(base + (int64_t)h * kPage * D + 8 * c);
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
+                    acc = fmaf(a, a, acc);
+                    acc = fmaf(b, b, acc);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    grid_dep_wait();
+    grid_dep_launch();
+    if (tok < total && lane == 0) {
+        if (!ok) set_dev_error(kDevErrBounds);
+        else norms[tok] = sqrtf(acc);
+    }
+}
+
 // ------------------------------------------------------------------ row gather
 // dst[sel_base_b + i] = src[tok_base_b + sel_idx[sel_base_b + i]] -- the inputs of the tokens
 // chosen for recomputation (QCFuse Phase 4: discrete recomputation of the Top-N indices).

@@ -428,6 +428,36 @@ extern "C" pcf_status pcf_select_topk(const pcf_layout* layout, const float* imp
                   layout->dev, importance, sel_idx, excl, row_pos);
 }
 
+extern "C" pcf_status pcf_select_topn_global(const pcf_layout* layout, const float* importance, int32_t* sel_idx,
+                                             uint16_t* excl, int32_t* row_pos, void* stream) {
+    pcf_status s = check_layout(layout);
+    if (s != PCF_OK) return s;
+    const int32_t* H = layout->host;
+    if ((H[L_TOTAL_TOKENS] > 0 && (!importance || !excl)) || (H[L_TOTAL_SEL] > 0 && !sel_idx) ||
+        (H[L_TOTAL_ROWS] > 0 && !row_pos))
+        return PCF_ERR_INVALID_ARG;
+    if (H[L_N_REQS] == 0) return PCF_OK;
+    if ((s = check_device()) != PCF_OK) return s;
+    const int words = (H[L_MAX_TOKENS] + 31) / 32;
+    if (words * 4 > 48 * 1024) return PCF_ERR_UNSUPPORTED;
+    return launch(topn_global_kernel, dim3(H[L_N_REQS]), dim3(kTopnThreads), words * 4,
+                  static_cast<cudaStream_t>(stream), layout->dev, importance, sel_idx, excl, row_pos);
+}
+
+extern "C" pcf_status pcf_key_norms(const pcf_layout* layout, const uint16_t* k_pool, float* norms, void* stream) {
+    pcf_status s = check_layout(layout);
+    if (s != PCF_OK) return s;
+    const int32_t* H = layout->host;
+    if (H[L_TOTAL_TOKENS] == 0) return PCF_OK;
+    if (!k_pool || !norms || !aligned16(k_pool)) return PCF_ERR_INVALID_ARG;
+    if ((s = check_device()) != PCF_OK) return s;
+    const int64_t blocks = ((int64_t)H[L_TOTAL_TOKENS] * 32 + 255) / 256;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const auto* kp = reinterpret_cast<const __nv_bfloat16*>(k_pool);
+    return H[L_D] == 128 ? launch(key_norm_kernel<128>, dim3((unsigned)blocks), dim3(256), 0, st, layout->dev, kp, norms)
+                         : launch(key_norm_kernel<64>, dim3((unsigned)blocks), dim3(256), 0, st, layout->dev, kp, norms);
+}
+
 extern "C" pcf_status pcf_gather_rows(const pcf_layout* layout, const int32_t* sel_idx, const uint16_t* src,
                                       int32_t row_elems, uint16_t* dst, void* stream) {
     pcf_status s = check_layout(layout);

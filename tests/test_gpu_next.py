@@ -1,0 +1,140 @@
+"""GPU parity of the two selection variants beyond the per-span hot path: the pages' global Top-N
+(one budget per request over all its cached tokens, QCFuse 2B) and anchor extraction (each span's
+tokens with the largest key norm, QCFuse 2A).  Selections are bit-exact when fed the oracle's fp32
+values; key norms are within 1e-5 relative of the fp64 oracle."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import position_independent_kv_critical_gb300 as pcf
+from oracle import method
+from workload import CONFIGS, PAGE, make_batch, make_layout, small_custom_batch
+
+from gpu_util import GpuBatch, assert_close_out
+
+pytestmark = pytest.mark.gpu
+
+NORM_RTOL = 1e-5
+
+
+def _layout(cfg, reqs):
+    n_phys = cfg.pool_spans * cfg.span_len // PAGE
+    return pcf.Layout(reqs, cfg.hq, cfg.hkv, cfg.d, n_phys, max(r.query_pos0 + r.n_query for r in reqs) + 1)
+
+
+def _run_global(L, imp):
+    sel = torch.empty(max(1, L.total_sel), dtype=torch.int32, device="cuda")
+    ex = torch.empty(max(1, L.total_pages), dtype=torch.int16, device="cuda")
+    rp = torch.empty(max(1, L.total_rows), dtype=torch.int32, device="cuda")
+    pcf.select_topn_global(L, torch.as_tensor(imp).cuda(), sel, ex, rp)
+    pcf.check_device_error()
+    return (sel[: L.total_sel].cpu().numpy(), ex[: L.total_pages].cpu().numpy().view(np.uint16),
+            rp[: L.total_rows].cpu().numpy())
+
+
+# ------------------------------------------------------------------ global Top-N
+
+@pytest.mark.parametrize("name", list(CONFIGS))
+def test_topn_global_bit_exact_planted_ties_full_size(name):
+    cfg = CONFIGS[name]
+    reqs = make_layout(cfg)
+    L = _layout(cfg, reqs)
+    rng = np.random.default_rng(cfg.seed + 7)
+    imp = (rng.integers(0, 24, size=L.total_tokens) * 0.03125).astype(np.float32)
+    sel, ex, rp = _run_global(L, imp)
+    tb = sb = pb = rb = 0
+    for r in reqs:
+        exp = method.select_topn_global_request(imp[tb: tb + r.n_cached], r.n_sel)
+        assert np.array_equal(sel[sb: sb + r.n_sel], exp)
+        npg = r.n_cached // PAGE
+        assert np.array_equal(ex[pb: pb + npg], method.exclusion_masks(exp, npg))
+        kpos = np.concatenate([s.pos0 + np.arange(s.n_pages * PAGE) for s in r.spans])
+        assert np.array_equal(rp[rb: rb + r.n_rows], method.row_positions(exp, kpos, r.n_query, r.query_pos0))
+        tb += r.n_cached
+        sb += r.n_sel
+        pb += npg
+        rb += r.n_rows
+
+
+@pytest.mark.parametrize("ks", [(0, 0), (32, 48), (5, 0), (0, 7)])
+def test_topn_global_budget_extremes(ks):
+    """Budgets of nothing, of every token, and all of it drawn from one span."""
+    b = small_custom_batch([(0, 2, 0, ks[0]), (4, 3, 64, ks[1])], n_query=5, n_phys_pages=8)
+    L = pcf.Layout(b.requests, b.hq, b.hkv, b.d, b.n_phys_pages, b.max_pos + 1)
+    rng = np.random.default_rng(sum(ks))
+    imp = rng.random(L.total_tokens).astype(np.float32)
+    sel, _, _ = _run_global(L, imp)
+    assert np.array_equal(sel, method.select_topn_global_request(imp, b.requests[0].n_sel))
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama8b_layer"])
+def test_topn_global_selection_drives_the_fused_attention(name):
+    """Global selection on the oracle's fp32 scores, then the fused attention over it, against the
+    oracle's attention with the oracle's global selection."""
+    gb = GpuBatch(make_batch(name))
+    r = gb.b.requests[0]
+    imp32 = gb.oracle_score(0).astype(np.float32)
+    pad = np.zeros(gb.L.total_tokens, dtype=np.float32)
+    pad[: r.n_cached] = imp32
+    pcf.select_topn_global(gb.L, torch.as_tensor(pad).cuda(), gb.cf.sel_idx, gb.cf.excl, gb.cf.row_pos)
+    pcf.check_device_error()
+    sel_gpu = gb.cf.sel_idx[: r.n_sel].cpu().numpy()
+    sel = method.select_topn_global_request(imp32, r.n_sel)
+    assert np.array_equal(sel_gpu, sel)
+    out = gb.attention()
+    exp, _ = gb.oracle_attention(0, sel)
+    assert_close_out(out[: r.n_rows], exp, f"{name} global Top-N attention")
+
+
+# ------------------------------------------------------------------ anchors
+
+def _norms_gpu(gb):
+    norms = torch.empty(gb.L.total_tokens, dtype=torch.float32, device="cuda")
+    pcf.key_norms(gb.L, gb.k_pool, norms)
+    pcf.check_device_error()
+    return norms
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama8b_layer", "concurrent_reuse"])
+def test_key_norms_match_oracle(name):
+    gb = GpuBatch(make_batch(name))
+    got = _norms_gpu(gb).cpu().numpy()
+    ids = range(len(gb.b.requests)) if name != "concurrent_reuse" else (0, 17, 31)
+    for i in ids:
+        r, K, _, _ = gb.oracle_request(i)
+        tb = gb.tok_base[i]
+        np.testing.assert_allclose(got[tb: tb + r.n_cached], method.key_norms(K), rtol=NORM_RTOL)
+
+
+@pytest.mark.parametrize("name,m_pct", [("tiny", 5), ("llama8b_layer", 3), ("concurrent_reuse", 2)])
+def test_anchors_bit_exact_on_oracle_norms_and_close_on_gpu_norms(name, m_pct):
+    """Anchors = per-span Top-m on the key norms: a layout whose span k's are the anchor counts,
+    run through pcf_select_topk; bit-exact on the oracle's fp32 norms, and (almost always) the same
+    tokens from the GPU's own norms."""
+    b = make_batch(name)
+    reqs = [dataclasses.replace(r, spans=[dataclasses.replace(s, k=method.k_from_percent(m_pct, s.n_pages * PAGE))
+                                          for s in r.spans]) for r in b.requests]
+    gb = GpuBatch(dataclasses.replace(b, requests=reqs))
+    oracle_norms = np.zeros(gb.L.total_tokens, dtype=np.float32)
+    for i in range(len(reqs)):
+        _, K, _, _ = gb.oracle_request(i)
+        oracle_norms[gb.tok_base[i]: gb.tok_base[i] + K.shape[0]] = method.key_norms(K)
+    sel, _, _ = gb.topk(oracle_norms)
+    gpu_norms = _norms_gpu(gb)
+    pcf.select_topk(gb.L, gpu_norms, gb.cf.sel_idx, gb.cf.excl, gb.cf.row_pos)
+    pcf.check_device_error()
+    sel_g = gb.cf.sel_idx[: gb.L.total_sel].cpu().numpy()
+    same = total = 0
+    for i, r in enumerate(reqs):
+        lens = [s.n_pages * PAGE for s in r.spans]
+        exp = method.select_anchors_request(oracle_norms[gb.tok_base[i]: gb.tok_base[i] + r.n_cached], lens,
+                                            [s.k for s in r.spans])
+        sb = gb.sel_base[i]
+        assert np.array_equal(sel[sb: sb + r.n_sel], exp)
+        same += len(np.intersect1d(sel_g[sb: sb + r.n_sel], exp))
+        total += len(exp)
+    assert same >= 0.99 * total, (same, total)
