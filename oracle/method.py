@@ -18,7 +18,8 @@ Steps, in the order the pages give them:
    MiniPIC 2.1 score equation).
 
 Offline, before any request (QCFuse 2A, second summary Phase 1): each span's anchor tokens, the
-few with the highest key norm.
+few with the highest key norm; at request time (Phase 2) the query attends over the request's
+anchors put in front of it as a prefix.
 
 Readings where the pages are silent (also listed in the design doc): rotate-half RoPE pairing; softmax
 over the request's cached keys only for scoring; a plain sum over heads and query tokens; query
@@ -141,6 +142,25 @@ def select_anchors_request(norms: np.ndarray, span_lens: Sequence[int], span_m: 
     (a small share of the span's tokens), ties to the lower index, ascending; the same per-span
     selection as the recompute Top-N, on the key norms instead of the importance."""
     return select_topk_request(norms, span_lens, span_m)
+
+
+def anchor_count(pct: int, length: int) -> int:
+    """Anchors of a span of ``length`` tokens at ``pct`` percent, rounded up to whole pages of 16:
+    16 * ceil(pct * length / 1600).  The pages give only "a small share"; whole pages let the
+    anchors be packed into pages of their own and read like any cached span."""
+    return PAGE * (-((-int(pct) * int(length)) // (100 * PAGE)))
+
+
+def anchor_probe_request(q: np.ndarray, k: np.ndarray, v: np.ndarray, K_anchor: np.ndarray,
+                         V_anchor: np.ndarray, theta: float) -> np.ndarray:
+    """QCFuse, section 2A (injection) and Phase 2: the anchors are put in front of the query as a
+    prefix, at positions 0 .. A-1 in span order, the query tokens follow at A .. A+T-1, and each
+    query token attends over the anchors and, causally, over the query tokens; fp64 [T][Hq][d].
+    ``q`` [T][Hq][d], ``k``/``v`` [T][Hkv][d] the query tokens' own projections, ``K_anchor``/
+    ``V_anchor`` [A][Hkv][d] the anchors' cached (unrotated) keys and values."""
+    A, T = K_anchor.shape[0], q.shape[0]
+    return fused_attention_request(q, k, v, A + np.arange(T, dtype=np.int64), K_anchor, V_anchor,
+                                   np.arange(A, dtype=np.int64), np.zeros((0,), dtype=np.int64), theta)
 
 
 def row_positions(sel: np.ndarray, k_pos: np.ndarray, n_query: int, query_pos0: int) -> np.ndarray:

@@ -266,6 +266,36 @@ def test_anchors_worked_example():
     assert list(method.select_anchors_request(norms, [4, 4], [2, 1])) == [1, 3, 6]
 
 
+def test_anchor_count_whole_pages():
+    assert [method.anchor_count(p, 512) for p in (0, 1, 3, 6, 7, 100)] == [0, 16, 16, 32, 48, 512]
+    assert method.anchor_count(5, 1024) == 64
+
+
+def test_anchor_probe_equals_causal_prefill_over_the_prefixed_sequence():
+    """The probe's query rows are the last T rows of a plain causal prefill over [anchors; query]
+    at positions 0 .. A+T-1 (the anchors' own query rows do not matter)."""
+    rng = np.random.default_rng(21)
+    A, T, hq, hkv, d = 32, 6, 4, 2, 16
+    Ka, Va = rng.standard_normal((A, hkv, d)), rng.standard_normal((A, hkv, d))
+    q, k, v = rng.standard_normal((T, hq, d)), rng.standard_normal((T, hkv, d)), rng.standard_normal((T, hkv, d))
+    got = method.anchor_probe_request(q, k, v, Ka, Va, 1e4)
+    q_all = np.concatenate([rng.standard_normal((A, hq, d)), q])
+    full = method.full_prefill(q_all, np.concatenate([Ka, k]), np.concatenate([Va, v]),
+                               np.arange(A + T), 1e4)
+    np.testing.assert_allclose(got, full[A:], atol=1e-12)
+
+
+def test_anchor_probe_without_anchors_is_the_query_alone():
+    rng = np.random.default_rng(22)
+    T, hq, hkv, d = 5, 2, 1, 8
+    q, k, v = rng.standard_normal((T, hq, d)), rng.standard_normal((T, hkv, d)), rng.standard_normal((T, hkv, d))
+    z = np.zeros((0, hkv, d))
+    got = method.anchor_probe_request(q, k, v, z, z, 1e4)
+    # the first query token sees only itself: its output is its own value row
+    np.testing.assert_allclose(got[0], np.repeat(v[0], hq // hkv, axis=0), atol=1e-12)
+    np.testing.assert_allclose(got, method.full_prefill(q, k, v, np.arange(T), 1e4), atol=1e-12)
+
+
 def test_k_from_percent_golden_table():
     with open(os.path.join(GOLDEN, "recompute_counts.txt")) as fh:
         rows = [ln.split("#")[0].split() for ln in fh if ln.split("#")[0].strip()]
