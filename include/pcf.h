@@ -166,6 +166,16 @@ pcf_status pcf_select_topn_global(const pcf_layout* layout, const float* importa
  * counts, fed these norms as the importance.  k_pool as for pcf_score (16-byte aligned). */
 pcf_status pcf_key_norms(const pcf_layout* layout, const uint16_t* k_pool, float* norms, void* stream);
 
+/* Anchor pages (QCFuse 2A injection / Phase 2): `layout` is an anchor-selection layout (span k's =
+ * anchor counts, every one a multiple of 16, else PCF_ERR_INVALID_ARG) and sel_idx its selection
+ * (pcf_select_topk on pcf_key_norms).  Copies anchor i of the batch (selection order) to page
+ * i / 16, row i % 16 of k_anchor / v_anchor, [total_sel / 16][Hkv][16][d] bf16, every kv head.
+ * The query then attends over them as a prefix with pcf_fused_attention on a second layout whose
+ * request b has one span (phys_first_page = sel_base_b / 16, n_pages = anchors_b / 16, pos0 = 0,
+ * k = 0) and its query at query_pos0 = anchors_b, pools k_anchor / v_anchor. */
+pcf_status pcf_pack_anchor_pages(const pcf_layout* layout, const int32_t* sel_idx, const uint16_t* k_pool,
+                                 const uint16_t* v_pool, uint16_t* k_anchor, uint16_t* v_anchor, void* stream);
+
 /* Row gather of the recompute batch: dst[sel_base_b + i][:] = src[tok_base_b + sel_idx[...]][:]
  * for every selected row; src [total_tokens][row_elems], dst [total_sel][row_elems], bf16;
  * row_elems a positive multiple of 8. */

@@ -22,7 +22,8 @@ from . import _lib
 from ._lib import PcfError  # noqa: F401
 
 __all__ = ["Layout", "CacheFusion", "PcfError", "k_from_percent", "rope_table", "score", "select_topk",
-           "gather_rows", "fused_attention", "check_device_error", "load_library", "score_noalloc"]
+           "gather_rows", "fused_attention", "check_device_error", "load_library", "score_noalloc",
+           "select_topn_global", "key_norms", "pack_anchor_pages"]
 
 
 def load_library():
@@ -174,6 +175,16 @@ def key_norms(layout: Layout, k_pool, norms, stream=None):
     _need(norms, torch.float32, "norms")
     _lib.check("pcf_key_norms", _lib.load().pcf_key_norms(
         ctypes.byref(layout.ref), _p(k_pool), _p(norms), _stream(stream)))
+
+
+def pack_anchor_pages(layout: Layout, sel_idx, k_pool, v_pool, k_anchor, v_anchor, stream=None):
+    """Copy the selected anchors' K/V rows into pages of their own (anchor i -> page i/16, row i%16)."""
+    for t, n in ((k_pool, "k_pool"), (v_pool, "v_pool"), (k_anchor, "k_anchor"), (v_anchor, "v_anchor")):
+        _need(t, torch.bfloat16, n)
+    _need(sel_idx, torch.int32, "sel_idx")
+    _lib.check("pcf_pack_anchor_pages", _lib.load().pcf_pack_anchor_pages(
+        ctypes.byref(layout.ref), _p(sel_idx), _p(k_pool), _p(v_pool), _p(k_anchor), _p(v_anchor),
+        _stream(stream)))
 
 
 def gather_rows(layout: Layout, sel_idx, src, dst, stream=None):

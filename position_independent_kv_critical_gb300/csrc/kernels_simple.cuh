@@ -470,6 +470,49 @@ __global__ void __launch_bounds__(256) key_norm_kernel(const int32_t* __restrict
     }
 }
 
+// ------------------------------------------------------------------ anchor pages
+// QCFuse section 2A (injection): a request's anchors, selected per span in whole pages, are
+// copied out of the shared pool into pages of their own, anchor i of the batch (in selection
+// order) at page i / 16, row i % 16, every kv head, K and V alike; the fused attention then reads
+// those pages as the prefix of the query.  One block per anchor page (its 16 anchors belong to
+// one request because every request's anchor count is a multiple of 16): 16-byte chunks in
+// destination order, so the stores are contiguous.
+template <int D>
+__global__ void __launch_bounds__(256) pack_anchor_kernel(const int32_t* __restrict__ L,
+                                                          const int32_t* __restrict__ sel_idx,
+                                                          const uint4* __restrict__ k_pool,
+                                                          const uint4* __restrict__ v_pool,
+                                                          uint4* __restrict__ k_anchor,
+                                                          uint4* __restrict__ v_anchor) {
+    constexpr int CPR = D / 8;   // 16-byte chunks per row
+    const int32_t page = blockIdx.x;
+    const int32_t first = page * kPage;   // first anchor of the page
+    const int n_reqs = L[L_N_REQS], hkv = L[L_HKV], n_phys = L[L_N_PHYS];
+    const int32_t* REQ = L + L[L_OFF_REQ];
+    int lo = 0, hi = n_reqs - 1;   // last request with sel_base <= first
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (REQ[mid * R_STRIDE + R_SEL_BASE] <= first) lo = mid; else hi = mid - 1;
+    }
+    const int32_t* R = REQ + lo * R_STRIDE;
+    const int32_t n_tok = R[R_N_PAGES] * kPage, tok_base = R[R_TOK_BASE];
+    const int32_t* blk = L + L[L_OFF_BLOCK];
+    grid_dep_wait();   // the anchors' indices come from the selection kernel
+    grid_dep_launch();
+    for (int q = threadIdx.x; q < hkv * kPage * CPR; q += blockDim.x) {
+        const int h = q / (kPage * CPR), slot = (q / CPR) % kPage, c = q % CPR;
+        const int32_t j = sel_idx[first + slot];
+        if (j < 0 || j >= n_tok) { set_dev_error(kDevErrBounds); continue; }
+        const int32_t t = tok_base + j;
+        const int32_t ph = blk[t / kPage];
+        if (ph < 0 || ph >= n_phys) { set_dev_error(kDevErrBounds); continue; }
+        const int64_t src = (((int64_t)ph * hkv + h) * kPage + t % kPage) * CPR + c;
+        const int64_t dst = (((int64_t)page * hkv + h) * kPage + slot) * CPR + c;
+        k_anchor[dst] = k_pool[src];
+        v_anchor[dst] = v_pool[src];
+    }
+}
+
 // ------------------------------------------------------------------ row gather
 // dst[sel_base_b + i] = src[tok_base_b + sel_idx[sel_base_b + i]] -- the inputs of the tokens
 // chosen for recomputation (QCFuse Phase 4: discrete recomputation of the Top-N indices).

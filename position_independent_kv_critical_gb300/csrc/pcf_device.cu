@@ -458,6 +458,30 @@ extern "C" pcf_status pcf_key_norms(const pcf_layout* layout, const uint16_t* k_
                          : launch(key_norm_kernel<64>, dim3((unsigned)blocks), dim3(256), 0, st, layout->dev, kp, norms);
 }
 
+extern "C" pcf_status pcf_pack_anchor_pages(const pcf_layout* layout, const int32_t* sel_idx, const uint16_t* k_pool,
+                                            const uint16_t* v_pool, uint16_t* k_anchor, uint16_t* v_anchor,
+                                            void* stream) {
+    pcf_status s = check_layout(layout);
+    if (s != PCF_OK) return s;
+    const int32_t* H = layout->host;
+    // every request's anchors must fill whole pages
+    for (int b = 0; b < H[L_N_REQS]; ++b)
+        if (H[H[L_OFF_REQ] + b * R_STRIDE + R_N_SEL] % kPage != 0) return PCF_ERR_INVALID_ARG;
+    if (H[L_TOTAL_SEL] == 0) return PCF_OK;
+    if (!sel_idx || !k_pool || !v_pool || !k_anchor || !v_anchor) return PCF_ERR_INVALID_ARG;
+    for (const void* p : {(const void*)k_pool, (const void*)v_pool, (const void*)k_anchor, (const void*)v_anchor})
+        if (!aligned16(p)) return PCF_ERR_INVALID_ARG;
+    if ((s = check_device()) != PCF_OK) return s;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const dim3 grid(H[L_TOTAL_SEL] / kPage);
+    const auto* kp = reinterpret_cast<const uint4*>(k_pool);
+    const auto* vp = reinterpret_cast<const uint4*>(v_pool);
+    auto* ka = reinterpret_cast<uint4*>(k_anchor);
+    auto* va = reinterpret_cast<uint4*>(v_anchor);
+    return H[L_D] == 128 ? launch(pack_anchor_kernel<128>, grid, dim3(256), 0, st, layout->dev, sel_idx, kp, vp, ka, va)
+                         : launch(pack_anchor_kernel<64>, grid, dim3(256), 0, st, layout->dev, sel_idx, kp, vp, ka, va);
+}
+
 extern "C" pcf_status pcf_gather_rows(const pcf_layout* layout, const int32_t* sel_idx, const uint16_t* src,
                                       int32_t row_elems, uint16_t* dst, void* stream) {
     pcf_status s = check_layout(layout);

@@ -138,3 +138,67 @@ def test_anchors_bit_exact_on_oracle_norms_and_close_on_gpu_norms(name, m_pct):
         same += len(np.intersect1d(sel_g[sb: sb + r.n_sel], exp))
         total += len(exp)
     assert same >= 0.99 * total, (same, total)
+
+
+# ------------------------------------------------------------------ anchor-prefixed query probing
+
+def _anchor_batch(name, pct):
+    b = make_batch(name)
+    reqs = [dataclasses.replace(r, spans=[dataclasses.replace(s, k=method.anchor_count(pct, s.n_pages * PAGE))
+                                          for s in r.spans]) for r in b.requests]
+    return dataclasses.replace(b, requests=reqs)
+
+
+@pytest.mark.parametrize("name,pct,req_ids", [("tiny", 12, (0,)), ("llama8b_layer", 6, (0,)),
+                                              ("concurrent_reuse", 3, (0, 13, 31))])
+def test_anchor_probe_matches_oracle(name, pct, req_ids):
+    """Anchors from the oracle's fp32 key norms (per span, whole pages), packed into pages of their
+    own (bit-exact), then the query tokens attend over them as a prefix through the fused
+    attention on a second layout; against the oracle's probe."""
+    ab = _anchor_batch(name, pct)
+    gb = GpuBatch(ab)
+    reqs = ab.requests
+    norms = np.zeros(gb.L.total_tokens, dtype=np.float32)
+    for i in range(len(reqs)):
+        _, K, _, _ = gb.oracle_request(i)
+        norms[gb.tok_base[i]: gb.tok_base[i] + K.shape[0]] = method.key_norms(K)
+    gb.topk(norms)
+    A_tot = gb.L.total_sel
+    ka = torch.empty((A_tot // PAGE, ab.hkv, PAGE, ab.d), dtype=torch.bfloat16, device="cuda")
+    va = torch.empty_like(ka)
+    pcf.pack_anchor_pages(gb.L, gb.cf.sel_idx, gb.k_pool, gb.v_pool, ka, va)
+    pcf.check_device_error()
+    sel = gb.cf.sel_idx[:A_tot].cpu().numpy()
+    ka_rows = ka.permute(0, 2, 1, 3).reshape(A_tot, ab.hkv, ab.d).double().cpu().numpy()
+    va_rows = va.permute(0, 2, 1, 3).reshape(A_tot, ab.hkv, ab.d).double().cpu().numpy()
+    # the probe: one span of anchor pages per request, the query right after it
+    probe = [dataclasses.replace(r, spans=[dataclasses.replace(r.spans[0], phys_first_page=gb.sel_base[i] // PAGE,
+                                                               n_pages=r.n_sel // PAGE, pos0=0, k=0)],
+                                 query_pos0=r.n_sel) for i, r in enumerate(reqs)]
+    T = [r.n_query for r in reqs]
+    g = torch.Generator().manual_seed(ab.seed + 99)
+    mk = lambda h: torch.randn((sum(T), h, ab.d), generator=g).to(torch.bfloat16)
+    q, k, v = mk(ab.hq), mk(ab.hkv), mk(ab.hkv)
+    PL = pcf.Layout(probe, ab.hq, ab.hkv, ab.d, A_tot // PAGE, max(r.n_sel + r.n_query for r in reqs) + 1)
+    rope = pcf.rope_table(ab.d, ab.theta, max(r.n_sel + r.n_query for r in reqs) + 1).cuda()
+    pcf_cf = pcf.CacheFusion(PL, rope, row_elems=0)
+    pcf.select_topk(PL, torch.zeros(max(1, PL.total_tokens), dtype=torch.float32, device="cuda"),
+                    pcf_cf.sel_idx, pcf_cf.excl, pcf_cf.row_pos)
+    pcf.fused_attention(PL, q.cuda(), k.cuda(), v.cuda(), ka, va, pcf_cf.excl, pcf_cf.row_pos, rope,
+                        pcf_cf.out, pcf_cf.ws_attn)
+    pcf.check_device_error()
+    out = pcf_cf.out[: PL.total_rows].float().cpu().numpy()
+    qb = np.concatenate([[0], np.cumsum(T)])
+    for i in req_ids:
+        r = reqs[i]
+        sb = gb.sel_base[i]
+        _, K, V, _ = gb.oracle_request(i)
+        exp_sel = method.select_anchors_request(norms[gb.tok_base[i]: gb.tok_base[i] + r.n_cached],
+                                                [s.n_pages * PAGE for s in r.spans], [s.k for s in r.spans])
+        assert np.array_equal(sel[sb: sb + r.n_sel], exp_sel)
+        assert np.array_equal(ka_rows[sb: sb + r.n_sel], K[exp_sel])
+        assert np.array_equal(va_rows[sb: sb + r.n_sel], V[exp_sel])
+        sl = slice(qb[i], qb[i + 1])
+        exp = method.anchor_probe_request(q[sl].double().numpy(), k[sl].double().numpy(), v[sl].double().numpy(),
+                                          K[exp_sel], V[exp_sel], ab.theta)
+        assert_close_out(out[sl], exp, f"{name} anchor probe request {i}")
