@@ -206,6 +206,66 @@ def run_reference(args):
     }))
 
 
+def _anchor_probe_setup(args, pcf, b, k_pool, dev):
+    """Offline: key norms, per-span anchors (whole pages) and their packed pages; online (the timed
+    call): the query tokens attend over their request's anchors as a prefix (positions 0..A-1, the
+    query at A..A+T-1).  Returns the timed call, its algorithmic flops and a timer of the offline
+    pass."""
+    import dataclasses
+    v_pool = b.v_pool.to(dev)
+    count = lambda n: PAGE * (-((-args.anchor_pct * n) // (100 * PAGE)))   # whole pages per span
+    reqs = [dataclasses.replace(r, spans=[dataclasses.replace(s, k=count(s.n_pages * PAGE)) for s in r.spans])
+            for r in b.requests]
+    AL = pcf.Layout(reqs, b.hq, b.hkv, b.d, b.n_phys_pages, b.max_pos + 1, device=str(dev))
+    n_anchor = AL.total_sel
+    norms = torch.empty(max(1, AL.total_tokens), dtype=torch.float32, device=dev)
+    sel = torch.empty(max(1, n_anchor), dtype=torch.int32, device=dev)
+    ex = torch.empty(max(1, AL.total_pages), dtype=torch.int16, device=dev)
+    rp = torch.empty(max(1, AL.total_rows), dtype=torch.int32, device=dev)
+    ka = torch.empty((max(1, n_anchor // PAGE), b.hkv, PAGE, b.d), dtype=torch.bfloat16, device=dev)
+    va = torch.empty_like(ka)
+
+    def offline_pass():
+        pcf.key_norms(AL, k_pool, norms)
+        pcf.select_topk(AL, norms, sel, ex, rp)
+        pcf.pack_anchor_pages(AL, sel, k_pool, v_pool, ka, va)
+
+    offline_pass()
+    sel_base = np.concatenate([[0], np.cumsum([r.n_sel for r in reqs])])
+    probe = [dataclasses.replace(r, spans=[dataclasses.replace(r.spans[0], phys_first_page=int(sel_base[i]) // PAGE,
+                                                               n_pages=r.n_sel // PAGE, pos0=0, k=0)],
+                                 query_pos0=r.n_sel) for i, r in enumerate(reqs)]
+    mp = max(r.n_sel + r.n_query for r in reqs) + 1
+    PL = pcf.Layout(probe, b.hq, b.hkv, b.d, max(1, n_anchor // PAGE), mp, device=str(dev))
+    rope = pcf.rope_table(b.d, b.theta, mp).to(dev)
+    pcf_cf = pcf.CacheFusion(PL, rope, row_elems=0, device=str(dev))
+    pcf.select_topk(PL, torch.zeros(max(1, PL.total_tokens), dtype=torch.float32, device=dev),
+                    pcf_cf.sel_idx, pcf_cf.excl, pcf_cf.row_pos)
+    g = torch.Generator().manual_seed(b.seed + 99)
+    T = sum(r.n_query for r in reqs)
+    q = b.q_query.to(dev)
+    k = torch.randn((T, b.hkv, b.d), generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn((T, b.hkv, b.d), generator=g).to(torch.bfloat16).to(dev)
+    # every query token sees its request's anchors and the query tokens up to itself
+    flops = float(sum(4 * b.d * b.hq * (r.n_query * r.n_sel + r.n_query * (r.n_query + 1) // 2) for r in reqs))
+
+    def call():
+        pcf.fused_attention(PL, q, k, v, ka, va, pcf_cf.excl, pcf_cf.row_pos, rope, pcf_cf.out, pcf_cf.ws_attn)
+
+    def time_offline():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        offline_pass()
+        e1.record()
+        torch.cuda.synchronize()
+        return 1e3 * e0.elapsed_time(e1)
+
+    hw = PL.host.numpy()   # compaction scan (cached pages), rotation, attention, split merge (layout word 33)
+    launches = (1 if PL.total_pages else 0) + 2 + (1 if hw[33] > 0 else 0)
+    return call, flops, time_offline, launches
+
+
 def run_op(args, pcf, b, L, cf, k_pool, dev, world, rank, local):
     """Time one selection variant alone: anchor key norms (HBM-bound: reads every cached key once)
     or the global Top-N (one block per request, launch- and latency-bound)."""
@@ -222,10 +282,14 @@ def run_op(args, pcf, b, L, cf, k_pool, dev, world, rank, local):
                        device=str(dev))
     norms = torch.empty(max(1, L.total_tokens), dtype=torch.float32, device=dev)
     pcf.key_norms(L, k_pool, norms)
+    offline = None
+    per_call = 1
     if args.op == "key_norms":
         call = lambda: pcf.key_norms(L, k_pool, norms)
-    else:
+    elif args.op == "topn_global":
         call = lambda: pcf.select_topn_global(L, norms, cf.sel_idx, cf.excl, cf.row_pos)
+    else:
+        call, probe_flops, offline, per_call = _anchor_probe_setup(args, pcf, b, k_pool, dev)
     for _ in range(max(3, args.warmup)):
         call()
     pcf.check_device_error()
@@ -249,8 +313,14 @@ def run_op(args, pcf, b, L, cf, k_pool, dev, world, rank, local):
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
-    _, _, hbm, src = _peaks()
-    if args.op == "key_norms":
+    peak, _, hbm, src = _peaks()
+    if args.op == "anchor_probe":
+        tf = world * probe_flops / (ms / 1e3) / 1e12
+        metric, value, unit, hib = "anchor-prefixed query probe (fused attention) time per call", ms * 1e3, "us", False
+        roof = {"bound": "tensor", "achieved": tf / world, "peak": peak, "unit": "TFLOP/s", "frac": tf / world / peak,
+                "peak_source": src + " bf16 burst", "traffic": None, "algorithmic_flops_per_launch": probe_flops,
+                "offline_anchor_pass_us": offline()}
+    elif args.op == "key_norms":
         nbytes = L.total_tokens * (b.hkv * b.d * 2 + 4)     # every cached key read once, one fp32 out
         gbs = world * nbytes / (ms / 1e3) / 1e9
         metric, value, unit, hib = "anchor key norms over the span pool: key bytes read per second", gbs, "GB/s", True
@@ -266,10 +336,11 @@ def run_op(args, pcf, b, L, cf, k_pool, dev, world, rank, local):
         print(json.dumps({
             "op": args.op, "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": hib, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32" if args.op == "key_norms" else "u32", "data": "synthetic",
+            "vs_baseline": None, "dtype": {"key_norms": "f32", "topn_global": "u32"}.get(args.op, "bf16"),
+            "data": "synthetic",
             "config": {"workload": f"{args.config}: {DESCR[args.config]}", "tokens": L.total_tokens,
                        "l2": "flushed between timed calls (512 MB write)"},
-            "roofline": roof, "gpu_launches": K, "clocks": clk,
+            "roofline": roof, "gpu_launches": K * per_call, "clocks": clk,
         }))
 
 
@@ -282,9 +353,11 @@ def main():
     ap.add_argument("--pct", type=int, default=None)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "key_norms", "topn_global"],
-                    help="step: the hot path (default); key_norms / topn_global: one of the two "
-                         "selection variants alone, on the workload's layout")
+    ap.add_argument("--op", default="step", choices=["step", "key_norms", "topn_global", "anchor_probe"],
+                    help="step: the hot path (default); key_norms / topn_global / anchor_probe: one "
+                         "of the variants alone, on the workload's layout")
+    ap.add_argument("--anchor-pct", type=int, default=6,
+                    help="anchor_probe: anchors per span, percent of its tokens in whole pages")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -8,8 +8,6 @@
 #include <cstring>
 #include <map>
 #include <mutex>
-#include <set>
-#include <tuple>
 #include <utility>
 
 #include "../../include/pcf.h"
@@ -202,22 +200,21 @@ AttnWs attn_ws(const int32_t* H) {
     return w;
 }
 
-// the dynamic shared-memory limit of a kernel, raised once per (kernel, device, size)
+// the dynamic shared-memory limit of a kernel, per device: only ever raised (a launch with less
+// than the limit is fine, so a kernel launched with several sizes keeps the largest)
 std::mutex g_smem_mu;
-std::set<std::tuple<const void*, int, int>> g_smem_done;
+std::map<std::pair<const void*, int>, int> g_smem_limit;
 template <typename K>
 pcf_status set_smem(K kernel, int bytes) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PCF_ERR_CUDA;
-    const auto key = std::make_tuple(reinterpret_cast<const void*>(kernel), dev, bytes);
-    {
-        std::lock_guard<std::mutex> lock(g_smem_mu);
-        if (g_smem_done.count(key)) return PCF_OK;
-    }
+    const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+    std::lock_guard<std::mutex> lock(g_smem_mu);
+    auto it = g_smem_limit.find(key);
+    if (it != g_smem_limit.end() && it->second >= bytes) return PCF_OK;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
         return PCF_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_smem_mu);
-    g_smem_done.insert(key);
+    g_smem_limit[key] = bytes;
     return PCF_OK;
 }
 
