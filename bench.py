@@ -81,6 +81,20 @@ def _dist():
     return world, rank, local
 
 
+def _max_over_ranks(ms: float, world: int, dev) -> float:
+    """The slowest rank's step time (each rank runs its own copy of the workload: weak scaling)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_throughput(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job tokens/s: every rank processed its workload within the slowest rank's time."""
+    return world * tokens_per_rank / (ms / 1e3)
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -308,11 +322,7 @@ def run_op(args, pcf, b, L, cf, k_pool, dev, world, rank, local):
     torch.cuda.synchronize()
     clk = clocks.stop()
     pcf.check_device_error()
-    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = _max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev), world, dev)
     peak, _, hbm, src = _peaks()
     if args.op == "anchor_probe":
         tf = world * probe_flops / (ms / 1e3) / 1e12
@@ -444,13 +454,9 @@ def main():
     score_ms = [e[0].elapsed_time(e[1]) for e in evb]
     topk_gather_ms = [e[1].elapsed_time(e[2]) for e in evb]
     attn_ms = [e[2].elapsed_time(e[3]) for e in evb]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = _max_over_ranks(statistics.mean(step_ms), world, dev)
     tokens = sum(r.n_cached + r.n_query for r in b.requests)
-    value = world * tokens / (ms / 1e3)
+    value = _job_throughput(tokens, world, ms)
 
     sel = cf.sel_idx[: L.total_sel].cpu().numpy()
     row_pos = cf.row_pos[: L.total_rows].cpu().numpy()

@@ -220,3 +220,20 @@ def test_device_calls_fail_loudly_without_gpu():
             ctypes.byref(L.ref), ctypes.c_void_p(imp.data_ptr()), ctypes.c_void_p(sel.data_ptr()),
             ctypes.c_void_p(ex.data_ptr()), ctypes.c_void_p(rp.data_ptr()), None))
     assert e.value.status == -7
+
+
+def test_variant_entry_points_validate_before_touching_a_device(lib):
+    """Global Top-N, key norms and anchor packing reject bad arguments on the host (no device
+    needed): null buffers, and anchor counts that do not fill whole pages."""
+    PCF_ERR_INVALID_ARG = -1
+    b = small_custom_batch([(0, 2, 0, 3), (2, 2, 32, 5)], n_query=4)
+    L = pcf.Layout(b.requests, b.hq, b.hkv, b.d, b.n_phys_pages, 4096, device="cpu")
+    ref = ctypes.byref(L.ref)
+    assert lib.pcf_select_topn_global(ref, None, None, None, None, None) == PCF_ERR_INVALID_ARG
+    assert lib.pcf_key_norms(ref, None, None, None) == PCF_ERR_INVALID_ARG
+    # 3 + 5 anchors: not a whole page
+    assert lib.pcf_pack_anchor_pages(ref, None, None, None, None, None, None) == PCF_ERR_INVALID_ARG
+    b16 = small_custom_batch([(0, 2, 0, 16), (2, 2, 32, 0)], n_query=4)
+    L16 = pcf.Layout(b16.requests, b16.hq, b16.hkv, b16.d, b16.n_phys_pages, 4096, device="cpu")
+    # whole pages, but no buffers
+    assert lib.pcf_pack_anchor_pages(ctypes.byref(L16.ref), None, None, None, None, None, None) == PCF_ERR_INVALID_ARG
