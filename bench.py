@@ -280,6 +280,89 @@ def _anchor_probe_setup(args, pcf, b, k_pool, dev):
     return call, flops, time_offline, launches
 
 
+def run_layer_prefetch(args, pcf, b, L, cf, k_pool, dev, rank, local):
+    """Layers whose pools live in pinned host memory: layer l+1's referenced pages stream in on a
+    copy stream (pcf_prefetch_pool_pages) while layer l's fused attention runs on two alternating
+    device pools.  Reports the time per layer pipelined, and the attention and the copies alone."""
+    n_layers = 4
+    g = torch.Generator().manual_seed(b.seed + 321)
+    host = [(b.k_pool, b.v_pool)] + [(torch.randn(b.k_pool.shape, generator=g).to(torch.bfloat16),
+                                      torch.randn(b.v_pool.shape, generator=g).to(torch.bfloat16))
+                                     for _ in range(n_layers - 1)]
+    host = [(k.pin_memory(), v.pin_memory()) for k, v in host]
+    buf = [(torch.empty_like(b.k_pool, device=dev), torch.empty_like(b.v_pool, device=dev)) for _ in range(2)]
+    rope = cf.rope
+    q_query, q_fresh, k_fresh, v_fresh = (t.to(dev) for t in (b.q_query, b.q_fresh, b.k_fresh, b.v_fresh))
+    pcf.prefetch_pool_pages(L, host[0][0], host[0][1], buf[0][0], buf[0][1])
+    pcf.score(L, q_query, buf[0][0], rope, cf.importance, cf.ws_score)
+    pcf.select_topk(L, cf.importance, cf.sel_idx, cf.excl, cf.row_pos)
+    main, copy = torch.cuda.current_stream(), torch.cuda.Stream(device=dev)
+    attn = lambda kv: pcf.fused_attention(L, q_fresh, k_fresh, v_fresh, kv[0], kv[1], cf.excl, cf.row_pos, rope,
+                                          cf.out, cf.ws_attn)
+
+    def pipelined():
+        ready = [torch.cuda.Event() for _ in range(n_layers)]
+        done = [torch.cuda.Event() for _ in range(n_layers)]
+        with torch.cuda.stream(copy):
+            pcf.prefetch_pool_pages(L, host[0][0], host[0][1], buf[0][0], buf[0][1], stream=copy)
+            ready[0].record(copy)
+        for l in range(n_layers):
+            main.wait_event(ready[l])
+            if l + 1 < n_layers:
+                with torch.cuda.stream(copy):
+                    if l >= 1:
+                        copy.wait_event(done[l - 1])     # the buffer layer l+1 reuses is free
+                    d = buf[(l + 1) & 1]
+                    pcf.prefetch_pool_pages(L, host[l + 1][0], host[l + 1][1], d[0], d[1], stream=copy)
+                    ready[l + 1].record(copy)
+            attn(buf[l & 1])
+            done[l].record(main)
+
+    def attention_only():
+        for l in range(n_layers):
+            attn(buf[l & 1])
+
+    def copies_only():
+        for l in range(n_layers):
+            pcf.prefetch_pool_pages(L, host[l][0], host[l][1], buf[l & 1][0], buf[l & 1][1])
+
+    def timed(fn, reps):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        for _ in range(reps):
+            fn()
+        e1.record(main)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps / n_layers
+
+    reps = max(1, min(args.steps, 20))
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms_pipe = timed(pipelined, reps)
+    clk = clocks.stop()
+    ms_attn = timed(attention_only, reps)
+    ms_copy = timed(copies_only, reps)
+    pcf.check_device_error()
+    pages = set()
+    for r in b.requests:
+        for sp in r.spans:
+            pages.update(range(sp.phys_first_page, sp.phys_first_page + sp.n_pages))
+    nbytes = 2 * len(pages) * b.hkv * PAGE * b.d * 2
+    if rank == 0:
+        print(json.dumps({
+            "op": "layer_prefetch", "metric": "fused-attention layer time with the next layer's pool prefetched",
+            "value": ms_pipe * 1e3, "unit": "us", "n_gpus": 1, "steps": reps, "warmup": 2, "ms_per_step": ms_pipe,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{args.config}: {DESCR[args.config]}", "layers": n_layers,
+                       "prefetch_bytes_per_layer": nbytes, "host_pools": "pinned"},
+            "attention_only_us_per_layer": ms_attn * 1e3, "copy_only_us_per_layer": ms_copy * 1e3,
+            "copy_gbs": nbytes / (ms_copy / 1e3) / 1e9, "clocks": clk,
+        }))
+
+
 def run_op(args, pcf, b, L, cf, k_pool, dev, world, rank, local):
     """Time one selection variant alone: anchor key norms (HBM-bound: reads every cached key once)
     or the global Top-N (one block per request, launch- and latency-bound)."""
@@ -363,7 +446,8 @@ def main():
     ap.add_argument("--pct", type=int, default=None)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "key_norms", "topn_global", "anchor_probe"],
+    ap.add_argument("--op", default="step",
+                    choices=["step", "key_norms", "topn_global", "anchor_probe", "layer_prefetch"],
                     help="step: the hot path (default); key_norms / topn_global / anchor_probe: one "
                          "of the variants alone, on the workload's layout")
     ap.add_argument("--anchor-pct", type=int, default=6,
@@ -390,6 +474,9 @@ def main():
     g = lambda t: t.to(dev)
     k_pool, v_pool = g(b.k_pool), g(b.v_pool)
     q_query, q_fresh, k_fresh, v_fresh = g(b.q_query), g(b.q_fresh), g(b.k_fresh), g(b.v_fresh)
+    if args.op == "layer_prefetch":
+        run_layer_prefetch(args, pcf, b, L, cf, k_pool, dev, rank, local)
+        return
     if args.op != "step":
         run_op(args, pcf, b, L, cf, k_pool, dev, world, rank, local)
         return

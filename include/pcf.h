@@ -176,6 +176,17 @@ pcf_status pcf_key_norms(const pcf_layout* layout, const uint16_t* k_pool, float
 pcf_status pcf_pack_anchor_pages(const pcf_layout* layout, const int32_t* sel_idx, const uint16_t* k_pool,
                                  const uint16_t* v_pool, uint16_t* k_anchor, uint16_t* v_anchor, void* stream);
 
+/* Layer-pipelined pool prefetch (QCFuse 2C / Phase 4: while layer i is reconstructed, layer i+1's
+ * cache is loaded; here from host memory, the SSD tier being out of scope).  Copies every physical
+ * page the layout's spans reference, each once (spans shared by several requests, or touching,
+ * merge into one run), from src_k / src_v to the same page offsets of dst_k / dst_v: one
+ * cudaMemcpyAsync per run and pool, queued on `stream` (host sources should be pinned for the
+ * copies to overlap kernels).  Pools as for pcf_score, [n_phys][Hkv][16][d] bf16; src_v and dst_v
+ * may both be NULL (K only, as the critical-layer scoring needs).  Pages the layout does not
+ * reference are not touched. */
+pcf_status pcf_prefetch_pool_pages(const pcf_layout* layout, const uint16_t* src_k, const uint16_t* src_v,
+                                   uint16_t* dst_k, uint16_t* dst_v, void* stream);
+
 /* Row gather of the recompute batch: dst[sel_base_b + i][:] = src[tok_base_b + sel_idx[...]][:]
  * for every selected row; src [total_tokens][row_elems], dst [total_sel][row_elems], bf16;
  * row_elems a positive multiple of 8. */

@@ -23,7 +23,7 @@ from ._lib import PcfError  # noqa: F401
 
 __all__ = ["Layout", "CacheFusion", "PcfError", "k_from_percent", "rope_table", "score", "select_topk",
            "gather_rows", "fused_attention", "check_device_error", "load_library", "score_noalloc",
-           "select_topn_global", "key_norms", "pack_anchor_pages"]
+           "select_topn_global", "key_norms", "pack_anchor_pages", "prefetch_pool_pages"]
 
 
 def load_library():
@@ -185,6 +185,17 @@ def pack_anchor_pages(layout: Layout, sel_idx, k_pool, v_pool, k_anchor, v_ancho
     _lib.check("pcf_pack_anchor_pages", _lib.load().pcf_pack_anchor_pages(
         ctypes.byref(layout.ref), _p(sel_idx), _p(k_pool), _p(v_pool), _p(k_anchor), _p(v_anchor),
         _stream(stream)))
+
+
+def prefetch_pool_pages(layout: Layout, src_k, src_v, dst_k, dst_v, stream=None):
+    """Queue copies of the pool pages the layout references (src -> dst, same page offsets)."""
+    for t, n in ((src_k, "src_k"), (dst_k, "dst_k")):
+        _need(t, torch.bfloat16, n)
+    if (src_v is None) != (dst_v is None):
+        raise ValueError("src_v and dst_v: both or neither")
+    _lib.check("pcf_prefetch_pool_pages", _lib.load().pcf_prefetch_pool_pages(
+        ctypes.byref(layout.ref), _p(src_k), _p(src_v) if src_v is not None else None, _p(dst_k),
+        _p(dst_v) if dst_v is not None else None, _stream(stream)))
 
 
 def gather_rows(layout: Layout, sel_idx, src, dst, stream=None):

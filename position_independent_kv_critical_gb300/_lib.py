@@ -30,7 +30,7 @@ EXPORTS = (
     "pcf_layout_build", "pcf_layout_query", "pcf_score_workspace_bytes", "pcf_score",
     "pcf_select_topk", "pcf_gather_rows", "pcf_attention_workspace_bytes", "pcf_fused_attention",
     "pcf_check_device_error", "pcf_score_noalloc", "pcf_copy_async", "pcf_select_topn_global",
-    "pcf_key_norms", "pcf_pack_anchor_pages",
+    "pcf_key_norms", "pcf_pack_anchor_pages", "pcf_prefetch_pool_pages",
 )
 
 
@@ -89,6 +89,8 @@ def _declare(lib):
     lib.pcf_key_norms.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p]
     lib.pcf_pack_anchor_pages.restype = c_int32
     lib.pcf_pack_anchor_pages.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    lib.pcf_prefetch_pool_pages.restype = c_int32
+    lib.pcf_prefetch_pool_pages.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     lib.pcf_gather_rows.restype = c_int32
     lib.pcf_gather_rows.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_int32, c_void_p, c_void_p]
     lib.pcf_fused_attention.restype = c_int32

@@ -9,6 +9,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "../../include/pcf.h"
 #include "kernel_attn.cuh"
@@ -524,6 +525,40 @@ extern "C" pcf_status pcf_copy_async(int32_t n, void* const* dst, const void* co
     for (int32_t i = 0; i < n; ++i)
         if (bytes[i] > 0 && cudaMemcpyAsync(dst[i], src[i], bytes[i], cudaMemcpyDefault, st) != cudaSuccess)
             return PCF_ERR_CUDA;
+    return PCF_OK;
+}
+
+extern "C" pcf_status pcf_prefetch_pool_pages(const pcf_layout* layout, const uint16_t* src_k, const uint16_t* src_v,
+                                              uint16_t* dst_k, uint16_t* dst_v, void* stream) {
+    pcf_status s = check_layout(layout);
+    if (s != PCF_OK) return s;
+    const int32_t* H = layout->host;
+    if (!src_k || !dst_k || (!src_v) != (!dst_v)) return PCF_ERR_INVALID_ARG;
+    // the physical page runs the layout's spans reference, each once; touching runs merge
+    std::vector<std::pair<int64_t, int64_t>> runs;   // [first page, end page)
+    const int32_t* SP = H + H[L_OFF_SPAN];
+    for (int i = 0; i < H[L_N_SPANS]; ++i) {
+        const int64_t a = SP[i * S_STRIDE + S_PHYS_FIRST], n = SP[i * S_STRIDE + S_N_PAGES];
+        if (a < 0 || n < 0 || a + n > H[L_N_PHYS]) return PCF_ERR_INVALID_ARG;
+        if (n > 0) runs.emplace_back(a, a + n);
+    }
+    std::sort(runs.begin(), runs.end());
+    std::vector<std::pair<int64_t, int64_t>> merged;
+    for (const auto& r : runs) {
+        if (!merged.empty() && r.first <= merged.back().second) merged.back().second = std::max(merged.back().second, r.second);
+        else merged.push_back(r);
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PCF_ERR_NO_DEVICE;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t page_elems = (int64_t)H[L_HKV] * kPage * H[L_D];   // one page, every kv head
+    for (const auto& r : merged) {
+        const int64_t off = r.first * page_elems;
+        const size_t bytes = (size_t)((r.second - r.first) * page_elems) * 2;
+        if (cudaMemcpyAsync(dst_k + off, src_k + off, bytes, cudaMemcpyDefault, st) != cudaSuccess) return PCF_ERR_CUDA;
+        if (src_v && cudaMemcpyAsync(dst_v + off, src_v + off, bytes, cudaMemcpyDefault, st) != cudaSuccess)
+            return PCF_ERR_CUDA;
+    }
     return PCF_OK;
 }
 

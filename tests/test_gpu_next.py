@@ -202,3 +202,63 @@ def test_anchor_probe_matches_oracle(name, pct, req_ids):
         exp = method.anchor_probe_request(q[sl].double().numpy(), k[sl].double().numpy(), v[sl].double().numpy(),
                                           K[exp_sel], V[exp_sel], ab.theta)
         assert_close_out(out[sl], exp, f"{name} anchor probe request {i}")
+
+
+# ------------------------------------------------------------------ layer-pipelined pool prefetch
+
+def test_prefetch_copies_exactly_the_referenced_pages():
+    """32 requests over a shared pool: every page some span references arrives (once), the others
+    keep what the device pool held."""
+    b = make_batch("concurrent_reuse")
+    L = pcf.Layout(b.requests, b.hq, b.hkv, b.d, b.n_phys_pages, b.max_pos + 1)
+    hk, hv = b.k_pool.pin_memory(), b.v_pool.pin_memory()
+    dk = torch.full_like(b.k_pool, 7.0, device="cuda")
+    dv = torch.full_like(b.v_pool, 7.0, device="cuda")
+    pcf.prefetch_pool_pages(L, hk, hv, dk, dv)
+    torch.cuda.synchronize()
+    used = np.zeros(b.n_phys_pages, dtype=bool)
+    for r in b.requests:
+        for s in r.spans:
+            used[s.phys_first_page: s.phys_first_page + s.n_pages] = True
+    assert used.any() and not used.all()
+    gk, gv = dk.cpu(), dv.cpu()
+    u = torch.as_tensor(used)
+    assert torch.equal(gk[u].view(torch.int16), b.k_pool[u].view(torch.int16))
+    assert torch.equal(gv[u].view(torch.int16), b.v_pool[u].view(torch.int16))
+    assert bool((gk[~u] == 7.0).all()) and bool((gv[~u] == 7.0).all())
+
+
+def test_two_layer_pipeline_matches_resident_pools():
+    """Layer 1's pool streams in from pinned host memory on a copy stream while layer 0's fused
+    attention runs; each layer's output equals the one computed with its pool already resident."""
+    gb = GpuBatch(make_batch("llama8b_layer"))
+    b = gb.b
+    g = torch.Generator().manual_seed(b.seed + 123)
+    host_k = [b.k_pool, torch.randn(b.k_pool.shape, generator=g).to(torch.bfloat16)]
+    host_v = [b.v_pool, torch.randn(b.v_pool.shape, generator=g).to(torch.bfloat16)]
+    host_k = [t.pin_memory() for t in host_k]
+    host_v = [t.pin_memory() for t in host_v]
+    gb.score()
+    gb.topk()
+    ref = []
+    for l in range(2):
+        gb.k_pool, gb.v_pool = host_k[l].cuda(), host_v[l].cuda()
+        ref.append(gb.attention().copy())
+    dk = [torch.empty_like(host_k[0], device="cuda") for _ in range(2)]
+    dv = [torch.empty_like(host_v[0], device="cuda") for _ in range(2)]
+    copy = torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(2)]
+    with torch.cuda.stream(copy):
+        pcf.prefetch_pool_pages(gb.L, host_k[0], host_v[0], dk[0], dv[0], stream=copy)
+        ready[0].record(copy)
+    outs = []
+    for l in range(2):
+        torch.cuda.current_stream().wait_event(ready[l])
+        if l + 1 < 2:
+            with torch.cuda.stream(copy):
+                pcf.prefetch_pool_pages(gb.L, host_k[l + 1], host_v[l + 1], dk[l + 1], dv[l + 1], stream=copy)
+                ready[l + 1].record(copy)
+        gb.k_pool, gb.v_pool = dk[l], dv[l]
+        outs.append(gb.attention().copy())
+    for l in range(2):
+        assert np.array_equal(outs[l], ref[l]), l

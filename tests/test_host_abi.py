@@ -237,3 +237,8 @@ def test_variant_entry_points_validate_before_touching_a_device(lib):
     L16 = pcf.Layout(b16.requests, b16.hq, b16.hkv, b16.d, b16.n_phys_pages, 4096, device="cpu")
     # whole pages, but no buffers
     assert lib.pcf_pack_anchor_pages(ctypes.byref(L16.ref), None, None, None, None, None, None) == PCF_ERR_INVALID_ARG
+    # prefetch: K pools required, V pools both or neither
+    k = torch.zeros(b.n_phys_pages * b.hkv * 16 * b.d, dtype=torch.bfloat16)
+    pk = ctypes.c_void_p(k.data_ptr())
+    assert lib.pcf_prefetch_pool_pages(ref, None, None, pk, None, None) == PCF_ERR_INVALID_ARG
+    assert lib.pcf_prefetch_pool_pages(ref, pk, pk, pk, None, None) == PCF_ERR_INVALID_ARG
