@@ -208,6 +208,17 @@ pcf_status pcf_fused_attention(const pcf_layout* layout, const uint16_t* q_fresh
                                const uint16_t* excl, const int32_t* row_pos, const float* rope,
                                uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
+/* pcf_fused_attention with two caller-created CUDA events (cudaEvent_t, non-NULL, else
+ * PCF_ERR_INVALID_ARG) recorded on `stream` right before and right after the attention kernel's
+ * launch, for timing that kernel alone (its cudaEventElapsedTime).  An event between two kernels
+ * ends their programmatic launch overlap, so a timed call runs slightly slower than an untimed
+ * one. */
+pcf_status pcf_fused_attention_timed(const pcf_layout* layout, const uint16_t* q_fresh, const uint16_t* k_fresh,
+                                     const uint16_t* v_fresh, const uint16_t* k_pool, const uint16_t* v_pool,
+                                     const uint16_t* excl, const int32_t* row_pos, const float* rope, uint16_t* out,
+                                     void* ws, size_t ws_bytes, void* ev_kernel_start, void* ev_kernel_stop,
+                                     void* stream);
+
 /* Largest scoring workspace pcf_score_noalloc can serve (16 MiB), i.e. the size of the scratch
  * array built into the library. */
 #define PCF_SCORE_NOALLOC_MAX_WORKSPACE ((size_t)16 << 20)

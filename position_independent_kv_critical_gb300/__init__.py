@@ -206,14 +206,25 @@ def gather_rows(layout: Layout, sel_idx, src, dst, stream=None):
 
 
 def fused_attention(layout: Layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope,
-                    out, ws, stream=None):
+                    out, ws, stream=None, kernel_events=None):
+    """``kernel_events``: optional (start, stop) torch.cuda.Event pair recorded around the attention
+    kernel alone (pcf_fused_attention_timed)."""
     for t, n in ((q_fresh, "q_fresh"), (k_fresh, "k_fresh"), (v_fresh, "v_fresh"), (k_pool, "k_pool"),
                  (v_pool, "v_pool"), (out, "out")):
         _need(t, torch.bfloat16, n)
-    _lib.check("pcf_fused_attention", _lib.load().pcf_fused_attention(
-        ctypes.byref(layout.ref), _p(q_fresh), _p(k_fresh), _p(v_fresh), _p(k_pool), _p(v_pool),
-        _p(excl), _p(row_pos), _p(rope), _p(out), _p(ws), ws.numel() * ws.element_size(),
-        _stream(stream)))
+    args = (ctypes.byref(layout.ref), _p(q_fresh), _p(k_fresh), _p(v_fresh), _p(k_pool), _p(v_pool),
+            _p(excl), _p(row_pos), _p(rope), _p(out), _p(ws), ws.numel() * ws.element_size())
+    if kernel_events is None:
+        _lib.check("pcf_fused_attention", _lib.load().pcf_fused_attention(*args, _stream(stream)))
+        return
+    st = torch.cuda.current_stream() if stream is None else stream
+    handles = []
+    for ev in kernel_events:
+        if not ev.cuda_event:        # torch creates its events on their first record
+            ev.record(st)
+        handles.append(ctypes.c_void_p(ev.cuda_event))
+    _lib.check("pcf_fused_attention_timed", _lib.load().pcf_fused_attention_timed(
+        *args, handles[0], handles[1], _stream(stream)))
 
 
 def check_device_error(stream=None):

@@ -30,7 +30,7 @@ EXPORTS = (
     "pcf_layout_build", "pcf_layout_query", "pcf_score_workspace_bytes", "pcf_score",
     "pcf_select_topk", "pcf_gather_rows", "pcf_attention_workspace_bytes", "pcf_fused_attention",
     "pcf_check_device_error", "pcf_score_noalloc", "pcf_copy_async", "pcf_select_topn_global",
-    "pcf_key_norms", "pcf_pack_anchor_pages", "pcf_prefetch_pool_pages",
+    "pcf_key_norms", "pcf_pack_anchor_pages", "pcf_prefetch_pool_pages", "pcf_fused_attention_timed",
 )
 
 
@@ -95,6 +95,8 @@ def _declare(lib):
     lib.pcf_gather_rows.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_int32, c_void_p, c_void_p]
     lib.pcf_fused_attention.restype = c_int32
     lib.pcf_fused_attention.argtypes = [P(LayoutRef)] + [c_void_p] * 10 + [c_size_t, c_void_p]
+    lib.pcf_fused_attention_timed.restype = c_int32
+    lib.pcf_fused_attention_timed.argtypes = [P(LayoutRef)] + [c_void_p] * 10 + [c_size_t] + [c_void_p] * 3
     lib.pcf_score_noalloc.restype = c_int32
     lib.pcf_score_noalloc.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     lib.pcf_check_device_error.restype = c_int32

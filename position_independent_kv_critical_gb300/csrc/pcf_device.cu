@@ -317,9 +317,13 @@ template <int D>
 pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const uint16_t* k_fresh,
                           const uint16_t* v_fresh, const uint16_t* k_pool, const uint16_t* v_pool,
                           const uint16_t* excl, const int32_t* row_pos, const float* rope, uint16_t* out, void* ws,
-                          cudaStream_t st) {
+                          cudaStream_t st, cudaEvent_t ev_start = nullptr, cudaEvent_t ev_stop = nullptr) {
     const int32_t* H = lay->host;
-    if (H[L_N_ATTN_ITEMS] == 0) return PCF_OK;
+    if (H[L_N_ATTN_ITEMS] == 0) {   // no attention kernel: the timing events mark an empty span
+        if (ev_start && cudaEventRecord(ev_start, st) != cudaSuccess) return PCF_ERR_CUDA;
+        if (ev_stop && cudaEventRecord(ev_stop, st) != cudaSuccess) return PCF_ERR_CUDA;
+        return PCF_OK;
+    }
     const AttnWs w = attn_ws(H);
     uint8_t* base = static_cast<uint8_t*>(ws);
     __half* q_rot = reinterpret_cast<__half*>(base + w.q);
@@ -369,8 +373,10 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     AttnParams p{lay->dev, kpos_c, row_pos, reinterpret_cast<__nv_bfloat16*>(out), nullptr, part_o, part_ml, sched};
     // persistent: at most one CTA per SM, items handed out in list order (largest estimate first)
     const int grid = std::min<int>(H[L_N_ATTN_ITEMS], kNumSms);
+    if (ev_start && cudaEventRecord(ev_start, st) != cudaSuccess) return PCF_ERR_CUDA;
     if ((s = launch(kern, dim3(grid), dim3(kAttnThreads), SM::kAlloc, st, tq, tkc, tvc, tkf, tvf, p)) != PCF_OK)
         return s;
+    if (ev_stop && cudaEventRecord(ev_stop, st) != cudaSuccess) return PCF_ERR_CUDA;
     if (H[L_N_COMB] > 0) {
         if ((s = launch(combine_kernel<D>, dim3(H[L_N_COMB], D / 8), dim3(256), 0, st, lay->dev,
                         (const __nv_bfloat16*)part_o, (const float2*)part_ml,
@@ -493,14 +499,20 @@ extern "C" pcf_status pcf_gather_rows(const pcf_layout* layout, const int32_t* s
                   sel_idx, reinterpret_cast<const uint4*>(src), row_elems / 8, reinterpret_cast<uint4*>(dst));
 }
 
-extern "C" pcf_status pcf_fused_attention(const pcf_layout* layout, const uint16_t* q_fresh, const uint16_t* k_fresh,
-                                          const uint16_t* v_fresh, const uint16_t* k_pool, const uint16_t* v_pool,
-                                          const uint16_t* excl, const int32_t* row_pos, const float* rope,
-                                          uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+namespace {
+pcf_status fused_attention_entry(const pcf_layout* layout, const uint16_t* q_fresh, const uint16_t* k_fresh,
+                                 const uint16_t* v_fresh, const uint16_t* k_pool, const uint16_t* v_pool,
+                                 const uint16_t* excl, const int32_t* row_pos, const float* rope, uint16_t* out,
+                                 void* ws, size_t ws_bytes, cudaEvent_t ev_start, cudaEvent_t ev_stop, void* stream) {
     pcf_status s = check_layout(layout);
     if (s != PCF_OK) return s;
     const int32_t* H = layout->host;
-    if (H[L_TOTAL_ROWS] == 0) return PCF_OK;
+    if (H[L_TOTAL_ROWS] == 0) {
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        if (ev_start && cudaEventRecord(ev_start, st) != cudaSuccess) return PCF_ERR_CUDA;
+        if (ev_stop && cudaEventRecord(ev_stop, st) != cudaSuccess) return PCF_ERR_CUDA;
+        return PCF_OK;
+    }
     if (!q_fresh || !k_fresh || !v_fresh || !row_pos || !rope || !out || !ws) return PCF_ERR_INVALID_ARG;
     if (H[L_TOTAL_TOKENS] > 0 && (!k_pool || !v_pool || !excl)) return PCF_ERR_INVALID_ARG;
     const void* al[] = {q_fresh, k_fresh, v_fresh, rope, out, ws};
@@ -510,9 +522,31 @@ extern "C" pcf_status pcf_fused_attention(const pcf_layout* layout, const uint16
     if (ws_bytes < attn_ws(H).total) return PCF_ERR_WORKSPACE_TOO_SMALL;
     if ((s = check_device()) != PCF_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return H[L_D] == 128
-               ? attention_impl<128>(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope, out, ws, st)
-               : attention_impl<64>(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope, out, ws, st);
+    return H[L_D] == 128 ? attention_impl<128>(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope,
+                                               out, ws, st, ev_start, ev_stop)
+                         : attention_impl<64>(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope,
+                                              out, ws, st, ev_start, ev_stop);
+}
+}  // namespace
+
+extern "C" pcf_status pcf_fused_attention(const pcf_layout* layout, const uint16_t* q_fresh, const uint16_t* k_fresh,
+                                          const uint16_t* v_fresh, const uint16_t* k_pool, const uint16_t* v_pool,
+                                          const uint16_t* excl, const int32_t* row_pos, const float* rope,
+                                          uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+    return fused_attention_entry(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope, out, ws,
+                                 ws_bytes, nullptr, nullptr, stream);
+}
+
+extern "C" pcf_status pcf_fused_attention_timed(const pcf_layout* layout, const uint16_t* q_fresh,
+                                                const uint16_t* k_fresh, const uint16_t* v_fresh,
+                                                const uint16_t* k_pool, const uint16_t* v_pool, const uint16_t* excl,
+                                                const int32_t* row_pos, const float* rope, uint16_t* out, void* ws,
+                                                size_t ws_bytes, void* ev_kernel_start, void* ev_kernel_stop,
+                                                void* stream) {
+    if (!ev_kernel_start || !ev_kernel_stop) return PCF_ERR_INVALID_ARG;
+    return fused_attention_entry(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope, out, ws,
+                                 ws_bytes, static_cast<cudaEvent_t>(ev_kernel_start),
+                                 static_cast<cudaEvent_t>(ev_kernel_stop), stream);
 }
 
 extern "C" pcf_status pcf_copy_async(int32_t n, void* const* dst, const void* const* src, const size_t* bytes,
