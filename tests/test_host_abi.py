@@ -242,3 +242,32 @@ def test_variant_entry_points_validate_before_touching_a_device(lib):
     pk = ctypes.c_void_p(k.data_ptr())
     assert lib.pcf_prefetch_pool_pages(ref, None, None, pk, None, None) == PCF_ERR_INVALID_ARG
     assert lib.pcf_prefetch_pool_pages(ref, pk, pk, pk, None, None) == PCF_ERR_INVALID_ARG
+
+
+def test_variant_layouts_build_with_the_expected_totals():
+    """The layouts the variants use: the whole span pool as one query-less request (anchor key
+    norms), anchor counts in whole pages (anchor packing), and the probe (one span of anchor pages
+    per request, nothing recomputed, the query right after the anchors)."""
+    from oracle import method
+    from workload import Request, Span
+    cfg = CONFIGS["concurrent_reuse"]
+    pps = cfg.span_len // PAGE
+    n_phys = cfg.pool_spans * pps
+    pool = [Request(spans=[Span(i * pps, pps, i * cfg.span_len, 0) for i in range(cfg.pool_spans)], n_query=0,
+                    query_pos0=cfg.pool_spans * cfg.span_len)]
+    L = pcf.Layout(pool, cfg.hq, cfg.hkv, cfg.d, n_phys, cfg.pool_spans * cfg.span_len + 1, device="cpu")
+    assert (L.total_tokens, L.total_sel, L.total_rows, L.total_query) == (cfg.pool_spans * cfg.span_len, 0, 0, 0)
+    reqs = make_layout(cfg)
+    anchors = [Request(spans=[Span(s.phys_first_page, s.n_pages, s.pos0, method.anchor_count(6, s.n_pages * PAGE))
+                              for s in r.spans], n_query=r.n_query, query_pos0=r.query_pos0) for r in reqs]
+    A = pcf.Layout(anchors, cfg.hq, cfg.hkv, cfg.d, n_phys, max(r.query_pos0 + r.n_query for r in reqs) + 1,
+                   device="cpu")
+    per_req = [r.n_sel for r in anchors]
+    assert all(n % PAGE == 0 for n in per_req) and A.total_sel == sum(per_req)
+    base = np.concatenate([[0], np.cumsum(per_req)])
+    probe = [Request(spans=[Span(int(base[i]) // PAGE, r.n_sel // PAGE, 0, 0)], n_query=r.n_query, query_pos0=r.n_sel)
+             for i, r in enumerate(anchors)]
+    P = pcf.Layout(probe, cfg.hq, cfg.hkv, cfg.d, A.total_sel // PAGE,
+                   max(r.n_sel + r.n_query for r in anchors) + 1, device="cpu")
+    assert P.total_tokens == A.total_sel and P.total_sel == 0
+    assert P.total_rows == sum(r.n_query for r in reqs)
