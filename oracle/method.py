@@ -21,7 +21,7 @@ Offline, before any request (QCFuse 2A, second summary Phase 1): each span's anc
 few with the highest key norm; at request time (Phase 2) the query attends over the request's
 anchors put in front of it as a prefix.
 
-Readings where the pages are silent (also listed in the design doc): rotate-half RoPE pairing; softmax
+Readings where the pages are silent: rotate-half RoPE pairing; softmax
 over the request's cached keys only for scoring; a plain sum over heads and query tokens; query
 head h reads kv head floor(h / g); a key is visible to a row iff its logical position is <= the
 row's; scale 1/sqrt(d); no temperature, cap or sink.

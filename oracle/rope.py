@@ -5,8 +5,8 @@ stores unrotated keys k~_j and the score of query t against cached key j is
 (R_t q_t)^T (R_pi(j) k~_j) / sqrt(d), with R the rotation matrix and pi(j) the key's logical
 position in the current request.
 
-The pages do not fix the pairing of dimensions or the frequencies.  Reading used here (also in
-DESIGN.md): the "rotate-half" convention -- dimension i is paired with i + d/2 for i < d/2, and
+The pages do not fix the pairing of dimensions or the frequencies.  Reading used here: the
+"rotate-half" convention -- dimension i is paired with i + d/2 for i < d/2, and
 the pair turns by the angle p * theta^(-2i/d).  No frequency scaling.
 """
 from __future__ import annotations

@@ -18,7 +18,7 @@ Five named workloads are defined (sizes from the build's benchmark definition):
 * ``batch70b``        64 q / 8 kv heads, 64 requests x 16 spans x 1024 tokens from a pool of
                       256 spans (Zipf(1.0)), 128 query tokens, recompute 10 %.
 
-Readings of what the source pages leave open (all listed in the design doc):
+Readings of what the source pages leave open:
 * a request's spans are laid contiguously in draw order from a base offset b ~ U{0..4095};
 * Zipf draws are without replacement (a document appears once per prompt), rank probability
   proportional to r^-a over the pool;
