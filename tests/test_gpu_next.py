@@ -1,7 +1,9 @@
-"""GPU parity of the two selection variants beyond the per-span hot path: the pages' global Top-N
-(one budget per request over all its cached tokens, QCFuse 2B) and anchor extraction (each span's
-tokens with the largest key norm, QCFuse 2A).  Selections are bit-exact when fed the oracle's fp32
-values; key norms are within 1e-5 relative of the fp64 oracle."""
+"""GPU parity of the variants beyond the per-span hot path: the pages' global Top-N (one budget
+per request over all its cached tokens, QCFuse 2B), anchor extraction (each span's tokens with the
+largest key norm, QCFuse 2A), anchor-prefixed query probing (QCFuse 2A injection / Phase 2) and the
+layer-pipelined pool prefetch (QCFuse 2C / Phase 4, host tier).  Selections and copies are
+bit-exact (selections when fed the oracle's fp32 values); key norms are within 1e-5 relative of
+the fp64 oracle; attention outputs within 2e-2 absolute + 1e-2 relative."""
 from __future__ import annotations
 
 import dataclasses
