@@ -311,6 +311,65 @@ def test_exclusion_masks_bits():
         assert bool((int(m[j // 16]) >> (j % 16)) & 1) == (j in set(sel.tolist()))
 
 
+# ---------- row positions and the recompute gather (QCFuse Phase 4: the Top-N indices are
+# recomputed at their own positions, then the query follows) ----------
+
+class _Sp:
+    def __init__(self, phys_first_page, n_pages, pos0):
+        self.phys_first_page, self.n_pages, self.pos0 = phys_first_page, n_pages, pos0
+
+
+def test_row_positions_worked_example():
+    # span A: one page at positions 100..115; span B: two pages at 300..331; query of 3 tokens at
+    # 332..334.  Request-local tokens 3 (A), 17 and 30 (B offsets 1 and 14) are recomputed.
+    hkv, d = 1, 4
+    pool = np.zeros((3, hkv, 16, d))
+    _, _, kpos = method.request_cached([_Sp(0, 1, 100), _Sp(1, 2, 300)], pool, pool)
+    got = method.row_positions(np.array([3, 17, 30]), kpos, 3, 332)
+    assert got.tolist() == [103, 301, 314, 332, 333, 334]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_row_positions_ordered_and_query_contiguous(seed):
+    rng = np.random.default_rng(seed)
+    spans, pos = [], int(rng.integers(0, 4096))
+    for i in range(int(rng.integers(1, 6))):
+        n = int(rng.integers(1, 5))
+        spans.append(_Sp(i * 4, n, pos))
+        pos += 16 * n + 16 * int(rng.integers(0, 3))       # spans may leave gaps
+    pool = np.zeros((4 * len(spans), 1, 16, 2))
+    _, _, kpos = method.request_cached(spans, pool, pool)
+    # positions written out span by span, independently of request_cached
+    direct = [s.pos0 + t for s in spans for t in range(16 * s.n_pages)]
+    n_tok = len(direct)
+    sel = np.sort(rng.choice(n_tok, size=int(rng.integers(0, n_tok + 1)), replace=False))
+    nq, q0 = int(rng.integers(0, 9)), pos + 5
+    got = method.row_positions(sel, kpos, nq, q0)
+    assert len(got) == len(sel) + nq
+    assert got[: len(sel)].tolist() == [direct[j] for j in sel.tolist()]
+    assert np.all(np.diff(got[: len(sel)]) > 0)                 # recomputed rows in position order
+    assert got[len(sel):].tolist() == list(range(q0, q0 + nq))  # query rows follow, contiguous
+    if len(sel) and nq:
+        assert got[len(sel) - 1] < got[len(sel)]
+
+
+def test_gather_rows_worked_example():
+    src = np.arange(15, dtype=np.int64).reshape(5, 3)
+    got = method.gather_rows(src, np.array([4, 0, 2]))
+    assert got.tolist() == [[12, 13, 14], [0, 1, 2], [6, 7, 8]]
+    assert got.dtype == src.dtype
+    assert method.gather_rows(src, np.zeros((0,), dtype=np.int64)).shape == (0, 3)
+
+
+def test_gather_rows_of_an_ascending_selection_keep_the_selection_order():
+    # a bf16-exact integer pattern: row j is j*8 + column, so a gathered row names its source
+    src = (np.arange(40 * 8, dtype=np.float64).reshape(40, 8))
+    sel = np.array([1, 2, 7, 19, 33, 39])
+    got = method.gather_rows(src, sel)
+    assert [int(r[0]) // 8 for r in got] == sel.tolist()
+    assert all(np.array_equal(r, np.arange(8) + 8 * j) for r, j in zip(got, sel))
+
+
 # ---------- attention ----------
 
 def _sdpa(q, k, v, mask=None):
