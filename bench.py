@@ -1,8 +1,9 @@
 """Benchmark of the cache-fusion hot path at the critical layer on GB300.
 
-One step = score (query -> cached keys, RoPE in-kernel) + per-span top-k + gather of the
-recompute rows + fused attention of recomputed and query rows over cached-minus-selected plus
-fresh KV, on one batch of synthetic input already resident in HBM.
+One step = score (query -> cached keys, each key rotated to its request's position at use time)
++ per-span top-k + gather of the recompute rows + fused attention of recomputed and query rows
+over cached-minus-selected plus fresh KV, on one batch of synthetic input already resident in HBM.
+The default workload is the largest single-GPU one, the 70B-shaped batch of 64 requests.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--pct P] [--impl reference]
 
@@ -163,13 +164,16 @@ def oracle_prepare(b):
                 kf=b.k_fresh.double().numpy(), vf=b.v_fresh.double().numpy())
 
 
-def oracle_step(b, prep, req_ids):
+def oracle_step(b, prep, req_ids, row_stride=1):
     """The fp64 oracle on the given requests: score, per-span top-k, gather, fused attention.
-    Returns the tokens (cached + query) it processed."""
+    With row_stride > 1 the attention runs on every row_stride-th row only and its time counts
+    row_stride times (rows spread evenly over the causal order, so the estimate is unbiased).
+    Returns (tokens processed, seconds of oracle work those tokens take)."""
     from oracle import method
     qb, rb = b.query_bases(), b.row_bases()
-    tokens = 0
+    tokens, secs = 0, 0.0
     for i in req_ids:
+        t0 = time.perf_counter()
         r = b.requests[i]
         K, V, kpos = method.request_cached(r.spans, prep["kp"], prep["vp"])
         q = prep["qq"][qb[i]: qb[i] + r.n_query]
@@ -178,18 +182,30 @@ def oracle_step(b, prep, req_ids):
                                          [s.k for s in r.spans])
         method.gather_rows(np.arange(r.n_cached), sel)
         row_pos = method.row_positions(sel, kpos, r.n_query, r.query_pos0)
+        t1 = time.perf_counter()
         sl = slice(rb[i], rb[i] + r.n_rows)
         method.fused_attention_request(prep["qf"][sl], prep["kf"][sl], prep["vf"][sl], row_pos, K, V, kpos,
-                                       sel, b.theta)
+                                       sel, b.theta, rows=np.arange(0, r.n_rows, row_stride))
+        secs += (t1 - t0) + row_stride * (time.perf_counter() - t1)
         tokens += r.n_cached + r.n_query
-    return tokens
+    return tokens, secs
 
 
 def _oracle_sample(b):
-    """Requests the bounded oracle sample covers (whole requests, ~10-30 s of CPU work)."""
+    """Requests and attention row stride of the bounded oracle sample (a few seconds of CPU work
+    per step): whole small workloads; one request of the large ones with the attention on every
+    16th row (the attention over a 16k-token request takes the fp64 oracle most of a minute)."""
     n = len(b.requests)
-    budget = {"tiny": n, "llama8b_layer": n, "concurrent_reuse": 1, "long_context": 1, "batch70b": 1}
-    return list(range(min(n, budget.get(b.cfg_name, 1))))
+    if b.cfg_name in ("tiny", "llama8b_layer"):
+        return list(range(n)), 1
+    return [0], 16
+
+
+def _sample_text(b, ids, stride):
+    s = f"{len(ids)} of {len(b.requests)} requests of the {b.cfg_name} workload"
+    if stride > 1:
+        s += f", attention on every {stride}th row with its time counted {stride}x"
+    return s
 
 
 def run_reference(args):
@@ -198,18 +214,18 @@ def run_reference(args):
         return
     b = make_batch(args.config, args.pct)
     prep = oracle_prepare(b)
-    ids = _oracle_sample(b)
+    ids, stride = _oracle_sample(b)
     for _ in range(args.warmup):
-        oracle_step(b, prep, ids)
-    t0 = time.perf_counter()
-    tokens = 0
+        oracle_step(b, prep, ids, stride)
+    tokens, dt = 0, 0.0
     for _ in range(args.steps):
-        tokens += oracle_step(b, prep, ids)
-    dt = time.perf_counter() - t0
+        tk, sec = oracle_step(b, prep, ids, stride)
+        tokens += tk
+        dt += sec
     value = tokens / dt
     cores = len(os.sched_getaffinity(0))
-    sample = (f"{len(ids)} of {len(b.requests)} requests of the {args.config} workload per step "
-              f"(score + top-k + gather + fused attention, fp64 NumPy)")
+    sample = (f"{_sample_text(b, ids, stride)} per step (score + top-k + gather + fused attention, "
+              f"fp64 NumPy, BLAS threads = all cores)")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
@@ -442,7 +458,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="llama8b_layer", choices=list(CONFIGS))
+    ap.add_argument("--config", default="batch70b", choices=list(CONFIGS))
     ap.add_argument("--pct", type=int, default=None)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -622,18 +638,20 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # the oracle as it stands, repeated on the same requests until about 10 s of CPU work
         prep = oracle_prepare(b)
-        ids = _oracle_sample(b)
+        ids, stride = _oracle_sample(b)
         t1 = time.perf_counter()
         tok = reps = 0
+        dt = 0.0
         while reps < 1 or (time.perf_counter() - t1 < 10.0 and reps < 50):
-            tok += oracle_step(b, prep, ids)
+            tk, sec = oracle_step(b, prep, ids, stride)
+            tok += tk
+            dt += sec
             reps += 1
-        dt = time.perf_counter() - t1
         line["cpu_baseline"] = {"value": tok / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
                                 "kind": "oracle",
-                                "sample": f"{len(ids)} of {len(b.requests)} requests, full oracle step (score, top-k, "
-                                          f"gather, attention; fp64 NumPy, BLAS threads = all cores) x {reps}, "
-                                          f"{dt:.1f} s"}
+                                "sample": f"{_sample_text(b, ids, stride)}, oracle step (score, top-k, gather, "
+                                          f"attention; fp64 NumPy, BLAS threads = all cores) x {reps}, "
+                                          f"{time.perf_counter() - t1:.1f} s of CPU time"}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -56,6 +56,8 @@ typedef int32_t pcf_status;
 #define PCF_ERR_WORKSPACE_TOO_SMALL  -5
 #define PCF_ERR_DEVICE_BOUNDS        -6  /* a kernel met an out-of-range index (reported by check) */
 #define PCF_ERR_NO_DEVICE            -7  /* no sm_103 device is current */
+#define PCF_ERR_DEVICE_RANGE         -8  /* a rotated query or key left the fp16 operand range
+                                            (infinities included; reported by check) */
 
 /* One cached span of a request: n_pages consecutive physical pages starting at phys_first_page,
  * holding tokens at logical positions pos0 .. pos0 + 16*n_pages - 1; k of its tokens are to be
@@ -82,6 +84,8 @@ typedef struct pcf_dims {
     int32_t head_dim;      /* d in {64, 128} */
     int32_t n_phys_pages;  /* pages in the pool */
     int32_t max_pos;       /* rows of the rope table; every position must be < max_pos <= 1<<20 */
+    int32_t n_sms;         /* SMs the work lists are balanced over (the device's multiprocessor
+                              count); <= 0 selects 152, GB300's count; at most 4096 */
 } pcf_dims;
 
 typedef struct pcf_layout {
@@ -112,7 +116,9 @@ pcf_status pcf_rope_table_init(float* table, int32_t head_dim, double theta, int
 pcf_status pcf_layout_words(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims* dims,
                             int64_t* n_words);
 
-/* Host-only.  Validates the batch and writes the layout blob: per request, the block table
+/* Host-only.  Validates the batch and writes the layout blob (MiniPIC section 1 "concurrency
+ * barrier" and section 2.1: per-request logical positions over shared physical pages; section 2.2
+ * "Padding": spans start on page boundaries): per request, the block table
  * (logical page -> physical page), the logical position of every page's first token, span
  * records, row/selection offsets and the kernels' work lists.  Errors (PCF_ERR_INVALID_ARG):
  * null pointers, n_reqs < 1, a span outside the pool or with n_pages < 1, positions not strictly
@@ -187,7 +193,9 @@ pcf_status pcf_pack_anchor_pages(const pcf_layout* layout, const int32_t* sel_id
 pcf_status pcf_prefetch_pool_pages(const pcf_layout* layout, const uint16_t* src_k, const uint16_t* src_v,
                                    uint16_t* dst_k, uint16_t* dst_v, void* stream);
 
-/* Row gather of the recompute batch: dst[sel_base_b + i][:] = src[tok_base_b + sel_idx[...]][:]
+/* Row gather of the recompute batch (QCFuse Phase 4, second summary: the Top-N tokens are recomputed
+ * discretely, so their inputs are collected into one dense batch):
+ * dst[sel_base_b + i][:] = src[tok_base_b + sel_idx[...]][:]
  * for every selected row; src [total_tokens][row_elems], dst [total_sel][row_elems], bf16;
  * row_elems a positive multiple of 8. */
 pcf_status pcf_gather_rows(const pcf_layout* layout, const int32_t* sel_idx, const uint16_t* src,
@@ -200,8 +208,10 @@ pcf_status pcf_attention_workspace_bytes(const int32_t* layout_host, size_t* byt
  * For each row r of request b (its recomputed tokens then its query tokens) and q head h:
  *   out[r][h] = sum_u softmax_u(s_u) v_u,  s_u = (R_{pos(r)} q_{r,h}) . (R_{pos(u)} k_u) / sqrt(d)
  * over keys u = the cached tokens of b whose excl bit is clear, at pi(j), plus the fresh rows of
- * b at row_pos; u is visible iff pos(u) <= row_pos[r].  Cached keys are rotated in the kernel,
- * in shared memory, from the unrotated pool.  ws: >= pcf_attention_workspace_bytes bytes. */
+ * b at row_pos; u is visible iff pos(u) <= row_pos[r].  The pool stays unrotated and is never
+ * written: the cached keys that take part are read from their pages through the block table and
+ * rotated to the request's positions by a pass of this call (into ws, with their V rows beside
+ * them), which the attention kernel then streams.  ws: >= pcf_attention_workspace_bytes bytes. */
 pcf_status pcf_fused_attention(const pcf_layout* layout, const uint16_t* q_fresh,
                                const uint16_t* k_fresh, const uint16_t* v_fresh,
                                const uint16_t* k_pool, const uint16_t* v_pool,
@@ -233,8 +243,9 @@ pcf_status pcf_fused_attention_timed(const pcf_layout* layout, const uint16_t* q
  *   reachable from the library.
  *   Limit: a batch whose pcf_score_workspace_bytes exceeds the array size is rejected with
  *   PCF_ERR_WORKSPACE_TOO_SMALL before any work is queued.
- *   Set-up: the first call on each device looks up the array's device address (with that device
- *   current); make that first call before any stream capture.
+ *   Set-up: the first call on each device (and again after that device's context was reset)
+ *   looks up the array's device address, with that device current; make that first call before
+ *   any stream capture.
  *   Sharing: every call on a device uses the same array, which keeps the last call's contents
  *   (the call clears what must start at zero itself).  Calls that overlap on the GPU -- on
  *   different streams, or from different threads -- race on it and must be serialized by the
@@ -243,7 +254,11 @@ pcf_status pcf_score_noalloc(const pcf_layout* layout, const uint16_t* q_query, 
                              const float* rope, float* importance, void* stream);
 
 /* Synchronizes `stream`, then reads and clears the device error word: PCF_OK,
- * PCF_ERR_DEVICE_TIMEOUT or PCF_ERR_DEVICE_BOUNDS (PCF_ERR_CUDA if the sync itself failed). */
+ * PCF_ERR_DEVICE_TIMEOUT, PCF_ERR_DEVICE_BOUNDS or PCF_ERR_DEVICE_RANGE (the first error raised
+ * since the last check; PCF_ERR_CUDA if the sync itself failed).  The rotated queries and keys
+ * enter the tensor cores as fp16: a value whose magnitude rounds above 65504 (inputs far outside
+ * the usual activation range) raises PCF_ERR_DEVICE_RANGE instead of being clamped silently, and
+ * the results of that call must be discarded. */
 pcf_status pcf_check_device_error(void* stream);
 
 /* Queues `n` asynchronous copies on `stream`, in order: copy i moves bytes[i] bytes from src[i]

@@ -6,7 +6,7 @@ the current CUDA stream) and allocates buffers through torch.  There is no CPU f
 the built library or an sm_103 device the calls raise.
 
 Hot path for one batch at the critical layer:
-  ``score``          importance of every cached token (query -> cached keys, RoPE in-kernel)
+  ``score``          importance of every cached token (query -> cached keys, each key rotated to its request's position at use time)
   ``select_topk``    per-span top-k tokens to recompute, exclusion bits, row positions
   ``gather_rows``    rows of the selected tokens (input of the recomputation)
   ``fused_attention`` recomputed + query rows over cached-minus-selected + fresh KV
@@ -76,7 +76,11 @@ class Layout:
                 arr[j] = _lib.SpanDesc(int(s.phys_first_page), int(s.n_pages), int(s.pos0), int(s.k))
             self._span_arrays.append(arr)
             reqs[i] = _lib.RequestDesc(len(r.spans), arr, int(r.n_query), int(r.query_pos0))
-        dims = _lib.Dims(hq, hkv, d, n_phys_pages, max_pos)
+        # the work lists are balanced over the SMs of the device the batch runs on
+        n_sms = 0
+        if device != "cpu" and torch.cuda.is_available():
+            n_sms = torch.cuda.get_device_properties(torch.device(device)).multi_processor_count
+        dims = _lib.Dims(hq, hkv, d, n_phys_pages, max_pos, n_sms)
         n = ctypes.c_int64(0)
         _lib.check("pcf_layout_words", lib.pcf_layout_words(reqs, len(requests), ctypes.byref(dims),
                                                             ctypes.byref(n)))

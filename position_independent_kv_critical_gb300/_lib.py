@@ -16,7 +16,7 @@ PCF_OK = 0
 STATUS = {
     0: "PCF_OK", -1: "PCF_ERR_INVALID_ARG", -2: "PCF_ERR_UNSUPPORTED", -3: "PCF_ERR_CUDA",
     -4: "PCF_ERR_DEVICE_TIMEOUT", -5: "PCF_ERR_WORKSPACE_TOO_SMALL", -6: "PCF_ERR_DEVICE_BOUNDS",
-    -7: "PCF_ERR_NO_DEVICE",
+    -7: "PCF_ERR_NO_DEVICE", -8: "PCF_ERR_DEVICE_RANGE",
 }
 HEADER_FIELDS = {
     "words": 1, "n_reqs": 2, "hq": 3, "hkv": 4, "d": 5, "n_phys_pages": 6, "max_pos": 7,
@@ -45,7 +45,7 @@ class RequestDesc(ctypes.Structure):
 
 class Dims(ctypes.Structure):
     _fields_ = [("n_q_heads", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32),
-                ("n_phys_pages", c_int32), ("max_pos", c_int32)]
+                ("n_phys_pages", c_int32), ("max_pos", c_int32), ("n_sms", c_int32)]
 
 
 class LayoutRef(ctypes.Structure):

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob a, RopeJob b, Ro
         const float4 v = __ldg(cs4 + q);
         cs[4 * q] = v.x; cs[4 * q + 1] = v.y; cs[4 * q + 2] = v.z; cs[4 * q + 3] = v.w;
     }
+    float big = 0.f;   // largest rotated magnitude of the row: above fp16's range it is an error
     for (int h0 = hbeg; h0 < hend; h0 += HB) {
         uint4 xa[HB], xb[HB], va[HB], vb[HB];
 #pragma unroll
@@ -125,8 +126,8 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob a, RopeJob b, Ro
                 const float c0 = cs[4 * e], s0 = cs[4 * e + 1], c1 = cs[4 * e + 2], s1 = cs[4 * e + 3];
                 const float a0 = bf16_lo(ia[e]) * J.scale, a1 = bf16_hi(ia[e]) * J.scale;
                 const float b0 = bf16_lo(ib[e]) * J.scale, b1 = bf16_hi(ib[e]) * J.scale;
-                oa[e] = pack_f16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
-                ob[e] = pack_f16x2(fmaf(b0, c0, a0 * s0), fmaf(b1, c1, a1 * s1));
+                oa[e] = pack_f16x2_track(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1), big);
+                ob[e] = pack_f16x2_track(fmaf(b0, c0, a0 * s0), fmaf(b1, c1, a1 * s1), big);
             }
             const int64_t orow = ((int64_t)(h / J.gg) * orow_n + oi) * J.gg + (h % J.gg);
             __half* dst = J.out + orow * D;
@@ -139,6 +140,7 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob a, RopeJob b, Ro
             }
         }
     }
+    if (!(big < kF16Limit)) set_dev_error(kDevErrRange);
 }
 
 // ------------------------------------------------------------------ block scan helper

@@ -18,7 +18,7 @@ constexpr int kQTilesPerCta = 2;         // 128-row query tiles sharing each rot
 constexpr int kPagesPerTile = kTileKeys / kPage;
 constexpr int kMaxPosLimit = 1 << 20;
 constexpr int kItemWords = 4;
-constexpr int kNumSms = 152;            // GB300; the attention kernels run one CTA per SM
+constexpr int kDefaultSms = 152;        // GB300's SM count: the plan's target when the caller names none
 constexpr int kMaxSplits = 16;          // key-range splits of one attention (or LSE) work unit
 
 enum : int {
@@ -30,6 +30,7 @@ enum : int {
     L_OFF_REQ = 24, L_OFF_SPAN = 25, L_OFF_BLOCK = 26, L_OFF_PAGEPOS = 27, L_OFF_ATTN = 28,
     L_OFF_LSE = 29, L_OFF_IMP = 30, L_OFF_QPOS = 31, L_OFF_COMB = 32, L_N_COMB = 33,
     L_ATTN_SLOTS = 34, L_OFF_PAIR = 35, L_N_PAIRS = 36,
+    L_N_SMS = 37,         // SMs the work lists were planned for (the persistent grids use the device's own count)
     L_TOTAL_VALID = 38,   // cached keys that take part in the attention (not recomputed), all requests
     L_HEADER = 40
 };

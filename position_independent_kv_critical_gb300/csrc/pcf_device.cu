@@ -124,21 +124,38 @@ pcf_status check_layout(const pcf_layout* lay) {
     return PCF_OK;
 }
 
-// sm_103 (GB300) must be the current device (the answer is kept per device ordinal)
-pcf_status check_device() {
-    static std::atomic<signed char> known[256];   // 0 unknown, 1 sm_103, -1 other
-    int dev = 0, major = 0, minor = 0;
+// sm_103 (GB300) must be the current device.  The answer and the device's SM count are kept per
+// device ordinal: sms[dev] > 0 is the count of an sm_103 device, -1 marks another architecture.
+std::atomic<int> g_dev_sms[256];
+
+pcf_status check_device(int* n_sms = nullptr) {
+    int dev = 0, major = 0, minor = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PCF_ERR_NO_DEVICE;
-    if (dev >= 0 && dev < 256) {
-        const signed char k = known[dev].load(std::memory_order_relaxed);
-        if (k != 0) return k > 0 ? PCF_OK : PCF_ERR_NO_DEVICE;
+    const bool cached = dev >= 0 && dev < 256;
+    if (cached) {
+        const int k = g_dev_sms[dev].load(std::memory_order_relaxed);
+        if (k != 0) {
+            if (k < 0) return PCF_ERR_NO_DEVICE;
+            if (n_sms) *n_sms = k;
+            return PCF_OK;
+        }
     }
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
         return PCF_ERR_NO_DEVICE;
     const bool ok = major == 10 && minor == 3;
-    if (dev >= 0 && dev < 256) known[dev].store(ok ? 1 : -1, std::memory_order_relaxed);
-    return ok ? PCF_OK : PCF_ERR_NO_DEVICE;
+    if (cached) g_dev_sms[dev].store(ok ? sms : -1, std::memory_order_relaxed);
+    if (!ok) return PCF_ERR_NO_DEVICE;
+    if (n_sms) *n_sms = sms;
+    return PCF_OK;
+}
+
+// the current device's SM count (after check_device succeeded on it)
+int device_sms() {
+    int n = kDefaultSms;
+    check_device(&n);
+    return n;
 }
 
 // Every kernel of the library is launched with programmatic stream serialization: its CTAs may be
@@ -225,7 +242,7 @@ template <int D>
 int64_t rope_threads(RopeJob& j) {
     if (!j.x) return 0;
     const int64_t rows_x = (int64_t)j.n_rows * (D / 16);
-    j.hpt = rows_x >= 4 * kNumSms * 256 ? j.heads : 4;
+    j.hpt = rows_x >= 4 * device_sms() * 256 ? j.heads : 4;
     return rows_x * ((j.heads + j.hpt - 1) / j.hpt);
 }
 
@@ -297,7 +314,7 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
         AttnParams p{lay->dev, nullptr, nullptr, nullptr, lse, nullptr, nullptr, cnt + H[L_TOTAL_KTILES]};
         // persistent: at most one CTA per SM, items handed out in list order
-        const int grid = std::min<int>(H[L_N_LSE_ITEMS], kNumSms);
+        const int grid = std::min<int>(H[L_N_LSE_ITEMS], device_sms());
         if ((s = launch(kern, dim3(grid), dim3(kAttnThreads), SM::kAlloc, st, tq128, tkc, zero, zero, zero, p)) !=
             PCF_OK)
             return s;
@@ -372,7 +389,7 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     float2* part_ml = reinterpret_cast<float2*>(base + w.pml);
     AttnParams p{lay->dev, kpos_c, row_pos, reinterpret_cast<__nv_bfloat16*>(out), nullptr, part_o, part_ml, sched};
     // persistent: at most one CTA per SM, items handed out in list order (largest estimate first)
-    const int grid = std::min<int>(H[L_N_ATTN_ITEMS], kNumSms);
+    const int grid = std::min<int>(H[L_N_ATTN_ITEMS], device_sms());
     if (ev_start && cudaEventRecord(ev_start, st) != cudaSuccess) return PCF_ERR_CUDA;
     if ((s = launch(kern, dim3(grid), dim3(kAttnThreads), SM::kAlloc, st, tq, tkc, tvc, tkf, tvf, p)) != PCF_OK)
         return s;
@@ -606,6 +623,7 @@ extern "C" pcf_status pcf_check_device_error(void* stream) {
     }
     if (code == kDevErrTimeout) return PCF_ERR_DEVICE_TIMEOUT;
     if (code == kDevErrBounds) return PCF_ERR_DEVICE_BOUNDS;
+    if (code == kDevErrRange) return PCF_ERR_DEVICE_RANGE;
     return PCF_OK;
 }
 
@@ -617,19 +635,36 @@ static __device__ __align__(256) uint8_t g_pcf_noalloc_ws[PCF_SCORE_NOALLOC_MAX_
 
 namespace {
 std::mutex g_noalloc_mu;
-std::map<int, void*> g_noalloc_ptr;   // device ordinal -> device address of g_pcf_noalloc_ws
+// (device ordinal, CUDA context) -> device address of g_pcf_noalloc_ws.  Keyed on the context as
+// well: if the device's primary context is torn down and created again (cudaDeviceReset), the
+// module is loaded anew and the array may sit at another address.
+std::map<std::pair<int, void*>, void*> g_noalloc_ptr;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn g_ctx_get = nullptr;
+std::once_flag g_ctx_once;
 
 // The array's name is only a host-side stand-in in host code; its device address is looked up
-// once per device, with that device current.
+// once per device and context, with that device current.
 pcf_status noalloc_workspace(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PCF_ERR_NO_DEVICE;
+    std::call_once(g_ctx_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get = reinterpret_cast<CtxGetCurrentFn>(fn);
+    });
+    CUcontext ctx = nullptr;
+    if (!g_ctx_get || g_ctx_get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return PCF_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    auto it = g_noalloc_ptr.find(dev);
+    const auto key = std::make_pair(dev, static_cast<void*>(ctx));
+    auto it = g_noalloc_ptr.find(key);
     if (it == g_noalloc_ptr.end()) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_pcf_noalloc_ws) != cudaSuccess || p == nullptr) return PCF_ERR_CUDA;
-        it = g_noalloc_ptr.emplace(dev, p).first;
+        it = g_noalloc_ptr.emplace(key, p).first;
     }
     *out = it->second;
     return PCF_OK;

@@ -26,6 +26,7 @@ extern "C" const char* pcf_status_string(pcf_status s) {
         case PCF_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
         case PCF_ERR_DEVICE_BOUNDS: return "a kernel met an out-of-range index";
         case PCF_ERR_NO_DEVICE: return "no sm_103 device is current";
+        case PCF_ERR_DEVICE_RANGE: return "a rotated query or key is outside the fp16 range (|x| > 65504)";
         default: return "unknown status";
     }
 }
@@ -63,6 +64,7 @@ struct Plan {
     int32_t n_spans = 0, max_tokens = 0, max_rows = 0, max_query = 0, total_ktiles = 0;
     int32_t n_attn = 0, n_lse = 0, n_imp = 0, lse_slots = 0, max_span_len = 0;
     int32_t n_comb = 0, attn_slots = 0, n_pairs = 0, imp_tiles = 1;
+    int32_t n_sms = kDefaultSms;        // SMs the work lists are planned for
     std::vector<int32_t> lse_chunks;
     std::vector<int32_t> pair_base;     // per request: first pair record
     std::vector<int32_t> pair_tiles;    // per pair record: estimated key tiles of the pair
@@ -71,12 +73,12 @@ struct Plan {
 
 inline int32_t cdiv(int64_t a, int64_t b) { return (int32_t)((a + b - 1) / b); }
 
-// Estimated finishing time (in key tiles) of CTAs with the given costs on kNumSms SMs that take
+// Estimated finishing time (in key tiles) of CTAs with the given costs on n_sms SMs that take
 // one CTA each at a time, launched in decreasing cost order (the order of the work lists).
-double lpt_makespan(std::vector<double>& costs) {
+double lpt_makespan(std::vector<double>& costs, int32_t n_sms) {
     std::sort(costs.begin(), costs.end(), std::greater<double>());
     std::priority_queue<double, std::vector<double>, std::greater<double>> sm;
-    for (int i = 0; i < kNumSms; ++i) sm.push(0.0);
+    for (int i = 0; i < n_sms; ++i) sm.push(0.0);
     double end = 0.0;
     for (double c : costs) {
         const double t = sm.top() + c;
@@ -92,9 +94,9 @@ double lpt_makespan(std::vector<double>& costs) {
 // and any split adds `combine` tiles (the merge of the partial results).  Batches with enough
 // units to fill the GPU several times are not split.
 void choose_splits(const std::vector<int32_t>& tiles, int32_t copies, double overhead, double combine,
-                   int32_t max_split, std::vector<int32_t>* splits) {
+                   int32_t max_split, int32_t n_sms, std::vector<int32_t>* splits) {
     splits->assign(tiles.size(), 1);
-    if (tiles.empty() || (int64_t)tiles.size() * copies >= 4 * kNumSms) return;
+    if (tiles.empty() || (int64_t)tiles.size() * copies >= 4 * n_sms) return;
     int32_t max_t = 1;
     for (int32_t t : tiles) max_t = std::max(max_t, t);
     double best = 0.0;
@@ -108,7 +110,7 @@ void choose_splits(const std::vector<int32_t>& tiles, int32_t copies, double ove
             any = any || sp > 1;
             costs.insert(costs.end(), (size_t)copies * sp, overhead + (double)t / sp);
         }
-        const double end = lpt_makespan(costs) + (any ? combine : 0.0);
+        const double end = lpt_makespan(costs, n_sms) + (any ? combine : 0.0);
         if (c == max_t || end < best - 1e-9) {
             best = end;
             best_c = c;
@@ -134,6 +136,8 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
     if (d.n_q_heads % d.n_kv_heads != 0) return PCF_ERR_UNSUPPORTED;
     const int g = d.n_q_heads / d.n_kv_heads;
     if (g > kTileRows || kTileRows % g != 0) return PCF_ERR_UNSUPPORTED;
+    if (d.n_sms > 4096) return PCF_ERR_INVALID_ARG;
+    plan->n_sms = d.n_sms > 0 ? d.n_sms : kDefaultSms;
 
     int64_t tot_tok = 0, tot_q = 0, tot_rows = 0, tot_sel = 0, tot_spans = 0, tot_kt = 0;
     for (int b = 0; b < n_reqs; ++b) {
@@ -214,7 +218,8 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
             plan->pair_tiles.push_back(nct + (int32_t)(last / kTileKeys) + 1);
         }
     }
-    choose_splits(plan->pair_tiles, d.n_kv_heads, kAttnCtaOverhead, kAttnCombineCost, kMaxSplits, &plan->pair_split);
+    choose_splits(plan->pair_tiles, d.n_kv_heads, kAttnCtaOverhead, kAttnCombineCost, kMaxSplits, plan->n_sms,
+                  &plan->pair_split);
     // LSE pass: units (request, query tile pair) over all cached tiles, split into key chunks
     std::vector<int32_t> lse_split;
     {
@@ -228,7 +233,7 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
                 for (int32_t p = 0; p < cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta); ++p) tiles.push_back(nkt);
         }
         std::vector<int32_t> sp;
-        choose_splits(tiles, d.n_kv_heads, kLseCtaOverhead, 0.0, kMaxSplits, &sp);
+        choose_splits(tiles, d.n_kv_heads, kLseCtaOverhead, 0.0, kMaxSplits, plan->n_sms, &sp);
         size_t u = 0;
         for (int b = 0; b < n_reqs; ++b) {
             const pcf_request_desc& r = reqs[b];
@@ -254,7 +259,7 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
             for (int s = 0; s < reqs[b].n_spans; ++s) n_pg += reqs[b].spans[s].n_pages;
             if (n_pg > 0) tiles.push_back(cdiv(n_pg, kPagesPerTile));
         }
-        choose_splits(tiles, d.n_kv_heads, kImpCtaOverhead, 0.0, 1 << 20, &sp);
+        choose_splits(tiles, d.n_kv_heads, kImpCtaOverhead, 0.0, 1 << 20, plan->n_sms, &sp);
         int32_t run = 1;
         for (size_t u = 0; u < tiles.size(); ++u) run = std::max(run, cdiv(tiles[u], sp[u]));
         plan->imp_tiles = run;
@@ -352,6 +357,7 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
     H[L_N_COMB] = plan.n_comb;
     H[L_ATTN_SLOTS] = plan.attn_slots;
     H[L_N_PAIRS] = plan.n_pairs;
+    H[L_N_SMS] = plan.n_sms;
 
     int64_t off = L_HEADER;
     H[L_OFF_REQ] = (int32_t)off;    off += (int64_t)n_reqs * R_STRIDE;

@@ -9,7 +9,7 @@
 
 namespace pcf {
 
-enum : int { kDevErrNone = 0, kDevErrTimeout = 1, kDevErrBounds = 2 };
+enum : int { kDevErrNone = 0, kDevErrTimeout = 1, kDevErrBounds = 2, kDevErrRange = 3 };
 
 // Device error word of this library (one per loaded module); read and cleared by
 // pcf_check_device_error.  Defined here: the library is a single CUDA translation unit.
@@ -324,6 +324,14 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+// Largest magnitude that rounds to a finite fp16 (65504 plus half a unit in the last place).
+constexpr float kF16Limit = 65520.0f;
+// The same, recording in `big` (as the running maximum of |lo|, |hi|) whether a value was out of
+// fp16 range; the caller raises kDevErrRange once for the whole row instead of clamping silently.
+__device__ __forceinline__ uint32_t pack_f16x2_track(float lo, float hi, float& big) {
+    big = max3f(big, fabsf(lo), fabsf(hi));
+    return pack_f16x2(lo, hi);
 }
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }

@@ -63,9 +63,9 @@ class GpuBatch:
     def oracle_request(self, i):
         b = self.b
         r = b.requests[i]
-        kp = b.k_pool.double().numpy()
-        vp = b.v_pool.double().numpy()
-        K, V, kpos = method.request_cached(r.spans, kp, vp)
+        if not hasattr(self, "_pool64"):    # exact fp64 copies of the bf16 pools, made once
+            self._pool64 = (b.k_pool.double().numpy(), b.v_pool.double().numpy())
+        K, V, kpos = method.request_cached(r.spans, *self._pool64)
         return r, K, V, kpos
 
     def oracle_score(self, i):

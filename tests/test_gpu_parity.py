@@ -39,11 +39,17 @@ def _sample_rows(n_rows, n_sel, k=48):
     return np.array(sorted(rows))
 
 
-def check_batch(gb: GpuBatch, req_ids=None, sample_rows=False):
+def check_batch(gb: GpuBatch, req_ids=None, sample_rows=False, imp_only_ids=()):
+    """Importance, top-k and attention of the requests `req_ids` (all by default) against the
+    oracle; `imp_only_ids` are further requests whose importance alone is compared."""
     b = gb.b
     ids = list(range(len(b.requests))) if req_ids is None else list(req_ids)
     # 1) importance
     got_imp = gb.score()
+    for i in imp_only_ids:
+        r = b.requests[i]
+        t0 = gb.tok_base[i]
+        assert_close_imp(got_imp[t0: t0 + r.n_cached], gb.oracle_score(i), f"importance req {i}")
     imps = {}
     for i in ids:
         r = b.requests[i]
@@ -97,8 +103,21 @@ def test_long_context_sweep_sampled(pct):
     check_batch(gpu_batch("long_context", pct), sample_rows=True)
 
 
+def _heaviest_span_requests(b, n=2):
+    """Requests holding the physical spans that the Zipf draws reference most often."""
+    refs = {}
+    for i, r in enumerate(b.requests):
+        for s in r.spans:
+            refs.setdefault(s.phys_first_page, []).append(i)
+    top = sorted(refs.items(), key=lambda kv: (-len(kv[1]), kv[0]))[:n]
+    return [reqs[len(reqs) // 2] for _, reqs in top]
+
+
 def test_batch70b_sampled():
-    check_batch(gpu_batch("batch70b"), req_ids=[0, 63], sample_rows=True)
+    gb = gpu_batch("batch70b")
+    spread = list(range(0, 64, 9))                     # 0, 9, ..., 63: eight requests over the batch
+    extra = [i for i in spread + _heaviest_span_requests(gb.b) if i not in (0, 63)]
+    check_batch(gb, req_ids=[0, 63], sample_rows=True, imp_only_ids=sorted(set(extra)))
 
 
 # ------------------------------------------------------------------ top-k at full size, planted ties
@@ -270,6 +289,33 @@ def test_mixed_requests_in_one_batch():
                                            ([], 4, 10),
                                            ([(0, 3, 9000, 48), (29, 11, 9100, 100)], 130, 9400)])
     check_batch(GpuBatch(b))
+
+
+@pytest.mark.parametrize("name,scale", [("tiny", 4.0), ("llama8b_layer", 3.0)])
+def test_large_magnitude_keys_and_queries(name, scale):
+    # keys and queries several times the unit scale (power-of-two-exact where possible): sharper
+    # softmaxes and rotated operands far from 1, still inside the fp16 operand range
+    import dataclasses
+    b = make_batch(name)
+    s = lambda t: (t.float() * scale).to(torch.bfloat16)
+    check_batch(GpuBatch(dataclasses.replace(b, k_pool=s(b.k_pool), q_query=s(b.q_query), q_fresh=s(b.q_fresh),
+                                             k_fresh=s(b.k_fresh))))
+
+
+def test_fp16_range_overflow_is_reported_not_clamped():
+    import dataclasses
+    b = make_batch("tiny")
+    k = b.k_pool.clone()
+    page = b.requests[0].spans[2].phys_first_page
+    k[page, 1, 5, 3] = 2.0e5          # one cached key element far beyond the fp16 range
+    gb = GpuBatch(dataclasses.replace(b, k_pool=k))
+    pcf.score(gb.L, gb.q_query, gb.k_pool, gb.rope, gb.cf.importance, gb.cf.ws_score)
+    with pytest.raises(pcf.PcfError) as e:
+        pcf.check_device_error()
+    assert e.value.status == -8           # PCF_ERR_DEVICE_RANGE
+    pcf.check_device_error()              # the word was cleared: the next check is clean
+    gb_ok = GpuBatch(b)
+    assert_close_imp(gb_ok.score()[: b.requests[0].n_cached], gb_ok.oracle_score(0), "after a range error")
 
 
 def test_device_error_word_clean_after_runs():

@@ -206,6 +206,31 @@ def test_layout_too_small_buffer_and_query():
     assert lib.pcf_attention_workspace_bytes(buf, ctypes.byref(ws)) == 0 and ws.value > 0
 
 
+def test_work_lists_are_planned_for_the_named_sm_count():
+    lib = _lib.load()
+    spans = (_lib.SpanDesc * 2)(_lib.SpanDesc(0, 64, 0, 100), _lib.SpanDesc(64, 64, 1024, 100))
+    reqs = (_lib.RequestDesc * 1)(_lib.RequestDesc(2, spans, 64, 2048))
+
+    def build(n_sms):
+        dims = _lib.Dims(32, 8, 128, 128, 4096, n_sms)
+        n = ctypes.c_int64(0)
+        st = lib.pcf_layout_words(reqs, 1, ctypes.byref(dims), ctypes.byref(n))
+        if st != 0:
+            return st, None
+        buf = (ctypes.c_int32 * n.value)()
+        assert lib.pcf_layout_build(reqs, 1, ctypes.byref(dims), buf, n.value) == 0
+        return 0, np.frombuffer(buf, dtype=np.int32).copy()
+
+    assert build(4097)[0] == -1
+    _, default = build(0)
+    _, gb300 = build(152)
+    _, small = build(8)
+    assert default[37] == 152 and small[37] == 8
+    assert np.array_equal(default, gb300)
+    # one request of 144 rows: on a small GPU its key range needs no split across CTAs
+    assert small[L_N_ATTN] <= default[L_N_ATTN]
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_device_calls_fail_loudly_without_gpu():
     b = small_custom_batch([(0, 2, 0, 3)], n_query=4)
