@@ -15,6 +15,8 @@ What it computes, and from which passage:
   keys only, summed over heads and query tokens into one importance value per cached token
   (QCFuse: Query-Centric Cache Fusion ..., section 2B "Critical-layer attention profiling";
   second summary, Phase 3 "only the key cache of one critical layer").
+* ``method.score_layers_request``  the same importance taken at every layer and summed over the
+  layers (the all-layer comparison point of QCFuse section 4 "Resultados", QCAll).
 * ``method.select_topk_request``  the tokens with the highest importance, chosen per span, ties to
   the lower index (QCFuse section 2B "Top-N tokens"; per-span selection is the workload's reading).
 * ``method.fused_attention_request``  causal attention of the recomputed rows and the query rows

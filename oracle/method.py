@@ -98,6 +98,21 @@ def score_request(q: np.ndarray, q_pos: np.ndarray, K: np.ndarray, k_pos: np.nda
     return imp
 
 
+def score_layers_request(q_layers: Sequence[np.ndarray], q_pos: np.ndarray, K_layers: Sequence[np.ndarray],
+                         k_pos: np.ndarray, theta: float) -> Tuple[np.ndarray, np.ndarray]:
+    """Importance taken at every layer instead of one critical layer (the all-layer comparison
+    point of QCFuse, section 4 "Resultados", QCAll; the last layer alone is QCLast): layer l's
+    query tokens attend over layer l's cached keys exactly as in ``score_request``, and the
+    request's importance is the plain sum of the layers' importances (the pages name no rule for
+    combining layers; a mean would rank the tokens the same way).
+
+    q_layers[l] [T][Hq][d], K_layers[l] [N][Hkv][d] unrotated; positions are the request's, the
+    same at every layer.  Returns (per-layer importance [L][N], their sum over layers [N])."""
+    per = np.stack([score_request(q, q_pos, K, k_pos, theta) for q, K in zip(q_layers, K_layers)]) \
+        if len(q_layers) else np.zeros((0, len(k_pos)))
+    return per, per.sum(axis=0)
+
+
 def select_topk_request(imp: np.ndarray, span_lens: Sequence[int], span_k: Sequence[int]
                         ) -> np.ndarray:
     """Per span: the k_s request-local token indices with the largest importance, ties to the

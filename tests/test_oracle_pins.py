@@ -167,6 +167,50 @@ def test_importance_brute_force_python_loops():
     np.testing.assert_allclose(method.score_request(q, qpos, K, kpos, theta), ref, atol=1e-12)
 
 
+# ---------- all-layer importance (QCAll) ----------
+
+def test_layer_importance_sums_to_layers_times_heads_times_queries():
+    rng = np.random.default_rng(11)
+    L, T, hq, hkv, d, N = 3, 5, 4, 2, 16, 40
+    qs = [rng.standard_normal((T, hq, d)) for _ in range(L)]
+    Ks = [rng.standard_normal((N, hkv, d)) for _ in range(L)]
+    kpos, qpos = 7 + np.arange(N), 50 + np.arange(T)
+    per, tot = method.score_layers_request(qs, qpos, Ks, kpos, 1e4)
+    assert per.shape == (L, N) and tot.shape == (N,)
+    np.testing.assert_allclose(per.sum(axis=1), np.full(L, hq * T), atol=1e-11)
+    assert abs(tot.sum() - L * hq * T) < 1e-10
+
+
+def test_layer_importance_of_identical_layers_is_l_times_one_layer_and_zero_query_is_uniform():
+    rng = np.random.default_rng(12)
+    T, hq, hkv, d, N = 3, 2, 1, 8, 24
+    q = rng.standard_normal((T, hq, d))
+    K = rng.standard_normal((N, hkv, d))
+    kpos, qpos = np.arange(N), N + np.arange(T)
+    one = method.score_request(q, qpos, K, kpos, 1e4)
+    per, tot = method.score_layers_request([q] * 4, qpos, [K] * 4, kpos, 1e4)
+    np.testing.assert_allclose(tot, 4 * one, rtol=1e-14)
+    # a layer whose query is zero spreads its weight evenly: hq*T/N per token (closed form)
+    per, tot = method.score_layers_request([q, np.zeros_like(q)], qpos, [K, K], kpos, 1e4)
+    np.testing.assert_allclose(per[1], np.full(N, hq * T / N), atol=1e-13)
+    np.testing.assert_allclose(tot, one + hq * T / N, rtol=1e-13)
+
+
+def test_layer_importance_pairs_each_query_with_its_own_layers_keys():
+    # two-key worked example per layer (d = 2, positions 0): layer 0 scores 0 and ln 3 (weights
+    # 1/4, 3/4), layer 1 the keys swapped (3/4, 1/4); taking layer 0's keys for both layers, or
+    # layer 1's query for both, changes the per-layer rows
+    q = np.array([[[math.sqrt(2.0), 0.0]]])
+    K0 = np.array([[[0.0, 0.0]], [[math.log(3.0), 0.0]]])
+    K1 = K0[::-1].copy()
+    per, tot = method.score_layers_request([q, q], np.array([0]), [K0, K1], np.array([0, 0]), 1e4)
+    np.testing.assert_allclose(per, [[0.25, 0.75], [0.75, 0.25]], atol=1e-15)
+    np.testing.assert_allclose(tot, [1.0, 1.0], atol=1e-15)
+    q2 = np.array([[[0.0, 0.0]]])     # layer 1's query carries no preference: weights 1/2, 1/2
+    per, _ = method.score_layers_request([q, q2], np.array([0]), [K0, K1], np.array([0, 0]), 1e4)
+    np.testing.assert_allclose(per, [[0.25, 0.75], [0.5, 0.5]], atol=1e-15)
+
+
 # ---------- top-k ----------
 
 def _brute_topk(vals, k):
