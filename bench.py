@@ -399,6 +399,15 @@ def run_op(args, pcf, b, L, cf, k_pool, dev, world, rank, local):
     per_call = 1
     if args.op == "key_norms":
         call = lambda: pcf.key_norms(L, k_pool, norms)
+    elif args.op == "score_layers":
+        from workload import layer_inputs
+        qs, ks = layer_inputs(b, args.layers)
+        qs, ks = [t.to(dev) for t in qs], [t.to(dev) for t in ks]
+        per = torch.empty((args.layers, max(1, L.total_tokens)), dtype=torch.float32, device=dev)
+        tot = torch.empty(max(1, L.total_tokens), dtype=torch.float32, device=dev)
+        call = lambda: pcf.score_layers(L, qs, ks, cf.rope, per, tot, cf.ws_score)
+        hw = L.host.numpy()   # per layer: rotation, LSE pass, importance pass (layout words 19, 20)
+        per_call = int(args.layers * (1 + int(hw[19] > 0) + int(hw[20] > 0)) + 1)
     elif args.op == "topn_global":
         call = lambda: pcf.select_topn_global(L, norms, cf.sel_idx, cf.excl, cf.row_pos)
     else:
@@ -429,6 +438,15 @@ def run_op(args, pcf, b, L, cf, k_pool, dev, world, rank, local):
         roof = {"bound": "tensor", "achieved": tf / world, "peak": peak, "unit": "TFLOP/s", "frac": tf / world / peak,
                 "peak_source": src + " bf16 burst", "traffic": None, "algorithmic_flops_per_launch": probe_flops,
                 "offline_anchor_pass_us": offline()}
+    elif args.op == "score_layers":
+        # one Q K^T per layer: 2*Hq*T*N*d flops per request (the implementation's two passes issue
+        # twice that; both are reported)
+        flops = float(args.layers * sum(2 * b.hq * r.n_query * r.n_cached * b.d for r in b.requests))
+        tf = flops / (ms / 1e3) / 1e12
+        metric, value, unit, hib = f"all-layer scoring ({args.layers} layers) time per call", ms * 1e3, "us", False
+        roof = {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                "issued_tflops": 2 * tf, "issued_frac": 2 * tf / peak, "peak_source": src + " bf16 burst",
+                "traffic": None, "algorithmic_flops_per_launch": flops}
     elif args.op == "key_norms":
         nbytes = L.total_tokens * (b.hkv * b.d * 2 + 4)     # every cached key read once, one fp32 out
         gbs = world * nbytes / (ms / 1e3) / 1e9
@@ -448,7 +466,8 @@ def run_op(args, pcf, b, L, cf, k_pool, dev, world, rank, local):
             "vs_baseline": None, "dtype": {"key_norms": "f32", "topn_global": "u32"}.get(args.op, "bf16"),
             "data": "synthetic",
             "config": {"workload": f"{args.config}: {DESCR[args.config]}", "tokens": L.total_tokens,
-                       "l2": "flushed between timed calls (512 MB write)"},
+                       "l2": "flushed between timed calls (512 MB write)",
+                       **({"layers": args.layers} if args.op == "score_layers" else {})},
             "roofline": roof, "gpu_launches": K * per_call, "clocks": clk,
         }))
 
@@ -463,9 +482,11 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", default="step",
-                    choices=["step", "key_norms", "topn_global", "anchor_probe", "layer_prefetch"],
-                    help="step: the hot path (default); key_norms / topn_global / anchor_probe: one "
-                         "of the variants alone, on the workload's layout")
+                    choices=["step", "key_norms", "topn_global", "anchor_probe", "layer_prefetch",
+                             "score_layers"],
+                    help="step: the hot path (default); key_norms / topn_global / anchor_probe / "
+                         "score_layers: one of the variants alone, on the workload's layout")
+    ap.add_argument("--layers", type=int, default=4, help="score_layers: layers scored per call")
     ap.add_argument("--anchor-pct", type=int, default=6,
                     help="anchor_probe: anchors per span, percent of its tokens in whole pages")
     args = ap.parse_args()

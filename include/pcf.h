@@ -144,6 +144,20 @@ pcf_status pcf_score_workspace_bytes(const int32_t* layout_host, size_t* bytes);
 pcf_status pcf_score(const pcf_layout* layout, const uint16_t* q_query, const uint16_t* k_pool,
                      const float* rope, float* importance, void* ws, size_t ws_bytes, void* stream);
 
+/* Importance at every layer instead of one critical layer (QCFuse section 4 "Resultados": the
+ * all-layer method QCAll the critical layer is compared with; the last layer alone is QCLast).
+ * For each layer l: importance_layers[l][:] = pcf_score of layer l's query q_query_layers[l] over
+ * layer l's key pool k_pool_layers[l] (same layout, positions and rope table at every layer);
+ * then importance_sum[j] = sum over l of importance_layers[l][j], added in layer order in fp32
+ * (the pages name no rule for combining layers; the sum ranks tokens like the mean).
+ * q_query_layers / k_pool_layers: host arrays of n_layers (1 .. 4096) device pointers, each laid
+ * out as for pcf_score; importance_layers [n_layers][total_tokens] and importance_sum
+ * [total_tokens] fp32, device, 16-byte aligned.  ws: the scoring workspace
+ * (pcf_score_workspace_bytes), reused layer after layer on `stream`.  Deterministic. */
+pcf_status pcf_score_layers(const pcf_layout* layout, int32_t n_layers, const uint16_t* const* q_query_layers,
+                            const uint16_t* const* k_pool_layers, const float* rope, float* importance_layers,
+                            float* importance_sum, void* ws, size_t ws_bytes, void* stream);
+
 /* Per-span Top-k (QCFuse 2B "Top-N tokens", taken per span).  For every span s of request b:
  * the k_s request-local token indices with the largest importance, ties to the lower index,
  * written in ascending order to sel_idx[sel_base_b + offset of s ...].  Also writes
@@ -260,6 +274,17 @@ pcf_status pcf_score_noalloc(const pcf_layout* layout, const uint16_t* q_query, 
  * the usual activation range) raises PCF_ERR_DEVICE_RANGE instead of being clamped silently, and
  * the results of that call must be discarded. */
 pcf_status pcf_check_device_error(void* stream);
+
+/* Check of the failure-detection path (the pages have no counterpart: a library self-test).
+ * Every wait of the library's kernels is bounded; when one runs out, the kernel raises an abort
+ * flag and the device error word, drains what it has in flight and returns.  This call launches a
+ * one-thread-block kernel whose only work is such a wait, with a limit of `limit_cycles` GPU clock
+ * cycles (1000 .. 2e8, about 0.1 s at most), on a barrier that nothing ever arrives on.  The wait
+ * gives up, so flag[0] (device int32) becomes 1 and the next pcf_check_device_error returns
+ * PCF_ERR_DEVICE_TIMEOUT; the device stays usable.  flag[0] == 2 would mean the wait returned
+ * without its arrival.  Errors: PCF_ERR_INVALID_ARG for a limit out of range or a null or
+ * misaligned flag; PCF_ERR_NO_DEVICE. */
+pcf_status pcf_wait_limit_check(int64_t limit_cycles, int32_t* flag, void* stream);
 
 /* Queues `n` asynchronous copies on `stream`, in order: copy i moves bytes[i] bytes from src[i]
  * to dst[i] with one cudaMemcpyAsync of kind cudaMemcpyDefault (the direction follows from the

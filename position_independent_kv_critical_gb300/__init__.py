@@ -23,7 +23,8 @@ from ._lib import PcfError  # noqa: F401
 
 __all__ = ["Layout", "CacheFusion", "PcfError", "k_from_percent", "rope_table", "score", "select_topk",
            "gather_rows", "fused_attention", "check_device_error", "load_library", "score_noalloc",
-           "select_topn_global", "key_norms", "pack_anchor_pages", "prefetch_pool_pages"]
+           "select_topn_global", "key_norms", "pack_anchor_pages", "prefetch_pool_pages",
+           "wait_limit_check", "score_layers"]
 
 
 def load_library():
@@ -144,6 +145,25 @@ def score(layout: Layout, q_query, k_pool, rope, importance, ws, stream=None):
         ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def score_layers(layout: Layout, q_layers, k_layers, rope, importance_layers, importance_sum, ws,
+                 stream=None):
+    """Importance at every layer (``q_layers[l]`` over ``k_layers[l]``) into
+    ``importance_layers[l]`` and their sum over the layers into ``importance_sum``."""
+    if len(q_layers) != len(k_layers) or not q_layers:
+        raise ValueError("q_layers and k_layers: one tensor per layer, at least one layer")
+    for t in list(q_layers) + list(k_layers):
+        _need(t, torch.bfloat16, "layer input")
+    _need(rope, torch.float32, "rope")
+    _need(importance_layers, torch.float32, "importance_layers")
+    _need(importance_sum, torch.float32, "importance_sum")
+    n = len(q_layers)
+    qp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in q_layers])
+    kp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in k_layers])
+    _lib.check("pcf_score_layers", _lib.load().pcf_score_layers(
+        ctypes.byref(layout.ref), n, qp, kp, _p(rope), _p(importance_layers), _p(importance_sum), _p(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def score_noalloc(layout: Layout, q_query, k_pool, rope, importance, stream=None):
     """``score`` with the library's built-in scratch array instead of a workspace (no allocation)."""
     _need(q_query, torch.bfloat16, "q_query")
@@ -229,6 +249,14 @@ def fused_attention(layout: Layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, e
         handles.append(ctypes.c_void_p(ev.cuda_event))
     _lib.check("pcf_fused_attention_timed", _lib.load().pcf_fused_attention_timed(
         *args, handles[0], handles[1], _stream(stream)))
+
+
+def wait_limit_check(limit_cycles: int, flag, stream=None):
+    """Launch the bounded-wait check kernel (a wait that gives up after ``limit_cycles``); the next
+    ``check_device_error`` then raises PcfError with PCF_ERR_DEVICE_TIMEOUT."""
+    _need(flag, torch.int32, "flag")
+    _lib.check("pcf_wait_limit_check", _lib.load().pcf_wait_limit_check(
+        int(limit_cycles), _p(flag), _stream(stream)))
 
 
 def check_device_error(stream=None):

@@ -31,6 +31,7 @@ EXPORTS = (
     "pcf_select_topk", "pcf_gather_rows", "pcf_attention_workspace_bytes", "pcf_fused_attention",
     "pcf_check_device_error", "pcf_score_noalloc", "pcf_copy_async", "pcf_select_topn_global",
     "pcf_key_norms", "pcf_pack_anchor_pages", "pcf_prefetch_pool_pages", "pcf_fused_attention_timed",
+    "pcf_wait_limit_check", "pcf_score_layers",
 )
 
 
@@ -81,6 +82,9 @@ def _declare(lib):
         getattr(lib, fn).argtypes = [c_void_p, P(c_size_t)]
     lib.pcf_score.restype = c_int32
     lib.pcf_score.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.pcf_score_layers.restype = c_int32
+    lib.pcf_score_layers.argtypes = [P(LayoutRef), c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_size_t, c_void_p]
     lib.pcf_select_topk.restype = c_int32
     lib.pcf_select_topk.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     lib.pcf_select_topn_global.restype = c_int32
@@ -101,6 +105,8 @@ def _declare(lib):
     lib.pcf_score_noalloc.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     lib.pcf_check_device_error.restype = c_int32
     lib.pcf_check_device_error.argtypes = [c_void_p]
+    lib.pcf_wait_limit_check.restype = c_int32
+    lib.pcf_wait_limit_check.argtypes = [c_int64, c_void_p, c_void_p]
     lib.pcf_copy_async.restype = c_int32
     lib.pcf_copy_async.argtypes = [c_int32, c_void_p, c_void_p, c_void_p, c_void_p]
 

@@ -632,4 +632,51 @@ __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict_
     *reinterpret_cast<uint4*>(out + ((int64_t)out_row * Hq + kvh * g + hl) * D + 8 * c) = o;
 }
 
+// ------------------------------------------------------------------ layer sum
+// All-layer importance: out[j] = sum over l of per_layer[l][j], added in layer order (fp32,
+// deterministic).  Four tokens per thread (16-byte loads); a tail of n % 4 tokens is done by the
+// first threads one at a time.
+__global__ void __launch_bounds__(256) layer_sum_kernel(const float* __restrict__ per_layer, int32_t n_layers,
+                                                        int64_t n, float* __restrict__ out) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t n4 = n / 4;
+    if (gid < n4) {
+        float4 acc = reinterpret_cast<const float4*>(per_layer)[gid];
+        for (int l = 1; l < n_layers; ++l) {
+            const float4 v = reinterpret_cast<const float4*>(per_layer + (int64_t)l * n)[gid];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        reinterpret_cast<float4*>(out)[gid] = acc;
+    } else if (gid - n4 < n - 4 * n4) {
+        const int64_t j = 4 * n4 + (gid - n4);
+        float acc = per_layer[j];
+        for (int l = 1; l < n_layers; ++l) acc += per_layer[(int64_t)l * n + j];
+        out[j] = acc;
+    }
+}
+
+// ------------------------------------------------------------------ bounded-wait check
+// Exercises the library's bounded mbarrier wait where it gives up: one thread initialises a
+// barrier that expects one arrival, which never comes, and waits on it with a limit of `limit`
+// clock cycles.  The wait runs out, raises the CTA's abort flag and the device error word
+// (timeout), and the kernel returns: no copies, MMAs or tensor memory are involved, so there is
+// nothing to drain.  Lane 0 records in flag[0] whether the wait returned false (1) or, against
+// all expectation, true (2).
+__global__ void __launch_bounds__(32) wait_limit_check_kernel(long long limit, int32_t* flag) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_word;
+    grid_dep_wait();
+    grid_dep_launch();
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        abort_word = 0;
+        const bool done = mbar_wait(&bar, 0, reinterpret_cast<volatile int*>(&abort_word), limit);
+        flag[0] = done ? 2 : 1;
+    }
+    __syncwarp();
+}
+
 }  // namespace pcf

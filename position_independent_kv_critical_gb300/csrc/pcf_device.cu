@@ -433,6 +433,40 @@ extern "C" pcf_status pcf_score(const pcf_layout* layout, const uint16_t* q_quer
                          : score_impl<64>(layout, q_query, k_pool, rope, importance, ws, st);
 }
 
+extern "C" pcf_status pcf_score_layers(const pcf_layout* layout, int32_t n_layers,
+                                       const uint16_t* const* q_query_layers, const uint16_t* const* k_pool_layers,
+                                       const float* rope, float* importance_layers, float* importance_sum, void* ws,
+                                       size_t ws_bytes, void* stream) {
+    pcf_status s = check_layout(layout);
+    if (s != PCF_OK) return s;
+    const int32_t* H = layout->host;
+    if (n_layers < 1 || n_layers > 4096 || !q_query_layers || !k_pool_layers) return PCF_ERR_INVALID_ARG;
+    if (H[L_TOTAL_TOKENS] == 0) return PCF_OK;
+    if (!rope || !importance_layers || !importance_sum || !ws) return PCF_ERR_INVALID_ARG;
+    if (!aligned16(rope) || !aligned16(ws) || !aligned16(importance_layers) || !aligned16(importance_sum))
+        return PCF_ERR_INVALID_ARG;
+    for (int l = 0; l < n_layers; ++l) {
+        const uint16_t* q = q_query_layers[l];
+        const uint16_t* k = k_pool_layers[l];
+        if (!k || !aligned16(k) || (H[L_TOTAL_QUERY] > 0 && (!q || !aligned16(q)))) return PCF_ERR_INVALID_ARG;
+    }
+    if (ws_bytes < score_ws(H).total) return PCF_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_device()) != PCF_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t n = H[L_TOTAL_TOKENS];
+    // layer by layer on the stream (the workspace is reused: each layer's kernels start after the
+    // previous layer's have finished with it)
+    for (int l = 0; l < n_layers; ++l) {
+        float* imp = importance_layers + (int64_t)l * n;
+        s = H[L_D] == 128 ? score_impl<128>(layout, q_query_layers[l], k_pool_layers[l], rope, imp, ws, st)
+                          : score_impl<64>(layout, q_query_layers[l], k_pool_layers[l], rope, imp, ws, st);
+        if (s != PCF_OK) return s;
+    }
+    const int64_t threads = n / 4 + n % 4;
+    return launch(layer_sum_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st,
+                  (const float*)importance_layers, n_layers, n, importance_sum);
+}
+
 extern "C" pcf_status pcf_select_topk(const pcf_layout* layout, const float* importance, int32_t* sel_idx,
                                       uint16_t* excl, int32_t* row_pos, void* stream) {
     pcf_status s = check_layout(layout);
@@ -611,6 +645,15 @@ extern "C" pcf_status pcf_prefetch_pool_pages(const pcf_layout* layout, const ui
             return PCF_ERR_CUDA;
     }
     return PCF_OK;
+}
+
+extern "C" pcf_status pcf_wait_limit_check(int64_t limit_cycles, int32_t* flag, void* stream) {
+    if (limit_cycles < 1000 || limit_cycles > 200000000LL || !flag || (reinterpret_cast<uintptr_t>(flag) & 3u))
+        return PCF_ERR_INVALID_ARG;
+    pcf_status s = check_device();
+    if (s != PCF_OK) return s;
+    return launch(wait_limit_check_kernel, dim3(1), dim3(32), 0, static_cast<cudaStream_t>(stream),
+                  (long long)limit_cycles, flag);
 }
 
 extern "C" pcf_status pcf_check_device_error(void* stream) {

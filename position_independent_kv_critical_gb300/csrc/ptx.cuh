@@ -88,14 +88,15 @@ __device__ __forceinline__ uint32_t mbar_test_wait(uint64_t* bar, uint32_t parit
 }
 
 // Bounded wait for the phase of `parity` to complete.  Returns false (and raises the CTA's abort
-// flag plus the device error word) when the limit runs out or another role already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// flag plus the device error word) when `limit` cycles run out or another role already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          long long limit = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             *abort_flag = 1;
             set_dev_error(kDevErrTimeout);
             return false;

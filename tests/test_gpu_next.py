@@ -264,3 +264,52 @@ def test_two_layer_pipeline_matches_resident_pools():
         outs.append(gb.attention().copy())
     for l in range(2):
         assert np.array_equal(outs[l], ref[l]), l
+
+
+# ------------------------------------------------------------------ all-layer importance (QCAll)
+
+@pytest.mark.parametrize("name,n_layers", [("tiny", 3), ("llama8b_layer", 4), ("long_context", 4)])
+def test_all_layer_importance_matches_oracle(name, n_layers):
+    from workload import layer_inputs
+    b = make_batch(name)
+    gb = GpuBatch(b)
+    qs, ks = layer_inputs(b, n_layers)
+    qd = [t.cuda() for t in qs]
+    kd = [t.cuda() for t in ks]
+    n = gb.L.total_tokens
+    per = torch.full((n_layers, n), float("nan"), dtype=torch.float32, device="cuda")
+    tot = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda")
+    pcf.score_layers(gb.L, qd, kd, gb.rope, per, tot, gb.cf.ws_score)
+    pcf.check_device_error()
+    per_h, tot_h = per.cpu().numpy(), tot.cpu().numpy()
+    # the sum is the layers' fp32 values added in layer order
+    acc = per_h[0].copy()
+    for l in range(1, n_layers):
+        acc += per_h[l]
+    assert np.array_equal(tot_h, acc)
+    r = b.requests[0]
+    K_l, kpos = [], None
+    for k in ks:
+        K, _, kpos = method.request_cached(r.spans, k.double().numpy(), b.v_pool.double().numpy())
+        K_l.append(K)
+    qpos = r.query_pos0 + np.arange(r.n_query)
+    exp_per, exp_tot = method.score_layers_request([q.double().numpy() for q in qs], qpos, K_l, kpos, b.theta)
+    for l in range(n_layers):
+        err = np.abs(per_h[l, : r.n_cached] - exp_per[l])
+        assert np.all(err <= 1e-3 * np.abs(exp_per[l]) + 1e-7), f"layer {l}: max rel {(err / exp_per[l]).max():.2e}"
+    err = np.abs(tot_h[: r.n_cached] - exp_tot)
+    assert np.all(err <= 1e-3 * np.abs(exp_tot) + 1e-7)
+    # layer 0 is the critical-layer call itself
+    assert np.array_equal(per_h[0], gb.score())
+
+
+def test_all_layer_importance_of_one_layer_is_the_critical_layer_score():
+    b = make_batch("llama8b_layer")
+    gb = GpuBatch(b)
+    n = gb.L.total_tokens
+    per = torch.empty((1, n), dtype=torch.float32, device="cuda")
+    tot = torch.empty((n,), dtype=torch.float32, device="cuda")
+    pcf.score_layers(gb.L, [gb.q_query], [gb.k_pool], gb.rope, per, tot, gb.cf.ws_score)
+    pcf.check_device_error()
+    one = gb.score()
+    assert np.array_equal(per[0].cpu().numpy(), one) and np.array_equal(tot.cpu().numpy(), one)

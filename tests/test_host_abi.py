@@ -296,3 +296,33 @@ def test_variant_layouts_build_with_the_expected_totals():
                    max(r.n_sel + r.n_query for r in anchors) + 1, device="cpu")
     assert P.total_tokens == A.total_sel and P.total_sel == 0
     assert P.total_rows == sum(r.n_query for r in reqs)
+
+
+def test_wait_limit_check_validates_on_the_host(lib):
+    """The bounded-wait check rejects limits outside [1000, 2e8] cycles and a null or misaligned
+    flag before looking for a device."""
+    PCF_ERR_INVALID_ARG = -1
+    flag = torch.zeros(2, dtype=torch.int32)
+    p = flag.data_ptr()
+    assert lib.pcf_wait_limit_check(999, ctypes.c_void_p(p), None) == PCF_ERR_INVALID_ARG
+    assert lib.pcf_wait_limit_check(200000001, ctypes.c_void_p(p), None) == PCF_ERR_INVALID_ARG
+    assert lib.pcf_wait_limit_check(100000, None, None) == PCF_ERR_INVALID_ARG
+    assert lib.pcf_wait_limit_check(100000, ctypes.c_void_p(p + 2), None) == PCF_ERR_INVALID_ARG
+
+
+def test_score_layers_validates_on_the_host(lib):
+    """All-layer scoring rejects a layer count outside [1, 4096], missing pointer arrays and a
+    null layer pool before looking for a device."""
+    PCF_ERR_INVALID_ARG = -1
+    b = small_custom_batch([(0, 2, 0, 3)], n_query=4)
+    L = pcf.Layout(b.requests, b.hq, b.hkv, b.d, b.n_phys_pages, 4096, device="cpu")
+    ref = ctypes.byref(L.ref)
+    buf = torch.zeros(4096, dtype=torch.float32)
+    p = ctypes.c_void_p(buf.data_ptr())
+    arr = (ctypes.c_void_p * 2)(buf.data_ptr(), buf.data_ptr())
+    nul = (ctypes.c_void_p * 2)(buf.data_ptr(), None)
+    assert lib.pcf_score_layers(ref, 0, arr, arr, p, p, p, p, 1 << 20, None) == PCF_ERR_INVALID_ARG
+    assert lib.pcf_score_layers(ref, 4097, arr, arr, p, p, p, p, 1 << 20, None) == PCF_ERR_INVALID_ARG
+    assert lib.pcf_score_layers(ref, 2, None, arr, p, p, p, p, 1 << 20, None) == PCF_ERR_INVALID_ARG
+    assert lib.pcf_score_layers(ref, 2, arr, nul, p, p, p, p, 1 << 20, None) == PCF_ERR_INVALID_ARG
+    assert lib.pcf_score_layers(ref, 2, arr, arr, p, None, p, p, 1 << 20, None) == PCF_ERR_INVALID_ARG

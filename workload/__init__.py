@@ -258,6 +258,17 @@ def make_batch(cfg_name: str, pct: Optional[int] = None) -> Batch:
                                     cfg.seed)
 
 
+def layer_inputs(b: Batch, n_layers: int):
+    """Per-layer scoring inputs for all-layer importance: layer 0 is the batch's own query and key
+    pool, layer l >= 1 draws both anew (query seed + 1000 + 2l, keys seed + 1001 + 2l), same shapes
+    and positions.  Returns (query list, key-pool list), CPU bf16."""
+    qs, ks = [b.q_query], [b.k_pool]
+    for l in range(1, n_layers):
+        qs.append(_randn_bf16(tuple(b.q_query.shape), b.seed + 1000 + 2 * l))
+        ks.append(_randn_bf16(tuple(b.k_pool.shape), b.seed + 1001 + 2 * l))
+    return qs, ks
+
+
 def hidden_rows(tok: torch.Tensor, row_elems: int) -> torch.Tensor:
     """Deterministic stand-in for per-token hidden states, evaluable for any token subset on any
     device: value(tok, col) = ((tok*131 + col*7) mod 512 - 256) / 64, exact in bf16."""
