@@ -487,6 +487,9 @@ def main():
                     help="step: the hot path (default); key_norms / topn_global / anchor_probe / "
                          "score_layers: one of the variants alone, on the workload's layout")
     ap.add_argument("--layers", type=int, default=4, help="score_layers: layers scored per call")
+    ap.add_argument("--paged", action="store_true",
+                    help="step: fused attention through pcf_fused_attention_paged (cached K/V read from the "
+                         "pool pages, keys rotated in the kernel)")
     ap.add_argument("--anchor-pct", type=int, default=6,
                     help="anchor_probe: anchors per span, percent of its tokens in whole pages")
     args = ap.parse_args()
@@ -507,7 +510,7 @@ def main():
     L = pcf.Layout(b.requests, b.hq, b.hkv, b.d, b.n_phys_pages, max_pos, device=str(dev))
     rope = pcf.rope_table(b.d, b.theta, max_pos).to(dev)
     D = b.hq * b.d
-    cf = pcf.CacheFusion(L, rope, row_elems=D, device=str(dev))
+    cf = pcf.CacheFusion(L, rope, row_elems=D, device=str(dev), paged=args.paged)
     g = lambda t: t.to(dev)
     k_pool, v_pool = g(b.k_pool), g(b.v_pool)
     q_query, q_fresh, k_fresh, v_fresh = g(b.q_query), g(b.q_fresh), g(b.k_fresh), g(b.v_fresh)
@@ -528,7 +531,7 @@ def main():
 
     def attn():
         pcf.fused_attention(L, q_fresh, k_fresh, v_fresh, k_pool, v_pool, cf.excl, cf.row_pos, rope, cf.out,
-                            cf.ws_attn)
+                            cf.ws_attn, paged=args.paged)
 
     for _ in range(max(3, args.warmup)):
         front()
@@ -585,7 +588,7 @@ def main():
         flush.zero_()
         front()
         pcf.fused_attention(L, q_fresh, k_fresh, v_fresh, k_pool, v_pool, cf.excl, cf.row_pos, rope, cf.out,
-                            cf.ws_attn, kernel_events=(evk[i][0], evk[i][1]))
+                            cf.ws_attn, kernel_events=(evk[i][0], evk[i][1]), paged=args.paged)
     torch.cuda.synchronize()
     pcf.check_device_error()
     kernel_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evk)
@@ -636,17 +639,23 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.config}: {DESCR[args.config]}",
                    "recompute_pct": args.pct if args.pct is not None else CONFIGS[args.config].pct,
-                   "tokens_per_step": tokens, "l2": "flushed between timed steps (512 MB write)"},
-        "roofline": {"bound": "tensor", "kernel": "attn_kernel (fused attention, persistent tcgen05)",
+                   "tokens_per_step": tokens, "l2": "flushed between timed steps (512 MB write)",
+                   **({"attention": "paged"} if args.paged else {})},
+        "roofline": {"bound": "tensor",
+                     "kernel": "attn_kernel (fused attention, persistent tcgen05" +
+                               (", paged: pool pages, keys rotated in shared memory)" if args.paged else ")"),
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": src + " bf16 burst", "frac_of_sustained": achieved / peak_sus if peak_sus else None,
                      "traffic": _recorded_traffic(args.config), "traffic_unit": "bytes per launch (ncu DRAM read+write)",
                      "algorithmic_flops_per_launch": flops, "ms_per_launch": kernel_ms,
                      "timing": "CUDA events recorded on the launching stream right before and after the attention "
                                "kernel's launch (pcf_fused_attention_timed), mean over a pass of the same steps",
-                     "call": {"what": "pcf_fused_attention: compaction scan + rotation pass + attention kernel + "
-                                      "split merge", "ms": a_ms, "achieved": achieved_call,
-                              "frac": achieved_call / peak}},
+                     "call": {"what": ("pcf_fused_attention_paged: page scan + fresh-row rotation + attention "
+                                       "kernel + split merge" if args.paged else
+                                       "pcf_fused_attention: compaction scan + rotation pass + attention kernel + "
+                                       "split merge"), "ms": a_ms, "achieved": achieved_call,
+                              "frac": achieved_call / peak,
+                              "workspace_bytes": int(cf.ws_attn.numel())}},
         "breakdown_ms": {"score": statistics.mean(score_ms), "topk_gather": statistics.mean(topk_gather_ms),
                          "attention": a_ms},
         "score_tflops": score_flops / (statistics.mean(score_ms) / 1e3) / 1e12,

@@ -232,16 +232,40 @@ pcf_status pcf_fused_attention(const pcf_layout* layout, const uint16_t* q_fresh
                                const uint16_t* excl, const int32_t* row_pos, const float* rope,
                                uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
-/* pcf_fused_attention with two caller-created CUDA events (cudaEvent_t, non-NULL, else
- * PCF_ERR_INVALID_ARG) recorded on `stream` right before and right after the attention kernel's
- * launch, for timing that kernel alone (its cudaEventElapsedTime).  An event between two kernels
- * ends their programmatic launch overlap, so a timed call runs slightly slower than an untimed
- * one. */
+/* Bytes of device workspace pcf_fused_attention_paged needs for this layout: the rotated fresh rows
+ * (Q and K), per-page counters and the split-merge partials -- it grows with the batch's rows, not
+ * with its cached tokens. */
+pcf_status pcf_attention_paged_workspace_bytes(const int32_t* layout_host, size_t* bytes);
+
+/* The same fused attention as pcf_fused_attention (same arguments, result within the same
+ * tolerances, same errors), computed without any copy of the cached keys or values (MiniPIC 2.1,
+ * "Implementation": the cos/sin lookup and fused multiply-adds sit in the attention kernel;
+ * "Benefit": one block serves concurrent requests at different offsets without duplication).
+ * The kernel copies each cached tile's pool pages (through the block table) straight into shared
+ * memory, rotates the keys there to the request's positions before the tensor-core contraction,
+ * and writes each recomputed token's fresh key and value over its stale cached copy in place.
+ * ws: >= pcf_attention_paged_workspace_bytes bytes (rotated fresh rows and split partials only),
+ * against pcf_attention_workspace_bytes, which also holds a rotated copy of the batch's kept
+ * cached keys with their values.  The rotation runs on the SMs' arithmetic units beside the
+ * softmax, once per tile and query-tile pair, so the kernel takes about twice as long as the one
+ * behind pcf_fused_attention on GB300; it is meant for callers whose device memory cannot hold
+ * the per-request copy. */
+pcf_status pcf_fused_attention_paged(const pcf_layout* layout, const uint16_t* q_fresh, const uint16_t* k_fresh,
+                                     const uint16_t* v_fresh, const uint16_t* k_pool, const uint16_t* v_pool,
+                                     const uint16_t* excl, const int32_t* row_pos, const float* rope,
+                                     uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+/* pcf_fused_attention (paged == 0) or pcf_fused_attention_paged (paged != 0, ws sized by
+ * pcf_attention_paged_workspace_bytes) with two caller-created CUDA events (cudaEvent_t, non-NULL,
+ * else PCF_ERR_INVALID_ARG) recorded on `stream` right before and right after the attention
+ * kernel's launch, for timing that kernel alone (its cudaEventElapsedTime).  An event between two
+ * kernels ends their programmatic launch overlap, so a timed call runs slightly slower than an
+ * untimed one. */
 pcf_status pcf_fused_attention_timed(const pcf_layout* layout, const uint16_t* q_fresh, const uint16_t* k_fresh,
                                      const uint16_t* v_fresh, const uint16_t* k_pool, const uint16_t* v_pool,
                                      const uint16_t* excl, const int32_t* row_pos, const float* rope, uint16_t* out,
                                      void* ws, size_t ws_bytes, void* ev_kernel_start, void* ev_kernel_stop,
-                                     void* stream);
+                                     int32_t paged, void* stream);
 
 /* Largest scoring workspace pcf_score_noalloc can serve (16 MiB), i.e. the size of the scratch
  * array built into the library. */

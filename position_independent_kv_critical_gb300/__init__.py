@@ -134,6 +134,12 @@ class Layout:
             ctypes.c_void_p(self.host.data_ptr()), ctypes.byref(v)))
         return int(v.value)
 
+    def attention_paged_workspace_bytes(self) -> int:
+        v = ctypes.c_size_t(0)
+        _lib.check("pcf_attention_paged_workspace_bytes", _lib.load().pcf_attention_paged_workspace_bytes(
+            ctypes.c_void_p(self.host.data_ptr()), ctypes.byref(v)))
+        return int(v.value)
+
 
 def score(layout: Layout, q_query, k_pool, rope, importance, ws, stream=None):
     _need(q_query, torch.bfloat16, "q_query")
@@ -230,16 +236,19 @@ def gather_rows(layout: Layout, sel_idx, src, dst, stream=None):
 
 
 def fused_attention(layout: Layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope,
-                    out, ws, stream=None, kernel_events=None):
-    """``kernel_events``: optional (start, stop) torch.cuda.Event pair recorded around the attention
-    kernel alone (pcf_fused_attention_timed)."""
+                    out, ws, stream=None, kernel_events=None, paged=False):
+    """``paged``: the variant that reads cached K/V straight from the pool pages and rotates the
+    keys in the kernel (pcf_fused_attention_paged; ``ws`` sized by
+    ``Layout.attention_paged_workspace_bytes``).  ``kernel_events``: optional (start, stop)
+    torch.cuda.Event pair recorded around the attention kernel alone (pcf_fused_attention_timed)."""
     for t, n in ((q_fresh, "q_fresh"), (k_fresh, "k_fresh"), (v_fresh, "v_fresh"), (k_pool, "k_pool"),
                  (v_pool, "v_pool"), (out, "out")):
         _need(t, torch.bfloat16, n)
     args = (ctypes.byref(layout.ref), _p(q_fresh), _p(k_fresh), _p(v_fresh), _p(k_pool), _p(v_pool),
             _p(excl), _p(row_pos), _p(rope), _p(out), _p(ws), ws.numel() * ws.element_size())
     if kernel_events is None:
-        _lib.check("pcf_fused_attention", _lib.load().pcf_fused_attention(*args, _stream(stream)))
+        fn = "pcf_fused_attention_paged" if paged else "pcf_fused_attention"
+        _lib.check(fn, getattr(_lib.load(), fn)(*args, _stream(stream)))
         return
     st = torch.cuda.current_stream() if stream is None else stream
     handles = []
@@ -248,7 +257,7 @@ def fused_attention(layout: Layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, e
             ev.record(st)
         handles.append(ctypes.c_void_p(ev.cuda_event))
     _lib.check("pcf_fused_attention_timed", _lib.load().pcf_fused_attention_timed(
-        *args, handles[0], handles[1], _stream(stream)))
+        *args, handles[0], handles[1], int(bool(paged)), _stream(stream)))
 
 
 def wait_limit_check(limit_cycles: int, flag, stream=None):
@@ -264,20 +273,24 @@ def check_device_error(stream=None):
 
 
 class CacheFusion:
-    """Buffers for one batch on one device plus the four calls of the hot path in order."""
+    """Buffers for one batch on one device plus the four calls of the hot path in order.
+    ``paged=True`` runs the fused attention through pcf_fused_attention_paged (no copy of the
+    cached keys and values; a workspace that grows with the rows only)."""
 
     def __init__(self, layout: Layout, rope_dev: torch.Tensor, row_elems: int = 0,
-                 device: str = "cuda"):
+                 device: str = "cuda", paged: bool = False):
         L = layout
         self.layout = L
         self.rope = rope_dev
+        self.paged = paged
         self.importance = torch.empty(max(1, L.total_tokens), dtype=torch.float32, device=device)
         self.sel_idx = torch.empty(max(1, L.total_sel), dtype=torch.int32, device=device)
         self.excl = torch.zeros(max(1, L.total_pages), dtype=torch.int16, device=device)
         self.row_pos = torch.empty(max(1, L.total_rows), dtype=torch.int32, device=device)
         self.out = torch.empty((max(1, L.total_rows), L.hq, L.d), dtype=torch.bfloat16, device=device)
         self.ws_score = torch.empty(max(16, L.score_workspace_bytes()), dtype=torch.uint8, device=device)
-        self.ws_attn = torch.empty(max(16, L.attention_workspace_bytes()), dtype=torch.uint8, device=device)
+        ws_attn = L.attention_paged_workspace_bytes() if paged else L.attention_workspace_bytes()
+        self.ws_attn = torch.empty(max(16, ws_attn), dtype=torch.uint8, device=device)
         self.gathered = (torch.empty((max(1, L.total_sel), row_elems), dtype=torch.bfloat16, device=device)
                          if row_elems else None)
 
@@ -288,7 +301,7 @@ class CacheFusion:
         if hidden is not None and self.gathered is not None:
             gather_rows(L, self.sel_idx, hidden, self.gathered, stream)
         fused_attention(L, q_fresh, k_fresh, v_fresh, k_pool, v_pool, self.excl, self.row_pos,
-                        self.rope, self.out, self.ws_attn, stream)
+                        self.rope, self.out, self.ws_attn, stream, paged=self.paged)
         return self.out
 
     def step_from_host(self, q_query_h, q_fresh_h, k_fresh_h, v_fresh_h, k_pool, v_pool, out_h, sel_h,
@@ -350,7 +363,7 @@ class CacheFusion:
             gather_rows(L, self.sel_idx, hidden, self.gathered)
         main.wait_event(self._ev_fresh[i])
         fused_attention(L, qf, kf, vf, k_pool, v_pool, self.excl, self.row_pos, self.rope, self.out,
-                        self.ws_attn)
+                        self.ws_attn, paged=self.paged)
         self._ev_used[i].record(main)
         self._d2h.wait_event(self._ev_used[i])
         copies([out_h, sel_h], [self.out, self.sel_idx],

@@ -52,7 +52,11 @@
 
 namespace pcf {
 
-constexpr int kAttnThreads = 448;   // 14 warps: at most 4 per SM sub-partition (128 registers)
+// 14 warps (at most 4 per SM sub-partition, so each may hold 128+ registers); the paged variant
+// adds two rotator warps (16 warps, 128 registers each)
+constexpr int kAttnThreads = 448;
+constexpr int kAttnThreadsPaged = 512;
+template <bool PAGED> constexpr int attn_threads() { return PAGED ? kAttnThreadsPaged : kAttnThreads; }
 constexpr int kWarpSoftB = 4;
 constexpr int kWarpMma = 8;
 constexpr int kWarpTma = 9;
@@ -60,14 +64,17 @@ constexpr int kWarpTmaV = 10;
 constexpr int kWarpMmaB = 11;
 constexpr int kWarpPvA = 12;
 constexpr int kWarpPvB = 13;
+constexpr int kWarpRot = 14;        // warps 14 and 15: rotation of the cached key tiles
+constexpr int kRotThreads = 64;
 constexpr int kNoPos = 0x7FFFFFFF;
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr uint32_t kTmemO = 256;     // O_A at 256, O_B at 384
+constexpr int kStageRows = 32;       // fresh keys of a tile's recomputed tokens staged with the tile
 
 struct AttnParams {
     const int32_t* layout;
-    const int32_t* kpos_c;     // attention: logical position of every compacted cached key
+    const int32_t* kpos_c;     // attention (compacted): logical position of every compacted cached key
     const int32_t* row_pos;    // attention: logical position of every row
     __nv_bfloat16* out;        // attention: [rows][Hq][D]
     float2* lse_part;          // LSE: (running max in log2 units, running sum); per request
@@ -75,6 +82,13 @@ struct AttnParams {
     __nv_bfloat16* part_o;     // attention with a split key range: normalized partial O per slot
     float2* part_ml;           //   and its (running max, running sum) per row
     int32_t* sched;            // items handed out beyond the first gridDim.x; zero on entry
+    // paged attention only:
+    const uint16_t* excl;      // recompute bits per logical page
+    const int32_t* cidx;       // per logical page, the request's kept tokens before it (plus the
+                               //   request's base R_CBASE)
+    const __half* k_rot;       // rotated fresh keys [Hkv][rows][D] fp16
+    const __nv_bfloat16* v_fresh;   // fresh values [rows][Hkv][D]
+    const float2* rope;        // (cos, sin) table [max_pos][D/2]
 };
 
 // One item as the scheduler hands it to the other roles.
@@ -90,10 +104,12 @@ struct AttnItem {
     int32_t cbase;             // first compacted cached key of the request
     int32_t nsplit, slot_base; // attention: key-range splits of the pair and its first partial slot
     int32_t lse_base, lse_chunks;   // LSE: the request's partials and its chunks
-    int32_t pad[4];
+    int32_t page_base;         // first logical page of the request (block table, positions, bits)
+    int32_t n_pages, n_sel;    // the request's cached pages and recomputed tokens
+    int32_t pad;
 };
 
-template <int D, bool LSE>
+template <int D, bool LSE, bool PAGED = false>
 struct AttnSmem {
     static constexpr int kHalves = D / 64;
     static constexpr int kQ = kTileRows * D * 2;          // one Q tile
@@ -102,23 +118,36 @@ struct AttnSmem {
     static constexpr int oQ = 0;
     static constexpr int oK = oQ + kQTilesPerCta * kQ;
     static constexpr int oV = oK + kKStages * kK;
-    static constexpr int oKpos = oV + kVStages * kV;
-    static constexpr int oBar = oKpos + kKStages * kTileKeys * 4;
-    static constexpr int kNumBars = 38;
+    // attention: per K stage, the fresh rotated keys of the tile's recomputed tokens (a block of
+    // consecutive fresh rows, kStageRows of them, copied with the tile) and per page of the tile
+    // its recompute bits and the rank of its first recomputed token
+    static constexpr int kKst = PAGED ? kStageRows * D * 2 : 0;
+    static constexpr int oKst = oV + kVStages * kV;
+    static constexpr int oKpos = oKst + kKStages * kKst;
+    static constexpr int oMeta = oKpos + kKStages * kTileKeys * 4;   // (paged: 64 bytes a stage)
+    // attention: per K stage, the (cos, sin) table rows the rotators start from: for each page of
+    // the tile and each run of 2*D/16 of its keys, the row at the run's first position
+    static constexpr int kRope = PAGED ? kPagesPerTile * 32 * 16 : 0;   // 32 float4 per page: 4 KB
+    static constexpr int oRope = oMeta + kKStages * kPagesPerTile * 8;
+    // attention: each softmax thread's output pointers, kept here across the tile loop
+    static constexpr int oPark = oRope + kKStages * kRope;
+    static constexpr int oBar = oPark + (PAGED ? 256 * 16 : 0);
+    static constexpr int kNumBars = 42;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int oItem = oMisc + 64;
     static constexpr int kBytes = oItem + 2 * (int)sizeof(AttnItem);
     static constexpr int kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
+    static_assert(kAlloc <= 232448, "more dynamic shared memory than a GB300 block can have");
     static constexpr uint32_t kTmemCols = 512;   // LSE: 2 tiles x 2 S buffers of 128 columns
 };
 
 // barrier slots
 enum : int {
     B_Q_FULL = 0,      // the item's Q tiles landed (one phase per item)
-    B_K_FULL = 1,      // [2] rotated K tile landed
+    B_K_FULL = 1,      // [2] the stage holds the rotated fp16 K tile (every rotator thread arrives)
     B_K_EMPTY = 3,     // [2] both Q K^T that read the stage are done (one commit per issuer)
     B_KPOS_FREE = 5,   // [2] both softmax groups are done with the stage's key positions (256 arrivals)
-    B_V_FULL = 7,      // [2]
+    B_V_FULL = 7,      // [2] the stage holds the V tile, recomputed tokens' rows replaced (V warp)
     B_V_EMPTY = 9,     // [2] both P V that read the stage are done (one commit per issuer)
     B_S_FULL = 11,     // [4] per (Q tile, S half-buffer): S = Q K^T of a 64-key half landed (LSE:
                        //     of a whole key tile, per 128-column buffer)
@@ -131,25 +160,33 @@ enum : int {
     B_O_FREE = 30,     // [2] per Q tile: the softmax group has read the item's O (128 arrivals)
     B_ITEM_FULL = 32,  // [2] item slot written by the scheduler
     B_ITEM_EMPTY = 34, // [2] every consumer role has read the slot
-    B_KPOS_FULL = 36   // [2] the K tile's key positions written (every producer lane)
+    B_KPOS_FULL = 36,  // [2] the K tile's key positions written (every producer lane)
+    B_KRAW_FULL = 38,  // [2] the K tile's copy landed (TMA; the rotators then make it B_K_FULL)
+    B_VRAW_FULL = 40   // [2] the V tile's copy landed (TMA; the V producer then makes it B_V_FULL)
 };
 
-template <int D, bool LSE>
-__global__ void __launch_bounds__(kAttnThreads)
+template <int D, bool LSE, bool PAGED>
+__global__ void __launch_bounds__(attn_threads<PAGED>())
 attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kcache,
             const __grid_constant__ CUtensorMap tm_vcache, const __grid_constant__ CUtensorMap tm_kfresh,
-            const __grid_constant__ CUtensorMap tm_vfresh, const AttnParams prm) {
-    using SM = AttnSmem<D, LSE>;
+            const __grid_constant__ CUtensorMap tm_vfresh, const __grid_constant__ CUtensorMap tm_kstage,
+            const AttnParams prm) {
+    static_assert(!(LSE && PAGED), "the scoring pass reads the rotated copy");
+    using SM = AttnSmem<D, LSE, PAGED>;
     constexpr int H = SM::kHalves;
     // slot readers: lane 0 of the 8 softmax warps and of the 2 Q K^T issuers (+ 2 P V issuers and
     // the V producer outside LSE mode)
-    constexpr int kItemReaders = LSE ? 10 : 13;
+    // (paged: and lane 0 of the two rotator warps)
+    constexpr int kItemReaders = LSE ? 10 : (PAGED ? 15 : 13);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     auto sQ = [&](int t) { return smem + SM::oQ + t * SM::kQ; };
     auto sKs = [&](int st) { return smem + SM::oK + st * SM::kK; };
     auto sVs = [&](int st) { return smem + SM::oV + st * SM::kV; };
     auto sKpos = [&](int st) { return reinterpret_cast<int32_t*>(smem + SM::oKpos) + st * kTileKeys; };
+    auto sKst = [&](int st) { return smem + SM::oKst + st * SM::kKst; };
+    auto sMeta = [&](int st) { return reinterpret_cast<int2*>(smem + SM::oMeta) + st * kPagesPerTile; };
+    auto sRope = [&](int st) { return reinterpret_cast<float4*>(smem + SM::oRope + st * SM::kRope); };
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::oBar);
     int32_t* misc = reinterpret_cast<int32_t*>(smem + SM::oMisc);
     // misc: [0] tmem base, [4] abort
@@ -167,13 +204,15 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         mbar_init(&bars[B_Q_FULL], 1);
         mbar_init(&bars[B_Q_EMPTY], kQTilesPerCta);
         for (int s2 = 0; s2 < kKStages; ++s2) {
-            mbar_init(&bars[B_K_FULL + s2], 1);
+            mbar_init(&bars[B_KRAW_FULL + s2], 1);
+            mbar_init(&bars[B_K_FULL + s2], PAGED ? kRotThreads : 1);
             mbar_init(&bars[B_KPOS_FULL + s2], 32);
             mbar_init(&bars[B_K_EMPTY + s2], kQTilesPerCta);
             mbar_init(&bars[B_KPOS_FREE + s2], 256);
         }
         for (int s2 = 0; s2 < kVStages; ++s2) {
-            mbar_init(&bars[B_V_FULL + s2], 1);
+            mbar_init(&bars[B_VRAW_FULL + s2], 1);
+            mbar_init(&bars[B_V_FULL + s2], PAGED ? 32 : 1);
             mbar_init(&bars[B_V_EMPTY + s2], kQTilesPerCta);
         }
         for (int t = 0; t < kQTilesPerCta; ++t) {
@@ -202,7 +241,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tmem_alloc(reinterpret_cast<uint32_t*>(misc), SM::kTmemCols);
         tmem_relinquish();
     }
-    // (every K and V stage is filled by whole-tile copies: rows past a tensor's end read as 0)
+    // (every K and V stage is filled whole: a cached tile by eight page copies, a page past the
+    // request's last repeating that last page; a query-row tile by one copy whose rows past the
+    // tensor's end read as 0; keys that are not there carry position kNoPos and are masked)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -221,6 +262,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             prefetch_tmap(&tm_kcache);
             if (!LSE) prefetch_tmap(&tm_kfresh);
         }
+        const int Hkv = L[L_HKV];
         int kc = 0;                                   // K tiles this CTA issued before the item
         int last_k[kKStages] = {-1, -1}, last_q = -1;  // for the final drain
         bool ok = true;
@@ -234,7 +276,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             w.kvh = w.qpair = w.chunk = w.n_ct = w.n_ft = w.t0 = w.jb = w.n_loc = 0;
             w.n_rows = w.row_base = w.cbase = w.nsplit = w.slot_base = 0;
             w.lse_base = w.lse_chunks = 0;
-            w.pad[0] = w.pad[1] = 0;
+            w.page_base = w.n_pages = w.n_sel = w.pad = 0;
             const int32_t* R = L;
             if (idx < n_items) {
                 const int32_t* item = items + kItemWords * idx;
@@ -246,6 +288,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 w.n_rows = LSE ? R[R_N_QUERY] : R[R_N_ROWS];
                 w.row_base = R[R_ROW_BASE];
                 w.cbase = R[R_CBASE];
+                w.page_base = R[R_PAGE_BASE];
+                w.n_pages = R[R_N_PAGES];
+                w.n_sel = R[R_N_SEL];
                 if (LSE) {
                     // LSE: tiles of all the request's cached tokens, cut into chunks
                     const int nkt = R[R_N_KTILES], chunks = R[R_LSE_CHUNKS];
@@ -256,23 +301,38 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     w.lse_base = R[R_LSE_BASE];
                     w.lse_chunks = chunks;
                 } else {
-                    // visible tiles: key positions increase along the compacted cached tiles and
-                    // along the fresh rows, so each count is the number of tiles whose first key
-                    // is at or before the pair's last row (the lanes test 32 tiles at a time)
-                    const int n_rows_req = R[R_N_ROWS];
+                    // visible tiles: key positions increase along the cached tiles and along the
+                    // fresh tiles, so each count is the number of tiles whose first key is at or
+                    // before the pair's last row (the lanes test 32 tiles at a time).  Compacted:
+                    // the cached tiles hold the kept cached keys and the fresh tiles every row of
+                    // the request.  Paged: the cached tiles are the request's pool pages, a
+                    // recomputed token's fresh key sitting in its cached copy's place, and only
+                    // the query rows form fresh tiles.
+                    const int n_rows_req = R[R_N_ROWS], n_sel = R[R_N_SEL];
                     const int32_t row_base = R[R_ROW_BASE];
                     const int row0 = w.qpair * kQTilesPerCta * toks_per_tile;
                     const int nrow = min(kQTilesPerCta * toks_per_tile, n_rows_req - row0);
-                    const int nkt = (R[R_N_PAGES] * kPage - R[R_N_SEL] + kTileKeys - 1) / kTileKeys;
                     const int32_t pmax = nrow > 0 ? prm.row_pos[row_base + row0 + nrow - 1] : -1;
-                    const int nft_total = (n_rows_req + kTileKeys - 1) / kTileKeys;
-                    const int32_t* kpc = prm.kpos_c + R[R_CBASE];
                     int nct = 0, nft = 0;
-                    for (int b = 0; b < nkt; b += 32)
-                        nct += __popc(__ballot_sync(0xffffffffu, b + lane < nkt && kpc[(b + lane) * kTileKeys] <= pmax));
-                    for (int b = 0; b < nft_total; b += 32)
-                        nft += __popc(__ballot_sync(0xffffffffu, b + lane < nft_total &&
-                                                                     prm.row_pos[row_base + (b + lane) * kTileKeys] <= pmax));
+                    if (PAGED) {
+                        const int nkt = (R[R_N_PAGES] + kPagesPerTile - 1) / kPagesPerTile;
+                        const int nft_total = (n_rows_req - n_sel + kTileKeys - 1) / kTileKeys;
+                        const int32_t* pp = L + L[L_OFF_PAGEPOS] + R[R_PAGE_BASE];
+                        for (int b = 0; b < nkt; b += 32)
+                            nct += __popc(__ballot_sync(0xffffffffu, b + lane < nkt && pp[(b + lane) * kPagesPerTile] <= pmax));
+                        for (int b = 0; b < nft_total; b += 32)
+                            nft += __popc(__ballot_sync(0xffffffffu, b + lane < nft_total &&
+                                                                         prm.row_pos[row_base + n_sel + (b + lane) * kTileKeys] <= pmax));
+                    } else {
+                        const int nkt = (R[R_N_PAGES] * kPage - n_sel + kTileKeys - 1) / kTileKeys;
+                        const int nft_total = (n_rows_req + kTileKeys - 1) / kTileKeys;
+                        const int32_t* kpc = prm.kpos_c + R[R_CBASE];
+                        for (int b = 0; b < nkt; b += 32)
+                            nct += __popc(__ballot_sync(0xffffffffu, b + lane < nkt && kpc[(b + lane) * kTileKeys] <= pmax));
+                        for (int b = 0; b < nft_total; b += 32)
+                            nft += __popc(__ballot_sync(0xffffffffu, b + lane < nft_total &&
+                                                                         prm.row_pos[row_base + (b + lane) * kTileKeys] <= pmax));
+                    }
                     const int32_t* PR = L + L[L_OFF_PAIR] + (R[R_PAIR_BASE] + w.qpair) * P_STRIDE;
                     const int n_all = nct + nft, ns = PR[P_NSPLIT];
                     w.n_ct = nct;
@@ -296,36 +356,68 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const int n_rows_req = LSE ? R[R_N_QUERY] : R[R_N_ROWS];
             const int32_t row_base = R[R_ROW_BASE];
             const int row0 = w.qpair * kQTilesPerCta * toks_per_tile;
-            const int32_t kc_row0 = LSE ? w.kvh * L[L_TOTAL_TOKENS] + R[R_TOK_BASE]
-                                        : w.kvh * L[L_TOTAL_VALID] + R[R_CBASE];
-            const int32_t kf_row0 = w.kvh * L[L_TOTAL_ROWS] + row_base;
-            // key positions, which only the softmax waits for: lane l holds those of keys l, l+32,
-            // l+64, l+96 of a tile (kNoPos for a missing key), loaded one tile ahead; the first
-            // tile's are requested now, before the wait for the Q buffer
-            const int n_ct = w.n_ct, n_tiles = w.n_ct + w.n_ft;
-            const int n_kept = R[R_N_PAGES] * kPage - R[R_N_SEL];
-            const int32_t* page_pos = L + L[L_OFF_PAGEPOS] + R[R_PAGE_BASE];
-            auto meta = [&](int j, int32_t (&pos)[4]) {
+            const int32_t kc_row0 = LSE ? w.kvh * L[L_TOTAL_TOKENS] + R[R_TOK_BASE] : 0;
+            // first fresh row of the fresh tiles: paged, the request's first query row; compacted, its
+            // first row
+            const int32_t fbase = PAGED ? w.n_sel : 0;
+            const int32_t kf_row0 = w.kvh * L[L_TOTAL_ROWS] + row_base + fbase;
+            const int n_qrows = n_rows_req - fbase;
+            const int n_kept = w.n_pages * kPage - w.n_sel;   // compacted cached keys of the request
+            // key positions, which only the softmax waits for, and the pool rows of a cached tile's
+            // pages: lane l holds the positions of keys 4l .. 4l+3 of a tile (kNoPos for a missing
+            // key) and, for l < 8, the first pool row of page l of the tile (a page past the
+            // request's last copies that last page instead: finite data whose keys are masked).
+            // Loaded one tile ahead; the first tile's are requested now, before the Q buffer wait.
+            const int n_ct = w.n_ct;
+            const int32_t* page_pos = L + L[L_OFF_PAGEPOS] + w.page_base;
+            const int32_t* blk = L + L[L_OFF_BLOCK] + w.page_base;
+            // For a cached tile of the attention, lane l < 8 also loads page l's recompute bits and
+            // the rank (among the request's recomputed tokens) of its first recomputed token.
+            // It also loads 128 bytes of the tile's table rows: lane l takes 8 of the 32 float4 of
+            // page l / 4 (the rows at the page's first position and, for d = 64, 8 positions on).
+            auto meta = [&](int j, int32_t (&pos)[4], int32_t& prow, uint32_t& ex, int32_t& sel, float4 (&tr)[8]) {
+                prow = 0;
+                ex = 0u;
+                sel = 0;
+                if (j < n_ct && !LSE && !PAGED) {
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int key = lane + 32 * r;
-                    pos[r] = kNoPos;
-                    if (j < n_ct) {
-                        if (LSE) {
-                            const int lp = (w.t0 + j) * kPagesPerTile + key / kPage;
-                            if (lp < R[R_N_PAGES]) pos[r] = page_pos[lp] + key % kPage;
-                        } else {
-                            const int ci = j * kTileKeys + key;
-                            if (ci < n_kept) pos[r] = prm.kpos_c[R[R_CBASE] + ci];
+                    for (int r = 0; r < 4; ++r) {
+                        const int ci = j * kTileKeys + 4 * lane + r;
+                        pos[r] = ci < n_kept ? prm.kpos_c[w.cbase + ci] : kNoPos;
+                    }
+                } else if (j < n_ct) {
+                    const int pg = (w.t0 + j) * kPagesPerTile;
+                    const int lp = pg + lane / 4;   // keys 4l .. 4l+3 lie in page l / 4 of the tile
+                    const int32_t p0 = lp < w.n_pages ? page_pos[lp] : kNoPos;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) pos[r] = lp < w.n_pages ? p0 + (4 * lane + r) % kPage : kNoPos;
+                    if (PAGED) {
+                        constexpr int F4 = D / 4;                 // float4 per table row
+                        const int f0 = (lane % 4) * 8;            // this lane's first float4 of the page
+                        const int32_t row = page_pos[lp < w.n_pages ? lp : w.n_pages - 1] + (f0 / F4) * (2 * D / 16);
+                        const float4* src = reinterpret_cast<const float4*>(prm.rope + (int64_t)row * (D / 2)) + f0 % F4;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) tr[q] = src[q];
+                    }
+                    if (PAGED && lane < kPagesPerTile) {
+                        prow = (blk[min(pg + lane, w.n_pages - 1)] * Hkv + w.kvh) * kPage;
+                        if (pg + lane < w.n_pages) {
+                            ex = prm.excl[w.page_base + pg + lane];
+                            sel = kPage * (pg + lane) - (prm.cidx[w.page_base + pg + lane] - w.cbase);
                         }
-                    } else if (j < n_tiles) {
-                        const int fr = (j - n_ct) * kTileKeys + key;
-                        if (fr < n_rows_req) pos[r] = prm.row_pos[row_base + fr];
+                    }
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int fr = (j - n_ct) * kTileKeys + 4 * lane + r;   // fresh row from fbase on
+                        pos[r] = fr < n_qrows ? prm.row_pos[row_base + fbase + fr] : kNoPos;
                     }
                 }
             };
-            int32_t pos_n[4];
-            if (w.n_loc > 0) meta(w.jb, pos_n);
+            int32_t pos_n[4], prow_n = 0, sel_n = 0;
+            uint32_t ex_n = 0;
+            float4 tr_n[8];
+            if (w.n_loc > 0) meta(w.jb, pos_n, prow_n, ex_n, sel_n, tr_n);
             // the item's Q tiles, once both Q K^T issuers are done with the previous item's
             if (lane == 0) {
                 const int32_t qy = LSE ? (w.kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE] + row0) * g
@@ -346,39 +438,63 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            // its K tiles: lane 0 issues the copy as soon as the stage is free (the Q K^T wait only
-            // for it); then the lanes write the tile's key positions
+            // its K tiles: the copies start as soon as the stage is free (the rotators wait only for
+            // them); then the lanes write the tile's key positions
             for (int jj = 0; jj < w.n_loc; ++jj, ++kc) {
                 const int j = w.jb + jj, ks = kc & 1;
+                // paged: the copy lands on the rotators' barrier; otherwise the rotated copy is the
+                // operand itself
+                uint64_t* raw = &bars[(PAGED ? B_KRAW_FULL : B_K_FULL) + ks];
+                const bool paged = PAGED && j < n_ct;
+                // a cached tile holding recomputed tokens also brings their fresh keys: the block of
+                // kStageRows fresh rows from the tile's first recomputed token on
+                const bool stage_fresh = paged && __ballot_sync(0xffffffffu, lane < kPagesPerTile && ex_n != 0u) != 0u;
+                const int32_t sel_first = __shfl_sync(0xffffffffu, sel_n, 0);
                 if (lane == 0) {
                     ok = kc < kKStages || (mbar_wait(&bars[B_K_EMPTY + ks], ((kc >> 1) - 1) & 1, abort_flag) &&
                                            mbar_wait(&bars[B_KPOS_FREE + ks], ((kc >> 1) - 1) & 1, abort_flag));
-                    if (ok) {
-                        uint64_t* full = &bars[B_K_FULL + ks];
-                        mbar_arrive_expect_tx(full, H * 16384);
-                        const CUtensorMap* map = j < n_ct ? &tm_kcache : &tm_kfresh;
-                        const int32_t y = j < n_ct ? kc_row0 + (w.t0 + j) * kTileKeys : kf_row0 + (j - n_ct) * kTileKeys;
-                        for (int hb = 0; hb < H; ++hb) tma_load_2d(sKs(ks) + hb * 16384, map, full, hb * 64, y);
-                    }
+                    if (ok) mbar_arrive_expect_tx(raw, H * 16384 + (stage_fresh ? SM::kKst : 0));
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
-                last_k[ks] = kc;
+                if (paged) {
+                    // the tile's eight pool pages, 16 rows of this kv head each: lane 8*hb + m copies
+                    // half hb of page m into its 2 KB slice of the stage
+                    const int m = lane % kPagesPerTile, hb = lane / kPagesPerTile;
+                    const int32_t y = __shfl_sync(0xffffffffu, prow_n, m);
+                    if (lane < kPagesPerTile * H)
+                        tma_load_2d(sKs(ks) + hb * 16384 + m * (kPage * 128), &tm_kcache, raw, hb * 64, y);
+                    if (stage_fresh && lane == 0)
+                        for (int hb2 = 0; hb2 < H; ++hb2)
+                            tma_load_2d(sKst(ks) + hb2 * (kStageRows * 128), &tm_kstage, raw, hb2 * 64,
+                                        w.kvh * L[L_TOTAL_ROWS] + row_base + sel_first);
+                    if (lane < kPagesPerTile) sMeta(ks)[lane] = make_int2((int)ex_n, sel_n);
 #pragma unroll
-                for (int r = 0; r < 4; ++r) sKpos(ks)[lane + 32 * r] = pos_n[r];
+                    for (int q = 0; q < 8; ++q) sRope(ks)[lane * 8 + q] = tr_n[q];
+                } else if (lane == 0) {
+                    const CUtensorMap* map = j < n_ct ? &tm_kcache : &tm_kfresh;
+                    const int32_t yc = LSE ? kc_row0 + (w.t0 + j) * kTileKeys
+                                           : w.kvh * L[L_TOTAL_VALID] + w.cbase + j * kTileKeys;
+                    const int32_t y = j < n_ct ? yc : kf_row0 + (j - n_ct) * kTileKeys;
+                    for (int hb = 0; hb < H; ++hb) tma_load_2d(sKs(ks) + hb * 16384, map, raw, hb * 64, y);
+                }
+                last_k[ks] = kc;
+                *reinterpret_cast<int4*>(sKpos(ks) + 4 * lane) = make_int4(pos_n[0], pos_n[1], pos_n[2], pos_n[3]);
                 mbar_arrive(&bars[B_KPOS_FULL + ks]);
-                if (jj + 1 < w.n_loc) meta(j + 1, pos_n);
+                if (jj + 1 < w.n_loc) meta(j + 1, pos_n, prow_n, ex_n, sel_n, tr_n);
             }
         }
         // every copy this warp started has landed before the CTA exits
         if (lane == 0) {
             if (last_q >= 0) mbar_drain(&bars[B_Q_FULL], last_q & 1);
             for (int s2 = 0; s2 < kKStages; ++s2)
-                if (last_k[s2] >= 0) mbar_drain(&bars[B_K_FULL + s2], (last_k[s2] >> 1) & 1);
+                if (last_k[s2] >= 0) mbar_drain(&bars[(PAGED ? B_KRAW_FULL : B_K_FULL) + s2], (last_k[s2] >> 1) & 1);
         }
     } else if (warp == kWarpTmaV) {
         // ------------------------------------------------------------ V producer
-        if (!LSE && lane == 0) {
+        if (!LSE && !PAGED && lane == 0) {
+            // compacted: the kept cached V rows (copied next to the compacted keys) or the fresh
+            // rows, one copy per half of a tile
             prefetch_tmap(&tm_vcache);
             prefetch_tmap(&tm_vfresh);
             int vc = 0;
@@ -409,6 +525,228 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             for (int s2 = 0; s2 < kVStages; ++s2)
                 if (last_v[s2] >= 0) mbar_drain(&bars[B_V_FULL + s2], (last_v[s2] >> 1) & 1);
+        } else if (PAGED) {
+            // paged: V tiles of the cached pages (one copy per page and half, as for K) or of the
+            // query rows.  Once a cached tile has landed, the recomputed tokens' cached V rows are
+            // overwritten with their fresh rows: lane l takes page l / 4 of the tile and a quarter
+            // of each row's 16-byte chunks.  The recompute bits are loaded one tile ahead and the
+            // first fresh rows while the tile's copy is in flight.
+            if (lane == 0) {
+                prefetch_tmap(&tm_vcache);
+                prefetch_tmap(&tm_vfresh);
+            }
+            const int Hkv = L[L_HKV];
+            constexpr int CH = D / 8;          // 16-byte chunks per row
+            constexpr int CPL = CH / 4;        // chunks per lane
+            constexpr int kPre = 2;            // fresh rows loaded ahead per lane
+            const int m = lane / 4, qtr = lane % 4;
+            int vc = 0;
+            int last_v[kVStages] = {-1, -1};
+            auto stage_row = [&](int vs, int key, int ch) {
+                return reinterpret_cast<uint4*>(sVs(vs) + (ch / 8) * 16384 + sw128_off(key, ch % 8));
+            };
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                AttnItem w;
+                ok = take_item(it, w);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_ITEM_EMPTY + (it & 1)]);
+                if (w.req < 0) break;
+                const int32_t* blk = L + L[L_OFF_BLOCK] + w.page_base;
+                auto page_bits = [&](int j, uint32_t& ex, int& sel) {
+                    ex = 0u;
+                    sel = 0;
+                    const int lp = j * kPagesPerTile + m;
+                    if (j < w.n_ct && lp < w.n_pages) {
+                        ex = prm.excl[w.page_base + lp];
+                        if (ex) sel = kPage * lp - (prm.cidx[w.page_base + lp] - w.cbase);   // recomputed before it
+                    }
+                };
+                uint32_t ex_n = 0;
+                int sel_n = 0;
+                if (w.n_loc > 0) page_bits(w.jb, ex_n, sel_n);
+                for (int jj = 0; ok && jj < w.n_loc; ++jj, ++vc) {
+                    const int j = w.jb + jj, vs = vc & 1;
+                    uint64_t* raw = &bars[B_VRAW_FULL + vs];
+                    if (lane == 0) {
+                        ok = vc < kVStages || mbar_wait(&bars[B_V_EMPTY + vs], ((vc >> 1) - 1) & 1, abort_flag);
+                        if (ok) mbar_arrive_expect_tx(raw, H * 16384);
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    if (j < w.n_ct) {
+                        const int mm = lane % kPagesPerTile, hb = lane / kPagesPerTile;
+                        if (lane < kPagesPerTile * H) {
+                            const int lq = min(j * kPagesPerTile + mm, w.n_pages - 1);
+                            tma_load_2d(sVs(vs) + hb * 16384 + mm * (kPage * 128), &tm_vcache, raw, hb * 64,
+                                        (blk[lq] * Hkv + w.kvh) * kPage);
+                        }
+                    } else if (lane == 0) {
+                        const int32_t fr = w.row_base + w.n_sel + (j - w.n_ct) * kTileKeys;
+                        for (int hb = 0; hb < H; ++hb)
+                            tma_load_3d(sVs(vs) + hb * 16384, &tm_vfresh, raw, hb * 64, w.kvh, fr);
+                    }
+                    last_v[vs] = vc;
+                    uint32_t ex = ex_n;
+                    int sel = sel_n;
+                    // the first fresh rows, and the next tile's bits, while the copy is in flight
+                    int pre_r[kPre], n_pre = 0;
+                    uint4 pre[kPre][CPL];
+#pragma unroll
+                    for (int i = 0; i < kPre; ++i) {
+                        if (ex != 0u && sel < w.n_sel) {
+                            pre_r[i] = __ffs(ex) - 1;
+                            const uint4* src = reinterpret_cast<const uint4*>(
+                                prm.v_fresh + ((int64_t)(w.row_base + sel) * Hkv + w.kvh) * D);
+#pragma unroll
+                            for (int q = 0; q < CPL; ++q) pre[i][q] = src[qtr * CPL + q];
+                            n_pre = i + 1;
+                            ex &= ex - 1u;
+                            ++sel;
+                        }
+                    }
+                    if (jj + 1 < w.n_loc) page_bits(j + 1, ex_n, sel_n);
+                    ok = mbar_wait(raw, (vc >> 1) & 1, abort_flag);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+#pragma unroll
+                    for (int i = 0; i < kPre; ++i)
+                        if (i < n_pre)
+#pragma unroll
+                            for (int q = 0; q < CPL; ++q) *stage_row(vs, kPage * m + pre_r[i], qtr * CPL + q) = pre[i][q];
+                    for (; ex != 0u; ex &= ex - 1u, ++sel) {   // rows beyond the first kPre
+                        if (sel >= w.n_sel) { set_dev_error(kDevErrBounds); break; }
+                        const int r = __ffs(ex) - 1;
+                        const uint4* src = reinterpret_cast<const uint4*>(
+                            prm.v_fresh + ((int64_t)(w.row_base + sel) * Hkv + w.kvh) * D);
+                        uint4 v[CPL];
+#pragma unroll
+                        for (int q = 0; q < CPL; ++q) v[q] = src[qtr * CPL + q];
+#pragma unroll
+                        for (int q = 0; q < CPL; ++q) *stage_row(vs, kPage * m + r, qtr * CPL + q) = v[q];
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    mbar_arrive(&bars[B_V_FULL + vs]);
+                }
+            }
+            if (lane == 0)
+                for (int s2 = 0; s2 < kVStages; ++s2)
+                    if (last_v[s2] >= 0) mbar_drain(&bars[B_VRAW_FULL + s2], (last_v[s2] >> 1) & 1);
+        }
+    } else if (PAGED && warp >= kWarpRot) {
+        // ------------------------------------------------------------ K rotation (warps 14, 15)
+        // MiniPIC 2.1: cached keys are rotated when used, to the request's logical positions.  A
+        // cached tile holds 8 pool pages; thread t rotates 16-byte chunk pair c (dimensions 8c ..
+        // 8c+7 and D/2 + 8c ..) of 2*CP consecutive keys of page m = t / 8, in place: bf16 in,
+        // rotated fp16 out.  The keys of a page sit at consecutive positions p0 + r, so the
+        // (cos, sin) pairs come from one table row (staged with the tile by the producer) and then
+        // advance by one position step -- a rotation by theta_i, itself table row 1 -- from key to
+        // key.  The arithmetic runs on packed fp32 pairs (two frequencies per instruction).  A
+        // recomputed token's cached key is then overwritten with its fresh rotated key (same
+        // position), which the producer staged with the tile as well.
+        constexpr int CP = D / 16;
+        constexpr int KPT = 2 * CP;
+        const int rt = tid - kWarpRot * 32;
+        const int m = rt / 8, c = rt % CP, r0 = ((rt % 8) / CP) * KPT;
+        const uint32_t o_hi = D == 128 ? 16384u : 0u;
+        const int c_hi = D == 128 ? c : c + 4;
+        const uint32_t st_hi = D == 128 ? (uint32_t)(kStageRows * 128) : 0u;
+        const int f4 = m * 32 + (r0 / KPT) * (D / 4) + 4 * c;   // this thread's float4 in a staged table
+        // one position step for frequencies 8c + 2e, 8c + 2e + 1: (cos, sin, -sin) as packed pairs
+        uint64_t STC[4], STS[4], NSTS[4];
+        {
+            const float4* t1 = reinterpret_cast<const float4*>(prm.rope + D / 2 + 8 * c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 v = t1[e];
+                STC[e] = f2_pack(v.x, v.z);
+                STS[e] = f2_pack(v.y, v.w);
+                NSTS[e] = f2_pack(-v.y, -v.w);
+            }
+        }
+        int kc = 0;
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+            AttnItem w;
+            ok = take_item(it, w);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_ITEM_EMPTY + (it & 1)]);
+            if (w.req < 0) break;
+            for (int jj = 0; jj < w.n_loc; ++jj, ++kc) {
+                const int j = w.jb + jj, ks = kc & 1;
+                const bool rot = j < w.n_ct;
+                ok = mbar_wait(&bars[B_KPOS_FULL + ks], (kc >> 1) & 1, abort_flag) &&
+                     mbar_wait(&bars[B_KRAW_FULL + ks], (kc >> 1) & 1, abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                if (rot) {
+                    uint8_t* stage = sKs(ks);
+                    // (cos, sin, -sin) at the first key, packed by frequency pairs
+                    uint64_t C[4], S[4], NS[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 v = sRope(ks)[f4 + e];
+                        C[e] = f2_pack(v.x, v.z);
+                        S[e] = f2_pack(v.y, v.w);
+                        NS[e] = f2_pack(-v.y, -v.w);
+                    }
+                    float big = 0.f;
+#pragma unroll 2
+                    for (int r = 0; r < KPT; ++r) {
+                        const int key = kPage * m + r0 + r;
+                        uint4* plo = reinterpret_cast<uint4*>(stage + sw128_off(key, c));
+                        uint4* phi = reinterpret_cast<uint4*>(stage + o_hi + sw128_off(key, c_hi));
+                        const uint4 a = *plo, b = *phi;
+                        const uint32_t ia[4] = {a.x, a.y, a.z, a.w}, ib[4] = {b.x, b.y, b.z, b.w};
+                        uint32_t oa[4], ob[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint64_t A = bf16x2_to_f2(ia[e]), B = bf16x2_to_f2(ib[e]);
+                            float y0, y1, z0, z1;
+                            f2_unpack(f2_fma(B, NS[e], f2_mul(A, C[e])), y0, y1);   // a cos - b sin
+                            f2_unpack(f2_fma(A, S[e], f2_mul(B, C[e])), z0, z1);    // b cos + a sin
+                            oa[e] = pack_f16x2_track(y0, y1, big);
+                            ob[e] = pack_f16x2_track(z0, z1, big);
+                        }
+                        *plo = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+                        *phi = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+                        // the next key's angles: one position further
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint64_t cn = f2_fma(S[e], NSTS[e], f2_mul(C[e], STC[e]));
+                            const uint64_t sn = f2_fma(C[e], STS[e], f2_mul(S[e], STC[e]));
+                            NS[e] = f2_fma(C[e], NSTS[e], f2_mul(NS[e], STC[e]));
+                            C[e] = cn;
+                            S[e] = sn;
+                        }
+                    }
+                    if (big > kF16Limit) set_dev_error(kDevErrRange);
+                    // recomputed tokens: their fresh keys, already rotated to the same positions
+                    const int2 pm = sMeta(ks)[m];
+                    const int32_t sel_first = sMeta(ks)[0].y;
+                    uint32_t ex = ((uint32_t)pm.x >> r0) & ((1u << KPT) - 1u);
+                    int sel = pm.y + __popc((uint32_t)pm.x & ((1u << r0) - 1u));
+                    for (; ex != 0u; ex &= ex - 1u, ++sel) {
+                        const int key = kPage * m + r0 + __ffs(ex) - 1;
+                        if (sel >= w.n_sel) { set_dev_error(kDevErrBounds); break; }
+                        const int srow = sel - sel_first;
+                        uint4 lo, hi;
+                        if (srow < kStageRows) {
+                            lo = *reinterpret_cast<const uint4*>(sKst(ks) + sw128_off(srow, c));
+                            hi = *reinterpret_cast<const uint4*>(sKst(ks) + st_hi + sw128_off(srow, c_hi));
+                        } else {   // beyond the staged block: from global memory
+                            const __half* src = prm.k_rot + ((int64_t)w.kvh * L[L_TOTAL_ROWS] + w.row_base + sel) * D;
+                            lo = *reinterpret_cast<const uint4*>(src + 8 * c);
+                            hi = *reinterpret_cast<const uint4*>(src + D / 2 + 8 * c);
+                        }
+                        *reinterpret_cast<uint4*>(stage + sw128_off(key, c)) = lo;
+                        *reinterpret_cast<uint4*>(stage + o_hi + sw128_off(key, c_hi)) = hi;
+                    }
+                    fence_proxy_async_smem();
+                }
+                mbar_arrive(&bars[B_K_FULL + ks]);
+            }
         }
     } else if (warp == kWarpMma || warp == kWarpMmaB || warp == kWarpPvA || warp == kWarpPvB) {
         // ------------------------------------------------------------ MMA issuers
@@ -549,6 +887,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         ml_slot = prm.part_ml + prow;
                     }
                 }
+            }
+            if (PAGED) {   // parked in shared memory across the tile loop, where registers are scarce
+                volatile uint64_t* park = reinterpret_cast<volatile uint64_t*>(smem + SM::oPark) + 2 * (warp * 32 + lane);
+                park[0] = reinterpret_cast<uint64_t>(out_row);
+                park[1] = reinterpret_cast<uint64_t>(ml_slot);
             }
             float m_run = -INFINITY, l_run = 0.f;
             int cut = 0;
@@ -716,6 +1059,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
             }
             if (!ok) break;
+            if (PAGED) {
+                volatile uint64_t* park = reinterpret_cast<volatile uint64_t*>(smem + SM::oPark) + 2 * (warp * 32 + lane);
+                out_row = reinterpret_cast<__nv_bfloat16*>(park[0]);
+                ml_slot = reinterpret_cast<float2*>(park[1]);
+            }
             if (ml_slot != nullptr) *ml_slot = make_float2(w.n_loc > 0 ? m_run : -INFINITY, l_run);
             if (!LSE) {
                 // if the next item is already published, start loading this row's position for it
@@ -740,7 +1088,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         uint32_t o[32];
                         tmem_ld32(tO + cc * 32, o);
                         tmem_ld_wait();
-                        if (valid) {
+                        if (out_row != nullptr) {
 #pragma unroll
                             for (int qq = 0; qq < 4; ++qq) {
                                 uint4 v;

@@ -198,6 +198,8 @@ ScoreWs score_ws(const int32_t* H) {
     return w;
 }
 
+// The compacted attention's workspace: rotated fresh rows, and the rotated copy of the kept
+// cached keys with their V rows and positions (it grows with the batch's cached tokens).
 struct AttnWs {
     size_t q, k, kc, vc, kpos, cidx, po, pml, sched, total;
 };
@@ -210,6 +212,24 @@ AttnWs attn_ws(const int32_t* H) {
     w.vc = align_up(w.kc + valid_rows * 2);
     w.kpos = align_up(w.vc + valid_rows * 2);
     w.cidx = align_up(w.kpos + (size_t)H[L_TOTAL_VALID] * sizeof(int32_t));
+    w.po = align_up(w.cidx + (size_t)H[L_TOTAL_PAGES] * sizeof(int32_t));
+    const size_t prow = (size_t)H[L_ATTN_SLOTS] * kQTilesPerCta * kTileRows;   // partial rows
+    w.pml = align_up(w.po + prow * H[L_D] * 2);
+    w.sched = align_up(w.pml + prow * sizeof(float2));   // the attention kernel's item counter
+    w.total = align_up(w.sched + sizeof(int32_t));
+    return w;
+}
+
+// The paged attention's workspace grows with the batch's rows, not with its cached tokens: the
+// cached keys and values are read from the pool pages by the attention kernel itself.
+struct PagedWs {
+    size_t q, k, cidx, po, pml, sched, total;
+};
+PagedWs paged_ws(const int32_t* H) {
+    PagedWs w;
+    w.q = 0;
+    w.k = align_up((size_t)H[L_TOTAL_ROWS] * H[L_HQ] * H[L_D] * 2);
+    w.cidx = align_up(w.k + (size_t)H[L_TOTAL_ROWS] * H[L_HKV] * H[L_D] * 2);
     w.po = align_up(w.cidx + (size_t)H[L_TOTAL_PAGES] * sizeof(int32_t));
     const size_t prow = (size_t)H[L_ATTN_SLOTS] * kQTilesPerCta * kTileRows;   // partial rows
     w.pml = align_up(w.po + prow * H[L_D] * 2);
@@ -310,12 +330,13 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
 
     if (H[L_N_LSE_ITEMS] > 0) {
         using SM = AttnSmem<D, true>;
-        auto kern = attn_kernel<D, true>;
+        auto kern = attn_kernel<D, true, false>;
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
-        AttnParams p{lay->dev, nullptr, nullptr, nullptr, lse, nullptr, nullptr, cnt + H[L_TOTAL_KTILES]};
+        AttnParams p{lay->dev, nullptr, nullptr, nullptr, lse, nullptr, nullptr, cnt + H[L_TOTAL_KTILES],
+                     nullptr, nullptr, nullptr, nullptr, rope2};
         // persistent: at most one CTA per SM, items handed out in list order
         const int grid = std::min<int>(H[L_N_LSE_ITEMS], device_sms());
-        if ((s = launch(kern, dim3(grid), dim3(kAttnThreads), SM::kAlloc, st, tq128, tkc, zero, zero, zero, p)) !=
+        if ((s = launch(kern, dim3(grid), dim3(kAttnThreads), SM::kAlloc, st, tq128, tkc, zero, zero, zero, zero, p)) !=
             PCF_OK)
             return s;
     }
@@ -382,16 +403,99 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     if ((s = make_map_2d(&tkf, k_rot, D, (uint64_t)H[L_HKV] * rows, D * 2, 128, kF16)) != PCF_OK) return s;
     if ((s = make_map_3d(&tvf, v_fresh, D, H[L_HKV], rows, 128)) != PCF_OK) return s;
 
-    using SM = AttnSmem<D, false>;
-    auto kern = attn_kernel<D, false>;
+    using SM = AttnSmem<D, false, false>;
+    auto kern = attn_kernel<D, false, false>;
     if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
     __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(base + w.po);
     float2* part_ml = reinterpret_cast<float2*>(base + w.pml);
-    AttnParams p{lay->dev, kpos_c, row_pos, reinterpret_cast<__nv_bfloat16*>(out), nullptr, part_o, part_ml, sched};
+    AttnParams p{lay->dev, kpos_c, row_pos, reinterpret_cast<__nv_bfloat16*>(out), nullptr, part_o, part_ml, sched,
+                 nullptr, nullptr, nullptr, nullptr, rope2};
     // persistent: at most one CTA per SM, items handed out in list order (largest estimate first)
     const int grid = std::min<int>(H[L_N_ATTN_ITEMS], device_sms());
     if (ev_start && cudaEventRecord(ev_start, st) != cudaSuccess) return PCF_ERR_CUDA;
-    if ((s = launch(kern, dim3(grid), dim3(kAttnThreads), SM::kAlloc, st, tq, tkc, tvc, tkf, tvf, p)) != PCF_OK)
+    CUtensorMap unused;
+    std::memset(&unused, 0, sizeof(unused));
+    if ((s = launch(kern, dim3(grid), dim3(kAttnThreads), SM::kAlloc, st, tq, tkc, tvc, tkf, tvf, unused, p)) != PCF_OK)
+        return s;
+    if (ev_stop && cudaEventRecord(ev_stop, st) != cudaSuccess) return PCF_ERR_CUDA;
+    if (H[L_N_COMB] > 0) {
+        if ((s = launch(combine_kernel<D>, dim3(H[L_N_COMB], D / 8), dim3(256), 0, st, lay->dev,
+                        (const __nv_bfloat16*)part_o, (const float2*)part_ml,
+                        reinterpret_cast<__nv_bfloat16*>(out))) != PCF_OK)
+            return s;
+    }
+    return PCF_OK;
+}
+
+template <int D>
+pcf_status paged_attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const uint16_t* k_fresh,
+                          const uint16_t* v_fresh, const uint16_t* k_pool, const uint16_t* v_pool,
+                          const uint16_t* excl, const int32_t* row_pos, const float* rope, uint16_t* out, void* ws,
+                          cudaStream_t st, cudaEvent_t ev_start = nullptr, cudaEvent_t ev_stop = nullptr) {
+    const int32_t* H = lay->host;
+    if (H[L_N_ATTN_ITEMS] == 0) {   // no attention kernel: the timing events mark an empty span
+        if (ev_start && cudaEventRecord(ev_start, st) != cudaSuccess) return PCF_ERR_CUDA;
+        if (ev_stop && cudaEventRecord(ev_stop, st) != cudaSuccess) return PCF_ERR_CUDA;
+        return PCF_OK;
+    }
+    const PagedWs w = paged_ws(H);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    __half* q_rot = reinterpret_cast<__half*>(base + w.q);
+    __half* k_rot = reinterpret_cast<__half*>(base + w.k);
+    int32_t* cidx = reinterpret_cast<int32_t*>(base + w.cidx);
+    const int g = H[L_GROUP];
+    const float2* rope2 = reinterpret_cast<const float2*>(rope);
+    const int32_t rows = H[L_TOTAL_ROWS];
+    const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_fresh), row_pos, q_rot, rows, H[L_HQ], g, scale_log2,
+               nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+    RopeJob kj{reinterpret_cast<const __nv_bfloat16*>(k_fresh), row_pos, k_rot, rows, H[L_HKV], 1, 1.f,
+               nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+    RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
+                 nullptr, 0, 4};
+    pcf_status s;
+    // per page, the request's kept tokens before it: a recomputed token's rank among the request's
+    // recomputed rows follows from it, and the attention kernel puts that fresh row in its place
+    if (H[L_TOTAL_PAGES] > 0) {
+        if ((s = launch(compact_scan_kernel, dim3(H[L_N_REQS]), dim3(kScanThreads), 0, st, lay->dev, excl, cidx)) !=
+            PCF_OK)
+            return s;
+    }
+    int32_t* sched = reinterpret_cast<int32_t*>(base + w.sched);
+    // the fresh rows (recomputed tokens and queries) are rotated once, at their row positions
+    s = launch_rope<D>(qj, kj, none, rope2, H[L_MAX_POS], st, sched, 1);
+    if (s != PCF_OK) return s;
+
+    CUtensorMap tq, tkp, tvp, tkf, tvf;
+    if ((s = make_map_2d(&tq, q_rot, D, (uint64_t)H[L_HKV] * rows * g, D * 2, 128, kF16)) != PCF_OK) return s;
+    // the pool, unrotated and read only: one page (16 rows of one kv head) per copy.  A batch
+    // without cached tokens never reads these maps: point them at the fresh rows.
+    if (H[L_TOTAL_PAGES] > 0) {
+        const uint64_t pr = (uint64_t)H[L_N_PHYS] * H[L_HKV] * kPage;
+        if ((s = make_map_2d(&tkp, k_pool, D, pr, D * 2, kPage)) != PCF_OK) return s;
+        if ((s = make_map_2d(&tvp, v_pool, D, pr, D * 2, kPage)) != PCF_OK) return s;
+    } else {
+        if ((s = make_map_2d(&tkp, k_fresh, D, (uint64_t)H[L_HKV] * rows, D * 2, kPage)) != PCF_OK) return s;
+        if ((s = make_map_2d(&tvp, v_fresh, D, (uint64_t)H[L_HKV] * rows, D * 2, kPage)) != PCF_OK) return s;
+    }
+    if ((s = make_map_2d(&tkf, k_rot, D, (uint64_t)H[L_HKV] * rows, D * 2, 128, kF16)) != PCF_OK) return s;
+    if ((s = make_map_3d(&tvf, v_fresh, D, H[L_HKV], rows, 128)) != PCF_OK) return s;
+    // the fresh keys of a cached tile's recomputed tokens, staged with the tile
+    CUtensorMap tks;
+    if ((s = make_map_2d(&tks, k_rot, D, (uint64_t)H[L_HKV] * rows, D * 2, kStageRows, kF16)) != PCF_OK) return s;
+
+    using SM = AttnSmem<D, false, true>;
+    auto kern = attn_kernel<D, false, true>;
+    if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
+    __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(base + w.po);
+    float2* part_ml = reinterpret_cast<float2*>(base + w.pml);
+    AttnParams p{lay->dev, nullptr, row_pos, reinterpret_cast<__nv_bfloat16*>(out), nullptr, part_o, part_ml, sched,
+                 excl, cidx, k_rot, reinterpret_cast<const __nv_bfloat16*>(v_fresh), rope2};
+    // persistent: at most one CTA per SM, items handed out in list order (largest estimate first)
+    const int grid = std::min<int>(H[L_N_ATTN_ITEMS], device_sms());
+    if (ev_start && cudaEventRecord(ev_start, st) != cudaSuccess) return PCF_ERR_CUDA;
+    if ((s = launch(kern, dim3(grid), dim3(kAttnThreadsPaged), SM::kAlloc, st, tq, tkp, tvp, tkf, tvf, tks, p)) !=
+        PCF_OK)
         return s;
     if (ev_stop && cudaEventRecord(ev_stop, st) != cudaSuccess) return PCF_ERR_CUDA;
     if (H[L_N_COMB] > 0) {
@@ -414,6 +518,12 @@ extern "C" pcf_status pcf_score_workspace_bytes(const int32_t* layout_host, size
 extern "C" pcf_status pcf_attention_workspace_bytes(const int32_t* layout_host, size_t* bytes) {
     if (!layout_host || !bytes || layout_host[L_MAGIC] != kMagic) return PCF_ERR_INVALID_ARG;
     *bytes = attn_ws(layout_host).total;
+    return PCF_OK;
+}
+
+extern "C" pcf_status pcf_attention_paged_workspace_bytes(const int32_t* layout_host, size_t* bytes) {
+    if (!layout_host || !bytes || layout_host[L_MAGIC] != kMagic) return PCF_ERR_INVALID_ARG;
+    *bytes = paged_ws(layout_host).total;
     return PCF_OK;
 }
 
@@ -554,7 +664,8 @@ namespace {
 pcf_status fused_attention_entry(const pcf_layout* layout, const uint16_t* q_fresh, const uint16_t* k_fresh,
                                  const uint16_t* v_fresh, const uint16_t* k_pool, const uint16_t* v_pool,
                                  const uint16_t* excl, const int32_t* row_pos, const float* rope, uint16_t* out,
-                                 void* ws, size_t ws_bytes, cudaEvent_t ev_start, cudaEvent_t ev_stop, void* stream) {
+                                 void* ws, size_t ws_bytes, cudaEvent_t ev_start, cudaEvent_t ev_stop, void* stream,
+                                 bool paged) {
     pcf_status s = check_layout(layout);
     if (s != PCF_OK) return s;
     const int32_t* H = layout->host;
@@ -570,9 +681,14 @@ pcf_status fused_attention_entry(const pcf_layout* layout, const uint16_t* q_fre
     for (const void* p : al)
         if (!aligned16(p)) return PCF_ERR_INVALID_ARG;
     if ((k_pool && !aligned16(k_pool)) || (v_pool && !aligned16(v_pool))) return PCF_ERR_INVALID_ARG;
-    if (ws_bytes < attn_ws(H).total) return PCF_ERR_WORKSPACE_TOO_SMALL;
+    if (ws_bytes < (paged ? paged_ws(H).total : attn_ws(H).total)) return PCF_ERR_WORKSPACE_TOO_SMALL;
     if ((s = check_device()) != PCF_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (paged)
+        return H[L_D] == 128 ? paged_attention_impl<128>(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl,
+                                                         row_pos, rope, out, ws, st, ev_start, ev_stop)
+                             : paged_attention_impl<64>(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl,
+                                                        row_pos, rope, out, ws, st, ev_start, ev_stop);
     return H[L_D] == 128 ? attention_impl<128>(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope,
                                                out, ws, st, ev_start, ev_stop)
                          : attention_impl<64>(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope,
@@ -585,7 +701,16 @@ extern "C" pcf_status pcf_fused_attention(const pcf_layout* layout, const uint16
                                           const uint16_t* excl, const int32_t* row_pos, const float* rope,
                                           uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
     return fused_attention_entry(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope, out, ws,
-                                 ws_bytes, nullptr, nullptr, stream);
+                                 ws_bytes, nullptr, nullptr, stream, false);
+}
+
+extern "C" pcf_status pcf_fused_attention_paged(const pcf_layout* layout, const uint16_t* q_fresh,
+                                                const uint16_t* k_fresh, const uint16_t* v_fresh,
+                                                const uint16_t* k_pool, const uint16_t* v_pool, const uint16_t* excl,
+                                                const int32_t* row_pos, const float* rope, uint16_t* out, void* ws,
+                                                size_t ws_bytes, void* stream) {
+    return fused_attention_entry(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope, out, ws,
+                                 ws_bytes, nullptr, nullptr, stream, true);
 }
 
 extern "C" pcf_status pcf_fused_attention_timed(const pcf_layout* layout, const uint16_t* q_fresh,
@@ -593,11 +718,11 @@ extern "C" pcf_status pcf_fused_attention_timed(const pcf_layout* layout, const 
                                                 const uint16_t* k_pool, const uint16_t* v_pool, const uint16_t* excl,
                                                 const int32_t* row_pos, const float* rope, uint16_t* out, void* ws,
                                                 size_t ws_bytes, void* ev_kernel_start, void* ev_kernel_stop,
-                                                void* stream) {
+                                                int32_t paged, void* stream) {
     if (!ev_kernel_start || !ev_kernel_stop) return PCF_ERR_INVALID_ARG;
     return fused_attention_entry(layout, q_fresh, k_fresh, v_fresh, k_pool, v_pool, excl, row_pos, rope, out, ws,
                                  ws_bytes, static_cast<cudaEvent_t>(ev_kernel_start),
-                                 static_cast<cudaEvent_t>(ev_kernel_stop), stream);
+                                 static_cast<cudaEvent_t>(ev_kernel_stop), stream, paged != 0);
 }
 
 extern "C" pcf_status pcf_copy_async(int32_t n, void* const* dst, const void* const* src, const size_t* bytes,

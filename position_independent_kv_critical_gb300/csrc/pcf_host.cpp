@@ -186,10 +186,11 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
     plan->total_ktiles = (int32_t)tot_kt;
 
     // Attention work units: (request, pair of 128-row query tiles), each run once per kv head.  A
-    // pair sees the tiles of taking-part cached keys (the compacted copy: recomputed tokens left
-    // out) up to its last row's position and the fresh tiles up to its last row.  Rows are selected
-    // tokens in position order, then query tokens; before the selection is known, a selected row
-    // is only known to lie inside its span, so the span's end bounds its cached tiles.
+    // pair sees the request's cached tiles (eight pages each; a recomputed token's fresh key takes
+    // its cached copy's place) up to its last row's position and the tiles of query rows up to its
+    // last row.  Rows are selected tokens in position order, then query tokens; before the
+    // selection is known, a selected row is only known to lie inside its span, so the span's end
+    // bounds its cached tiles.
     plan->pair_base.assign(n_reqs, 0);
     plan->pair_tiles.clear();
     for (int b = 0; b < n_reqs; ++b) {
@@ -202,7 +203,7 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
             cum_k.push_back(n_sel);
             cum_pages.push_back(n_pg);
         }
-        const int32_t nkt_c = cdiv(n_pg * kPage - n_sel, kTileKeys);   // compacted cached tiles
+        const int32_t nkt = cdiv(n_pg, kPagesPerTile);
         const int64_t rows = n_sel + r.n_query;
         const int64_t npairs = cdiv(rows * g, kTileRows * kQTilesPerCta);
         const int64_t toks_per_pair = (int64_t)kQTilesPerCta * (kTileRows / g);
@@ -210,12 +211,14 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
         size_t s = 0;
         for (int64_t p = 0; p < npairs; ++p) {
             const int64_t last = std::min<int64_t>((p + 1) * toks_per_pair, rows) - 1;
-            int32_t nct = nkt_c;
+            int32_t nct = nkt, nft = 0;
             if (last < n_sel) {
                 while (s + 1 < cum_k.size() && cum_k[s + 1] <= last) ++s;
-                nct = cdiv(cum_pages[s + 1] * kPage - cum_k[s + 1], kTileKeys);
+                nct = cdiv(cum_pages[s + 1], kPagesPerTile);
+            } else {
+                nft = (int32_t)((last - n_sel) / kTileKeys) + 1;
             }
-            plan->pair_tiles.push_back(nct + (int32_t)(last / kTileKeys) + 1);
+            plan->pair_tiles.push_back(nct + nft);
         }
     }
     choose_splits(plan->pair_tiles, d.n_kv_heads, kAttnCtaOverhead, kAttnCombineCost, kMaxSplits, plan->n_sms,

@@ -49,13 +49,21 @@ class GpuBatch:
                 self.cf.excl[: self.L.total_pages].cpu().numpy().view(np.uint16),
                 self.cf.row_pos[: self.L.total_rows].cpu().numpy())
 
-    def attention(self, excl=None, row_pos=None):
+    def attention(self, excl=None, row_pos=None, paged=False):
+        """The fused attention (paged: the variant that reads the pool pages and rotates in the
+        kernel, with its own, smaller workspace)."""
         ex = self.cf.excl if excl is None else torch.as_tensor(
             np.asarray(excl, dtype=np.uint16).view(np.int16)).to(self.dev)
         rp = self.cf.row_pos if row_pos is None else torch.as_tensor(
             np.asarray(row_pos, dtype=np.int32)).to(self.dev)
+        ws = self.cf.ws_attn
+        if paged:
+            if not hasattr(self, "ws_paged"):
+                self.ws_paged = torch.empty(max(16, self.L.attention_paged_workspace_bytes()), dtype=torch.uint8,
+                                            device=self.dev)
+            ws = self.ws_paged
         pcf.fused_attention(self.L, self.q_fresh, self.k_fresh, self.v_fresh, self.k_pool, self.v_pool,
-                            ex, rp, self.rope, self.cf.out, self.cf.ws_attn)
+                            ex, rp, self.rope, self.cf.out, ws, paged=paged)
         pcf.check_device_error()
         return self.cf.out[: self.L.total_rows].float().cpu().numpy()
 

@@ -39,9 +39,10 @@ def _sample_rows(n_rows, n_sel, k=48):
     return np.array(sorted(rows))
 
 
-def check_batch(gb: GpuBatch, req_ids=None, sample_rows=False, imp_only_ids=()):
+def check_batch(gb: GpuBatch, req_ids=None, sample_rows=False, imp_only_ids=(), paged=False):
     """Importance, top-k and attention of the requests `req_ids` (all by default) against the
-    oracle; `imp_only_ids` are further requests whose importance alone is compared."""
+    oracle; `imp_only_ids` are further requests whose importance alone is compared; `paged` runs
+    the attention through pcf_fused_attention_paged."""
     b = gb.b
     ids = list(range(len(b.requests))) if req_ids is None else list(req_ids)
     # 1) importance
@@ -73,7 +74,7 @@ def check_batch(gb: GpuBatch, req_ids=None, sample_rows=False, imp_only_ids=()):
     assert np.array_equal(excl, exp_excl)
     assert np.array_equal(row_pos, exp_rp)
     # 3) attention with the oracle's selection
-    out = gb.attention(exp_excl, exp_rp)
+    out = gb.attention(exp_excl, exp_rp, paged=paged)
     for i in ids:
         r = b.requests[i]
         rows = _sample_rows(r.n_rows, r.n_sel) if sample_rows else None

@@ -326,3 +326,34 @@ def test_score_layers_validates_on_the_host(lib):
     assert lib.pcf_score_layers(ref, 2, None, arr, p, p, p, p, 1 << 20, None) == PCF_ERR_INVALID_ARG
     assert lib.pcf_score_layers(ref, 2, arr, nul, p, p, p, p, 1 << 20, None) == PCF_ERR_INVALID_ARG
     assert lib.pcf_score_layers(ref, 2, arr, arr, p, None, p, p, 1 << 20, None) == PCF_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["concurrent_reuse", "batch70b"])
+def test_paged_attention_workspace_holds_no_copy_of_the_cached_keys(name):
+    """The paged attention keeps no copy of the cached keys or values: its workspace is the
+    compacted call's minus (at least) the rotated K and copied V of every kept cached token."""
+    from workload import CONFIGS, make_layout
+    cfg = CONFIGS[name]
+    reqs = make_layout(cfg)
+    L = pcf.Layout(reqs, cfg.hq, cfg.hkv, cfg.d, cfg.pool_spans * cfg.span_len // 16,
+                   max(r.query_pos0 + r.n_query for r in reqs) + 1, device="cpu")
+    paged, compact = L.attention_paged_workspace_bytes(), L.attention_workspace_bytes()
+    kv_copy = 2 * cfg.hkv * cfg.d * 2 * (L.total_tokens - L.total_sel)
+    assert compact - paged >= kv_copy
+
+
+def test_paged_attention_workspace_does_not_grow_with_cached_tokens():
+    """Same rows, four times the cached tokens: the compacted call's workspace grows with them; the
+    paged call's, apart from the split partials (which follow the work plan's key-range splits),
+    grows only by a 4-byte counter per page."""
+    small = small_custom_batch([(0, 8, 0, 16)], n_query=32, hq=8, hkv=2, d=128, theta=5e5, n_phys_pages=64)
+    big = small_custom_batch([(0, 32, 0, 16)], n_query=32, hq=8, hkv=2, d=128, theta=5e5, n_phys_pages=64)
+    Ls = pcf.Layout(small.requests, 8, 2, 128, 64, 4096, device="cpu")
+    Lb = pcf.Layout(big.requests, 8, 2, 128, 64, 4096, device="cpu")
+    L_ATTN_SLOTS = 34
+
+    def without_partials(L):   # 256 partial rows per slot: d bf16 values and a (max, sum) pair
+        return L.attention_paged_workspace_bytes() - int(L.host[L_ATTN_SLOTS]) * 256 * (128 * 2 + 8)
+
+    assert without_partials(Lb) <= without_partials(Ls) + 4 * (Lb.total_pages - Ls.total_pages) + 4096
+    assert Lb.attention_workspace_bytes() > 3 * Ls.attention_workspace_bytes() // 2
