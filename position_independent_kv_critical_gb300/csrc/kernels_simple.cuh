@@ -310,21 +310,39 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const int32_t* __res
 // ------------------------------------------------------------------ global Top-N
 // QCFuse section 2B read literally: one Top-N over all of a request's cached tokens, with the
 // request's budget N = sum of its spans' k (so the rows, their order and every buffer size stay
-// those of the per-span selection).  One block per request: a 4-pass 8-bit radix select of the
-// N-th largest key (fp32 bits, monotone for the non-negative importance and norms), then the
-// tokens above it and the lowest-indexed ones equal to it, written in ascending order with the
-// same outputs as topk_kernel; the block also writes the query rows' positions.
+// those of the per-span selection).  One block per request: a radix select of the N-th largest
+// key (fp32 bits, monotone for the non-negative importance and norms), then the tokens above it
+// and the lowest-indexed ones equal to it, written in ascending order with the same outputs as
+// topk_kernel; the block also writes the query rows' positions.
+// The keys of one request sit in a narrow range (importance values share their sign and most of
+// their exponent), so the select starts at the highest bit in which the request's smallest and
+// largest keys differ and takes 11-bit digits (2048 bins) from there; a request of up to
+// kTopnSmemKeys tokens keeps its keys in shared memory for all the passes.  Index order: warp w
+// owns a contiguous segment of the request and walks it 32 tokens at a time (lane l on token
+// base + l), so that loads are coalesced and shared-memory accesses conflict-free; ranks inside a
+// warp come from ballots, the warps' starting ranks from a scan of their counts, and a ballot of
+// the selected tokens is exactly one word of the bitmap.
 constexpr int kTopnThreads = 1024;
+constexpr int kTopnBins = 2048;
+constexpr int kTopnDigit = 11;
+constexpr int kTopnSmemKeys = 32768;
+
+// dynamic shared memory: [bitmap of the largest request, in 16-byte groups][its keys, if staged]
+__host__ __device__ inline size_t topn_smem_bytes(int max_tokens) {
+    return (size_t)((max_tokens + 127) / 128) * 16 + (max_tokens <= kTopnSmemKeys ? (size_t)max_tokens * 4 : 0);
+}
+
 __global__ void __launch_bounds__(kTopnThreads) topn_global_kernel(const int32_t* __restrict__ L,
                                                                    const float* __restrict__ imp,
                                                                    int32_t* __restrict__ sel_idx,
                                                                    uint16_t* __restrict__ excl,
                                                                    int32_t* __restrict__ row_pos) {
-    extern __shared__ uint32_t s_bits[];   // selected-token bitmap of the request
-    __shared__ int s_hist[256];
+    extern __shared__ __align__(16) uint32_t s_dyn[];
+    __shared__ int s_hist[kTopnBins];
     __shared__ int s_warp[kTopnThreads / 32];
+    __shared__ uint32_t s_red[2][kTopnThreads / 32];
     __shared__ int s_bucket, s_above;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     // layout fields first: they do not depend on the previous kernel, which may still be running
     const int32_t* R = L + L[L_OFF_REQ] + blockIdx.x * R_STRIDE;
     const int len = R[R_N_PAGES] * kPage;
@@ -335,92 +353,149 @@ __global__ void __launch_bounds__(kTopnThreads) topn_global_kernel(const int32_t
     const int32_t* ppos = L + L[L_OFF_PAGEPOS] + R[R_PAGE_BASE];
     uint16_t* ex = excl + R[R_PAGE_BASE];
     const int nq = R[R_N_QUERY], p0 = R[R_QUERY_POS0];
-    const int nwords = (len + 31) >> 5;
-    for (int i = tid; i < nwords; i += kTopnThreads) s_bits[i] = 0u;
+    const int max_tok = L[L_MAX_TOKENS];
+    uint32_t* s_bits = s_dyn;
+    uint32_t* s_keys = s_dyn + ((max_tok + 127) / 128) * 4;   // the host sizes the allocation alike
+    // staged when the largest request fits: the allocation follows that one
+    const bool staged = max_tok <= kTopnSmemKeys;
+    const bool partial = k > 0 && k < len;
     grid_dep_wait();
     grid_dep_launch();
     for (int t = tid; t < nq; t += kTopnThreads) row_pos[rrow + k + t] = p0 + t;
 
+    // the keys (staged), and their smallest and largest
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+    if (partial) {
+        for (int i = tid; i < len; i += kTopnThreads) {
+            const uint32_t key = order_key(v[i]);
+            if (staged) s_keys[i] = key;
+            kmin = min(kmin, key);
+            kmax = max(kmax, key);
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+            kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+        }
+        if (lane == 0) { s_red[0][wid] = kmin; s_red[1][wid] = kmax; }
+        __syncthreads();
+        kmin = s_red[0][lane];
+        kmax = s_red[1][lane];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+            kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+        }
+    }
+    auto key_at = [&](int i) { return staged ? s_keys[i] : order_key(v[i]); };
+
     uint32_t thr = 0;      // key of the k-th largest value
     int need_eq = 0;       // how many tokens equal to thr are taken (lowest indices first)
-    if (k > 0 && k < len) {
-        uint32_t prefix = 0, pmask = 0;
-        int remaining = k;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            if (tid < 256) s_hist[tid] = 0;
-            __syncthreads();
-            for (int i = tid; i < len; i += kTopnThreads) {
-                const uint32_t key = order_key(v[i]);
-                if ((key & pmask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
-            }
-            __syncthreads();
-            if (tid < 32) {
-                // lane l owns buckets 255-8l .. 248-8l (descending)
-                int cnt[8], tot = 0;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) { cnt[q] = s_hist[255 - 8 * tid - q]; tot += cnt[q]; }
-                int incl = tot;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (tid >= o) incl += y;
+    if (partial) {
+        if (kmin == kmax) {
+            thr = kmax;
+            need_eq = k;
+        } else {
+            const int hb = 31 - __clz(kmin ^ kmax);       // every key shares the bits above hb
+            uint32_t pmask = hb == 31 ? 0u : ~((2u << hb) - 1u);
+            uint32_t prefix = kmax & pmask;
+            int remaining = k;
+            for (int top = hb; top >= 0;) {
+                const int w = min(kTopnDigit, top + 1), shift = top + 1 - w;
+                const int nb = 1 << w;
+                const uint32_t dmask = (uint32_t)nb - 1u;
+                for (int b = tid; b < nb; b += kTopnThreads) s_hist[b] = 0;
+                __syncthreads();
+                for (int i = tid; i < len; i += kTopnThreads) {
+                    const uint32_t key = key_at(i);
+                    if ((key & pmask) == prefix) atomicAdd(&s_hist[(key >> shift) & dmask], 1);
                 }
-                const int excl_sum = incl - tot;
-                const bool here = excl_sum < remaining && incl >= remaining;
-                const unsigned m = __ballot_sync(0xffffffffu, here);
-                if (here && tid == __ffs(m) - 1) {
-                    int acc = excl_sum;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        if (acc + cnt[q] >= remaining) { s_bucket = 255 - 8 * tid - q; s_above = acc; break; }
-                        acc += cnt[q];
-                    }
+                __syncthreads();
+                // bins in descending order, two per thread: the bucket holding the remaining-th
+                // largest is where the count of larger keys first reaches it
+                const int b_hi = nb - 1 - 2 * tid, b_lo = b_hi - 1;
+                const int c_hi = b_hi >= 0 ? s_hist[b_hi] : 0, c_lo = b_lo >= 0 ? s_hist[b_lo] : 0;
+                const int above = block_excl_scan<kTopnThreads>(c_hi + c_lo, s_warp, nullptr);
+                if (above < remaining && above + c_hi + c_lo >= remaining) {
+                    if (above + c_hi >= remaining) { s_bucket = b_hi; s_above = above; }
+                    else { s_bucket = b_lo; s_above = above + c_hi; }
                 }
+                __syncthreads();
+                prefix |= (uint32_t)s_bucket << shift;
+                pmask |= dmask << shift;
+                remaining -= s_above;
+                top = shift - 1;
+                __syncthreads();
             }
-            __syncthreads();
-            const int bucket = s_bucket;
-            remaining -= s_above;
-            prefix |= (uint32_t)bucket << shift;
-            pmask |= 255u << shift;
-            __syncthreads();
+            thr = prefix;
+            need_eq = remaining;
         }
-        thr = prefix;
-        need_eq = remaining;
     }
-    // contiguous index range per thread keeps index order in the scans
-    const int per = (len + kTopnThreads - 1) / kTopnThreads;
-    const int i0 = min(len, tid * per), i1 = min(len, i0 + per);
-    int n_eq = 0;
-    if (k > 0 && k < len)
-        for (int i = i0; i < i1; ++i) n_eq += (order_key(v[i]) == thr);
-    const int eq_before = block_excl_scan<kTopnThreads>(n_eq, s_warp, nullptr);
-    int n_sel = 0;
-    {
-        int eq_rank = eq_before;
-        for (int i = i0; i < i1; ++i) {
-            bool take;
-            if (k >= len) take = true;
-            else if (k == 0) take = false;
-            else {
-                const uint32_t key = order_key(v[i]);
-                take = key > thr || (key == thr && eq_rank < need_eq);
-                eq_rank += (key == thr);
+
+    // index order (see above): warp segments of 32-token groups
+    constexpr int NW = kTopnThreads / 32;
+    const int seg = ((len + NW * 32 - 1) / (NW * 32)) * 32;
+    const int s0 = min(len, wid * seg), s1 = min(len, s0 + seg);
+    const unsigned lt = (1u << lane) - 1u;
+    auto scan_warps = [&](int cnt, int* total) {   // exclusive scan of one count per warp
+        if (lane == 0) s_warp[wid] = cnt;
+        __syncthreads();
+        if (wid == 0) {
+            int x = s_warp[lane];
+            const int c = x;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
             }
-            if (take) { ++n_sel; atomicOr(&s_bits[i >> 5], 1u << (i & 31)); }
+            s_warp[lane] = x - c;
+            if (lane == 31) s_above = x;
         }
+        __syncthreads();
+        const int before = s_warp[wid];
+        if (total) *total = s_above;
+        __syncthreads();
+        return before;
+    };
+    // 1) tokens equal to the threshold before each warp's segment
+    int eq_w = 0;
+    if (partial)
+        for (int b = s0; b < s1; b += 32) {
+            const int i = b + lane;
+            eq_w += __popc(__ballot_sync(0xffffffffu, i < s1 && key_at(i) == thr));
+        }
+    int eq_rank = scan_warps(eq_w, nullptr);
+    // 2) the selection, as bitmap words
+    int sel_w = 0;
+    for (int b = s0; b < s1; b += 32) {
+        const int i = b + lane;
+        const bool valid = i < s1;
+        const uint32_t key = (valid && partial) ? key_at(i) : 0u;
+        const bool is_eq = valid && partial && key == thr;
+        const unsigned eqm = __ballot_sync(0xffffffffu, is_eq);
+        bool take;
+        if (!valid || k == 0) take = false;
+        else if (k >= len) take = true;
+        else take = key > thr || (is_eq && eq_rank + __popc(eqm & lt) < need_eq);
+        eq_rank += __popc(eqm);
+        const unsigned tm = __ballot_sync(0xffffffffu, take);
+        if (lane == 0) s_bits[b >> 5] = tm;
+        sel_w += __popc(tm);
     }
     int total = 0;
-    const int out_before = block_excl_scan<kTopnThreads>(n_sel, s_warp, &total);
+    int o = scan_warps(sel_w, &total);
     if (tid == 0 && total != k) set_dev_error(kDevErrBounds);
-    int o = out_before;
-    for (int i = i0; i < i1; ++i) {
-        if ((s_bits[i >> 5] >> (i & 31)) & 1u) {
-            if (o < k) {
-                sel_idx[sel_base + o] = i;
-                row_pos[rrow + o] = ppos[i >> 4] + (i & 15);
+    // 3) the selected tokens in ascending order, with their positions
+    for (int b = s0; b < s1; b += 32) {
+        const unsigned tm = s_bits[b >> 5];
+        if ((tm >> lane) & 1u) {
+            const int oo = o + __popc(tm & lt), i = b + lane;
+            if (oo < k) {
+                sel_idx[sel_base + oo] = i;
+                row_pos[rrow + oo] = ppos[i >> 4] + (i & 15);
             }
-            ++o;
         }
+        o += __popc(tm);
     }
     __syncthreads();
     for (int p = tid; p < len / kPage; p += kTopnThreads)

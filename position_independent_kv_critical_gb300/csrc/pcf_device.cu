@@ -605,7 +605,9 @@ extern "C" pcf_status pcf_select_topn_global(const pcf_layout* layout, const flo
     if ((s = check_device()) != PCF_OK) return s;
     const int words = (H[L_MAX_TOKENS] + 31) / 32;
     if (words * 4 > 48 * 1024) return PCF_ERR_UNSUPPORTED;
-    return launch(topn_global_kernel, dim3(H[L_N_REQS]), dim3(kTopnThreads), words * 4,
+    const size_t smem = topn_smem_bytes(H[L_MAX_TOKENS]);   // bitmap, then the keys when they fit
+    if ((s = set_smem(topn_global_kernel, (int)smem)) != PCF_OK) return s;
+    return launch(topn_global_kernel, dim3(H[L_N_REQS]), dim3(kTopnThreads), smem,
                   static_cast<cudaStream_t>(stream), layout->dev, importance, sel_idx, excl, row_pos);
 }
 
