@@ -488,8 +488,8 @@ def main():
                          "score_layers: one of the variants alone, on the workload's layout")
     ap.add_argument("--layers", type=int, default=4, help="score_layers: layers scored per call")
     ap.add_argument("--paged", action="store_true",
-                    help="step: fused attention through pcf_fused_attention_paged (cached K/V read from the "
-                         "pool pages, keys rotated in the kernel)")
+                    help="step: scoring and fused attention through pcf_score_paged / pcf_fused_attention_paged "
+                         "(cached K/V read from the pool pages, keys rotated in the kernels, no per-request copy)")
     ap.add_argument("--anchor-pct", type=int, default=6,
                     help="anchor_probe: anchors per span, percent of its tokens in whole pages")
     args = ap.parse_args()
@@ -525,7 +525,7 @@ def main():
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
 
     def front():
-        pcf.score(L, q_query, k_pool, rope, cf.importance, cf.ws_score)
+        pcf.score(L, q_query, k_pool, rope, cf.importance, cf.ws_score, paged=args.paged)
         pcf.select_topk(L, cf.importance, cf.sel_idx, cf.excl, cf.row_pos)
         pcf.gather_rows(L, cf.sel_idx, hidden, cf.gathered)
 
@@ -569,7 +569,7 @@ def main():
     for i in range(Kb):
         flush.zero_()
         evb[i][0].record(stream)
-        pcf.score(L, q_query, k_pool, rope, cf.importance, cf.ws_score)
+        pcf.score(L, q_query, k_pool, rope, cf.importance, cf.ws_score, paged=args.paged)
         evb[i][1].record(stream)
         pcf.select_topk(L, cf.importance, cf.sel_idx, cf.excl, cf.row_pos)
         pcf.gather_rows(L, cf.sel_idx, hidden, cf.gathered)
@@ -655,7 +655,8 @@ def main():
                                        "pcf_fused_attention: compaction scan + rotation pass + attention kernel + "
                                        "split merge"), "ms": a_ms, "achieved": achieved_call,
                               "frac": achieved_call / peak,
-                              "workspace_bytes": int(cf.ws_attn.numel())}},
+                              "workspace_bytes": int(cf.ws_attn.numel()),
+                              "score_workspace_bytes": int(cf.ws_score.numel())}},
         "breakdown_ms": {"score": statistics.mean(score_ms), "topk_gather": statistics.mean(topk_gather_ms),
                          "attention": a_ms},
         "score_tflops": score_flops / (statistics.mean(score_ms) / 1e3) / 1e12,

@@ -158,6 +158,20 @@ pcf_status pcf_score_layers(const pcf_layout* layout, int32_t n_layers, const ui
                             const uint16_t* const* k_pool_layers, const float* rope, float* importance_layers,
                             float* importance_sum, void* ws, size_t ws_bytes, void* stream);
 
+/* Bytes of device workspace pcf_score_paged needs: the rotated query rows, the row LSE and
+ * importance partials and counters -- no copy of the cached keys. */
+pcf_status pcf_score_paged_workspace_bytes(const int32_t* layout_host, size_t* bytes);
+
+/* The same scoring as pcf_score (same arguments and result within the same tolerance), without any
+ * copy of the cached keys: both passes copy each key tile from its pool pages (through the block
+ * table) and rotate it in shared memory to the request's positions before the tensor-core
+ * contraction (MiniPIC 2.1).  ws: >= pcf_score_paged_workspace_bytes.  The rotation is repeated for
+ * every query-tile pair and query chunk that reads a tile, so this takes longer than pcf_score;
+ * with pcf_fused_attention_paged it completes a hot path that keeps no per-request copy of the
+ * cached keys or values. */
+pcf_status pcf_score_paged(const pcf_layout* layout, const uint16_t* q_query, const uint16_t* k_pool,
+                           const float* rope, float* importance, void* ws, size_t ws_bytes, void* stream);
+
 /* Per-span Top-k (QCFuse 2B "Top-N tokens", taken per span).  For every span s of request b:
  * the k_s request-local token indices with the largest importance, ties to the lower index,
  * written in ascending order to sel_idx[sel_base_b + offset of s ...].  Also writes

@@ -134,6 +134,12 @@ class Layout:
             ctypes.c_void_p(self.host.data_ptr()), ctypes.byref(v)))
         return int(v.value)
 
+    def score_paged_workspace_bytes(self) -> int:
+        v = ctypes.c_size_t(0)
+        _lib.check("pcf_score_paged_workspace_bytes", _lib.load().pcf_score_paged_workspace_bytes(
+            ctypes.c_void_p(self.host.data_ptr()), ctypes.byref(v)))
+        return int(v.value)
+
     def attention_paged_workspace_bytes(self) -> int:
         v = ctypes.c_size_t(0)
         _lib.check("pcf_attention_paged_workspace_bytes", _lib.load().pcf_attention_paged_workspace_bytes(
@@ -141,12 +147,15 @@ class Layout:
         return int(v.value)
 
 
-def score(layout: Layout, q_query, k_pool, rope, importance, ws, stream=None):
+def score(layout: Layout, q_query, k_pool, rope, importance, ws, stream=None, paged=False):
+    """``paged``: pcf_score_paged (keys read from the pool pages and rotated in the kernels; ``ws``
+    sized by ``Layout.score_paged_workspace_bytes``)."""
     _need(q_query, torch.bfloat16, "q_query")
     _need(k_pool, torch.bfloat16, "k_pool")
     _need(rope, torch.float32, "rope")
     _need(importance, torch.float32, "importance")
-    _lib.check("pcf_score", _lib.load().pcf_score(
+    fn = "pcf_score_paged" if paged else "pcf_score"
+    _lib.check(fn, getattr(_lib.load(), fn)(
         ctypes.byref(layout.ref), _p(q_query), _p(k_pool), _p(rope), _p(importance), _p(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -274,8 +283,9 @@ def check_device_error(stream=None):
 
 class CacheFusion:
     """Buffers for one batch on one device plus the four calls of the hot path in order.
-    ``paged=True`` runs the fused attention through pcf_fused_attention_paged (no copy of the
-    cached keys and values; a workspace that grows with the rows only)."""
+    ``paged=True`` runs scoring and the fused attention through pcf_score_paged and
+    pcf_fused_attention_paged (no copy of the cached keys or values; workspaces that grow with the
+    query and fresh rows only)."""
 
     def __init__(self, layout: Layout, rope_dev: torch.Tensor, row_elems: int = 0,
                  device: str = "cuda", paged: bool = False):
@@ -288,7 +298,8 @@ class CacheFusion:
         self.excl = torch.zeros(max(1, L.total_pages), dtype=torch.int16, device=device)
         self.row_pos = torch.empty(max(1, L.total_rows), dtype=torch.int32, device=device)
         self.out = torch.empty((max(1, L.total_rows), L.hq, L.d), dtype=torch.bfloat16, device=device)
-        self.ws_score = torch.empty(max(16, L.score_workspace_bytes()), dtype=torch.uint8, device=device)
+        ws_score = L.score_paged_workspace_bytes() if paged else L.score_workspace_bytes()
+        self.ws_score = torch.empty(max(16, ws_score), dtype=torch.uint8, device=device)
         ws_attn = L.attention_paged_workspace_bytes() if paged else L.attention_workspace_bytes()
         self.ws_attn = torch.empty(max(16, ws_attn), dtype=torch.uint8, device=device)
         self.gathered = (torch.empty((max(1, L.total_sel), row_elems), dtype=torch.bfloat16, device=device)
@@ -296,7 +307,7 @@ class CacheFusion:
 
     def step(self, q_query, k_pool, v_pool, q_fresh, k_fresh, v_fresh, hidden=None, stream=None):
         L = self.layout
-        score(L, q_query, k_pool, self.rope, self.importance, self.ws_score, stream)
+        score(L, q_query, k_pool, self.rope, self.importance, self.ws_score, stream, paged=self.paged)
         select_topk(L, self.importance, self.sel_idx, self.excl, self.row_pos, stream)
         if hidden is not None and self.gathered is not None:
             gather_rows(L, self.sel_idx, hidden, self.gathered, stream)
@@ -355,7 +366,7 @@ class CacheFusion:
         copies([qf, kf, vf], [q_fresh_h, k_fresh_h, v_fresh_h], n_in[1:], self._h2d)
         self._ev_fresh[i].record(self._h2d)
         main.wait_event(self._ev_q[i])
-        score(L, qq, k_pool, self.rope, self.importance, self.ws_score)
+        score(L, qq, k_pool, self.rope, self.importance, self.ws_score, paged=self.paged)
         if self._ev_down is not None:      # sel_idx and out of the previous step are on their way down
             main.wait_event(self._ev_down)
         select_topk(L, self.importance, self.sel_idx, self.excl, self.row_pos)

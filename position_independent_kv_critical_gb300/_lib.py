@@ -32,7 +32,7 @@ EXPORTS = (
     "pcf_check_device_error", "pcf_score_noalloc", "pcf_copy_async", "pcf_select_topn_global",
     "pcf_key_norms", "pcf_pack_anchor_pages", "pcf_prefetch_pool_pages", "pcf_fused_attention_timed",
     "pcf_wait_limit_check", "pcf_score_layers", "pcf_fused_attention_paged",
-    "pcf_attention_paged_workspace_bytes",
+    "pcf_attention_paged_workspace_bytes", "pcf_score_paged", "pcf_score_paged_workspace_bytes",
 )
 
 
@@ -78,11 +78,14 @@ def _declare(lib):
     lib.pcf_layout_build.argtypes = [P(RequestDesc), c_int32, P(Dims), c_void_p, c_int64]
     lib.pcf_layout_query.restype = c_int32
     lib.pcf_layout_query.argtypes = [c_void_p, c_int32, P(c_int64)]
-    for fn in ("pcf_score_workspace_bytes", "pcf_attention_workspace_bytes", "pcf_attention_paged_workspace_bytes"):
+    for fn in ("pcf_score_workspace_bytes", "pcf_attention_workspace_bytes", "pcf_attention_paged_workspace_bytes",
+               "pcf_score_paged_workspace_bytes"):
         getattr(lib, fn).restype = c_int32
         getattr(lib, fn).argtypes = [c_void_p, P(c_size_t)]
     lib.pcf_score.restype = c_int32
     lib.pcf_score.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.pcf_score_paged.restype = c_int32
+    lib.pcf_score_paged.argtypes = [P(LayoutRef), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
     lib.pcf_score_layers.restype = c_int32
     lib.pcf_score_layers.argtypes = [P(LayoutRef), c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_size_t, c_void_p]

@@ -56,7 +56,11 @@ namespace pcf {
 // adds two rotator warps (16 warps, 128 registers each)
 constexpr int kAttnThreads = 448;
 constexpr int kAttnThreadsPaged = 512;
-template <bool PAGED> constexpr int attn_threads() { return PAGED ? kAttnThreadsPaged : kAttnThreads; }
+// (the paged scoring pass needs no extra warps: its rotators are the two P V issuer warps, idle
+// without P V)
+template <bool PAGED, bool LSE = false> __host__ __device__ constexpr int attn_threads() {
+    return PAGED && !LSE ? kAttnThreadsPaged : kAttnThreads;
+}
 constexpr int kWarpSoftB = 4;
 constexpr int kWarpMma = 8;
 constexpr int kWarpTma = 9;
@@ -64,7 +68,7 @@ constexpr int kWarpTmaV = 10;
 constexpr int kWarpMmaB = 11;
 constexpr int kWarpPvA = 12;
 constexpr int kWarpPvB = 13;
-constexpr int kWarpRot = 14;        // warps 14 and 15: rotation of the cached key tiles
+constexpr int kWarpRot = 14;        // warps 14 and 15: rotation of the cached key tiles (scoring: 12, 13)
 constexpr int kRotThreads = 64;
 constexpr int kNoPos = 0x7FFFFFFF;
 constexpr int kKStages = 2;
@@ -121,7 +125,7 @@ struct AttnSmem {
     // attention: per K stage, the fresh rotated keys of the tile's recomputed tokens (a block of
     // consecutive fresh rows, kStageRows of them, copied with the tile) and per page of the tile
     // its recompute bits and the rank of its first recomputed token
-    static constexpr int kKst = PAGED ? kStageRows * D * 2 : 0;
+    static constexpr int kKst = PAGED && !LSE ? kStageRows * D * 2 : 0;
     static constexpr int oKst = oV + kVStages * kV;
     static constexpr int oKpos = oKst + kKStages * kKst;
     static constexpr int oMeta = oKpos + kKStages * kTileKeys * 4;   // (paged: 64 bytes a stage)
@@ -131,7 +135,7 @@ struct AttnSmem {
     static constexpr int oRope = oMeta + kKStages * kPagesPerTile * 8;
     // attention: each softmax thread's output pointers, kept here across the tile loop
     static constexpr int oPark = oRope + kKStages * kRope;
-    static constexpr int oBar = oPark + (PAGED ? 256 * 16 : 0);
+    static constexpr int oBar = oPark + (PAGED && !LSE ? 256 * 16 : 0);
     static constexpr int kNumBars = 42;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int oItem = oMisc + 64;
@@ -165,19 +169,64 @@ enum : int {
     B_VRAW_FULL = 40   // [2] the V tile's copy landed (TMA; the V producer then makes it B_V_FULL)
 };
 
+// In-place rotation of part of a cached K tile in a stage (128-byte swizzled rows, the two 64-wide
+// halves 16 KB apart for d = 128): 16-byte chunk pair c -- dimensions 8c .. 8c+7 and d/2 + 8c .. --
+// of the N keys key0 .. key0+N-1, which sit at consecutive positions.  (C, S, -S) hold the cos and
+// sin of the thread's eight frequencies at key0's position as packed fp32 pairs (frequencies 8c+2e
+// and 8c+2e+1 in pair e) and advance by one position step (STC, STS, -STS: the table's row 1) from
+// key to key.  bf16 in, fp16 out; a value out of fp16 range raises the range error.
+template <int D, int N>
+__device__ __forceinline__ void rotate_page_keys(uint8_t* stage, int key0, int c, uint64_t (&C)[4], uint64_t (&S)[4],
+                                                 uint64_t (&NS)[4], const uint64_t (&STC)[4],
+                                                 const uint64_t (&STS)[4], const uint64_t (&NSTS)[4]) {
+    const uint32_t o_hi = D == 128 ? 16384u : 0u;
+    const int c_hi = D == 128 ? c : c + 4;
+    float big = 0.f;
+#pragma unroll 2
+    for (int r = 0; r < N; ++r) {
+        const int key = key0 + r;
+        uint4* plo = reinterpret_cast<uint4*>(stage + sw128_off(key, c));
+        uint4* phi = reinterpret_cast<uint4*>(stage + o_hi + sw128_off(key, c_hi));
+        const uint4 a = *plo, b = *phi;
+        const uint32_t ia[4] = {a.x, a.y, a.z, a.w}, ib[4] = {b.x, b.y, b.z, b.w};
+        uint32_t oa[4], ob[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint64_t A = bf16x2_to_f2(ia[e]), B = bf16x2_to_f2(ib[e]);
+            float y0, y1, z0, z1;
+            f2_unpack(f2_fma(B, NS[e], f2_mul(A, C[e])), y0, y1);   // a cos - b sin
+            f2_unpack(f2_fma(A, S[e], f2_mul(B, C[e])), z0, z1);    // b cos + a sin
+            oa[e] = pack_f16x2_track(y0, y1, big);
+            ob[e] = pack_f16x2_track(z0, z1, big);
+        }
+        *plo = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+        *phi = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+        // the next key's angles: one position further
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint64_t cn = f2_fma(S[e], NSTS[e], f2_mul(C[e], STC[e]));
+            const uint64_t sn = f2_fma(C[e], STS[e], f2_mul(S[e], STC[e]));
+            NS[e] = f2_fma(C[e], NSTS[e], f2_mul(NS[e], STC[e]));
+            C[e] = cn;
+            S[e] = sn;
+        }
+    }
+    if (big > kF16Limit) set_dev_error(kDevErrRange);
+}
+
 template <int D, bool LSE, bool PAGED>
-__global__ void __launch_bounds__(attn_threads<PAGED>())
+__global__ void __launch_bounds__(attn_threads<PAGED, LSE>())
 attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kcache,
             const __grid_constant__ CUtensorMap tm_vcache, const __grid_constant__ CUtensorMap tm_kfresh,
             const __grid_constant__ CUtensorMap tm_vfresh, const __grid_constant__ CUtensorMap tm_kstage,
             const AttnParams prm) {
-    static_assert(!(LSE && PAGED), "the scoring pass reads the rotated copy");
     using SM = AttnSmem<D, LSE, PAGED>;
     constexpr int H = SM::kHalves;
     // slot readers: lane 0 of the 8 softmax warps and of the 2 Q K^T issuers (+ 2 P V issuers and
     // the V producer outside LSE mode)
     // (paged: and lane 0 of the two rotator warps)
-    constexpr int kItemReaders = LSE ? 10 : (PAGED ? 15 : 13);
+    constexpr int kItemReaders = (LSE ? 10 : 13) + (PAGED ? 2 : 0);
+    constexpr int kRot0 = LSE ? kWarpPvA : kWarpRot;   // first rotator warp (paged)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     auto sQ = [&](int t) { return smem + SM::oQ + t * SM::kQ; };
@@ -401,7 +450,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     }
                     if (PAGED && lane < kPagesPerTile) {
                         prow = (blk[min(pg + lane, w.n_pages - 1)] * Hkv + w.kvh) * kPage;
-                        if (pg + lane < w.n_pages) {
+                        if (!LSE && pg + lane < w.n_pages) {
                             ex = prm.excl[w.page_base + pg + lane];
                             sel = kPage * (pg + lane) - (prm.cidx[w.page_base + pg + lane] - w.cbase);
                         }
@@ -525,7 +574,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             for (int s2 = 0; s2 < kVStages; ++s2)
                 if (last_v[s2] >= 0) mbar_drain(&bars[B_V_FULL + s2], (last_v[s2] >> 1) & 1);
-        } else if (PAGED) {
+        } else if (PAGED && !LSE) {
             // paged: V tiles of the cached pages (one copy per page and half, as for K) or of the
             // query rows.  Once a cached tile has landed, the recomputed tokens' cached V rows are
             // overwritten with their fresh rows: lane l takes page l / 4 of the tile and a quarter
@@ -634,7 +683,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 for (int s2 = 0; s2 < kVStages; ++s2)
                     if (last_v[s2] >= 0) mbar_drain(&bars[B_VRAW_FULL + s2], (last_v[s2] >> 1) & 1);
         }
-    } else if (PAGED && warp >= kWarpRot) {
+    } else if (PAGED && warp >= kRot0 && warp < kRot0 + 2) {
         // ------------------------------------------------------------ K rotation (warps 14, 15)
         // MiniPIC 2.1: cached keys are rotated when used, to the request's logical positions.  A
         // cached tile holds 8 pool pages; thread t rotates 16-byte chunk pair c (dimensions 8c ..
@@ -647,7 +696,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         // position), which the producer staged with the tile as well.
         constexpr int CP = D / 16;
         constexpr int KPT = 2 * CP;
-        const int rt = tid - kWarpRot * 32;
+        const int rt = tid - kRot0 * 32;
         const int m = rt / 8, c = rt % CP, r0 = ((rt % 8) / CP) * KPT;
         const uint32_t o_hi = D == 128 ? 16384u : 0u;
         const int c_hi = D == 128 ? c : c + 4;
@@ -691,37 +740,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         S[e] = f2_pack(v.y, v.w);
                         NS[e] = f2_pack(-v.y, -v.w);
                     }
-                    float big = 0.f;
-#pragma unroll 2
-                    for (int r = 0; r < KPT; ++r) {
-                        const int key = kPage * m + r0 + r;
-                        uint4* plo = reinterpret_cast<uint4*>(stage + sw128_off(key, c));
-                        uint4* phi = reinterpret_cast<uint4*>(stage + o_hi + sw128_off(key, c_hi));
-                        const uint4 a = *plo, b = *phi;
-                        const uint32_t ia[4] = {a.x, a.y, a.z, a.w}, ib[4] = {b.x, b.y, b.z, b.w};
-                        uint32_t oa[4], ob[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint64_t A = bf16x2_to_f2(ia[e]), B = bf16x2_to_f2(ib[e]);
-                            float y0, y1, z0, z1;
-                            f2_unpack(f2_fma(B, NS[e], f2_mul(A, C[e])), y0, y1);   // a cos - b sin
-                            f2_unpack(f2_fma(A, S[e], f2_mul(B, C[e])), z0, z1);    // b cos + a sin
-                            oa[e] = pack_f16x2_track(y0, y1, big);
-                            ob[e] = pack_f16x2_track(z0, z1, big);
-                        }
-                        *plo = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-                        *phi = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-                        // the next key's angles: one position further
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint64_t cn = f2_fma(S[e], NSTS[e], f2_mul(C[e], STC[e]));
-                            const uint64_t sn = f2_fma(C[e], STS[e], f2_mul(S[e], STC[e]));
-                            NS[e] = f2_fma(C[e], NSTS[e], f2_mul(NS[e], STC[e]));
-                            C[e] = cn;
-                            S[e] = sn;
-                        }
-                    }
-                    if (big > kF16Limit) set_dev_error(kDevErrRange);
+                    rotate_page_keys<D, KPT>(stage, kPage * m + r0, c, C, S, NS, STC, STS, NSTS);
                     // recomputed tokens: their fresh keys, already rotated to the same positions
                     const int2 pm = sMeta(ks)[m];
                     const int32_t sel_first = sMeta(ks)[0].y;
@@ -888,7 +907,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     }
                 }
             }
-            if (PAGED) {   // parked in shared memory across the tile loop, where registers are scarce
+            if (PAGED && !LSE) {   // parked in shared memory across the tile loop, where registers are scarce
                 volatile uint64_t* park = reinterpret_cast<volatile uint64_t*>(smem + SM::oPark) + 2 * (warp * 32 + lane);
                 park[0] = reinterpret_cast<uint64_t>(out_row);
                 park[1] = reinterpret_cast<uint64_t>(ml_slot);
@@ -1059,7 +1078,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
             }
             if (!ok) break;
-            if (PAGED) {
+            if (PAGED && !LSE) {
                 volatile uint64_t* park = reinterpret_cast<volatile uint64_t*>(smem + SM::oPark) + 2 * (warp * 32 + lane);
                 out_row = reinterpret_cast<__nv_bfloat16*>(park[0]);
                 ml_slot = reinterpret_cast<float2*>(park[1]);

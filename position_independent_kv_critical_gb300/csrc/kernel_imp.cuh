@@ -28,6 +28,10 @@
 namespace pcf {
 
 constexpr int kImpThreads = 320;
+// paged variant: two more warps (10, 11) rotate each key tile, copied from the pool pages, in place
+constexpr int kImpThreadsPaged = 384;
+constexpr int kImpWarpRot = 10;
+template <bool PAGED> __host__ __device__ constexpr int imp_threads() { return PAGED ? kImpThreadsPaged : kImpThreads; }
 constexpr int kImpExpThreads = 256;
 constexpr int kImpWarpMma = 8;
 constexpr int kImpWarpTma = 9;
@@ -39,6 +43,7 @@ struct ImpParams {
     float* part;             // [2][Hkv][total_tokens]: query column half, kv head, token
     int32_t* counters;       // [total key tiles], zero on entry, left zero on exit
     float* importance;       // [total_tokens]
+    const float2* rope;      // paged: (cos, sin) table [max_pos][D/2]
 };
 
 template <int D>
@@ -53,7 +58,7 @@ struct ImpSmem {
     static constexpr int oQlse = oQ + 2 * kQ;          // 2 slabs (one per query-chunk buffer)
     static constexpr int oKones = oQlse + 2 * kSlabQ;
     static constexpr int oBar = oKones + kSlabK;
-    static constexpr int kNumBars = 16;
+    static constexpr int kNumBars = 18;
     static constexpr int oMisc = oBar + kNumBars * 8;
     static constexpr int kBytes = oMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;
@@ -61,12 +66,13 @@ struct ImpSmem {
 };
 
 enum : int { I_K_FULL = 0 /*2*/, I_K_EMPTY = 2 /*2*/, I_Q_FULL = 4 /*2*/, I_Q_EMPTY = 6 /*2*/,
-             I_ACC_FULL = 8 /*2*/, I_ACC_FREE = 10 /*2*/, I_LSE_FULL = 12 /*2*/, I_DRAIN = 14 };
+             I_ACC_FULL = 8 /*2*/, I_ACC_FREE = 10 /*2*/, I_LSE_FULL = 12 /*2*/, I_DRAIN = 14,
+             I_KRAW_FULL = 16 /*2: paged, the key tile's page copies landed*/ };
 
 __device__ __forceinline__ void named_sync_exp() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-template <int D>
-__global__ void __launch_bounds__(kImpThreads, 1)
+template <int D, bool PAGED>
+__global__ void __launch_bounds__(imp_threads<PAGED>(), 1)
 imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kcache,
            const ImpParams prm) {
     using SM = ImpSmem<D>;
@@ -103,7 +109,8 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars[I_K_FULL + b], 1);
+            mbar_init(&bars[I_K_FULL + b], PAGED ? 64 : 1);
+            mbar_init(&bars[I_KRAW_FULL + b], 1);
             mbar_init(&bars[I_K_EMPTY + b], 1);
             mbar_init(&bars[I_Q_FULL + b], 1);
             mbar_init(&bars[I_Q_EMPTY + b], 1);
@@ -124,7 +131,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         tmem_relinquish();
     }
     // the K=16 slabs start at zero; the key side gets its two columns of ones
-    for (int i = tid; i < (2 * SM::kSlabQ + SM::kSlabK) / 16; i += kImpThreads)
+    for (int i = tid; i < (2 * SM::kSlabQ + SM::kSlabK) / 16; i += imp_threads<PAGED>())
         reinterpret_cast<uint4*>(sQlse(0))[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     if (tid < kTileKeys) {
@@ -143,8 +150,27 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             prefetch_tmap(&tm_kcache);
             const int32_t ky0 = kvh * L[L_TOTAL_TOKENS] + R[R_TOK_BASE] + t0 * kTileKeys;
             const int32_t qy0 = (kvh * L[L_TOTAL_QUERY] + R[R_Q_BASE]) * g;
+            const int32_t* blk = L + L[L_OFF_BLOCK] + R[R_PAGE_BASE];
             int lastk[2] = {-1, -1}, lastq[2] = {-1, -1};
             bool ok = true;
+            // key tile t0 + i into stage kb: the rotated copy (one box per half) or, paged, its eight
+            // pool pages (one 16-row box per page and half, a page past the request's last
+            // repeating that last page), which the rotator warps then rotate in place
+            auto load_k = [&](int kb, int i) {
+                uint64_t* bar = &bars[(PAGED ? I_KRAW_FULL : I_K_FULL) + kb];
+                mbar_arrive_expect_tx(bar, H * 16384);
+                if (PAGED) {
+                    for (int m = 0; m < kPagesPerTile; ++m) {
+                        const int lp = min((t0 + i) * kPagesPerTile + m, n_pages - 1);
+                        const int32_t y = (blk[lp] * Hkv + kvh) * kPage;
+                        for (int hb = 0; hb < H; ++hb)
+                            tma_load_2d(sKs(kb) + hb * 16384 + m * (kPage * 128), &tm_kcache, bar, hb * 64, y);
+                    }
+                } else {
+                    for (int hb = 0; hb < H; ++hb)
+                        tma_load_2d(sKs(kb) + hb * 16384, &tm_kcache, bar, hb * 64, ky0 + i * kTileKeys);
+                }
+            };
             for (int qc = 0; !q_resident && ok && qc < n_qc; ++qc) {
                 // chunk qc into buffer qc & 1 once chunk qc - 2 is done with it, then the run's tiles
                 const int qb = qc & 1;
@@ -157,20 +183,16 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 for (int i = 0; i < nt; ++i) {
                     const int s = qc * nt + i, kb = s & 1;
                     if (s >= 2 && !(ok = mbar_wait(&bars[I_K_EMPTY + kb], ((s >> 1) - 1) & 1, abort_flag))) break;
-                    mbar_arrive_expect_tx(&bars[I_K_FULL + kb], H * 16384);
-                    for (int hb = 0; hb < H; ++hb)
-                        tma_load_2d(sKs(kb) + hb * 16384, &tm_kcache, &bars[I_K_FULL + kb], hb * 64,
-                                    ky0 + i * kTileKeys);
+                    load_k(kb, i);
                     lastk[kb] = s;
                 }
             }
-            for (int i = 0; q_resident && ok && i < nt; ++i) {
+            // (a request without query rows has no steps: nothing is loaded)
+            for (int i = 0; q_resident && n_steps > 0 && ok && i < nt; ++i) {
                 // rotated key tile t0 + i (rows past the request's keys are never summed)
                 const int kb = i & 1;
                 if (i >= 2 && !(ok = mbar_wait(&bars[I_K_EMPTY + kb], ((i >> 1) - 1) & 1, abort_flag))) break;
-                mbar_arrive_expect_tx(&bars[I_K_FULL + kb], H * 16384);
-                for (int hb = 0; hb < H; ++hb)
-                    tma_load_2d(sKs(kb) + hb * 16384, &tm_kcache, &bars[I_K_FULL + kb], hb * 64, ky0 + i * kTileKeys);
+                load_k(kb, i);
                 lastk[kb] = i;
                 for (int qc = 0; i == 0 && qc < n_qc; ++qc) {   // each chunk once, into buffer qc
                     mbar_arrive_expect_tx(&bars[I_Q_FULL + qc], H * kImpQRows * 128);
@@ -181,7 +203,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 }
             }
             for (int b = 0; b < 2; ++b) {
-                if (lastk[b] >= 0) mbar_drain(&bars[I_K_FULL + b], (lastk[b] >> 1) & 1);
+                if (lastk[b] >= 0) mbar_drain(&bars[(PAGED ? I_KRAW_FULL : I_K_FULL) + b], (lastk[b] >> 1) & 1);
                 if (lastq[b] >= 0) mbar_drain(&bars[I_Q_FULL + b], (lastq[b] >> 1) & 1);
             }
         }
@@ -221,6 +243,53 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             }
             mma_commit(&bars[I_DRAIN]);
             mbar_drain(&bars[I_DRAIN], 0);
+        }
+    } else if (PAGED && warp >= kImpWarpRot) {
+        // warps 10, 11 (paged): every key tile the producer copies from the pool pages is rotated in
+        // place to the request's positions, in the producer's order, before the MMA reads it.
+        // Thread t takes page t / 8 of the tile and 16-byte chunk pair c of 2*D/16 consecutive keys
+        // (see rotate_page_keys); its table row is loaded one tile ahead.
+        constexpr int CP = D / 16;
+        constexpr int KPT = 2 * CP;
+        const int rt = tid - kImpWarpRot * 32;
+        const int m = rt / 8, c = rt % CP, r0 = ((rt % 8) / CP) * KPT;
+        const int32_t* page_pos = L + L[L_OFF_PAGEPOS] + R[R_PAGE_BASE];
+        uint64_t STC[4], STS[4], NSTS[4];
+        {
+            const float4* t1 = reinterpret_cast<const float4*>(prm.rope + D / 2 + 8 * c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 v = t1[e];
+                STC[e] = f2_pack(v.x, v.z);
+                STS[e] = f2_pack(v.y, v.w);
+                NSTS[e] = f2_pack(-v.y, -v.w);
+            }
+        }
+        const int n_loads = n_steps == 0 ? 0 : (q_resident ? nt : n_steps);
+        float4 tr[4];
+        auto table_row = [&](int sidx) {
+            const int i = q_resident ? sidx : sidx % nt;
+            const int lp = min((t0 + i) * kPagesPerTile + m, n_pages - 1);
+            const float4* tp = reinterpret_cast<const float4*>(prm.rope + (int64_t)(page_pos[lp] + r0) * (D / 2) + 8 * c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tr[e] = tp[e];
+        };
+        if (n_loads > 0) table_row(0);
+        for (int sidx = 0; sidx < n_loads; ++sidx) {
+            const int kb = sidx & 1;
+            const bool okr = mbar_wait(&bars[I_KRAW_FULL + kb], (sidx >> 1) & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, okr)) break;
+            uint64_t C[4], S[4], NS[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                C[e] = f2_pack(tr[e].x, tr[e].z);
+                S[e] = f2_pack(tr[e].y, tr[e].w);
+                NS[e] = f2_pack(-tr[e].y, -tr[e].w);
+            }
+            if (sidx + 1 < n_loads) table_row(sidx + 1);
+            rotate_page_keys<D, KPT>(sKs(kb), kPage * m + r0, c, C, S, NS, STC, STS, NSTS);
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[I_K_FULL + kb]);
         }
     } else {
         // warps 0-7: thread owns key `key` of every tile of the run, query columns ch*128 .. +127

@@ -342,10 +342,78 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
     }
     if (H[L_N_IMP_ITEMS] > 0) {
         using SM = ImpSmem<D>;
-        auto kern = imp_kernel<D>;
+        auto kern = imp_kernel<D, false>;
         if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
-        ImpParams p{lay->dev, lse, part, cnt, importance};
+        ImpParams p{lay->dev, lse, part, cnt, importance, rope2};
         if ((s = launch(kern, dim3(H[L_N_IMP_ITEMS]), dim3(kImpThreads), SM::kAlloc, st, tq256, tkc, p)) != PCF_OK)
+            return s;
+    }
+    return PCF_OK;
+}
+
+// Paged scoring: the same two passes, reading the cached keys from their pool pages and rotating
+// them inside the kernels (no copy of the cached keys).  Workspace: rotated query rows, the row
+// LSE partials, the importance partials and the counters.
+struct ScorePagedWs {
+    size_t q, lse, part, cnt, total;
+};
+ScorePagedWs score_paged_ws(const int32_t* H) {
+    ScorePagedWs w;
+    w.q = 0;
+    w.lse = align_up(w.q + (size_t)H[L_TOTAL_QUERY] * H[L_HQ] * H[L_D] * 2);
+    w.part = align_up(w.lse + (size_t)H[L_LSE_SLOTS] * sizeof(float2));
+    w.cnt = align_up(w.part + 2 * (size_t)H[L_HKV] * H[L_TOTAL_TOKENS] * sizeof(float));
+    w.total = align_up(w.cnt + ((size_t)H[L_TOTAL_KTILES] + 1) * sizeof(int32_t));
+    return w;
+}
+
+template <int D>
+pcf_status score_paged_impl(const pcf_layout* lay, const uint16_t* q_query, const uint16_t* k_pool, const float* rope,
+                            float* importance, void* ws, cudaStream_t st) {
+    const int32_t* H = lay->host;
+    const ScorePagedWs w = score_paged_ws(H);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    __half* q_rot = reinterpret_cast<__half*>(base + w.q);
+    float2* lse = reinterpret_cast<float2*>(base + w.lse);
+    float* part = reinterpret_cast<float*>(base + w.part);
+    int32_t* cnt = reinterpret_cast<int32_t*>(base + w.cnt);
+    const int g = H[L_GROUP];
+    const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    const float2* rope2 = reinterpret_cast<const float2*>(rope);
+    const int32_t n_cnt = H[L_TOTAL_KTILES] + 1;   // cleared by the rotation kernel
+    RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_query), lay->dev + H[L_OFF_QPOS], q_rot, H[L_TOTAL_QUERY],
+               H[L_HQ], g, scale_log2, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+    RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
+                 nullptr, 0, 4};
+    pcf_status s = launch_rope<D>(qj, none, none, rope2, H[L_MAX_POS], st, cnt, n_cnt);
+    if (s != PCF_OK) return s;
+
+    CUtensorMap tq128, tq256, tkp, zero;
+    std::memset(&zero, 0, sizeof(zero));
+    const uint64_t qrows = (uint64_t)H[L_HKV] * H[L_TOTAL_QUERY] * g;
+    if ((s = make_map_2d(&tq128, q_rot, D, qrows, D * 2, 128, kF16)) != PCF_OK) return s;
+    if ((s = make_map_2d(&tq256, q_rot, D, qrows, D * 2, 256, kF16)) != PCF_OK) return s;
+    // the pool, unrotated and read only: one page (16 rows of one kv head) per copy
+    if ((s = make_map_2d(&tkp, k_pool, D, (uint64_t)H[L_N_PHYS] * H[L_HKV] * kPage, D * 2, kPage)) != PCF_OK)
+        return s;
+    if (H[L_N_LSE_ITEMS] > 0) {
+        using SM = AttnSmem<D, true, true>;
+        auto kern = attn_kernel<D, true, true>;
+        if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
+        AttnParams p{lay->dev, nullptr, nullptr, nullptr, lse, nullptr, nullptr, cnt + H[L_TOTAL_KTILES],
+                     nullptr, nullptr, nullptr, nullptr, rope2};
+        const int grid = std::min<int>(H[L_N_LSE_ITEMS], device_sms());
+        if ((s = launch(kern, dim3(grid), dim3(attn_threads<true, true>()), SM::kAlloc, st, tq128, tkp, zero, zero,
+                        zero, zero, p)) != PCF_OK)
+            return s;
+    }
+    if (H[L_N_IMP_ITEMS] > 0) {
+        using SM = ImpSmem<D>;
+        auto kern = imp_kernel<D, true>;
+        if ((s = set_smem(kern, SM::kAlloc)) != PCF_OK) return s;
+        ImpParams p{lay->dev, lse, part, cnt, importance, rope2};
+        if ((s = launch(kern, dim3(H[L_N_IMP_ITEMS]), dim3(kImpThreadsPaged), SM::kAlloc, st, tq256, tkp, p)) !=
+            PCF_OK)
             return s;
     }
     return PCF_OK;
@@ -575,6 +643,28 @@ extern "C" pcf_status pcf_score_layers(const pcf_layout* layout, int32_t n_layer
     const int64_t threads = n / 4 + n % 4;
     return launch(layer_sum_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st,
                   (const float*)importance_layers, n_layers, n, importance_sum);
+}
+
+extern "C" pcf_status pcf_score_paged_workspace_bytes(const int32_t* layout_host, size_t* bytes) {
+    if (!layout_host || !bytes || layout_host[L_MAGIC] != kMagic) return PCF_ERR_INVALID_ARG;
+    *bytes = score_paged_ws(layout_host).total;
+    return PCF_OK;
+}
+
+extern "C" pcf_status pcf_score_paged(const pcf_layout* layout, const uint16_t* q_query, const uint16_t* k_pool,
+                                      const float* rope, float* importance, void* ws, size_t ws_bytes, void* stream) {
+    pcf_status s = check_layout(layout);
+    if (s != PCF_OK) return s;
+    const int32_t* H = layout->host;
+    if (H[L_TOTAL_TOKENS] == 0) return PCF_OK;
+    if (!k_pool || !rope || !importance || !ws || (H[L_TOTAL_QUERY] > 0 && !q_query)) return PCF_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(rope) || !aligned16(ws) || (q_query && !aligned16(q_query)))
+        return PCF_ERR_INVALID_ARG;
+    if (ws_bytes < score_paged_ws(H).total) return PCF_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_device()) != PCF_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return H[L_D] == 128 ? score_paged_impl<128>(layout, q_query, k_pool, rope, importance, ws, st)
+                         : score_paged_impl<64>(layout, q_query, k_pool, rope, importance, ws, st);
 }
 
 extern "C" pcf_status pcf_select_topk(const pcf_layout* layout, const float* importance, int32_t* sel_idx,

@@ -34,8 +34,14 @@ class GpuBatch:
         self.page_base = [t // 16 for t in self.tok_base]
 
     # ---- GPU calls
-    def score(self):
-        pcf.score(self.L, self.q_query, self.k_pool, self.rope, self.cf.importance, self.cf.ws_score)
+    def score(self, paged=False):
+        ws = self.cf.ws_score
+        if paged:
+            if not hasattr(self, "ws_score_paged"):
+                self.ws_score_paged = torch.empty(max(16, self.L.score_paged_workspace_bytes()), dtype=torch.uint8,
+                                                  device=self.dev)
+            ws = self.ws_score_paged
+        pcf.score(self.L, self.q_query, self.k_pool, self.rope, self.cf.importance, ws, paged=paged)
         pcf.check_device_error()
         return self.cf.importance[: self.L.total_tokens].cpu().numpy()
 

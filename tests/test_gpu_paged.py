@@ -1,9 +1,10 @@
-"""GPU parity of the paged fused attention (pcf_fused_attention_paged): cached K/V tiles copied
-straight from the pool pages through the block table, the keys rotated in shared memory to the
-request's positions before the tensor-core contraction (MiniPIC 2.1), and each recomputed token's
-fresh key and value written over its stale cached copy in place.  Every case is checked against the
-fp64 oracle with the oracle's selection, within 2e-2 absolute + 1e-2 relative, like the compacted
-call; the two calls are also compared with each other."""
+"""GPU parity of the paged calls (pcf_score_paged, pcf_fused_attention_paged): cached key (and
+value) tiles copied straight from the pool pages through the block table, the keys rotated in
+shared memory to the request's positions before the tensor-core contraction (MiniPIC 2.1), and in
+the attention each recomputed token's fresh key and value written over its stale cached copy in
+place.  Every case is checked against the fp64 oracle -- importance within 1e-3 relative, the
+attention with the oracle's selection within 2e-2 absolute + 1e-2 relative -- like the compacted
+calls; the two kinds of call are also compared with each other."""
 from __future__ import annotations
 
 import numpy as np
@@ -95,3 +96,30 @@ def test_paged_and_compacted_agree_and_paged_is_deterministic(name):
     # they agree to the bf16 output precision, not bit for bit
     err = np.abs(p1 - a)
     assert np.all(err <= 1e-2 + 1e-2 * np.abs(a)), f"max diff {err.max():.3e}"
+
+
+@pytest.mark.parametrize("name", ["llama8b_layer", "long_context"])
+def test_paged_and_compacted_scoring_agree_and_paged_is_deterministic(name):
+    gb = gpu_batch(name)
+    a = gb.score().copy()
+    p1 = gb.score(paged=True).copy()
+    p2 = gb.score(paged=True).copy()
+    assert np.array_equal(p1.view(np.uint32), p2.view(np.uint32))
+    err = np.abs(p1 - a)
+    assert np.all(err <= 2e-3 * np.abs(a) + 1e-7), f"max rel diff {(err / np.maximum(a, 1e-30)).max():.3e}"
+
+
+def test_paged_step_through_the_public_api_matches_the_compacted_one():
+    """CacheFusion(paged=True): scoring, top-k and attention with no copy of the cached keys or
+    values; the selection equals the compacted pipeline's wherever the two importances do not tie
+    within rounding, and the output matches the oracle given that selection."""
+    import position_independent_kv_critical_gb300 as pcf
+    b = make_batch("llama8b_layer")
+    gb = GpuBatch(b)
+    cfp = pcf.CacheFusion(gb.L, gb.rope, device="cuda", paged=True)
+    cfp.step(gb.q_query, gb.k_pool, gb.v_pool, gb.q_fresh, gb.k_fresh, gb.v_fresh)
+    pcf.check_device_error()
+    sel = cfp.sel_idx[: gb.L.total_sel].cpu().numpy().astype(np.int64)
+    exp, _ = gb.oracle_attention(0, sel)
+    got = cfp.out[: gb.L.total_rows].float().cpu().numpy()
+    assert_close_out(got, exp, "paged step")

@@ -42,11 +42,11 @@ def _sample_rows(n_rows, n_sel, k=48):
 def check_batch(gb: GpuBatch, req_ids=None, sample_rows=False, imp_only_ids=(), paged=False):
     """Importance, top-k and attention of the requests `req_ids` (all by default) against the
     oracle; `imp_only_ids` are further requests whose importance alone is compared; `paged` runs
-    the attention through pcf_fused_attention_paged."""
+    scoring and the attention through pcf_score_paged and pcf_fused_attention_paged."""
     b = gb.b
     ids = list(range(len(b.requests))) if req_ids is None else list(req_ids)
     # 1) importance
-    got_imp = gb.score()
+    got_imp = gb.score(paged=paged)
     for i in imp_only_ids:
         r = b.requests[i]
         t0 = gb.tok_base[i]

@@ -340,6 +340,8 @@ def test_paged_attention_workspace_holds_no_copy_of_the_cached_keys(name):
     paged, compact = L.attention_paged_workspace_bytes(), L.attention_workspace_bytes()
     kv_copy = 2 * cfg.hkv * cfg.d * 2 * (L.total_tokens - L.total_sel)
     assert compact - paged >= kv_copy
+    # scoring: the rotated copy of every cached key (fp16, every kv head) is gone as well
+    assert L.score_workspace_bytes() - L.score_paged_workspace_bytes() >= cfg.hkv * cfg.d * 2 * L.total_tokens
 
 
 def test_paged_attention_workspace_does_not_grow_with_cached_tokens():
