@@ -769,15 +769,19 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
     } else if (warp == kWarpMma || warp == kWarpMmaB || warp == kWarpPvA || warp == kWarpPvB) {
         // ------------------------------------------------------------ MMA issuers
+        // The warp runs the loop converged (every lane waits, `ok` kept uniform by a vote) and
+        // lane 0 alone issues: the descriptor arithmetic stays warp-uniform.
         const bool qk_role = warp == kWarpMma || warp == kWarpMmaB;
         const int t = (warp == kWarpMma || warp == kWarpPvA) ? 0 : 1;
-        if (lane == 0 && (qk_role || !LSE)) {
+        const uint32_t leader = lane == 0 ? 1u : 0u;
+        if (qk_role || !LSE) {
             int hq = 0, kc = 0;   // halves / key tiles this CTA processed before the item
             bool ok = true;
             for (int it = 0; ok; ++it) {
                 AttnItem w;
-                if (!(ok = take_item(it, w))) break;
-                mbar_arrive(&bars[B_ITEM_EMPTY + (it & 1)]);
+                ok = __all_sync(0xffffffffu, take_item(it, w));
+                if (!ok) break;
+                if (leader) mbar_arrive(&bars[B_ITEM_EMPTY + (it & 1)]);
                 if (w.req < 0) break;
                 const int nq = 2 * w.n_loc;   // halves of this item's key range
                 if (qk_role && LSE) {
@@ -785,50 +789,50 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     // halves) into S buffer kt & 1 of 128 columns, which the softmax frees once it has
                     // loaded the tile two before
                     constexpr uint32_t idesc_qk = idesc_f16(128, 128);
-                    const uint32_t aQ = smem_u32(sQ(t));
-                    ok = mbar_wait(&bars[B_Q_FULL], it & 1, abort_flag);
+                    const uint32_t aQ = desc_sw128_lo(smem_u32(sQ(t)), 16);
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_Q_FULL], it & 1, abort_flag));
                     for (int j = 0; ok && j < w.n_loc; ++j) {
                         const int kt = kc + j;
-                        ok = mbar_wait(&bars[B_K_FULL + (kt & 1)], (kt >> 1) & 1, abort_flag) &&
-                             (kt < 2 || mbar_wait(&bars[B_P_FULL + 2 * t + (kt & 1)], ((kt - 2) >> 1) & 1, abort_flag));
+                        ok = __all_sync(0xffffffffu,
+                                        mbar_wait(&bars[B_K_FULL + (kt & 1)], (kt >> 1) & 1, abort_flag) &&
+                                            (kt < 2 || mbar_wait(&bars[B_P_FULL + 2 * t + (kt & 1)],
+                                                                 ((kt - 2) >> 1) & 1, abort_flag)));
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t aK = smem_u32(sKs(kt & 1));
+                        const uint32_t aK = desc_sw128_lo(smem_u32(sKs(kt & 1)), 16);
                         const uint32_t tS = tmem + t * 256 + (kt & 1) * 128;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint64_t a = desc_sw128_kmajor(aQ + (kk >> 2) * 16384 + (kk & 3) * 32);
-                            const uint64_t b = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
-                            mma_bf16_ss(tS, a, b, idesc_qk, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&bars[B_S_FULL + 2 * t + (kt & 1)]);
-                        mma_commit(&bars[B_K_EMPTY + (kt & 1)]);
+                        for (int k4 = 0; k4 < D / 64; ++k4)   // 64 columns of d (one swizzle atom) a block
+                            mma_ss_k4(leader, tS, aQ + k4 * 1024, aK + k4 * 1024, kDescSw128Hi, idesc_qk,
+                                      k4 > 0 ? 1u : 0u);
+                        mma_commit_by(leader, &bars[B_S_FULL + 2 * t + (kt & 1)]);
+                        mma_commit_by(leader, &bars[B_K_EMPTY + (kt & 1)]);
                     }
-                    if (ok) mma_commit(&bars[B_Q_EMPTY]);
+                    if (ok) mma_commit_by(leader, &bars[B_Q_EMPTY]);
                 } else if (qk_role) {
                     // Q K^T of half q = 2j + h of local key tile j: keys 64h .. 64h+63 into S buffer
                     // (hq + q) & 1, which the half two before it (P V done) frees
                     constexpr uint32_t idesc_qk = idesc_f16(128, 64);
-                    const uint32_t aQ = smem_u32(sQ(t));
-                    ok = mbar_wait(&bars[B_Q_FULL], it & 1, abort_flag);
+                    const uint32_t aQ = desc_sw128_lo(smem_u32(sQ(t)), 16);
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_Q_FULL], it & 1, abort_flag));
                     for (int q = 0; ok && q < nq; ++q) {
                         const int hg = hq + q, kt = kc + (q >> 1), h = q & 1;
-                        ok = (h == 1 || mbar_wait(&bars[B_K_FULL + (kt & 1)], (kt >> 1) & 1, abort_flag)) &&
-                             (hg < 2 || mbar_wait(&bars[B_PV_DONE + 2 * t + (hg & 1)], ((hg - 2) >> 1) & 1, abort_flag));
+                        ok = __all_sync(0xffffffffu,
+                                        (h == 1 || mbar_wait(&bars[B_K_FULL + (kt & 1)], (kt >> 1) & 1, abort_flag)) &&
+                                            (hg < 2 || mbar_wait(&bars[B_PV_DONE + 2 * t + (hg & 1)],
+                                                                 ((hg - 2) >> 1) & 1, abort_flag)));
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t aK = smem_u32(sKs(kt & 1)) + h * 64 * 128;
+                        const uint32_t aK = desc_sw128_lo(smem_u32(sKs(kt & 1)) + h * 64 * 128, 16);
                         const uint32_t tS = tmem + t * 128 + (hg & 1) * 64;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint64_t a = desc_sw128_kmajor(aQ + (kk >> 2) * 16384 + (kk & 3) * 32);
-                            const uint64_t b = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
-                            mma_bf16_ss(tS, a, b, idesc_qk, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&bars[B_S_FULL + 2 * t + (hg & 1)]);
-                        if (h == 1) mma_commit(&bars[B_K_EMPTY + (kt & 1)]);
+                        for (int k4 = 0; k4 < D / 64; ++k4)
+                            mma_ss_k4(leader, tS, aQ + k4 * 1024, aK + k4 * 1024, kDescSw128Hi, idesc_qk,
+                                      k4 > 0 ? 1u : 0u);
+                        mma_commit_by(leader, &bars[B_S_FULL + 2 * t + (hg & 1)]);
+                        if (h == 1) mma_commit_by(leader, &bars[B_K_EMPTY + (kt & 1)]);
                     }
-                    if (ok) mma_commit(&bars[B_Q_EMPTY]);
+                    if (ok) mma_commit_by(leader, &bars[B_Q_EMPTY]);
                 } else {
                     // O += P(q) V(q): M=128, N=d in one instruction, K=64 keys in four steps; the
                     // item's first P V overwrites O once the softmax has read the previous item's
@@ -836,28 +840,27 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     const uint32_t tO = tmem + kTmemO + t * 128;
                     for (int q = 0; ok && q < nq; ++q) {
                         const int hg = hq + q, kt = kc + (q >> 1), h = q & 1;
-                        ok = mbar_wait(&bars[B_P_FULL + 2 * t + (hg & 1)], (hg >> 1) & 1, abort_flag) &&
-                             (h == 1 || mbar_wait(&bars[B_V_FULL + (kt & 1)], (kt >> 1) & 1, abort_flag)) &&
-                             (q > 0 || it == 0 || mbar_wait(&bars[B_O_FREE + t], (it - 1) & 1, abort_flag));
+                        ok = __all_sync(0xffffffffu,
+                                        mbar_wait(&bars[B_P_FULL + 2 * t + (hg & 1)], (hg >> 1) & 1, abort_flag) &&
+                                            (h == 1 || mbar_wait(&bars[B_V_FULL + (kt & 1)], (kt >> 1) & 1, abort_flag)) &&
+                                            (q > 0 || it == 0 ||
+                                             mbar_wait(&bars[B_O_FREE + t], (it - 1) & 1, abort_flag)));
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t aV = smem_u32(sVs(kt & 1)) + h * 64 * 128;
+                        const uint32_t aV = desc_sw128_lo(smem_u32(sVs(kt & 1)) + h * 64 * 128, 16384);
                         const uint32_t tP = tmem + t * 128 + (hg & 1) * 64;
-#pragma unroll
-                        for (int kk = 0; kk < 64 / 16; ++kk)
-                            mma_bf16_ts(tO, tP + kk * 8, desc_sw128_mn(aV + kk * 2048, 16384), idesc_pv,
-                                        (q > 0 || kk > 0) ? 1u : 0u);
-                        mma_commit(&bars[B_PV_DONE + 2 * t + (hg & 1)]);
-                        if (h == 1) mma_commit(&bars[B_V_EMPTY + (kt & 1)]);
+                        mma_ts_k4(leader, tO, tP, aV, kDescSw128Hi, idesc_pv, q > 0 ? 1u : 0u);
+                        mma_commit_by(leader, &bars[B_PV_DONE + 2 * t + (hg & 1)]);
+                        if (h == 1) mma_commit_by(leader, &bars[B_V_EMPTY + (kt & 1)]);
                     }
-                    if (ok) mma_commit(&bars[B_O_DONE + t]);
+                    if (ok) mma_commit_by(leader, &bars[B_O_DONE + t]);
                 }
                 hq += nq;
                 kc += w.n_loc;
             }
             const int di = (qk_role ? 0 : 2) + t;
-            mma_commit(&bars[B_DRAIN + di]);
-            mbar_drain(&bars[B_DRAIN + di], 0);
+            mma_commit_by(leader, &bars[B_DRAIN + di]);
+            if (leader) mbar_drain(&bars[B_DRAIN + di], 0);
         }
     } else {
         // ------------------------------------------------------------ softmax (warps 0-7)

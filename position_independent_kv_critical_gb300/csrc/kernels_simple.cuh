@@ -34,111 +34,221 @@ struct RopeJob {
     __nv_bfloat16* v_out;    //   V rows, [heads][n_out][D] like out
     int32_t* pos_out;        //   logical position of every compacted row
     int32_t n_out;           //   compacted rows
-    int32_t hpt;             // heads per thread (a multiple of 4, or all of them)
 };
 
-// One thread per (row, group of hpt heads, 16-byte chunk pair c): the row's position, its cos/sin
-// values and (in page gather mode) its page and compacted row are fetched once for the group,
-// whose heads are loaded four at a time.  Large jobs take all heads per thread (the least
-// repeated work); small ones split the heads for parallelism.
-template <int D>
-__global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob a, RopeJob b, RopeJob c3,
-                                                        const float2* __restrict__ rope, int32_t max_pos,
-                                                        int64_t n_a, int64_t n_ab, int32_t* __restrict__ zero,
-                                                        int32_t n_zero) {
+// The work is cut into tiles of 16 rows (one page in page gather mode) x up to 8 heads; a tile's
+// bf16 rows and the cos/sin rows of its 16 positions are staged in shared memory by bulk copies
+// (a page's heads are contiguous in the pool, so one copy each for K and V; a row's heads are
+// contiguous in row mode, so one copy per row), on a ring of stages filled by one producer warp.
+// The rotation reads shared memory only, so the bytes in flight per SM are set by the ring, not
+// by registers: the per-row lookups (page, position, compacted row) are dependent loads, and a
+// thread-per-row kernel that holds its data in registers runs out of warps to hide them with.
+constexpr int kRopeRows = 16;            // rows of a tile
+constexpr int kRopeHeads = 8;            // heads of a tile
+constexpr int kRopeConsumerWarps = 16;   // four per SM sub-partition: the rotation is latency-bound
+constexpr int kRopeThreads = (kRopeConsumerWarps + 1) * 32;   // + the producer warp
+
+// A stage holds a tile's K rows (and V rows when the launch copies V) plus the cos/sin rows of its
+// 16 positions; the ring takes as many stages as fit (the bytes in flight per SM are what keeps
+// HBM busy: about one DRAM latency's worth of copy bandwidth, some 60 KB, beside the stage being
+// rotated).
+template <int D, bool WITH_V>
+struct RopeSmem {
+    static constexpr uint32_t kX = kRopeRows * kRopeHeads * D * 2;   // a tile's rows of K or V
+    static constexpr uint32_t kCs = kRopeRows * D * 4;               // cos/sin of 16 positions
+    static constexpr uint32_t kStage = (WITH_V ? 2 : 1) * kX + kCs;
+    static constexpr int kStages = (int)((232448u - 1024u) / kStage) < 8 ? (int)((232448u - 1024u) / kStage) : 8;
+    static constexpr uint32_t kMeta = kStages * kStage;              // int4 per stage
+    static constexpr uint32_t kFull = kMeta + kStages * 16;          // mbarriers
+    static constexpr uint32_t kEmpty = kFull + kStages * 8;
+    static constexpr uint32_t kAbort = kEmpty + kStages * 8;
+    static constexpr uint32_t kBytes = kAbort + 16;
+    static_assert(kStages >= 2 && kBytes <= 232448, "rotation ring exceeds shared memory");
+};
+
+// A tile of one of the three jobs: rows [r0, r0 + nr), heads [h0, h0 + G).
+struct RopeTile {
+    int job;
+    int32_t r0, nr, h0, G;
+};
+__device__ __forceinline__ RopeTile rope_tile(int64_t t, int64_t t_a, int64_t t_ab, const RopeJob& a,
+                                              const RopeJob& b, const RopeJob& c3) {
+    RopeTile T;
+    T.job = t < t_a ? 0 : (t < t_ab ? 1 : 2);
+    const RopeJob& J = T.job == 0 ? a : (T.job == 1 ? b : c3);
+    const int64_t local = t - (T.job == 0 ? 0 : (T.job == 1 ? t_a : t_ab));
+    const int ng = (J.heads + kRopeHeads - 1) / kRopeHeads;
+    T.r0 = (int32_t)(local / ng) * kRopeRows;
+    T.h0 = (int32_t)(local % ng) * kRopeHeads;
+    T.nr = min(kRopeRows, J.n_rows - T.r0);
+    T.G = min(kRopeHeads, J.heads - T.h0);
+    return T;
+}
+
+// Persistent: CTA b takes tiles b, b + gridDim.x, ...  Tiles are numbered job by job; a job's
+// tiles run row block by row block, head groups fastest (neighbouring tiles share cos/sin rows).
+// WITH_V: some job of the launch copies V rows (the compacted cached keys); the others must not.
+template <int D, bool WITH_V>
+__global__ void __launch_bounds__(kRopeThreads, 1) rope_rows_kernel(RopeJob a, RopeJob b, RopeJob c3,
+                                                                    const float2* __restrict__ rope, int32_t max_pos,
+                                                                    int64_t t_a, int64_t t_ab, int64_t t_all,
+                                                                    int32_t* __restrict__ zero, int32_t n_zero) {
+    using SM = RopeSmem<D, WITH_V>;
+    constexpr int kRopeStages = SM::kStages;
     constexpr int CPR = D / 16;   // 16-byte chunk pairs per head row
-    constexpr int HB = 4;         // heads per thread
-    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    int4* s_meta = reinterpret_cast<int4*>(smem + SM::kMeta);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kFull);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + SM::kEmpty);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::kAbort);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < kRopeStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kRopeConsumerWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
     grid_dep_wait();
     grid_dep_launch();
     // counters of the kernels that follow, cleared here rather than by a separate memset
-    for (int64_t i = gid; i < n_zero; i += (int64_t)gridDim.x * blockDim.x) zero[i] = 0;
-    RopeJob J;   // a copy in registers (a reference into the parameters would go through the stack)
-    if (gid < n_a) J = a;
-    else if (gid < n_ab) J = b;
-    else J = c3;
-    const int64_t lid = gid < n_a ? gid : (gid < n_ab ? gid - n_a : gid - n_ab);
-    const int ng = (J.heads + J.hpt - 1) / J.hpt;
-    if (J.x == nullptr || lid >= (int64_t)J.n_rows * ng * CPR) return;
-    const int c = (int)(lid % CPR);
-    const int hbeg = (int)((lid / CPR) % ng) * J.hpt;
-    const int hend = min(J.heads, hbeg + J.hpt);
-    const int32_t row = (int32_t)(lid / CPR / ng);
-    int32_t p;
-    const __nv_bfloat16* src0;    // head 0 of the row
-    const __nv_bfloat16* vsrc0 = nullptr;
-    int64_t hstride;              // elements from one head of the row to the next
-    int32_t orow_n = J.n_rows, oi = row;
-    if (J.blk != nullptr) {
-        const int32_t ph = J.blk[row / kPage];
-        if (ph < 0 || ph >= J.n_phys) { set_dev_error(kDevErrBounds); return; }
-        p = J.page_pos[row / kPage] + row % kPage;
-        const int64_t off = ((int64_t)ph * J.heads * kPage + row % kPage) * D;
-        src0 = J.x + off;
-        hstride = (int64_t)kPage * D;
-        if (J.excl != nullptr) {
-            const uint32_t ex = J.excl[row / kPage], bit = 1u << (row % kPage);
-            if (ex & bit) return;   // recomputed: its fresh row replaces it
-            oi = J.cidx[row / kPage] + row % kPage - __popc(ex & (bit - 1u));   // kept tokens before it
-            orow_n = J.n_out;
-            if (oi < 0 || oi >= J.n_out) { set_dev_error(kDevErrBounds); return; }
-            vsrc0 = J.v_src + off;
-            if (c == 0 && hbeg == 0) J.pos_out[oi] = p;
-        }
-    } else {
-        p = J.pos[row];
-        src0 = J.x + (int64_t)row * J.heads * D;
-        hstride = D;
-    }
-    if (p < 0 || p >= max_pos) { set_dev_error(kDevErrBounds); return; }
-    const float4* cs4 = reinterpret_cast<const float4*>(rope + (int64_t)p * (D / 2) + 8 * c);
-    float cs[16];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float4 v = __ldg(cs4 + q);
-        cs[4 * q] = v.x; cs[4 * q + 1] = v.y; cs[4 * q + 2] = v.z; cs[4 * q + 3] = v.w;
-    }
-    float big = 0.f;   // largest rotated magnitude of the row: above fp16's range it is an error
-    for (int h0 = hbeg; h0 < hend; h0 += HB) {
-        uint4 xa[HB], xb[HB], va[HB], vb[HB];
-#pragma unroll
-        for (int k = 0; k < HB; ++k) {
-            if (h0 + k < hend) {
-                const __nv_bfloat16* src = src0 + (h0 + k) * hstride;
-                xa[k] = *reinterpret_cast<const uint4*>(src + 8 * c);
-                xb[k] = *reinterpret_cast<const uint4*>(src + D / 2 + 8 * c);
-                if (vsrc0 != nullptr) {
-                    const __nv_bfloat16* vs = vsrc0 + (h0 + k) * hstride;
-                    va[k] = *reinterpret_cast<const uint4*>(vs + 8 * c);
-                    vb[k] = *reinterpret_cast<const uint4*>(vs + D / 2 + 8 * c);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + tid; i < n_zero; i += (int64_t)gridDim.x * blockDim.x)
+        zero[i] = 0;
+
+    if (warp == kRopeConsumerWarps) {
+        // ---------------- producer: metadata, then the bulk copies of the tile
+        int64_t issued = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < t_all; t += gridDim.x, ++issued) {
+            const int s = (int)(issued % kRopeStages);
+            if (issued >= kRopeStages &&
+                !mbar_wait(&empty[s], (uint32_t)((issued / kRopeStages - 1) & 1), abort_flag)) {
+                ok = false;
+                break;
+            }
+            const RopeTile T = rope_tile(t, t_a, t_ab, a, b, c3);
+            const RopeJob& J = T.job == 0 ? a : (T.job == 1 ? b : c3);
+            uint8_t* xs = smem + s * SM::kStage;
+            uint8_t* vs = xs + SM::kX;
+            uint8_t* cs = vs + (WITH_V ? SM::kX : 0);
+            uint32_t valid = 0, ex = 0;
+            int32_t ci = 0, pp = 0, ph = 0;
+            if (J.blk != nullptr) {   // one page, all of its rows
+                const int32_t page = T.r0 / kRopeRows;
+                if (lane == 0) {
+                    ph = J.blk[page];
+                    pp = J.page_pos[page];
+                    if (J.excl != nullptr) {
+                        ex = J.excl[page];
+                        ci = J.cidx[page];
+                    }
+                    if (ph < 0 || ph >= J.n_phys || pp < 0 || pp > max_pos - kRopeRows) {
+                        set_dev_error(kDevErrBounds);
+                    } else {
+                        valid = (T.nr >= 32 ? 0xFFFFFFFFu : ((1u << T.nr) - 1u)) & ~ex;
+                    }
+                }
+                valid = __shfl_sync(0xffffffffu, valid, 0);
+                ph = __shfl_sync(0xffffffffu, ph, 0);
+                pp = __shfl_sync(0xffffffffu, pp, 0);
+                const uint32_t xb = (uint32_t)T.G * kRopeRows * D * 2;
+                const bool with_v = WITH_V && J.v_src != nullptr;
+                if (lane == 0) {
+                    s_meta[s] = make_int4((int)valid, (int)ex, ci, pp);
+                    mbar_arrive_expect_tx(&full[s], valid ? xb * (with_v ? 2u : 1u) + kRopeRows * D * 4 : 0u);
+                }
+                __syncwarp();
+                if (valid) {
+                    const int64_t off = ((int64_t)ph * J.heads + T.h0) * kRopeRows * D;
+                    if (lane == 0) bulk_load(xs, J.x + off, xb, &full[s]);
+                    if (lane == 1 && with_v) bulk_load(vs, J.v_src + off, xb, &full[s]);
+                    if (lane == 2) bulk_load(cs, rope + (int64_t)pp * (D / 2), kRopeRows * D * 4, &full[s]);
+                }
+            } else {                   // 16 rows at their own positions
+                int32_t p = 0;
+                bool v = false;
+                if (lane < T.nr) {
+                    p = J.pos[T.r0 + lane];
+                    v = p >= 0 && p < max_pos;
+                    if (!v) set_dev_error(kDevErrBounds);
+                }
+                valid = __ballot_sync(0xffffffffu, v);
+                const uint32_t rb = (uint32_t)T.G * D * 2;
+                if (lane == 0) {
+                    s_meta[s] = make_int4((int)valid, 0, 0, 0);
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(valid) * (rb + D * 4));
+                }
+                __syncwarp();
+                if (v) {
+                    bulk_load(xs + lane * rb, J.x + ((int64_t)(T.r0 + lane) * J.heads + T.h0) * D, rb, &full[s]);
+                    bulk_load(cs + lane * D * 4, rope + (int64_t)p * (D / 2), D * 4, &full[s]);
                 }
             }
         }
-#pragma unroll
-        for (int k = 0; k < HB; ++k) {
-            const int h = h0 + k;
-            if (h >= hend) break;
-            const uint32_t ia[4] = {xa[k].x, xa[k].y, xa[k].z, xa[k].w};
-            const uint32_t ib[4] = {xb[k].x, xb[k].y, xb[k].z, xb[k].w};
+        if (!ok) {   // an abort: let the copies still in flight land before the CTA exits
+            if (lane == 0)
+                for (int64_t j = issued > kRopeStages ? issued - kRopeStages : 0; j < issued; ++j)
+                    mbar_drain(&full[j % kRopeStages], (uint32_t)((j / kRopeStages) & 1));
+        }
+        return;
+    }
+
+    // ---------------- consumers: rotate from shared memory, store fp16 (and the kept V rows)
+    float big = 0.f;   // largest rotated magnitude: above fp16's range it is an error
+    int64_t k = 0;
+    for (int64_t t = blockIdx.x; t < t_all; t += gridDim.x, ++k) {
+        const int s = (int)(k % kRopeStages);
+        if (!mbar_wait(&full[s], (uint32_t)((k / kRopeStages) & 1), abort_flag)) break;
+        const RopeTile T = rope_tile(t, t_a, t_ab, a, b, c3);
+        const RopeJob& J = T.job == 0 ? a : (T.job == 1 ? b : c3);
+        const int4 meta = s_meta[s];
+        const uint32_t valid = (uint32_t)meta.x, ex = (uint32_t)meta.y;
+        const uint8_t* xs = smem + s * SM::kStage;
+        const uint8_t* vs = xs + SM::kX;
+        const uint8_t* cs = vs + (WITH_V ? SM::kX : 0);
+        const bool paged = J.blk != nullptr, compact = paged && J.excl != nullptr;
+        const int32_t orow_n = compact ? J.n_out : J.n_rows;
+        constexpr int kItems = kRopeRows * kRopeHeads * CPR;   // (row, head, chunk pair), chunk pairs fastest
+        for (int it = tid; it < kItems; it += kRopeConsumerWarps * 32) {
+            const int c = it % CPR, h = (it / CPR) % kRopeHeads, r = it / (CPR * kRopeHeads);
+            if (h >= T.G || !((valid >> r) & 1u)) continue;
+            int32_t oi = T.r0 + r;
+            if (compact) {
+                oi = meta.z + r - __popc(ex & ((1u << r) - 1u));   // kept tokens of the page before it
+                if (oi < 0 || oi >= J.n_out) { set_dev_error(kDevErrBounds); continue; }
+                if (c == 0 && T.h0 + h == 0) J.pos_out[oi] = meta.w + r;
+            }
+            const int idx = paged ? h * kRopeRows + r : r * T.G + h;
+            const uint4 xa = *reinterpret_cast<const uint4*>(xs + idx * D * 2 + c * 16);
+            const uint4 xb = *reinterpret_cast<const uint4*>(xs + idx * D * 2 + D + c * 16);
+            const float4* cs4 = reinterpret_cast<const float4*>(cs + r * D * 4 + c * 64);
+            const uint32_t ia[4] = {xa.x, xa.y, xa.z, xa.w};
+            const uint32_t ib[4] = {xb.x, xb.y, xb.z, xb.w};
             uint32_t oa[4], ob[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float c0 = cs[4 * e], s0 = cs[4 * e + 1], c1 = cs[4 * e + 2], s1 = cs[4 * e + 3];
+                const float4 q = cs4[e];   // cos, sin of two consecutive frequencies
                 const float a0 = bf16_lo(ia[e]) * J.scale, a1 = bf16_hi(ia[e]) * J.scale;
                 const float b0 = bf16_lo(ib[e]) * J.scale, b1 = bf16_hi(ib[e]) * J.scale;
-                oa[e] = pack_f16x2_track(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1), big);
-                ob[e] = pack_f16x2_track(fmaf(b0, c0, a0 * s0), fmaf(b1, c1, a1 * s1), big);
+                oa[e] = pack_f16x2_track(fmaf(a0, q.x, -b0 * q.y), fmaf(a1, q.z, -b1 * q.w), big);
+                ob[e] = pack_f16x2_track(fmaf(b0, q.x, a0 * q.y), fmaf(b1, q.z, a1 * q.w), big);
             }
-            const int64_t orow = ((int64_t)(h / J.gg) * orow_n + oi) * J.gg + (h % J.gg);
+            const int hh = T.h0 + h;
+            const int64_t orow = ((int64_t)(hh / J.gg) * orow_n + oi) * J.gg + (hh % J.gg);
             __half* dst = J.out + orow * D;
             *reinterpret_cast<uint4*>(dst + 8 * c) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
             *reinterpret_cast<uint4*>(dst + D / 2 + 8 * c) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-            if (vsrc0 != nullptr) {   // the compacted token's V row, unchanged
+            if (WITH_V && compact && J.v_src != nullptr) {   // the kept token's V row, unchanged
                 __nv_bfloat16* vd = J.v_out + orow * D;
-                *reinterpret_cast<uint4*>(vd + 8 * c) = va[k];
-                *reinterpret_cast<uint4*>(vd + D / 2 + 8 * c) = vb[k];
+                *reinterpret_cast<uint4*>(vd + 8 * c) = *reinterpret_cast<const uint4*>(vs + idx * D * 2 + c * 16);
+                *reinterpret_cast<uint4*>(vd + D / 2 + 8 * c) =
+                    *reinterpret_cast<const uint4*>(vs + idx * D * 2 + D + c * 16);
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
     }
     if (!(big < kF16Limit)) set_dev_error(kDevErrRange);
 }

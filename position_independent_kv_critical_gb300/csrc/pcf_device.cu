@@ -256,25 +256,32 @@ pcf_status set_smem(K kernel, int bytes) {
     return PCF_OK;
 }
 
-// threads of a RoPE job: one per (row, head group, chunk pair); a job with enough rows to fill the
-// GPU a few times over takes all heads per thread, a smaller one groups of four
-template <int D>
-int64_t rope_threads(RopeJob& j) {
-    if (!j.x) return 0;
-    const int64_t rows_x = (int64_t)j.n_rows * (D / 16);
-    j.hpt = rows_x >= 4 * device_sms() * 256 ? j.heads : 4;
-    return rows_x * ((j.heads + j.hpt - 1) / j.hpt);
+// tiles of a RoPE job: 16-row blocks x groups of 8 heads
+int64_t rope_tiles(const RopeJob& j) {
+    if (!j.x || j.n_rows <= 0 || j.heads <= 0) return 0;
+    return (int64_t)((j.n_rows + kRopeRows - 1) / kRopeRows) * ((j.heads + kRopeHeads - 1) / kRopeHeads);
 }
 
 template <int D>
 pcf_status launch_rope(RopeJob a, RopeJob b, RopeJob c, const float2* rope, int32_t max_pos, cudaStream_t st,
                        int32_t* zero = nullptr, int32_t n_zero = 0) {
-    const int64_t n_a = rope_threads<D>(a), n_b = rope_threads<D>(b), n_c = rope_threads<D>(c);
-    const int64_t n = std::max<int64_t>(n_a + n_b + n_c, n_zero);
-    if (n == 0) return PCF_OK;
-    const int64_t blocks = (n + 255) / 256;
-    return launch(rope_rows_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, st, a, b, c, rope, max_pos, n_a,
-                  n_a + n_b, zero, n_zero);
+    // a job without rows takes no tiles
+    if (!a.x || a.n_rows <= 0) a.x = nullptr;
+    if (!b.x || b.n_rows <= 0) b.x = nullptr;
+    if (!c.x || c.n_rows <= 0) c.x = nullptr;
+    const int64_t t_a = rope_tiles(a), t_ab = t_a + rope_tiles(b), t_all = t_ab + rope_tiles(c);
+    if (t_all == 0 && n_zero == 0) return PCF_OK;
+    // persistent: one CTA per SM (the ring takes most of its shared memory), fewer for small jobs
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(t_all, device_sms()));
+    const bool with_v = (a.x && a.v_src) || (b.x && b.v_src) || (c.x && c.v_src);
+    auto go = [&](auto kernel, uint32_t bytes) -> pcf_status {
+        pcf_status s = set_smem(kernel, (int)bytes);
+        if (s != PCF_OK) return s;
+        return launch(kernel, dim3((unsigned)blocks), dim3(kRopeThreads), bytes, st, a, b, c, rope, max_pos, t_a,
+                      t_ab, t_all, zero, n_zero);
+    };
+    return with_v ? go(rope_rows_kernel<D, true>, RopeSmem<D, true>::kBytes)
+                  : go(rope_rows_kernel<D, false>, RopeSmem<D, false>::kBytes);
 }
 
 // the batch's cached keys, gathered from their pages and rotated to each request's positions
@@ -282,7 +289,7 @@ RopeJob cached_key_job(const pcf_layout* lay, const uint16_t* k_pool, __half* kc
     const int32_t* H = lay->host;
     return RopeJob{reinterpret_cast<const __nv_bfloat16*>(k_pool), nullptr, kc, H[L_TOTAL_TOKENS], H[L_HKV], 1, 1.f,
                    lay->dev + H[L_OFF_BLOCK], lay->dev + H[L_OFF_PAGEPOS], H[L_N_PHYS],
-                   nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+                   nullptr, nullptr, nullptr, nullptr, nullptr, 0};
 }
 // the cached keys that take part in the attention, compacted (rotated K, V copied, positions)
 RopeJob kept_key_job(const pcf_layout* lay, const uint16_t* k_pool, const uint16_t* v_pool, const uint16_t* excl,
@@ -314,9 +321,9 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
 
     const int32_t n_cnt = H[L_TOTAL_KTILES] + 1;   // cleared by the rotation kernel
     RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_query), lay->dev + H[L_OFF_QPOS], q_rot, H[L_TOTAL_QUERY],
-               H[L_HQ], g, scale_log2, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+               H[L_HQ], g, scale_log2, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0};
     RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
-                 nullptr, 0, 4};
+                 nullptr, 0};
     pcf_status s = launch_rope<D>(qj, cached_key_job(lay, k_pool, kc), none, rope2, H[L_MAX_POS], st, cnt, n_cnt);
     if (s != PCF_OK) return s;
 
@@ -382,9 +389,9 @@ pcf_status score_paged_impl(const pcf_layout* lay, const uint16_t* q_query, cons
     const float2* rope2 = reinterpret_cast<const float2*>(rope);
     const int32_t n_cnt = H[L_TOTAL_KTILES] + 1;   // cleared by the rotation kernel
     RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_query), lay->dev + H[L_OFF_QPOS], q_rot, H[L_TOTAL_QUERY],
-               H[L_HQ], g, scale_log2, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+               H[L_HQ], g, scale_log2, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0};
     RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
-                 nullptr, 0, 4};
+                 nullptr, 0};
     pcf_status s = launch_rope<D>(qj, none, none, rope2, H[L_MAX_POS], st, cnt, n_cnt);
     if (s != PCF_OK) return s;
 
@@ -443,9 +450,9 @@ pcf_status attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, const 
     const int32_t rows = H[L_TOTAL_ROWS];
     const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_fresh), row_pos, q_rot, rows, H[L_HQ], g, scale_log2,
-               nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+               nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0};
     RopeJob kj{reinterpret_cast<const __nv_bfloat16*>(k_fresh), row_pos, k_rot, rows, H[L_HKV], 1, 1.f,
-               nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+               nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0};
     pcf_status s;
     if (H[L_TOTAL_PAGES] > 0) {
         if ((s = launch(compact_scan_kernel, dim3(H[L_N_REQS]), dim3(kScanThreads), 0, st, lay->dev, excl, cidx)) !=
@@ -516,11 +523,11 @@ pcf_status paged_attention_impl(const pcf_layout* lay, const uint16_t* q_fresh, 
     const int32_t rows = H[L_TOTAL_ROWS];
     const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     RopeJob qj{reinterpret_cast<const __nv_bfloat16*>(q_fresh), row_pos, q_rot, rows, H[L_HQ], g, scale_log2,
-               nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+               nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0};
     RopeJob kj{reinterpret_cast<const __nv_bfloat16*>(k_fresh), row_pos, k_rot, rows, H[L_HKV], 1, 1.f,
-               nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 4};
+               nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr, 0};
     RopeJob none{nullptr, nullptr, nullptr, 0, 0, 1, 1.f, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
-                 nullptr, 0, 4};
+                 nullptr, 0};
     pcf_status s;
     // per page, the request's kept tokens before it: a recomputed token's rank among the request's
     // recomputed rows follows from it, and the attention kernel puts that fresh row in its place

@@ -210,6 +210,60 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Four K = 16 steps of D[tmem] (+)= A[smem] * B[smem]^T in one block, for a warp that runs the
+// issue loop converged: every lane executes it, only `leader`'s predicate issues.  The operands
+// are 128-byte-swizzled K-major: step kk starts 32 bytes further along K, i.e. 2 more in the low
+// word of both descriptors (whose high words, `hi`, stay fixed).  Building the descriptors in the
+// block keeps their arithmetic next to the instructions that use them.
+__device__ __forceinline__ void mma_ss_k4(uint32_t leader, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                          uint32_t hi, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred L, p, t;\n\t.reg .b64 da, db;\n\t.reg .b32 la, lb;\n\t"
+        "setp.ne.b32 L, %0, 0;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.eq.b32 t, %0, %0;\n\t"
+        "mov.b64 da, {%2, %4};\n\tmov.b64 db, {%3, %4};\n\t"
+        "@L tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %5, p;\n\t"
+        "add.u32 la, %2, 2;\n\tadd.u32 lb, %3, 2;\n\t"
+        "mov.b64 da, {la, %4};\n\tmov.b64 db, {lb, %4};\n\t"
+        "@L tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %5, t;\n\t"
+        "add.u32 la, %2, 4;\n\tadd.u32 lb, %3, 4;\n\t"
+        "mov.b64 da, {la, %4};\n\tmov.b64 db, {lb, %4};\n\t"
+        "@L tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %5, t;\n\t"
+        "add.u32 la, %2, 6;\n\tadd.u32 lb, %3, 6;\n\t"
+        "mov.b64 da, {la, %4};\n\tmov.b64 db, {lb, %4};\n\t"
+        "@L tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %5, t;\n\t}\n" ::"r"(leader),
+        "r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Four K = 16 steps of D[tmem] (+)= A[tmem] * B[smem]^T (A: 8 TMEM columns a step; B MN-major,
+// 128-byte swizzle, 2048 bytes a step, i.e. 128 more in the descriptor's low word).
+__device__ __forceinline__ void mma_ts_k4(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                          uint32_t hi, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred L, p, t;\n\t.reg .b64 db;\n\t.reg .b32 ta, lb;\n\t"
+        "setp.ne.b32 L, %0, 0;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.eq.b32 t, %0, %0;\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "@L tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], db, %5, p;\n\t"
+        "add.u32 ta, %2, 8;\n\tadd.u32 lb, %3, 128;\n\tmov.b64 db, {lb, %4};\n\t"
+        "@L tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], db, %5, t;\n\t"
+        "add.u32 ta, %2, 16;\n\tadd.u32 lb, %3, 256;\n\tmov.b64 db, {lb, %4};\n\t"
+        "@L tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], db, %5, t;\n\t"
+        "add.u32 ta, %2, 24;\n\tadd.u32 lb, %3, 384;\n\tmov.b64 db, {lb, %4};\n\t"
+        "@L tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], db, %5, t;\n\t}\n" ::"r"(leader),
+        "r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// tcgen05.commit by `leader` only (the lane that issued the MMAs), the warp converged.
+__device__ __forceinline__ void mma_commit_by(uint32_t leader, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred L;\n\tsetp.ne.b32 L, %0, 0;\n\t"
+        "@L tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}\n" ::"r"(leader),
+        "r"(smem_u32(bar))
+        : "memory");
+}
 // Arrive on `bar` once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
@@ -268,6 +322,12 @@ __device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t atom_
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(atom_stride >> 4) << 16) |
            ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
+// The same 128-byte-swizzle descriptors as two 32-bit words: the low word holds the start address
+// and the leading byte offset, the high word (fixed) the 1024-byte stride, version and swizzle.
+__device__ __forceinline__ uint32_t desc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes) {
+    return ((saddr & 0x3FFFFu) >> 4) | ((lbo_bytes >> 4) << 16);
+}
+constexpr uint32_t kDescSw128Hi = (1024u >> 4) | (1u << (46 - 32)) | (2u << (61 - 32));
 // UMMA shared-memory descriptor, no swizzle, K-major: 8-row x 16-byte core matrices; `k_stride`
 // bytes between core matrices adjacent along K, `row_stride` bytes between 8-row groups.
 __device__ __forceinline__ uint64_t desc_noswz_kmajor(uint32_t saddr, uint32_t k_stride, uint32_t row_stride) {
