@@ -223,13 +223,14 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 ok = ok && (s < 2 || mbar_wait(&bars[I_ACC_FREE + a], ((s >> 1) - 1) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t aK = smem_u32(sKs(kidx & 1)), aQ = smem_u32(sQs(qb));
+                // base descriptors plus constant step offsets: one thread then issues at the rate
+                // shared memory allows, where descriptors rebuilt from the address each step do not
+                const uint64_t dK = desc_sw128_kmajor(smem_u32(sKs(kidx & 1)));
+                const uint64_t dQ = desc_sw128_kmajor(smem_u32(sQs(qb)));
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t da = desc_sw128_kmajor(aK + (kk >> 2) * 16384 + (kk & 3) * 32);
-                    const uint64_t dq = desc_sw128_kmajor(aQ + (kk >> 2) * (kImpQRows * 128) + (kk & 3) * 32);
-                    mma_bf16_ss(tmem + a * kImpQRows, da, dq, idesc, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16_ss(tmem + a * kImpQRows, dK + sw128_k_step(kk), dQ + sw128_k_step(kk, kImpQRows * 128),
+                                idesc, kk > 0 ? 1u : 0u);
                 // + 1 * (-lse2_hi) + 1 * (-lse2_lo) per query row
                 mma_bf16_ss(tmem + a * kImpQRows, desc_noswz_kmajor(smem_u32(sKones), 128, 256),
                             desc_noswz_kmajor(smem_u32(sQlse(qb)), 128, 256), idesc, 1u);

@@ -45,8 +45,12 @@ struct RopeJob {
 // thread-per-row kernel that holds its data in registers runs out of warps to hide them with.
 constexpr int kRopeRows = 16;            // rows of a tile
 constexpr int kRopeHeads = 8;            // heads of a tile
-constexpr int kRopeConsumerWarps = 16;   // four per SM sub-partition: the rotation is latency-bound
-constexpr int kRopeThreads = (kRopeConsumerWarps + 1) * 32;   // + the producer warp
+// consumer warps: rotating keys alone is latency-bound and wants four per SM sub-partition; with
+// the V rows copied too the stages are larger and two per sub-partition keep up (measured)
+template <bool WITH_V>
+__host__ __device__ constexpr int rope_consumer_warps() { return WITH_V ? 8 : 16; }
+template <bool WITH_V>
+__host__ __device__ constexpr int rope_threads() { return (rope_consumer_warps<WITH_V>() + 1) * 32; }   // + the producer warp
 
 // A stage holds a tile's K rows (and V rows when the launch copies V) plus the cos/sin rows of its
 // 16 positions; the ring takes as many stages as fit (the bytes in flight per SM are what keeps
@@ -89,12 +93,13 @@ __device__ __forceinline__ RopeTile rope_tile(int64_t t, int64_t t_a, int64_t t_
 // tiles run row block by row block, head groups fastest (neighbouring tiles share cos/sin rows).
 // WITH_V: some job of the launch copies V rows (the compacted cached keys); the others must not.
 template <int D, bool WITH_V>
-__global__ void __launch_bounds__(kRopeThreads, 1) rope_rows_kernel(RopeJob a, RopeJob b, RopeJob c3,
+__global__ void __launch_bounds__(rope_threads<WITH_V>(), 1) rope_rows_kernel(RopeJob a, RopeJob b, RopeJob c3,
                                                                     const float2* __restrict__ rope, int32_t max_pos,
                                                                     int64_t t_a, int64_t t_ab, int64_t t_all,
                                                                     int32_t* __restrict__ zero, int32_t n_zero) {
     using SM = RopeSmem<D, WITH_V>;
     constexpr int kRopeStages = SM::kStages;
+    constexpr int kRopeConsumerWarps = rope_consumer_warps<WITH_V>();
     constexpr int CPR = D / 16;   // 16-byte chunk pairs per head row
     extern __shared__ __align__(1024) uint8_t smem[];
     int4* s_meta = reinterpret_cast<int4*>(smem + SM::kMeta);

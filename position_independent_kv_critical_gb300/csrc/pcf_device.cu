@@ -274,14 +274,14 @@ pcf_status launch_rope(RopeJob a, RopeJob b, RopeJob c, const float2* rope, int3
     // persistent: one CTA per SM (the ring takes most of its shared memory), fewer for small jobs
     const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(t_all, device_sms()));
     const bool with_v = (a.x && a.v_src) || (b.x && b.v_src) || (c.x && c.v_src);
-    auto go = [&](auto kernel, uint32_t bytes) -> pcf_status {
+    auto go = [&](auto kernel, uint32_t bytes, int threads) -> pcf_status {
         pcf_status s = set_smem(kernel, (int)bytes);
         if (s != PCF_OK) return s;
-        return launch(kernel, dim3((unsigned)blocks), dim3(kRopeThreads), bytes, st, a, b, c, rope, max_pos, t_a,
-                      t_ab, t_all, zero, n_zero);
+        return launch(kernel, dim3((unsigned)blocks), dim3(threads), bytes, st, a, b, c, rope, max_pos, t_a, t_ab,
+                      t_all, zero, n_zero);
     };
-    return with_v ? go(rope_rows_kernel<D, true>, RopeSmem<D, true>::kBytes)
-                  : go(rope_rows_kernel<D, false>, RopeSmem<D, false>::kBytes);
+    return with_v ? go(rope_rows_kernel<D, true>, RopeSmem<D, true>::kBytes, rope_threads<true>())
+                  : go(rope_rows_kernel<D, false>, RopeSmem<D, false>::kBytes, rope_threads<false>());
 }
 
 // the batch's cached keys, gathered from their pages and rotated to each request's positions

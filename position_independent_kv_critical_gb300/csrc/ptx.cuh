@@ -328,6 +328,13 @@ __device__ __forceinline__ uint32_t desc_sw128_lo(uint32_t saddr, uint32_t lbo_b
     return ((saddr & 0x3FFFFu) >> 4) | ((lbo_bytes >> 4) << 16);
 }
 constexpr uint32_t kDescSw128Hi = (1024u >> 4) | (1u << (46 - 32)) | (2u << (61 - 32));
+// Offset, in descriptor units (16 bytes, added to the start-address field), of K = 16 step kk of a
+// 128-byte-swizzled K-major operand whose rows hold 64 elements of K per 1024-byte-stride atom
+// column (atoms of 64 K elements are `atom_bytes` apart): 32 bytes a step inside an atom.  The
+// start field cannot carry into the next field: shared addresses stay below 2^18 bytes.
+__host__ __device__ constexpr uint64_t sw128_k_step(int kk, uint32_t atom_bytes = 16384) {
+    return (uint64_t)(((uint32_t)(kk >> 2) * atom_bytes + (uint32_t)(kk & 3) * 32u) >> 4);
+}
 // UMMA shared-memory descriptor, no swizzle, K-major: 8-row x 16-byte core matrices; `k_stride`
 // bytes between core matrices adjacent along K, `row_stride` bytes between 8-row groups.
 __device__ __forceinline__ uint64_t desc_noswz_kmajor(uint32_t saddr, uint32_t k_stride, uint32_t row_stride) {
