@@ -307,6 +307,8 @@ class CacheFusion:
 
     def step(self, q_query, k_pool, v_pool, q_fresh, k_fresh, v_fresh, hidden=None, stream=None):
         L = self.layout
+        if getattr(self, "_ev_down", None) is not None:   # a step_from_host download may still read out
+            (stream if stream is not None else torch.cuda.current_stream()).wait_event(self._ev_down)
         score(L, q_query, k_pool, self.rope, self.importance, self.ws_score, stream, paged=self.paged)
         select_topk(L, self.importance, self.sel_idx, self.excl, self.row_pos, stream)
         if hidden is not None and self.gathered is not None:
@@ -322,8 +324,10 @@ class CacheFusion:
 
         The copies run on two streams of their own and overlap the kernels: the query rows go up
         first (scoring needs only them), the fresh Q/K/V rows while scoring runs, and the results
-        come down while the next step starts.  Device input buffers alternate between two slots, so
-        a step's uploads never overwrite rows the previous step's kernels may still read.  The host
+        come down while the next step runs.  Device input buffers alternate between two slots, so
+        a step's uploads never overwrite rows the previous step's kernels may still read, and so do
+        the device copies of O and the selection (slot 0 is ``out`` / ``sel_idx``), so a step's
+        kernels never wait for the previous step's results to reach the host.  The host
         inputs must stay unchanged, and ``out_h`` / ``sel_h`` unread, until ``wait_host_results()``
         (or a device synchronisation) has returned."""
         L = self.layout
@@ -337,6 +341,7 @@ class CacheFusion:
             self._h2d = torch.cuda.Stream()
             self._d2h = torch.cuda.Stream()
             self._slots = [tuple(torch.empty_like(t, device=self.out.device) for t in host_in) for _ in range(2)]
+            self._out_slots = [(self.out, self.sel_idx), (torch.empty_like(self.out), torch.empty_like(self.sel_idx))]
             self._ev_q = [torch.cuda.Event() for _ in range(2)]
             self._ev_fresh = [torch.cuda.Event() for _ in range(2)]
             self._ev_used = [torch.cuda.Event() for _ in range(2)]   # slot i's last reader is done
@@ -345,6 +350,7 @@ class CacheFusion:
             self._it = 0
         i = self._it & 1
         qq, qf, kf, vf = self._slots[i]
+        out_d, sel_d = self._out_slots[i]
         n_in = [t.numel() * t.element_size() for t in host_in]
         if any(n != d.numel() * d.element_size() for n, d in zip(n_in, self._slots[i])):
             raise ValueError("step_from_host inputs changed size between steps")
@@ -367,17 +373,17 @@ class CacheFusion:
         self._ev_fresh[i].record(self._h2d)
         main.wait_event(self._ev_q[i])
         score(L, qq, k_pool, self.rope, self.importance, self.ws_score, paged=self.paged)
-        if self._ev_down is not None:      # sel_idx and out of the previous step are on their way down
-            main.wait_event(self._ev_down)
-        select_topk(L, self.importance, self.sel_idx, self.excl, self.row_pos)
+        if self._it >= 2:                  # this slot's results of two steps ago are on the host
+            main.wait_event(self._ev_down_slot[i])
+        select_topk(L, self.importance, sel_d, self.excl, self.row_pos)
         if hidden is not None and self.gathered is not None:
-            gather_rows(L, self.sel_idx, hidden, self.gathered)
+            gather_rows(L, sel_d, hidden, self.gathered)
         main.wait_event(self._ev_fresh[i])
-        fused_attention(L, qf, kf, vf, k_pool, v_pool, self.excl, self.row_pos, self.rope, self.out,
+        fused_attention(L, qf, kf, vf, k_pool, v_pool, self.excl, self.row_pos, self.rope, out_d,
                         self.ws_attn, paged=self.paged)
         self._ev_used[i].record(main)
         self._d2h.wait_event(self._ev_used[i])
-        copies([out_h, sel_h], [self.out, self.sel_idx],
+        copies([out_h, sel_h], [out_d, sel_d],
                [out_h.numel() * out_h.element_size(), sel_h.numel() * sel_h.element_size()], self._d2h)
         self._ev_down_slot[i].record(self._d2h)
         self._ev_down = self._ev_down_slot[i]
