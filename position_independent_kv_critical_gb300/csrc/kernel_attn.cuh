@@ -2,10 +2,15 @@
 //
 // MiniPIC, section 2.1: cached keys k~_j stay unrotated in shared pages and are rotated at use time
 // to the key's per-request logical position pi(j), so score(t, j) = (R_t q_t)^T (R_pi(j) k~_j) /
-// sqrt(d).  The rotation of a request's cached keys runs once per call (rope_rows_kernel in page
-// gather mode, into the call's workspace) rather than inside this kernel: a cached key tile is
-// visited by every 256-row query block of the request, and rotating it there costs more than
-// writing and re-reading the rotated tile once.
+// sqrt(d).  Two ways to feed the cached keys:
+//   compacted (PAGED = false): the rotation runs once per call (rope_rows_kernel in page gather
+//     mode, into the call's workspace), which also leaves the recomputed tokens out and copies the
+//     kept V rows beside the kept keys; a cached key tile is visited by every 256-row query block
+//     of the request, and rotating it here costs more than writing and re-reading it once.
+//   paged (PAGED = true): K and V tiles are TMA-copied from the pool pages through the block
+//     table (one 16-row box per page), two rotator warps rotate each K tile in shared memory to
+//     the request's positions before the MMA reads it, and the recomputed tokens' fresh K and V
+//     rows overwrite their stale cached copies in place; no per-request copy of the cache.
 // QCFuse, section 2C / Phase 4 (and the sparse attention kernel of its section 3): the recomputed
 // tokens and the query tokens attend over the cached keys minus the recomputed ones plus the
 // fresh rows, keeping causal order on logical positions.
@@ -23,29 +28,31 @@
 //   warps 8/11  Q K^T issue for tile A / B (warp 8 also owns the TMEM allocation)
 //   warps 12/13 P V issue for tile A / B.  Each key tile is processed in two 64-key halves and S
 //               is double-buffered per query tile: P(q) V runs, then Q K(q+2) goes into the
-//               buffer P(q) came from, while the softmax already works on S(q+1).  Four
-//               single-thread issuers keep four independent MMA streams in flight: one thread's
-//               stream of 128-row MMAs with N <= 128 is bound by per-instruction latency (about
-//               100 cycles an instruction), not by the tensor core's rate
+//               buffer P(q) came from, while the softmax already works on S(q+1).  Four issuer
+//               warps keep four independent MMA streams in flight; each runs its loop with the
+//               whole warp converged and lane 0 issuing (measured faster than lane 0 alone)
 //   warp  9     scheduler (takes the next item, counts its visible key tiles, publishes it in one
 //               of two shared-memory slots), Q loads, K producer: rotated K tiles (compacted
 //               cached or fresh, fp16, TMA) and, per key, its logical position; 2-stage ring
-//   warp  10    V producer (TMA): compacted cached V tiles / fresh V tiles; 2-stage ring
+//   warp  10    V producer (TMA): compacted cached V tiles / fresh V tiles; 2-stage ring (paged:
+//               the pool pages, then each recomputed token's fresh V row over its cached one)
+//   warps 14/15 (paged only) rotators: each cached K tile rotated in place, the fresh keys of its
+//               recomputed tokens written over their cached copies
 // TMEM: tile t's two S half-buffers at columns t*128 + {0, 64} (64 fp32 columns = 64 keys each),
 // O_A at [256,256+d), O_B at [384,384+d).  S = Q K^T is fp16 x fp16 (M=128, N=64 keys, K=d); P
 // (bf16 pairs, 32 columns) overwrites the S half it came from and is the A operand of
 // O += P V (M=128, N=d in one instruction, K=64 keys, V as an MN-major bf16 operand whose two
 // 64-wide halves are 16 KB apart).
-// The cached keys arrive compacted: recomputed tokens' cached copies are left out of the rotated
-// K/V copy, so every cached key streamed takes part.  Key positions increase along the cached
+// Compacted, every cached key streamed takes part; paged, a recomputed token's slot holds its
+// fresh row, and only the query rows form fresh tiles.  Key positions increase along the cached
 // keys and along the fresh rows, and missing keys (past a ragged end) carry position kNoPos, so a
 // row's visible keys in a tile are a prefix of it; only rows whose causal limit falls inside a
 // tile need per-element masking.
 // LSE mode (critical-layer scoring, pass 1) runs the same pipeline without P/V and writes the
 // per-row running max and sum of one key chunk (the importance kernel combines a row's chunks).  Having no O, it gives each query tile two S
 // buffers of a whole key tile (128 columns) and issues Q K^T with N = 128: half the MMA
-// instructions of two 64-key halves, and back-to-back MMAs on changing operands complete at about
-// one per 100 cycles whatever N <= 128 is.
+// instructions of two 64-key halves.  In paged scoring the two P V issuer warps, idle without
+// P V, are the rotators.
 #pragma once
 #include "layout_format.h"
 #include "ptx.cuh"
