@@ -164,19 +164,25 @@ def oracle_prepare(b):
                 kf=b.k_fresh.double().numpy(), vf=b.v_fresh.double().numpy())
 
 
-def oracle_step(b, prep, req_ids, row_stride=1):
+def oracle_step(b, prep, req_ids, row_stride=1, head_div=1):
     """The fp64 oracle on the given requests: score, per-span top-k, gather, fused attention.
     With row_stride > 1 the attention runs on every row_stride-th row only and its time counts
-    row_stride times (rows spread evenly over the causal order, so the estimate is unbiased).
-    Returns (tokens processed, seconds of oracle work those tokens take)."""
+    row_stride times (rows spread evenly over the causal order, so the estimate is unbiased); with
+    head_div > 1 everything runs on the first Hkv / head_div kv heads and their query heads (a
+    problem of the same shape with fewer heads) and its time counts head_div times.
+    Returns (tokens processed, seconds of oracle work those tokens take, wall seconds outside the
+    attention, wall seconds of the sampled attention)."""
     from oracle import method
     qb, rb = b.query_bases(), b.row_bases()
-    tokens, secs = 0, 0.0
+    hk = b.hkv // head_div
+    hq = hk * (b.hq // b.hkv)
+    kp, vp = prep["kp"][:, :hk], prep["vp"][:, :hk]
+    tokens, secs, w_fixed, w_attn = 0, 0.0, 0.0, 0.0
     for i in req_ids:
         t0 = time.perf_counter()
         r = b.requests[i]
-        K, V, kpos = method.request_cached(r.spans, prep["kp"], prep["vp"])
-        q = prep["qq"][qb[i]: qb[i] + r.n_query]
+        K, V, kpos = method.request_cached(r.spans, kp, vp)
+        q = prep["qq"][qb[i]: qb[i] + r.n_query, :hq]
         imp = method.score_request(q, r.query_pos0 + np.arange(r.n_query), K, kpos, b.theta)
         sel = method.select_topk_request(imp.astype(np.float32), [s.n_pages * 16 for s in r.spans],
                                          [s.k for s in r.spans])
@@ -184,15 +190,18 @@ def oracle_step(b, prep, req_ids, row_stride=1):
         row_pos = method.row_positions(sel, kpos, r.n_query, r.query_pos0)
         t1 = time.perf_counter()
         sl = slice(rb[i], rb[i] + r.n_rows)
-        method.fused_attention_request(prep["qf"][sl], prep["kf"][sl], prep["vf"][sl], row_pos, K, V, kpos,
-                                       sel, b.theta, rows=np.arange(0, r.n_rows, row_stride))
-        secs += (t1 - t0) + row_stride * (time.perf_counter() - t1)
+        method.fused_attention_request(prep["qf"][sl, :hq], prep["kf"][sl, :hk], prep["vf"][sl, :hk], row_pos, K, V,
+                                       kpos, sel, b.theta, rows=np.arange(0, r.n_rows, row_stride))
+        t2 = time.perf_counter()
+        secs += head_div * ((t1 - t0) + row_stride * (t2 - t1))
+        w_fixed += t1 - t0
+        w_attn += t2 - t1
         tokens += r.n_cached + r.n_query
-    return tokens, secs
+    return tokens, secs, w_fixed, w_attn
 
 
 def _oracle_sample(b):
-    """Requests and attention row stride of the bounded oracle sample (a few seconds of CPU work
+    """Requests and attention row stride of the base oracle sample (a few seconds of CPU work
     per step): whole small workloads; one request of the large ones with the attention on every
     16th row (the attention over a 16k-token request takes the fp64 oracle most of a minute)."""
     n = len(b.requests)
@@ -201,10 +210,29 @@ def _oracle_sample(b):
     return [0], 16
 
 
-def _sample_text(b, ids, stride):
+def _fit_sample(b, ids, stride, w_fixed, w_attn, budget_s):
+    """Coarsen the sample until one step is estimated to take at most budget_s of wall time: first
+    a sparser attention row sample (at least 16 rows a request), then fewer heads."""
+    max_stride = max(1, min(b.requests[i].n_rows for i in ids) // 16)
+    s, h = stride, 1
+    def est(s2, h2):
+        return (w_fixed + w_attn * stride / s2) / h2
+    while est(s, h) > budget_s:
+        if s * 2 <= max_stride:
+            s *= 2
+        elif b.hkv % (h * 2) == 0:
+            h *= 2
+        else:
+            break
+    return s, h
+
+
+def _sample_text(b, ids, stride, head_div=1):
     s = f"{len(ids)} of {len(b.requests)} requests of the {b.cfg_name} workload"
     if stride > 1:
         s += f", attention on every {stride}th row with its time counted {stride}x"
+    if head_div > 1:
+        s += f", {b.hkv // head_div} of {b.hkv} kv heads (and their query heads) with the time counted {head_div}x"
     return s
 
 
@@ -215,16 +243,21 @@ def run_reference(args):
     b = make_batch(args.config, args.pct)
     prep = oracle_prepare(b)
     ids, stride = _oracle_sample(b)
-    for _ in range(args.warmup):
-        oracle_step(b, prep, ids, stride)
+    # the whole --steps K --warmup W run is kept to about three minutes: the first warm-up step
+    # (an extra one if W = 0) measures the base sample, and the rest use a sample coarsened to fit
+    budget = 180.0 / max(1, args.steps + args.warmup)
+    _, _, w_fixed, w_attn = oracle_step(b, prep, ids, stride)
+    stride, hdiv = _fit_sample(b, ids, stride, w_fixed, w_attn, budget)
+    for _ in range(max(0, args.warmup - 1)):
+        oracle_step(b, prep, ids, stride, hdiv)
     tokens, dt = 0, 0.0
     for _ in range(args.steps):
-        tk, sec = oracle_step(b, prep, ids, stride)
+        tk, sec, _, _ = oracle_step(b, prep, ids, stride, hdiv)
         tokens += tk
         dt += sec
     value = tokens / dt
     cores = len(os.sched_getaffinity(0))
-    sample = (f"{_sample_text(b, ids, stride)} per step (score + top-k + gather + fused attention, "
+    sample = (f"{_sample_text(b, ids, stride, hdiv)} per step (score + top-k + gather + fused attention, "
               f"fp64 NumPy, BLAS threads = all cores)")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -674,7 +707,7 @@ def main():
         tok = reps = 0
         dt = 0.0
         while reps < 1 or (time.perf_counter() - t1 < 10.0 and reps < 50):
-            tk, sec = oracle_step(b, prep, ids, stride)
+            tk, sec, _, _ = oracle_step(b, prep, ids, stride)
             tok += tk
             dt += sec
             reps += 1
