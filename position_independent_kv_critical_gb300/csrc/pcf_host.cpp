@@ -485,9 +485,28 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
         span_base += r.n_spans;
         kt_base += nkt;
     }
-    std::stable_sort(attn.begin(), attn.end(), [](const AttnItem& a, const AttnItem& b) {
-        return a.cost > b.cost;
-    });
+    // Hand-out order.  With a few items per SM (small batches): longest first, so that the CTAs
+    // finishing last hold short items.  With many: grouped by (request, kv head) unit -- units in
+    // decreasing total cost, each unit's items longest first -- so that the CTAs running at one
+    // time share a few units' K/V tiles in L2 (a unit's items all read prefixes of the same keys)
+    // instead of each streaming its own unit's from DRAM; the dynamic hand-out still balances the
+    // end, where the last unit's short items run.
+    if ((int64_t)attn.size() >= 8LL * plan.n_sms) {
+        std::vector<double> ucost((size_t)n_reqs * d.n_kv_heads, 0.0);
+        for (const AttnItem& a : attn) ucost[(size_t)a.req * d.n_kv_heads + a.kvh] += a.cost;
+        std::stable_sort(attn.begin(), attn.end(), [&](const AttnItem& a, const AttnItem& b) {
+            const double ua = ucost[(size_t)a.req * d.n_kv_heads + a.kvh];
+            const double ub = ucost[(size_t)b.req * d.n_kv_heads + b.kvh];
+            if (ua != ub) return ua > ub;
+            if (a.req != b.req) return a.req < b.req;
+            if (a.kvh != b.kvh) return a.kvh < b.kvh;
+            return a.cost > b.cost;
+        });
+    } else {
+        std::stable_sort(attn.begin(), attn.end(), [](const AttnItem& a, const AttnItem& b) {
+            return a.cost > b.cost;
+        });
+    }
     int32_t* ATT = blob + H[L_OFF_ATTN];
     for (size_t i = 0; i < attn.size(); ++i) {
         ATT[kItemWords * i + 0] = attn[i].req;

@@ -80,6 +80,25 @@ def _blob(layout):
     return layout.host.numpy()
 
 
+@pytest.mark.parametrize("name,grouped", [("batch70b", True), ("concurrent_reuse", True),
+                                          ("long_context", False), ("llama8b_layer", False)])
+def test_attention_items_grouped_by_unit_when_many(name, grouped):
+    """With many attention items per SM the work list keeps each (request, kv head) unit's items
+    in one run, so that the CTAs running at one time share a few units' keys in L2; with few
+    (small batches) the list stays longest-first, which interleaves the units."""
+    cfg = CONFIGS[name]
+    reqs = make_layout(cfg)
+    n_phys = cfg.pool_spans * cfg.span_len // PAGE
+    max_pos = max(r.query_pos0 + r.n_query for r in reqs)
+    L = pcf.Layout(reqs, cfg.hq, cfg.hkv, cfg.d, n_phys, max_pos, device="cpu")
+    B = _blob(L)
+    items = B[B[L_OFF_ATTN]: B[L_OFF_ATTN] + 4 * B[L_N_ATTN]].reshape(-1, 4)
+    assert (len(items) >= 8 * int(B[37])) == grouped
+    units = [(int(r), int(h)) for r, h, _, _ in items]
+    runs = sum(1 for i in range(len(units)) if i == 0 or units[i] != units[i - 1])
+    assert (runs == len(set(units))) == grouped
+
+
 @pytest.mark.parametrize("name", list(CONFIGS))
 def test_layout_totals_and_block_table(name):
     cfg = CONFIGS[name]
