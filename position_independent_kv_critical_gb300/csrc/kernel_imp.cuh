@@ -12,12 +12,14 @@
 // the key tiles from the call's rotated copy of the batch's cached keys (MiniPIC 2.1: rotation to
 // the request's logical positions at use time).
 //
-// One CTA per (request, run of key tiles, kv head).  Key tiles stream through a two-stage ring;
-// up to two 256-row query chunks stay in the two query buffers for the whole run (more chunks
-// stream through them), and the S^T accumulator is double-buffered in TMEM, so the tensor core
-// works on the next (tile, chunk) step while the exponentials of the current one run.  Each
-// (kv head, query column half) writes its own partial sum per key; the last CTA of a run adds them
-// in fixed order (heads, then halves: deterministic).
+// One CTA per (request, run of key tiles, kv head, pair of 256-row query chunks).  Key tiles
+// stream through a two-stage ring past the CTA's (at most two) query chunks, which stay in the two
+// query buffers for the whole run, so each key tile is read once per CTA (a request with more
+// than two chunks has one CTA per pair, neighbours in the work list that share the key tiles in
+// L2); the S^T accumulator is double-buffered in TMEM, so the tensor core works on the next
+// (tile, chunk) step while the exponentials of the current one run.  Each (chunk pair, query
+// column half, kv head) writes its own partial sum per key; the last CTA of a run adds them in
+// fixed order (chunk pairs, heads, halves: deterministic).
 //   warps 0-7  exp-sum: warp w owns keys 32(w%4) .. +31 (its TMEM lane quarter) and the query
 //              columns 128(w/4) .. +127 of every step
 //   warp  8    TMEM allocation + single-thread tcgen05.mma issue
@@ -35,7 +37,6 @@ template <bool PAGED> __host__ __device__ constexpr int imp_threads() { return P
 constexpr int kImpExpThreads = 256;
 constexpr int kImpWarpMma = 8;
 constexpr int kImpWarpTma = 9;
-constexpr int kImpQRows = 256;
 
 struct ImpParams {
     const int32_t* layout;
@@ -65,7 +66,7 @@ struct ImpSmem {
     static constexpr uint32_t kTmemCols = 512;         // 2 accumulators of 256 columns
 };
 
-enum : int { I_K_FULL = 0 /*2*/, I_K_EMPTY = 2 /*2*/, I_Q_FULL = 4 /*2*/, I_Q_EMPTY = 6 /*2*/,
+enum : int { I_K_FULL = 0 /*2*/, I_K_EMPTY = 2 /*2*/, I_Q_FULL = 4 /*2*/, /* 6, 7 unused */
              I_ACC_FULL = 8 /*2*/, I_ACC_FREE = 10 /*2*/, I_LSE_FULL = 12 /*2*/, I_DRAIN = 14,
              I_KRAW_FULL = 16 /*2: paged, the key tile's page copies landed*/ };
 
@@ -90,22 +91,18 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t* L = prm.layout;
     const int32_t* item = L + L[L_OFF_IMP] + kItemWords * blockIdx.x;
-    const int req = item[0], t0 = item[1], kvh = item[2], nt = item[3];
+    const int req = item[0], t0 = item[1], kvh = item[2] & 0xFFFF, cp = item[2] >> 16, nt = item[3];
     const int32_t* R = L + L[L_OFF_REQ] + req * R_STRIDE;
     const int Hkv = L[L_HKV], g = L[L_GROUP];
     const int n_pages = R[R_N_PAGES];
     const int n_q = R[R_N_QUERY] * g;
-    const int n_qc = (n_q + kImpQRows - 1) / kImpQRows;
+    const int n_cp = imp_chunk_pairs(R[R_N_QUERY], g);   // CTAs of this (run, kv head)
+    const int qc0 = 2 * cp;                               // this CTA's first query chunk
+    const int n_qc = max(0, min(2, (n_q + kImpQRows - 1) / kImpQRows - qc0));
     const int n_steps = nt * n_qc;
-    // up to two chunks stay in their own buffers, loaded once, and the steps go tile by tile
-    // (step s = tile s / n_qc, chunk s % n_qc); with more chunks the steps go chunk by chunk
-    // (chunk s / nt, tile s % nt): each chunk is loaded once while the run's key tiles stream
-    // past it, and the per-key sums are carried from chunk to chunk through the partials
-    const bool q_resident = n_qc <= 2;
-    auto step_of = [&](int s, int& i, int& qc) {
-        if (q_resident) { i = s / n_qc; qc = s - i * n_qc; }
-        else { qc = s / nt; i = s - qc * nt; }
-    };
+    // the (at most two) chunks stay in their own buffers, loaded once, and the steps go tile by
+    // tile: step s = local tile s / n_qc, local chunk s % n_qc
+    auto step_of = [&](int s, int& i, int& qc) { i = s / n_qc; qc = s - i * n_qc; };
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -113,7 +110,6 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             mbar_init(&bars[I_KRAW_FULL + b], 1);
             mbar_init(&bars[I_K_EMPTY + b], 1);
             mbar_init(&bars[I_Q_FULL + b], 1);
-            mbar_init(&bars[I_Q_EMPTY + b], 1);
             mbar_init(&bars[I_ACC_FULL + b], 1);
             mbar_init(&bars[I_ACC_FREE + b], kImpExpThreads);
             mbar_init(&bars[I_LSE_FULL + b], kImpExpThreads);
@@ -171,24 +167,8 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                         tma_load_2d(sKs(kb) + hb * 16384, &tm_kcache, bar, hb * 64, ky0 + i * kTileKeys);
                 }
             };
-            for (int qc = 0; !q_resident && ok && qc < n_qc; ++qc) {
-                // chunk qc into buffer qc & 1 once chunk qc - 2 is done with it, then the run's tiles
-                const int qb = qc & 1;
-                if (qc >= 2 && !(ok = mbar_wait(&bars[I_Q_EMPTY + qb], ((qc >> 1) - 1) & 1, abort_flag))) break;
-                mbar_arrive_expect_tx(&bars[I_Q_FULL + qb], H * kImpQRows * 128);
-                for (int hb = 0; hb < H; ++hb)
-                    tma_load_2d(sQs(qb) + hb * kImpQRows * 128, &tm_q, &bars[I_Q_FULL + qb], hb * 64,
-                                qy0 + qc * kImpQRows);
-                lastq[qb] = qc;
-                for (int i = 0; i < nt; ++i) {
-                    const int s = qc * nt + i, kb = s & 1;
-                    if (s >= 2 && !(ok = mbar_wait(&bars[I_K_EMPTY + kb], ((s >> 1) - 1) & 1, abort_flag))) break;
-                    load_k(kb, i);
-                    lastk[kb] = s;
-                }
-            }
             // (a request without query rows has no steps: nothing is loaded)
-            for (int i = 0; q_resident && n_steps > 0 && ok && i < nt; ++i) {
+            for (int i = 0; n_steps > 0 && ok && i < nt; ++i) {
                 // rotated key tile t0 + i (rows past the request's keys are never summed)
                 const int kb = i & 1;
                 if (i >= 2 && !(ok = mbar_wait(&bars[I_K_EMPTY + kb], ((i >> 1) - 1) & 1, abort_flag))) break;
@@ -198,7 +178,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     mbar_arrive_expect_tx(&bars[I_Q_FULL + qc], H * kImpQRows * 128);
                     for (int hb = 0; hb < H; ++hb)
                         tma_load_2d(sQs(qc) + hb * kImpQRows * 128, &tm_q, &bars[I_Q_FULL + qc], hb * 64,
-                                    qy0 + qc * kImpQRows);
+                                    qy0 + (qc0 + qc) * kImpQRows);
                     lastq[qc] = 0;
                 }
             }
@@ -214,12 +194,11 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             for (int s = 0; ok && s < n_steps; ++s) {
                 int i, qc;
                 step_of(s, i, qc);
-                const int a = s & 1, qb = qc & 1;
-                // K stage: per tile in tile order, per step in chunk order
-                const int kidx = q_resident ? i : s;
-                if (!q_resident || qc == 0) ok = mbar_wait(&bars[I_K_FULL + (kidx & 1)], (kidx >> 1) & 1, abort_flag);
-                ok = ok && mbar_wait(&bars[I_Q_FULL + qb], q_resident ? 0 : ((qc >> 1) & 1), abort_flag) &&
-                     mbar_wait(&bars[I_LSE_FULL + qb], q_resident ? 0 : ((qc >> 1) & 1), abort_flag);
+                const int a = s & 1, qb = qc;
+                // K stage: per tile in tile order; the chunks (and their -lse2 slabs) load once
+                const int kidx = i;
+                if (qc == 0) ok = mbar_wait(&bars[I_K_FULL + (kidx & 1)], (kidx >> 1) & 1, abort_flag);
+                ok = ok && mbar_wait(&bars[I_Q_FULL + qb], 0, abort_flag) && mbar_wait(&bars[I_LSE_FULL + qb], 0, abort_flag);
                 ok = ok && (s < 2 || mbar_wait(&bars[I_ACC_FREE + a], ((s >> 1) - 1) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
@@ -235,12 +214,7 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 mma_bf16_ss(tmem + a * kImpQRows, desc_noswz_kmajor(smem_u32(sKones), 128, 256),
                             desc_noswz_kmajor(smem_u32(sQlse(qb)), 128, 256), idesc, 1u);
                 mma_commit(&bars[I_ACC_FULL + a]);
-                if (q_resident) {
-                    if (qc == n_qc - 1) mma_commit(&bars[I_K_EMPTY + (i & 1)]);
-                } else {
-                    mma_commit(&bars[I_K_EMPTY + (s & 1)]);
-                    if (i == nt - 1) mma_commit(&bars[I_Q_EMPTY + qb]);
-                }
+                if (qc == n_qc - 1) mma_commit(&bars[I_K_EMPTY + (i & 1)]);
             }
             mma_commit(&bars[I_DRAIN]);
             mbar_drain(&bars[I_DRAIN], 0);
@@ -266,10 +240,10 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 NSTS[e] = f2_pack(-v.y, -v.w);
             }
         }
-        const int n_loads = n_steps == 0 ? 0 : (q_resident ? nt : n_steps);
+        const int n_loads = n_steps == 0 ? 0 : nt;   // each key tile once
         float4 tr[4];
         auto table_row = [&](int sidx) {
-            const int i = q_resident ? sidx : sidx % nt;
+            const int i = sidx;
             const int lp = min((t0 + i) * kPagesPerTile + m, n_pages - 1);
             const float4* tp = reinterpret_cast<const float4*>(prm.rope + (int64_t)(page_pos[lp] + r0) * (D / 2) + 8 * c);
 #pragma unroll
@@ -301,12 +275,12 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         const int total_tokens = L[L_TOTAL_TOKENS];
         const int32_t tok_base = R[R_TOK_BASE];
-        // -lse2 of query chunk qc into slab qc & 1, as fp16 hi + lo (-30000 past the last row:
-        // those columns contribute 0); thread tid writes row tid.  lse2 combines the row's key
-        // chunks in chunk order: M = max of the maxima, lse2 = M + log2(sum_c s_c 2^(m_c - M)).
+        // -lse2 of the CTA's query chunk qc (0 or 1) into slab qc, as fp16 hi + lo (-30000 past the
+        // last row: those columns contribute 0); thread tid writes row tid.  lse2 combines the row's
+        // key chunks in chunk order: M = max of the maxima, lse2 = M + log2(sum_c s_c 2^(m_c - M)).
         auto prep = [&](int qc) {
             uint8_t* slab = sQlse(qc & 1);
-            const int n = qc * kImpQRows + tid;
+            const int n = (qc0 + qc) * kImpQRows + tid;
             float v = -30000.f;
             if (n < n_q && chunks > 0) {
                 float2 c2[kMaxSplits];
@@ -332,7 +306,8 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (n_qc >= 2 && n_steps > 1) prep(1);
         bool ok = true;
         uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-        float* part_h = prm.part + ((int64_t)ch * Hkv + kvh) * total_tokens;   // this thread's half
+        // this thread's (chunk pair, query column half, kv head) partial
+        float* part_h = prm.part + ((int64_t)(cp * 2 + ch) * Hkv + kvh) * total_tokens;
         for (int s = 0; s < n_steps; ++s) {
             int i, qc;
             step_of(s, i, qc);
@@ -340,8 +315,6 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             const int t = t0 + i;
             const bool valid_key = (t * kPagesPerTile + key / kPage) < n_pages;
             float* dst = part_h + tok_base + t * kTileKeys + key;
-            // chunk order: the key's sum over the earlier chunks, read while this step runs
-            const float carried = (!q_resident && qc > 0 && valid_key) ? *dst : 0.f;
             if (ok) ok = mbar_wait(&bars[I_ACC_FULL + a], (s >> 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
@@ -359,26 +332,25 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     for (int e = 0; e < 32; e += 2)
                         acc2[(e >> 1) & 1] = f2_add(acc2[(e >> 1) & 1], f2_pack(ex2(__uint_as_float(sv[cc][e])),
                                                                               ex2(__uint_as_float(sv[cc][e + 1]))));
-                // the last step of chunk qc is complete, so its slab takes chunk qc + 2
-                if (!q_resident && i == nt - 1 && qc + 2 < n_qc) prep(qc + 2);
             }
-            if (!q_resident || qc == n_qc - 1) {
+            if (qc == n_qc - 1) {   // the key's sum over the CTA's chunks
                 float a0, a1, b0, b1;
                 f2_unpack(acc2[0], a0, a1);
                 f2_unpack(acc2[1], b0, b1);
                 acc2[0] = acc2[1] = f2_pack(0.f, 0.f);
-                if (ok && valid_key) *dst = carried + ((a0 + b0) + (a1 + b1));
+                if (ok && valid_key) *dst = (a0 + b0) + (a1 + b1);
             }
         }
         if (n_qc == 0)   // a request without query rows: every importance is 0
             for (int i = 0; i < nt; ++i)
                 if (((t0 + i) * kPagesPerTile + key / kPage) < n_pages)
                     part_h[tok_base + (t0 + i) * kTileKeys + key] = 0.f;
-        // the last of the run's Hkv CTAs sums the heads in order (the named barriers order the
-        // partial writes before, and the reads after, thread 0's acquire-release increment)
+        // the last of the run's Hkv * n_cp CTAs sums the chunk pairs and heads in order (the named
+        // barriers order the partial writes before, and the reads after, thread 0's
+        // acquire-release increment)
         named_sync_exp();
         const int cidx = R[R_KTILE_BASE] + t0;
-        if (tid == 0) misc[5] = (atomic_add_acq_rel_gpu(&prm.counters[cidx], 1) == Hkv - 1) ? 1 : 0;
+        if (tid == 0) misc[5] = (atomic_add_acq_rel_gpu(&prm.counters[cidx], 1) == Hkv * n_cp - 1) ? 1 : 0;
         named_sync_exp();
         if (misc[5]) {
             for (int idx = tid; idx < nt * kTileKeys; idx += kImpExpThreads) {
@@ -386,9 +358,10 @@ imp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 if ((t * kPagesPerTile + k / kPage) >= n_pages) continue;
                 const int32_t tok = R[R_TOK_BASE] + t * kTileKeys + k;
                 float sum = 0.f;
-                for (int h = 0; h < Hkv; ++h)
-                    sum += __ldcg(prm.part + (int64_t)h * total_tokens + tok) +
-                           __ldcg(prm.part + ((int64_t)Hkv + h) * total_tokens + tok);
+                for (int p = 0; p < n_cp; ++p)
+                    for (int h = 0; h < Hkv; ++h)
+                        sum += __ldcg(prm.part + ((int64_t)(2 * p) * Hkv + h) * total_tokens + tok) +
+                               __ldcg(prm.part + ((int64_t)(2 * p + 1) * Hkv + h) * total_tokens + tok);
                 prm.importance[tok] = sum;
             }
             if (tid == 0) prm.counters[cidx] = 0;

@@ -20,6 +20,19 @@ constexpr int kMaxPosLimit = 1 << 20;
 constexpr int kItemWords = 4;
 constexpr int kDefaultSms = 152;        // GB300's SM count: the plan's target when the caller names none
 constexpr int kMaxSplits = 16;          // key-range splits of one attention (or LSE) work unit
+constexpr int kImpQRows = 256;          // query rows of one importance chunk (the MMA's N)
+
+// importance CTAs of a request per (run of key tiles, kv head): one per pair of query chunks (a
+// CTA keeps its two chunks resident and streams its key tiles once)
+#ifdef __CUDACC__
+#define PCF_HOST_DEVICE __host__ __device__
+#else
+#define PCF_HOST_DEVICE
+#endif
+PCF_HOST_DEVICE inline int32_t imp_chunk_pairs(int64_t n_query, int32_t group) {
+    const int64_t chunks = (n_query * group + kImpQRows - 1) / kImpQRows;
+    return chunks > 2 ? (int32_t)((chunks + 1) / 2) : 1;
+}
 
 enum : int {
     L_MAGIC = 0, L_WORDS = 1, L_N_REQS = 2, L_HQ = 3, L_HKV = 4, L_D = 5, L_N_PHYS = 6,
@@ -57,12 +70,13 @@ enum : int {
 enum : int { P_NSPLIT = 0, P_SLOT_BASE = 1, P_STRIDE = 2 };
 
 // work items (kItemWords each)
-//   attention : {req, kv head, q tile pair, key-range split}   largest estimated cost first
+//   attention : {req, kv head, q tile pair, key-range split}   largest estimated cost first, or
+//               with many items per SM grouped by (req, kv head) unit
 //   lse       : {req, kv head, q tile pair, key chunk}
 //               (each chunk writes its rows' partial (max, sum); the importance kernel combines
 //               a row's chunks into its log2-sum-exp)
 // (a "q tile pair" p covers the 128-row query tiles 2p and 2p+1 of the request)
-//   importance: {req, first key tile, kv head, key tiles}
+//   importance: {req, first key tile, kv head | chunk pair << 16, key tiles}
 //   combine   : {req, kv head, q tile pair, 0}   pairs whose key range was split
 
 }  // namespace pcf

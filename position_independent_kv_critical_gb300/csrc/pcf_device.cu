@@ -181,6 +181,10 @@ size_t align_up(size_t x) { return (x + 1023) & ~size_t(1023); }
 
 // rotated copy of every cached key of the batch: [Hkv][total_tokens][D] fp16
 size_t kc_bytes(const int32_t* H) { return (size_t)H[L_HKV] * H[L_TOTAL_TOKENS] * H[L_D] * 2; }
+// importance partials: [chunk pair][query column half][kv head][token]
+size_t imp_part_floats(const int32_t* H) {
+    return 2 * (size_t)imp_chunk_pairs(H[L_MAX_QUERY], H[L_GROUP]) * H[L_HKV] * H[L_TOTAL_TOKENS];
+}
 
 struct ScoreWs {
     size_t q, kc, lse, part, cnt, total;
@@ -191,8 +195,9 @@ ScoreWs score_ws(const int32_t* H) {
     w.kc = align_up(w.q + (size_t)H[L_TOTAL_QUERY] * H[L_HQ] * H[L_D] * 2);
     w.lse = align_up(w.kc + kc_bytes(H));
     w.part = align_up(w.lse + (size_t)H[L_LSE_SLOTS] * sizeof(float2));
-    // importance partials: per kv head and token, one per half of the query columns
-    w.cnt = align_up(w.part + 2 * (size_t)H[L_HKV] * H[L_TOTAL_TOKENS] * sizeof(float));
+    // importance partials: per kv head and token, one per half of the query columns and pair of
+    // query chunks
+    w.cnt = align_up(w.part + imp_part_floats(H) * sizeof(float));
     // counters: importance runs (one per key tile at most) and the LSE kernel's item counter
     w.total = align_up(w.cnt + ((size_t)H[L_TOTAL_KTILES] + 1) * sizeof(int32_t));
     return w;
@@ -369,7 +374,7 @@ ScorePagedWs score_paged_ws(const int32_t* H) {
     w.q = 0;
     w.lse = align_up(w.q + (size_t)H[L_TOTAL_QUERY] * H[L_HQ] * H[L_D] * 2);
     w.part = align_up(w.lse + (size_t)H[L_LSE_SLOTS] * sizeof(float2));
-    w.cnt = align_up(w.part + 2 * (size_t)H[L_HKV] * H[L_TOTAL_TOKENS] * sizeof(float));
+    w.cnt = align_up(w.part + imp_part_floats(H) * sizeof(float));
     w.total = align_up(w.cnt + ((size_t)H[L_TOTAL_KTILES] + 1) * sizeof(int32_t));
     return w;
 }

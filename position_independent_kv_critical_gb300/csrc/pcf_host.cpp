@@ -289,7 +289,7 @@ pcf_status validate(const pcf_request_desc* reqs, int32_t n_reqs, const pcf_dims
             n_lse += (int64_t)d.n_kv_heads * cdiv((int64_t)r.n_query * g, kTileRows * kQTilesPerCta) * chunks;
             slots += (int64_t)r.n_query * d.n_q_heads * chunks;
         }
-        if (nkt > 0) n_imp += (int64_t)cdiv(nkt, plan->imp_tiles) * d.n_kv_heads;
+        if (nkt > 0) n_imp += (int64_t)cdiv(nkt, plan->imp_tiles) * d.n_kv_heads * imp_chunk_pairs(r.n_query, g);
     }
     plan->n_pairs = (int32_t)plan->pair_tiles.size();
     if (n_attn >= lim || n_lse >= lim || n_imp >= lim || slots >= lim || attn_slots >= lim / 256)
@@ -466,16 +466,19 @@ extern "C" pcf_status pcf_layout_build(const pcf_request_desc* reqs, int32_t n_r
                     }
             lse_base += r.n_query * d.n_q_heads * plan.lse_chunks[b];
         }
-        // importance work: (run of key tiles, kv head); the request's tiles are cut into
-        // ceil(nkt / imp_tiles) runs of near-equal length
+        // importance work: (run of key tiles, kv head, pair of query chunks); the request's tiles
+        // are cut into ceil(nkt / imp_tiles) runs of near-equal length, and a run's chunk pairs are
+        // neighbours in the list so that their CTAs run together and share the key tiles in L2
         if (nkt > 0) {
             const int32_t runs = cdiv(nkt, plan.imp_tiles);
+            const int32_t n_cp = imp_chunk_pairs(r.n_query, g);
             for (int32_t u = 0; u < runs; ++u) {
                 const int32_t t0 = (int32_t)((int64_t)u * nkt / runs), t1 = (int32_t)((int64_t)(u + 1) * nkt / runs);
-                for (int32_t h = 0; h < d.n_kv_heads; ++h) {
-                    int32_t* it = IMP + kItemWords * n_imp++;
-                    it[0] = b; it[1] = t0; it[2] = h; it[3] = t1 - t0;
-                }
+                for (int32_t h = 0; h < d.n_kv_heads; ++h)
+                    for (int32_t cp = 0; cp < n_cp; ++cp) {
+                        int32_t* it = IMP + kItemWords * n_imp++;
+                        it[0] = b; it[1] = t0; it[2] = h | (cp << 16); it[3] = t1 - t0;
+                    }
             }
         }
         tok_base += n_tok;

@@ -147,11 +147,19 @@ def test_layout_totals_and_block_table(name):
     comb = B[B[L_OFF_COMB]: B[L_OFF_COMB] + 4 * B[L_N_COMB]].reshape(-1, 4)
     assert {tuple(x[:3]) for x in comb.tolist()} == {(b, h, t) for (b, t), n in nsplit.items() if n > 1
                                                       for h in range(cfg.hkv)}
-    # importance runs {req, first tile, kv head, tiles}: every (request, key tile, kv head) once
+    # importance runs {req, first tile, kv head | chunk pair << 16, tiles}: every (request, key
+    # tile, kv head, pair of 256-row query chunks) once; a request with at most two chunks has one
+    # pair, which keeps them both resident
     imp = B[B[L_OFF_IMP]: B[L_OFF_IMP] + 4 * B[L_N_IMP]].reshape(-1, 4)
-    covered = [(int(q), t, int(h)) for q, t0, h, nt in imp.tolist() for t in range(t0, t0 + nt)]
-    assert sorted(covered) == sorted((b, t, h) for b, r in enumerate(reqs)
-                                     for t in range(-(-r.n_cached // 128)) for h in range(cfg.hkv))
+    covered = [(int(q), t, int(hc) & 0xFFFF, int(hc) >> 16) for q, t0, hc, nt in imp.tolist()
+               for t in range(t0, t0 + nt)]
+
+    def pairs(r):
+        chunks = -(-r.n_query * g // 256)
+        return -(-chunks // 2) if chunks > 2 else 1
+    assert sorted(covered) == sorted((b, t, h, p) for b, r in enumerate(reqs)
+                                     for t in range(-(-r.n_cached // 128)) for h in range(cfg.hkv)
+                                     for p in range(pairs(r)))
     assert all(nt >= 1 for nt in imp[:, 3])
 
 
