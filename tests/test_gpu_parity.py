@@ -284,6 +284,17 @@ def test_edge_cases(case, shape):
     check_batch(GpuBatch(b))
 
 
+@pytest.mark.parametrize("shape", [dict(hq=12, hkv=3, d=128), dict(hq=24, hkv=12, d=64)])
+def test_head_counts_not_multiples_of_eight(shape):
+    """The rotation kernels stage tiles of up to 8 heads: 12 query heads make a full group and a
+    group of 4, 12 kv heads the same for the cached keys' pages, and 3 kv heads one short page
+    group; ragged spans and a query count that is not a multiple of 16 rows."""
+    b = small_custom_batch([(0, 3, 0, 5), (3, 5, 48, 19), (8, 2, 300, 0)], 21, n_phys_pages=12,
+                           theta=1e4, **shape)
+    check_batch(GpuBatch(b))
+    check_batch(GpuBatch(b), paged=True)
+
+
 def test_mixed_requests_in_one_batch():
     b = small_custom_batch([(0, 3, 7, 5)], n_query=2, hq=8, hkv=2, d=128, theta=5e5, n_phys_pages=40,
                            extra_requests=[([(3, 17, 100, 40), (20, 9, 2000, 3)], 33, 3000),
