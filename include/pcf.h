@@ -166,7 +166,8 @@ pcf_status pcf_score_paged_workspace_bytes(const int32_t* layout_host, size_t* b
  * copy of the cached keys: both passes copy each key tile from its pool pages (through the block
  * table) and rotate it in shared memory to the request's positions before the tensor-core
  * contraction (MiniPIC 2.1).  ws: >= pcf_score_paged_workspace_bytes.  The rotation is repeated for
- * every query-tile pair and query chunk that reads a tile, so this takes longer than pcf_score;
+ * every query-tile pair (row LSE) and every pair of 256-row query chunks (importance) that reads a
+ * tile, so this takes longer than pcf_score;
  * with pcf_fused_attention_paged it completes a hot path that keeps no per-request copy of the
  * cached keys or values. */
 pcf_status pcf_score_paged(const pcf_layout* layout, const uint16_t* q_query, const uint16_t* k_pool,
