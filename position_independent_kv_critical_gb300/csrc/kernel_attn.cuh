@@ -51,22 +51,27 @@
 // LSE mode (critical-layer scoring, pass 1) runs the same pipeline without P/V and writes the
 // per-row running max and sum of one key chunk (the importance kernel combines a row's chunks).  Having no O, it gives each query tile two S
 // buffers of a whole key tile (128 columns) and issues Q K^T with N = 128: half the MMA
-// instructions of two 64-key halves.  In paged scoring the two P V issuer warps, idle without
-// P V, are the rotators.
+// instructions of two 64-key halves.  Without pages the CTA has 12 warps, and each softmax thread
+// loads its row's 128 scores at once and frees the S buffer before the arithmetic (with 14 warps'
+// register budget it took them in two parts and held the buffer through the first part's);
+// in paged scoring the two P V issuer warps, idle without P V, are the rotators and the scores
+// come in two parts.
 #pragma once
 #include "layout_format.h"
 #include "ptx.cuh"
 
 namespace pcf {
 
-// 14 warps (at most 4 per SM sub-partition, so each may hold 128+ registers); the paged variant
-// adds two rotator warps (16 warps, 128 registers each)
+// 14 warps (at most 4 per SM sub-partition, so each may hold 128 registers); the paged variant
+// adds two rotator warps (16 warps, 128 registers each); scoring without pages needs no P V
+// issuers and runs 12 warps (3 per sub-partition, up to 168 registers: room for a whole key
+// tile's scores in the softmax)
 constexpr int kAttnThreads = 448;
 constexpr int kAttnThreadsPaged = 512;
 // (the paged scoring pass needs no extra warps: its rotators are the two P V issuer warps, idle
 // without P V)
 template <bool PAGED, bool LSE = false> __host__ __device__ constexpr int attn_threads() {
-    return PAGED && !LSE ? kAttnThreadsPaged : kAttnThreads;
+    return PAGED && !LSE ? kAttnThreadsPaged : (LSE && !PAGED ? 384 : kAttnThreads);
 }
 constexpr int kWarpSoftB = 4;
 constexpr int kWarpMma = 8;
@@ -950,6 +955,50 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         }
                         mbar_arrive(&bars[B_KPOS_FREE + ks]);
                     }
+                    if constexpr (!PAGED) {
+                        // the whole key tile's 128 scores in registers (12 warps leave room), the S
+                        // buffer released as soon as they have landed
+                        const bool full = __all_sync(0xffffffffu, cut >= kTileKeys);
+                        uint32_t sv[128];
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4)
+                            tmem_ld32(tS0 + c4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c4 * 32]));
+                        tmem_ld_wait();
+                        tc_fence_before();
+                        mbar_arrive(&bars[B_P_FULL + 2 * t + ks]);
+                        if (!full) {
+#pragma unroll
+                            for (int e = 0; e < 128; ++e)
+                                if (e >= cut) sv[e] = __float_as_uint(-INFINITY);
+                        }
+                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                        for (int e = 0; e < 128; e += 8) {
+                            m4[0] = max3f(m4[0], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+                            m4[1] = max3f(m4[1], __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
+                            m4[2] = max3f(m4[2], __uint_as_float(sv[e + 4]), __uint_as_float(sv[e + 5]));
+                            m4[3] = max3f(m4[3], __uint_as_float(sv[e + 6]), __uint_as_float(sv[e + 7]));
+                        }
+                        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                        const float m_new = fmaxf(m_run, mx);
+                        if (m_new > m_run + 8.0f) {   // lazy rescale: keep the terms <= 2^8
+                            l_run *= ex2(m_run - m_new);
+                            m_run = m_new;
+                        }
+                        const float msub = m_run == -INFINITY ? 0.f : m_run;
+                        const uint64_t negm2 = f2_pack(-msub, -msub);
+                        uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) {
+                            float d0, d1;
+                            f2_unpack(f2_add(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), negm2), d0, d1);
+                            acc2[e & 1] = f2_add(acc2[e & 1], f2_pack(ex2(d0), ex2(d1)));
+                        }
+                        float a0, a1, b0, b1;
+                        f2_unpack(acc2[0], a0, a1);
+                        f2_unpack(acc2[1], b0, b1);
+                        l_run += (a0 + b0) + (a1 + b1);
+                    } else
 #pragma unroll 1
                     for (int h = 0; h < 2; ++h) {
                         const int cut_h = cut - 64 * h;

@@ -348,7 +348,7 @@ pcf_status score_impl(const pcf_layout* lay, const uint16_t* q_query, const uint
                      nullptr, nullptr, nullptr, nullptr, rope2};
         // persistent: at most one CTA per SM, items handed out in list order
         const int grid = std::min<int>(H[L_N_LSE_ITEMS], device_sms());
-        if ((s = launch(kern, dim3(grid), dim3(kAttnThreads), SM::kAlloc, st, tq128, tkc, zero, zero, zero, zero, p)) !=
+        if ((s = launch(kern, dim3(grid), dim3(attn_threads<false, true>()), SM::kAlloc, st, tq128, tkc, zero, zero, zero, zero, p)) !=
             PCF_OK)
             return s;
     }
