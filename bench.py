@@ -7,8 +7,9 @@ The default workload is the largest single-GPU one, the 70B-shaped batch of 64 r
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--pct P] [--impl reference]
 
-Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica of the workload
-(requests shard with no exchange: weak scaling); the time is the max over ranks.
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own shard of requests, a batch
+of the workload's shape drawn with the rank's own seed (no exchange: weak scaling); the time is
+the max over ranks.
 """
 from __future__ import annotations
 
@@ -538,7 +539,7 @@ def main():
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    b = make_batch(args.config, args.pct)
+    b = make_batch(args.config, args.pct, shard=rank)   # each rank its own requests
     max_pos = b.max_pos + 1
     L = pcf.Layout(b.requests, b.hq, b.hkv, b.d, b.n_phys_pages, max_pos, device=str(dev))
     rope = pcf.rope_table(b.d, b.theta, max_pos).to(dev)

@@ -61,6 +61,11 @@ class WorkloadConfig:
     def seed(self) -> int:
         return self.index * 1000 + 17
 
+    def shard_seed(self, shard: int) -> int:
+        """Master seed of shard ``shard`` of the workload (one per rank under weak scaling): shard 0
+        is the workload itself; the others draw different requests of the same shape."""
+        return self.seed + 7919 * int(shard)
+
 
 CONFIGS = {
     "tiny": WorkloadConfig("tiny", 1, n_reqs=1, hq=8, hkv=2, d=64, theta=1e4, span_len=128,
@@ -199,10 +204,11 @@ def _zipf_draw(rng: np.random.Generator, n_pool: int, n_draw: int, a: float) -> 
     return [int(x) for x in rng.choice(n_pool, size=n_draw, replace=False, p=p)]
 
 
-def make_layout(cfg: WorkloadConfig, pct: Optional[int] = None) -> List[Request]:
-    """Span placement for every request of ``cfg`` (seeded, deterministic)."""
+def make_layout(cfg: WorkloadConfig, pct: Optional[int] = None, shard: int = 0) -> List[Request]:
+    """Span placement for every request of ``cfg`` (seeded, deterministic; ``shard`` > 0 draws
+    another set of requests with the same sizes)."""
     pct = cfg.pct if pct is None else pct
-    rng = np.random.default_rng(cfg.seed)
+    rng = np.random.default_rng(cfg.shard_seed(shard))
     pages_per_span = cfg.span_len // PAGE
     reqs: List[Request] = []
     for _ in range(cfg.n_reqs):
@@ -250,12 +256,14 @@ def make_batch_from_requests(name: str, requests: List[Request], hq: int, hkv: i
                  q_fresh=q_fresh, k_fresh=k_fresh, v_fresh=v_fresh, seed=seed)
 
 
-def make_batch(cfg_name: str, pct: Optional[int] = None) -> Batch:
+def make_batch(cfg_name: str, pct: Optional[int] = None, shard: int = 0) -> Batch:
+    """The workload's batch; ``shard`` r > 0 gives rank r of a weak-scaling run its own requests
+    and tensors (same shapes, token counts and statistics, other draws)."""
     cfg = CONFIGS[cfg_name]
-    reqs = make_layout(cfg, pct)
+    reqs = make_layout(cfg, pct, shard)
     n_phys = cfg.pool_spans * (cfg.span_len // PAGE)
     return make_batch_from_requests(cfg.name, reqs, cfg.hq, cfg.hkv, cfg.d, cfg.theta, n_phys,
-                                    cfg.seed)
+                                    cfg.shard_seed(shard))
 
 
 def layer_inputs(b: Batch, n_layers: int):
