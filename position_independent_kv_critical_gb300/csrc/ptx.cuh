@@ -199,17 +199,6 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem]^T: A read from TMEM (lane = row, each 32-bit column holds two
-// consecutive K elements), B from shared memory; bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 // Four K = 16 steps of D[tmem] (+)= A[smem] * B[smem]^T in one block, for a warp that runs the
 // issue loop converged: every lane executes it, only `leader`'s predicate issues.  The operands
 // are 128-byte-swizzled K-major: step kk starts 32 bytes further along K, i.e. 2 more in the low
@@ -297,14 +286,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         PCF_W32(r)
         : "memory");
 }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-            taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -315,14 +296,8 @@ __device__ __forceinline__ uint64_t desc_sw128_kmajor(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// Same swizzle, MN-major operand: 64-element (128-byte) wide atoms of 8 K rows; consecutive 8-row
-// K groups are 1024 bytes apart (stride byte offset) and consecutive 64-wide atoms along N are
-// `atom_stride` bytes apart (leading byte offset).
-__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t atom_stride) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(atom_stride >> 4) << 16) |
-           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-// The same 128-byte-swizzle descriptors as two 32-bit words: the low word holds the start address
+// 128-byte-swizzle descriptors as two 32-bit words (K-major as above with lbo 16; MN-major with
+// lbo = the byte distance between 64-wide atoms along N): the low word holds the start address
 // and the leading byte offset, the high word (fixed) the 1024-byte stride, version and swizzle.
 __device__ __forceinline__ uint32_t desc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes) {
     return ((saddr & 0x3FFFFu) >> 4) | ((lbo_bytes >> 4) << 16);
